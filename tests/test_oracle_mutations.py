@@ -1,0 +1,94 @@
+"""Plant plausible mistakes in the oracle (on the CPU) and check a pin catches each.
+
+Each mutant replaces one oracle function for the duration of one check; the
+check is an existing pin's comparison and must now fail.
+"""
+
+import json
+import os
+
+import numpy as np
+import pytest
+
+from oracle import gdn, mamba2
+from oracle.partition import levels_needed
+
+GOLDEN = os.path.join(os.path.dirname(__file__), "golden")
+
+
+def _case(T=24, seed=0):
+    rng = np.random.default_rng(seed)
+    q = rng.standard_normal((T, 3))
+    k = rng.standard_normal((T, 3))
+    v = rng.standard_normal((T, 2))
+    la = -np.log1p(np.exp(rng.standard_normal(T)))
+    lam = np.log1p(np.exp(rng.standard_normal((T, levels_needed(T)))))
+    return q, k, v, la, lam
+
+
+def _golden_alpha_half_ok():
+    with open(os.path.join(GOLDEN, "worked_forward.json")) as f:
+        g = json.load(f)
+    lam = np.tile(10.0 ** np.arange(4), (4, 1))
+    one = np.ones((4, 1))
+    o = mamba2.forward_dense(one, one, one, np.full(4, -np.log(2.0)), lam)[:, 0]
+    return np.allclose(o, g["alpha_half"]["o"], rtol=1e-12)
+
+
+def _dense_vs_recurrent_ok():
+    q, k, v, la, lam = _case()
+    return np.allclose(mamba2.forward_dense(q, k, v, la, lam), mamba2.forward_recurrent(q, k, v, la, lam)[0],
+                       rtol=1e-10, atol=1e-12)
+
+
+def test_unmutated_pins_pass():
+    assert _golden_alpha_half_ok()
+    assert _dense_vs_recurrent_ok()
+
+
+def test_level_off_by_one_is_caught(monkeypatch):
+    orig = mamba2.level_array
+    monkeypatch.setattr(mamba2, "level_array", lambda t, s: np.maximum(orig(t, s) - 1, 0))
+    assert not _golden_alpha_half_ok()
+    assert not _dense_vs_recurrent_ok()
+
+
+def test_level_exclusive_token_is_caught(monkeypatch):
+    # reading the state as excluding token t (level 0 dropped)
+    orig = mamba2.hier_mask
+    monkeypatch.setattr(mamba2, "hier_mask", lambda lam: orig(lam) - np.diag(np.asarray(lam)[:, 0]))
+    assert not _golden_alpha_half_ok()
+    assert not _dense_vs_recurrent_ok()
+
+
+def test_decay_closed_interval_is_caught(monkeypatch):
+    # product of alpha over [s, t] instead of (s, t]
+    orig = mamba2.decay_matrix
+    monkeypatch.setattr(mamba2, "decay_matrix", lambda la: orig(la) * np.exp(np.asarray(la, np.float64))[None, :])
+    assert not _golden_alpha_half_ok()
+    assert not _dense_vs_recurrent_ok()
+
+
+def test_transposed_mask_is_caught(monkeypatch):
+    # lambda indexed by the key's position instead of the query's
+    def bad(lam):
+        lam = np.asarray(lam, np.float64)
+        T = lam.shape[0]
+        t = np.arange(T)[:, None]
+        s = np.arange(T)[None, :]
+        lv = mamba2.level_array(t, s)
+        out = np.where(s <= t, lam[np.broadcast_to(s, (T, T)), lv], 0.0)
+        return out
+    monkeypatch.setattr(mamba2, "hier_mask", bad)
+    assert not _dense_vs_recurrent_ok()
+
+
+def test_gdn_missing_beta_is_caught(monkeypatch):
+    with open(os.path.join(GOLDEN, "worked_gdn.json")) as f:
+        g = json.load(f)
+    orig = gdn.gdn_coeff
+    monkeypatch.setattr(gdn, "gdn_coeff", lambda q, k, beta, la: orig(q, k, beta, la) / np.asarray(beta)[None, :])
+    one = np.ones((2, 1))
+    o = gdn.gdn_forward_A(one, one, np.array([[1.0], [2.0]]), np.array([0.5, 0.5]), np.zeros(2),
+                          np.array([[1.0, 10.0], [1.0, 10.0]]))[:, 0]
+    assert not np.allclose(o, g["reading_A"]["o"])
