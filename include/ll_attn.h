@@ -1,0 +1,168 @@
+/*
+ * ll_attn.h -- C ABI of libllattn.so: GB300 (sm_103a) log-linear attention.
+ *
+ * Operations (sources are the pages' titles and sections):
+ *   ll_attn_fwd          causal log-linear Mamba-2 forward
+ *                          o_t = sum_{s<=t} (q_t . k_s) Gamma(t,s) lam_t[l(t,s)] v_s,
+ *                        i.e. O = (Q K^T . M^S . M^H) V.  "Log-Linear Attention"
+ *                        study note (dimensionstp.github.io) §3-4 "Parallel form"
+ *                        and §3-5 (M = M^S . M^H, Log-Linear Mamba-2); computed
+ *                        chunk-wise in O(T log T) as in §3-1 / the chunk-scan of
+ *                        the gist.science (zh) summary §2.3.
+ *   ll_attn_decode_step  one token of Fenwick-state decoding: study note §3-3
+ *                        "Recurrent form" (o_t = sum_l lam_t^(l) q_t^T S_t^(l))
+ *                        and §3-6 "Memory-efficient decoding"; carry/merge as in
+ *                        the drawer analogy of the gist.science (zh) summary.
+ *   ll_gdn_fwd           Log-Linear Gated DeltaNet forward, study note §3-5 and
+ *                        gist.science (de) Technische Zusammenfassung §2; the
+ *                        gated delta rule itself is not on the pages (reading A:
+ *                        O = (C_GDN . M^H) V, every level state follows the full
+ *                        gated-delta transition).
+ *
+ * Definitions used throughout:
+ *   level l(t,s) = 0 if s == t, else floor(log2(t xor s)) + 1   (0 <= s <= t);
+ *   Gamma(t,s)   = prod_{r=s+1..t} alpha_r, passed as log_alpha (float32);
+ *   a Fenwick level l >= 1 of query t is non-empty iff bit l-1 of t is set.
+ *
+ * Conventions for every entry point:
+ *   - All tensor pointers are DEVICE pointers owned by the caller; the library
+ *     never allocates, frees or keeps them.  Layouts are contiguous, row-major,
+ *     head-major; every pointer must be 16-byte aligned.
+ *   - Calls are asynchronous on `stream` (a cudaStream_t; NULL = legacy default
+ *     stream).  Argument errors are detected on the host before anything is
+ *     launched and return LL_ERR_INVALID_ARG / LL_ERR_UNSUPPORTED /
+ *     LL_ERR_WORKSPACE without touching device memory.  A launch failure
+ *     returns LL_ERR_CUDA.
+ *   - Conditions only the device can see (a decode position that does not fit
+ *     the stored levels; a bounded device-side wait that expired) set a
+ *     device error word; ll_last_device_error() synchronises the stream and
+ *     reports (and clears) it.  No kernel traps or spins unboundedly.
+ *   - Output values are unspecified after an error.
+ *   - Only one call may use a given workspace at a time.
+ */
+#ifndef LL_ATTN_H
+#define LL_ATTN_H
+
+#include <stddef.h>
+#include <stdint.h>
+
+/* Symbols of the C ABI are the only ones the shared library exports. */
+#if defined(__GNUC__)
+#define LL_API __attribute__((visibility("default")))
+#else
+#define LL_API
+#endif
+
+#ifdef __cplusplus
+extern "C" {
+#endif
+
+typedef enum {
+  LL_OK = 0,
+  LL_ERR_INVALID_ARG = 1, /* null pointer, bad size, misaligned pointer     */
+  LL_ERR_UNSUPPORTED = 2, /* valid but not implemented (e.g. head dim 96)   */
+  LL_ERR_CUDA = 3,        /* a CUDA runtime call or launch failed            */
+  LL_ERR_TIMEOUT = 4,     /* a bounded device-side wait expired             */
+  LL_ERR_WORKSPACE = 5,   /* workspace pointer null or too small            */
+  LL_ERR_DEVICE = 6       /* device-side argument check failed (e.g. decode
+                             position beyond the stored levels)             */
+} ll_status;
+
+typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
+
+/* Problem shape of a forward call.
+ *   B, H      batch rows and heads (>= 1)
+ *   T         sequence length (>= 1), a multiple of `chunk`
+ *   dk, dv    key / value head dims, each in {16, 32, 64, 128}
+ *   L         number of lambda levels per token, >= levels touched by T
+ *             (1 if T == 1, else bit_length(T-1) + 1)
+ *   chunk     chunk length of the chunked algorithm, in {16, 32, 64, 128}; the
+ *             result does not depend on it (up to rounding).  The bf16
+ *             tensor-core path of ll_attn_fwd tiles by 128 tokens whatever
+ *             `chunk` is (it needs T % 128 == 0 and dk == dv == 128).
+ *   Ls        number of stored decode levels of state_out (levels 1..Ls);
+ *             0 = no state export
+ *   io        dtype of q, k, v and o (LL_F32 or LL_BF16); log_alpha, lam,
+ *             beta are always float32; accumulation is float32.           */
+typedef struct {
+  int B, H, T, dk, dv, L, chunk, Ls;
+  ll_dtype io;
+} ll_shape;
+
+/* Library version (major*10000 + minor*100 + patch). */
+LL_API int ll_version(void);
+
+/* Human-readable name of a status code (static string). */
+LL_API const char* ll_status_str(ll_status s);
+
+/* Synchronise `stream`, then read and clear the device error word.
+ * Returns LL_OK, LL_ERR_TIMEOUT or LL_ERR_DEVICE (or LL_ERR_CUDA if the
+ * synchronisation itself failed). */
+LL_API ll_status ll_last_device_error(void* stream);
+
+/* Bytes of workspace ll_attn_fwd needs for `shape` (0 on invalid shape). */
+LL_API size_t ll_attn_fwd_workspace_size(const ll_shape* shape);
+
+/* Number of kernel launches one ll_attn_fwd call with `shape` makes
+ * (0 on an invalid shape); useful when capturing calls in CUDA graphs. */
+LL_API int ll_attn_fwd_launches(const ll_shape* shape);
+
+/* Log-linear Mamba-2 forward.
+ *   q          [B,H,T,dk]  io dtype
+ *   k          [B,H,T,dk]  io dtype
+ *   v          [B,H,T,dv]  io dtype
+ *   log_alpha  [B,H,T]     float32, log of the per-step decay alpha_t (<= 0
+ *                          for a decay; larger values are computed as given
+ *                          and may overflow)
+ *   lam        [B,H,T,L]   float32, lam[t][l] weights level l of query t
+ *   o          [B,H,T,dv]  io dtype, written
+ *   state_out  [B,H,Ls,dv,dk] float32 or NULL: the Fenwick level states of
+ *              position T (slot i = level i+1; bucket of level l is non-empty
+ *              iff bit l-1 of T is set; each decayed to token T-1), ready for
+ *              ll_attn_decode_step at t = T.  Empty levels are written as 0.
+ *   scale_out  [B,H,Ls]    float32 or NULL (required iff state_out): lazy
+ *              decay scale of each slot, written as 1 (non-empty) or 0 (empty).
+ *   workspace  device scratch of >= ll_attn_fwd_workspace_size(shape) bytes,
+ *              256-byte aligned, caller-owned, contents need not be cleared.
+ * Requires Ls >= bit_length(T) when state_out is given. */
+LL_API ll_status ll_attn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                      const float* log_alpha, const float* lam, void* o, float* state_out,
+                      float* scale_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step of log-linear Mamba-2 for every (b, h).
+ *   B, H, dk, dv  as above (dk, dv in {16, 32, 64, 128}); Ls stored levels
+ *   io            dtype of q, k, v, o
+ *   t      [B]          int64, position of this token in each batch row
+ *   q, k   [B,H,dk]     io dtype;   v [B,H,dv] io dtype
+ *   log_alpha [B,H]     float32
+ *   lam    [B,H,Ls+1]   float32, lam[0] weights the token itself (level 0)
+ *   states [B,H,Ls,dv,dk] float32, in/out.  Slot i holds level i+1 as
+ *          S_stored with true state = scale * S_stored; on entry the
+ *          non-empty slots are the set bits of t (levels of query t), decayed
+ *          to t-1.  On exit they describe position t+1.
+ *   scales [B,H,Ls]     float32, in/out, the lazy per-slot scales.
+ *   o      [B,H,dv]     io dtype, written.
+ * Per (b,h) the step reads the non-empty states once and writes one merged
+ * state (level ctz(t+1)+1).  A position with t+1 >= 2^Ls or t < 0 sets the
+ * device error word (LL_ERR_DEVICE) and leaves that row untouched. */
+LL_API ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,
+                              const void* q, const void* k, const void* v, const float* log_alpha,
+                              const float* lam, float* states, float* scales, void* o, void* stream);
+
+/* Bytes of workspace ll_gdn_fwd needs for `shape` (0 on invalid shape). */
+LL_API size_t ll_gdn_fwd_workspace_size(const ll_shape* shape);
+
+/* Log-Linear Gated DeltaNet forward (reading A), same layouts as
+ * ll_attn_fwd plus
+ *   beta  [B,H,T] float32, delta-rule write strength.
+ * shape->Ls must be 0 (no state export).  Keys are expected to be
+ * L2-normalised (as in Gated DeltaNet); this is not checked. */
+LL_API ll_status ll_gdn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                     const float* log_alpha, const float* beta, const float* lam, void* o,
+                     void* workspace, size_t ws_bytes, void* stream);
+
+#ifdef __cplusplus
+}
+#endif
+
+#endif /* LL_ATTN_H */

@@ -6,14 +6,12 @@ that ABI; ``synth`` draws seeded synthetic inputs.  Importing the package does
 not load the library; ``binding.lib()`` does, and raises if it is missing.
 """
 
-__all__ = ["binding", "synth"]
+import importlib
+
+__all__ = ["binding", "synth", "build"]
 
 
 def __getattr__(name):
-    if name == "binding":
-        from . import binding
-        return binding
-    if name == "synth":
-        from . import synth
-        return synth
+    if name in __all__:
+        return importlib.import_module(f"{__name__}.{name}")
     raise AttributeError(name)

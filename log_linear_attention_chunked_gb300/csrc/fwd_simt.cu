@@ -1,0 +1,311 @@
+// Chunked log-linear Mamba-2 forward on CUDA cores (float32 FMA throughout).
+//
+// This is the exact-precision path (float32 io, 1e-5 budget) and the path for
+// shapes the tensor-core kernel does not take.  Algorithm ("Log-Linear
+// Attention" study note §3-4 parallel form, computed chunk-wise as in the
+// gist.science (zh) summary §2.3: dense inside a chunk, O(log(T/C)) state
+// passes between chunks):
+//
+//   chunk c (Ce tokens, cs = inclusive cumsum of log_alpha inside the chunk)
+//   (1) intra   : o_i += sum_{j<=i in c} (q_i.k_j) exp(cs_i - cs_j) lam_i[bitlen(i^j)] v_j
+//   (2) state   : S_c  = sum_{j in c} exp(cs_end - cs_j) v_j k_j^T          [dv x dk]
+//   (3) Fenwick : F_c  = S_c + sum_{m < cto(c)} exp(dec_m) F_{c - 2^m}
+//                 F_c covers the 2^cto(c) chunks ending at c, decayed to the
+//                 end of chunk c; G_c is the sum of log_alpha over that block.
+//   (4) inter   : for every set bit h of c, the level  log2(Ce)+1+h  bucket of
+//                 every query in chunk c is the block of F_e,
+//                 e = (c with bits 0..h cleared) + 2^h - 1, and
+//                 o_i += lam_i[log2(Ce)+1+h] exp(cs_i + D_h) F_e q_i,
+//                 D_h = sum of G over the lower set bits of c (decay from the
+//                 end of e to the start of chunk c).
+//   (5) export  : the level states of position T are F nodes of the Fenwick
+//                 prefix query of N = T/Ce, decayed to token T-1.
+//
+// Cumulative decays are kept in double: the inputs and outputs are float32 and
+// the exponent of a decay factor must not lose the absolute accuracy that a
+// float32 running sum would lose at long range.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace llattn {
+
+namespace {
+
+constexpr int kThreads = 256;
+
+// The SIMT kernels stage a chunk of q, k, v in shared memory; chunks longer
+// than this many elements per operand are processed as shorter chunks (the
+// result does not depend on the chunk length).
+constexpr int kMaxChunkElems = 8192;
+
+struct SimtPlan {
+  int Ce, N, lc;  // effective chunk, #chunks, log2(Ce)
+  size_t off_S, off_F, off_tot, off_G, off_O, total;
+};
+
+SimtPlan plan_of(const ll_shape& s) {
+  SimtPlan p{};
+  int d = std::max(s.dk, s.dv);
+  p.Ce = s.chunk;
+  while (p.Ce * d > kMaxChunkElems && p.Ce > 16) p.Ce >>= 1;
+  p.N = s.T / p.Ce;
+  p.lc = ilog2(p.Ce);
+  const size_t BH = (size_t)s.B * s.H;
+  const size_t mat = (size_t)s.dv * s.dk;
+  size_t off = 0;
+  p.off_S = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  p.off_F = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  p.off_tot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
+  p.off_G = off;   off = align_up(off + BH * p.N * sizeof(double), 256);
+  p.off_O = off;
+  if (s.io != LL_F32) off = align_up(off + BH * (size_t)s.T * s.dv * sizeof(float), 256);
+  p.total = off;
+  return p;
+}
+
+// (1) + (2): one CTA per (chunk, head).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restrict__ q, const IO* __restrict__ k,
+                                                              const IO* __restrict__ v,
+                                                              const float* __restrict__ log_alpha,
+                                                              const float* __restrict__ lam, float* o_intra,
+                                                              float* __restrict__ S, double* __restrict__ tot, int T,
+                                                              int dk, int dv, int L, int Ce) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int c = blockIdx.x;
+  const int N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int dkp = dk + 1, dvp = dv + 1, Cp = Ce + 1;
+
+  double* cs = reinterpret_cast<double*>(smem_raw);
+  float* wdec = reinterpret_cast<float*>(cs + Ce);
+  float* qs = wdec + Ce;
+  float* ks = qs + Ce * dkp;
+  float* vs = ks + Ce * dkp;
+  float* P = vs + Ce * dvp;
+
+  const size_t t0 = (size_t)c * Ce;
+  const size_t row0 = bh * T + t0;
+  if (tid == 0) {
+    double acc = 0.0;
+    for (int i = 0; i < Ce; ++i) {
+      acc += (double)log_alpha[row0 + i];
+      cs[i] = acc;
+    }
+    tot[bh * N + c] = acc;
+  }
+  for (int x = tid; x < Ce * dk; x += kThreads) {
+    int i = x / dk, f = x % dk;
+    qs[i * dkp + f] = to_f(q[(row0 + i) * dk + f]);
+    ks[i * dkp + f] = to_f(k[(row0 + i) * dk + f]);
+  }
+  for (int x = tid; x < Ce * dv; x += kThreads) {
+    int i = x / dv, e = x % dv;
+    vs[i * dvp + e] = to_f(v[(row0 + i) * dv + e]);
+  }
+  __syncthreads();
+  for (int j = tid; j < Ce; j += kThreads) wdec[j] = expf((float)(cs[Ce - 1] - cs[j]));
+
+  // masked scores P[i][j]
+  for (int x = tid; x < Ce * Ce; x += kThreads) {
+    int i = x / Ce, j = x % Ce;
+    float p = 0.f;
+    if (j <= i) {
+      float dot = 0.f;
+      for (int f = 0; f < dk; ++f) dot = fmaf(qs[i * dkp + f], ks[j * dkp + f], dot);
+      int lv = bitlen((unsigned)(i ^ j));
+      p = dot * expf((float)(cs[i] - cs[j])) * lam[(row0 + i) * L + lv];
+    }
+    P[i * Cp + j] = p;
+  }
+  __syncthreads();
+
+  // intra output
+  for (int x = tid; x < Ce * dv; x += kThreads) {
+    int i = x / dv, e = x % dv;
+    float acc = 0.f;
+    for (int j = 0; j <= i; ++j) acc = fmaf(P[i * Cp + j], vs[j * dvp + e], acc);
+    o_intra[(row0 + i) * dv + e] = acc;
+  }
+
+  // chunk state S_c[e][f] = sum_j wdec_j v_j[e] k_j[f]
+  float* Sc = S + (bh * N + c) * (size_t)dv * dk;
+  for (int x = tid; x < dv * dk; x += kThreads) {
+    int e = x / dk, f = x % dk;
+    float acc = 0.f;
+    for (int j = 0; j < Ce; ++j) acc = fmaf(wdec[j] * vs[j * dvp + e], ks[j * dkp + f], acc);
+    Sc[x] = acc;
+  }
+}
+
+// (3): sequential over chunks, parallel over matrix elements and heads.
+__global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __restrict__ S, float* __restrict__ F,
+                                                                const double* __restrict__ tot,
+                                                                double* __restrict__ G, int N, int mat) {
+  extern __shared__ double Gs[];  // [N]
+  const size_t bh = blockIdx.y;
+  if (threadIdx.x == 0) {
+    for (int i = 0; i < N; ++i) {
+      double g = tot[bh * N + i];
+      for (int m = 0; (i >> m) & 1; ++m) g += Gs[i - (1 << m)];
+      Gs[i] = g;
+    }
+  }
+  __syncthreads();
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < N; i += kThreads) G[bh * N + i] = Gs[i];
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  if (idx >= mat) return;
+  const float* Sb = S + bh * N * (size_t)mat;
+  float* Fb = F + bh * N * (size_t)mat;
+  for (int i = 0; i < N; ++i) {
+    float acc = Sb[(size_t)i * mat + idx];
+    double dec = tot[bh * N + i];
+    for (int m = 0; (i >> m) & 1; ++m) {
+      const int j = i - (1 << m);
+      acc = fmaf(expf((float)dec), Fb[(size_t)j * mat + idx], acc);
+      dec += Gs[j];
+    }
+    Fb[(size_t)i * mat + idx] = acc;
+  }
+}
+
+// (4): one CTA per (chunk, head); adds the inter-chunk levels to the intra
+// result and writes o.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restrict__ q,
+                                                              const float* __restrict__ log_alpha,
+                                                              const float* __restrict__ lam,
+                                                              const float* o_intra,
+                                                              const float* __restrict__ F,
+                                                              const double* __restrict__ G, IO* o, int T,
+                                                              int dk, int dv, int L, int Ce, int lc) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int c = blockIdx.x;
+  const int N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int dkp = dk + 1;
+  double* cs = reinterpret_cast<double*>(smem_raw);
+  float* w = reinterpret_cast<float*>(cs + Ce);
+  float* qs = w + Ce;
+  float* Fs = qs + Ce * dk;
+  float* Oc = Fs + dv * dkp;
+
+  const size_t row0 = bh * T + (size_t)c * Ce;
+  if (tid == 0) {
+    double acc = 0.0;
+    for (int i = 0; i < Ce; ++i) {
+      acc += (double)log_alpha[row0 + i];
+      cs[i] = acc;
+    }
+  }
+  for (int x = tid; x < Ce * dk; x += kThreads) qs[x] = to_f(q[row0 * dk + x]);
+  for (int x = tid; x < Ce * dv; x += kThreads) Oc[x] = o_intra[row0 * dv + x];
+  __syncthreads();
+
+  const size_t mat = (size_t)dv * dk;
+  double D = 0.0;
+  for (int h = 0; (c >> h) != 0; ++h) {
+    if (!((c >> h) & 1)) continue;
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    const float* Fe = F + (bh * N + e) * mat;
+    for (int x = tid; x < (int)mat; x += kThreads) Fs[(x / dk) * dkp + (x % dk)] = Fe[x];
+    for (int i = tid; i < Ce; i += kThreads)
+      w[i] = lam[(row0 + i) * L + lc + 1 + h] * expf((float)(cs[i] + D));
+    __syncthreads();
+    for (int x = tid; x < Ce * dv; x += kThreads) {
+      int i = x / dv, ev = x % dv;
+      float acc = 0.f;
+      for (int f = 0; f < dk; ++f) acc = fmaf(Fs[ev * dkp + f], qs[i * dk + f], acc);
+      Oc[x] = fmaf(w[i], acc, Oc[x]);
+    }
+    D += G[bh * N + e];
+    __syncthreads();
+  }
+  for (int x = tid; x < Ce * dv; x += kThreads) o[row0 * dv + x] = from_f<IO>(Oc[x]);
+}
+
+// (5): level states of position T (= N chunks), decayed to token T-1.
+__global__ void __launch_bounds__(kThreads) simt_export_kernel(const float* __restrict__ F,
+                                                               const double* __restrict__ G,
+                                                               float* __restrict__ state_out,
+                                                               float* __restrict__ scale_out, int N, int mat, int Ls,
+                                                               int lc) {
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  double D = 0.0;
+  for (int slot = 0; slot < Ls; ++slot) {
+    const int h = slot + 1 - (lc + 1);  // level slot+1 = lc + 1 + h
+    float val = 0.f, sc = 0.f;
+    if (h >= 0 && h < 31 && ((N >> h) & 1)) {
+      const int e = ((N >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+      if (idx < mat) val = expf((float)D) * F[(bh * N + e) * (size_t)mat + idx];
+      sc = 1.f;
+      D += G[bh * N + e];
+    }
+    if (idx < mat) state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
+  }
+}
+
+template <typename IO>
+ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
+  const ll_shape& s = a.s;
+  unsigned char* ws = static_cast<unsigned char*>(a.ws);
+  float* S = reinterpret_cast<float*>(ws + p.off_S);
+  float* F = reinterpret_cast<float*>(ws + p.off_F);
+  double* tot = reinterpret_cast<double*>(ws + p.off_tot);
+  double* G = reinterpret_cast<double*>(ws + p.off_G);
+  float* o_intra = (s.io == LL_F32) ? static_cast<float*>(a.o) : reinterpret_cast<float*>(ws + p.off_O);
+  const int BH = s.B * s.H;
+  const int Ce = p.Ce;
+  const int mat = s.dv * s.dk;
+
+  size_t sm1 = Ce * sizeof(double) + Ce * sizeof(float) +
+               sizeof(float) * ((size_t)2 * Ce * (s.dk + 1) + (size_t)Ce * (s.dv + 1) + (size_t)Ce * (Ce + 1));
+  LL_CUDA_OK(cudaFuncSetAttribute(simt_chunk_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
+  simt_chunk_kernel<IO><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
+      static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.lam,
+      o_intra, S, tot, s.T, s.dk, s.dv, s.L, Ce);
+  LL_CUDA_OK(cudaGetLastError());
+
+  size_t sm2 = (size_t)p.N * sizeof(double);
+  if (sm2 > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
+  LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2));
+  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm2, a.stream>>>(S, F, tot, G, p.N,
+                                                                                              mat);
+  LL_CUDA_OK(cudaGetLastError());
+
+  size_t sm3 = Ce * sizeof(double) + Ce * sizeof(float) +
+               sizeof(float) * ((size_t)Ce * s.dk + (size_t)s.dv * (s.dk + 1) + (size_t)Ce * s.dv);
+  LL_CUDA_OK(cudaFuncSetAttribute(simt_inter_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
+  simt_inter_kernel<IO><<<dim3(p.N, BH), kThreads, sm3, a.stream>>>(static_cast<const IO*>(a.q), a.log_alpha,
+                                                                     a.lam, o_intra, F, G, static_cast<IO*>(a.o), s.T,
+                                                                     s.dk, s.dv, s.L, Ce, p.lc);
+  LL_CUDA_OK(cudaGetLastError());
+
+  if (a.state_out) {
+    simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
+        F, G, a.state_out, a.scale_out, p.N, mat, s.Ls, p.lc);
+    LL_CUDA_OK(cudaGetLastError());
+  }
+  return LL_OK;
+}
+
+}  // namespace
+
+size_t fwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
+
+int fwd_simt_launches(const ll_shape& s) { return s.Ls > 0 ? 4 : 3; }
+
+ll_status fwd_simt_launch(const FwdArgs& a) {
+  SimtPlan p = plan_of(a.s);
+  if (a.ws_bytes < p.total) return LL_ERR_WORKSPACE;
+  if (a.s.io == LL_F32) return launch_typed<float>(a, p);
+  return launch_typed<__nv_bfloat16>(a, p);
+}
+
+}  // namespace llattn

@@ -1,0 +1,109 @@
+"""The C ABI library loads, exports every declared symbol, and rejects bad
+arguments on the host (no GPU needed: nothing here launches a kernel)."""
+
+import ctypes
+import os
+import re
+
+import pytest
+
+ROOT = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+HEADER = os.path.join(ROOT, "include", "ll_attn.h")
+
+
+@pytest.fixture(scope="module")
+def L():
+    from log_linear_attention_chunked_gb300 import binding
+    if not os.path.exists(binding.LIB_PATH):
+        from log_linear_attention_chunked_gb300 import build
+        build.build()
+    return binding.lib()
+
+
+def declared_symbols():
+    src = open(HEADER).read()
+    return sorted(set(re.findall(r"LL_API\s+[\w\s\*]+?\b(ll_\w+)\s*\(", src)))
+
+
+def test_header_declares_the_abi():
+    from log_linear_attention_chunked_gb300 import binding
+    assert declared_symbols() == sorted(binding.SYMBOLS)
+
+
+def test_every_declared_symbol_is_exported(L):
+    for name in declared_symbols():
+        assert hasattr(L, name), name
+
+
+def test_version_and_status_strings(L):
+    from log_linear_attention_chunked_gb300 import binding
+    assert binding.ll_version() >= 100
+    for code in range(7):
+        assert binding.ll_status_str(code)
+    assert binding.ll_status_str(99) == "unknown status"
+
+
+def _shape(**kw):
+    from log_linear_attention_chunked_gb300 import binding
+    d = dict(B=1, H=2, T=64, dk=16, dv=16, L=7, chunk=16, Ls=0, io=binding.LL_F32)
+    d.update(kw)
+    return binding.make_shape(**d)
+
+
+def test_workspace_size_queries(L):
+    from log_linear_attention_chunked_gb300 import binding
+    assert binding.ll_attn_fwd_workspace_size(_shape()) > 0
+    assert binding.ll_attn_fwd_workspace_size(_shape(chunk=24)) == 0      # not a power of two
+    assert binding.ll_attn_fwd_workspace_size(_shape(T=72)) == 0          # T % chunk != 0
+    assert binding.ll_attn_fwd_workspace_size(_shape(L=6)) == 0           # too few levels for T=64
+    assert binding.ll_attn_fwd_workspace_size(_shape(dk=96)) == 0         # unsupported head dim
+    big = binding.ll_attn_fwd_workspace_size(_shape(B=1, H=16, T=16384, dk=128, dv=128, L=15, chunk=64,
+                                                    io=binding.LL_BF16))
+    assert big > 0
+
+
+FAKE = 0x7f0000000000  # never dereferenced: every case below fails a host-side check first
+
+
+def _fwd(L, shape, ptrs=None, ws=FAKE, ws_bytes=1 << 40, state=None, scale=None):
+    p = ptrs or [FAKE] * 6
+    vp = ctypes.c_void_p
+    return L.ll_attn_fwd(ctypes.byref(shape), *[vp(x) if x else None for x in p],
+                         vp(state) if state else None, vp(scale) if scale else None,
+                         vp(ws) if ws else None, ctypes.c_size_t(ws_bytes), None)
+
+
+def test_fwd_rejects_bad_args_on_host(L):
+    assert _fwd(L, _shape(chunk=24)) == 1
+    assert _fwd(L, _shape(T=0)) == 1
+    assert _fwd(L, _shape(dk=96)) == 2
+    assert _fwd(L, _shape(), ptrs=[FAKE, 0, FAKE, FAKE, FAKE, FAKE]) == 1       # null k
+    assert _fwd(L, _shape(), ptrs=[FAKE + 4, FAKE, FAKE, FAKE, FAKE, FAKE]) == 1  # misaligned q
+    assert _fwd(L, _shape(), ws=0) == 5                                         # no workspace
+    assert _fwd(L, _shape(), ws_bytes=16) == 5                                  # workspace too small
+    assert _fwd(L, _shape(), ws=FAKE + 16) == 5                                 # workspace not 256-aligned
+    assert _fwd(L, _shape(Ls=7), state=FAKE) == 1                               # state without scale
+    assert _fwd(L, _shape(Ls=6), state=FAKE, scale=FAKE) == 1                   # Ls < bit_length(T)
+
+
+def test_decode_rejects_bad_args_on_host(L):
+    vp = ctypes.c_void_p
+    args = [vp(FAKE)] * 10
+    assert L.ll_attn_decode_step(0, 1, 16, 16, 4, 0, *args) == 1
+    assert L.ll_attn_decode_step(1, 1, 96, 16, 4, 0, *args) == 2
+    assert L.ll_attn_decode_step(1, 1, 16, 16, 63, 0, *args) == 1
+    bad = list(args)
+    bad[3] = None
+    assert L.ll_attn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
+    bad = list(args)
+    bad[0] = vp(FAKE + 8)
+    assert L.ll_attn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
+
+
+def test_gdn_rejects_bad_args_on_host(L):
+    from log_linear_attention_chunked_gb300 import binding
+    vp = ctypes.c_void_p
+    s = _shape(Ls=3)
+    assert L.ll_gdn_fwd(ctypes.byref(s), *([vp(FAKE)] * 8), ctypes.c_size_t(1 << 40), None) == 1
+    s = _shape()
+    assert L.ll_gdn_fwd(ctypes.byref(s), *([vp(FAKE)] * 7), None, ctypes.c_size_t(0), None) in (2, 5)
