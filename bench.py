@@ -211,7 +211,8 @@ def main():
             return
         pool = oracle_pool(cores, cfg)
         # calibrate: size each step so that all steps take about a minute of wall time
-        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 8, seed=999)
+        oracle_sample(pool, cores, cfg["T"], cores, seed=998)  # workers finish their set-up
+        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 16, seed=999)
         row_wall = wall / n
         rows_per_step = max(cores, int(60.0 / max(args.steps, 1) / row_wall) // cores * cores)
         for i in range(args.warmup):
@@ -342,7 +343,8 @@ def main():
 
     cpu = None
     if pool is not None:
-        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 4, seed=999)
+        oracle_sample(pool, cores, cfg["T"], cores, seed=998)  # workers finish their set-up
+        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 16, seed=999)
         rows_total = max(cores, int(12.0 / (wall / n)))  # about 12 s of wall time on all cores
         tps, n, secs = oracle_sample(pool, cores, cfg["T"], rows_total)
         pool.close()
