@@ -149,6 +149,32 @@ LL_API ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dt
                               const void* q, const void* k, const void* v, const float* log_alpha,
                               const float* lam, float* states, float* scales, void* o, void* stream);
 
+/* Size in bytes of the fixed device scratch of ll_attn_fwd_noalloc. */
+#define LL_NOALLOC_SCRATCH_BYTES (32u << 20)
+
+/* ll_attn_fwd for callers that cannot allocate device memory.  The paper has
+ * no counterpart of this entry point; it exists for callers that can neither
+ * pass a workspace nor allocate one -- a host application that reserves all
+ * device memory for its own pool at start-up and forbids later cudaMalloc,
+ * a plugin of such a runtime with no allocator to hand down, or a loop where
+ * a cudaMalloc (which may synchronise the device) is not acceptable.
+ *   Arguments, layouts and results are those of ll_attn_fwd without
+ *   `workspace`/`ws_bytes`.  The scratch is a fixed array of
+ *   LL_NOALLOC_SCRATCH_BYTES inside the library's device image, held on every
+ *   GPU that loads the library until the process exits.  The call allocates
+ *   and frees nothing.
+ *   Returns LL_ERR_WORKSPACE when ll_attn_fwd_workspace_size(shape) exceeds
+ *   LL_NOALLOC_SCRATCH_BYTES (the shape is too large for the fixed scratch),
+ *   and LL_ERR_INVALID_ARG for an invalid shape.
+ *   All calls on a device share the one scratch array, which keeps the last
+ *   call's contents (the forward needs none of it cleared): calls whose
+ *   execution overlaps on the GPU (other streams, other host threads) race.
+ *   The first call on each device (with that device current) looks up the
+ *   array's device address; make that first call before any stream capture. */
+LL_API ll_status ll_attn_fwd_noalloc(const ll_shape* shape, const void* q, const void* k, const void* v,
+                                     const float* log_alpha, const float* lam, void* o, float* state_out,
+                                     float* scale_out, void* stream);
+
 /* Bytes of workspace ll_gdn_fwd needs for `shape` (0 on invalid shape). */
 LL_API size_t ll_gdn_fwd_workspace_size(const ll_shape* shape);
 

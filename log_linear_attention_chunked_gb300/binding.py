@@ -24,7 +24,7 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 
 # every symbol the header declares
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
-           "ll_attn_fwd", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd")
+           "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd")
 
 
 class LLError(RuntimeError):
@@ -64,6 +64,8 @@ def lib() -> ctypes.CDLL:
     L.ll_attn_fwd_launches.argtypes = [shp]
     L.ll_attn_fwd.restype = i32
     L.ll_attn_fwd.argtypes = [shp, vp, vp, vp, fp, fp, vp, fp, fp, vp, sz, vp]
+    L.ll_attn_fwd_noalloc.restype = i32
+    L.ll_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, fp, fp, vp, fp, fp, vp]
     L.ll_attn_decode_step.restype = i32
     L.ll_attn_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp, vp]
     L.ll_gdn_fwd_workspace_size.restype = sz
@@ -149,6 +151,34 @@ def ll_attn_fwd(q, k, v, log_alpha, lam, chunk: int, *, o=None, state_out=None, 
                            _ptr(state_out), _ptr(scale_out), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
                            _stream(q.device))
     _check(st, "ll_attn_fwd")
+    return o
+
+
+NOALLOC_SCRATCH_BYTES = 32 << 20  # LL_NOALLOC_SCRATCH_BYTES of the header
+
+
+def ll_attn_fwd_noalloc(q, k, v, log_alpha, lam, chunk: int, *, o, state_out=None, scale_out=None):
+    """ll_attn_fwd for callers that cannot allocate device memory: the library
+    uses its own fixed scratch array (NOALLOC_SCRATCH_BYTES per device) instead
+    of a workspace.  The caller passes every input and the output ``o``; this
+    wrapper allocates nothing either.  Overlapping calls on one device race."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    io = _io(q.dtype)
+    for x, n in ((q, "q"), (k, "k"), (v, "v"), (o, "o")):
+        _need(x, n, q.dtype)
+    _need(log_alpha, "log_alpha", torch.float32)
+    _need(lam, "lam", torch.float32)
+    Ls = 0
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32)
+        _need(scale_out, "scale_out", torch.float32)
+        Ls = state_out.shape[2]
+    shape = make_shape(B, H, T, dk, dv, L, chunk, Ls, io)
+    st = lib().ll_attn_fwd_noalloc(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(lam),
+                                   _ptr(o), _ptr(state_out), _ptr(scale_out), _stream(q.device))
+    _check(st, "ll_attn_fwd_noalloc")
     return o
 
 
