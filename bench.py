@@ -1,21 +1,27 @@
-"""Throughput of the log-linear Mamba-2 forward (T=16384, H=16, d=128, bf16).
+"""Throughput of the log-linear attention hot path on GB300.
 
     python bench.py [--gpus N] [--steps K] [--warmup W] [--impl ours|reference]
                     [--workload NAME]
 
-One step = one ll_attn_fwd call over the whole workload (all of the hot path:
-intra-chunk attention, chunk states, Fenwick tree, inter-chunk levels).
-Inputs are resident in HBM when a timed step starts; L2 is flushed between
-steps (a write of 2x the L2 size, outside the timed events).  Each step is
-timed with CUDA events on the launching stream; `value` = tokens of all
-ranks / max over ranks of the mean step time.  `e2e` times the same call with
-the inputs copied from pinned host memory and the output copied back, all
-inside the timed region.
+Default workload: the log-linear Mamba-2 forward at B=1, H=16, T=16384,
+d=128, bf16 in / float32 accumulate.  One step = one ll_attn_fwd call over the
+whole workload (every step of the hot path: intra-chunk attention, chunk
+states, the Fenwick node tree and the inter-chunk levels).  Other workloads:
+`decode_b64_t64k` (one ll_attn_decode_step for 64 x 32 heads with 17 stored
+levels, positions 65536 onward) and `gdn_bf16_t4k` (one ll_gdn_fwd).
 
-With torchrun (N > 1) every rank runs the same workload on its own GPU with
+Inputs are resident in HBM when a timed step starts.  The forward workloads
+flush L2 between steps (a write of 2x the L2 size, outside the timed
+events); the decode workload streams 2.3 GB of states, far larger than L2.
+Each step is timed with CUDA events on the launching stream; `value` = units
+of all ranks / max over ranks of the mean step time.  `e2e` times the same
+public call with its inputs copied from pinned host memory and its output
+copied back, all inside the timed region.
+
+Under torchrun (N > 1) every rank runs the same workload on its own GPU with
 no collective in the data path (weak scaling); a barrier brackets the timed
 region.  `--impl reference` times the float64 CPU oracle instead (rank 0
-only), on a bounded sample of query rows per step.
+only), on a bounded sample of the workload per step.
 """
 
 from __future__ import annotations
@@ -33,29 +39,45 @@ ROOT = os.path.dirname(os.path.abspath(__file__))
 if ROOT not in sys.path:
     sys.path.insert(0, ROOT)
 
-METRIC = "log-linear Mamba-2 fwd tokens/s at T=16K,H=16,d=128; % of roofline"
 PROFILES = os.path.join(ROOT, "profiles")
+METRICS = {
+    "mamba2": "log-linear Mamba-2 fwd tokens/s at T=16K,H=16,d=128; % of roofline",
+    "decode": "log-linear Mamba-2 Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); % of HBM roofline",
+    "gdn": "log-linear Gated DeltaNet fwd tokens/s (B=2, H=16, T=4096, d=128)",
+}
 
 
 # ----------------------------------------------------------------------------
-# algorithmic work of one forward (counted per (b, h), times B*H)
+# algorithmic work (counted per (b, h), times B*H)
 # ----------------------------------------------------------------------------
 def algorithmic_bytes(cfg) -> int:
-    """q, k, v read once, log_alpha and lam (float32) read once, o written once."""
+    """Forward: q, k, v read once, log_alpha and lam (float32) read once, o
+    written once; plus beta for Gated DeltaNet."""
     b_io = 2 if cfg["io"] == "bf16" else 4
-    d = cfg["dk"]
-    per_bh = cfg["T"] * (3 * d * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
+    per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
+    if cfg["kind"] == "gdn":
+        per_bh += cfg["T"] * 4
     return per_bh * cfg["B"] * cfg["H"]
 
 
 def algorithmic_flops(cfg) -> int:
-    """Causal pairs inside a chunk, chunk states, tree combines and the
-    popcount(c) non-empty inter-chunk levels of every chunk c."""
+    """Forward: causal pairs inside a chunk, chunk states, tree combines and
+    the popcount(c) non-empty inter-chunk levels of every chunk c."""
     T, C, d = cfg["T"], cfg["chunk"], cfg["dk"]
     N = T // C
     P = sum(bin(c).count("1") for c in range(N))
-    per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
+    if cfg["kind"] == "gdn":
+        per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d
+        per_bh = N * per_chunk + P * (6 * C * d * d + 2 * C * C * d)
+    else:
+        per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
     return per_bh * cfg["B"] * cfg["H"]
+
+
+def decode_bytes(B, H, d, Ls, t) -> int:
+    """One decode step: the popcount(t) non-empty states read once and one merged
+    state written (float32), q, k, v and o (bf16), log_alpha and lam (float32)."""
+    return B * H * ((bin(t).count("1") + 1) * d * d * 4 + 3 * d * 2 + 4 * (Ls + 1) + 4 + d * 2)
 
 
 def measured_peaks():
@@ -63,8 +85,8 @@ def measured_peaks():
     if os.path.exists(path):
         with open(path) as f:
             p = json.load(f)
-        return p["hbm_gbs"], p["bf16_tflops"], "measured"
-    return 6800.0, 1900.0, "fallback"
+        return p["hbm_gbs"], p["bf16_tflops"], p.get("sm_max_mhz", 2070.0), "measured"
+    return 6800.0, 1900.0, 2070.0, "fallback"
 
 
 def kernel_source_hash() -> str:
@@ -139,23 +161,48 @@ class ClockSampler:
 
 
 # ----------------------------------------------------------------------------
-# oracle timing (CPU baseline / reference arm)
+# oracle timing (CPU baseline / reference arm), in spawned single-threaded workers
 # ----------------------------------------------------------------------------
 _W = {}
 
 
 def _oracle_init(cfg, tag):
     """Worker set-up (untimed): draw one (b, h) slice of the workload."""
+    import numpy as np
     from log_linear_attention_chunked_gb300 import synth
+    _W["cfg"] = cfg
+    if cfg["kind"] == "decode":
+        rng = np.random.default_rng(7)
+        d, Ls, S = cfg["dk"], cfg["Ls"], cfg["steps"]
+        _W["x"] = (rng.standard_normal((Ls, d, d)) * 0.01, rng.standard_normal((S, d)) / np.sqrt(d),
+                   rng.standard_normal((S, d)) / np.sqrt(d), rng.standard_normal((S, d)),
+                   -np.log1p(np.exp(rng.standard_normal(S))), np.log1p(np.exp(rng.standard_normal((S, Ls + 1)))))
+        return
     inp = synth.make_inputs(dict(cfg, B=1, H=1), tag=tag)
-    _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in ("q", "k", "v", "log_alpha", "lam"))
+    names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] == "gdn" else ())
+    _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in names)
 
 
-def _oracle_rows_worker(rows):
-    from oracle import mamba2
-    q, k, v, la, lam = _W["x"]
-    mamba2.forward_rows(q, k, v, la, lam, rows)
-    return len(rows)
+def _oracle_worker(job):
+    """One bounded piece of oracle work; returns the number of tokens it covered."""
+    cfg = _W["cfg"]
+    if cfg["kind"] == "mamba2":
+        from oracle import mamba2
+        q, k, v, la, lam = _W["x"]
+        mamba2.forward_rows(q, k, v, la, lam, job)
+        return float(len(job))
+    if cfg["kind"] == "gdn":
+        from oracle import gdn
+        q, k, v, la, lam, beta = _W["x"]
+        gdn.gdn_rows_A(q, k, v, beta, la, lam, job)
+        return float(len(job))
+    from oracle import decode
+    S, q, k, v, la, lam = _W["x"]
+    n = job
+    t0 = cfg["T"]
+    ne = [((t0 >> i) & 1) == 1 for i in range(S.shape[0])]
+    decode.decode_steps(S, ne, t0, q[:n], k[:n], v[:n], la[:n], lam[:n])
+    return n / cfg["H"]  # one (b, h) step is 1/H of a token of a batch row
 
 
 def oracle_pool(cores: int, cfg: dict, tag: str = "oracle"):
@@ -166,18 +213,126 @@ def oracle_pool(cores: int, cfg: dict, tag: str = "oracle"):
     return mp.get_context("spawn").Pool(cores, initializer=_oracle_init, initargs=(cfg, tag))
 
 
-def oracle_sample(pool, cores, T, rows_total, seed=0):
-    """Time the float64 oracle (row-restricted dense form) on `rows_total`
-    query rows drawn uniformly from [0, T), split over `cores` processes.
-    Returns (rows per second of wall time, rows, seconds)."""
+def oracle_jobs(cfg, cores, size, seed):
     import numpy as np
     rng = np.random.default_rng(seed)
-    per = max(1, rows_total // cores)
-    jobs = [sorted(int(x) for x in rng.integers(0, T, per)) for _ in range(cores)]
+    if cfg["kind"] in ("mamba2", "gdn"):
+        return [sorted(int(x) for x in rng.integers(0, cfg["T"], size)) for _ in range(cores)]
+    return [min(cfg["steps"], size) for _ in range(cores)]
+
+
+def oracle_sample(pool, cfg, cores, size, seed=0):
+    """Run `cores` jobs of `size` units in parallel; returns (tokens/s, tokens, seconds)."""
+    jobs = oracle_jobs(cfg, cores, size, seed)
     t0 = time.perf_counter()
-    n = sum(pool.map(_oracle_rows_worker, jobs, chunksize=1))
+    n = sum(pool.map(_oracle_worker, jobs, chunksize=1))
     wall = time.perf_counter() - t0
     return n / wall, n, wall
+
+
+def calibrate(pool, cfg, cores, budget_s):
+    """Job size so that one sample takes about `budget_s` seconds of wall time."""
+    small = 16
+    cap = cfg.get("steps", 256) if cfg["kind"] == "decode" else 10 ** 6
+    oracle_sample(pool, cfg, cores, 1, seed=998)  # workers finish their set-up
+    _, n, wall = oracle_sample(pool, cfg, cores, small, seed=999)
+    return int(min(cap, max(1, budget_s / (wall / small))))
+
+
+def sample_desc(cfg, size):
+    if cfg["kind"] == "mamba2":
+        return f"{size} uniformly drawn query rows per process of the row-restricted dense float64 form"
+    if cfg["kind"] == "gdn":
+        return (f"{size} uniformly drawn query rows per process of the row-restricted float64 reading-A form "
+                "(each call builds its unit-triangular system)")
+    return f"{size} float64 decode steps of one (b, h) per process"
+
+
+# ----------------------------------------------------------------------------
+# GPU workloads
+# ----------------------------------------------------------------------------
+def forward_workload(cfg, dev, rank, binding, synth, torch):
+    """Forward (Mamba-2 or Gated DeltaNet): device and pinned host inputs, step functions."""
+    gdn = cfg["kind"] == "gdn"
+    inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
+    names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if gdn else ())
+    host = {n: inp_host[n].pin_memory() for n in names}
+    g = {n: host[n].to(dev) for n in names}
+    Bn, H, T, dk = g["q"].shape
+    dv = g["v"].shape[-1]
+    shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], 0, binding._io(g["q"].dtype))
+    if gdn:
+        ws = binding.alloc_workspace(binding.ll_gdn_fwd_workspace_size(shape), dev)
+        launches = 2
+    else:
+        ws = binding.alloc_workspace(binding.ll_attn_fwd_workspace_size(shape), dev)
+        launches = binding.ll_attn_fwd_launches(shape)
+    o = torch.empty(Bn, H, T, dv, dtype=g["q"].dtype, device=dev)
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+
+    def step(i=0):
+        if gdn:
+            binding.ll_gdn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
+                               workspace=ws)
+        else:
+            binding.ll_attn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["lam"], cfg["chunk"], o=o, workspace=ws)
+
+    def e2e_step(i=0):
+        for n in names:
+            g[n].copy_(host[n], non_blocking=True)
+        step(i)
+        o_host.copy_(o, non_blocking=True)
+
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = o_host.numel() * o_host.element_size()
+    return dict(step=step, e2e_step=e2e_step, units=Bn * H * T, h2d=h2d, d2h=d2h, launches=launches, flush=True,
+                abytes=algorithmic_bytes(cfg), aflops=algorithmic_flops(cfg))
+
+
+def decode_workload(cfg, dev, rank, binding, synth, torch):
+    """Decode: 2.3 GB of level states (random values: the work of a step does not
+    depend on them), per-step inputs drawn once, positions 65536 onward."""
+    Bn, H, d, Ls, S = cfg["B"], cfg["H"], cfg["dk"], cfg["Ls"], cfg["steps"]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(cfg["seed"] + rank)
+    states = torch.randn(Bn, H, Ls, d, d, device=dev, generator=gen) * 0.01
+    scales = torch.ones(Bn, H, Ls, device=dev)
+    dec = synth.make_decode_inputs(cfg, device="cpu", B=Bn, H=H)
+    names = ("q", "k", "v", "log_alpha", "lam")
+    host = {n: dec[n].pin_memory() for n in names}
+    g = {n: host[n].to(dev) for n in names}
+    t_host = torch.tensor([[cfg["T"] + i] * Bn for i in range(S)], dtype=torch.int64).pin_memory()
+    t_dev = t_host.to(dev)
+    o = torch.empty(Bn, H, d, dtype=g["q"].dtype, device=dev)
+    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
+    pos = [0]
+
+    def step(i=0):
+        s = pos[0] % S
+        binding.ll_attn_decode_step(t_dev[s], g["q"][s], g["k"][s], g["v"][s], g["log_alpha"][s], g["lam"][s],
+                                    states, scales, o=o)
+        pos[0] += 1
+
+    def reset():
+        pos[0] = 0
+        scales.fill_(1.0)
+
+    xs = {n: torch.empty_like(g[n][0]) for n in names}
+    t_x = torch.empty_like(t_dev[0])
+
+    def e2e_step(i=0):
+        s = pos[0] % S
+        for n in names:
+            xs[n].copy_(host[n][s], non_blocking=True)
+        t_x.copy_(t_host[s], non_blocking=True)
+        binding.ll_attn_decode_step(t_x, xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["lam"], states, scales, o=o)
+        o_host.copy_(o, non_blocking=True)
+        pos[0] += 1
+
+    h2d = sum(host[n][0].numel() * host[n].element_size() for n in names) + Bn * 8
+    d2h = o_host.numel() * o_host.element_size()
+    return dict(step=step, e2e_step=e2e_step, reset=reset, units=Bn, h2d=h2d, d2h=d2h, launches=1, flush=False,
+                step_bytes=lambda i: decode_bytes(Bn, H, d, Ls, cfg["T"] + (i % S)))
 
 
 # ----------------------------------------------------------------------------
@@ -199,10 +354,16 @@ def main():
 
     from log_linear_attention_chunked_gb300 import synth
     cfg = dict(synth.WORKLOADS[args.workload])
+    kind = cfg["kind"]
+    metric = METRICS[kind]
     config = {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "dk": cfg["dk"],
               "dv": cfg["dv"], "chunk": cfg["chunk"], "L": cfg["L"], "io": cfg["io"],
-              "l2": "flushed between steps (write of 2x L2)", "parallelism": f"replicas x{world} (b,h) weak"}
-    tokens_per_step = cfg["B"] * cfg["H"] * cfg["T"]
+              "parallelism": f"replicas x{world} (b,h) weak"}
+    if kind == "decode":
+        config.update(Ls=cfg["Ls"], positions=f"{cfg['T']}..{cfg['T'] + cfg['steps'] - 1} cycled",
+                      l2="states (2.3 GB) larger than L2, no flush")
+    else:
+        config["l2"] = "flushed between steps (write of 2x L2)"
 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
@@ -210,28 +371,23 @@ def main():
         if rank != 0:
             return
         pool = oracle_pool(cores, cfg)
-        # calibrate: size each step so that all steps take about a minute of wall time
-        oracle_sample(pool, cores, cfg["T"], cores, seed=998)  # workers finish their set-up
-        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 16, seed=999)
-        row_wall = wall / n
-        rows_per_step = max(cores, int(60.0 / max(args.steps, 1) / row_wall) // cores * cores)
+        size = calibrate(pool, cfg, cores, budget_s=60.0 / max(args.steps + args.warmup, 1))
         for i in range(args.warmup):
-            oracle_sample(pool, cores, cfg["T"], cores, seed=1000 + i)
-        times, rows = [], 0
+            oracle_sample(pool, cfg, cores, size, seed=1000 + i)
+        times, units = [], 0.0
         for i in range(args.steps):
-            _, n, wall = oracle_sample(pool, cores, cfg["T"], rows_per_step, seed=i)
+            _, n, wall = oracle_sample(pool, cfg, cores, size, seed=i)
             times.append(wall)
-            rows += n
+            units += n
         pool.close()
         total = sum(times)
-        value = rows / total
-        line = {"impl": "reference", "metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
+        value = units / total
+        line = {"impl": "reference", "metric": metric, "value": value, "unit": "tokens/s", "n_gpus": args.gpus,
                 "steps": args.steps, "warmup": args.warmup, "ms_per_step": 1e3 * total / args.steps,
                 "higher_is_better": True, "scaling": "weak", "vs_baseline": None, "dtype": "f64",
                 "data": "synthetic", "config": config,
                 "cpu_baseline": {"value": value, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-                                 "sample": f"{rows_per_step} uniformly drawn query rows per step of the row-restricted "
-                                           f"dense float64 form, {cores} single-threaded processes"},
+                                 "sample": sample_desc(cfg, size) + f", {cores} single-threaded processes"},
                 "e2e": {"value": value, "unit": "tokens/s", "h2d_bytes_per_step": 0, "d2h_bytes_per_step": 0}}
         print(json.dumps(line))
         return
@@ -250,34 +406,27 @@ def main():
     torch.cuda.set_device(dev)
     binding.lib()
 
-    inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
-    names = ("q", "k", "v", "log_alpha", "lam")
-    host = {n: inp_host[n].pin_memory() for n in names}
-    g = {n: host[n].to(dev) for n in names}
-    Bn, H, T, dk = g["q"].shape
-    dv = g["v"].shape[-1]
-    shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], 0, binding._io(g["q"].dtype))
-    ws = binding.alloc_workspace(binding.ll_attn_fwd_workspace_size(shape), dev)
-    o = torch.empty(Bn, H, T, dv, dtype=g["q"].dtype, device=dev)
-    o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
-    launches_per_call = binding.ll_attn_fwd_launches(shape)
+    if kind == "decode":
+        w = decode_workload(cfg, dev, rank, binding, synth, torch)
+    else:
+        w = forward_workload(cfg, dev, rank, binding, synth, torch)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
-    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev)
+    flush = torch.empty(2 * l2 // 4, dtype=torch.float32, device=dev) if w["flush"] else None
     stream = torch.cuda.current_stream(dev)
-
-    def step():
-        binding.ll_attn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["lam"], cfg["chunk"], o=o, workspace=ws)
 
     def barrier():
         if world > 1:
             torch.distributed.barrier()
 
-    for _ in range(args.warmup):
-        flush.fill_(1.0)
-        step()
+    for i in range(args.warmup):
+        if flush is not None:
+            flush.fill_(1.0)
+        w["step"](i)
     torch.cuda.synchronize()
     if binding.ll_last_device_error() != 0:
         raise RuntimeError("device error during warm-up")
+    if "reset" in w:
+        w["reset"]()
 
     ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
     sampler = ClockSampler(dev.index)
@@ -286,9 +435,10 @@ def main():
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
     for i in range(args.steps):
-        flush.fill_(float(i))
+        if flush is not None:
+            flush.fill_(float(i))
         ev[i][0].record(stream)
-        step()
+        w["step"](i)
         ev[i][1].record(stream)
     torch.cuda.synchronize()
     wall = time.perf_counter() - wall0
@@ -302,11 +452,11 @@ def main():
         t = torch.tensor([mean_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         mean_ms = float(t.item())
-    value = tokens_per_step * world / (mean_ms * 1e-3)
+    value = w["units"] * world / (mean_ms * 1e-3)
 
-    # end to end: pinned host inputs -> device -> forward -> host output
-    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
-    d2h = o_host.numel() * o_host.element_size()
+    # end to end through the public call: host inputs in, host output out
+    if "reset" in w:
+        w["reset"]()
     e2e_steps = max(3, min(args.steps, 50))
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(e2e_steps + 2):
@@ -314,10 +464,7 @@ def main():
             barrier()
             torch.cuda.synchronize()
             e0.record(stream)
-        for n in names:
-            g[n].copy_(host[n], non_blocking=True)
-        step()
-        o_host.copy_(o, non_blocking=True)
+        w["e2e_step"](i)
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = e0.elapsed_time(e1) / e2e_steps
@@ -325,40 +472,52 @@ def main():
         t = torch.tensor([e2e_ms], device=dev)
         torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
         e2e_ms = float(t.item())
-    e2e = {"value": tokens_per_step * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": h2d,
-           "d2h_bytes_per_step": d2h, "ms_per_step": e2e_ms}
+    e2e = {"value": w["units"] * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": w["h2d"],
+           "d2h_bytes_per_step": w["d2h"], "ms_per_step": e2e_ms}
 
-    # roofline of the dominant kernel (one launch per call on the tensor-core path)
-    hbm, bf16, src = measured_peaks()
-    abytes = algorithmic_bytes(cfg)
-    aflops = algorithmic_flops(cfg)
-    achieved_gbs = abytes / (mean_ms * 1e-3) / 1e9
+    # roofline of the dominant kernel
+    hbm, bf16, sm_mhz, src = measured_peaks()
     traffic, kname = ncu_traffic(args.workload)
-    roofline = {"bound": "hbm", "achieved": achieved_gbs, "peak": hbm, "unit": "GB/s", "frac": achieved_gbs / hbm,
-                "traffic": traffic, "peak_source": f"{src} (HBM copy)",
-                "algorithmic_bytes_per_launch": abytes, "launches_per_step": launches_per_call,
-                "kernel": kname,
-                "tensor": {"achieved_tflops": aflops / (mean_ms * 1e-3) / 1e12, "peak_tflops": bf16,
-                           "frac": aflops / (mean_ms * 1e-3) / 1e12 / bf16, "algorithmic_flops": aflops}}
+    if kind == "decode":
+        abytes = sum(w["step_bytes"](i) for i in range(args.steps)) / args.steps
+        achieved = abytes / (mean_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": traffic, "peak_source": f"{src} (HBM copy)",
+                    "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname}
+    elif kind == "gdn":
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
+        aflops = w["aflops"]
+        achieved = aflops / (mean_ms * 1e-3) / 1e12
+        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                    "frac": achieved / alu_peak, "traffic": traffic,
+                    "peak_source": f"float32 FMA: {sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz ({src} clock)",
+                    "algorithmic_flops_per_step": aflops, "launches_per_step": w["launches"], "kernel": kname,
+                    "hbm": {"achieved_gbs": w["abytes"] / (mean_ms * 1e-3) / 1e9, "peak": hbm}}
+    else:
+        abytes, aflops = w["abytes"], w["aflops"]
+        achieved = abytes / (mean_ms * 1e-3) / 1e9
+        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                    "traffic": traffic, "peak_source": f"{src} (HBM copy)",
+                    "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname,
+                    "tensor": {"achieved_tflops": aflops / (mean_ms * 1e-3) / 1e12, "peak_tflops": bf16,
+                               "frac": aflops / (mean_ms * 1e-3) / 1e12 / bf16, "algorithmic_flops": aflops}}
 
     cpu = None
     if pool is not None:
-        oracle_sample(pool, cores, cfg["T"], cores, seed=998)  # workers finish their set-up
-        _, n, wall = oracle_sample(pool, cores, cfg["T"], cores * 16, seed=999)
-        rows_total = max(cores, int(12.0 / (wall / n)))  # about 12 s of wall time on all cores
-        tps, n, secs = oracle_sample(pool, cores, cfg["T"], rows_total)
+        size = calibrate(pool, cfg, cores, budget_s=12.0)
+        tps, n, secs = oracle_sample(pool, cfg, cores, size)
         pool.close()
         cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": f"{n} uniformly drawn query rows of the row-restricted dense float64 form "
-                         f"({secs:.1f} s wall, {cores} single-threaded processes)"}
+               "sample": sample_desc(cfg, size) + f" ({secs:.1f} s wall, {cores} single-threaded processes)"}
 
     if rank == 0:
-        line = {"metric": METRIC, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+        line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
                 "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": cfg["io"] if cfg["io"] != "f32" else "f32", "data": "synthetic",
-                "config": config, "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": launches_per_call * args.steps,
-                "wall_s_timed_region": wall, "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
+                "vs_baseline": None, "dtype": cfg["io"], "data": "synthetic", "config": config,
+                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
+                "gpu_launches": w["launches"] * args.steps, "wall_s_timed_region": wall,
+                "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
         print(json.dumps(line))
     if world > 1:
         torch.distributed.destroy_process_group()
