@@ -63,8 +63,9 @@ constexpr uint32_t kOffF1 = kOffF0 + kTileBytes;
 constexpr uint32_t kAuxBytes = kTile * 4 + kTile * kLmax * 4;  // log_alpha row + lambda rows
 constexpr uint32_t kOffAux0 = kOffF1 + kTileBytes;
 constexpr uint32_t kOffAux1 = kOffAux0 + kAuxBytes;
-constexpr uint32_t kOffCs = kOffAux1 + kAuxBytes;      // float[128]
-constexpr uint32_t kOffMisc = kOffCs + kTile * 4;        // quadrant totals, tmem base, abort flag
+constexpr uint32_t kOffCs = kOffAux1 + kAuxBytes;      // float[128] cumsum x log2(e)
+constexpr uint32_t kOffCol = kOffCs + kTile * 4;       // float[128] exp(cs_e - cs_s), e = end of s's 32-group
+constexpr uint32_t kOffMisc = kOffCol + kTile * 4;     // quadrant totals, tmem base, abort flag
 constexpr uint32_t kOffBars = kOffMisc + 64;             // mbarriers
 
 // mbarriers (all with arrival count 1: one producer arrive + TMA bytes, one
@@ -157,7 +158,7 @@ __device__ __forceinline__ void wait_flag(const Ctx& c, size_t idx) {
   unsigned ns = 32;
   while (ld_acquire_u64(f) != c.p->token) {
     __nanosleep(ns);
-    if (ns < 1024) ns <<= 1;
+    if (ns < 128) ns <<= 1;
     if (*c.abort_s) return;
     if (*reinterpret_cast<volatile uint64_t*>(c.p->abort_word) == c.p->token) {
       *c.abort_s = 1;
@@ -176,6 +177,14 @@ __device__ __forceinline__ void wait_flag_w(const Ctx& c, size_t idx) {
   __syncwarp();
   // every lane acquires the flag itself, so its own later loads are ordered after it
   (void)ld_acquire_u64(c.p->flags + idx);
+}
+
+// 2^x with the hardware approximation (relative error ~2^-22, flushes
+// subnormals): ample for factors that end in bf16 operands.
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
 }
 
 __device__ __forceinline__ int node_of_level(int j, int h) { return ((j >> (h + 1)) << (h + 1)) + (1 << h) - 1; }
@@ -306,18 +315,6 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
 }
 
 // ------------------------------------------------------------------ epilogue
-__device__ __forceinline__ float pick8(int l, float l0, float l1, float l2, float l3, float l4, float l5, float l6,
-                                       float l7) {
-  float r = l0;
-  r = (l == 1) ? l1 : r;
-  r = (l == 2) ? l2 : r;
-  r = (l == 3) ? l3 : r;
-  r = (l == 4) ? l4 : r;
-  r = (l == 5) ? l5 : r;
-  r = (l == 6) ? l6 : r;
-  r = (l == 7) ? l7 : r;
-  return r;
-}
 
 __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const TcParams& p = *c.p;
@@ -329,6 +326,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);  // this warp's lane quadrant
   unsigned char* s = c.base;
   float* cs_s = reinterpret_cast<float*>(s + kOffCs);
+  float* col_s = reinterpret_cast<float*>(s + kOffCol);
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
   uint32_t it = 0, lcnt = 0;
 
@@ -352,15 +350,21 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
     float off = 0.f;
     for (int qq = 0; qq < q; ++qq) off += qtot[qq];
     const float cs_t = x + off;
-    if (hf == 0) cs_s[row] = cs_t;
+    const float cs2_t = cs_t * kLog2e;                                   // base-2 log decay
+    const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);      // end of this 32-group
+    if (hf == 0) {
+      cs_s[row] = cs2_t;
+      col_s[row] = ex2(cs2_grp_end - cs2_t);
+    }
     __syncwarp();
     named_bar_sync(1, kEpi);
-    const float cs_end = cs_s[kTile - 1];
+    const float cs2_end = cs_s[kTile - 1];
+    const float cs_end = cs2_end * 0.69314718055994531f;  // natural log decay of the whole tile
 
     // decayed V for the chunk state: X[s] = exp(cs_end - cs_s) V[s]
     wait_bar_w(c, B_KV_FULL, it & 1);
     {
-      const float dec = exp2f((cs_end - cs_t) * kLog2e);
+      const float dec = ex2(cs2_end - cs2_t);
       const uint32_t off_row = hf * kHalf + row * 128;
       const uint4* src = reinterpret_cast<const uint4*>(s + kOffV + off_row);
       uint4* dst = reinterpret_cast<uint4*>(s + kOffX + off_row);
@@ -424,36 +428,41 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         dst[c8] = v;
       }
       if (leader) p.G[node_j] = dec;
-      fence_proxy_async_global();
-      __threadfence();
       __syncwarp();
-    named_bar_sync(1, kEpi);
-      if (leader) st_release_u64(p.flags + node_j, p.token);
+      named_bar_sync(1, kEpi);  // every row of F_j is written (CTA scope)
+      if (leader) {
+        __threadfence();        // ... and visible at gpu scope before the flag
+        st_release_u64(p.flags + node_j, p.token);
+      }
     }
 
-    // masked scores -> P (bf16, K-major swizzled) in X
-    const float l0 = lam_s[row * p.L + 0], l1 = lam_s[row * p.L + 1], l2 = lam_s[row * p.L + 2],
-                l3 = lam_s[row * p.L + 3], l4 = lam_s[row * p.L + 4], l5 = lam_s[row * p.L + 5],
-                l6 = lam_s[row * p.L + 6], l7 = lam_s[row * p.L + 7];
+    // masked scores -> P (bf16, K-major swizzled) in X.  Thread row t, column
+    // groups g of 32:  g < q (all s < t): the level is constant over the group
+    // and exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s), e = 32 g + 31,
+    // the second factor from the per-tile table;  g == q: per element;
+    // g > q: zero.
+    const float* lam_row = lam_s + row * p.L;
     wait_bar_w(c, B_S_DONE, it & 1);
     __syncwarp();
     tc_fence_after();
 #pragma unroll
     for (int c32 = 0; c32 < 2; ++c32) {
-      const int s0 = 64 * hf + 32 * c32;
+      const int g = 2 * hf + c32;
+      const int s0 = 32 * g;
       float v[32];
-      if ((s0 >> 5) <= q) {
+      if (g < q) {
+        tmem_ld32(tl + kTmS + s0, v);
+        const float rf = lam_row[32 - __clz(row ^ s0)] * ex2(cs2_t - cs_s[s0 + 31]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int i = 0; i < 32; ++i) v[i] *= rf * col_s[s0 + i];
+      } else if (g == q) {
         tmem_ld32(tl + kTmS + s0, v);
         tmem_ld_wait();
 #pragma unroll
         for (int i = 0; i < 32; ++i) {
-          const int sidx = s0 + i;
-          float pv = 0.f;
-          if (sidx <= row) {
-            const int lv = 32 - __clz(row ^ sidx);
-            pv = v[i] * exp2f((cs_t - cs_s[sidx]) * kLog2e) * pick8(lv, l0, l1, l2, l3, l4, l5, l6, l7);
-          }
-          v[i] = pv;
+          const float e = ex2(cs2_t - cs_s[s0 + i]) * lam_row[32 - __clz(lane ^ i)];
+          v[i] = (i <= lane) ? v[i] * e : 0.f;
         }
       } else {
 #pragma unroll

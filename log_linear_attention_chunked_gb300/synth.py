@@ -72,10 +72,12 @@ def _uniform(shape, seed, device):
     return torch.rand(shape, generator=g, device=device, dtype=torch.float32)
 
 
-def _fill(out, name, seed, draw, B, H, device):
+def _fill(out, name, seed, draw, B, H, device, kind=None):
+    """Fill out[b, h] with draw(kind, seed of (name, b, h)); `name` salts the
+    seed, `kind` (default: name) selects the distribution."""
     for b in range(B):
         for h in range(H):
-            out[b, h] = draw(name, slice_seed(seed, name, b, h), device)
+            out[b, h] = draw(kind or name, slice_seed(seed, name, b, h), device)
 
 
 def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="softplus",
@@ -166,7 +168,7 @@ def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None) -
               "log_alpha": (B, H, S), "lam": (B, H, S, Ls + 1)}
     for name, shp in shapes.items():
         buf = torch.empty(shp, device=device, dtype=torch.float32)
-        _fill(buf, "dec_" + name, seed, draw, B, H, device)
+        _fill(buf, "dec_" + name, seed, draw, B, H, device, kind=name)
         # step-major layout [S, B, H, ...] so that one step is one contiguous slab
         buf = buf.movedim(2, 0).contiguous()
         out[name] = buf.to(dt) if name in ("q", "k", "v") else buf
