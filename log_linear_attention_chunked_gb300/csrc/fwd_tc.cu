@@ -15,7 +15,9 @@
 // one accumulator per tile, the pages' "level fusion".)
 //
 // Roles (320 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
-// i * gridDim.x in head-major order):
+// i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
+// tiles running at the same time are few positions of many heads and the
+// chains of node dependencies inside one round of tiles stay short):
 //   warp 0      TMA producer: K, V, Q tiles, log_alpha + lambda rows, F nodes
 //               (after their publication flags are seen)
 //   warp 1      TMEM owner and MMA issuer (one thread)
@@ -204,7 +206,7 @@ __device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap*
   uint32_t it = 0, fcnt = 0;
   unsigned char* s = c.base;
   for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int bh = u / p.Nt, j = u % p.Nt;
+    const int bh = u % p.BH, j = u / p.BH;
     const int row0 = bh * p.T + j * kTile;
     // K, V
     if (it > 0) wait_bar(c, B_KV_FREE, (it - 1) & 1);
@@ -280,7 +282,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   };
 
   for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int j = u % p.Nt;
+    const int j = u / p.BH;
     // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
     wait_bar(c, B_KV_FULL, it & 1);
     wait_bar(c, B_VT_READY, it & 1);
@@ -331,7 +333,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   uint32_t it = 0, lcnt = 0;
 
   for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int bh = u / p.Nt, j = u % p.Nt;
+    const int bh = u % p.BH, j = u / p.BH;
     const int slot = it & 1;
     const float* la_s = reinterpret_cast<const float*>(s + (slot ? kOffAux1 : kOffAux0));
     const float* lam_s = la_s + kTile;
