@@ -24,6 +24,8 @@
 //   warps 2..9  epilogue: thread (quadrant q = warp % 4, half hf) owns row
 //               32q + lane and columns [64 hf, 64 hf + 64) of every 128x128
 //               accumulator
+//   warp 10     publisher: makes each written node visible at gpu scope and
+//               raises its flag, off the epilogue's path
 // Cross-CTA dependencies only point to tiles of lower index, every CTA walks
 // its tiles in increasing order, and the cooperative launch makes all CTAs
 // co-resident, so the waits always make progress.  Every wait is bounded;
@@ -45,7 +47,8 @@ using namespace sm100;
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kLmax = 24;
-constexpr int kThreads = 320;
+constexpr int kThreads = 352;
+constexpr int kPubWarp = 10;
 constexpr int kEpi = 256;
 constexpr uint32_t kHalf = kTile * 64 * 2;  // one [128 x 64] bf16 swizzled block: 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalf;  // 32 KB
@@ -75,7 +78,7 @@ constexpr uint32_t kOffBars = kOffMisc + 64;             // mbarriers
 enum Bar : int {
   B_KV_FULL, B_Q_FULL, B_AUX_FULL0, B_AUX_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_KV_FREE,
   B_Q_FREE, B_AUX_FREE0, B_AUX_FREE1, B_VT_READY, B_STATE_DONE, B_STATE_FREE, B_S_DONE, B_S_FREE, B_P_READY,
-  B_LVL_DONE, B_LVL_FREE, B_O_DONE, B_O_FREE, B_FINAL, kNumBars
+  B_LVL_DONE, B_LVL_FREE, B_O_DONE, B_O_FREE, B_FINAL, B_FJ_WRITTEN, kNumBars
 };
 constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8 + 1024;  // + slack to align the base to 1024
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -83,6 +86,9 @@ static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 struct TcParams {
   const float* log_alpha;
   const float* lam;
+  const __nv_bfloat16* q;
+  const __nv_bfloat16* k;
+  const __nv_bfloat16* v;
   __nv_bfloat16* o;
   __nv_bfloat16* F;  // [BH * Nt, 128, 128] Fenwick nodes
   float* G;          // [BH * Nt] log-decay totals of the nodes
@@ -208,6 +214,16 @@ __device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap*
   for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
     const int bh = u % p.BH, j = u / p.BH;
     const int row0 = bh * p.T + j * kTile;
+    // stage the next tile's inputs in L2 while this one is processed
+    const int un = u + gridDim.x;
+    if (un < total) {
+      const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
+      bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
+      bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+    }
     // K, V
     if (it > 0) wait_bar(c, B_KV_FREE, (it - 1) & 1);
     mbar_arrive_expect_tx(c.bars + B_KV_FULL, 2 * kTileBytes);
@@ -298,10 +314,8 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
 #pragma unroll
     for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmS, desc_k(sQ, kk), desc_k(sK, kk), id_qk, kk > 0);
     umma_commit(c.bars + B_S_DONE);
-    // first inter level overlaps the epilogue's masking of the scores
     const int nlev = __popc(j);
-    if (nlev > 0) issue_level();
-    // intra output: D[t][dv] = sum_s P[t][s] V[s][dv]
+    // intra output (issued before the levels, which may wait for other tiles' nodes): D[t][dv] = sum_s P[t][s] V[s][dv]
     wait_bar(c, B_P_READY, it & 1);
     if (it > 0) wait_bar(c, B_O_FREE, (it - 1) & 1);
     tc_fence_after();
@@ -309,7 +323,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
     for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmO, desc_k(sX, kk), desc_mn(sV, kk), id_pv, kk > 0);
     umma_commit(c.bars + B_O_DONE);
     umma_commit(c.bars + B_KV_FREE);
-    for (int l = 1; l < nlev; ++l) issue_level();
+    for (int l = 0; l < nlev; ++l) issue_level();
     umma_commit(c.bars + B_Q_FREE);
   }
   umma_commit(c.bars + B_FINAL);
@@ -372,14 +386,15 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       uint4* dst = reinterpret_cast<uint4*>(s + kOffX + off_row);
 #pragma unroll
       for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 v = src[c8];
+        const int cc = c8 ^ (row & 7);  // lanes of a warp spread over the banks
+        uint4 v = src[cc];
         uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
         for (int i = 0; i < 4; ++i) {
           const float2 f = unpack_bf16x2(w[i]);
           w[i] = pack_bf16x2(f.x * dec, f.y * dec);
         }
-        dst[c8] = v;
+        dst[cc] = v;
       }
     }
     fence_proxy_async_shared();
@@ -432,10 +447,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       if (leader) p.G[node_j] = dec;
       __syncwarp();
       named_bar_sync(1, kEpi);  // every row of F_j is written (CTA scope)
-      if (leader) {
-        __threadfence();        // ... and visible at gpu scope before the flag
-        st_release_u64(p.flags + node_j, p.token);
-      }
+      if (leader) mbar_arrive(c.bars + B_FJ_WRITTEN);  // the publisher warp makes it visible
     }
 
     // masked scores -> P (bf16, K-major swizzled) in X.  Thread row t, column
@@ -554,6 +566,21 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   }
 }
 
+// ------------------------------------------------------------------ publisher (warp 10)
+// Makes each tile's node visible at gpu scope and raises its flag, so the
+// epilogue never stalls on the fence.
+__device__ void publisher(const Ctx& c) {
+  const TcParams& p = *c.p;
+  const int total = p.BH * p.Nt;
+  uint32_t it = 0;
+  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
+    const size_t node_j = (size_t)(u % p.BH) * p.Nt + u / p.BH;
+    wait_bar(c, B_FJ_WRITTEN, it & 1);
+    __threadfence();
+    st_release_u64(p.flags + node_j, p.token);
+  }
+}
+
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf, TcParams p) {
@@ -588,6 +615,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     if (lane == 0) producer(c, &tq, &tk, &tv, &tf);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(c, tmem);
+  } else if (warp == kPubWarp) {
+    if (lane == 0) publisher(c);
   } else {
     epilogue(c, tmem, warp, lane);
   }
@@ -704,6 +733,9 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   TcParams p;
   p.log_alpha = a.log_alpha;
   p.lam = a.lam;
+  p.q = static_cast<const __nv_bfloat16*>(a.q);
+  p.k = static_cast<const __nv_bfloat16*>(a.k);
+  p.v = static_cast<const __nv_bfloat16*>(a.v);
   p.o = static_cast<__nv_bfloat16*>(a.o);
   p.F = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_F);
   p.G = reinterpret_cast<float*>(ws + plan.off_G);
