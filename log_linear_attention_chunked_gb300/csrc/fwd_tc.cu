@@ -14,24 +14,34 @@
 // gist.science (zh) summary §2.3; the per-level contractions are summed in
 // one accumulator per tile, the pages' "level fusion".)
 //
-// Roles (320 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
+// Roles (352 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
 // i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
 // tiles running at the same time are few positions of many heads and the
 // chains of node dependencies inside one round of tiles stay short):
-//   warp 0      TMA producer: K, V, Q tiles, log_alpha + lambda rows, F nodes
-//               (after their publication flags are seen)
+//   warp 0      TMA producer: K, V, Q tiles, F nodes (after their publication
+//               flags are seen), L2 prefetch of the next tile
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2..9  epilogue: thread (quadrant q = warp % 4, half hf) owns row
-//               32q + lane and columns [64 hf, 64 hf + 64) of every 128x128
-//               accumulator
-//   warp 10     publisher: makes each written node visible at gpu scope and
-//               raises its flag, off the epilogue's path
+//               32q + lane of every 128x128 accumulator
+//   warp 10     store warp: TMA stores of the staged nodes and outputs, then
+//               the gpu-scope publication of each node
+// Software pipeline: in step i the epilogue runs the front half of tile i
+// (cumsum, decayed V, chunk state, masked scores P) and then the back half of
+// tile i-1 (inter-tile levels + output); a node F_j of odd j, which merges
+// nodes published in the same step, is completed after the mask.  The nodes the back
+// half reads were published by tiles of the previous step, so it rarely
+// waits; the tensor cores run tile i's products while the epilogue finishes
+// tile i-1.  Q is double-buffered for that; the state and PV accumulators of
+// consecutive tiles alternate between two TMEM regions.  P goes back to TMEM
+// (bf16, over the scores) as the A operand of PV, so the X buffer is free
+// after the state product and stages every global store for the TMA.
 // Cross-CTA dependencies only point to tiles of lower index, every CTA walks
 // its tiles in increasing order, and the cooperative launch makes all CTAs
 // co-resident, so the waits always make progress.  Every wait is bounded;
 // a wait that expires records LL_ERR_TIMEOUT and the kernel runs on to its
 // end without the missing data.
 #include <cudaTypedefs.h>
+#include <cuda_fp16.h>
 
 #include <atomic>
 
@@ -55,32 +65,35 @@ constexpr uint32_t kTileBytes = 2 * kHalf;  // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
-// TMEM columns of the four 128-column fp32 accumulators
-constexpr uint32_t kTmState = 0, kTmS = 128, kTmO = 256, kTmLvl = 384;
+// TMEM columns: two 128-column regions that hold the chunk state and then the
+// intra output PV of alternating tiles; the scores (then P, bf16, in their
+// first 64 columns, then odd-numbered level products); level products.
+constexpr uint32_t kTmR0 = 0, kTmS = 256, kTmLvl = 384;
 
-// shared-memory layout (offsets from a 1024-aligned base)
-constexpr uint32_t kOffQ = 0;
-constexpr uint32_t kOffK = kOffQ + kTileBytes;
+// shared-memory layout (offsets from the dynamic base, which must be 1024-aligned)
+constexpr uint32_t kOffQ0 = 0;
+constexpr uint32_t kOffQ1 = kOffQ0 + kTileBytes;
+constexpr uint32_t kOffK = kOffQ1 + kTileBytes;
 constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffX = kOffV + kTileBytes;  // decayed V, then P
+constexpr uint32_t kOffX = kOffV + kTileBytes;  // decayed V, then staging of TMA stores
 constexpr uint32_t kOffF0 = kOffX + kTileBytes;
 constexpr uint32_t kOffF1 = kOffF0 + kTileBytes;
-constexpr uint32_t kAuxBytes = kTile * 4 + kTile * kLmax * 4;  // log_alpha row + lambda rows
-constexpr uint32_t kOffAux0 = kOffF1 + kTileBytes;
-constexpr uint32_t kOffAux1 = kOffAux0 + kAuxBytes;
-constexpr uint32_t kOffCs = kOffAux1 + kAuxBytes;      // float[128] cumsum x log2(e)
-constexpr uint32_t kOffCol = kOffCs + kTile * 4;       // float[128] exp(cs_e - cs_s), e = end of s's 32-group
-constexpr uint32_t kOffMisc = kOffCol + kTile * 4;     // quadrant totals, tmem base, abort flag
-constexpr uint32_t kOffBars = kOffMisc + 64;             // mbarriers
+constexpr uint32_t kOffCs = kOffF1 + kTileBytes;  // float[128] cumsum x log2(e)
+constexpr uint32_t kOffCol = kOffCs + kTile * 4;  // float[128] exp(cs_e - cs_s), e = end of s's 32-group
+constexpr uint32_t kOffLam = kOffCol + kTile * 4; // half[6][128] lambda levels 0..5 / the row's max
+// misc: quadrant totals [0,16), abort flag 16, merge "more pieces" words 20/24,
+// tmem base 32, piece descriptors (R, R_end, last) x 2 at [40, 64)
+constexpr uint32_t kOffMisc = kOffLam + 6 * kTile * 2;
+constexpr uint32_t kOffBars = kOffMisc + 64;            // mbarriers
 
 // mbarriers (all with arrival count 1: one producer arrive + TMA bytes, one
-// tcgen05.commit, or one elected epilogue thread)
+// tcgen05.commit, or one elected thread)
 enum Bar : int {
-  B_KV_FULL, B_Q_FULL, B_AUX_FULL0, B_AUX_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_KV_FREE,
-  B_Q_FREE, B_AUX_FREE0, B_AUX_FREE1, B_VT_READY, B_STATE_DONE, B_STATE_FREE, B_S_DONE, B_S_FREE, B_P_READY,
-  B_LVL_DONE, B_LVL_FREE, B_O_DONE, B_O_FREE, B_FINAL, B_FJ_WRITTEN, kNumBars
+  B_K_FULL, B_V_FULL, B_Q_FULL0, B_Q_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_K_FREE, B_V_FREE,
+  B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_LVL_DONE0, B_LVL_DONE1, B_LVL_FREE0,
+  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_PC_FULL0, B_PC_FULL1, B_PC_FREE0, B_PC_FREE1, kNumBars
 };
-constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8 + 1024;  // + slack to align the base to 1024
+constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
 
 struct TcParams {
@@ -89,10 +102,11 @@ struct TcParams {
   const __nv_bfloat16* q;
   const __nv_bfloat16* k;
   const __nv_bfloat16* v;
-  __nv_bfloat16* o;
   __nv_bfloat16* F;  // [BH * Nt, 128, 128] Fenwick nodes
   float* G;          // [BH * Nt] log-decay totals of the nodes
-  uint64_t* flags;   // [BH * Nt] publication tokens
+  uint64_t* flags;   // [BH * Nt] publication tokens of the nodes
+  float* Gt;         // [BH * Nt] log-decay totals of the tiles
+  uint64_t* rflags;  // [BH * Nt] publication tokens of the raw states (odd tiles, in the node rows of R)
   uint64_t* abort_word;
   uint64_t token;
   int BH, T, Nt, L;
@@ -157,9 +171,9 @@ __device__ __forceinline__ void drain_bar(const Ctx& c, int b, uint32_t par) {
     if (globaltimer_ns() - t0 > kTimeoutNs / 8) return;
 }
 
-// Bounded wait until node `idx` of this call is published.
-__device__ __forceinline__ void wait_flag(const Ctx& c, size_t idx) {
-  const uint64_t* f = c.p->flags + idx;
+// Bounded wait until entry `idx` of the flag array `flags` carries this call's token.
+__device__ __forceinline__ void wait_flag(const Ctx& c, const uint64_t* flags, size_t idx) {
+  const uint64_t* f = flags + idx;
   if (ld_acquire_u64(f) == c.p->token) return;
   if (*c.abort_s) return;
   const uint64_t t0 = globaltimer_ns();
@@ -179,12 +193,16 @@ __device__ __forceinline__ void wait_flag(const Ctx& c, size_t idx) {
   }
 }
 
-// Warp-uniform version of wait_flag (all lanes wait for the same node).
-__device__ __forceinline__ void wait_flag_w(const Ctx& c, size_t idx) {
-  if ((threadIdx.x & 31) == 0) wait_flag(c, idx);
+// Warp-collective: lane i < n acquires node idx (published with its log-decay
+// total) and returns that total.  The flags are read together; only the
+// lanes whose node is not published yet spin.
+__device__ __forceinline__ float acquire_nodes(const Ctx& c, int n, size_t idx) {
+  const bool mine = (int)(threadIdx.x & 31) < n;
+  bool ok = !mine || ld_relaxed_u64(c.p->flags + idx) == c.p->token;
+  if (!ok) wait_flag(c, c.p->flags, idx);
   __syncwarp();
-  // every lane acquires the flag itself, so its own later loads are ordered after it
-  (void)ld_acquire_u64(c.p->flags + idx);
+  fence_acq_rel_gpu();
+  return mine ? c.p->G[idx] : 0.f;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22, flushes
@@ -197,6 +215,9 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ int node_of_level(int j, int h) { return ((j >> (h + 1)) << (h + 1)) + (1 << h) - 1; }
 
+// Number of tiles CTA blockIdx.x processes (blockIdx.x < total).
+__device__ __forceinline__ int tiles_of_cta(int total) { return (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1; }
+
 // K-major operand (rows of 128 B, K split in two 64-column blocks), k-step kk of 16.
 __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
   return sw128_desc(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
@@ -205,68 +226,135 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
 __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, kHalf, 1024); }
 
 // ------------------------------------------------------------------ producer
+// Per step i: K, V and Q of tile i; the nodes of tile i-1's levels (F ring);
+// for odd j the pieces of the merge F_j = S_j + sum of the decayed states of
+// tiles (j - 2^cto(j), j), into the K and V buffers once the products of
+// tile i have read them.  The pieces are found by a look-back from j - 1:
+// a node that is already published covers its whole block; otherwise that
+// tile's raw state (published right after its readout) is taken and the walk
+// continues one tile down, so no merge ever waits for another merge.
+// Only the first four level nodes go before the pieces: the load of level k
+// needs the ring slot of level k - 2, whose product needs the epilogue to
+// have read level k - 4, which it does after the merge.
+// Once a wait has expired nothing new is armed; the drain at the end waits
+// (bounded) for the copies already issued.
 __device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                         const CUtensorMap* tf) {
+                         const CUtensorMap* tf, const CUtensorMap* tr) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
-  uint32_t it = 0, fcnt = 0;
+  const int n = tiles_of_cta(total);
+  uint32_t kc = 0, vc = 0, qc[2] = {0, 0}, fcnt = 0, npc[2] = {0, 0};
   unsigned char* s = c.base;
-  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int bh = u % p.BH, j = u / p.BH;
-    const int row0 = bh * p.T + j * kTile;
-    // stage the next tile's inputs in L2 while this one is processed
-    const int un = u + gridDim.x;
-    if (un < total) {
-      const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
-      bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
-      bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
-    }
-    // K, V
-    if (it > 0) wait_bar(c, B_KV_FREE, (it - 1) & 1);
-    mbar_arrive_expect_tx(c.bars + B_KV_FULL, 2 * kTileBytes);
-    tma_load_2d(s + kOffK, tk, c.bars + B_KV_FULL, 0, row0);
-    tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_KV_FULL, 64, row0);
-    tma_load_2d(s + kOffV, tv, c.bars + B_KV_FULL, 0, row0);
-    tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_KV_FULL, 64, row0);
-    // log_alpha + lambda rows
-    const int slot = it & 1;
-    if (it >= 2) wait_bar(c, B_AUX_FREE0 + slot, ((it - 2) >> 1) & 1);
-    unsigned char* aux = s + (slot ? kOffAux1 : kOffAux0);
-    const uint32_t lam_bytes = (uint32_t)(kTile * p.L * 4);
-    mbar_arrive_expect_tx(c.bars + B_AUX_FULL0 + slot, kTile * 4 + lam_bytes);
-    bulk_load(aux, p.log_alpha + (size_t)row0, kTile * 4, c.bars + B_AUX_FULL0 + slot);
-    bulk_load(aux + kTile * 4, p.lam + (size_t)row0 * p.L, lam_bytes, c.bars + B_AUX_FULL0 + slot);
-    // Q
-    if (it > 0) wait_bar(c, B_Q_FREE, (it - 1) & 1);
-    mbar_arrive_expect_tx(c.bars + B_Q_FULL, kTileBytes);
-    tma_load_2d(s + kOffQ, tq, c.bars + B_Q_FULL, 0, row0);
-    tma_load_2d(s + kOffQ + kHalf, tq, c.bars + B_Q_FULL, 64, row0);
-    // Fenwick nodes of the inter-tile levels, lowest level first
-    for (int h = 0; (j >> h) != 0; ++h) {
-      if (!((j >> h) & 1)) continue;
-      const int e = node_of_level(j, h);
-      const size_t node = (size_t)bh * p.Nt + e;
-      wait_flag(c, node);
+  float* pdesc = reinterpret_cast<float*>(s + kOffMisc + 40);  // per piece buffer: R, R_end, last
+
+  // the level nodes of tile (bhp, jp) from its first-th level on, at most count of them
+  auto load_levels = [&](int bhp, int jp, int first, int count) {
+    int l = 0;
+    for (int h = 0; (jp >> h) != 0 && count > 0; ++h) {
+      if (!((jp >> h) & 1)) continue;
+      if (l++ < first) continue;
+      if (*c.abort_s) return;
+      const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
+      wait_flag(c, p.flags, node);
       fence_proxy_async_global();
       const int fs = fcnt & 1;
       if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
+      if (*c.abort_s) return;
       unsigned char* fdst = s + (fs ? kOffF1 : kOffF0);
       mbar_arrive_expect_tx(c.bars + B_F_FULL0 + fs, kTileBytes);
       tma_load_2d(fdst, tf, c.bars + B_F_FULL0 + fs, 0, (int)(node * kD));
       tma_load_2d(fdst + kHalf, tf, c.bars + B_F_FULL0 + fs, 64, (int)(node * kD));
       ++fcnt;
+      --count;
     }
+  };
+
+  for (int it = 0; it <= n && !*c.abort_s; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    const int bh = u % p.BH, j = u / p.BH;
+    if (it < n) {
+      const int row0 = bh * p.T + j * kTile;
+      // stage the next tile's inputs in L2 while this one is processed
+      if (it + 1 < n) {
+        const int un = u + gridDim.x;
+        const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
+        bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
+        bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
+        bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
+        bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
+        bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+      }
+      // K and V go where the previous tile's products and merge pieces were
+      if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);
+      if (npc[0] > 0) wait_bar(c, B_PC_FREE0, (npc[0] - 1) & 1);
+      if (*c.abort_s) break;
+      mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
+      tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
+      tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_K_FULL, 64, row0);
+      ++kc;
+      if (it > 0) wait_bar(c, B_V_FREE, (it - 1) & 1);
+      if (npc[1] > 0) wait_bar(c, B_PC_FREE1, (npc[1] - 1) & 1);
+      if (*c.abort_s) break;
+      mbar_arrive_expect_tx(c.bars + B_V_FULL, kTileBytes);
+      tma_load_2d(s + kOffV, tv, c.bars + B_V_FULL, 0, row0);
+      tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_V_FULL, 64, row0);
+      ++vc;
+      const int qs = it & 1;
+      if (it >= 2) wait_bar(c, B_Q_FREE0 + qs, ((it - 2) >> 1) & 1);
+      if (*c.abort_s) break;
+      unsigned char* qdst = s + (qs ? kOffQ1 : kOffQ0);
+      mbar_arrive_expect_tx(c.bars + B_Q_FULL0 + qs, kTileBytes);
+      tma_load_2d(qdst, tq, c.bars + B_Q_FULL0 + qs, 0, row0);
+      tma_load_2d(qdst + kHalf, tq, c.bars + B_Q_FULL0 + qs, 64, row0);
+      ++qc[qs];
+    }
+    const int up = u - gridDim.x;
+    if (it >= 1) load_levels(up % p.BH, up / p.BH, 0, 4);
+    if (it < n && (j & 1)) {
+      // merge pieces of tile j, most recent first, alternately into K and V
+      const int stop = j - (1 << (__ffs(~j) - 1));
+      float R = 0.f;
+      bool used[2] = {false, false};
+      for (int e = j - 1, idx = 0; e > stop && !*c.abort_s; ++idx) {
+        const size_t node = (size_t)bh * p.Nt + e;
+        bool full = true;
+        if (e & 1) {
+          full = ld_relaxed_u64(p.flags + node) == p.token;
+          if (full) fence_acq_rel_gpu();
+          else wait_flag(c, p.rflags, node);
+        } else {
+          wait_flag(c, p.flags, node);  // even tiles publish their state as the node at once
+        }
+        fence_proxy_async_global();
+        const float g = full ? p.G[node] : p.Gt[node];
+        const int size = full ? 1 << (__ffs(~e) - 1) : 1;
+        const int b = idx & 1;
+        if (!used[b]) {
+          wait_bar(c, b ? B_V_FREE : B_K_FREE, it & 1);  // the products of this tile have read the buffer
+          used[b] = true;
+        }
+        if (npc[b] > 0) wait_bar(c, B_PC_FREE0 + b, (npc[b] - 1) & 1);
+        if (*c.abort_s) break;
+        pdesc[3 * b] = R;
+        pdesc[3 * b + 1] = R + g;
+        pdesc[3 * b + 2] = (e - size <= stop) ? 1.f : 0.f;
+        unsigned char* dst = s + (b ? kOffV : kOffK);
+        mbar_arrive_expect_tx(c.bars + B_PC_FULL0 + b, kTileBytes);
+        tma_load_2d(dst, full ? tf : tr, c.bars + B_PC_FULL0 + b, 0, (int)(node * kD));
+        tma_load_2d(dst + kHalf, full ? tf : tr, c.bars + B_PC_FULL0 + b, 64, (int)(node * kD));
+        ++npc[b];
+        R += g;
+        e -= size;
+      }
+    }
+    if (it >= 1) load_levels(up % p.BH, up / p.BH, 4, 64);
   }
-  // drain: every load armed above has landed before the CTA may exit
-  if (it > 0) {
-    drain_bar(c, B_KV_FULL, (it - 1) & 1);
-    drain_bar(c, B_Q_FULL, (it - 1) & 1);
-    const uint32_t last = it - 1;
-    drain_bar(c, B_AUX_FULL0 + (last & 1), (last >> 1) & 1);
-    if (it >= 2) drain_bar(c, B_AUX_FULL0 + ((last - 1) & 1), ((last - 1) >> 1) & 1);
+  // drain: every copy armed above has landed before the CTA may exit
+  if (kc > 0) drain_bar(c, B_K_FULL, (kc - 1) & 1);
+  if (vc > 0) drain_bar(c, B_V_FULL, (vc - 1) & 1);
+  for (int b = 0; b < 2; ++b) {
+    if (qc[b] > 0) drain_bar(c, B_Q_FULL0 + b, (qc[b] - 1) & 1);
+    if (npc[b] > 0) drain_bar(c, B_PC_FULL0 + b, (npc[b] - 1) & 1);
   }
   if (fcnt > 0) drain_bar(c, B_F_FULL0 + ((fcnt - 1) & 1), ((fcnt - 1) >> 1) & 1);
   if (fcnt > 1) drain_bar(c, B_F_FULL0 + ((fcnt - 2) & 1), ((fcnt - 2) >> 1) & 1);
@@ -276,55 +364,72 @@ __device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap*
 __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
-  const uint32_t sQ = smem_u32(c.base + kOffQ), sK = smem_u32(c.base + kOffK), sV = smem_u32(c.base + kOffV),
-                 sX = smem_u32(c.base + kOffX), sF0 = smem_u32(c.base + kOffF0), sF1 = smem_u32(c.base + kOffF1);
+  const int n = tiles_of_cta(total);
+  const uint32_t sQ0 = smem_u32(c.base + kOffQ0), sQ1 = smem_u32(c.base + kOffQ1), sK = smem_u32(c.base + kOffK),
+                 sV = smem_u32(c.base + kOffV), sX = smem_u32(c.base + kOffX), sF0 = smem_u32(c.base + kOffF0),
+                 sF1 = smem_u32(c.base + kOffF1);
   constexpr uint32_t id_state = idesc_bf16(128, 128, true, true);   // Vt^T (MN) x K (MN)
   constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);    // Q (K) x K|F (K)
-  constexpr uint32_t id_pv = idesc_bf16(128, 128, false, true);     // P (K) x V (MN)
-  uint32_t it = 0, fcnt = 0, lcnt = 0;
+  constexpr uint32_t id_pv = idesc_bf16(128, 128, false, true);     // P (TMEM) x V (MN)
+  uint32_t fcnt = 0, nb[2] = {0, 0};
 
-  auto issue_level = [&]() {
+  // level l of the previous tile, D[t][dv] = Q[t] . F[dv], into buffer l & 1
+  // (even: the level region; odd: the scores' region, free once PV has read P)
+  auto issue_level = [&](uint32_t sQ, int l) {
+    const int b = l & 1;
     const int fs = fcnt & 1;
     wait_bar(c, B_F_FULL0 + fs, (fcnt >> 1) & 1);
-    if (lcnt > 0) wait_bar(c, B_LVL_FREE, (lcnt - 1) & 1);
+    if (nb[b] > 0) wait_bar(c, B_LVL_FREE0 + b, (nb[b] - 1) & 1);
     tc_fence_after();
     const uint32_t sF = fs ? sF1 : sF0;
+    const uint32_t d = tmem + (b ? kTmS : kTmLvl);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmLvl, desc_k(sQ, kk), desc_k(sF, kk), id_qk, kk > 0);
-    umma_commit(c.bars + B_LVL_DONE);
+    for (int kk = 0; kk < 8; ++kk) umma_bf16(d, desc_k(sQ, kk), desc_k(sF, kk), id_qk, kk > 0);
+    umma_commit(c.bars + B_LVL_DONE0 + b);
     umma_commit(c.bars + B_F_FREE0 + fs);
     ++fcnt;
-    ++lcnt;
+    ++nb[b];
   };
 
-  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int j = u / p.BH;
-    // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
-    wait_bar(c, B_KV_FULL, it & 1);
-    wait_bar(c, B_VT_READY, it & 1);
-    if (it > 0) wait_bar(c, B_STATE_FREE, (it - 1) & 1);
-    tc_fence_after();
+  int jp = 0;
+  for (int it = 0; it <= n; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    const int j = it < n ? u / p.BH : 0;
+    const int nlev_p = it >= 1 ? __popc(jp) : 0;
+    const uint32_t sQp = (it - 1) & 1 ? sQ1 : sQ0;
+    const uint32_t tR = tmem + kTmR0 + (it & 1) * 128;
+    if (it < n) {
+      // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
+      wait_bar(c, B_K_FULL, it & 1);
+      wait_bar(c, B_VT_READY, it & 1);
+      tc_fence_after();
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmState, desc_mn(sX, kk), desc_mn(sK, kk), id_state, kk > 0);
-    umma_commit(c.bars + B_STATE_DONE);
-    // scores: D[t][s] = Q[t] . K[s]
-    wait_bar(c, B_Q_FULL, it & 1);
-    if (it > 0) wait_bar(c, B_S_FREE, (it - 1) & 1);
-    tc_fence_after();
+      for (int kk = 0; kk < 8; ++kk) umma_bf16(tR, desc_mn(sX, kk), desc_mn(sK, kk), id_state, kk > 0);
+      umma_commit(c.bars + B_STATE_DONE);
+      // scores: D[t][s] = Q[t] . K[s]
+      const uint32_t sQ = it & 1 ? sQ1 : sQ0;
+      wait_bar(c, B_Q_FULL0 + (it & 1), (it >> 1) & 1);
+      tc_fence_after();
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmS, desc_k(sQ, kk), desc_k(sK, kk), id_qk, kk > 0);
-    umma_commit(c.bars + B_S_DONE);
-    const int nlev = __popc(j);
-    // intra output (issued before the levels, which may wait for other tiles' nodes): D[t][dv] = sum_s P[t][s] V[s][dv]
-    wait_bar(c, B_P_READY, it & 1);
-    if (it > 0) wait_bar(c, B_O_FREE, (it - 1) & 1);
-    tc_fence_after();
+      for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmS, desc_k(sQ, kk), desc_k(sK, kk), id_qk, kk > 0);
+      umma_commit(c.bars + B_S_DONE);
+      umma_commit(c.bars + B_K_FREE);
+    }
+    if (it < n) {
+      // intra output: D[t][dv] = sum_s P[t][s] V[s][dv], P from TMEM, into the state's region
+      wait_bar(c, B_P_READY, it & 1);
+      tc_fence_after();
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmO, desc_k(sX, kk), desc_mn(sV, kk), id_pv, kk > 0);
-    umma_commit(c.bars + B_O_DONE);
-    umma_commit(c.bars + B_KV_FREE);
-    for (int l = 0; l < nlev; ++l) issue_level();
-    umma_commit(c.bars + B_Q_FREE);
+      for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(tR, tmem + kTmS + kk * 8, desc_mn(sV, kk), id_pv, kk > 0);
+      umma_commit(c.bars + B_O_DONE);
+      umma_commit(c.bars + B_V_FREE);
+    }
+    // the previous tile's levels after PV, which never waits on another CTA
+    if (it >= 1) {
+      for (int l = 0; l < nlev_p; ++l) issue_level(sQp, l);
+      umma_commit(c.bars + B_Q_FREE0 + ((it - 1) & 1));
+    }
+    jp = j;
   }
   umma_commit(c.bars + B_FINAL);
   drain_bar(c, B_FINAL, 0);
@@ -335,6 +440,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
 __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
+  const int n = tiles_of_cta(total);
   const int q = warp & 3;
   const int hf = (warp - 2) >> 2;
   const int row = 32 * q + lane;
@@ -343,250 +449,406 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   unsigned char* s = c.base;
   float* cs_s = reinterpret_cast<float*>(s + kOffCs);
   float* col_s = reinterpret_cast<float*>(s + kOffCol);
+  __half* lamh = reinterpret_cast<__half*>(s + kOffLam);
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
-  uint32_t it = 0, lcnt = 0;
+  unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;  // this thread's 128 B of a staged tile
+  uint32_t ne[2] = {0, 0};   // level products consumed per buffer
+  uint32_t npc[2] = {0, 0};  // merge pieces consumed per buffer (K, V)
+  uint32_t xs = 0;          // X stagings so far
 
-  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const int bh = u % p.BH, j = u / p.BH;
-    const int slot = it & 1;
-    const float* la_s = reinterpret_cast<const float*>(s + (slot ? kOffAux1 : kOffAux0));
-    const float* lam_s = la_s + kTile;
-    wait_bar_w(c, B_AUX_FULL0 + slot, (it >> 1) & 1);
-
-    // inclusive cumsum of log_alpha over the tile
-    float x = la_s[row];
+  // stages 64 values (this thread's row, columns [64 hf, 64 hf + 64)) as bf16
+  // in X for the store warp; the previous staging has been read out of X
+  auto stage = [&](const float* a) {
+    if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
 #pragma unroll
-    for (int o = 1; o < 32; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    if (hf == 0 && lane == 31) qtot[q] = x;
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    float off = 0.f;
-    for (int qq = 0; qq < q; ++qq) off += qtot[qq];
-    const float cs_t = x + off;
-    const float cs2_t = cs_t * kLog2e;                                   // base-2 log decay
-    const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);      // end of this 32-group
-    if (hf == 0) {
-      cs_s[row] = cs2_t;
-      col_s[row] = ex2(cs2_grp_end - cs2_t);
-    }
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    const float cs2_end = cs_s[kTile - 1];
-    const float cs_end = cs2_end * 0.69314718055994531f;  // natural log decay of the whole tile
-
-    // decayed V for the chunk state: X[s] = exp(cs_end - cs_s) V[s]
-    wait_bar_w(c, B_KV_FULL, it & 1);
-    {
-      const float dec = ex2(cs2_end - cs2_t);
-      const uint32_t off_row = hf * kHalf + row * 128;
-      const uint4* src = reinterpret_cast<const uint4*>(s + kOffV + off_row);
-      uint4* dst = reinterpret_cast<uint4*>(s + kOffX + off_row);
-#pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        const int cc = c8 ^ (row & 7);  // lanes of a warp spread over the banks
-        uint4 v = src[cc];
-        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
-#pragma unroll
-        for (int i = 0; i < 4; ++i) {
-          const float2 f = unpack_bf16x2(w[i]);
-          w[i] = pack_bf16x2(f.x * dec, f.y * dec);
-        }
-        dst[cc] = v;
-      }
+    for (int c8 = 0; c8 < 8; ++c8) {
+      uint4 w;
+      w.x = pack_bf16x2(a[8 * c8 + 0], a[8 * c8 + 1]);
+      w.y = pack_bf16x2(a[8 * c8 + 2], a[8 * c8 + 3]);
+      w.z = pack_bf16x2(a[8 * c8 + 4], a[8 * c8 + 5]);
+      w.w = pack_bf16x2(a[8 * c8 + 6], a[8 * c8 + 7]);
+      *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) = w;
     }
     fence_proxy_async_shared();
     __syncwarp();
     named_bar_sync(1, kEpi);
-    if (leader) mbar_arrive(c.bars + B_VT_READY);
+    if (leader) mbar_arrive(c.bars + B_X_STAGED);
+    ++xs;
+  };
 
-    // chunk state -> Fenwick node F_j, published for later tiles
-    wait_bar_w(c, B_STATE_DONE, it & 1);
-    __syncwarp();
-    tc_fence_after();
-    float acc[64];
-    tmem_ld32(tl + kTmState + 64 * hf, acc);
-    tmem_ld32(tl + kTmState + 64 * hf + 32, acc + 32);
-    tmem_ld_wait();
-    tc_fence_before();
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    if (leader) mbar_arrive(c.bars + B_STATE_FREE);
-    {
-      const size_t node_j = (size_t)bh * p.Nt + j;
-      float dec = cs_end;  // log decay from the end of node j - 2^m to the end of tile j
-      for (int m = 0; (j >> m) & 1; ++m) {
-        const size_t node = node_j - ((size_t)1 << m);
-        wait_flag_w(c, node);
-        const uint4* src = reinterpret_cast<const uint4*>(p.F + (node * kD + row) * kD + 64 * hf);
-        const float sc = exp2f(dec * kLog2e);
+  // this row's log_alpha and intra-level lambdas, read one tile ahead
+  float la_n = 0.f, lam_n[8];
+  auto fetch = [&](int u) {
+    const size_t r = (size_t)(u % p.BH) * p.T + (size_t)(u / p.BH) * kTile + row;
+    la_n = __ldg(p.log_alpha + r);
+    const float* lr = p.lam + r * p.L;
+#pragma unroll
+    for (int l = 0; l < 8; ++l) lam_n[l] = __ldg(lr + l);
+  };
+  fetch(blockIdx.x);
+
+  // log decays of the previous tile's levels: lane l < popc(jp) holds the sum
+  // of the totals of the nodes of the levels below its own
+  auto level_decays = [&](int jp, int bhp) {
+    const int nl = __popc(jp);
+    int rest = jp;  // clear the lane lowest set bits: lane l gets the l-th level
+    for (int k = 0; k < lane && rest != 0; ++k) rest &= rest - 1;
+    const size_t idx = (size_t)bhp * p.Nt + (lane < nl ? node_of_level(jp, __ffs(rest) - 1) : 0);
+    const float g = acquire_nodes(c, nl, idx);
+    float x = g;
+#pragma unroll
+    for (int o = 1; o < 16; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    return x - g;
+  };
+
+  float cs_prev = 0.f, lam_c = 0.f;
+  int jp = 0, bhp = 0;
+  for (int it = 0; it <= n; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    int bh = 0, j = 0;
+    float cs_t = 0.f, cs_end = 0.f;
+    if (it < n) {
+      // ================= front half of tile it
+      bh = u % p.BH;
+      j = u / p.BH;
+      const float la = la_n;
+      float lam[8];
+#pragma unroll
+      for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
+      if (it + 1 < n) fetch(u + gridDim.x);
+      if (it >= 1 && jp != 0)  // the previous tile's first level lambda, ahead of its back half
+        lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jp) - 1));
+
+      // inclusive cumsum of log_alpha over the tile
+      float x = la;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (hf == 0 && lane == 31) qtot[q] = x;
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      float off = 0.f;
+      for (int qq = 0; qq < q; ++qq) off += qtot[qq];
+      cs_t = x + off;
+      const float cs2_t = cs_t * kLog2e;                                   // base-2 log decay
+      const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);      // end of this 32-group
+      if (hf == 0) {
+        cs_s[row] = cs2_t;
+        col_s[row] = ex2(cs2_grp_end - cs2_t);
+      }
+      // lambda of levels 0..5 (the diagonal group), relative to the row's
+      // largest, as half; the largest rides in the exponent
+      float lmax = 0.f;
+#pragma unroll
+      for (int l = 0; l < 6; ++l) lmax = fmaxf(lmax, lam[l]);
+      const float cs2_diag = cs2_t + (lmax > 0.f ? __log2f(lmax) : -INFINITY);
+      if (hf == 0) {
+        const float inv = lmax > 0.f ? 1.f / lmax : 0.f;
+#pragma unroll
+        for (int l = 0; l < 6; ++l) lamh[l * kTile + row] = __float2half_rn(lam[l] * inv);
+      }
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      const float cs2_end = cs_s[kTile - 1];
+      cs_end = cs2_end * 0.69314718055994531f;  // natural log decay of the whole tile
+
+      // decayed V for the chunk state: X[s] = exp(cs_end - cs_s) V[s]
+      wait_bar_w(c, B_V_FULL, it & 1);
+      if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
+      {
+        const float dec = ex2(cs2_end - cs2_t);
+        const uint32_t off_row = hf * kHalf + row * 128;
+        const uint4* src = reinterpret_cast<const uint4*>(s + kOffV + off_row);
+        uint4* dst = reinterpret_cast<uint4*>(s + kOffX + off_row);
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
-          const uint4 v = src[c8];
+          const int cc = c8 ^ (row & 7);  // lanes of a warp spread over the banks
+          uint4 v = src[cc];
+          uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack_bf16x2(w[i]);
+            w[i] = pack_bf16x2(f.x * dec, f.y * dec);
+          }
+          dst[cc] = v;
+        }
+      }
+      fence_proxy_async_shared();
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      if (leader) mbar_arrive(c.bars + B_VT_READY);
+
+      // chunk state S_j (its TMEM region takes PV after P_READY); the state
+      // product has read X, so X stages it at once: for even j as the node
+      // F_j = S_j, for odd j as the raw state, merged after the mask
+      const uint32_t tR = tl + kTmR0 + (it & 1) * 128;
+      const size_t node_j = (size_t)bh * p.Nt + j;
+      {
+        wait_bar_w(c, B_STATE_DONE, it & 1);
+        __syncwarp();
+        tc_fence_after();
+        float acc[64];
+        tmem_ld32(tR + 64 * hf, acc);
+        tmem_ld32(tR + 64 * hf + 32, acc + 32);
+        tmem_ld_wait();
+        if (leader) {
+          p.Gt[node_j] = cs_end;
+          if (!(j & 1)) p.G[node_j] = cs_end;
+        }
+        stage(acc);
+      }
+
+      // masked scores -> P (bf16) back into the scores' TMEM columns.  This
+      // thread takes columns 32 g + 16 hf + [0, 16) of each 32-group g, so
+      // both warps of a quadrant share its diagonal group.  g < q (all s < t):
+      // the level (6 or 7) is constant over the group and exp(cs_t - cs_s) =
+      // exp(cs_t - cs_e) exp(cs_e - cs_s), e = 32 g + 31, the second factor
+      // from the per-tile table;  g == q: per element, levels 0..5 from the
+      // half table;  g > q: zero.
+      wait_bar_w(c, B_S_DONE, it & 1);
+      __syncwarp();
+      tc_fence_after();
+      uint32_t pw[2][8];
+#pragma unroll
+      for (int g = 0; g < 4; ++g) {
+        const int s0 = 32 * g + 16 * hf;
+        float v[16];
+        if (g < q) {
+          tmem_ld16(tl + kTmS + s0, v);
+          const float lg = (q ^ g) == 1 ? lam[6] : lam[7];  // level 5 + bitlen(q ^ g)
+          const float rf = lg * ex2(cs2_t - cs_s[32 * g + 31]);
+          const float4* cp = reinterpret_cast<const float4*>(col_s + s0);
+          float cf[16];
+#pragma unroll
+          for (int i4 = 0; i4 < 4; ++i4) {
+            const float4 f = cp[i4];
+            cf[4 * i4] = f.x; cf[4 * i4 + 1] = f.y; cf[4 * i4 + 2] = f.z; cf[4 * i4 + 3] = f.w;
+          }
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] *= rf * cf[i];
+        } else if (g == q) {
+          tmem_ld16(tl + kTmS + s0, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 16; ++i) {
+            const int x = 16 * hf + i;  // column inside the diagonal group
+            const float e = ex2(cs2_diag - cs_s[s0 + i]) * __half2float(lamh[(32 - __clz(lane ^ x)) * kTile + row]);
+            v[i] = (x <= lane) ? v[i] * e : 0.f;
+          }
+        } else {
+#pragma unroll
+          for (int i = 0; i < 16; ++i) v[i] = 0.f;
+        }
+        uint32_t w[8];
+#pragma unroll
+        for (int i = 0; i < 8; ++i) w[i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
+        if (g < 2) {
+#pragma unroll
+          for (int i = 0; i < 8; ++i) pw[g][i] = w[i];
+        } else {
+          tmem_st8(tl + kTmS + 16 * g + 8 * hf, w);
+        }
+        if (g == 1) {
+          // P (64 columns) overwrites the scores of groups 0 and 1, which the
+          // quadrant's other warp reads too: both have read them before either writes
+          tc_fence_before();
+          named_bar_sync(2 + q, 64);
+          tc_fence_after();
+          tmem_st8(tl + kTmS + 8 * hf, pw[0]);
+          tmem_st8(tl + kTmS + 16 + 8 * hf, pw[1]);
+        }
+      }
+      tmem_st_wait();
+      if (it > 0) wait_bar_w(c, B_O_DONE, (it - 1) & 1);  // PV of the previous tile (read in the back half)
+      tc_fence_before();  // orders the state and score reads and the P writes before the PV product
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      if (leader) mbar_arrive(c.bars + B_P_READY);
+
+      if (j & 1) {
+        // odd j: F_j = S_j + the decayed states of tiles (j - 2^cto(j), j),
+        // brought by the producer as pieces (published nodes or raw states)
+        // into K and V; S_j is still staged in X (bf16)
+        float acc[64];
+        const unsigned char* xr = s + kOffX + hf * kHalf + row * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(xr + ((c8 ^ (row & 7)) << 4));
           const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 f = unpack_bf16x2(w[i]);
-            acc[c8 * 8 + 2 * i] = fmaf(sc, f.x, acc[c8 * 8 + 2 * i]);
-            acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
+            acc[c8 * 8 + 2 * i] = f.x;
+            acc[c8 * 8 + 2 * i + 1] = f.y;
           }
         }
-        dec += p.G[node];
-      }
-      uint4* dst = reinterpret_cast<uint4*>(p.F + (node_j * kD + row) * kD + 64 * hf);
+        const float* pdesc = reinterpret_cast<const float*>(s + kOffMisc + 40);
+        // the leader decides whether another piece follows, so every warp
+        // runs the same number of named barriers (alternating words)
+        volatile int* more_s = reinterpret_cast<volatile int*>(s + kOffMisc + 20);
+        const int max_pieces = (1 << (__ffs(~j) - 1)) - 1;
+        float r_end = 0.f;
+        for (int idx = 0; idx < max_pieces; ++idx) {
+          const int b = idx & 1;
+          wait_bar_w(c, B_PC_FULL0 + b, npc[b] & 1);
+          const float r0 = pdesc[3 * b];
+          r_end = pdesc[3 * b + 1];
+          const float sc = ex2((cs_end + r0) * kLog2e);  // decay from the piece's end to the end of tile j
+          const unsigned char* src = s + (b ? kOffV : kOffK) + hf * kHalf + row * 128;
 #pragma unroll
-      for (int c8 = 0; c8 < 8; ++c8) {
-        uint4 v;
-        uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+          for (int c8 = 0; c8 < 8; ++c8) {
+            const uint4 v = *reinterpret_cast<const uint4*>(src + ((c8 ^ (row & 7)) << 4));
+            const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
 #pragma unroll
-        for (int i = 0; i < 4; ++i) w[i] = pack_bf16x2(acc[c8 * 8 + 2 * i], acc[c8 * 8 + 2 * i + 1]);
-        dst[c8] = v;
-      }
-      if (leader) p.G[node_j] = dec;
-      __syncwarp();
-      named_bar_sync(1, kEpi);  // every row of F_j is written (CTA scope)
-      if (leader) mbar_arrive(c.bars + B_FJ_WRITTEN);  // the publisher warp makes it visible
-    }
-
-    // masked scores -> P (bf16, K-major swizzled) in X.  Thread row t, column
-    // groups g of 32:  g < q (all s < t): the level is constant over the group
-    // and exp(cs_t - cs_s) = exp(cs_t - cs_e) exp(cs_e - cs_s), e = 32 g + 31,
-    // the second factor from the per-tile table;  g == q: per element;
-    // g > q: zero.
-    const float* lam_row = lam_s + row * p.L;
-    wait_bar_w(c, B_S_DONE, it & 1);
-    __syncwarp();
-    tc_fence_after();
-#pragma unroll
-    for (int c32 = 0; c32 < 2; ++c32) {
-      const int g = 2 * hf + c32;
-      const int s0 = 32 * g;
-      float v[32];
-      if (g < q) {
-        tmem_ld32(tl + kTmS + s0, v);
-        const float rf = lam_row[32 - __clz(row ^ s0)] * ex2(cs2_t - cs_s[s0 + 31]);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] *= rf * col_s[s0 + i];
-      } else if (g == q) {
-        tmem_ld32(tl + kTmS + s0, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int i = 0; i < 32; ++i) {
-          const float e = ex2(cs2_t - cs_s[s0 + i]) * lam_row[32 - __clz(lane ^ i)];
-          v[i] = (i <= lane) ? v[i] * e : 0.f;
+            for (int i = 0; i < 4; ++i) {
+              const float2 f = unpack_bf16x2(w[i]);
+              acc[c8 * 8 + 2 * i] = fmaf(sc, f.x, acc[c8 * 8 + 2 * i]);
+              acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
+            }
+          }
+          if (leader) more_s[idx & 1] = (pdesc[3 * b + 2] == 0.f && !*c.abort_s) ? 1 : 0;
+          __syncwarp();
+          named_bar_sync(1, kEpi);  // every row of the piece is read
+          if (leader) mbar_arrive(c.bars + B_PC_FREE0 + b);
+          ++npc[b];
+          if (!more_s[idx & 1]) break;
         }
-      } else {
-#pragma unroll
-        for (int i = 0; i < 32; ++i) v[i] = 0.f;
+        if (leader) p.G[node_j] = cs_end + r_end;
+        stage(acc);
       }
-      unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;
-#pragma unroll
-      for (int u4 = 0; u4 < 4; ++u4) {
-        const int c8 = 4 * c32 + u4;
-        uint4 w;
-        w.x = pack_bf16x2(v[8 * u4 + 0], v[8 * u4 + 1]);
-        w.y = pack_bf16x2(v[8 * u4 + 2], v[8 * u4 + 3]);
-        w.z = pack_bf16x2(v[8 * u4 + 4], v[8 * u4 + 5]);
-        w.w = pack_bf16x2(v[8 * u4 + 6], v[8 * u4 + 7]);
-        *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) = w;
-      }
-    }
-    tc_fence_before();
-    fence_proxy_async_shared();
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    if (leader) {
-      mbar_arrive(c.bars + B_S_FREE);
-      mbar_arrive(c.bars + B_P_READY);
     }
 
-    // inter-tile levels, accumulated in registers with their per-row weights
-    float oacc[64];
+    if (it >= 1) {
+      // ================= back half of tile it-1: inter-tile levels + output
+      const size_t rp = (size_t)bhp * p.T + (size_t)jp * kTile + row;
+      // (the CTA's last tile has no front half after it to load this in)
+      if (it == n && jp != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp) - 1));
+      const float dlev = jp != 0 ? level_decays(jp, bhp) : 0.f;
+      float oacc[64];
 #pragma unroll
-    for (int i = 0; i < 64; ++i) oacc[i] = 0.f;
-    float D = 0.f;
-    for (int h = 0; (j >> h) != 0; ++h) {
-      if (!((j >> h) & 1)) continue;
-      const size_t node = (size_t)bh * p.Nt + node_of_level(j, h);
-      const float w = lam_s[row * p.L + 8 + h] * exp2f((cs_t + D) * kLog2e);
-      wait_bar_w(c, B_LVL_DONE, lcnt & 1);
+      for (int i = 0; i < 64; ++i) oacc[i] = 0.f;
+      int l = 0;
+      for (int rem = jp; rem != 0; ++l) {
+        rem &= rem - 1;
+        const float lam_h = lam_c;
+        // the next level's lambda loads while this level is read
+        if (rem != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(rem) - 1));
+        const float w = lam_h * ex2((cs_prev + __shfl_sync(0xffffffffu, dlev, l)) * kLog2e);
+        const int b = l & 1;
+        wait_bar_w(c, B_LVL_DONE0 + b, ne[b] & 1);
+        __syncwarp();
+        tc_fence_after();
+        const uint32_t tb = tl + (b ? kTmS : kTmLvl) + 64 * hf;
+#pragma unroll
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float v[32];
+          tmem_ld32(tb + 32 * c32, v);
+          tmem_ld_wait();
+#pragma unroll
+          for (int i = 0; i < 32; ++i) oacc[32 * c32 + i] = fmaf(w, v[i], oacc[32 * c32 + i]);
+        }
+        tc_fence_before();
+        __syncwarp();
+        named_bar_sync(1, kEpi);
+        if (leader) mbar_arrive(c.bars + B_LVL_FREE0 + b);
+        ++ne[b];
+      }
+
+      // output = intra (PV) + inter, staged in X for a TMA store
+      if (it == n) wait_bar_w(c, B_O_DONE, (it - 1) & 1);
       __syncwarp();
       tc_fence_after();
+      const uint32_t tRp = tl + kTmR0 + ((it - 1) & 1) * 128 + 64 * hf;
 #pragma unroll
       for (int c32 = 0; c32 < 2; ++c32) {
         float v[32];
-        tmem_ld32(tl + kTmLvl + 64 * hf + 32 * c32, v);
+        tmem_ld32(tRp + 32 * c32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) oacc[32 * c32 + i] = fmaf(w, v[i], oacc[32 * c32 + i]);
+        for (int i = 0; i < 32; ++i) oacc[32 * c32 + i] += v[i];
       }
+      // the region is free once every thread is past this point; the next
+      // tile's VT_READY arrival (after later named barriers) hands it back
       tc_fence_before();
-      __syncwarp();
-    named_bar_sync(1, kEpi);
-      if (leader) mbar_arrive(c.bars + B_LVL_FREE);
-      ++lcnt;
-      wait_flag_w(c, node);
-      D += p.G[node];
+      stage(oacc);
     }
 
-    // output = intra + inter, bf16
-    wait_bar_w(c, B_O_DONE, it & 1);
-    __syncwarp();
-    tc_fence_after();
-    {
-      __nv_bfloat16* orow = p.o + ((size_t)bh * p.T + (size_t)j * kTile + row) * kD + 64 * hf;
-#pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float v[32];
-        tmem_ld32(tl + kTmO + 64 * hf + 32 * c32, v);
-        tmem_ld_wait();
-#pragma unroll
-        for (int u4 = 0; u4 < 4; ++u4) {
-          uint4 w;
-          const float* a = oacc + 32 * c32 + 8 * u4;
-          const float* b = v + 8 * u4;
-          w.x = pack_bf16x2(a[0] + b[0], a[1] + b[1]);
-          w.y = pack_bf16x2(a[2] + b[2], a[3] + b[3]);
-          w.z = pack_bf16x2(a[4] + b[4], a[5] + b[5]);
-          w.w = pack_bf16x2(a[6] + b[6], a[7] + b[7]);
-          reinterpret_cast<uint4*>(orow)[4 * c32 + u4] = w;
-        }
-      }
-    }
-    tc_fence_before();
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    if (leader) {
-      mbar_arrive(c.bars + B_O_FREE);
-      mbar_arrive(c.bars + B_AUX_FREE0 + slot);
-    }
+    cs_prev = cs_t;
+    jp = j;
+    bhp = bh;
   }
 }
 
-// ------------------------------------------------------------------ publisher (warp 10)
-// Makes each tile's node visible at gpu scope and raises its flag, so the
-// epilogue never stalls on the fence.
-__device__ void publisher(const Ctx& c) {
+// ------------------------------------------------------------------ store warp (warp 10)
+// Stores what the epilogue staged in X with the TMA, in the epilogue's order
+// (per step: the node F_j, or for odd j the raw state and then the merged
+// node; then the previous tile's output), hands X back once the copy has read
+// it, and publishes each node or raw state at gpu scope once its store is
+// complete.
+__device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMap* tf, const CUtensorMap* tr) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
-  uint32_t it = 0;
-  for (int u = blockIdx.x; u < total; u += gridDim.x, ++it) {
-    const size_t node_j = (size_t)(u % p.BH) * p.Nt + u / p.BH;
-    wait_bar(c, B_FJ_WRITTEN, it & 1);
-    __threadfence();
-    st_release_u64(p.flags + node_j, p.token);
+  const int n = tiles_of_cta(total);
+  const unsigned char* x = c.base + kOffX;
+  uint32_t xs = 0;
+  auto store = [&](const CUtensorMap* map, int row0) {
+    wait_bar(c, B_X_STAGED, xs & 1);
+    fence_proxy_async_shared();
+    tma_store_2d(map, x, 0, row0);
+    tma_store_2d(map, x + kHalf, 64, row0);
+    bulk_commit();
+    bulk_wait_read0();
+    mbar_arrive(c.bars + B_X_FREE);
+    ++xs;
+  };
+  // the node's bytes (async proxy) and its log-decay total (written by the
+  // epilogue before X_STAGED) are ordered before the release of the flag
+  auto publish = [&](uint64_t* flags, size_t node) {
+    bulk_wait0();
+    fence_proxy_async_global();
+    st_release_u64(flags + node, p.token);
+  };
+  for (int it = 0; it <= n; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    const int bh = u % p.BH, j = u / p.BH;
+    const size_t node_j = (size_t)bh * p.Nt + j;
+    if (it < n) {
+      if (!(j & 1)) {
+        store(tf, (int)(node_j * kD));
+        publish(p.flags, node_j);
+      } else {
+        store(tr, (int)(node_j * kD));
+        publish(p.rflags, node_j);
+        store(tf, (int)(node_j * kD));
+        publish(p.flags, node_j);
+      }
+    }
+    if (it >= 1) {
+      const int up = u - gridDim.x;
+      store(to, (up % p.BH) * p.T + (up / p.BH) * kTile);
+    }
   }
+  bulk_wait0();
 }
 
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
-                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf, TcParams p) {
-  extern __shared__ unsigned char smem_raw[];
-  unsigned char* base =
-      reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(smem_raw) + 1023) & ~uintptr_t(1023));
+                  const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf,
+                  const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tr, TcParams p) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  // the 128-byte swizzle of the operand tiles assumes a 1024-aligned base;
+  // the budget leaves no room to realign, so refuse (all threads) otherwise
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(p.err, kErrDeviceArg);
+    return;
+  }
+  unsigned char* base = smem_raw;
   const int warp = threadIdx.x >> 5, lane = threadIdx.x & 31;
   uint64_t* bars = reinterpret_cast<uint64_t*>(base + kOffBars);
   volatile int* abort_s = reinterpret_cast<volatile int*>(base + kOffMisc + 16);
@@ -601,6 +863,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tk);
     prefetch_tmap(&tv);
     prefetch_tmap(&tf);
+    prefetch_tmap(&to);
+    prefetch_tmap(&tr);
   }
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
@@ -612,11 +876,11 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer(c, &tq, &tk, &tv, &tf);
+    if (lane == 0) producer(c, &tq, &tk, &tv, &tf, &tr);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(c, tmem);
   } else if (warp == kPubWarp) {
-    if (lane == 0) publisher(c);
+    if (lane == 0) store_warp(c, &to, &tf, &tr);
   } else {
     epilogue(c, tmem, warp, lane);
   }
@@ -655,7 +919,7 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
 // ------------------------------------------------------------------ host side
 struct TcPlan {
   int Nt;
-  size_t off_F, off_G, off_flags, total;
+  size_t off_F, off_R, off_G, off_Gt, off_flags, off_rflags, total;
 };
 
 TcPlan tc_plan(const ll_shape& s) {
@@ -663,9 +927,12 @@ TcPlan tc_plan(const ll_shape& s) {
   p.Nt = s.T / kTile;
   const size_t nodes = (size_t)s.B * s.H * p.Nt;
   size_t off = 0;
-  p.off_F = off;     off = align_up(off + nodes * kD * kD * 2, 1024);
-  p.off_G = off;     off = align_up(off + nodes * 4, 256);
-  p.off_flags = off; off = align_up(off + (nodes + 1) * 8, 256);
+  p.off_F = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
+  p.off_R = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
+  p.off_G = off;      off = align_up(off + nodes * 4, 256);
+  p.off_Gt = off;     off = align_up(off + nodes * 4, 256);
+  p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
+  p.off_rflags = off; off = align_up(off + nodes * 8, 256);
   p.total = off;
   return p;
 }
@@ -725,9 +992,10 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   const int BH = s.B * s.H;
   const uint64_t rows = (uint64_t)BH * s.T;
   const uint64_t node_rows = (uint64_t)BH * plan.Nt * kD;
-  CUtensorMap tq, tk, tv, tf;
+  CUtensorMap tq, tk, tv, tf, to, tr;
   if (!make_map(&tq, a.q, rows) || !make_map(&tk, a.k, rows) || !make_map(&tv, a.v, rows) ||
-      !make_map(&tf, ws + plan.off_F, node_rows))
+      !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows) ||
+      !make_map(&tr, ws + plan.off_R, node_rows))
     return LL_ERR_CUDA;
 
   TcParams p;
@@ -736,10 +1004,11 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.q = static_cast<const __nv_bfloat16*>(a.q);
   p.k = static_cast<const __nv_bfloat16*>(a.k);
   p.v = static_cast<const __nv_bfloat16*>(a.v);
-  p.o = static_cast<__nv_bfloat16*>(a.o);
   p.F = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_F);
   p.G = reinterpret_cast<float*>(ws + plan.off_G);
   p.flags = reinterpret_cast<uint64_t*>(ws + plan.off_flags);
+  p.Gt = reinterpret_cast<float*>(ws + plan.off_Gt);
+  p.rflags = reinterpret_cast<uint64_t*>(ws + plan.off_rflags);
   p.abort_word = p.flags + (size_t)BH * plan.Nt;
   p.token = next_token();
   p.BH = BH;
@@ -757,7 +1026,7 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   const long long tiles = (long long)BH * plan.Nt;
   const int grid = (int)std::min<long long>(tiles, (long long)sms * per_sm);
 
-  void* args[] = {&tq, &tk, &tv, &tf, &p};
+  void* args[] = {&tq, &tk, &tv, &tf, &to, &tr, &p};
   LL_CUDA_OK(cudaLaunchCooperativeKernel((const void*)fwd_tc_kernel, dim3(grid), dim3(kThreads), args, kSmemBytes,
                                          a.stream));
   if (a.state_out) {

@@ -119,3 +119,32 @@ def test_repeated_calls_same_workspace(B):
     assert rel_err(outs[0].numpy(), _oracle(a)) <= TOL_BF16
     assert rel_err(outs[1].numpy(), _oracle(b)) <= TOL_BF16
     assert torch.equal(outs[0], outs[2])  # deterministic
+
+
+def _sampled_rows(T, per_tile=(0, 45, 77, 127)):
+    return np.array([j * 128 + r for j in range(T // 128) for r in per_tile])
+
+
+def _check_sampled(out, inp, rows):
+    f = {n: synth.to_f64(inp[n]) for n in ("q", "k", "v", "log_alpha", "lam")}
+    Bn, H = out.shape[:2]
+    ref = np.stack([np.stack([mamba2.forward_rows(f["q"][b, h], f["k"][b, h], f["v"][b, h], f["log_alpha"][b, h],
+                                                  f["lam"][b, h], rows) for h in range(H)]) for b in range(Bn)])
+    return rel_err(out[:, :, rows], ref)
+
+
+@pytest.mark.parametrize("la_mode", ["softplus", "slow"])
+def test_more_tiles_than_ctas(B, la_mode):
+    # 16 heads x 32 tiles = 512 tiles: most CTAs run 3-4 pipelined steps
+    T = 4096
+    inp = synth.make_inputs(_cfg(T, Bn=1, H=16), la_mode=la_mode, tag=f"tcsteps_{la_mode}")
+    assert _check_sampled(_run(B, inp), inp, _sampled_rows(T)) <= TOL_BF16
+
+
+def test_full_size_workload_sampled_rows(B):
+    # the 16K-token, 16-head workload the benchmark times, sampled rows of every tile
+    cfg = dict(synth.WORKLOADS["mamba2_bf16_t16k"])
+    inp = synth.make_inputs(cfg)
+    out = _run(B, inp)
+    assert np.isfinite(out).all()
+    assert _check_sampled(out, inp, _sampled_rows(cfg["T"], per_tile=(0, 127))) <= TOL_BF16
