@@ -81,17 +81,22 @@ constexpr uint32_t kOffF1 = kOffF0 + kTileBytes;
 constexpr uint32_t kOffCs = kOffF1 + kTileBytes;  // float[128] cumsum x log2(e)
 constexpr uint32_t kOffCol = kOffCs + kTile * 4;  // float[128] exp(cs_e - cs_s), e = end of s's 32-group
 constexpr uint32_t kOffLam = kOffCol + kTile * 4; // half[6][128] lambda levels 0..5 / the row's max
-// misc: quadrant totals [0,16), abort flag 16, merge "more pieces" words 20/24,
-// tmem base 32, piece descriptors (R, R_end, last) x 2 at [40, 64)
+// misc: quadrant totals [0,16), abort flag 16, tmem base 32
 constexpr uint32_t kOffMisc = kOffLam + 6 * kTile * 2;
-constexpr uint32_t kOffBars = kOffMisc + 64;            // mbarriers
+// node exchange between the producer and its consumers: level log decays of
+// the previous tile (float[2][16], by step parity) at 0, the F-ring piece
+// descriptors (R, R_end, last, own; float[2][4], by ring slot) at 128, the
+// number of merge pieces ahead of a tile's levels in the ring (int[2], by
+// step parity) at 160, the merge's "more pieces" words (int[2]) at 168
+constexpr uint32_t kOffNode = kOffMisc + 64;
+constexpr uint32_t kOffBars = kOffNode + 192;            // mbarriers
 
 // mbarriers (all with arrival count 1: one producer arrive + TMA bytes, one
 // tcgen05.commit, or one elected thread)
 enum Bar : int {
   B_K_FULL, B_V_FULL, B_Q_FULL0, B_Q_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_K_FREE, B_V_FREE,
   B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_LVL_DONE0, B_LVL_DONE1, B_LVL_FREE0,
-  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_PC_FULL0, B_PC_FULL1, B_PC_FREE0, B_PC_FREE1, kNumBars
+  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD, B_LVLD_FREE, kNumBars
 };
 constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -193,18 +198,6 @@ __device__ __forceinline__ void wait_flag(const Ctx& c, const uint64_t* flags, s
   }
 }
 
-// Warp-collective: lane i < n acquires node idx (published with its log-decay
-// total) and returns that total.  The flags are read together; only the
-// lanes whose node is not published yet spin.
-__device__ __forceinline__ float acquire_nodes(const Ctx& c, int n, size_t idx) {
-  const bool mine = (int)(threadIdx.x & 31) < n;
-  bool ok = !mine || ld_relaxed_u64(c.p->flags + idx) == c.p->token;
-  if (!ok) wait_flag(c, c.p->flags, idx);
-  __syncwarp();
-  fence_acq_rel_gpu();
-  return mine ? c.p->G[idx] : 0.f;
-}
-
 // 2^x with the hardware approximation (relative error ~2^-22, flushes
 // subnormals): ample for factors that end in bf16 operands.
 __device__ __forceinline__ float ex2(float x) {
@@ -225,98 +218,128 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
 // MN-major operand (rows = K, 64-element M/N blocks 16 KB apart), k-step kk of 16 rows.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, kHalf, 1024); }
 
-// ------------------------------------------------------------------ producer
-// Per step i: K, V and Q of tile i; the nodes of tile i-1's levels (F ring);
-// for odd j the pieces of the merge F_j = S_j + sum of the decayed states of
-// tiles (j - 2^cto(j), j), into the K and V buffers once the products of
-// tile i have read them.  The pieces are found by a look-back from j - 1:
-// a node that is already published covers its whole block; otherwise that
-// tile's raw state (published right after its readout) is taken and the walk
-// continues one tile down, so no merge ever waits for another merge.
-// Only the first four level nodes go before the pieces: the load of level k
-// needs the ring slot of level k - 2, whose product needs the epilogue to
-// have read level k - 4, which it does after the merge.
-// Once a wait has expired nothing new is armed; the drain at the end waits
-// (bounded) for the copies already issued.
-__device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv,
-                         const CUtensorMap* tf, const CUtensorMap* tr) {
+// ------------------------------------------------------------------ producers (warp 0, lanes 1 and 0)
+// Lane 1 streams K, V and Q of every tile.
+__device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
   const TcParams& p = *c.p;
-  const int total = p.BH * p.Nt;
-  const int n = tiles_of_cta(total);
-  uint32_t kc = 0, vc = 0, qc[2] = {0, 0}, fcnt = 0, npc[2] = {0, 0};
+  const int n = tiles_of_cta(p.BH * p.Nt);
+  uint32_t kc = 0, vc = 0, qc[2] = {0, 0};
   unsigned char* s = c.base;
-  float* pdesc = reinterpret_cast<float*>(s + kOffMisc + 40);  // per piece buffer: R, R_end, last
-
-  // the level nodes of tile (bhp, jp) from its first-th level on, at most count of them
-  auto load_levels = [&](int bhp, int jp, int first, int count) {
-    int l = 0;
-    for (int h = 0; (jp >> h) != 0 && count > 0; ++h) {
-      if (!((jp >> h) & 1)) continue;
-      if (l++ < first) continue;
-      if (*c.abort_s) return;
-      const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
-      wait_flag(c, p.flags, node);
-      fence_proxy_async_global();
-      const int fs = fcnt & 1;
-      if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
-      if (*c.abort_s) return;
-      unsigned char* fdst = s + (fs ? kOffF1 : kOffF0);
-      mbar_arrive_expect_tx(c.bars + B_F_FULL0 + fs, kTileBytes);
-      tma_load_2d(fdst, tf, c.bars + B_F_FULL0 + fs, 0, (int)(node * kD));
-      tma_load_2d(fdst + kHalf, tf, c.bars + B_F_FULL0 + fs, 64, (int)(node * kD));
-      ++fcnt;
-      --count;
+  for (int it = 0; it < n && !*c.abort_s; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    const int row0 = (u % p.BH) * p.T + (u / p.BH) * kTile;
+    // stage the next tile's inputs in L2 while this one is processed
+    if (it + 1 < n) {
+      const int un = u + gridDim.x;
+      const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
+      bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
+      bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
+      bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
     }
+    if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);
+    if (*c.abort_s) break;
+    mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
+    tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
+    tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_K_FULL, 64, row0);
+    ++kc;
+    if (it > 0) wait_bar(c, B_V_FREE, (it - 1) & 1);
+    if (*c.abort_s) break;
+    mbar_arrive_expect_tx(c.bars + B_V_FULL, kTileBytes);
+    tma_load_2d(s + kOffV, tv, c.bars + B_V_FULL, 0, row0);
+    tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_V_FULL, 64, row0);
+    ++vc;
+    const int qs = it & 1;
+    if (it >= 2) wait_bar(c, B_Q_FREE0 + qs, ((it - 2) >> 1) & 1);
+    if (*c.abort_s) break;
+    unsigned char* qdst = s + (qs ? kOffQ1 : kOffQ0);
+    mbar_arrive_expect_tx(c.bars + B_Q_FULL0 + qs, kTileBytes);
+    tma_load_2d(qdst, tq, c.bars + B_Q_FULL0 + qs, 0, row0);
+    tma_load_2d(qdst + kHalf, tq, c.bars + B_Q_FULL0 + qs, 64, row0);
+    ++qc[qs];
+  }
+  // drain: every copy armed above has landed before the CTA may exit
+  if (kc > 0) drain_bar(c, B_K_FULL, (kc - 1) & 1);
+  if (vc > 0) drain_bar(c, B_V_FULL, (vc - 1) & 1);
+  for (int b = 0; b < 2; ++b)
+    if (qc[b] > 0) drain_bar(c, B_Q_FULL0 + b, (qc[b] - 1) & 1);
+}
+
+// Lane 0 runs the F ring (two 32 KB slots).  Per step i: it acquires the
+// Fenwick nodes of tile i-1's levels, hands their log decays to the epilogue
+// (B_LVLD), loads them for the MMA; then, for odd j, it loads the pieces of
+// the merge F_j = S_j + sum of the decayed states of tiles (j - 2^cto(j), j)
+// for the epilogue: first the tile's own raw state, then a look-back from
+// j - 1 that takes a published node for its whole block or else one tile's
+// raw state (published right after its readout), so no merge ever waits for
+// another merge.  Once a wait has expired nothing new is armed.
+__device__ void producer_nodes(const Ctx& c, const CUtensorMap* tf, const CUtensorMap* tr) {
+  const TcParams& p = *c.p;
+  const int n = tiles_of_cta(p.BH * p.Nt);
+  unsigned char* s = c.base;
+  float* dl = reinterpret_cast<float*>(s + kOffNode);          // [2][16]
+  float* pdesc = reinterpret_cast<float*>(s + kOffNode + 128);  // [2][4]
+  int* npc_s = reinterpret_cast<int*>(s + kOffNode + 160);      // [2]
+  uint32_t fcnt = 0;
+  int npieces = 0;  // merge pieces of the previous tile
+
+  // one ring entry; desc (R, R_end, last, own) goes with a merge piece
+  auto ring_load = [&](const CUtensorMap* map, size_t node, const float* desc) {
+    const int fs = fcnt & 1;
+    if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
+    if (*c.abort_s) return false;
+    if (desc)
+      for (int i = 0; i < 4; ++i) pdesc[4 * fs + i] = desc[i];
+    unsigned char* dst = s + (fs ? kOffF1 : kOffF0);
+    mbar_arrive_expect_tx(c.bars + B_F_FULL0 + fs, kTileBytes);
+    tma_load_2d(dst, map, c.bars + B_F_FULL0 + fs, 0, (int)(node * kD));
+    tma_load_2d(dst + kHalf, map, c.bars + B_F_FULL0 + fs, 64, (int)(node * kD));
+    ++fcnt;
+    return true;
   };
 
   for (int it = 0; it <= n && !*c.abort_s; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
-    const int bh = u % p.BH, j = u / p.BH;
-    if (it < n) {
-      const int row0 = bh * p.T + j * kTile;
-      // stage the next tile's inputs in L2 while this one is processed
-      if (it + 1 < n) {
-        const int un = u + gridDim.x;
-        const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
-        bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
-        bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
-        bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
-        bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
-        bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+    if (it >= 1) {
+      const int up = u - gridDim.x;
+      const int bhp = up % p.BH, jp = up / p.BH;
+      // the back half two steps ago is done: the MMA and the epilogue have
+      // both passed the previous B_LVLD phase (so this arrival cannot run two
+      // phases ahead of a waiter) and nobody reads this parity's decays
+      if (it >= 2) wait_bar(c, B_LVLD_FREE, (it - 2) & 1);
+      float D = 0.f;
+      int l = 0;
+      for (int h = 0; (jp >> h) != 0; ++h) {
+        if (!((jp >> h) & 1)) continue;
+        const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
+        wait_flag(c, p.flags, node);
+        dl[16 * (it & 1) + l++] = D;
+        D += p.G[node];
       }
-      // K and V go where the previous tile's products and merge pieces were
-      if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);
-      if (npc[0] > 0) wait_bar(c, B_PC_FREE0, (npc[0] - 1) & 1);
-      if (*c.abort_s) break;
-      mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
-      tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
-      tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_K_FULL, 64, row0);
-      ++kc;
-      if (it > 0) wait_bar(c, B_V_FREE, (it - 1) & 1);
-      if (npc[1] > 0) wait_bar(c, B_PC_FREE1, (npc[1] - 1) & 1);
-      if (*c.abort_s) break;
-      mbar_arrive_expect_tx(c.bars + B_V_FULL, kTileBytes);
-      tma_load_2d(s + kOffV, tv, c.bars + B_V_FULL, 0, row0);
-      tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_V_FULL, 64, row0);
-      ++vc;
-      const int qs = it & 1;
-      if (it >= 2) wait_bar(c, B_Q_FREE0 + qs, ((it - 2) >> 1) & 1);
-      if (*c.abort_s) break;
-      unsigned char* qdst = s + (qs ? kOffQ1 : kOffQ0);
-      mbar_arrive_expect_tx(c.bars + B_Q_FULL0 + qs, kTileBytes);
-      tma_load_2d(qdst, tq, c.bars + B_Q_FULL0 + qs, 0, row0);
-      tma_load_2d(qdst + kHalf, tq, c.bars + B_Q_FULL0 + qs, 64, row0);
-      ++qc[qs];
+      npc_s[it & 1] = npieces;
+      mbar_arrive(c.bars + B_LVLD);
+      fence_proxy_async_global();
+      for (int h = 0; (jp >> h) != 0; ++h) {
+        if (!((jp >> h) & 1)) continue;
+        if (!ring_load(tf, (size_t)bhp * p.Nt + node_of_level(jp, h), nullptr)) break;
+      }
     }
-    const int up = u - gridDim.x;
-    if (it >= 1) load_levels(up % p.BH, up / p.BH, 0, 4);
-    if (it < n && (j & 1)) {
-      // merge pieces of tile j, most recent first, alternately into K and V
+    npieces = 0;
+    const int j = u / p.BH;
+    if (it < n && (j & 1) && !*c.abort_s) {
+      const size_t node_j = (size_t)(u % p.BH) * p.Nt + j;
+      // the tile's own raw state, weight 1
+      wait_flag(c, p.rflags, node_j);
+      fence_proxy_async_global();
+      const float own[4] = {0.f, 0.f, 0.f, 1.f};
+      if (!ring_load(tr, node_j, own)) continue;
+      ++npieces;
+      // look-back over tiles (stop, j - 1], most recent first
       const int stop = j - (1 << (__ffs(~j) - 1));
       float R = 0.f;
-      bool used[2] = {false, false};
-      for (int e = j - 1, idx = 0; e > stop && !*c.abort_s; ++idx) {
-        const size_t node = (size_t)bh * p.Nt + e;
+      for (int e = j - 1; e > stop;) {
+        const size_t node = node_j - (size_t)(j - e);
         bool full = true;
         if (e & 1) {
           full = ld_relaxed_u64(p.flags + node) == p.token;
@@ -328,34 +351,15 @@ __device__ void producer(const Ctx& c, const CUtensorMap* tq, const CUtensorMap*
         fence_proxy_async_global();
         const float g = full ? p.G[node] : p.Gt[node];
         const int size = full ? 1 << (__ffs(~e) - 1) : 1;
-        const int b = idx & 1;
-        if (!used[b]) {
-          wait_bar(c, b ? B_V_FREE : B_K_FREE, it & 1);  // the products of this tile have read the buffer
-          used[b] = true;
-        }
-        if (npc[b] > 0) wait_bar(c, B_PC_FREE0 + b, (npc[b] - 1) & 1);
-        if (*c.abort_s) break;
-        pdesc[3 * b] = R;
-        pdesc[3 * b + 1] = R + g;
-        pdesc[3 * b + 2] = (e - size <= stop) ? 1.f : 0.f;
-        unsigned char* dst = s + (b ? kOffV : kOffK);
-        mbar_arrive_expect_tx(c.bars + B_PC_FULL0 + b, kTileBytes);
-        tma_load_2d(dst, full ? tf : tr, c.bars + B_PC_FULL0 + b, 0, (int)(node * kD));
-        tma_load_2d(dst + kHalf, full ? tf : tr, c.bars + B_PC_FULL0 + b, 64, (int)(node * kD));
-        ++npc[b];
+        const float desc[4] = {R, R + g, (e - size <= stop) ? 1.f : 0.f, 0.f};
+        if (!ring_load(full ? tf : tr, node, desc)) break;
+        ++npieces;
         R += g;
         e -= size;
       }
     }
-    if (it >= 1) load_levels(up % p.BH, up / p.BH, 4, 64);
   }
   // drain: every copy armed above has landed before the CTA may exit
-  if (kc > 0) drain_bar(c, B_K_FULL, (kc - 1) & 1);
-  if (vc > 0) drain_bar(c, B_V_FULL, (vc - 1) & 1);
-  for (int b = 0; b < 2; ++b) {
-    if (qc[b] > 0) drain_bar(c, B_Q_FULL0 + b, (qc[b] - 1) & 1);
-    if (npc[b] > 0) drain_bar(c, B_PC_FULL0 + b, (npc[b] - 1) & 1);
-  }
   if (fcnt > 0) drain_bar(c, B_F_FULL0 + ((fcnt - 1) & 1), ((fcnt - 1) >> 1) & 1);
   if (fcnt > 1) drain_bar(c, B_F_FULL0 + ((fcnt - 2) & 1), ((fcnt - 2) >> 1) & 1);
 }
@@ -426,6 +430,9 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
     }
     // the previous tile's levels after PV, which never waits on another CTA
     if (it >= 1) {
+      // the previous tile's merge pieces come before these levels in the ring
+      wait_bar(c, B_LVLD, (it - 1) & 1);
+      fcnt += reinterpret_cast<const volatile int*>(c.base + kOffNode + 160)[it & 1];
       for (int l = 0; l < nlev_p; ++l) issue_level(sQp, l);
       umma_commit(c.bars + B_Q_FREE0 + ((it - 1) & 1));
     }
@@ -452,8 +459,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   __half* lamh = reinterpret_cast<__half*>(s + kOffLam);
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
   unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;  // this thread's 128 B of a staged tile
-  uint32_t ne[2] = {0, 0};   // level products consumed per buffer
-  uint32_t npc[2] = {0, 0};  // merge pieces consumed per buffer (K, V)
+  uint32_t ne[2] = {0, 0};  // level products consumed per buffer
+  uint32_t fpos = 0;        // F-ring entries passed (levels for the MMA, merge pieces here)
   uint32_t xs = 0;          // X stagings so far
 
   // stages 64 values (this thread's row, columns [64 hf, 64 hf + 64)) as bf16
@@ -486,23 +493,6 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
     for (int l = 0; l < 8; ++l) lam_n[l] = __ldg(lr + l);
   };
   fetch(blockIdx.x);
-
-  // log decays of the previous tile's levels: lane l < popc(jp) holds the sum
-  // of the totals of the nodes of the levels below its own
-  auto level_decays = [&](int jp, int bhp) {
-    const int nl = __popc(jp);
-    int rest = jp;  // clear the lane lowest set bits: lane l gets the l-th level
-    for (int k = 0; k < lane && rest != 0; ++k) rest &= rest - 1;
-    const size_t idx = (size_t)bhp * p.Nt + (lane < nl ? node_of_level(jp, __ffs(rest) - 1) : 0);
-    const float g = acquire_nodes(c, nl, idx);
-    float x = g;
-#pragma unroll
-    for (int o = 1; o < 16; o <<= 1) {
-      const float y = __shfl_up_sync(0xffffffffu, x, o);
-      if (lane >= o) x += y;
-    }
-    return x - g;
-  };
 
   float cs_prev = 0.f, lam_c = 0.f;
   int jp = 0, bhp = 0;
@@ -671,57 +661,6 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       named_bar_sync(1, kEpi);
       if (leader) mbar_arrive(c.bars + B_P_READY);
 
-      if (j & 1) {
-        // odd j: F_j = S_j + the decayed states of tiles (j - 2^cto(j), j),
-        // brought by the producer as pieces (published nodes or raw states)
-        // into K and V; S_j is still staged in X (bf16)
-        float acc[64];
-        const unsigned char* xr = s + kOffX + hf * kHalf + row * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(xr + ((c8 ^ (row & 7)) << 4));
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack_bf16x2(w[i]);
-            acc[c8 * 8 + 2 * i] = f.x;
-            acc[c8 * 8 + 2 * i + 1] = f.y;
-          }
-        }
-        const float* pdesc = reinterpret_cast<const float*>(s + kOffMisc + 40);
-        // the leader decides whether another piece follows, so every warp
-        // runs the same number of named barriers (alternating words)
-        volatile int* more_s = reinterpret_cast<volatile int*>(s + kOffMisc + 20);
-        const int max_pieces = (1 << (__ffs(~j) - 1)) - 1;
-        float r_end = 0.f;
-        for (int idx = 0; idx < max_pieces; ++idx) {
-          const int b = idx & 1;
-          wait_bar_w(c, B_PC_FULL0 + b, npc[b] & 1);
-          const float r0 = pdesc[3 * b];
-          r_end = pdesc[3 * b + 1];
-          const float sc = ex2((cs_end + r0) * kLog2e);  // decay from the piece's end to the end of tile j
-          const unsigned char* src = s + (b ? kOffV : kOffK) + hf * kHalf + row * 128;
-#pragma unroll
-          for (int c8 = 0; c8 < 8; ++c8) {
-            const uint4 v = *reinterpret_cast<const uint4*>(src + ((c8 ^ (row & 7)) << 4));
-            const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-            for (int i = 0; i < 4; ++i) {
-              const float2 f = unpack_bf16x2(w[i]);
-              acc[c8 * 8 + 2 * i] = fmaf(sc, f.x, acc[c8 * 8 + 2 * i]);
-              acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
-            }
-          }
-          if (leader) more_s[idx & 1] = (pdesc[3 * b + 2] == 0.f && !*c.abort_s) ? 1 : 0;
-          __syncwarp();
-          named_bar_sync(1, kEpi);  // every row of the piece is read
-          if (leader) mbar_arrive(c.bars + B_PC_FREE0 + b);
-          ++npc[b];
-          if (!more_s[idx & 1]) break;
-        }
-        if (leader) p.G[node_j] = cs_end + r_end;
-        stage(acc);
-      }
     }
 
     if (it >= 1) {
@@ -729,7 +668,9 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       const size_t rp = (size_t)bhp * p.T + (size_t)jp * kTile + row;
       // (the CTA's last tile has no front half after it to load this in)
       if (it == n && jp != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp) - 1));
-      const float dlev = jp != 0 ? level_decays(jp, bhp) : 0.f;
+      // log decays of the levels from the producer: lane l holds level l's
+      wait_bar_w(c, B_LVLD, (it - 1) & 1);
+      const float dlev = reinterpret_cast<const volatile float*>(s + kOffNode)[16 * (it & 1) + (lane & 15)];
       float oacc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) oacc[i] = 0.f;
@@ -777,6 +718,52 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // tile's VT_READY arrival (after later named barriers) hands it back
       tc_fence_before();
       stage(oacc);
+      if (leader) mbar_arrive(c.bars + B_LVLD_FREE);
+      fpos += __popc(jp);
+    }
+
+    if (it < n && (j & 1)) {
+      // odd j: F_j = S_j + the decayed states of tiles (j - 2^cto(j), j), from
+      // the producer's pieces in the F ring: the tile's own raw state (weight
+      // 1), then published nodes or raw states, most recent first.  Merged at
+      // the end of the step, when its inputs are long published.
+      const float* pdesc = reinterpret_cast<const float*>(s + kOffNode + 128);
+      // the leader decides whether another piece follows, so every warp runs
+      // the same number of named barriers (alternating words)
+      volatile int* more_s = reinterpret_cast<volatile int*>(s + kOffNode + 168);
+      const int max_pieces = 1 << (__ffs(~j) - 1);
+      float acc[64];
+#pragma unroll
+      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
+      float r_end = 0.f;
+      for (int idx = 0; idx < max_pieces; ++idx) {
+        const int fs = fpos & 1;
+        wait_bar_w(c, B_F_FULL0 + fs, (fpos >> 1) & 1);
+        const float* d = pdesc + 4 * fs;
+        r_end = d[1];
+        // decay from the piece's end to the end of tile j
+        const float sc = d[3] != 0.f ? 1.f : ex2((cs_end + d[0]) * kLog2e);
+        const unsigned char* src = s + (fs ? kOffF1 : kOffF0) + hf * kHalf + row * 128;
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint4 v = *reinterpret_cast<const uint4*>(src + ((c8 ^ (row & 7)) << 4));
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack_bf16x2(w[i]);
+            acc[c8 * 8 + 2 * i] = fmaf(sc, f.x, acc[c8 * 8 + 2 * i]);
+            acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
+          }
+        }
+        if (leader) more_s[idx & 1] = (d[3] != 0.f || d[2] == 0.f) && !*c.abort_s ? 1 : 0;
+        __syncwarp();
+        named_bar_sync(1, kEpi);  // every row of the piece is read
+        if (leader) mbar_arrive(c.bars + B_F_FREE0 + fs);
+        ++fpos;
+        if (!more_s[idx & 1]) break;
+      }
+      if (leader) p.G[(size_t)bh * p.Nt + j] = cs_end + r_end;
+      stage(acc);
     }
 
     cs_prev = cs_t;
@@ -787,10 +774,10 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
 
 // ------------------------------------------------------------------ store warp (warp 10)
 // Stores what the epilogue staged in X with the TMA, in the epilogue's order
-// (per step: the node F_j, or for odd j the raw state and then the merged
-// node; then the previous tile's output), hands X back once the copy has read
-// it, and publishes each node or raw state at gpu scope once its store is
-// complete.
+// (per step: the node F_j, or for odd j the raw state S_j; the previous
+// tile's output; for odd j the merged node F_j), hands X back once the copy
+// has read it, and publishes each node or raw state at gpu scope once its
+// store is complete.
 __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMap* tf, const CUtensorMap* tr) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
@@ -819,19 +806,16 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
     const int bh = u % p.BH, j = u / p.BH;
     const size_t node_j = (size_t)bh * p.Nt + j;
     if (it < n) {
-      if (!(j & 1)) {
-        store(tf, (int)(node_j * kD));
-        publish(p.flags, node_j);
-      } else {
-        store(tr, (int)(node_j * kD));
-        publish(p.rflags, node_j);
-        store(tf, (int)(node_j * kD));
-        publish(p.flags, node_j);
-      }
+      store(j & 1 ? tr : tf, (int)(node_j * kD));
+      publish(j & 1 ? p.rflags : p.flags, node_j);
     }
     if (it >= 1) {
       const int up = u - gridDim.x;
       store(to, (up % p.BH) * p.T + (up / p.BH) * kTile);
+    }
+    if (it < n && (j & 1)) {
+      store(tf, (int)(node_j * kD));
+      publish(p.flags, node_j);
     }
   }
   bulk_wait0();
@@ -876,7 +860,8 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer(c, &tq, &tk, &tv, &tf, &tr);
+    if (lane == 0) producer_nodes(c, &tf, &tr);
+    else if (lane == 1) producer_kvq(c, &tq, &tk, &tv);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(c, tmem);
   } else if (warp == kPubWarp) {
