@@ -14,21 +14,30 @@
 // gist.science (zh) summary §2.3; the per-level contractions are summed in
 // one accumulator per tile, the pages' "level fusion".)
 //
-// Roles (352 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
+// Roles (384 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
 // i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
 // tiles running at the same time are few positions of many heads and the
 // chains of node dependencies inside one round of tiles stay short):
-//   warp 0      TMA producer: K, V, Q tiles, F nodes (after their publication
-//               flags are seen), L2 prefetch of the next tile
+//   warp 0      lane 1: TMA loads of K, V, Q (+ L2 prefetch of the next tile);
+//               lane 0: the level nodes of the previous tile (F ring), once
+//               their publication words are seen, and their log decays
 //   warp 1      TMEM owner and MMA issuer (one thread)
 //   warps 2..9  epilogue: thread (quadrant q = warp % 4, half hf) owns row
 //               32q + lane of every 128x128 accumulator
-//   warp 10     store warp: TMA stores of the staged nodes and outputs, then
-//               the gpu-scope publication of each node
+//   warp 10     store warp: TMA stores of what the epilogue stages in X
+//               (nodes, raw states, outputs) and the gpu-scope publication of
+//               each node or raw state
+//   warp 11     the pieces of the odd-tile merges (into K and V)
+// Producer roles that wait on other CTAs have warps of their own: spinning
+// lanes of one warp take turns.
 // Software pipeline: in step i the epilogue runs the front half of tile i
-// (cumsum, decayed V, chunk state, masked scores P) and then the back half of
-// tile i-1 (inter-tile levels + output); a node F_j of odd j, which merges
-// nodes published in the same step, is completed after the mask.  The nodes the back
+// (cumsum, decayed V, chunk state staged for publication, masked scores P),
+// then the back half of tile i-1 (inter-tile levels + output), then, for odd
+// j, the merge F_j = S_j + the decayed states of tiles (j - 2^cto(j), j).
+// Every tile publishes its chunk state right after the readout (as the node
+// for even j, as the raw state for odd j), and the merge pieces come from a
+// look-back that takes a published node for its whole block or else one
+// tile's raw state, so no merge waits for another merge.  The nodes the back
 // half reads were published by tiles of the previous step, so it rarely
 // waits; the tensor cores run tile i's products while the epilogue finishes
 // tile i-1.  Q is double-buffered for that; the state and PV accumulators of
@@ -57,8 +66,9 @@ using namespace sm100;
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kLmax = 24;
-constexpr int kThreads = 352;
+constexpr int kThreads = 384;
 constexpr int kPubWarp = 10;
+constexpr int kPieceWarp = 11;
 constexpr int kEpi = 256;
 constexpr uint32_t kHalf = kTile * 64 * 2;  // one [128 x 64] bf16 swizzled block: 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalf;  // 32 KB
@@ -83,11 +93,11 @@ constexpr uint32_t kOffCol = kOffCs + kTile * 4;  // float[128] exp(cs_e - cs_s)
 constexpr uint32_t kOffLam = kOffCol + kTile * 4; // half[6][128] lambda levels 0..5 / the row's max
 // misc: quadrant totals [0,16), abort flag 16, tmem base 32
 constexpr uint32_t kOffMisc = kOffLam + 6 * kTile * 2;
-// node exchange between the producer and its consumers: level log decays of
-// the previous tile (float[2][16], by step parity) at 0, the F-ring piece
-// descriptors (R, R_end, last, own; float[2][4], by ring slot) at 128, the
-// number of merge pieces ahead of a tile's levels in the ring (int[2], by
-// step parity) at 160, the merge's "more pieces" words (int[2]) at 168
+// node exchange between the producers and their consumers: level log decays
+// of the previous tile (float[2][16], by step parity) at 0, the merge piece
+// descriptors (R, R_end, last, own; float[2][4], by buffer K/V) at 128, the
+// step-tagged count of levels whose decay is ready (u32[2], by step parity)
+// at 160, the merge's "more pieces" words (int[2]) at 168
 constexpr uint32_t kOffNode = kOffMisc + 64;
 constexpr uint32_t kOffBars = kOffNode + 192;            // mbarriers
 
@@ -96,7 +106,8 @@ constexpr uint32_t kOffBars = kOffNode + 192;            // mbarriers
 enum Bar : int {
   B_K_FULL, B_V_FULL, B_Q_FULL0, B_Q_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_K_FREE, B_V_FREE,
   B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_LVL_DONE0, B_LVL_DONE1, B_LVL_FREE0,
-  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD, B_LVLD_FREE, kNumBars
+  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD_FREE, B_PC_FULL0, B_PC_FULL1,
+  B_PC_FREE0, B_PC_FREE1, B_KV_REL, kNumBars
 };
 constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -109,11 +120,13 @@ struct TcParams {
   const __nv_bfloat16* v;
   __nv_bfloat16* F;  // [BH * Nt, 128, 128] Fenwick nodes
   float* G;          // [BH * Nt] log-decay totals of the nodes
-  uint64_t* flags;   // [BH * Nt] publication tokens of the nodes
-  float* Gt;         // [BH * Nt] log-decay totals of the tiles
-  uint64_t* rflags;  // [BH * Nt] publication tokens of the raw states (odd tiles, in the node rows of R)
+  // [BH * Nt] publication words: this call's token in the high half, the
+  // log-decay total (node, or tile for a raw state) in the low half, so one
+  // atomic load gives both
+  uint64_t* flags;   // nodes
+  uint64_t* rflags;  // raw states of odd tiles (in the node rows of R)
   uint64_t* abort_word;
-  uint64_t token;
+  uint32_t token;    // per call, never 0
   int BH, T, Nt, L;
   unsigned* err;
 };
@@ -129,7 +142,7 @@ __device__ __forceinline__ void note_abort(const Ctx& c) {
   if (!*c.abort_s) {
     *c.abort_s = 1;
     atomicOr(c.p->err, kErrTimeout);
-    *reinterpret_cast<volatile uint64_t*>(c.p->abort_word) = c.p->token;
+    *reinterpret_cast<volatile uint64_t*>(c.p->abort_word) = ((uint64_t)c.p->token << 32) | 0xffffffffu;
   }
 }
 
@@ -176,26 +189,34 @@ __device__ __forceinline__ void drain_bar(const Ctx& c, int b, uint32_t par) {
     if (globaltimer_ns() - t0 > kTimeoutNs / 8) return;
 }
 
-// Bounded wait until entry `idx` of the flag array `flags` carries this call's token.
-__device__ __forceinline__ void wait_flag(const Ctx& c, const uint64_t* flags, size_t idx) {
+__device__ __forceinline__ bool flag_ok(const Ctx& c, uint64_t w) { return (uint32_t)(w >> 32) == c.p->token; }
+__device__ __forceinline__ float flag_g(uint64_t w) { return __uint_as_float((uint32_t)w); }
+__device__ __forceinline__ bool aborted_elsewhere(const Ctx& c) {
+  return flag_ok(c, *reinterpret_cast<volatile uint64_t*>(c.p->abort_word));
+}
+
+// Bounded wait until entry `idx` of the word array `flags` carries this
+// call's token (acquire); returns the word.
+__device__ __forceinline__ uint64_t wait_flag(const Ctx& c, const uint64_t* flags, size_t idx) {
   const uint64_t* f = flags + idx;
-  if (ld_acquire_u64(f) == c.p->token) return;
-  if (*c.abort_s) return;
+  uint64_t w = ld_acquire_u64(f);
+  if (flag_ok(c, w) || *c.abort_s) return w;
   const uint64_t t0 = globaltimer_ns();
   unsigned ns = 32;
-  while (ld_acquire_u64(f) != c.p->token) {
+  while (!flag_ok(c, w = ld_acquire_u64(f))) {
     __nanosleep(ns);
     if (ns < 128) ns <<= 1;
-    if (*c.abort_s) return;
-    if (*reinterpret_cast<volatile uint64_t*>(c.p->abort_word) == c.p->token) {
+    if (*c.abort_s) return w;
+    if (aborted_elsewhere(c)) {
       *c.abort_s = 1;
-      return;
+      return w;
     }
     if (globaltimer_ns() - t0 > kTimeoutNs) {
       note_abort(c);
-      return;
+      return w;
     }
   }
+  return w;
 }
 
 // 2^x with the hardware approximation (relative error ~2^-22, flushes
@@ -218,8 +239,8 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
 // MN-major operand (rows = K, 64-element M/N blocks 16 KB apart), k-step kk of 16 rows.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, kHalf, 1024); }
 
-// ------------------------------------------------------------------ producers (warp 0, lanes 1 and 0)
-// Lane 1 streams K, V and Q of every tile.
+// ------------------------------------------------------------------ producers (warp 0 lanes 0 and 1, warp 11)
+// Warp 0 lane 1 streams K, V and Q of every tile.
 __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
@@ -238,7 +259,10 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
       bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
       bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
     }
-    if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);
+    if (it > 0) {
+      wait_bar(c, B_K_FREE, (it - 1) & 1);
+      wait_bar(c, B_KV_REL, (it - 1) & 1);  // merge pieces of tile it-1 are done with K and V
+    }
     if (*c.abort_s) break;
     mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
     tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
@@ -266,102 +290,121 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
     if (qc[b] > 0) drain_bar(c, B_Q_FULL0 + b, (qc[b] - 1) & 1);
 }
 
-// Lane 0 runs the F ring (two 32 KB slots).  Per step i: it acquires the
-// Fenwick nodes of tile i-1's levels, hands their log decays to the epilogue
-// (B_LVLD), loads them for the MMA; then, for odd j, it loads the pieces of
-// the merge F_j = S_j + sum of the decayed states of tiles (j - 2^cto(j), j)
-// for the epilogue: first the tile's own raw state, then a look-back from
-// j - 1 that takes a published node for its whole block or else one tile's
-// raw state (published right after its readout), so no merge ever waits for
-// another merge.  Once a wait has expired nothing new is armed.
-__device__ void producer_nodes(const Ctx& c, const CUtensorMap* tf, const CUtensorMap* tr) {
+// Warp 0 lane 0 runs the F ring (two 32 KB slots) of the level nodes for
+// the MMA.  Per step i it acquires the Fenwick nodes of tile i-1's levels in
+// order, hands each level's log decay to the epilogue (a step-tagged count
+// released in shared memory, so the epilogue starts on level 0 before later
+// nodes are published) and loads the node.  Once a wait has expired nothing
+// new is armed.
+__device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
   unsigned char* s = c.base;
-  float* dl = reinterpret_cast<float*>(s + kOffNode);          // [2][16]
-  float* pdesc = reinterpret_cast<float*>(s + kOffNode + 128);  // [2][4]
-  int* npc_s = reinterpret_cast<int*>(s + kOffNode + 160);      // [2]
+  float* dl = reinterpret_cast<float*>(s + kOffNode);               // [2][16]
+  uint32_t* nlr = reinterpret_cast<uint32_t*>(s + kOffNode + 160);  // [2]
   uint32_t fcnt = 0;
-  int npieces = 0;  // merge pieces of the previous tile
-
-  // one ring entry; desc (R, R_end, last, own) goes with a merge piece
-  auto ring_load = [&](const CUtensorMap* map, size_t node, const float* desc) {
-    const int fs = fcnt & 1;
-    if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
-    if (*c.abort_s) return false;
-    if (desc)
-      for (int i = 0; i < 4; ++i) pdesc[4 * fs + i] = desc[i];
-    unsigned char* dst = s + (fs ? kOffF1 : kOffF0);
-    mbar_arrive_expect_tx(c.bars + B_F_FULL0 + fs, kTileBytes);
-    tma_load_2d(dst, map, c.bars + B_F_FULL0 + fs, 0, (int)(node * kD));
-    tma_load_2d(dst + kHalf, map, c.bars + B_F_FULL0 + fs, 64, (int)(node * kD));
-    ++fcnt;
-    return true;
-  };
-
-  for (int it = 0; it <= n && !*c.abort_s; ++it) {
-    const int u = blockIdx.x + it * gridDim.x;
-    if (it >= 1) {
-      const int up = u - gridDim.x;
-      const int bhp = up % p.BH, jp = up / p.BH;
-      // the back half two steps ago is done: the MMA and the epilogue have
-      // both passed the previous B_LVLD phase (so this arrival cannot run two
-      // phases ahead of a waiter) and nobody reads this parity's decays
-      if (it >= 2) wait_bar(c, B_LVLD_FREE, (it - 2) & 1);
-      float D = 0.f;
-      int l = 0;
-      for (int h = 0; (jp >> h) != 0; ++h) {
-        if (!((jp >> h) & 1)) continue;
-        const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
-        wait_flag(c, p.flags, node);
-        dl[16 * (it & 1) + l++] = D;
-        D += p.G[node];
-      }
-      npc_s[it & 1] = npieces;
-      mbar_arrive(c.bars + B_LVLD);
+  for (int it = 1; it <= n && !*c.abort_s; ++it) {
+    const int up = blockIdx.x + (it - 1) * gridDim.x;
+    const int bhp = up % p.BH, jp = up / p.BH;
+    // the back half two steps ago is done (so is every earlier one, among
+    // them the reader of this parity's decays); every back half waits for
+    // this step's tag, so that barrier never runs two phases ahead
+    if (it >= 2) wait_bar(c, B_LVLD_FREE, (it - 2) & 1);
+    st_release_cta_u32(nlr + (it & 1), (uint32_t)it << 8);
+    float D = 0.f;
+    uint32_t l = 0;
+    for (int h = 0; (jp >> h) != 0 && !*c.abort_s; ++h) {
+      if (!((jp >> h) & 1)) continue;
+      const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
+      const uint64_t w = wait_flag(c, p.flags, node);
       fence_proxy_async_global();
-      for (int h = 0; (jp >> h) != 0; ++h) {
-        if (!((jp >> h) & 1)) continue;
-        if (!ring_load(tf, (size_t)bhp * p.Nt + node_of_level(jp, h), nullptr)) break;
-      }
-    }
-    npieces = 0;
-    const int j = u / p.BH;
-    if (it < n && (j & 1) && !*c.abort_s) {
-      const size_t node_j = (size_t)(u % p.BH) * p.Nt + j;
-      // the tile's own raw state, weight 1
-      wait_flag(c, p.rflags, node_j);
-      fence_proxy_async_global();
-      const float own[4] = {0.f, 0.f, 0.f, 1.f};
-      if (!ring_load(tr, node_j, own)) continue;
-      ++npieces;
-      // look-back over tiles (stop, j - 1], most recent first
-      const int stop = j - (1 << (__ffs(~j) - 1));
-      float R = 0.f;
-      for (int e = j - 1; e > stop;) {
-        const size_t node = node_j - (size_t)(j - e);
-        bool full = true;
-        if (e & 1) {
-          full = ld_relaxed_u64(p.flags + node) == p.token;
-          if (full) fence_acq_rel_gpu();
-          else wait_flag(c, p.rflags, node);
-        } else {
-          wait_flag(c, p.flags, node);  // even tiles publish their state as the node at once
-        }
-        fence_proxy_async_global();
-        const float g = full ? p.G[node] : p.Gt[node];
-        const int size = full ? 1 << (__ffs(~e) - 1) : 1;
-        const float desc[4] = {R, R + g, (e - size <= stop) ? 1.f : 0.f, 0.f};
-        if (!ring_load(full ? tf : tr, node, desc)) break;
-        ++npieces;
-        R += g;
-        e -= size;
-      }
+      dl[16 * (it & 1) + l] = D;
+      D += flag_g(w);
+      st_release_cta_u32(nlr + (it & 1), ((uint32_t)it << 8) | ++l);
+      const int fs = fcnt & 1;
+      if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
+      if (*c.abort_s) break;
+      unsigned char* dst = s + (fs ? kOffF1 : kOffF0);
+      mbar_arrive_expect_tx(c.bars + B_F_FULL0 + fs, kTileBytes);
+      tma_load_2d(dst, tf, c.bars + B_F_FULL0 + fs, 0, (int)(node * kD));
+      tma_load_2d(dst + kHalf, tf, c.bars + B_F_FULL0 + fs, 64, (int)(node * kD));
+      ++fcnt;
     }
   }
-  // drain: every copy armed above has landed before the CTA may exit
   if (fcnt > 0) drain_bar(c, B_F_FULL0 + ((fcnt - 1) & 1), ((fcnt - 1) >> 1) & 1);
   if (fcnt > 1) drain_bar(c, B_F_FULL0 + ((fcnt - 2) & 1), ((fcnt - 2) >> 1) & 1);
+}
+
+// Warp 11 brings the pieces of the merge F_j = S_j + sum of the decayed states
+// of tiles (j - 2^cto(j), j) for odd j into the K and V buffers (alternately,
+// once the products of tile j have read them): first the tile's own raw
+// state, then a look-back from j - 1 that takes a published node for its
+// whole block or else one tile's raw state (published right after its
+// readout), so no merge ever waits for another merge.  For even j it releases
+// the K and V buffers for the next tile (B_KV_REL) once the products of tile
+// j have read K; for odd j the epilogue does, after the last piece.
+__device__ void producer_pieces(const Ctx& c, const CUtensorMap* tf, const CUtensorMap* tr) {
+  const TcParams& p = *c.p;
+  const int n = tiles_of_cta(p.BH * p.Nt);
+  unsigned char* s = c.base;
+  float* pdesc = reinterpret_cast<float*>(s + kOffNode + 128);  // [2][4]
+  uint32_t npc[2] = {0, 0};
+  for (int it = 0; it < n && !*c.abort_s; ++it) {
+    const int u = blockIdx.x + it * gridDim.x;
+    const int j = u / p.BH;
+    if (!(j & 1)) {
+      wait_bar(c, B_K_FREE, it & 1);  // K of this tile was loaded: the release cannot run a phase ahead
+      mbar_arrive(c.bars + B_KV_REL);
+      continue;
+    }
+    const size_t node_j = (size_t)(u % p.BH) * p.Nt + j;
+    bool used[2] = {false, false};
+    auto place = [&](int b, const CUtensorMap* map, size_t node, const float* desc) {
+      if (!used[b]) {
+        wait_bar(c, b ? B_V_FREE : B_K_FREE, it & 1);  // the products of this tile have read the buffer
+        used[b] = true;
+      }
+      if (npc[b] > 0) wait_bar(c, B_PC_FREE0 + b, (npc[b] - 1) & 1);
+      if (*c.abort_s) return false;
+      for (int i = 0; i < 4; ++i) pdesc[4 * b + i] = desc[i];
+      unsigned char* dst = s + (b ? kOffV : kOffK);
+      mbar_arrive_expect_tx(c.bars + B_PC_FULL0 + b, kTileBytes);
+      tma_load_2d(dst, map, c.bars + B_PC_FULL0 + b, 0, (int)(node * kD));
+      tma_load_2d(dst + kHalf, map, c.bars + B_PC_FULL0 + b, 64, (int)(node * kD));
+      ++npc[b];
+      return true;
+    };
+    // the tile's own raw state, weight 1
+    wait_flag(c, p.rflags, node_j);
+    fence_proxy_async_global();
+    const float own[4] = {0.f, 0.f, 0.f, 1.f};
+    if (!place(0, tr, node_j, own)) break;
+    // look-back over tiles (stop, j - 1], most recent first
+    const int stop = j - (1 << (__ffs(~j) - 1));
+    float R = 0.f;
+    for (int e = j - 1, idx = 1; e > stop; ++idx) {
+      const size_t node = node_j - (size_t)(j - e);
+      bool full = true;
+      uint64_t w;
+      if (e & 1) {
+        w = ld_relaxed_u64(p.flags + node);
+        full = flag_ok(c, w);
+        if (full) fence_acq_rel_gpu();
+        else w = wait_flag(c, p.rflags, node);
+      } else {
+        w = wait_flag(c, p.flags, node);  // even tiles publish their state as the node at once
+      }
+      fence_proxy_async_global();
+      const float g = flag_g(w);
+      const int size = full ? 1 << (__ffs(~e) - 1) : 1;
+      const float desc[4] = {R, R + g, (e - size <= stop) ? 1.f : 0.f, 0.f};
+      if (!place(idx & 1, full ? tf : tr, node, desc)) break;
+      R += g;
+      e -= size;
+    }
+  }
+  for (int b = 0; b < 2; ++b)
+    if (npc[b] > 0) drain_bar(c, B_PC_FULL0 + b, (npc[b] - 1) & 1);
 }
 
 // ------------------------------------------------------------------ MMA issuer
@@ -430,9 +473,6 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
     }
     // the previous tile's levels after PV, which never waits on another CTA
     if (it >= 1) {
-      // the previous tile's merge pieces come before these levels in the ring
-      wait_bar(c, B_LVLD, (it - 1) & 1);
-      fcnt += reinterpret_cast<const volatile int*>(c.base + kOffNode + 160)[it & 1];
       for (int l = 0; l < nlev_p; ++l) issue_level(sQp, l);
       umma_commit(c.bars + B_Q_FREE0 + ((it - 1) & 1));
     }
@@ -458,29 +498,31 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   float* col_s = reinterpret_cast<float*>(s + kOffCol);
   __half* lamh = reinterpret_cast<__half*>(s + kOffLam);
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
+  volatile float* gpub_s = reinterpret_cast<volatile float*>(s + kOffMisc + 20);  // log-decay total to publish
   unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;  // this thread's 128 B of a staged tile
-  uint32_t ne[2] = {0, 0};  // level products consumed per buffer
-  uint32_t fpos = 0;        // F-ring entries passed (levels for the MMA, merge pieces here)
+  uint32_t ne[2] = {0, 0};   // level products consumed per buffer
+  uint32_t npc[2] = {0, 0};  // merge pieces consumed per buffer (K, V)
   uint32_t xs = 0;          // X stagings so far
 
-  // stages 64 values (this thread's row, columns [64 hf, 64 hf + 64)) as bf16
-  // in X for the store warp; the previous staging has been read out of X
-  auto stage = [&](const float* a) {
+  // stages a tile in X for the store warp (packed bf16 words, 8 per 16 bytes
+  // of this thread's row); the previous staging has been read out of X
+  auto stage_words = [&](const uint32_t* w) {
     if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
 #pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8) {
-      uint4 w;
-      w.x = pack_bf16x2(a[8 * c8 + 0], a[8 * c8 + 1]);
-      w.y = pack_bf16x2(a[8 * c8 + 2], a[8 * c8 + 3]);
-      w.z = pack_bf16x2(a[8 * c8 + 4], a[8 * c8 + 5]);
-      w.w = pack_bf16x2(a[8 * c8 + 6], a[8 * c8 + 7]);
-      *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) = w;
-    }
+    for (int c8 = 0; c8 < 8; ++c8)
+      *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) =
+          make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
     fence_proxy_async_shared();
     __syncwarp();
     named_bar_sync(1, kEpi);
     if (leader) mbar_arrive(c.bars + B_X_STAGED);
     ++xs;
+  };
+  auto stage = [&](const float* a) {
+    uint32_t w[32];
+#pragma unroll
+    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
+    stage_words(w);
   };
 
   // this row's log_alpha and intra-level lambdas, read one tile ahead
@@ -500,6 +542,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
     const int u = blockIdx.x + it * gridDim.x;
     int bh = 0, j = 0;
     float cs_t = 0.f, cs_end = 0.f;
+    uint32_t opk[32];  // the previous tile's output (bf16 pairs) until it is staged
     if (it < n) {
       // ================= front half of tile it
       bh = u % p.BH;
@@ -587,8 +630,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         tmem_ld32(tR + 64 * hf + 32, acc + 32);
         tmem_ld_wait();
         if (leader) {
-          p.Gt[node_j] = cs_end;
           if (!(j & 1)) p.G[node_j] = cs_end;
+          gpub_s[0] = cs_end;  // the word published with this node or raw state
         }
         stage(acc);
       }
@@ -668,9 +711,23 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       const size_t rp = (size_t)bhp * p.T + (size_t)jp * kTile + row;
       // (the CTA's last tile has no front half after it to load this in)
       if (it == n && jp != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp) - 1));
-      // log decays of the levels from the producer: lane l holds level l's
-      wait_bar_w(c, B_LVLD, (it - 1) & 1);
-      const float dlev = reinterpret_cast<const volatile float*>(s + kOffNode)[16 * (it & 1) + (lane & 15)];
+      // log decays of the levels, handed over one by one by the level producer
+      // under a step-tagged count; bounded wait until it covers `cnt` levels
+      const uint32_t* nlr = reinterpret_cast<const uint32_t*>(s + kOffNode + 160) + (it & 1);
+      const volatile float* dl = reinterpret_cast<const volatile float*>(s + kOffNode) + 16 * (it & 1);
+      auto wait_levels = [&](uint32_t cnt) {
+        const uint32_t want = ((uint32_t)it << 8) | cnt;
+        if (ld_acquire_cta_u32(nlr) >= want || *c.abort_s) return;
+        const uint64_t t0 = globaltimer_ns();
+        while (ld_acquire_cta_u32(nlr) < want) {
+          if (*c.abort_s) return;
+          if (globaltimer_ns() - t0 > kTimeoutNs) {
+            note_abort(c);
+            return;
+          }
+        }
+      };
+      wait_levels(0);  // the level producer has reached this step
       float oacc[64];
 #pragma unroll
       for (int i = 0; i < 64; ++i) oacc[i] = 0.f;
@@ -680,7 +737,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         const float lam_h = lam_c;
         // the next level's lambda loads while this level is read
         if (rem != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(rem) - 1));
-        const float w = lam_h * ex2((cs_prev + __shfl_sync(0xffffffffu, dlev, l)) * kLog2e);
+        wait_levels((uint32_t)(l + 1));
+        const float w = lam_h * ex2((cs_prev + dl[l]) * kLog2e);
         const int b = l & 1;
         wait_bar_w(c, B_LVL_DONE0 + b, ne[b] & 1);
         __syncwarp();
@@ -701,7 +759,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         ++ne[b];
       }
 
-      // output = intra (PV) + inter, staged in X for a TMA store
+      // output = intra (PV) + inter, bf16, staged after this step's merge
       if (it == n) wait_bar_w(c, B_O_DONE, (it - 1) & 1);
       __syncwarp();
       tc_fence_after();
@@ -712,21 +770,23 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         tmem_ld32(tRp + 32 * c32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 32; ++i) oacc[32 * c32 + i] += v[i];
+        for (int i = 0; i < 16; ++i)
+          opk[16 * c32 + i] = pack_bf16x2(oacc[32 * c32 + 2 * i] + v[2 * i], oacc[32 * c32 + 2 * i + 1] + v[2 * i + 1]);
       }
       // the region is free once every thread is past this point; the next
       // tile's VT_READY arrival (after later named barriers) hands it back
       tc_fence_before();
-      stage(oacc);
       if (leader) mbar_arrive(c.bars + B_LVLD_FREE);
-      fpos += __popc(jp);
+      stage_words(opk);
     }
 
     if (it < n && (j & 1)) {
       // odd j: F_j = S_j + the decayed states of tiles (j - 2^cto(j), j), from
-      // the producer's pieces in the F ring: the tile's own raw state (weight
-      // 1), then published nodes or raw states, most recent first.  Merged at
-      // the end of the step, when its inputs are long published.
+      // the piece producer in K and V: the tile's own raw state (weight 1),
+      // then published nodes or raw states, most recent first.  Merged after
+      // the back half, when its inputs are long published; K and V go to the
+      // next tile as soon as the last piece is read, and the result is staged
+      // in X while the output's store may still be reading it.
       const float* pdesc = reinterpret_cast<const float*>(s + kOffNode + 128);
       // the leader decides whether another piece follows, so every warp runs
       // the same number of named barriers (alternating words)
@@ -737,13 +797,13 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       for (int i = 0; i < 64; ++i) acc[i] = 0.f;
       float r_end = 0.f;
       for (int idx = 0; idx < max_pieces; ++idx) {
-        const int fs = fpos & 1;
-        wait_bar_w(c, B_F_FULL0 + fs, (fpos >> 1) & 1);
-        const float* d = pdesc + 4 * fs;
+        const int b = idx & 1;
+        wait_bar_w(c, B_PC_FULL0 + b, npc[b] & 1);
+        const float* d = pdesc + 4 * b;
         r_end = d[1];
         // decay from the piece's end to the end of tile j
         const float sc = d[3] != 0.f ? 1.f : ex2((cs_end + d[0]) * kLog2e);
-        const unsigned char* src = s + (fs ? kOffF1 : kOffF0) + hf * kHalf + row * 128;
+        const unsigned char* src = s + (b ? kOffV : kOffK) + hf * kHalf + row * 128;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const uint4 v = *reinterpret_cast<const uint4*>(src + ((c8 ^ (row & 7)) << 4));
@@ -755,14 +815,19 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
             acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
           }
         }
-        if (leader) more_s[idx & 1] = (d[3] != 0.f || d[2] == 0.f) && !*c.abort_s ? 1 : 0;
+        if (leader)
+          more_s[idx & 1] = (d[3] != 0.f || d[2] == 0.f) && !*c.abort_s && idx + 1 < max_pieces ? 1 : 0;
         __syncwarp();
         named_bar_sync(1, kEpi);  // every row of the piece is read
-        if (leader) mbar_arrive(c.bars + B_F_FREE0 + fs);
-        ++fpos;
+        if (leader) mbar_arrive(c.bars + B_PC_FREE0 + b);
+        ++npc[b];
         if (!more_s[idx & 1]) break;
       }
-      if (leader) p.G[(size_t)bh * p.Nt + j] = cs_end + r_end;
+      if (leader) {
+        mbar_arrive(c.bars + B_KV_REL);
+        p.G[(size_t)bh * p.Nt + j] = cs_end + r_end;
+        gpub_s[0] = cs_end + r_end;
+      }
       stage(acc);
     }
 
@@ -784,8 +849,11 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
   const int n = tiles_of_cta(total);
   const unsigned char* x = c.base + kOffX;
   uint32_t xs = 0;
+  const volatile float* gpub_s = reinterpret_cast<const volatile float*>(c.base + kOffMisc + 20);
+  float g = 0.f;
   auto store = [&](const CUtensorMap* map, int row0) {
     wait_bar(c, B_X_STAGED, xs & 1);
+    g = *gpub_s;
     fence_proxy_async_shared();
     tma_store_2d(map, x, 0, row0);
     tma_store_2d(map, x + kHalf, 64, row0);
@@ -794,20 +862,22 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
     mbar_arrive(c.bars + B_X_FREE);
     ++xs;
   };
-  // the node's bytes (async proxy) and its log-decay total (written by the
-  // epilogue before X_STAGED) are ordered before the release of the flag
-  auto publish = [&](uint64_t* flags, size_t node) {
+  // the node's bytes (async proxy) are complete and ordered before the
+  // release of its word, which carries the log-decay total the epilogue left
+  // in shared memory before X_STAGED (read before X is handed back)
+  auto publish = [&](uint64_t* flags, size_t node, float g) {
     bulk_wait0();
     fence_proxy_async_global();
-    st_release_u64(flags + node, p.token);
+    st_release_u64(flags + node, ((uint64_t)p.token << 32) | __float_as_uint(g));
   };
+
   for (int it = 0; it <= n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     const int bh = u % p.BH, j = u / p.BH;
     const size_t node_j = (size_t)bh * p.Nt + j;
     if (it < n) {
       store(j & 1 ? tr : tf, (int)(node_j * kD));
-      publish(j & 1 ? p.rflags : p.flags, node_j);
+      publish(j & 1 ? p.rflags : p.flags, node_j, g);
     }
     if (it >= 1) {
       const int up = u - gridDim.x;
@@ -815,7 +885,7 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
     }
     if (it < n && (j & 1)) {
       store(tf, (int)(node_j * kD));
-      publish(p.flags, node_j);
+      publish(p.flags, node_j, g);
     }
   }
   bulk_wait0();
@@ -860,8 +930,10 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_nodes(c, &tf, &tr);
+    if (lane == 0) producer_levels(c, &tf);
     else if (lane == 1) producer_kvq(c, &tq, &tk, &tv);
+  } else if (warp == kPieceWarp) {
+    if (lane == 0) producer_pieces(c, &tf, &tr);
   } else if (warp == 1) {
     if (lane == 0) mma_issuer(c, tmem);
   } else if (warp == kPubWarp) {
@@ -904,7 +976,7 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
 // ------------------------------------------------------------------ host side
 struct TcPlan {
   int Nt;
-  size_t off_F, off_R, off_G, off_Gt, off_flags, off_rflags, total;
+  size_t off_F, off_R, off_G, off_flags, off_rflags, total;
 };
 
 TcPlan tc_plan(const ll_shape& s) {
@@ -915,7 +987,6 @@ TcPlan tc_plan(const ll_shape& s) {
   p.off_F = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
   p.off_R = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
   p.off_G = off;      off = align_up(off + nodes * 4, 256);
-  p.off_Gt = off;     off = align_up(off + nodes * 4, 256);
   p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
   p.off_rflags = off; off = align_up(off + nodes * 8, 256);
   p.total = off;
@@ -949,13 +1020,13 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
-uint64_t next_token() {
-  static std::atomic<uint64_t> counter{0x5eed};
-  uint64_t x = counter.fetch_add(1) + 0x9E3779B97F4A7C15ull;
-  x = (x ^ (x >> 30)) * 0xBF58476D1CE4E5B9ull;
-  x = (x ^ (x >> 27)) * 0x94D049BB133111EBull;
-  x ^= x >> 31;
-  return x | 1ull;
+// Per-call token of the publication words: a process-wide counter, so two
+// calls on one workspace never share it (0 is skipped).
+uint32_t next_token() {
+  static std::atomic<uint32_t> counter{0x5eed};
+  uint32_t t = counter.fetch_add(1);
+  if (t == 0) t = counter.fetch_add(1);
+  return t;
 }
 
 }  // namespace
@@ -992,7 +1063,6 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.F = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_F);
   p.G = reinterpret_cast<float*>(ws + plan.off_G);
   p.flags = reinterpret_cast<uint64_t*>(ws + plan.off_flags);
-  p.Gt = reinterpret_cast<float*>(ws + plan.off_Gt);
   p.rflags = reinterpret_cast<uint64_t*>(ws + plan.off_rflags);
   p.abort_word = p.flags + (size_t)BH * plan.Nt;
   p.token = next_token();
