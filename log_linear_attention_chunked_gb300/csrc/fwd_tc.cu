@@ -7,9 +7,10 @@
 //   Fenwick F_j = S_j + sum_{m < cto(j)} exp(dec_m) F_{j-2^m}   (cto = trailing ones)
 //           published to global memory (bf16) with its log-decay total G_j
 //   intra   P = (Q K^T) . exp(cs_t - cs_s) . lam_t[bitlen(t^s)] (s <= t), O = P V
-//   inter   for each set bit h of j: D_h = Q F_e^T with
-//           e = (j with bits 0..h cleared) + 2^h - 1, and
-//           O += lam_t[8 + h] exp(cs_t + sum of G over the lower set bits) D_h
+//   inter   for each set bit h of j, with e = (j with bits 0..h cleared) +
+//           2^h - 1:  O += Q'_h F_e^T,  Q'_h[t] = lam_t[8 + h] exp(cs_t + sum
+//           of G over the lower set bits) Q[t]  (the row weights go on Q, so
+//           the tensor cores accumulate every level onto the output)
 // ("Log-Linear Attention" study note §3-4/§3-5; chunk-wise scan of the
 // gist.science (zh) summary §2.3; the per-level contractions are summed in
 // one accumulator per tile, the pages' "level fusion".)
@@ -76,9 +77,10 @@ constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 
 // TMEM columns: two 128-column regions that hold the chunk state and then the
-// intra output PV of alternating tiles; the scores (then P, bf16, in their
-// first 64 columns, then odd-numbered level products); level products.
-constexpr uint32_t kTmR0 = 0, kTmS = 256, kTmLvl = 384;
+// output (PV, then + the inter-tile levels) of alternating tiles; the scores
+// (then P, bf16, in their first 64 columns); two 64-column buffers of
+// level-weighted Q (bf16), the A operand of the level products.
+constexpr uint32_t kTmR0 = 0, kTmS = 256, kTmQP = 384;
 
 // shared-memory layout (offsets from the dynamic base, which must be 1024-aligned)
 constexpr uint32_t kOffQ0 = 0;
@@ -105,8 +107,8 @@ constexpr uint32_t kOffBars = kOffNode + 192;            // mbarriers
 // tcgen05.commit, or one elected thread)
 enum Bar : int {
   B_K_FULL, B_V_FULL, B_Q_FULL0, B_Q_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_K_FREE, B_V_FREE,
-  B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_LVL_DONE0, B_LVL_DONE1, B_LVL_FREE0,
-  B_LVL_FREE1, B_O_DONE, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD_FREE, B_PC_FULL0, B_PC_FULL1,
+  B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_QP_FULL0, B_QP_FULL1, B_QP_FREE0,
+  B_QP_FREE1, B_O_READY, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD_FREE, B_PC_FULL0, B_PC_FULL1,
   B_PC_FREE0, B_PC_FREE1, B_KV_REL, kNumBars
 };
 constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8;
@@ -416,26 +418,25 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
                  sV = smem_u32(c.base + kOffV), sX = smem_u32(c.base + kOffX), sF0 = smem_u32(c.base + kOffF0),
                  sF1 = smem_u32(c.base + kOffF1);
   constexpr uint32_t id_state = idesc_bf16(128, 128, true, true);   // Vt^T (MN) x K (MN)
-  constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);    // Q (K) x K|F (K)
+  constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);    // Q (K) x K (K); Q' (TMEM) x F (K)
   constexpr uint32_t id_pv = idesc_bf16(128, 128, false, true);     // P (TMEM) x V (MN)
-  uint32_t fcnt = 0, nb[2] = {0, 0};
+  uint32_t fcnt = 0, qpc = 0;
 
-  // level l of the previous tile, D[t][dv] = Q[t] . F[dv], into buffer l & 1
-  // (even: the level region; odd: the scores' region, free once PV has read P)
-  auto issue_level = [&](uint32_t sQ, int l) {
-    const int b = l & 1;
+  // one inter-tile level of the previous tile, accumulated onto its output:
+  // D[t][dv] += Q'[t] . F[dv], Q' = the level-weighted Q from the epilogue (TMEM)
+  auto issue_level = [&](uint32_t d) {
+    const int b = qpc & 1;
     const int fs = fcnt & 1;
     wait_bar(c, B_F_FULL0 + fs, (fcnt >> 1) & 1);
-    if (nb[b] > 0) wait_bar(c, B_LVL_FREE0 + b, (nb[b] - 1) & 1);
+    wait_bar(c, B_QP_FULL0 + b, (qpc >> 1) & 1);
     tc_fence_after();
     const uint32_t sF = fs ? sF1 : sF0;
-    const uint32_t d = tmem + (b ? kTmS : kTmLvl);
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16(d, desc_k(sQ, kk), desc_k(sF, kk), id_qk, kk > 0);
-    umma_commit(c.bars + B_LVL_DONE0 + b);
+    for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(d, tmem + kTmQP + 64 * b + kk * 8, desc_k(sF, kk), id_qk, 1);
+    umma_commit(c.bars + B_QP_FREE0 + b);
     umma_commit(c.bars + B_F_FREE0 + fs);
     ++fcnt;
-    ++nb[b];
+    ++qpc;
   };
 
   int jp = 0;
@@ -443,7 +444,6 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
     const int u = blockIdx.x + it * gridDim.x;
     const int j = it < n ? u / p.BH : 0;
     const int nlev_p = it >= 1 ? __popc(jp) : 0;
-    const uint32_t sQp = (it - 1) & 1 ? sQ1 : sQ0;
     const uint32_t tR = tmem + kTmR0 + (it & 1) * 128;
     if (it < n) {
       // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
@@ -468,12 +468,14 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(tR, tmem + kTmS + kk * 8, desc_mn(sV, kk), id_pv, kk > 0);
-      umma_commit(c.bars + B_O_DONE);
       umma_commit(c.bars + B_V_FREE);
     }
-    // the previous tile's levels after PV, which never waits on another CTA
+    // the previous tile's levels after PV, which never waits on another CTA;
+    // then its output (PV + levels) is complete, and its Q has been read
     if (it >= 1) {
-      for (int l = 0; l < nlev_p; ++l) issue_level(sQp, l);
+      const uint32_t tRp = tmem + kTmR0 + ((it - 1) & 1) * 128;
+      for (int l = 0; l < nlev_p; ++l) issue_level(tRp);
+      umma_commit(c.bars + B_O_READY);
       umma_commit(c.bars + B_Q_FREE0 + ((it - 1) & 1));
     }
     jp = j;
@@ -500,7 +502,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
   volatile float* gpub_s = reinterpret_cast<volatile float*>(s + kOffMisc + 20);  // log-decay total to publish
   unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;  // this thread's 128 B of a staged tile
-  uint32_t ne[2] = {0, 0};   // level products consumed per buffer
+  uint32_t qpc = 0;          // level-weighted Q tiles written (two TMEM buffers)
   uint32_t npc[2] = {0, 0};  // merge pieces consumed per buffer (K, V)
   uint32_t xs = 0;          // X stagings so far
 
@@ -698,7 +700,6 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         }
       }
       tmem_st_wait();
-      if (it > 0) wait_bar_w(c, B_O_DONE, (it - 1) & 1);  // PV of the previous tile (read in the back half)
       tc_fence_before();  // orders the state and score reads and the P writes before the PV product
       __syncwarp();
       named_bar_sync(1, kEpi);
@@ -728,39 +729,48 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         }
       };
       wait_levels(0);  // the level producer has reached this step
-      float oacc[64];
+      // this thread's half row of the previous tile's Q (bf16, from its smem tile)
+      uint4 qv[8];
+      {
+        const unsigned char* qrow = s + ((it - 1) & 1 ? kOffQ1 : kOffQ0) + hf * kHalf + row * 128;
 #pragma unroll
-      for (int i = 0; i < 64; ++i) oacc[i] = 0.f;
+        for (int c8 = 0; c8 < 8; ++c8) qv[c8] = *reinterpret_cast<const uint4*>(qrow + ((c8 ^ (row & 7)) << 4));
+      }
+      // inter-tile levels: Q'_l = lam_t[8 + h] exp(cs_t + D_l) Q_t goes to TMEM
+      // as the A operand of a product the MMA accumulates onto the output
       int l = 0;
       for (int rem = jp; rem != 0; ++l) {
         rem &= rem - 1;
         const float lam_h = lam_c;
-        // the next level's lambda loads while this level is read
+        // the next level's lambda loads while this level is written
         if (rem != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(rem) - 1));
         wait_levels((uint32_t)(l + 1));
         const float w = lam_h * ex2((cs_prev + dl[l]) * kLog2e);
-        const int b = l & 1;
-        wait_bar_w(c, B_LVL_DONE0 + b, ne[b] & 1);
+        uint32_t wq[32];
+#pragma unroll
+        for (int c8 = 0; c8 < 8; ++c8) {
+          const uint32_t* q4 = reinterpret_cast<const uint32_t*>(&qv[c8]);
+#pragma unroll
+          for (int i = 0; i < 4; ++i) {
+            const float2 f = unpack_bf16x2(q4[i]);
+            wq[4 * c8 + i] = pack_bf16x2(w * f.x, w * f.y);
+          }
+        }
+        const int b = qpc & 1;
+        if (qpc >= 2) wait_bar_w(c, B_QP_FREE0 + b, ((qpc - 2) >> 1) & 1);  // its previous product is done
         __syncwarp();
         tc_fence_after();
-        const uint32_t tb = tl + (b ? kTmS : kTmLvl) + 64 * hf;
-#pragma unroll
-        for (int c32 = 0; c32 < 2; ++c32) {
-          float v[32];
-          tmem_ld32(tb + 32 * c32, v);
-          tmem_ld_wait();
-#pragma unroll
-          for (int i = 0; i < 32; ++i) oacc[32 * c32 + i] = fmaf(w, v[i], oacc[32 * c32 + i]);
-        }
+        tmem_st32(tl + kTmQP + 64 * b + 32 * hf, wq);
+        tmem_st_wait();
         tc_fence_before();
         __syncwarp();
         named_bar_sync(1, kEpi);
-        if (leader) mbar_arrive(c.bars + B_LVL_FREE0 + b);
-        ++ne[b];
+        if (leader) mbar_arrive(c.bars + B_QP_FULL0 + b);
+        ++qpc;
       }
 
-      // output = intra (PV) + inter, bf16, staged after this step's merge
-      if (it == n) wait_bar_w(c, B_O_DONE, (it - 1) & 1);
+      // output = PV + levels, accumulated in TMEM; bf16, staged after this step's merge
+      wait_bar_w(c, B_O_READY, (it - 1) & 1);
       __syncwarp();
       tc_fence_after();
       const uint32_t tRp = tl + kTmR0 + ((it - 1) & 1) * 128 + 64 * hf;
@@ -770,8 +780,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         tmem_ld32(tRp + 32 * c32, v);
         tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i)
-          opk[16 * c32 + i] = pack_bf16x2(oacc[32 * c32 + 2 * i] + v[2 * i], oacc[32 * c32 + 2 * i + 1] + v[2 * i + 1]);
+        for (int i = 0; i < 16; ++i) opk[16 * c32 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
       }
       // the region is free once every thread is past this point; the next
       // tile's VT_READY arrival (after later named barriers) hands it back
