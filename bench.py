@@ -198,11 +198,16 @@ def _oracle_worker(job):
         return float(len(job))
     from oracle import decode
     S, q, k, v, la, lam = _W["x"]
-    n = job
     t0 = cfg["T"]
     ne = [((t0 >> i) & 1) == 1 for i in range(S.shape[0])]
-    decode.decode_steps(S, ne, t0, q[:n], k[:n], v[:n], la[:n], lam[:n])
-    return n / cfg["H"]  # one (b, h) step is 1/H of a token of a batch row
+    # `job` decode steps, cycling over the drawn step inputs (each pass
+    # restarts from the stored states at position T)
+    left = job
+    while left > 0:
+        m = min(left, q.shape[0])
+        decode.decode_steps(S, ne, t0, q[:m], k[:m], v[:m], la[:m], lam[:m])
+        left -= m
+    return job / cfg["H"]  # one (b, h) step is 1/H of a token of a batch row
 
 
 def oracle_pool(cores: int, cfg: dict, tag: str = "oracle"):
@@ -218,7 +223,7 @@ def oracle_jobs(cfg, cores, size, seed):
     rng = np.random.default_rng(seed)
     if cfg["kind"] in ("mamba2", "gdn"):
         return [sorted(int(x) for x in rng.integers(0, cfg["T"], size)) for _ in range(cores)]
-    return [min(cfg["steps"], size) for _ in range(cores)]
+    return [size for _ in range(cores)]
 
 
 def oracle_sample(pool, cfg, cores, size, seed=0):
@@ -233,10 +238,9 @@ def oracle_sample(pool, cfg, cores, size, seed=0):
 def calibrate(pool, cfg, cores, budget_s):
     """Job size so that one sample takes about `budget_s` seconds of wall time."""
     small = 16
-    cap = cfg.get("steps", 256) if cfg["kind"] == "decode" else 10 ** 6
     oracle_sample(pool, cfg, cores, 1, seed=998)  # workers finish their set-up
     _, n, wall = oracle_sample(pool, cfg, cores, small, seed=999)
-    return int(min(cap, max(1, budget_s / (wall / small))))
+    return int(min(10 ** 6, max(1, budget_s / (wall / small))))
 
 
 def sample_desc(cfg, size):

@@ -103,3 +103,39 @@ def test_decode_long_prefix_sampled(B):
 
 
 W_DECODE = synth.WORKLOADS["decode_b64_t64k"]
+
+
+def test_decode_full_batch_sampled(B):
+    """The benchmark's decode launch: 64 x 32 heads, 17 level slots, position
+    65536 onward.  The states of the non-empty levels are drawn at random (a
+    65536-token prefix for all 2048 heads would take the float64 oracle
+    hours); 8 steps run on the GPU and sampled heads are checked against the
+    oracle's step recurrence started from the same states."""
+    from oracle import decode
+    dev = torch.device("cuda")
+    cfg = dict(W_DECODE)
+    Bn, H, d, Ls, t0, n = cfg["B"], cfg["H"], cfg["dk"], cfg["Ls"], cfg["T"], 8
+    ne = [((t0 >> i) & 1) == 1 for i in range(Ls)]
+    gen = torch.Generator(device=dev)
+    gen.manual_seed(5)
+    st = torch.randn(Bn, H, Ls, d, d, device=dev, generator=gen) * 0.05
+    keep = torch.tensor(ne, device=dev)
+    st *= keep[None, None, :, None, None].float()
+    sc = keep.float().expand(Bn, H, Ls).contiguous()
+    pairs = [(0, 0), (13, 7), (31, 16), (63, 31)]
+    S0 = {pr: st[pr[0], pr[1]].double().cpu().numpy() for pr in pairs}
+    dec = synth.make_decode_inputs(cfg, device="cpu", steps=n)
+    g = {x: dec[x].to(dev) for x in ("q", "k", "v", "log_alpha", "lam")}
+    outs = []
+    for i in range(n):
+        t = torch.full((Bn,), t0 + i, dtype=torch.int64, device=dev)
+        outs.append(B.ll_attn_decode_step(t, g["q"][i], g["k"][i], g["v"][i], g["log_alpha"][i], g["lam"][i],
+                                          st, sc).float())
+    assert B.ll_last_device_error() == 0
+    out = torch.stack(outs, 0).cpu().numpy()  # [n, B, H, d]
+    for b, h in pairs:
+        f = {x: synth.to_f64(dec[x][:, b, h]) for x in ("q", "k", "v", "log_alpha", "lam")}
+        ref, S, nef = decode.decode_steps(S0[(b, h)], ne, t0, f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+        assert rel_err(out[:, b, h][None, None], ref[None, None]) <= TOL_BF16, (b, h)
+        true = (st[b, h] * sc[b, h][:, None, None]).double().cpu().numpy()
+        assert rel_err(true[nef][None, None], S[nef][None, None]) <= TOL_BF16, (b, h)
