@@ -61,6 +61,15 @@ def test_shapes(B, io, T, d, chunk):
     assert rel_err(_run(B, inp, chunk), _oracle(inp)) <= tol
 
 
+@pytest.mark.parametrize("T,io", [(2048, "f32"), (4160, "f32"), (8192, "f32"), (8192, "bf16")])
+def test_d128_chunk64_heights(B, T, io):
+    """d = 128 with 64-token chunks takes the register-tiled scan: up to eight
+    heights (T = 8192), and a chunk count that is not a power of two."""
+    inp = synth.make_inputs(_cfg(T, io=io), tag=f"gh{T}")
+    tol = TOL_GDN_F32 if io == "f32" else TOL_BF16
+    assert rel_err(_run(B, inp, 64), _oracle(inp)) <= tol
+
+
 @pytest.mark.parametrize("la_mode,lam_mode", [("zero", "softplus"), ("slow", "const"), ("slow", "onehot")])
 def test_decay_lambda_variants(B, la_mode, lam_mode):
     inp = synth.make_inputs(_cfg(1024, d=64, io="f32"), la_mode=la_mode, lam_mode=lam_mode, lam_level=9,
