@@ -68,7 +68,7 @@ constexpr int kSo = 17;    // output partials, [token][row]
 constexpr int kMaxHeights = 8;
 
 __host__ __device__ constexpr size_t smem_floats(int nh) {
-  return (size_t)nh * kR * kSx + 3 * kCe * kSx + 4 * kR * kSp1 + 4 * kR * kSp2 + kR * kSy + (size_t)nh * kCe;
+  return (size_t)nh * kR * kSx + 3 * kCe * kSx + 4 * kR * kSp1 + 4 * kR * kSp2 + kR * kSy + (size_t)2 * nh * kCe;
 }
 static_assert(4 * kCe * kSo <= 4 * kR * kSp1, "output partials alias the Y partials");
 
@@ -341,9 +341,11 @@ __global__ void __launch_bounds__(kThreads) gdn_scan_kernel(const float* __restr
 //            kept in registers until the chunk's output is written;
 //   phase 2  X_h <- gamma X_h - Y Kt: thread tile 4 rows x 8 columns over a
 //            quarter of the chunk's tokens, partials reduced in shared memory.
+// Phase 2 of one height and phase 1 of the next share a barrier interval.
 // Tiles are staged by cp.async into rows padded to 132 floats, so the 16-byte
 // loads of a warp fall on distinct banks.  The next chunk's W and Q' stream in
-// while phase 2 of the last height runs, its Kt during the reductions.
+// once phase 1 of the last height is done, its Kt once phase 2 is; Kt is
+// waited for only before the next chunk's first phase 2.
 namespace fast {
 using sm100::smem_u32;
 using sm100::bulk_prefetch_l2;
@@ -351,8 +353,12 @@ using sm100::bulk_prefetch_l2;
 __device__ __forceinline__ void cp_async16(float* dst, const float* src) {
   asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
 }
+__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
+  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
+}
 __device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
 __device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
+__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
 
 // 64 rows x 128 floats (contiguous in global) into a padded shared tile.
 __device__ __forceinline__ void stage_tile(float* dst, const float* src, int tid) {
@@ -380,160 +386,212 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan128_kernel(
   float* P1 = Ksm + kCe * kSx;        // [4][16][kSp1]; at the chunk end [4][64][kSo]
   float* P2 = P1 + 4 * kR * kSp1;     // [4][16][kSp2]
   float* Ysm = P2 + 4 * kR * kSp2;    // [16][kSy]
-  float* lamc = Ysm + kR * kSy;       // [nh][64]
+  float* lamc = Ysm + kR * kSy;       // [2][nh][64], by chunk parity
 
   const int ks = tid >> 6;            // split-K quarter
   const int u = tid & 63;
   const int rg = u & 3;               // rows rg + 4a
   const int cg = u >> 2;              // phase 1: tokens cg + 16j; phase 2: columns 4cg.., 64 + 4cg..
 
+  float oc[4][4];   // lambda-weighted Pq partials of this chunk
+  float gam = 1.f;
+
+  auto phase1 = [&](int h, const float* lamh) {
+    const float* Xh = X + h * kR * kSx;
+    float y[4][4], p[4][4];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int j = 0; j < 4; ++j) y[a][j] = p[a][j] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 8; ++s) {
+      const int f = ks * 32 + 4 * s;
+      float4 xa[4], wa[4], qa[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) xa[a] = *reinterpret_cast<const float4*>(Xh + (rg + 4 * a) * kSx + f);
+#pragma unroll
+      for (int j = 0; j < 4; ++j) {
+        wa[j] = *reinterpret_cast<const float4*>(Wsm + (cg + 16 * j) * kSx + f);
+        qa[j] = *reinterpret_cast<const float4*>(Qsm + (cg + 16 * j) * kSx + f);
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) {
+          y[a][j] = fmaf(xa[a].x, wa[j].x, y[a][j]);
+          y[a][j] = fmaf(xa[a].y, wa[j].y, y[a][j]);
+          y[a][j] = fmaf(xa[a].z, wa[j].z, y[a][j]);
+          y[a][j] = fmaf(xa[a].w, wa[j].w, y[a][j]);
+          p[a][j] = fmaf(xa[a].x, qa[j].x, p[a][j]);
+          p[a][j] = fmaf(xa[a].y, qa[j].y, p[a][j]);
+          p[a][j] = fmaf(xa[a].z, qa[j].z, p[a][j]);
+          p[a][j] = fmaf(xa[a].w, qa[j].w, p[a][j]);
+        }
+    }
+#pragma unroll
+    for (int j = 0; j < 4; ++j) {
+      const float lj = lamh[cg + 16 * j];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        P1[(ks * kR + rg + 4 * a) * kSp1 + cg + 16 * j] = y[a][j];
+        oc[a][j] = fmaf(lj, p[a][j], oc[a][j]);
+      }
+    }
+  };
+  auto reduce1 = [&]() {  // Y = sum of the four partials
+    const int r = tid >> 4, i4 = tid & 15;
+    float4 acc = *reinterpret_cast<const float4*>(P1 + r * kSp1 + 4 * i4);
+#pragma unroll
+    for (int q = 1; q < 4; ++q) {
+      const float4 t = *reinterpret_cast<const float4*>(P1 + (q * kR + r) * kSp1 + 4 * i4);
+      acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+    }
+    *reinterpret_cast<float4*>(Ysm + r * kSy + 4 * i4) = acc;
+  };
+  auto phase2 = [&]() {
+    float acc[4][8];
+#pragma unroll
+    for (int a = 0; a < 4; ++a)
+#pragma unroll
+      for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+#pragma unroll
+    for (int s = 0; s < 4; ++s) {
+      const int i = ks * 16 + 4 * s;
+      float4 ya[4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a) ya[a] = *reinterpret_cast<const float4*>(Ysm + (rg + 4 * a) * kSy + i);
+#pragma unroll
+      for (int t = 0; t < 4; ++t) {
+        const float4 k0 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 4 * cg);
+        const float4 k1 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 64 + 4 * cg);
+#pragma unroll
+        for (int a = 0; a < 4; ++a) {
+          const float yv = t == 0 ? ya[a].x : t == 1 ? ya[a].y : t == 2 ? ya[a].z : ya[a].w;
+          acc[a][0] = fmaf(yv, k0.x, acc[a][0]);
+          acc[a][1] = fmaf(yv, k0.y, acc[a][1]);
+          acc[a][2] = fmaf(yv, k0.z, acc[a][2]);
+          acc[a][3] = fmaf(yv, k0.w, acc[a][3]);
+          acc[a][4] = fmaf(yv, k1.x, acc[a][4]);
+          acc[a][5] = fmaf(yv, k1.y, acc[a][5]);
+          acc[a][6] = fmaf(yv, k1.z, acc[a][6]);
+          acc[a][7] = fmaf(yv, k1.w, acc[a][7]);
+        }
+      }
+    }
+#pragma unroll
+    for (int a = 0; a < 4; ++a) {
+      float* dst = P2 + (ks * kR + rg + 4 * a) * kSp2;
+      *reinterpret_cast<float4*>(dst + 4 * cg) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+      *reinterpret_cast<float4*>(dst + 64 + 4 * cg) = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+    }
+  };
+  auto reduce2 = [&](int h) {  // X_h <- gamma X_h - sum of the partials (this thread's 2 x 4 elements)
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int e = tid + m * kThreads;
+      const int r = e >> 5, f4 = e & 31;
+      float* xp = X + h * kR * kSx + r * kSx + 4 * f4;
+      float4 xv = *reinterpret_cast<const float4*>(xp);
+      xv.x *= gam; xv.y *= gam; xv.z *= gam; xv.w *= gam;
+#pragma unroll
+      for (int q = 0; q < 4; ++q) {
+        const float4 t = *reinterpret_cast<const float4*>(P2 + (q * kR + r) * kSp2 + 4 * f4);
+        xv.x -= t.x; xv.y -= t.y; xv.z -= t.z; xv.w -= t.w;
+      }
+      *reinterpret_cast<float4*>(xp) = xv;
+    }
+  };
+  // lambda of the levels above the chunk for chunk c1 (zero where the height is empty)
+  auto stage_lam = [&](int c1) {
+    float* dst = lamc + (c1 & 1) * nh * kCe;
+    const size_t rowc = bh * T + (size_t)c1 * kCe;
+    for (int x = tid; x < nh * kCe; x += kThreads) {
+      const int h = x >> 6, i = x & 63;
+      if (((c1 >> h) & 1) && lc + 1 + h < L) cp_async4(dst + x, lam + (rowc + i) * L + lc + 1 + h);
+      else dst[x] = 0.f;
+    }
+  };
+
   for (int c = 0; c < N; ++c) {
     const size_t row0 = bh * T + (size_t)c * kCe;
-    const float gam = expf(loggam[bh * N + c]);
-    // this thread's four output elements: token e >> 4, row e & 15
-    float oa[4];
+    const bool more = c + 1 < N;
+    gam = expf(loggam[bh * N + c]);
+    float oa[4];  // this thread's four intra outputs: token e >> 4, row e & 15
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int e = tid + m * kThreads;
       oa[m] = Oacc[(row0 + (e >> 4)) * dv + r0 + (e & 15)];
     }
-    float oc[4][4];
 #pragma unroll
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int j = 0; j < 4; ++j) oc[a][j] = 0.f;
 
-    const int hlast = c ? 31 - __clz(c) : -1;
-    for (int h = 0; h <= hlast; ++h) {
-      if (!((c >> h) & 1)) continue;
-      const float* Xh = X + h * kR * kSx;
-      // ---- phase 1
-      float y[4][4], p[4][4];
-#pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int j = 0; j < 4; ++j) y[a][j] = p[a][j] = 0.f;
-#pragma unroll
-      for (int s = 0; s < 8; ++s) {
-        const int f = ks * 32 + 4 * s;
-        float4 xa[4], wa[4], qa[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) xa[a] = *reinterpret_cast<const float4*>(Xh + (rg + 4 * a) * kSx + f);
-#pragma unroll
-        for (int j = 0; j < 4; ++j) {
-          wa[j] = *reinterpret_cast<const float4*>(Wsm + (cg + 16 * j) * kSx + f);
-          qa[j] = *reinterpret_cast<const float4*>(Qsm + (cg + 16 * j) * kSx + f);
-        }
-#pragma unroll
-        for (int a = 0; a < 4; ++a)
-#pragma unroll
-          for (int j = 0; j < 4; ++j) {
-            y[a][j] = fmaf(xa[a].x, wa[j].x, y[a][j]);
-            y[a][j] = fmaf(xa[a].y, wa[j].y, y[a][j]);
-            y[a][j] = fmaf(xa[a].z, wa[j].z, y[a][j]);
-            y[a][j] = fmaf(xa[a].w, wa[j].w, y[a][j]);
-            p[a][j] = fmaf(xa[a].x, qa[j].x, p[a][j]);
-            p[a][j] = fmaf(xa[a].y, qa[j].y, p[a][j]);
-            p[a][j] = fmaf(xa[a].z, qa[j].z, p[a][j]);
-            p[a][j] = fmaf(xa[a].w, qa[j].w, p[a][j]);
-          }
-      }
-#pragma unroll
-      for (int j = 0; j < 4; ++j) {
-        const float lj = lamc[h * kCe + cg + 16 * j];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) {
-          P1[(ks * kR + rg + 4 * a) * kSp1 + cg + 16 * j] = y[a][j];
-          oc[a][j] = fmaf(lj, p[a][j], oc[a][j]);
-        }
-      }
+    int jc = 0;  // carry height cto(c)
+    while ((c >> jc) & 1) ++jc;
+    const float* Sc = Sloc + (bh * N + c) * (size_t)dv * kDk + (size_t)r0 * kDk;
+    float4 sc[2];
+    if (c > 0) {
+      const float* lamh = lamc + (c & 1) * nh * kCe;
+      int h = __ffs(c) - 1;
+      phase1(h, lamh + h * kCe);
+      cp_async_wait0();  // Kt of this chunk (and lambda)
       __syncthreads();
-      const bool last = h == hlast;
-      if (last && c + 1 < N) {  // W and Q' of the next chunk are no longer read
-        stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
-        stage_tile(Qsm, Qp + (row0 + kCe) * kDk, tid);
+      if (more) {
+        stage_lam(c + 1);
         cp_async_commit();
-      }
-      {  // Y = sum of the four partials
-        const int r = tid >> 4, i4 = tid & 15;
-        float4 acc = *reinterpret_cast<const float4*>(P1 + r * kSp1 + 4 * i4);
-#pragma unroll
-        for (int q = 1; q < 4; ++q) {
-          const float4 t = *reinterpret_cast<const float4*>(P1 + (q * kR + r) * kSp1 + 4 * i4);
-          acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+        if ((c >> (h + 1)) == 0) {
+          stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+          stage_tile(Qsm, Qp + (row0 + kCe) * kDk, tid);
+          cp_async_commit();
         }
-        *reinterpret_cast<float4*>(Ysm + r * kSy + 4 * i4) = acc;
       }
+      reduce1();
       __syncthreads();
-      // ---- phase 2
-      float acc[4][8];
+      while (true) {
+        const int rest = c >> (h + 1);
+        const int hn = rest ? h + __ffs(rest) : -1;
+        if (hn < 0 && jc < nh) {
 #pragma unroll
-      for (int a = 0; a < 4; ++a)
-#pragma unroll
-        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
-#pragma unroll
-      for (int s = 0; s < 4; ++s) {
-        const int i = ks * 16 + 4 * s;
-        float4 ya[4];
-#pragma unroll
-        for (int a = 0; a < 4; ++a) ya[a] = *reinterpret_cast<const float4*>(Ysm + (rg + 4 * a) * kSy + i);
-#pragma unroll
-        for (int t = 0; t < 4; ++t) {
-          const float4 k0 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 4 * cg);
-          const float4 k1 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 64 + 4 * cg);
-#pragma unroll
-          for (int a = 0; a < 4; ++a) {
-            const float yv = t == 0 ? ya[a].x : t == 1 ? ya[a].y : t == 2 ? ya[a].z : ya[a].w;
-            acc[a][0] = fmaf(yv, k0.x, acc[a][0]);
-            acc[a][1] = fmaf(yv, k0.y, acc[a][1]);
-            acc[a][2] = fmaf(yv, k0.z, acc[a][2]);
-            acc[a][3] = fmaf(yv, k0.w, acc[a][3]);
-            acc[a][4] = fmaf(yv, k1.x, acc[a][4]);
-            acc[a][5] = fmaf(yv, k1.y, acc[a][5]);
-            acc[a][6] = fmaf(yv, k1.z, acc[a][6]);
-            acc[a][7] = fmaf(yv, k1.w, acc[a][7]);
+          for (int m = 0; m < 2; ++m) {
+            const int e = tid + m * kThreads;
+            sc[m] = *reinterpret_cast<const float4*>(Sc + (e >> 5) * kDk + 4 * (e & 31));
           }
         }
+        phase2();
+        if (hn >= 0) phase1(hn, lamh + hn * kCe);
+        __syncthreads();
+        if (hn < 0 && more) {
+          stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
+          cp_async_commit();
+        }
+        reduce2(h);
+        if (hn < 0) break;
+        if (more && (c >> (hn + 1)) == 0) {
+          stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+          stage_tile(Qsm, Qp + (row0 + kCe) * kDk, tid);
+          cp_async_commit();
+        }
+        reduce1();
+        __syncthreads();
+        h = hn;
       }
-#pragma unroll
-      for (int a = 0; a < 4; ++a) {
-        float* dst = P2 + (ks * kR + rg + 4 * a) * kSp2;
-        *reinterpret_cast<float4*>(dst + 4 * cg) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
-        *reinterpret_cast<float4*>(dst + 64 + 4 * cg) = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
-      }
-      __syncthreads();
-      if (last && c + 1 < N) {  // Kt of the next chunk is no longer read
-        stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
-        cp_async_commit();
-      }
-      // X_h <- gamma X_h - sum of the four partials (this thread's 2 x 4 elements)
+    } else if (jc < nh) {
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int e = tid + m * kThreads;
-        const int r = e >> 5, f4 = e & 31;
-        float* xp = X + h * kR * kSx + r * kSx + 4 * f4;
-        float4 xv = *reinterpret_cast<const float4*>(xp);
-        xv.x *= gam; xv.y *= gam; xv.z *= gam; xv.w *= gam;
-#pragma unroll
-        for (int q = 0; q < 4; ++q) {
-          const float4 t = *reinterpret_cast<const float4*>(P2 + (q * kR + r) * kSp2 + 4 * f4);
-          xv.x -= t.x; xv.y -= t.y; xv.z -= t.z; xv.w -= t.w;
-        }
-        *reinterpret_cast<float4*>(xp) = xv;
+        sc[m] = *reinterpret_cast<const float4*>(Sc + (e >> 5) * kDk + 4 * (e & 31));
       }
     }
 
     // carry into height cto(c): S_c + the transported levels below it (same
-    // element ownership as the X update above, so no barrier is needed)
-    int jc = 0;
-    while ((c >> jc) & 1) ++jc;
+    // element ownership as the X update, so no barrier is needed)
     if (jc < nh) {
-      const float* Sc = Sloc + (bh * N + c) * (size_t)dv * kDk + (size_t)r0 * kDk;
 #pragma unroll
       for (int m = 0; m < 2; ++m) {
         const int e = tid + m * kThreads;
         const int r = e >> 5, f4 = e & 31;
-        float4 acc = *reinterpret_cast<const float4*>(Sc + r * kDk + 4 * f4);
+        float4 acc = sc[m];
         for (int h = 0; h < jc; ++h) {
           const float4 t = *reinterpret_cast<const float4*>(X + h * kR * kSx + r * kSx + 4 * f4);
           acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
@@ -546,25 +604,23 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan128_kernel(
     for (int a = 0; a < 4; ++a)
 #pragma unroll
       for (int j = 0; j < 4; ++j) P1[(ks * kCe + cg + 16 * j) * kSo + rg + 4 * a] = oc[a][j];
-    if (c + 1 < N) {
-      if (c == 0) {  // chunk 0 has no live level: nothing was staged yet
-        stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
-        stage_tile(Qsm, Qp + (row0 + kCe) * kDk, tid);
-        stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
-        cp_async_commit();
-      }
-      const int c1 = c + 1;
-      for (int x = tid; x < nh * kCe; x += kThreads) {
-        const int h = x >> 6, i = x & 63;
-        lamc[x] = ((c1 >> h) & 1) && lc + 1 + h < L ? lam[(row0 + kCe + i) * L + lc + 1 + h] : 0.f;
-      }
-      if (tid == 0 && c + 2 < N) {
+    if (c == 0 && more) {  // chunk 0 has no live level: nothing was staged yet
+      stage_lam(1);
+      stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+      stage_tile(Qsm, Qp + (row0 + kCe) * kDk, tid);
+      cp_async_commit();
+      stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
+      cp_async_commit();
+    }
+    if (tid == 0) {
+      if (c + 2 < N) {
         const size_t rn = row0 + 2 * kCe;
         bulk_prefetch_l2(Wg + rn * kDk, kCe * kDk * 4);
         bulk_prefetch_l2(Qp + rn * kDk, kCe * kDk * 4);
         bulk_prefetch_l2(Kt + rn * kDk, kCe * kDk * 4);
         bulk_prefetch_l2(Oacc + rn * dv, kCe * dv * 4);
       }
+      if (more) bulk_prefetch_l2(Sc + (size_t)dv * kDk, kR * kDk * 4);
     }
     __syncthreads();
 #pragma unroll
@@ -576,9 +632,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan128_kernel(
       for (int q = 0; q < 4; ++q) v += P1[(q * kCe + i) * kSo + r];
       o[(row0 + i) * dv + r0 + r] = from_f<IO>(v);
     }
-    cp_async_wait0();
+    cp_async_wait1();  // all but the next chunk's Kt
     __syncthreads();
   }
+  cp_async_wait0();
 }
 
 }  // namespace fast
