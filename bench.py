@@ -89,26 +89,34 @@ def measured_peaks():
     return 6800.0, 1900.0, 2070.0, "fallback"
 
 
-def kernel_source_hash() -> str:
+# the sources each workload's kernels are built from: a traffic figure stays
+# valid while these files are unchanged
+KERNEL_SOURCES = {
+    "mamba2": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),
+    "decode": ("decode.cu", "common.cuh"),
+    "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
+}
+
+
+def kernel_source_hash(files) -> str:
     h = hashlib.sha256()
     csrc = os.path.join(ROOT, "log_linear_attention_chunked_gb300", "csrc")
-    for f in sorted(os.listdir(csrc)):
-        if f.endswith((".cu", ".cuh")):
-            with open(os.path.join(csrc, f), "rb") as fh:
-                h.update(f.encode())
-                h.update(fh.read())
+    for f in sorted(files):
+        with open(os.path.join(csrc, f), "rb") as fh:
+            h.update(f.encode())
+            h.update(fh.read())
     return h.hexdigest()[:16]
 
 
 def ncu_traffic(workload: str):
     """DRAM bytes per launch of the dominant kernel from the committed ncu
-    summary, or None when there is none or the kernels changed since."""
+    summary, or None when there is none or its sources changed since."""
     path = os.path.join(PROFILES, f"traffic_{workload}.json")
     if not os.path.exists(path):
         return None, None
     with open(path) as f:
         t = json.load(f)
-    if t.get("source_hash") != kernel_source_hash():
+    if t.get("source_hash") != kernel_source_hash(t.get("source_files", ())):
         return None, t.get("kernel")
     return t.get("dram_bytes_per_launch"), t.get("kernel")
 
