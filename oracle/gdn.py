@@ -110,36 +110,72 @@ def gdn_recurrent(q, k, v, beta, log_alpha) -> np.ndarray:
     return out
 
 
-def gdn_recurrent_levels_A(q, k, v, beta, log_alpha, lam):
-    """Reading A as a recurrence over Fenwick level states.
+def gdn_level_step(states: dict, t: int, q, k, v, beta: float, log_alpha: float, lam) -> np.ndarray:
+    """One token of reading A over the Fenwick level states of query t.
 
-    Each step: every level state is right-multiplied by alpha_t (I - beta_t
-    k_t k_t^T); level 0 receives beta_t v_t k_t^T; o_t = sum_l lam_t[l] S^(l)
-    q_t; then the carry merges levels 0..j (j = trailing ones of t) into
-    level j + 1 by addition.  Returns (O, final states dict).
+    `states` maps level -> true state (d_v x d_k) for the non-empty levels of
+    position t (levels >= 1), each after the transition of token t - 1, and
+    is updated in place to the states of position t + 1.  Every level is
+    right-multiplied by alpha_t (I - beta_t k_t k_t^T); level 0 receives
+    beta_t v_t k_t^T; o_t = sum_l lam[l] S^(l) q_t; then the carry merges
+    levels 0..j (j = trailing ones of t) into level j + 1 by addition.
+    Returns o_t.
     """
+    dk = k.shape[0]
+    P = np.exp(log_alpha) * (np.eye(dk) - beta * np.outer(k, k))
+    for lv in list(states):
+        states[lv] = states[lv] @ P
+    states[0] = beta * np.outer(v, k)
+    o = np.zeros(v.shape[0])
+    for lv, S in states.items():
+        o += lam[lv] * (S @ q)
+    j = 0
+    while (t >> j) & 1:
+        j += 1
+    merged = states.pop(0)
+    for lv in range(1, j + 1):
+        merged = merged + states.pop(lv)
+    assert (j + 1) not in states
+    states[j + 1] = merged
+    return o
+
+
+def gdn_recurrent_levels_A(q, k, v, beta, log_alpha, lam):
+    """Reading A as a recurrence over Fenwick level states, from position 0
+    (gdn_level_step for every token).  Returns (O, final states dict)."""
     q = np.asarray(q, np.float64)
     k = np.asarray(k, np.float64)
     v = np.asarray(v, np.float64)
     lam = np.asarray(lam, np.float64)
-    alpha = np.exp(np.asarray(log_alpha, np.float64))
-    dk = k.shape[1]
-    I = np.eye(dk)
+    log_alpha = np.asarray(log_alpha, np.float64)
+    beta = np.asarray(beta, np.float64)
     states: dict = {}
     out = np.zeros((q.shape[0], v.shape[1]))
     for t in range(q.shape[0]):
-        P = alpha[t] * (I - beta[t] * np.outer(k[t], k[t]))
-        for lv in list(states):
-            states[lv] = states[lv] @ P
-        states[0] = beta[t] * np.outer(v[t], k[t])
-        for lv, S in states.items():
-            out[t] += lam[t, lv] * (S @ q[t])
-        j = 0
-        while (t >> j) & 1:
-            j += 1
-        merged = states.pop(0)
-        for lv in range(1, j + 1):
-            merged = merged + states.pop(lv)
-        assert (j + 1) not in states
-        states[j + 1] = merged
+        out[t] = gdn_level_step(states, t, q[t], k[t], v[t], float(beta[t]), float(log_alpha[t]), lam[t])
     return out, states
+
+
+def gdn_decode_steps(S0, nonempty0, t0: int, q, k, v, beta, log_alpha, lam):
+    """Run len(q) Gated DeltaNet (reading A) decode steps from position t0.
+
+    S0 [Ls, dv, dk] true states, slot i = level i + 1, nonempty0 [Ls] (must be
+    the set bits of t0); q, k [n, dk]; v [n, dv]; beta, log_alpha [n];
+    lam [n, Ls + 1] (lam[:, 0] weights the token itself).
+    Returns (o [n, dv], S [Ls, dv, dk], nonempty [Ls]) after the last step.
+    """
+    from .decode import states_from_array, states_to_array
+
+    Ls = S0.shape[0]
+    expect = [(t0 >> (lv - 1)) & 1 == 1 for lv in range(1, Ls + 1)]
+    if list(map(bool, nonempty0)) != expect:
+        raise ValueError("non-empty levels must be the set bits of t0")
+    states = states_from_array(S0, nonempty0)
+    n = q.shape[0]
+    out = np.zeros((n, np.asarray(v).shape[1]))
+    for i in range(n):
+        out[i] = gdn_level_step(states, t0 + i, np.asarray(q[i], np.float64), np.asarray(k[i], np.float64),
+                                np.asarray(v[i], np.float64), float(beta[i]), float(log_alpha[i]),
+                                np.asarray(lam[i], np.float64))
+    S, ne = states_to_array(states, Ls, np.asarray(v).shape[1], np.asarray(k).shape[1])
+    return out, S, ne

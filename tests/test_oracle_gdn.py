@@ -92,3 +92,56 @@ def test_readings_differ_in_general():
     a = gdn.gdn_forward_A(q, k, v, beta, log_alpha, lam)
     b = gdn.gdn_forward_B(q, k, v, beta, log_alpha, lam)
     assert np.abs(a - b).max() > 1e-3
+
+
+# ---- decode (Gated DeltaNet, reading A): gdn_decode_steps
+
+
+def test_decode_from_zero_equals_dense_A():
+    """Decoding every token from position 0 reproduces the dense matrix form."""
+    T, d = 45, 6
+    q, k, v, beta, log_alpha, lam = _rand(T, d, levels_needed(T) + 1, seed=11)
+    Ls = levels_needed(T)
+    o, _, _ = gdn.gdn_decode_steps(np.zeros((Ls, d, d)), np.zeros(Ls, bool), 0, q, k, v, beta, log_alpha, lam)
+    want = gdn.gdn_forward_A(q, k, v, beta, log_alpha, lam[:, :levels_needed(T)])
+    np.testing.assert_allclose(o, want, rtol=1e-10, atol=1e-12)
+
+
+@pytest.mark.parametrize("t0", [1, 8, 13, 31])
+def test_decode_handoff_at_any_position(t0):
+    """Stopping at t0 and continuing from the returned states changes nothing."""
+    T, d = 40, 5
+    Ls = levels_needed(T)
+    q, k, v, beta, log_alpha, lam = _rand(T, d, Ls + 1, seed=12 + t0)
+    z = (np.zeros((Ls, d, d)), np.zeros(Ls, bool), 0)
+    o_all, S_all, ne_all = gdn.gdn_decode_steps(*z, q, k, v, beta, log_alpha, lam)
+    o1, S1, ne1 = gdn.gdn_decode_steps(*z, q[:t0], k[:t0], v[:t0], beta[:t0], log_alpha[:t0], lam[:t0])
+    assert list(ne1) == [bool((t0 >> i) & 1) for i in range(Ls)]
+    o2, S2, ne2 = gdn.gdn_decode_steps(S1, ne1, t0, q[t0:], k[t0:], v[t0:], beta[t0:], log_alpha[t0:], lam[t0:])
+    np.testing.assert_allclose(np.concatenate([o1, o2]), o_all, rtol=1e-12, atol=1e-14)
+    np.testing.assert_allclose(S2, S_all, rtol=1e-12, atol=1e-14)
+    assert list(ne2) == list(ne_all)
+
+
+def test_decode_equal_lambda_is_single_state_rule():
+    """With every lambda equal the level states sum to the one gated-delta state."""
+    T, d = 33, 7
+    Ls = levels_needed(T)
+    q, k, v, beta, log_alpha, _ = _rand(T, d, 1, seed=13)
+    lam = np.full((T, Ls + 1), 0.6)
+    o, S, ne = gdn.gdn_decode_steps(np.zeros((Ls, d, d)), np.zeros(Ls, bool), 0, q, k, v, beta, log_alpha, lam)
+    np.testing.assert_allclose(o, 0.6 * gdn.gdn_recurrent(q, k, v, beta, log_alpha), rtol=1e-10, atol=1e-12)
+    # and the stored levels of position T sum to the textbook state at T - 1
+    Sref = np.zeros((d, d))
+    I = np.eye(d)
+    for t in range(T):
+        Sref = np.exp(log_alpha[t]) * Sref @ (I - beta[t] * np.outer(k[t], k[t])) + beta[t] * np.outer(v[t], k[t])
+    np.testing.assert_allclose(S[ne].sum(axis=0), Sref, rtol=1e-10, atol=1e-12)
+
+
+def test_decode_rejects_levels_that_are_not_the_bits_of_t0():
+    d, Ls = 4, 5
+    q, k, v, beta, log_alpha, lam = _rand(2, d, Ls + 1, seed=14)
+    ne = np.array([True, False, False, False, False])  # t0 = 6 has bits 1 and 2
+    with pytest.raises(ValueError):
+        gdn.gdn_decode_steps(np.zeros((Ls, d, d)), ne, 6, q, k, v, beta, log_alpha, lam)

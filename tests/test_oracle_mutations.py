@@ -92,3 +92,56 @@ def test_gdn_missing_beta_is_caught(monkeypatch):
     o = gdn.gdn_forward_A(one, one, np.array([[1.0], [2.0]]), np.array([0.5, 0.5]), np.zeros(2),
                           np.array([[1.0, 10.0], [1.0, 10.0]]))[:, 0]
     assert not np.allclose(o, g["reading_A"]["o"])
+
+
+# ---- Gated DeltaNet decode step (gdn.gdn_level_step)
+
+def _gdn_decode_vs_dense_ok():
+    T, d = 30, 4
+    rng = np.random.default_rng(21)
+    q = rng.standard_normal((T, d))
+    k = rng.standard_normal((T, d))
+    k /= np.linalg.norm(k, axis=1, keepdims=True)
+    v = rng.standard_normal((T, d))
+    beta = 1.0 / (1.0 + np.exp(-rng.standard_normal(T)))
+    la = -np.log1p(np.exp(rng.standard_normal(T)))
+    Ls = levels_needed(T)
+    lam = np.log1p(np.exp(rng.standard_normal((T, Ls + 1))))
+    o, _, _ = gdn.gdn_decode_steps(np.zeros((Ls, d, d)), np.zeros(Ls, bool), 0, q, k, v, beta, la, lam)
+    return np.allclose(o, gdn.gdn_forward_A(q, k, v, beta, la, lam[:, :Ls]), rtol=1e-10, atol=1e-12)
+
+
+def _step_variant(write_first=False, carry_shift=0):
+    def step(states, t, q, k, v, beta, log_alpha, lam):
+        P = np.exp(log_alpha) * (np.eye(k.shape[0]) - beta * np.outer(k, k))
+        if write_first:  # the token's own write also goes through this step's transition
+            states[0] = beta * np.outer(v, k)
+        for lv in list(states):
+            states[lv] = states[lv] @ P
+        if not write_first:
+            states[0] = beta * np.outer(v, k)
+        o = sum(lam[lv] * (S @ q) for lv, S in states.items())
+        j = 0
+        while (t >> j) & 1:
+            j += 1
+        merged = states.pop(0)
+        for lv in range(1, j + 1):
+            merged = merged + states.pop(lv, 0)
+        states[j + 1 + carry_shift] = merged + states.pop(j + 1 + carry_shift, 0)
+        return o
+    return step
+
+
+def test_gdn_decode_unmutated_variant_passes(monkeypatch):
+    monkeypatch.setattr(gdn, "gdn_level_step", _step_variant())
+    assert _gdn_decode_vs_dense_ok()
+
+
+def test_gdn_decode_write_transitioned_is_caught(monkeypatch):
+    monkeypatch.setattr(gdn, "gdn_level_step", _step_variant(write_first=True))
+    assert not _gdn_decode_vs_dense_ok()
+
+
+def test_gdn_decode_carry_to_wrong_level_is_caught(monkeypatch):
+    monkeypatch.setattr(gdn, "gdn_level_step", _step_variant(carry_shift=1))
+    assert not _gdn_decode_vs_dense_ok()
