@@ -18,6 +18,8 @@
  *                        gated delta rule itself is not on the pages (reading A:
  *                        O = (C_GDN . M^H) V, every level state follows the full
  *                        gated-delta transition).
+ *   ll_gdn_decode_step   one token of Log-Linear Gated DeltaNet decoding over the
+ *                        Fenwick level states (reading A), study note §3-5/§3-6.
  *
  * Definitions used throughout:
  *   level l(t,s) = 0 if s == t, else floor(log2(t xor s)) + 1   (0 <= s <= t);
@@ -174,6 +176,28 @@ LL_API ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dt
 LL_API ll_status ll_attn_fwd_noalloc(const ll_shape* shape, const void* q, const void* k, const void* v,
                                      const float* log_alpha, const float* lam, void* o, float* state_out,
                                      float* scale_out, void* stream);
+
+/* One decode step of log-linear Gated DeltaNet (reading A) for every (b, h):
+ * study note §3-5 (the Gated DeltaNet variant) and §3-6 (decoding with
+ * O(log T) level states); the gated delta rule itself is the standard one
+ * (the pages print no delta-rule equations).
+ *   B, H, dk, dv, Ls, io, t, q, k, v, log_alpha, lam, o: as
+ *          ll_attn_decode_step (lam[0] weights the token itself)
+ *   beta   [B,H]        float32, delta-rule write strength
+ *   states [B,H,Ls,dv,dk] float32, in/out, TRUE states (no lazy scale: the
+ *          transition is not a scalar).  Slot i holds level i+1; on entry the
+ *          non-empty slots are the set bits of t, each after the transition of
+ *          token t-1; on exit they are the set bits of t+1.
+ * Per (b,h): every non-empty level S <- alpha S (I - beta k k^T); the token
+ * is level 0, beta v k^T; o = lam_0 beta (k.q) v + sum_l lam_l S^(l) q with
+ * the transitioned states; level 0 and slots 0..j-1 (j = ctz(t+1)) merge by
+ * addition into slot j.  Every non-empty state is read and written once.
+ * Keys are expected to be L2-normalised (not checked).  A position with
+ * t+1 >= 2^Ls or t < 0 sets the device error word (LL_ERR_DEVICE) and leaves
+ * that row untouched. */
+LL_API ll_status ll_gdn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,
+                                    const void* q, const void* k, const void* v, const float* log_alpha,
+                                    const float* beta, const float* lam, float* states, void* o, void* stream);
 
 /* Bytes of workspace ll_gdn_fwd needs for `shape` (0 on invalid shape). */
 LL_API size_t ll_gdn_fwd_workspace_size(const ll_shape* shape);

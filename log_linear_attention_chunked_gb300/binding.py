@@ -24,7 +24,8 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 
 # every symbol the header declares
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
-           "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd")
+           "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
+           "ll_gdn_decode_step")
 
 
 class LLError(RuntimeError):
@@ -68,6 +69,8 @@ def lib() -> ctypes.CDLL:
     L.ll_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, fp, fp, vp, fp, fp, vp]
     L.ll_attn_decode_step.restype = i32
     L.ll_attn_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp, vp]
+    L.ll_gdn_decode_step.restype = i32
+    L.ll_gdn_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp, vp]
     L.ll_gdn_fwd_workspace_size.restype = sz
     L.ll_gdn_fwd_workspace_size.argtypes = [shp]
     L.ll_gdn_fwd.restype = i32
@@ -202,6 +205,27 @@ def ll_attn_decode_step(t, q, k, v, log_alpha, lam, states, scales, *, o=None):
     st = lib().ll_attn_decode_step(B, H, dk, dv, Ls, io, _ptr(t), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                    _ptr(lam), _ptr(states), _ptr(scales), _ptr(o), _stream(q.device))
     _check(st, "ll_attn_decode_step")
+    return o
+
+
+def ll_gdn_decode_step(t, q, k, v, log_alpha, beta, lam, states, *, o=None):
+    """One Gated DeltaNet (reading A) decode step.  t [B] int64; q, k [B,H,dk];
+    v [B,H,dv]; log_alpha, beta [B,H]; lam [B,H,Ls+1]; states [B,H,Ls,dv,dk]
+    (true states) are updated in place.  Returns o [B,H,dv]."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Ls = states.shape[2]
+    io = _io(q.dtype)
+    _need(t, "t", torch.int64)
+    for x, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(x, n, q.dtype)
+    for x, n in ((log_alpha, "log_alpha"), (beta, "beta"), (lam, "lam"), (states, "states")):
+        _need(x, n, torch.float32)
+    if o is None:
+        o = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    st = lib().ll_gdn_decode_step(B, H, dk, dv, Ls, io, _ptr(t), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                  _ptr(beta), _ptr(lam), _ptr(states), _ptr(o), _stream(q.device))
+    _check(st, "ll_gdn_decode_step")
     return o
 
 

@@ -137,6 +137,22 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
                        static_cast<cudaStream_t>(stream), ew);
 }
 
+ll_status ll_gdn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
+                             const void* k, const void* v, const float* log_alpha, const float* beta,
+                             const float* lam, float* states, void* o, void* stream) {
+  if (B < 1 || H < 1 || Ls < 1 || Ls > 62) return LL_ERR_INVALID_ARG;
+  if (io != LL_F32 && io != LL_BF16) return LL_ERR_INVALID_ARG;
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return LL_ERR_UNSUPPORTED;
+  if (!t || !q || !k || !v || !log_alpha || !beta || !lam || !states || !o) return LL_ERR_INVALID_ARG;
+  if (!aligned16(t) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+      !aligned16(beta) || !aligned16(lam) || !aligned16(states) || !aligned16(o))
+    return LL_ERR_INVALID_ARG;
+  unsigned* ew = err_word();
+  if (!ew) return LL_ERR_CUDA;
+  return gdn_decode_launch(B, H, dk, dv, Ls, io, t, q, k, v, log_alpha, beta, lam, states, o,
+                           static_cast<cudaStream_t>(stream), ew);
+}
+
 size_t ll_gdn_fwd_workspace_size(const ll_shape* s) {
   if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
   return gdn_workspace(*s);

@@ -81,6 +81,9 @@ ll_status decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const
                         const void* k, const void* v, const float* log_alpha, const float* lam, float* states,
                         float* scales, void* o, cudaStream_t stream, unsigned* err);
 
+ll_status gdn_decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
+                            const void* k, const void* v, const float* log_alpha, const float* beta,
+                            const float* lam, float* states, void* o, cudaStream_t stream, unsigned* err);
 size_t gdn_workspace(const ll_shape& s);
 ll_status gdn_launch(const FwdArgs& a);
 

@@ -36,6 +36,10 @@ WORKLOADS = {
     # prefix of 65536 tokens (forward with state export), then 256 decode steps
     "decode_b64_t64k": dict(kind="decode", B=64, H=32, T=65536, dk=128, dv=128, chunk=64, L=17,
                             Ls=17, steps=256, io="bf16", seed=4, shift=0.0),
+    # Gated DeltaNet decode: the decode launch (64 x 32 heads, 17 level slots,
+    # position 65536 on) with the Gated DeltaNet forward's distributions
+    "gdn_decode_b64_t64k": dict(kind="gdn_decode", B=64, H=32, T=65536, dk=128, dv=128, chunk=64, L=17,
+                                Ls=17, steps=256, io="bf16", seed=5, shift=2.0),
 }
 
 _MASK64 = (1 << 64) - 1
@@ -142,30 +146,41 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
 
 def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None) -> dict:
     """Per-step decode inputs: q, k [S,B,H,dk], v [S,B,H,dv] (io dtype),
-    log_alpha [S,B,H], lam [S,B,H,Ls+1] (float32); config-1 distributions."""
+    log_alpha [S,B,H], lam [S,B,H,Ls+1] (float32); config-1 distributions.
+    For kind "gdn_decode" also beta [S,B,H], with k L2-normalised,
+    beta = sigmoid(N(0,1)) and log_alpha = -softplus(N(0,1) + shift)."""
     B = cfg["B"] if B is None else B
     H = cfg["H"] if H is None else H
     S = cfg["steps"] if steps is None else steps
     dk, dv, Ls = cfg["dk"], cfg["dv"], cfg["Ls"]
     seed = cfg["seed"] + 7919
     dt = io_dtype(cfg["io"])
+    gdn = cfg["kind"] == "gdn_decode"
+    shift = float(cfg.get("shift", 0.0)) if gdn else 0.0
 
     def draw(name, s, dev):
         if name == "q":
             return _normal((S, dk), s, dev) / math.sqrt(dk)
         if name == "k":
-            return _normal((S, dk), s, dev) / math.sqrt(dk)
+            x = _normal((S, dk), s, dev)
+            if gdn:
+                return x / x.norm(dim=-1, keepdim=True)
+            return x / math.sqrt(dk)
         if name == "v":
             return _normal((S, dv), s, dev)
         if name == "log_alpha":
-            return -torch.nn.functional.softplus(_normal((S,), s, dev))
+            return -torch.nn.functional.softplus(_normal((S,), s, dev) + shift)
         if name == "lam":
             return torch.nn.functional.softplus(_normal((S, Ls + 1), s, dev))
+        if name == "beta":
+            return torch.sigmoid(_normal((S,), s, dev))
         raise KeyError(name)
 
     out = {}
     shapes = {"q": (B, H, S, dk), "k": (B, H, S, dk), "v": (B, H, S, dv),
               "log_alpha": (B, H, S), "lam": (B, H, S, Ls + 1)}
+    if gdn:
+        shapes["beta"] = (B, H, S)
     for name, shp in shapes.items():
         buf = torch.empty(shp, device=device, dtype=torch.float32)
         _fill(buf, "dec_" + name, seed, draw, B, H, device, kind=name)

@@ -100,6 +100,22 @@ def test_decode_rejects_bad_args_on_host(L):
     assert L.ll_attn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
 
 
+def test_gdn_decode_rejects_bad_args_on_host(L):
+    vp = ctypes.c_void_p
+    args = [vp(FAKE)] * 10  # t, q, k, v, log_alpha, beta, lam, states, o, stream
+    assert L.ll_gdn_decode_step(0, 1, 16, 16, 4, 0, *args) == 1            # B < 1
+    assert L.ll_gdn_decode_step(1, 1, 96, 16, 4, 0, *args) == 2            # head dim
+    assert L.ll_gdn_decode_step(1, 1, 16, 16, 63, 0, *args) == 1           # Ls > 62
+    assert L.ll_gdn_decode_step(1, 1, 16, 16, 4, 5, *args) == 1            # io
+    for i in range(9):                                                     # every null tensor
+        bad = list(args)
+        bad[i] = None
+        assert L.ll_gdn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1, i
+    bad = list(args)
+    bad[5] = vp(FAKE + 4)                                                  # misaligned beta
+    assert L.ll_gdn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
+
+
 def test_gdn_rejects_bad_args_on_host(L):
     from log_linear_attention_chunked_gb300 import binding
     vp = ctypes.c_void_p
