@@ -44,6 +44,8 @@ METRICS = {
     "mamba2": "log-linear Mamba-2 fwd tokens/s at T=16K,H=16,d=128; % of roofline",
     "decode": "log-linear Mamba-2 Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); % of HBM roofline",
     "gdn": "log-linear Gated DeltaNet fwd tokens/s (B=2, H=16, T=4096, d=128)",
+    "gdn_decode": "log-linear Gated DeltaNet Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); "
+                  "% of HBM roofline",
 }
 
 
@@ -74,6 +76,16 @@ def algorithmic_flops(cfg) -> int:
     return per_bh * cfg["B"] * cfg["H"]
 
 
+def gdn_decode_bytes(B, H, d, Ls, t) -> int:
+    """One Gated DeltaNet decode step: the popcount(t) non-empty states read
+    once; the ones above the carry written back transitioned and the merged
+    one written (float32); q, k, v and o (bf16), log_alpha, beta and lam
+    (float32)."""
+    pc = bin(t).count("1")
+    j = ((t + 1) & -(t + 1)).bit_length() - 1  # trailing ones of t
+    return B * H * ((2 * pc - j + 1) * d * d * 4 + 3 * d * 2 + 4 * (Ls + 1) + 8 + d * 2)
+
+
 def decode_bytes(B, H, d, Ls, t) -> int:
     """One decode step: the popcount(t) non-empty states read once and one merged
     state written (float32), q, k, v and o (bf16), log_alpha and lam (float32)."""
@@ -94,6 +106,7 @@ def measured_peaks():
 KERNEL_SOURCES = {
     "mamba2": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),
     "decode": ("decode.cu", "common.cuh"),
+    "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
 }
 
@@ -186,6 +199,12 @@ def _oracle_init(cfg, tag):
                    rng.standard_normal((S, d)) / np.sqrt(d), rng.standard_normal((S, d)),
                    -np.log1p(np.exp(rng.standard_normal(S))), np.log1p(np.exp(rng.standard_normal((S, Ls + 1)))))
         return
+    if cfg["kind"] == "gdn_decode":
+        dec = synth.make_decode_inputs(cfg, B=1, H=1)
+        rng = np.random.default_rng(7)
+        _W["x"] = (rng.standard_normal((cfg["Ls"], cfg["dv"], cfg["dk"])) * 0.05,) + tuple(
+            synth.to_f64(dec[n][:, 0, 0]) for n in ("q", "k", "v", "log_alpha", "beta", "lam"))
+        return
     inp = synth.make_inputs(dict(cfg, B=1, H=1), tag=tag)
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] == "gdn" else ())
     _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in names)
@@ -204,6 +223,17 @@ def _oracle_worker(job):
         q, k, v, la, lam, beta = _W["x"]
         gdn.gdn_rows_A(q, k, v, beta, la, lam, job)
         return float(len(job))
+    if cfg["kind"] == "gdn_decode":
+        from oracle import gdn
+        S, q, k, v, la, beta, lam = _W["x"]
+        t0 = cfg["T"]
+        ne = [((t0 >> i) & 1) == 1 for i in range(S.shape[0])]
+        left = job
+        while left > 0:
+            m = min(left, q.shape[0])
+            gdn.gdn_decode_steps(S, ne, t0, q[:m], k[:m], v[:m], beta[:m], la[:m], lam[:m])
+            left -= m
+        return job / cfg["H"]
     from oracle import decode
     S, q, k, v, la, lam = _W["x"]
     t0 = cfg["T"]
@@ -257,6 +287,8 @@ def sample_desc(cfg, size):
     if cfg["kind"] == "gdn":
         return (f"{size} uniformly drawn query rows per process of the row-restricted float64 reading-A form "
                 "(each call builds its unit-triangular system)")
+    if cfg["kind"] == "gdn_decode":
+        return f"{size} float64 Gated DeltaNet decode steps of one (b, h) per process"
     return f"{size} float64 decode steps of one (b, h) per process"
 
 
@@ -305,12 +337,13 @@ def decode_workload(cfg, dev, rank, binding, synth, torch):
     """Decode: 2.3 GB of level states (random values: the work of a step does not
     depend on them), per-step inputs drawn once, positions 65536 onward."""
     Bn, H, d, Ls, S = cfg["B"], cfg["H"], cfg["dk"], cfg["Ls"], cfg["steps"]
+    gdn = cfg["kind"] == "gdn_decode"
     gen = torch.Generator(device=dev)
     gen.manual_seed(cfg["seed"] + rank)
     states = torch.randn(Bn, H, Ls, d, d, device=dev, generator=gen) * 0.01
     scales = torch.ones(Bn, H, Ls, device=dev)
     dec = synth.make_decode_inputs(cfg, device="cpu", B=Bn, H=H)
-    names = ("q", "k", "v", "log_alpha", "lam")
+    names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if gdn else ())
     host = {n: dec[n].pin_memory() for n in names}
     g = {n: host[n].to(dev) for n in names}
     t_host = torch.tensor([[cfg["T"] + i] * Bn for i in range(S)], dtype=torch.int64).pin_memory()
@@ -319,10 +352,15 @@ def decode_workload(cfg, dev, rank, binding, synth, torch):
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
     pos = [0]
 
+    def call(t, x):
+        if gdn:
+            binding.ll_gdn_decode_step(t, x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["lam"], states, o=o)
+        else:
+            binding.ll_attn_decode_step(t, x["q"], x["k"], x["v"], x["log_alpha"], x["lam"], states, scales, o=o)
+
     def step(i=0):
         s = pos[0] % S
-        binding.ll_attn_decode_step(t_dev[s], g["q"][s], g["k"][s], g["v"][s], g["log_alpha"][s], g["lam"][s],
-                                    states, scales, o=o)
+        call(t_dev[s], {n: g[n][s] for n in names})
         pos[0] += 1
 
     def reset():
@@ -337,14 +375,15 @@ def decode_workload(cfg, dev, rank, binding, synth, torch):
         for n in names:
             xs[n].copy_(host[n][s], non_blocking=True)
         t_x.copy_(t_host[s], non_blocking=True)
-        binding.ll_attn_decode_step(t_x, xs["q"], xs["k"], xs["v"], xs["log_alpha"], xs["lam"], states, scales, o=o)
+        call(t_x, xs)
         o_host.copy_(o, non_blocking=True)
         pos[0] += 1
 
     h2d = sum(host[n][0].numel() * host[n].element_size() for n in names) + Bn * 8
     d2h = o_host.numel() * o_host.element_size()
+    nbytes = gdn_decode_bytes if gdn else decode_bytes
     return dict(step=step, e2e_step=e2e_step, reset=reset, units=Bn, h2d=h2d, d2h=d2h, launches=1, flush=False,
-                step_bytes=lambda i: decode_bytes(Bn, H, d, Ls, cfg["T"] + (i % S)))
+                step_bytes=lambda i: nbytes(Bn, H, d, Ls, cfg["T"] + (i % S)))
 
 
 # ----------------------------------------------------------------------------
@@ -371,7 +410,7 @@ def main():
     config = {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "dk": cfg["dk"],
               "dv": cfg["dv"], "chunk": cfg["chunk"], "L": cfg["L"], "io": cfg["io"],
               "parallelism": f"replicas x{world} (b,h) weak"}
-    if kind == "decode":
+    if kind in ("decode", "gdn_decode"):
         config.update(Ls=cfg["Ls"], positions=f"{cfg['T']}..{cfg['T'] + cfg['steps'] - 1} cycled",
                       l2="states (2.3 GB) larger than L2, no flush")
     else:
@@ -418,7 +457,7 @@ def main():
     torch.cuda.set_device(dev)
     binding.lib()
 
-    if kind == "decode":
+    if kind in ("decode", "gdn_decode"):
         w = decode_workload(cfg, dev, rank, binding, synth, torch)
     else:
         w = forward_workload(cfg, dev, rank, binding, synth, torch)
@@ -490,7 +529,7 @@ def main():
     # roofline of the dominant kernel
     hbm, bf16, sm_mhz, src = measured_peaks()
     traffic, kname = ncu_traffic(args.workload)
-    if kind == "decode":
+    if kind in ("decode", "gdn_decode"):
         abytes = sum(w["step_bytes"](i) for i in range(args.steps)) / args.steps
         achieved = abytes / (mean_ms * 1e-3) / 1e9
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
