@@ -44,6 +44,7 @@ METRICS = {
     "mamba2": "log-linear Mamba-2 fwd tokens/s at T=16K,H=16,d=128; % of roofline",
     "decode": "log-linear Mamba-2 Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); % of HBM roofline",
     "gdn": "log-linear Gated DeltaNet fwd tokens/s (B=2, H=16, T=4096, d=128)",
+    "gdn_b": "log-linear Gated DeltaNet fwd, reading B, tokens/s (B=2, H=16, T=4096, d=128)",
     "gdn_decode": "log-linear Gated DeltaNet Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); "
                   "% of HBM roofline",
 }
@@ -57,7 +58,7 @@ def algorithmic_bytes(cfg) -> int:
     written once; plus beta for Gated DeltaNet."""
     b_io = 2 if cfg["io"] == "bf16" else 4
     per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
-    if cfg["kind"] == "gdn":
+    if cfg["kind"] in ("gdn", "gdn_b"):
         per_bh += cfg["T"] * 4
     return per_bh * cfg["B"] * cfg["H"]
 
@@ -71,6 +72,11 @@ def algorithmic_flops(cfg) -> int:
     if cfg["kind"] == "gdn":
         per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d
         per_bh = N * per_chunk + P * (6 * C * d * d + 2 * C * C * d)
+    elif cfg["kind"] == "gdn_b":
+        # the chunk factors (as above), the single-state pass (S W^T and the
+        # update, 4 C d^2 per chunk), then the log-linear Mamba-2 forward
+        per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d + 4 * C * d * d
+        per_bh = N * per_chunk + 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
     else:
         per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
     return per_bh * cfg["B"] * cfg["H"]
@@ -108,6 +114,7 @@ KERNEL_SOURCES = {
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
+    "gdn_b": ("gdn.cu", "fwd_tc.cu", "common.cuh", "sm100.cuh"),
 }
 
 
@@ -206,7 +213,7 @@ def _oracle_init(cfg, tag):
             synth.to_f64(dec[n][:, 0, 0]) for n in ("q", "k", "v", "log_alpha", "beta", "lam"))
         return
     inp = synth.make_inputs(dict(cfg, B=1, H=1), tag=tag)
-    names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] == "gdn" else ())
+    names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] in ("gdn", "gdn_b") else ())
     _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in names)
 
 
@@ -223,6 +230,12 @@ def _oracle_worker(job):
         q, k, v, la, lam, beta = _W["x"]
         gdn.gdn_rows_A(q, k, v, beta, la, lam, job)
         return float(len(job))
+    if cfg["kind"] == "gdn_b":
+        from oracle import gdn
+        q, k, v, la, lam, beta = _W["x"]
+        for _ in range(job):  # whole (b, h) slices: the pseudo-values couple every row
+            gdn.gdn_forward_B(q, k, v, beta, la, lam)
+        return float(job * q.shape[0])
     if cfg["kind"] == "gdn_decode":
         from oracle import gdn
         S, q, k, v, la, beta, lam = _W["x"]
@@ -275,7 +288,7 @@ def oracle_sample(pool, cfg, cores, size, seed=0):
 
 def calibrate(pool, cfg, cores, budget_s):
     """Job size so that one sample takes about `budget_s` seconds of wall time."""
-    small = 16
+    small = 1 if cfg["kind"] == "gdn_b" else 16
     oracle_sample(pool, cfg, cores, 1, seed=998)  # workers finish their set-up
     _, n, wall = oracle_sample(pool, cfg, cores, small, seed=999)
     return int(min(10 ** 6, max(1, budget_s / (wall / small))))
@@ -289,6 +302,9 @@ def sample_desc(cfg, size):
                 "(each call builds its unit-triangular system)")
     if cfg["kind"] == "gdn_decode":
         return f"{size} float64 Gated DeltaNet decode steps of one (b, h) per process"
+    if cfg["kind"] == "gdn_b":
+        return (f"{size} whole (b, h) slices ({cfg['T']} tokens) per process of the dense float64 reading-B "
+                "form (one triangular solve per slice)")
     return f"{size} float64 decode steps of one (b, h) per process"
 
 
@@ -297,7 +313,8 @@ def sample_desc(cfg, size):
 # ----------------------------------------------------------------------------
 def forward_workload(cfg, dev, rank, binding, synth, torch):
     """Forward (Mamba-2 or Gated DeltaNet): device and pinned host inputs, step functions."""
-    gdn = cfg["kind"] == "gdn"
+    gdn = cfg["kind"] in ("gdn", "gdn_b")
+    reading_b = cfg["kind"] == "gdn_b"
     inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if gdn else ())
     host = {n: inp_host[n].pin_memory() for n in names}
@@ -305,7 +322,10 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     Bn, H, T, dk = g["q"].shape
     dv = g["v"].shape[-1]
     shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], 0, binding._io(g["q"].dtype))
-    if gdn:
+    if reading_b:
+        ws = binding.alloc_workspace(binding.ll_gdn_fwd_b_workspace_size(shape), dev)
+        launches = 2 + binding.ll_attn_fwd_launches(shape)
+    elif gdn:
         ws = binding.alloc_workspace(binding.ll_gdn_fwd_workspace_size(shape), dev)
         launches = 2
     else:
@@ -315,7 +335,10 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
 
     def step(i=0):
-        if gdn:
+        if reading_b:
+            binding.ll_gdn_fwd_b(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
+                                 workspace=ws)
+        elif gdn:
             binding.ll_gdn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
                                workspace=ws)
         else:
@@ -535,7 +558,7 @@ def main():
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic, "peak_source": f"{src} (HBM copy)",
                     "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname}
-    elif kind == "gdn":
+    elif kind in ("gdn", "gdn_b"):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
         aflops = w["aflops"]

@@ -18,6 +18,8 @@
  *                        gated delta rule itself is not on the pages (reading A:
  *                        O = (C_GDN . M^H) V, every level state follows the full
  *                        gated-delta transition).
+ *   ll_gdn_fwd_b         the same forward under reading B (log-linear Mamba-2 on the
+ *                        delta-rule pseudo-values), study note §3-5.
  *   ll_gdn_decode_step   one token of Log-Linear Gated DeltaNet decoding over the
  *                        Fenwick level states (reading A), study note §3-5/§3-6.
  *
@@ -210,6 +212,26 @@ LL_API size_t ll_gdn_fwd_workspace_size(const ll_shape* shape);
 LL_API ll_status ll_gdn_fwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                      const float* log_alpha, const float* beta, const float* lam, void* o,
                      void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace ll_gdn_fwd_b needs for `shape` (0 when the shape is
+ * invalid or not supported by reading B: it needs dk = dv = 128 and
+ * chunk >= 64). */
+LL_API size_t ll_gdn_fwd_b_workspace_size(const ll_shape* shape);
+
+/* Log-Linear Gated DeltaNet forward, reading B: log-linear Mamba-2 applied
+ * to the delta rule's pseudo-values,
+ *   O = (Q K^T . M^S . M^H) U,  U = (I + diag(beta) SL(K K^T . M^S))^{-1} diag(beta) V,
+ * i.e. u_t = beta_t (v_t - alpha_t S_{t-1} k_t) with S the single
+ * gated-delta state.  The pages combine Gated DeltaNet with the hierarchical
+ * mask (study note §3-5; gist.science (de) Technische Zusammenfassung §2)
+ * without fixing where the mask acts; ll_gdn_fwd is reading A, this entry
+ * point the other plain reading.  Arguments, layouts, errors: as ll_gdn_fwd.
+ * Computed as a chunk-wise pass for U (float32) followed by ll_attn_fwd on
+ * (q, k, U) in the io dtype, so U is rounded to bf16 for bf16 io.
+ * Returns LL_ERR_UNSUPPORTED unless dk = dv = 128 and chunk >= 64. */
+LL_API ll_status ll_gdn_fwd_b(const ll_shape* shape, const void* q, const void* k, const void* v,
+                              const float* log_alpha, const float* beta, const float* lam, void* o,
+                              void* workspace, size_t ws_bytes, void* stream);
 
 #ifdef __cplusplus
 }

@@ -25,7 +25,7 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 # every symbol the header declares
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
            "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
-           "ll_gdn_decode_step")
+           "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b")
 
 
 class LLError(RuntimeError):
@@ -75,6 +75,10 @@ def lib() -> ctypes.CDLL:
     L.ll_gdn_fwd_workspace_size.argtypes = [shp]
     L.ll_gdn_fwd.restype = i32
     L.ll_gdn_fwd.argtypes = [shp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+    L.ll_gdn_fwd_b_workspace_size.restype = sz
+    L.ll_gdn_fwd_b_workspace_size.argtypes = [shp]
+    L.ll_gdn_fwd_b.restype = i32
+    L.ll_gdn_fwd_b.argtypes = [shp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
     _lib = L
     return L
 
@@ -121,6 +125,10 @@ def ll_attn_fwd_launches(shape: ll_shape) -> int:
 
 def ll_gdn_fwd_workspace_size(shape: ll_shape) -> int:
     return int(lib().ll_gdn_fwd_workspace_size(ctypes.byref(shape)))
+
+
+def ll_gdn_fwd_b_workspace_size(shape: ll_shape) -> int:
+    return int(lib().ll_gdn_fwd_b_workspace_size(ctypes.byref(shape)))
 
 
 def alloc_workspace(nbytes: int, device) -> torch.Tensor:
@@ -229,9 +237,7 @@ def ll_gdn_decode_step(t, q, k, v, log_alpha, beta, lam, states, *, o=None):
     return o
 
 
-def ll_gdn_fwd(q, k, v, log_alpha, beta, lam, chunk: int, *, o=None, workspace=None):
-    """Log-Linear Gated DeltaNet forward (reading A).  Shapes as ll_attn_fwd plus
-    beta [B,H,T] float32.  Returns o [B,H,T,dv]."""
+def _gdn_forward(entry: str, size_query, q, k, v, log_alpha, beta, lam, chunk, o, workspace):
     B, H, T, dk = q.shape
     dv = v.shape[-1]
     L = lam.shape[-1]
@@ -244,12 +250,25 @@ def ll_gdn_fwd(q, k, v, log_alpha, beta, lam, chunk: int, *, o=None, workspace=N
     if o is None:
         o = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
     if workspace is None:
-        workspace = alloc_workspace(ll_gdn_fwd_workspace_size(shape), q.device)
-    st = lib().ll_gdn_fwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta), _ptr(lam),
-                          _ptr(o), _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(q.device))
-    _check(st, "ll_gdn_fwd")
+        workspace = alloc_workspace(size_query(shape), q.device)
+    st = getattr(lib(), entry)(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(beta),
+                               _ptr(lam), _ptr(o), _ptr(workspace), ctypes.c_size_t(workspace.numel()),
+                               _stream(q.device))
+    _check(st, entry)
     return o
 
+
+def ll_gdn_fwd(q, k, v, log_alpha, beta, lam, chunk: int, *, o=None, workspace=None):
+    """Log-Linear Gated DeltaNet forward (reading A).  Shapes as ll_attn_fwd plus
+    beta [B,H,T] float32.  Returns o [B,H,T,dv]."""
+    return _gdn_forward("ll_gdn_fwd", ll_gdn_fwd_workspace_size, q, k, v, log_alpha, beta, lam, chunk, o, workspace)
+
+
+def ll_gdn_fwd_b(q, k, v, log_alpha, beta, lam, chunk: int, *, o=None, workspace=None):
+    """Log-Linear Gated DeltaNet forward, reading B (log-linear Mamba-2 on the
+    delta-rule pseudo-values).  Arguments as ll_gdn_fwd."""
+    return _gdn_forward("ll_gdn_fwd_b", ll_gdn_fwd_b_workspace_size, q, k, v, log_alpha, beta, lam, chunk, o,
+                        workspace)
 
 def ll_last_device_error(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device error status."""

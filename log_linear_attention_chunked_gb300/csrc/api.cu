@@ -137,6 +137,31 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
                        static_cast<cudaStream_t>(stream), ew);
 }
 
+size_t ll_gdn_fwd_b_workspace_size(const ll_shape* s) {
+  if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
+  return gdn_b_workspace(*s);
+}
+
+ll_status ll_gdn_fwd_b(const ll_shape* s, const void* q, const void* k, const void* v, const float* log_alpha,
+                       const float* beta, const float* lam, void* o, void* workspace, size_t ws_bytes,
+                       void* stream) {
+  ll_status st = check_shape(s);
+  if (st != LL_OK) return st;
+  if (s->Ls != 0) return LL_ERR_INVALID_ARG;
+  if (!q || !k || !v || !log_alpha || !beta || !lam || !o) return LL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(beta) ||
+      !aligned16(lam) || !aligned16(o))
+    return LL_ERR_INVALID_ARG;
+  const size_t need_ws = gdn_b_workspace(*s);
+  if (need_ws == 0) return LL_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
+  FwdArgs a{*s, q, k, v, log_alpha, lam, beta, o, nullptr, nullptr, workspace, ws_bytes,
+            static_cast<cudaStream_t>(stream), err_word()};
+  if (!a.err) return LL_ERR_CUDA;
+  return gdn_b_launch(a);
+}
+
 ll_status ll_gdn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
                              const void* k, const void* v, const float* log_alpha, const float* beta,
                              const float* lam, float* states, void* o, void* stream) {

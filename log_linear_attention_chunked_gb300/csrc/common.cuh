@@ -86,5 +86,7 @@ ll_status gdn_decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, c
                             const float* lam, float* states, void* o, cudaStream_t stream, unsigned* err);
 size_t gdn_workspace(const ll_shape& s);
 ll_status gdn_launch(const FwdArgs& a);
+size_t gdn_b_workspace(const ll_shape& s);
+ll_status gdn_b_launch(const FwdArgs& a);
 
 }  // namespace llattn

@@ -638,6 +638,156 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_scan128_kernel(
   cp_async_wait0();
 }
 
+// ------------------------------------------- reading B: one state, pseudo-values out
+// Reading B is log-linear Mamba-2 applied to the delta rule's pseudo-values
+// u_t = beta_t (v_t - alpha_t S_{t-1} k_t), S the single gated-delta state.
+// Per chunk, with S the state at the chunk start (S = 0 for chunk 0),
+//   U_c = U - W S^T          (U = Tinv diag(beta) V and W from the preparation)
+//   S  <- gamma S - (S W^T) Kt + S_c     (S_c = U^T Kt, the chunk's own state)
+// This kernel runs that recurrence for 16 d_v rows per CTA and writes U_c in
+// the io dtype, the values of the log-linear Mamba-2 forward that follows.
+// Tiles and thread mapping as in gdn_scan128_kernel (one product in phase 1).
+template <typename IO>
+__global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
+    const float* __restrict__ Wg, const float* __restrict__ Kt, const float* __restrict__ Sloc,
+    const float* __restrict__ loggam, const float* __restrict__ Ul, IO* __restrict__ U, int T, int dv, int N) {
+  extern __shared__ __align__(16) float sm[];
+  const size_t bh = blockIdx.y;
+  const int r0 = blockIdx.x * kR;
+  const int tid = threadIdx.x;
+  float* X = sm;                     // [16][kSx] the state rows
+  float* Wsm = X + kR * kSx;         // [64][kSx]
+  float* Ksm = Wsm + kCe * kSx;      // [64][kSx]
+  float* P1 = Ksm + kCe * kSx;       // [4][16][kSp1]
+  float* P2 = P1 + 4 * kR * kSp1;    // [4][16][kSp2]
+  float* Ysm = P2 + 4 * kR * kSp2;   // [16][kSy]
+  const int ks = tid >> 6, u = tid & 63, rg = u & 3, cg = u >> 2;
+
+  for (int c = 0; c < N; ++c) {
+    const size_t row0 = bh * T + (size_t)c * kCe;
+    const float* Sc = Sloc + (bh * N + c) * (size_t)dv * kDk + (size_t)r0 * kDk;
+    if (c > 0) {
+      // ---- Y = X W^T (split-K 4, partials through shared memory)
+      float y[4][4];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) y[a][j] = 0.f;
+#pragma unroll
+      for (int s8 = 0; s8 < 8; ++s8) {
+        const int f = ks * 32 + 4 * s8;
+        float4 xa[4], wa[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) xa[a] = *reinterpret_cast<const float4*>(X + (rg + 4 * a) * kSx + f);
+#pragma unroll
+        for (int j = 0; j < 4; ++j) wa[j] = *reinterpret_cast<const float4*>(Wsm + (cg + 16 * j) * kSx + f);
+#pragma unroll
+        for (int a = 0; a < 4; ++a)
+#pragma unroll
+          for (int j = 0; j < 4; ++j) {
+            y[a][j] = fmaf(xa[a].x, wa[j].x, y[a][j]);
+            y[a][j] = fmaf(xa[a].y, wa[j].y, y[a][j]);
+            y[a][j] = fmaf(xa[a].z, wa[j].z, y[a][j]);
+            y[a][j] = fmaf(xa[a].w, wa[j].w, y[a][j]);
+          }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int j = 0; j < 4; ++j) P1[(ks * kR + rg + 4 * a) * kSp1 + cg + 16 * j] = y[a][j];
+      __syncthreads();
+      {
+        const int r = tid >> 4, i4 = tid & 15;
+        float4 acc = *reinterpret_cast<const float4*>(P1 + r * kSp1 + 4 * i4);
+#pragma unroll
+        for (int q = 1; q < 4; ++q) {
+          const float4 t = *reinterpret_cast<const float4*>(P1 + (q * kR + r) * kSp1 + 4 * i4);
+          acc.x += t.x; acc.y += t.y; acc.z += t.z; acc.w += t.w;
+        }
+        *reinterpret_cast<float4*>(Ysm + r * kSy + 4 * i4) = acc;
+      }
+      __syncthreads();
+    }
+    // ---- U_c = U - Y^T for this CTA's rows (token e >> 4, row e & 15)
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + m * kThreads;
+      const int i = e >> 4, r = e & 15;
+      const size_t gi = (row0 + i) * dv + r0 + r;
+      U[gi] = from_f<IO>(c > 0 ? Ul[gi] - Ysm[r * kSy + i] : Ul[gi]);
+    }
+    if (c > 0) {
+      // ---- partials of Y Kt
+      float acc[4][8];
+#pragma unroll
+      for (int a = 0; a < 4; ++a)
+#pragma unroll
+        for (int b = 0; b < 8; ++b) acc[a][b] = 0.f;
+#pragma unroll
+      for (int s4 = 0; s4 < 4; ++s4) {
+        const int i = ks * 16 + 4 * s4;
+        float4 ya[4];
+#pragma unroll
+        for (int a = 0; a < 4; ++a) ya[a] = *reinterpret_cast<const float4*>(Ysm + (rg + 4 * a) * kSy + i);
+#pragma unroll
+        for (int t = 0; t < 4; ++t) {
+          const float4 k0 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 4 * cg);
+          const float4 k1 = *reinterpret_cast<const float4*>(Ksm + (i + t) * kSx + 64 + 4 * cg);
+#pragma unroll
+          for (int a = 0; a < 4; ++a) {
+            const float yv = t == 0 ? ya[a].x : t == 1 ? ya[a].y : t == 2 ? ya[a].z : ya[a].w;
+            acc[a][0] = fmaf(yv, k0.x, acc[a][0]);
+            acc[a][1] = fmaf(yv, k0.y, acc[a][1]);
+            acc[a][2] = fmaf(yv, k0.z, acc[a][2]);
+            acc[a][3] = fmaf(yv, k0.w, acc[a][3]);
+            acc[a][4] = fmaf(yv, k1.x, acc[a][4]);
+            acc[a][5] = fmaf(yv, k1.y, acc[a][5]);
+            acc[a][6] = fmaf(yv, k1.z, acc[a][6]);
+            acc[a][7] = fmaf(yv, k1.w, acc[a][7]);
+          }
+        }
+      }
+#pragma unroll
+      for (int a = 0; a < 4; ++a) {
+        float* dst = P2 + (ks * kR + rg + 4 * a) * kSp2;
+        *reinterpret_cast<float4*>(dst + 4 * cg) = make_float4(acc[a][0], acc[a][1], acc[a][2], acc[a][3]);
+        *reinterpret_cast<float4*>(dst + 64 + 4 * cg) = make_float4(acc[a][4], acc[a][5], acc[a][6], acc[a][7]);
+      }
+      __syncthreads();
+    }
+    // W and Kt of the next chunk (their last readers passed the barrier above)
+    if (c + 1 < N) {
+      stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+      stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
+      cp_async_commit();
+    }
+    // ---- X <- gamma X - sum of the partials + S_c (this thread's 2 x 4 elements)
+    const float gam = expf(loggam[bh * N + c]);
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int e = tid + m * kThreads;
+      const int r = e >> 5, f4 = e & 31;
+      float* xp = X + r * kSx + 4 * f4;
+      float4 xv = *reinterpret_cast<const float4*>(Sc + r * kDk + 4 * f4);
+      if (c > 0) {
+        const float4 x0 = *reinterpret_cast<const float4*>(xp);
+        xv.x = fmaf(gam, x0.x, xv.x); xv.y = fmaf(gam, x0.y, xv.y);
+        xv.z = fmaf(gam, x0.z, xv.z); xv.w = fmaf(gam, x0.w, xv.w);
+#pragma unroll
+        for (int q = 0; q < 4; ++q) {
+          const float4 t = *reinterpret_cast<const float4*>(P2 + (q * kR + r) * kSp2 + 4 * f4);
+          xv.x -= t.x; xv.y -= t.y; xv.z -= t.z; xv.w -= t.w;
+        }
+      }
+      *reinterpret_cast<float4*>(xp) = xv;
+    }
+    cp_async_wait0();
+    __syncthreads();
+  }
+}
+
+constexpr size_t b_scan_smem_floats() { return kR * kSx + 2 * kCe * kSx + 4 * kR * kSp1 + 4 * kR * kSp2 + kR * kSy; }
+
 }  // namespace fast
 
 // ------------------------------------------- kernel 1, d_k = d_v = 128, 64-token chunks
@@ -732,7 +882,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
     const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
     const float* __restrict__ log_alpha, const float* __restrict__ beta, const float* __restrict__ lam,
     float* __restrict__ Qp, float* __restrict__ Wg, float* __restrict__ Kt, float* __restrict__ Sloc,
-    float* __restrict__ loggam, float* __restrict__ Oacc, int T, int L) {
+    float* __restrict__ loggam, float* __restrict__ Oacc, float* __restrict__ Ug, int T, int L) {
   extern __shared__ __align__(16) float sm[];
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
@@ -929,6 +1079,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
       st4(orow + 4 * tj, c1[r][0], c1[r][1], c1[r][2], c1[r][3]);
       st4(orow + 64 + 4 * tj, c1[r][4], c1[r][5], c1[r][6], c1[r][7]);
     }
+    if (Ug) {  // the chunk's own pseudo-values U (reading B)
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        float* urow = Ug + (row0 + 4 * ti + r) * kDk;
+        st4(urow + 4 * tj, c2[r][0], c2[r][1], c2[r][2], c2[r][3]);
+        st4(urow + 64 + 4 * tj, c2[r][4], c2[r][5], c2[r][6], c2[r][7]);
+      }
+    }
     __syncthreads();  // every read of V is done
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
@@ -1011,7 +1169,7 @@ ll_status launch_typed(const FwdArgs& a, const GdnPlan& p) {
                                     (int)sm1));
     fast::gdn_prep128_kernel<IO><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
         static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha,
-        a.beta, a.lam, Qp, W, Kt, S, lg, O, s.T, s.L);
+        a.beta, a.lam, Qp, W, Kt, S, lg, O, nullptr, s.T, s.L);
   } else {
     const size_t sm1 = prep_smem_floats(p.Ce, s.dk, s.dv) * 4;
     LL_CUDA_OK(cudaFuncSetAttribute(gdn_prep_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
@@ -1049,6 +1207,85 @@ ll_status gdn_launch(const FwdArgs& a) {
   if (a.ws_bytes < p.total) return LL_ERR_WORKSPACE;
   if (a.s.io == LL_F32) return launch_typed<float>(a, p);
   return launch_typed<__nv_bfloat16>(a, p);
+}
+
+// ---------------------------------------------------------------- reading B
+// workspace: the preparation's buffers | U (float32) | U_c (io dtype, the
+// forward's values) | the log-linear Mamba-2 forward's own workspace
+namespace {
+
+struct GdnBPlan {
+  GdnPlan g;
+  size_t off_Ul, off_Uio, off_fwd, fwd_bytes, total;
+  bool ok;
+};
+
+GdnBPlan gdn_b_plan(const ll_shape& s) {
+  GdnBPlan b{};
+  b.g = gdn_plan(s);
+  b.ok = b.g.ok && b.g.fast_prep;
+  if (!b.ok) return b;
+  const size_t BH = (size_t)s.B * s.H;
+  const size_t esz = s.io == LL_F32 ? 4 : 2;
+  size_t off = b.g.total;
+  b.off_Ul = off;  off = align_up(off + BH * s.T * (size_t)s.dv * 4, 256);
+  b.off_Uio = off; off = align_up(off + BH * s.T * (size_t)s.dv * esz, 256);
+  b.fwd_bytes = fwd_tc_supported(s) ? fwd_tc_workspace(s) : fwd_simt_workspace(s);
+  b.off_fwd = off; off = align_up(off + b.fwd_bytes, 256);
+  b.total = off;
+  return b;
+}
+
+template <typename IO>
+ll_status launch_b_typed(const FwdArgs& a, const GdnBPlan& b) {
+  const ll_shape& s = a.s;
+  const GdnPlan& p = b.g;
+  unsigned char* ws = static_cast<unsigned char*>(a.ws);
+  float* Qp = reinterpret_cast<float*>(ws + p.off_Qp);
+  float* W = reinterpret_cast<float*>(ws + p.off_W);
+  float* Kt = reinterpret_cast<float*>(ws + p.off_Kt);
+  float* S = reinterpret_cast<float*>(ws + p.off_S);
+  float* lg = reinterpret_cast<float*>(ws + p.off_lg);
+  float* O = reinterpret_cast<float*>(ws + p.off_O);
+  float* Ul = reinterpret_cast<float*>(ws + b.off_Ul);
+  IO* Uio = reinterpret_cast<IO*>(ws + b.off_Uio);
+  const int BH = s.B * s.H;
+  const size_t sm1 = fast::prep_smem_floats() * 4;
+  LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_prep128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm1));
+  fast::gdn_prep128_kernel<IO><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
+      static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.beta,
+      a.lam, Qp, W, Kt, S, lg, O, Ul, s.T, s.L);
+  LL_CUDA_OK(cudaGetLastError());
+  const size_t sm2 = fast::b_scan_smem_floats() * 4;
+  LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_b_scan128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)sm2));
+  fast::gdn_b_scan128_kernel<IO><<<dim3(s.dv / fast::kR, BH), kThreads, sm2, a.stream>>>(W, Kt, S, lg, Ul, Uio, s.T,
+                                                                                         s.dv, p.N);
+  LL_CUDA_OK(cudaGetLastError());
+  FwdArgs f = a;
+  f.v = Uio;
+  f.beta = nullptr;
+  f.state_out = nullptr;
+  f.scale_out = nullptr;
+  f.ws = ws + b.off_fwd;
+  f.ws_bytes = b.fwd_bytes;
+  return fwd_tc_supported(s) ? fwd_tc_launch(f) : fwd_simt_launch(f);
+}
+
+}  // namespace
+
+size_t gdn_b_workspace(const ll_shape& s) {
+  const GdnBPlan b = gdn_b_plan(s);
+  return b.ok ? b.total : 0;
+}
+
+ll_status gdn_b_launch(const FwdArgs& a) {
+  const GdnBPlan b = gdn_b_plan(a.s);
+  if (!b.ok) return LL_ERR_UNSUPPORTED;
+  if (a.ws_bytes < b.total) return LL_ERR_WORKSPACE;
+  if (a.s.io == LL_F32) return launch_b_typed<float>(a, b);
+  return launch_b_typed<__nv_bfloat16>(a, b);
 }
 
 }  // namespace llattn

@@ -33,6 +33,9 @@ WORKLOADS = {
                              io="bf16", seed=2, shift=0.0),
     "gdn_bf16_t4k": dict(kind="gdn", B=2, H=16, T=4096, dk=128, dv=128, chunk=64, L=13,
                          io="bf16", seed=3, shift=2.0),
+    # the same workload under reading B (log-linear Mamba-2 on the delta-rule pseudo-values)
+    "gdn_b_bf16_t4k": dict(kind="gdn_b", B=2, H=16, T=4096, dk=128, dv=128, chunk=64, L=13,
+                           io="bf16", seed=3, shift=2.0),
     # prefix of 65536 tokens (forward with state export), then 256 decode steps
     "decode_b64_t64k": dict(kind="decode", B=64, H=32, T=65536, dk=128, dv=128, chunk=64, L=17,
                             Ls=17, steps=256, io="bf16", seed=4, shift=0.0),
@@ -100,7 +103,7 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
     T = cfg["T"] if T is None else T
     dk, dv, L = cfg["dk"], cfg["dv"], cfg["L"]
     seed = cfg["seed"] + (zlib.crc32(tag.encode()) << 8 if tag else 0)
-    gdn = cfg["kind"] == "gdn"
+    gdn = cfg["kind"] in ("gdn", "gdn_b")
     dt = io_dtype(cfg["io"])
     shift = float(cfg.get("shift", 0.0))
 

@@ -100,6 +100,19 @@ def test_decode_rejects_bad_args_on_host(L):
     assert L.ll_attn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
 
 
+def test_gdn_b_rejects_bad_args_on_host(L):
+    vp = ctypes.c_void_p
+    s = _shape(Ls=3)
+    assert L.ll_gdn_fwd_b(ctypes.byref(s), *([vp(FAKE)] * 8), ctypes.c_size_t(1 << 40), None) == 1
+    s = _shape()
+    args = [vp(FAKE)] * 7
+    for i in range(7):  # every null tensor
+        bad = list(args)
+        bad[i] = None
+        assert L.ll_gdn_fwd_b(ctypes.byref(s), *bad, vp(FAKE), ctypes.c_size_t(1 << 40), None) == 1, i
+    assert L.ll_gdn_fwd_b(ctypes.byref(s), *args, None, ctypes.c_size_t(0), None) in (2, 5)
+
+
 def test_gdn_decode_rejects_bad_args_on_host(L):
     vp = ctypes.c_void_p
     args = [vp(FAKE)] * 10  # t, q, k, v, log_alpha, beta, lam, states, o, stream
