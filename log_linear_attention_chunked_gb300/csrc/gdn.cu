@@ -665,7 +665,35 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
 
   for (int c = 0; c < N; ++c) {
     const size_t row0 = bh * T + (size_t)c * kCe;
+    const bool more = c + 1 < N;
     const float* Sc = Sloc + (bh * N + c) * (size_t)dv * kDk + (size_t)r0 * kDk;
+    // this chunk's inputs from global memory, loaded before the products
+    // that hide their latency: U (4 elements: token e >> 4, row e & 15) and
+    // S_c (2 x 4 elements of the state rows)
+    float ul[4];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) {
+      const int e = tid + m * kThreads;
+      ul[m] = Ul[(row0 + (e >> 4)) * dv + r0 + (e & 15)];
+    }
+    float4 scv[2];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) {
+      const int e = tid + m * kThreads;
+      scv[m] = *reinterpret_cast<const float4*>(Sc + (e >> 5) * kDk + 4 * (e & 31));
+    }
+    const float gam = expf(loggam[bh * N + c]);
+    if (tid == 0) {
+      if (c + 2 < N) {
+        const size_t rn = row0 + 2 * kCe;
+        bulk_prefetch_l2(Wg + rn * kDk, kCe * kDk * 4);
+        bulk_prefetch_l2(Kt + rn * kDk, kCe * kDk * 4);
+      }
+      if (more) {
+        bulk_prefetch_l2(Ul + (row0 + kCe) * dv, kCe * dv * 4);
+        bulk_prefetch_l2(Sc + (size_t)dv * kDk, kR * kDk * 4);
+      }
+    }
     if (c > 0) {
       // ---- Y = X W^T (split-K 4, partials through shared memory)
       float y[4][4];
@@ -696,6 +724,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
 #pragma unroll
         for (int j = 0; j < 4; ++j) P1[(ks * kR + rg + 4 * a) * kSp1 + cg + 16 * j] = y[a][j];
       __syncthreads();
+      if (more) {  // W is no longer read: the next chunk's streams in
+        stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+        cp_async_commit();
+      }
       {
         const int r = tid >> 4, i4 = tid & 15;
         float4 acc = *reinterpret_cast<const float4*>(P1 + r * kSp1 + 4 * i4);
@@ -706,15 +738,16 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
         }
         *reinterpret_cast<float4*>(Ysm + r * kSy + 4 * i4) = acc;
       }
+      if (more) cp_async_wait1();  // this chunk's Kt (the next W may still be in flight)
+      else cp_async_wait0();
       __syncthreads();
     }
-    // ---- U_c = U - Y^T for this CTA's rows (token e >> 4, row e & 15)
+    // ---- U_c = U - Y^T for this CTA's rows
 #pragma unroll
     for (int m = 0; m < 4; ++m) {
       const int e = tid + m * kThreads;
       const int i = e >> 4, r = e & 15;
-      const size_t gi = (row0 + i) * dv + r0 + r;
-      U[gi] = from_f<IO>(c > 0 ? Ul[gi] - Ysm[r * kSy + i] : Ul[gi]);
+      U[(row0 + i) * dv + r0 + r] = from_f<IO>(c > 0 ? ul[m] - Ysm[r * kSy + i] : ul[m]);
     }
     if (c > 0) {
       // ---- partials of Y Kt
@@ -755,20 +788,21 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
       }
       __syncthreads();
     }
-    // W and Kt of the next chunk (their last readers passed the barrier above)
-    if (c + 1 < N) {
-      stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
-      stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);
+    if (more) {
+      if (c == 0) {  // chunk 0 reads no tile: both of chunk 1's stream in now
+        stage_tile(Wsm, Wg + (row0 + kCe) * kDk, tid);
+        cp_async_commit();
+      }
+      stage_tile(Ksm, Kt + (row0 + kCe) * kDk, tid);  // Kt is no longer read
       cp_async_commit();
     }
     // ---- X <- gamma X - sum of the partials + S_c (this thread's 2 x 4 elements)
-    const float gam = expf(loggam[bh * N + c]);
 #pragma unroll
     for (int m = 0; m < 2; ++m) {
       const int e = tid + m * kThreads;
       const int r = e >> 5, f4 = e & 31;
       float* xp = X + r * kSx + 4 * f4;
-      float4 xv = *reinterpret_cast<const float4*>(Sc + r * kDk + 4 * f4);
+      float4 xv = scv[m];
       if (c > 0) {
         const float4 x0 = *reinterpret_cast<const float4*>(xp);
         xv.x = fmaf(gam, x0.x, xv.x); xv.y = fmaf(gam, x0.y, xv.y);
@@ -781,9 +815,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_b_scan128_kernel(
       }
       *reinterpret_cast<float4*>(xp) = xv;
     }
-    cp_async_wait0();
+    if (more) cp_async_wait1();  // the next chunk's W (its Kt may still be in flight)
     __syncthreads();
   }
+  cp_async_wait0();
 }
 
 constexpr size_t b_scan_smem_floats() { return kR * kSx + 2 * kCe * kSx + 4 * kR * kSp1 + 4 * kR * kSp2 + kR * kSy; }
