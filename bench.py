@@ -309,6 +309,25 @@ def sample_desc(cfg, size):
 
 
 # ----------------------------------------------------------------------------
+# multi-rank aggregation (one process per GPU; ranks hold independent replicas)
+# ----------------------------------------------------------------------------
+def max_over_ranks(x: float, world: int, device=None) -> float:
+    """The slowest rank's figure: every rank passes its own, all get the max."""
+    if world <= 1:
+        return x
+    import torch
+    import torch.distributed as dist
+    t = torch.tensor([float(x)], dtype=torch.float64, device=device)
+    dist.all_reduce(t, op=dist.ReduceOp.MAX)
+    return float(t.item())
+
+
+def whole_job_rate(units_per_rank: float, world: int, ms: float) -> float:
+    """Units of all ranks per second when every rank took (at most) `ms` per step."""
+    return units_per_rank * world / (ms * 1e-3)
+
+
+# ----------------------------------------------------------------------------
 # GPU workloads
 # ----------------------------------------------------------------------------
 def forward_workload(cfg, dev, rank, binding, synth, torch):
@@ -521,12 +540,8 @@ def main():
     if binding.ll_last_device_error() != 0:
         raise RuntimeError("device error during the timed region")
     step_ms = [a.elapsed_time(b) for a, b in ev]
-    mean_ms = sum(step_ms) / len(step_ms)
-    if world > 1:
-        t = torch.tensor([mean_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        mean_ms = float(t.item())
-    value = w["units"] * world / (mean_ms * 1e-3)
+    mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
+    value = whole_job_rate(w["units"], world, mean_ms)
 
     # end to end through the public call: host inputs in, host output out
     if "reset" in w:
@@ -541,12 +556,8 @@ def main():
         w["e2e_step"](i)
     e1.record(stream)
     torch.cuda.synchronize()
-    e2e_ms = e0.elapsed_time(e1) / e2e_steps
-    if world > 1:
-        t = torch.tensor([e2e_ms], device=dev)
-        torch.distributed.all_reduce(t, op=torch.distributed.ReduceOp.MAX)
-        e2e_ms = float(t.item())
-    e2e = {"value": w["units"] * world / (e2e_ms * 1e-3), "unit": "tokens/s", "h2d_bytes_per_step": w["h2d"],
+    e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
+    e2e = {"value": whole_job_rate(w["units"], world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": w["h2d"],
            "d2h_bytes_per_step": w["d2h"], "ms_per_step": e2e_ms}
 
     # roofline of the dominant kernel
