@@ -9,6 +9,8 @@
  *                        and §3-5 (M = M^S . M^H, Log-Linear Mamba-2); computed
  *                        chunk-wise in O(T log T) as in §3-1 / the chunk-scan of
  *                        the gist.science (zh) summary §2.3.
+ *   ll_attn_fwd_cont     the forward of a segment of new tokens after a prefix held
+ *                        as decode states (prefill continuation), §3-4/§3-6.
  *   ll_attn_decode_step  one token of Fenwick-state decoding: study note §3-3
  *                        "Recurrent form" (o_t = sum_l lam_t^(l) q_t^T S_t^(l))
  *                        and §3-6 "Memory-efficient decoding"; carry/merge as in
@@ -152,6 +154,34 @@ LL_API ll_status ll_attn_fwd(const ll_shape* shape, const void* q, const void* k
 LL_API ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,
                               const void* q, const void* k, const void* v, const float* log_alpha,
                               const float* lam, float* states, float* scales, void* o, void* stream);
+
+/* Bytes of workspace ll_attn_fwd_cont needs (0 when the shape or t0 is
+ * invalid for a continuation). */
+LL_API size_t ll_attn_fwd_cont_workspace_size(const ll_shape* shape, long long t0);
+
+/* Prefill continuation: ll_attn_fwd for the tokens at positions t0 .. t0+T-1
+ * of a sequence whose first t0 tokens are carried by their decode states
+ * (study note §3-6: the O(log T) level states; the chunk-wise form of §3-4 /
+ * the gist.science (zh) summary §2.3 for the new tokens).
+ *   shape      as ll_attn_fwd for the T new tokens; shape->Ls >= bit_length(t0+T)
+ *              slots; shape->L >= bit_length(t0+T-1)+1 (lam indexes absolute levels)
+ *   t0         position of the first new token; must be a multiple of the
+ *              smallest power of two >= T (the new tokens sit in one aligned
+ *              block of positions, as fixed-size power-of-two segments do)
+ *   state_in   [B,H,Ls,dv,dk] float32, scale_in [B,H,Ls]: the decode states of
+ *              position t0 (as ll_attn_fwd exports them or ll_attn_decode_step
+ *              leaves them; true state = scale * S, decayed to t0-1)
+ *   q, k, v, log_alpha, lam, o: the new tokens, layouts of ll_attn_fwd
+ *   state_out, scale_out: nullable (both or neither); the decode states of
+ *              position t0+T; must not overlap state_in / scale_in
+ *   workspace  >= ll_attn_fwd_cont_workspace_size(shape, t0) bytes, 256-aligned
+ * o_t = sum over all keys s <= t (prefix included) of
+ *       (q_t . k_s) Gamma(t,s) lam_t[l(t,s)] v_s.
+ * Runs on the CUDA-core path for every io dtype and head size. */
+LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const float* state_in,
+                                  const float* scale_in, const void* q, const void* k, const void* v,
+                                  const float* log_alpha, const float* lam, void* o, float* state_out,
+                                  float* scale_out, void* workspace, size_t ws_bytes, void* stream);
 
 /* Size in bytes of the fixed device scratch of ll_attn_fwd_noalloc. */
 #define LL_NOALLOC_SCRATCH_BYTES (32u << 20)

@@ -25,7 +25,8 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 # every symbol the header declares
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
            "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
-           "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b")
+           "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b", "ll_attn_fwd_cont_workspace_size",
+           "ll_attn_fwd_cont")
 
 
 class LLError(RuntimeError):
@@ -75,6 +76,10 @@ def lib() -> ctypes.CDLL:
     L.ll_gdn_fwd_workspace_size.argtypes = [shp]
     L.ll_gdn_fwd.restype = i32
     L.ll_gdn_fwd.argtypes = [shp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+    L.ll_attn_fwd_cont_workspace_size.restype = sz
+    L.ll_attn_fwd_cont_workspace_size.argtypes = [shp, ctypes.c_longlong]
+    L.ll_attn_fwd_cont.restype = i32
+    L.ll_attn_fwd_cont.argtypes = [shp, ctypes.c_longlong, fp, fp, vp, vp, vp, fp, fp, vp, fp, fp, vp, sz, vp]
     L.ll_gdn_fwd_b_workspace_size.restype = sz
     L.ll_gdn_fwd_b_workspace_size.argtypes = [shp]
     L.ll_gdn_fwd_b.restype = i32
@@ -213,6 +218,37 @@ def ll_attn_decode_step(t, q, k, v, log_alpha, lam, states, scales, *, o=None):
     st = lib().ll_attn_decode_step(B, H, dk, dv, Ls, io, _ptr(t), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                    _ptr(lam), _ptr(states), _ptr(scales), _ptr(o), _stream(q.device))
     _check(st, "ll_attn_decode_step")
+    return o
+
+
+def ll_attn_fwd_cont_workspace_size(shape: ll_shape, t0: int) -> int:
+    return int(lib().ll_attn_fwd_cont_workspace_size(ctypes.byref(shape), int(t0)))
+
+
+def ll_attn_fwd_cont(t0: int, state_in, scale_in, q, k, v, log_alpha, lam, chunk: int, *, o=None, state_out=None,
+                     scale_out=None, workspace=None):
+    """Prefill continuation at position t0 (a multiple of the smallest power of
+    two >= T).  state_in [B,H,Ls,dv,dk] / scale_in [B,H,Ls]: the decode states
+    of position t0; q, k, v, log_alpha, lam: the T new tokens; optional
+    state_out / scale_out receive the states of position t0 + T.  Returns o."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    Ls = state_in.shape[2]
+    io = _io(q.dtype)
+    for x, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(x, n, q.dtype)
+    for x, n in ((log_alpha, "log_alpha"), (lam, "lam"), (state_in, "state_in"), (scale_in, "scale_in")):
+        _need(x, n, torch.float32)
+    shape = make_shape(B, H, T, dk, dv, L, chunk, Ls, io)
+    if o is None:
+        o = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(ll_attn_fwd_cont_workspace_size(shape, t0), q.device)
+    st = lib().ll_attn_fwd_cont(ctypes.byref(shape), int(t0), _ptr(state_in), _ptr(scale_in), _ptr(q), _ptr(k),
+                                _ptr(v), _ptr(log_alpha), _ptr(lam), _ptr(o), _ptr(state_out), _ptr(scale_out),
+                                _ptr(workspace), ctypes.c_size_t(workspace.numel()), _stream(q.device))
+    _check(st, "ll_attn_fwd_cont")
     return o
 
 

@@ -121,6 +121,61 @@ ll_status ll_attn_fwd(const ll_shape* s, const void* q, const void* k, const voi
   return tc ? fwd_tc_launch(a) : fwd_simt_launch(a);
 }
 
+// Shape conditions of a prefill continuation at position t0 (beyond check_shape).
+static ll_status check_cont(const ll_shape* s, long long t0) {
+  ll_status st = check_shape(s);
+  if (st != LL_OK) return st;
+  if (t0 < 0 || t0 > (1ll << 61)) return LL_ERR_INVALID_ARG;
+  const long long T = s->T, t1 = t0 + T;
+  long long P = 1;
+  while (P < T) P <<= 1;
+  if (t0 % P != 0) return LL_ERR_INVALID_ARG;  // the segment must sit in one aligned block
+  int bl = 0;
+  for (long long x = t1; x; x >>= 1) ++bl;
+  if (s->Ls < 1 || s->Ls < bl) return LL_ERR_INVALID_ARG;  // the levels of t1 need slots
+  int need = 1;
+  for (long long x = t1 - 1; x; x >>= 1) ++need;
+  if (s->L < need) return LL_ERR_INVALID_ARG;  // the segment's keys reach levels up to bitlen(t1 - 1)
+  return LL_OK;
+}
+
+size_t ll_attn_fwd_cont_workspace_size(const ll_shape* s, long long t0) {
+  if (check_cont(s, t0) != LL_OK) return 0;
+  return fwd_simt_cont_workspace(*s);
+}
+
+ll_status ll_attn_fwd_cont(const ll_shape* s, long long t0, const float* state_in, const float* scale_in,
+                           const void* q, const void* k, const void* v, const float* log_alpha, const float* lam,
+                           void* o, float* state_out, float* scale_out, void* workspace, size_t ws_bytes,
+                           void* stream) {
+  ll_status st = check_cont(s, t0);
+  if (st != LL_OK) return st;
+  if (!state_in || !scale_in || !q || !k || !v || !log_alpha || !lam || !o) return LL_ERR_INVALID_ARG;
+  if ((state_out == nullptr) != (scale_out == nullptr)) return LL_ERR_INVALID_ARG;
+  if (!aligned16(state_in) || !aligned16(scale_in) || !aligned16(q) || !aligned16(k) || !aligned16(v) ||
+      !aligned16(log_alpha) || !aligned16(lam) || !aligned16(o) || (state_out && !aligned16(state_out)) ||
+      (scale_out && !aligned16(scale_out)))
+    return LL_ERR_INVALID_ARG;
+  if (state_out) {  // the new states are written while the old ones are read
+    const size_t n = (size_t)s->B * s->H * s->Ls * s->dv * s->dk * sizeof(float);
+    const size_t ns = (size_t)s->B * s->H * s->Ls * sizeof(float);
+    const uintptr_t a0 = reinterpret_cast<uintptr_t>(state_in), a1 = reinterpret_cast<uintptr_t>(state_out);
+    const uintptr_t c0 = reinterpret_cast<uintptr_t>(scale_in), c1 = reinterpret_cast<uintptr_t>(scale_out);
+    if (a0 < a1 + n && a1 < a0 + n) return LL_ERR_INVALID_ARG;
+    if (c0 < c1 + ns && c1 < c0 + ns) return LL_ERR_INVALID_ARG;
+  }
+  const size_t need_ws = fwd_simt_cont_workspace(*s);
+  if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
+  FwdArgs a{*s, q, k, v, log_alpha, lam, nullptr, o, state_out, scale_out, workspace, ws_bytes,
+            static_cast<cudaStream_t>(stream), err_word()};
+  if (!a.err) return LL_ERR_CUDA;
+  a.t0 = t0;
+  a.state_in = state_in;
+  a.scale_in = scale_in;
+  return fwd_simt_launch(a);
+}
+
 ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
                               const void* k, const void* v, const float* log_alpha, const float* lam,
                               float* states, float* scales, void* o, void* stream) {

@@ -66,9 +66,15 @@ struct FwdArgs {
   size_t ws_bytes;
   cudaStream_t stream;
   unsigned* err;
+  // prefill continuation: the tokens are positions t0 .. t0+T-1 and the
+  // decode states of position t0 (state_in/scale_in, Ls slots) carry the prefix
+  long long t0 = 0;
+  const float* state_in = nullptr;
+  const float* scale_in = nullptr;
 };
 
 size_t fwd_simt_workspace(const ll_shape& s);
+size_t fwd_simt_cont_workspace(const ll_shape& s);
 ll_status fwd_simt_launch(const FwdArgs& a);
 int fwd_simt_launches(const ll_shape& s);
 

@@ -21,6 +21,21 @@
 //   (5) export  : the level states of position T are F nodes of the Fenwick
 //                 prefix query of N = T/Ce, decayed to token T-1.
 //
+// Prefill continuation (the tokens are positions t0 .. t0+T-1, the prefix
+// enters as the decode states of position t0, decayed to t0-1; t0 is a
+// multiple of the smallest power of two P >= T, so the segment sits inside
+// one aligned block of P positions):
+//   every prefix bucket of t0 has a level above log2(P), which for every
+//   query of the segment is the same level (a key's level only changes where
+//   the query differs from t0 above it), so (4) adds, per non-empty slot l,
+//   o_i += lam_i[l] g_l exp(cs_i + D) S_l q_i with D the decay of the whole
+//   segment before the chunk; the segment's own levels are those of the
+//   relative positions.
+//   (6) the states of t1 = t0 + T: with b = bitlen(t1 xor t0), a prefix
+//   bucket of level l goes to level max(l, b) (decayed over the segment), the
+//   segment's buckets (its export at T) keep their level if T < P and go to
+//   level b if T = P; buckets that land on one level add.
+//
 // Cumulative decays are kept in double: the inputs and outputs are float32 and
 // the exponent of a decay factor must not lose the absolute accuracy that a
 // float32 running sum would lose at long range.
@@ -42,6 +57,7 @@ constexpr int kMaxChunkElems = 8192;
 struct SimtPlan {
   int Ce, N, lc;  // effective chunk, #chunks, log2(Ce)
   size_t off_S, off_F, off_tot, off_G, off_O, total;
+  size_t off_segS, off_segSc, total_cont;  // the segment's own export (continuation)
 };
 
 SimtPlan plan_of(const ll_shape& s) {
@@ -61,6 +77,9 @@ SimtPlan plan_of(const ll_shape& s) {
   p.off_O = off;
   if (s.io != LL_F32) off = align_up(off + BH * (size_t)s.T * s.dv * sizeof(float), 256);
   p.total = off;
+  p.off_segS = off;  off = align_up(off + BH * (size_t)std::max(s.Ls, 1) * mat * sizeof(float), 256);
+  p.off_segSc = off; off = align_up(off + BH * (size_t)std::max(s.Ls, 1) * sizeof(float), 256);
+  p.total_cont = off;
   return p;
 }
 
@@ -181,7 +200,10 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
                                                               const float* o_intra,
                                                               const float* __restrict__ F,
                                                               const double* __restrict__ G, IO* o, int T,
-                                                              int dk, int dv, int L, int Ce, int lc) {
+                                                              int dk, int dv, int L, int Ce, int lc,
+                                                              const float* __restrict__ pre_states,
+                                                              const float* __restrict__ pre_scales, int Ls,
+                                                              long long t0) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   const int c = blockIdx.x;
   const int N = gridDim.x;
@@ -225,6 +247,24 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
     D += G[bh * N + e];
     __syncthreads();
   }
+  // continuation: the prefix levels of t0, one state each, decayed over D and cs
+  if (pre_states) {
+    for (int slot = 0; slot < Ls; ++slot) {
+      if (!((t0 >> slot) & 1)) continue;
+      const float* Pe = pre_states + (bh * Ls + slot) * mat;
+      const float g = pre_scales[bh * Ls + slot];
+      for (int x = tid; x < (int)mat; x += kThreads) Fs[(x / dk) * dkp + (x % dk)] = Pe[x];
+      for (int i = tid; i < Ce; i += kThreads) w[i] = lam[(row0 + i) * L + slot + 1] * g * expf((float)(cs[i] + D));
+      __syncthreads();
+      for (int x = tid; x < Ce * dv; x += kThreads) {
+        int i = x / dv, ev = x % dv;
+        float acc = 0.f;
+        for (int f = 0; f < dk; ++f) acc = fmaf(Fs[ev * dkp + f], qs[i * dk + f], acc);
+        Oc[x] = fmaf(w[i], acc, Oc[x]);
+      }
+      __syncthreads();
+    }
+  }
   for (int x = tid; x < Ce * dv; x += kThreads) o[row0 * dv + x] = from_f<IO>(Oc[x]);
 }
 
@@ -249,6 +289,43 @@ __global__ void __launch_bounds__(kThreads) simt_export_kernel(const float* __re
     if (idx < mat) state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
   }
+}
+
+// (6): the decode states of t1 = t0 + T from the prefix states of t0 and the
+// segment's own export at T (relative).  One thread per matrix element.
+__global__ void __launch_bounds__(kThreads) simt_cont_export_kernel(
+    const float* __restrict__ pre_states, const float* __restrict__ pre_scales, const float* __restrict__ seg_states,
+    const float* __restrict__ seg_scales, const double* __restrict__ tot, float* __restrict__ state_out,
+    float* __restrict__ scale_out, int N, int mat, int Ls, long long t0, long long T) {
+  __shared__ float seg_decay;
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  if (threadIdx.x == 0) {
+    double g = 0.0;
+    for (int i = 0; i < N; ++i) g += tot[bh * N + i];
+    seg_decay = expf((float)g);
+  }
+  __syncthreads();
+  const long long t1 = t0 + T;
+  const int b = 64 - __clzll(t1 ^ t0);                 // bitlen(t1 xor t0)
+  const long long P = 1ll << (64 - __clzll(T - 1));  // smallest power of two >= T
+  if (idx < mat) {
+    for (int slot = 0; slot < Ls; ++slot) state_out[(bh * Ls + slot) * (size_t)mat + idx] = 0.f;
+    for (int slot = 0; slot < Ls; ++slot) {
+      if ((t0 >> slot) & 1) {  // prefix level slot+1
+        const int tgt = (slot + 1 > b ? slot + 1 : b) - 1;
+        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
+            pre_scales[bh * Ls + slot] * seg_decay * pre_states[(bh * Ls + slot) * (size_t)mat + idx];
+      }
+      if ((T >> slot) & 1) {   // segment level slot+1
+        const int tgt = (T < P ? slot + 1 : b) - 1;
+        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
+            seg_scales[bh * Ls + slot] * seg_states[(bh * Ls + slot) * (size_t)mat + idx];
+      }
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int slot = 0; slot < Ls; ++slot) scale_out[bh * Ls + slot] = ((t1 >> slot) & 1) ? 1.f : 0.f;
 }
 
 template <typename IO>
@@ -284,10 +361,20 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
   LL_CUDA_OK(cudaFuncSetAttribute(simt_inter_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
   simt_inter_kernel<IO><<<dim3(p.N, BH), kThreads, sm3, a.stream>>>(static_cast<const IO*>(a.q), a.log_alpha,
                                                                      a.lam, o_intra, F, G, static_cast<IO*>(a.o), s.T,
-                                                                     s.dk, s.dv, s.L, Ce, p.lc);
+                                                                     s.dk, s.dv, s.L, Ce, p.lc, a.state_in, a.scale_in,
+                                                                     s.Ls, a.t0);
   LL_CUDA_OK(cudaGetLastError());
 
-  if (a.state_out) {
+  if (a.state_out && a.state_in) {
+    float* segS = reinterpret_cast<float*>(ws + p.off_segS);
+    float* segSc = reinterpret_cast<float*>(ws + p.off_segSc);
+    simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
+        F, G, segS, segSc, p.N, mat, s.Ls, p.lc);
+    LL_CUDA_OK(cudaGetLastError());
+    simt_cont_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
+        a.state_in, a.scale_in, segS, segSc, tot, a.state_out, a.scale_out, p.N, mat, s.Ls, a.t0, s.T);
+    LL_CUDA_OK(cudaGetLastError());
+  } else if (a.state_out) {
     simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
         F, G, a.state_out, a.scale_out, p.N, mat, s.Ls, p.lc);
     LL_CUDA_OK(cudaGetLastError());
@@ -299,11 +386,13 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 
 size_t fwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
 
+size_t fwd_simt_cont_workspace(const ll_shape& s) { return plan_of(s).total_cont; }
+
 int fwd_simt_launches(const ll_shape& s) { return s.Ls > 0 ? 4 : 3; }
 
 ll_status fwd_simt_launch(const FwdArgs& a) {
   SimtPlan p = plan_of(a.s);
-  if (a.ws_bytes < p.total) return LL_ERR_WORKSPACE;
+  if (a.ws_bytes < (a.state_in ? p.total_cont : p.total)) return LL_ERR_WORKSPACE;
   if (a.s.io == LL_F32) return launch_typed<float>(a, p);
   return launch_typed<__nv_bfloat16>(a, p);
 }

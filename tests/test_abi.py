@@ -100,6 +100,27 @@ def test_decode_rejects_bad_args_on_host(L):
     assert L.ll_attn_decode_step(1, 1, 16, 16, 4, 0, *bad) == 1
 
 
+def test_cont_rejects_bad_args_on_host(L):
+    from log_linear_attention_chunked_gb300 import binding
+    vp = ctypes.c_void_p
+    ok = _shape(T=64, L=12, Ls=10)                                       # t0 = 512: t1 = 576, bitlen 10
+    assert L.ll_attn_fwd_cont_workspace_size(ctypes.byref(ok), 512) > 0
+    assert L.ll_attn_fwd_cont_workspace_size(ctypes.byref(ok), 96) == 0   # 96 is not a multiple of 64
+    assert L.ll_attn_fwd_cont_workspace_size(ctypes.byref(ok), -64) == 0
+    assert L.ll_attn_fwd_cont_workspace_size(ctypes.byref(_shape(T=64, L=12, Ls=9)), 512) == 0  # slots
+    assert L.ll_attn_fwd_cont_workspace_size(ctypes.byref(_shape(T=64, L=10, Ls=10)), 512) == 0  # levels
+    args = [vp(FAKE)] * 10  # state_in, scale_in, q, k, v, log_alpha, lam, o, state_out, scale_out
+    for i in range(8):      # every required tensor
+        bad = list(args)
+        bad[i] = None
+        assert L.ll_attn_fwd_cont(ctypes.byref(ok), 512, *bad, vp(FAKE), ctypes.c_size_t(1 << 40), None) == 1, i
+    bad = list(args)
+    bad[9] = None           # state_out without scale_out
+    assert L.ll_attn_fwd_cont(ctypes.byref(ok), 512, *bad, vp(FAKE), ctypes.c_size_t(1 << 40), None) == 1
+    same = list(args)       # state_out overlapping state_in
+    assert L.ll_attn_fwd_cont(ctypes.byref(ok), 512, *same, vp(FAKE), ctypes.c_size_t(1 << 40), None) == 1
+
+
 def test_gdn_b_rejects_bad_args_on_host(L):
     vp = ctypes.c_void_p
     s = _shape(Ls=3)
