@@ -177,7 +177,9 @@ LL_API size_t ll_attn_fwd_cont_workspace_size(const ll_shape* shape, long long t
  *   workspace  >= ll_attn_fwd_cont_workspace_size(shape, t0) bytes, 256-aligned
  * o_t = sum over all keys s <= t (prefix included) of
  *       (q_t . k_s) Gamma(t,s) lam_t[l(t,s)] v_s.
- * Runs on the CUDA-core path for every io dtype and head size. */
+ * bf16 io with d = 128 and T a multiple of 128 runs on the tensor-core path
+ * (the prefix levels become extra level products of every tile), every other
+ * shape on the CUDA-core path. */
 LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const float* state_in,
                                   const float* scale_in, const void* q, const void* k, const void* v,
                                   const float* log_alpha, const float* lam, void* o, float* state_out,

@@ -141,7 +141,7 @@ static ll_status check_cont(const ll_shape* s, long long t0) {
 
 size_t ll_attn_fwd_cont_workspace_size(const ll_shape* s, long long t0) {
   if (check_cont(s, t0) != LL_OK) return 0;
-  return fwd_simt_cont_workspace(*s);
+  return fwd_tc_cont_supported(*s, t0) ? fwd_tc_cont_workspace(*s) : fwd_simt_cont_workspace(*s);
 }
 
 ll_status ll_attn_fwd_cont(const ll_shape* s, long long t0, const float* state_in, const float* scale_in,
@@ -164,7 +164,8 @@ ll_status ll_attn_fwd_cont(const ll_shape* s, long long t0, const float* state_i
     if (a0 < a1 + n && a1 < a0 + n) return LL_ERR_INVALID_ARG;
     if (c0 < c1 + ns && c1 < c0 + ns) return LL_ERR_INVALID_ARG;
   }
-  const size_t need_ws = fwd_simt_cont_workspace(*s);
+  const bool tc = fwd_tc_cont_supported(*s, t0);
+  const size_t need_ws = tc ? fwd_tc_cont_workspace(*s) : fwd_simt_cont_workspace(*s);
   if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
   FwdArgs a{*s, q, k, v, log_alpha, lam, nullptr, o, state_out, scale_out, workspace, ws_bytes,
@@ -173,7 +174,7 @@ ll_status ll_attn_fwd_cont(const ll_shape* s, long long t0, const float* state_i
   a.t0 = t0;
   a.state_in = state_in;
   a.scale_in = scale_in;
-  return fwd_simt_launch(a);
+  return tc ? fwd_tc_launch(a) : fwd_simt_launch(a);
 }
 
 ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,

@@ -291,43 +291,6 @@ __global__ void __launch_bounds__(kThreads) simt_export_kernel(const float* __re
   }
 }
 
-// (6): the decode states of t1 = t0 + T from the prefix states of t0 and the
-// segment's own export at T (relative).  One thread per matrix element.
-__global__ void __launch_bounds__(kThreads) simt_cont_export_kernel(
-    const float* __restrict__ pre_states, const float* __restrict__ pre_scales, const float* __restrict__ seg_states,
-    const float* __restrict__ seg_scales, const double* __restrict__ tot, float* __restrict__ state_out,
-    float* __restrict__ scale_out, int N, int mat, int Ls, long long t0, long long T) {
-  __shared__ float seg_decay;
-  const size_t bh = blockIdx.y;
-  const int idx = blockIdx.x * kThreads + threadIdx.x;
-  if (threadIdx.x == 0) {
-    double g = 0.0;
-    for (int i = 0; i < N; ++i) g += tot[bh * N + i];
-    seg_decay = expf((float)g);
-  }
-  __syncthreads();
-  const long long t1 = t0 + T;
-  const int b = 64 - __clzll(t1 ^ t0);                 // bitlen(t1 xor t0)
-  const long long P = 1ll << (64 - __clzll(T - 1));  // smallest power of two >= T
-  if (idx < mat) {
-    for (int slot = 0; slot < Ls; ++slot) state_out[(bh * Ls + slot) * (size_t)mat + idx] = 0.f;
-    for (int slot = 0; slot < Ls; ++slot) {
-      if ((t0 >> slot) & 1) {  // prefix level slot+1
-        const int tgt = (slot + 1 > b ? slot + 1 : b) - 1;
-        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
-            pre_scales[bh * Ls + slot] * seg_decay * pre_states[(bh * Ls + slot) * (size_t)mat + idx];
-      }
-      if ((T >> slot) & 1) {   // segment level slot+1
-        const int tgt = (T < P ? slot + 1 : b) - 1;
-        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
-            seg_scales[bh * Ls + slot] * seg_states[(bh * Ls + slot) * (size_t)mat + idx];
-      }
-    }
-  }
-  if (blockIdx.x == 0 && threadIdx.x == 0)
-    for (int slot = 0; slot < Ls; ++slot) scale_out[bh * Ls + slot] = ((t1 >> slot) & 1) ? 1.f : 0.f;
-}
-
 template <typename IO>
 ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
   const ll_shape& s = a.s;
@@ -371,9 +334,9 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
     simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
         F, G, segS, segSc, p.N, mat, s.Ls, p.lc);
     LL_CUDA_OK(cudaGetLastError());
-    simt_cont_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
-        a.state_in, a.scale_in, segS, segSc, tot, a.state_out, a.scale_out, p.N, mat, s.Ls, a.t0, s.T);
-    LL_CUDA_OK(cudaGetLastError());
+    const ll_status st = cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha, a.state_out,
+                                            a.scale_out, BH, s.T, mat, s.Ls, a.t0, a.stream);
+    if (st != LL_OK) return st;
   } else if (a.state_out) {
     simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
         F, G, a.state_out, a.scale_out, p.N, mat, s.Ls, p.lc);
@@ -395,6 +358,57 @@ ll_status fwd_simt_launch(const FwdArgs& a) {
   if (a.ws_bytes < (a.state_in ? p.total_cont : p.total)) return LL_ERR_WORKSPACE;
   if (a.s.io == LL_F32) return launch_typed<float>(a, p);
   return launch_typed<__nv_bfloat16>(a, p);
+}
+
+// (6): the decode states of t1 = t0 + T from the prefix states of t0 and the
+// segment's own export at T (relative); shared by both forward paths.  One
+// thread per matrix element; the segment's total decay is a block sum of its
+// log_alpha.
+__global__ void __launch_bounds__(kThreads) cont_export_kernel(
+    const float* __restrict__ pre_states, const float* __restrict__ pre_scales, const float* __restrict__ seg_states,
+    const float* __restrict__ seg_scales, const float* __restrict__ log_alpha, float* __restrict__ state_out,
+    float* __restrict__ scale_out, int T, int mat, int Ls, long long t0) {
+  __shared__ double part[kThreads];
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  double g = 0.0;
+  for (int i = threadIdx.x; i < T; i += kThreads) g += (double)log_alpha[bh * T + i];
+  part[threadIdx.x] = g;
+  __syncthreads();
+  for (int o = kThreads / 2; o > 0; o >>= 1) {
+    if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
+    __syncthreads();
+  }
+  const float seg_decay = expf((float)part[0]);
+  const long long t1 = t0 + T;
+  const int b = 64 - __clzll(t1 ^ t0);                         // bitlen(t1 xor t0)
+  const long long P = 1ll << (64 - __clzll((long long)T - 1));  // smallest power of two >= T
+  if (idx < mat) {
+    for (int slot = 0; slot < Ls; ++slot) state_out[(bh * Ls + slot) * (size_t)mat + idx] = 0.f;
+    for (int slot = 0; slot < Ls; ++slot) {
+      if ((t0 >> slot) & 1) {  // prefix level slot+1
+        const int tgt = (slot + 1 > b ? slot + 1 : b) - 1;
+        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
+            pre_scales[bh * Ls + slot] * seg_decay * pre_states[(bh * Ls + slot) * (size_t)mat + idx];
+      }
+      if ((T >> slot) & 1) {   // segment level slot+1
+        const int tgt = (T < P ? slot + 1 : b) - 1;
+        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
+            seg_scales[bh * Ls + slot] * seg_states[(bh * Ls + slot) * (size_t)mat + idx];
+      }
+    }
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int slot = 0; slot < Ls; ++slot) scale_out[bh * Ls + slot] = ((t1 >> slot) & 1) ? 1.f : 0.f;
+}
+
+ll_status cont_export_launch(const float* pre_states, const float* pre_scales, const float* seg_states,
+                             const float* seg_scales, const float* log_alpha, float* state_out, float* scale_out,
+                             int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream) {
+  cont_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, stream>>>(
+      pre_states, pre_scales, seg_states, seg_scales, log_alpha, state_out, scale_out, T, mat, Ls, t0);
+  LL_CUDA_OK(cudaGetLastError());
+  return LL_OK;
 }
 
 }  // namespace llattn

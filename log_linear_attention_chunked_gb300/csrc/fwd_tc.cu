@@ -130,6 +130,10 @@ struct TcParams {
   uint64_t* abort_word;
   uint32_t token;    // per call, never 0
   int BH, T, Nt, L;
+  // prefill continuation: absolute index of the first tile (a multiple of the
+  // smallest power of two >= Nt, so its set bits lie above every tile's own);
+  // its levels read the prefix nodes at F[BH * Nt + bh * kPreSlots + h]
+  int c0t;
   unsigned* err;
 };
 
@@ -231,6 +235,9 @@ __device__ __forceinline__ float ex2(float x) {
 
 __device__ __forceinline__ int node_of_level(int j, int h) { return ((j >> (h + 1)) << (h + 1)) + (1 << h) - 1; }
 
+// prefix nodes (continuation) per head: one per tile height
+constexpr int kPreSlots = 16;
+
 // Number of tiles CTA blockIdx.x processes (blockIdx.x < total).
 __device__ __forceinline__ int tiles_of_cta(int total) { return (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1; }
 
@@ -315,13 +322,23 @@ __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
     st_release_cta_u32(nlr + (it & 1), (uint32_t)it << 8);
     float D = 0.f;
     uint32_t l = 0;
-    for (int h = 0; (jp >> h) != 0 && !*c.abort_s; ++h) {
-      if (!((jp >> h) & 1)) continue;
-      const size_t node = (size_t)bhp * p.Nt + node_of_level(jp, h);
-      const uint64_t w = wait_flag(c, p.flags, node);
-      fence_proxy_async_global();
+    const int ja = jp | p.c0t;  // absolute tile index: the segment's bits, then the start tile's
+    for (int h = 0; (ja >> h) != 0 && !*c.abort_s; ++h) {
+      if (!((ja >> h) & 1)) continue;
+      // a prefix level (continuation) holds the prefix bucket, decayed to the
+      // segment start and written before this kernel: no word to wait for,
+      // and every later prefix level shares the same decay D
+      const bool pre = !((jp >> h) & 1);
+      const size_t node = pre ? (size_t)p.BH * p.Nt + (size_t)bhp * kPreSlots + h
+                              : (size_t)bhp * p.Nt + node_of_level(jp, h);
+      float g = 0.f;
+      if (!pre) {
+        const uint64_t w = wait_flag(c, p.flags, node);
+        fence_proxy_async_global();
+        g = flag_g(w);
+      }
       dl[16 * (it & 1) + l] = D;
-      D += flag_g(w);
+      D += g;
       st_release_cta_u32(nlr + (it & 1), ((uint32_t)it << 8) | ++l);
       const int fs = fcnt & 1;
       if (fcnt >= 2) wait_bar(c, B_F_FREE0 + fs, ((fcnt - 2) >> 1) & 1);
@@ -443,7 +460,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   for (int it = 0; it <= n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     const int j = it < n ? u / p.BH : 0;
-    const int nlev_p = it >= 1 ? __popc(jp) : 0;
+    const int nlev_p = it >= 1 ? __popc(jp | p.c0t) : 0;
     const uint32_t tR = tmem + kTmR0 + (it & 1) * 128;
     if (it < n) {
       // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
@@ -554,8 +571,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
 #pragma unroll
       for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
       if (it + 1 < n) fetch(u + gridDim.x);
-      if (it >= 1 && jp != 0)  // the previous tile's first level lambda, ahead of its back half
-        lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jp) - 1));
+      if (it >= 1 && (jp | p.c0t) != 0)  // the previous tile's first level lambda, ahead of its back half
+        lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jp | p.c0t) - 1));
 
       // inclusive cumsum of log_alpha over the tile
       float x = la;
@@ -711,7 +728,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // ================= back half of tile it-1: inter-tile levels + output
       const size_t rp = (size_t)bhp * p.T + (size_t)jp * kTile + row;
       // (the CTA's last tile has no front half after it to load this in)
-      if (it == n && jp != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp) - 1));
+      if (it == n && (jp | p.c0t) != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp | p.c0t) - 1));
       // log decays of the levels, handed over one by one by the level producer
       // under a step-tagged count; bounded wait until it covers `cnt` levels
       const uint32_t* nlr = reinterpret_cast<const uint32_t*>(s + kOffNode + 160) + (it & 1);
@@ -739,7 +756,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // inter-tile levels: Q'_l = lam_t[8 + h] exp(cs_t + D_l) Q_t goes to TMEM
       // as the A operand of a product the MMA accumulates onto the output
       int l = 0;
-      for (int rem = jp; rem != 0; ++l) {
+      for (int rem = jp | p.c0t; rem != 0; ++l) {
         rem &= rem - 1;
         const float lam_h = lam_c;
         // the next level's lambda loads while this level is written
@@ -961,6 +978,23 @@ __global__ void __launch_bounds__(kThreads, 1)
 }
 
 // Level states of position T read from the Fenwick nodes (float32, decayed to T-1).
+// Continuation: the prefix states of position t0 (true state = scale * S,
+// decayed to t0 - 1) as bf16 nodes, one per tile height h (level 8 + h).
+__global__ void __launch_bounds__(256) tc_prefix_nodes_kernel(const float* __restrict__ state_in,
+                                                              const float* __restrict__ scale_in,
+                                                              __nv_bfloat16* __restrict__ F, int BH, int Nt, int Ls,
+                                                              long long t0) {
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  constexpr int mat = kD * kD;
+  for (int slot = 7; slot < Ls; ++slot) {  // levels 8 .. Ls (t0 is a multiple of the tile: no lower ones)
+    if (!((t0 >> slot) & 1)) continue;
+    const int h = slot + 1 - 8;              // tile height: bit h of t0 / 128
+    const size_t node = (size_t)BH * Nt + bh * kPreSlots + h;
+    F[node * mat + idx] = __float2bfloat16_rn(scale_in[bh * Ls + slot] * state_in[(bh * Ls + slot) * (size_t)mat + idx]);
+  }
+}
+
 __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __restrict__ F,
                                                         const float* __restrict__ G, float* __restrict__ state_out,
                                                         float* __restrict__ scale_out, int Nt, int Ls) {
@@ -986,19 +1020,27 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
 struct TcPlan {
   int Nt;
   size_t off_F, off_R, off_G, off_flags, off_rflags, total;
+  size_t off_segS, off_segSc, total_cont;  // the segment's own export (continuation)
 };
 
+// F holds the tiles' nodes, then kPreSlots prefix nodes per head (used by a
+// continuation only, always reserved so one layout serves both)
 TcPlan tc_plan(const ll_shape& s) {
   TcPlan p{};
   p.Nt = s.T / kTile;
-  const size_t nodes = (size_t)s.B * s.H * p.Nt;
+  const size_t BH = (size_t)s.B * s.H;
+  const size_t nodes = BH * p.Nt;
   size_t off = 0;
-  p.off_F = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
+  p.off_F = off;      off = align_up(off + (nodes + BH * kPreSlots) * kD * kD * 2, 1024);
   p.off_R = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
   p.off_G = off;      off = align_up(off + nodes * 4, 256);
   p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
   p.off_rflags = off; off = align_up(off + nodes * 8, 256);
   p.total = off;
+  const size_t slots = (size_t)std::max(s.Ls, 1);
+  p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
+  p.off_segSc = off;  off = align_up(off + BH * slots * 4, 256);
+  p.total_cont = off;
   return p;
 }
 
@@ -1042,8 +1084,17 @@ uint32_t next_token() {
 
 bool fwd_tc_supported(const ll_shape& s) {
   return s.io == LL_BF16 && s.dk == kD && s.dv == kD && s.T % kTile == 0 && s.L <= kLmax &&
-         (long long)s.B * s.H * s.T <= (1ll << 31) - 1;
+         (long long)s.B * s.H * (s.T + kPreSlots * kTile) <= (1ll << 31) - 1;
 }
+
+// A continuation at t0 (already checked: t0 a multiple of the smallest power
+// of two >= T) on this path: every prefix level must have a node slot and
+// every tile at most 16 levels, which L <= kLmax gives.
+bool fwd_tc_cont_supported(const ll_shape& s, long long t0) {
+  return fwd_tc_supported(s) && t0 / kTile < (1ll << 30) && s.Ls <= 7 + kPreSlots;
+}
+
+size_t fwd_tc_cont_workspace(const ll_shape& s) { return tc_plan(s).total_cont; }
 
 size_t fwd_tc_workspace(const ll_shape& s) { return tc_plan(s).total; }
 
@@ -1052,11 +1103,11 @@ int fwd_tc_launches(const ll_shape& s) { return s.Ls > 0 ? 2 : 1; }
 ll_status fwd_tc_launch(const FwdArgs& a) {
   const ll_shape& s = a.s;
   const TcPlan plan = tc_plan(s);
-  if (a.ws_bytes < plan.total) return LL_ERR_WORKSPACE;
+  if (a.ws_bytes < (a.state_in ? plan.total_cont : plan.total)) return LL_ERR_WORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(a.ws);
   const int BH = s.B * s.H;
   const uint64_t rows = (uint64_t)BH * s.T;
-  const uint64_t node_rows = (uint64_t)BH * plan.Nt * kD;
+  const uint64_t node_rows = ((uint64_t)BH * plan.Nt + (uint64_t)BH * kPreSlots) * kD;
   CUtensorMap tq, tk, tv, tf, to, tr;
   if (!make_map(&tq, a.q, rows) || !make_map(&tk, a.k, rows) || !make_map(&tv, a.v, rows) ||
       !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows) ||
@@ -1080,6 +1131,12 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.Nt = plan.Nt;
   p.L = s.L;
   p.err = a.err;
+  p.c0t = a.state_in ? (int)(a.t0 / kTile) : 0;
+  if (a.state_in) {
+    tc_prefix_nodes_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(a.state_in, a.scale_in, p.F, BH, plan.Nt,
+                                                                         s.Ls, a.t0);
+    LL_CUDA_OK(cudaGetLastError());
+  }
 
   int dev = 0, sms = 0, per_sm = 0;
   LL_CUDA_OK(cudaGetDevice(&dev));
@@ -1093,6 +1150,14 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   void* args[] = {&tq, &tk, &tv, &tf, &to, &tr, &p};
   LL_CUDA_OK(cudaLaunchCooperativeKernel((const void*)fwd_tc_kernel, dim3(grid), dim3(kThreads), args, kSmemBytes,
                                          a.stream));
+  if (a.state_out && a.state_in) {
+    float* segS = reinterpret_cast<float*>(ws + plan.off_segS);
+    float* segSc = reinterpret_cast<float*>(ws + plan.off_segSc);
+    tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, segS, segSc, plan.Nt, s.Ls);
+    LL_CUDA_OK(cudaGetLastError());
+    return cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha, a.state_out, a.scale_out, BH, s.T,
+                              kD * kD, s.Ls, a.t0, a.stream);
+  }
   if (a.state_out) {
     tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, a.state_out, a.scale_out, plan.Nt,
                                                                    s.Ls);

@@ -65,7 +65,11 @@ def _cont(B, inp, t0, T, Ls, chunk, S0, sc0):
     ("f32", 64, 128, 1024, 64),
     ("f32", 32, 128, 0, 32),       # no prefix
     ("bf16", 64, 256, 1792, 64),   # three prefix buckets
-    ("bf16", 128, 512, 1536, 128),
+    ("bf16", 128, 512, 1536, 128),   # from here on the tensor-core path (bf16, d = 128)
+    ("bf16", 128, 128, 128, 64),     # prefix bucket at the first tile level
+    ("bf16", 128, 256, 768, 64),     # two prefix buckets, the segment closes its block
+    ("bf16", 128, 384, 3584, 64),    # T < P, three prefix buckets
+    ("bf16", 128, 1024, 3072, 128),  # eight tiles per head
 ])
 def test_matches_dense_rows(B, io, d, T, t0, chunk):
     inp, Ls = _inputs(io, d, T, t0, f"c{io}{d}{T}{t0}")
@@ -113,3 +117,32 @@ def test_refuses_unaligned_start(B):
     shape = B.make_shape(1, 1, 256, 32, 32, 12, 32, 11, 0)
     assert B.ll_attn_fwd_cont_workspace_size(shape, 768) > 0
     assert B.ll_attn_fwd_cont_workspace_size(shape, 640) == 0   # 640 is not a multiple of 256
+
+
+def test_chained_segments_tensor_cores(B):
+    """bf16, d = 128: a 1024-token prefix by ll_attn_fwd (tensor cores, with
+    state export), then two 512-token continuations on the tensor-core path."""
+    dev = torch.device("cuda")
+    d, t0, T = 128, 1024, 512
+    inp, Ls = _inputs("bf16", d, 2 * T, t0, "chaintc")
+    g = {n: inp[n].to(dev) for n in ("q", "k", "v", "log_alpha", "lam")}
+    Bn, H = g["q"].shape[:2]
+    st = torch.empty(Bn, H, Ls, d, d, device=dev)
+    sc = torch.empty(Bn, H, Ls, device=dev)
+    cut = lambda x, a, b: x[:, :, a:b].contiguous()
+    B.ll_attn_fwd(*(cut(g[n], 0, t0) for n in ("q", "k", "v", "log_alpha", "lam")), 64, state_out=st, scale_out=sc)
+    outs = []
+    for seg in range(2):
+        a = t0 + seg * T
+        st2, sc2 = torch.empty_like(st), torch.empty_like(sc)
+        outs.append(B.ll_attn_fwd_cont(a, st, sc, *(cut(g[n], a, a + T) for n in ("q", "k", "v", "log_alpha", "lam")),
+                                       64, state_out=st2, scale_out=sc2).float().cpu().numpy())
+        st, sc = st2, sc2
+    assert B.ll_last_device_error() == 0
+    f = {n: synth.to_f64(inp[n]) for n in ("q", "k", "v", "log_alpha", "lam")}
+    full = mamba2.forward_dense_bh(f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+    assert rel_err(np.concatenate(outs, 2), full[:, :, t0:]) <= TOL_BF16
+    want = _prefix_states(f, t0 + 2 * T, Ls)
+    ne = [((t0 + 2 * T) >> i) & 1 == 1 for i in range(Ls)]
+    true = (st * sc[..., None, None]).cpu().numpy()
+    assert rel_err(true[:, :, ne], want[:, :, ne]) <= TOL_BF16
