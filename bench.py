@@ -45,6 +45,8 @@ METRICS = {
     "decode": "log-linear Mamba-2 Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); % of HBM roofline",
     "gdn": "log-linear Gated DeltaNet fwd tokens/s (B=2, H=16, T=4096, d=128)",
     "gdn_b": "log-linear Gated DeltaNet fwd, reading B, tokens/s (B=2, H=16, T=4096, d=128)",
+    "mamba2_cont": "log-linear Mamba-2 prefill continuation tokens/s (16K new tokens at 49152, H=16, d=128); "
+                   "% of roofline",
     "gdn_decode": "log-linear Gated DeltaNet Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); "
                   "% of HBM roofline",
 }
@@ -60,6 +62,9 @@ def algorithmic_bytes(cfg) -> int:
     per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
     if cfg["kind"] in ("gdn", "gdn_b"):
         per_bh += cfg["T"] * 4
+    if cfg["kind"] == "mamba2_cont":  # the prefix states read, the states of t0 + T written (float32)
+        t0, t1, d = cfg["t0"], cfg["t0"] + cfg["T"], cfg["dk"]
+        per_bh += (bin(t0).count("1") + bin(t1).count("1")) * d * d * 4 + 2 * cfg["Ls"] * 4
     return per_bh * cfg["B"] * cfg["H"]
 
 
@@ -79,6 +84,8 @@ def algorithmic_flops(cfg) -> int:
         per_bh = N * per_chunk + 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
     else:
         per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
+        if cfg["kind"] == "mamba2_cont":  # every token also reads the prefix levels
+            per_bh += 2 * d * d * T * bin(cfg["t0"]).count("1")
     return per_bh * cfg["B"] * cfg["H"]
 
 
@@ -115,6 +122,7 @@ KERNEL_SOURCES = {
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
     "gdn_b": ("gdn.cu", "fwd_tc.cu", "common.cuh", "sm100.cuh"),
+    "mamba2_cont": ("fwd_tc.cu", "fwd_simt.cu", "common.cuh", "sm100.cuh"),
 }
 
 
@@ -212,6 +220,8 @@ def _oracle_init(cfg, tag):
         _W["x"] = (rng.standard_normal((cfg["Ls"], cfg["dv"], cfg["dk"])) * 0.05,) + tuple(
             synth.to_f64(dec[n][:, 0, 0]) for n in ("q", "k", "v", "log_alpha", "beta", "lam"))
         return
+    if cfg["kind"] == "mamba2_cont":  # the whole sequence: the oracle has no prefix states
+        cfg = dict(cfg, kind="mamba2", T=cfg["t0"] + cfg["T"])
     inp = synth.make_inputs(dict(cfg, B=1, H=1), tag=tag)
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] in ("gdn", "gdn_b") else ())
     _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in names)
@@ -220,7 +230,7 @@ def _oracle_init(cfg, tag):
 def _oracle_worker(job):
     """One bounded piece of oracle work; returns the number of tokens it covered."""
     cfg = _W["cfg"]
-    if cfg["kind"] == "mamba2":
+    if cfg["kind"] in ("mamba2", "mamba2_cont"):
         from oracle import mamba2
         q, k, v, la, lam = _W["x"]
         mamba2.forward_rows(q, k, v, la, lam, job)
@@ -274,6 +284,8 @@ def oracle_jobs(cfg, cores, size, seed):
     rng = np.random.default_rng(seed)
     if cfg["kind"] in ("mamba2", "gdn"):
         return [sorted(int(x) for x in rng.integers(0, cfg["T"], size)) for _ in range(cores)]
+    if cfg["kind"] == "mamba2_cont":  # rows of the new tokens, positions t0 .. t0 + T - 1
+        return [sorted(int(x) for x in rng.integers(cfg["t0"], cfg["t0"] + cfg["T"], size)) for _ in range(cores)]
     return [size for _ in range(cores)]
 
 
@@ -297,6 +309,9 @@ def calibrate(pool, cfg, cores, budget_s):
 def sample_desc(cfg, size):
     if cfg["kind"] == "mamba2":
         return f"{size} uniformly drawn query rows per process of the row-restricted dense float64 form"
+    if cfg["kind"] == "mamba2_cont":
+        return (f"{size} uniformly drawn rows of the new tokens per process of the row-restricted dense float64 "
+                "form over the whole sequence")
     if cfg["kind"] == "gdn":
         return (f"{size} uniformly drawn query rows per process of the row-restricted float64 reading-A form "
                 "(each call builds its unit-triangular system)")
@@ -334,6 +349,7 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     """Forward (Mamba-2 or Gated DeltaNet): device and pinned host inputs, step functions."""
     gdn = cfg["kind"] in ("gdn", "gdn_b")
     reading_b = cfg["kind"] == "gdn_b"
+    cont = cfg["kind"] == "mamba2_cont"
     inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if gdn else ())
     host = {n: inp_host[n].pin_memory() for n in names}
@@ -341,7 +357,18 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     Bn, H, T, dk = g["q"].shape
     dv = g["v"].shape[-1]
     shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], 0, binding._io(g["q"].dtype))
-    if reading_b:
+    if cont:
+        t0, Ls = cfg["t0"], cfg["Ls"]
+        shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], Ls, binding._io(g["q"].dtype))
+        ws = binding.alloc_workspace(binding.ll_attn_fwd_cont_workspace_size(shape, t0), dev)
+        gen = torch.Generator(device=dev)
+        gen.manual_seed(cfg["seed"] + 17 + rank)
+        keep = torch.tensor([float((t0 >> i) & 1) for i in range(Ls)], device=dev)
+        st_in = torch.randn(Bn, H, Ls, dv, dk, device=dev, generator=gen) * 0.01 * keep[None, None, :, None, None]
+        sc_in = keep.expand(Bn, H, Ls).contiguous()
+        st_out, sc_out = torch.empty_like(st_in), torch.empty_like(sc_in)
+        launches = 5  # prefix nodes, forward, segment export, segment decay, merge
+    elif reading_b:
         ws = binding.alloc_workspace(binding.ll_gdn_fwd_b_workspace_size(shape), dev)
         launches = 2 + binding.ll_attn_fwd_launches(shape)
     elif gdn:
@@ -354,7 +381,10 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
 
     def step(i=0):
-        if reading_b:
+        if cont:
+            binding.ll_attn_fwd_cont(t0, st_in, sc_in, g["q"], g["k"], g["v"], g["log_alpha"], g["lam"],
+                                     cfg["chunk"], o=o, state_out=st_out, scale_out=sc_out, workspace=ws)
+        elif reading_b:
             binding.ll_gdn_fwd_b(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
                                  workspace=ws)
         elif gdn:
@@ -455,6 +485,9 @@ def main():
     if kind in ("decode", "gdn_decode"):
         config.update(Ls=cfg["Ls"], positions=f"{cfg['T']}..{cfg['T'] + cfg['steps'] - 1} cycled",
                       l2="states (2.3 GB) larger than L2, no flush")
+    elif kind == "mamba2_cont":
+        config.update(t0=cfg["t0"], Ls=cfg["Ls"], l2="flushed between steps (write of 2x L2)",
+                      prefix="decode states of position t0 (random values on its set bits), states of t0+T exported")
     else:
         config["l2"] = "flushed between steps (write of 2x L2)"
 

@@ -77,8 +77,8 @@ size_t fwd_simt_workspace(const ll_shape& s);
 size_t fwd_simt_cont_workspace(const ll_shape& s);
 // the decode states of t0 + T after a continuation (both forward paths)
 ll_status cont_export_launch(const float* pre_states, const float* pre_scales, const float* seg_states,
-                             const float* seg_scales, const float* log_alpha, float* state_out, float* scale_out,
-                             int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream);
+                             const float* seg_scales, const float* log_alpha, float* seg_decay, float* state_out,
+                             float* scale_out, int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream);
 ll_status fwd_simt_launch(const FwdArgs& a);
 int fwd_simt_launches(const ll_shape& s);
 

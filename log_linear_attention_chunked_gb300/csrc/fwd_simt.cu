@@ -57,7 +57,7 @@ constexpr int kMaxChunkElems = 8192;
 struct SimtPlan {
   int Ce, N, lc;  // effective chunk, #chunks, log2(Ce)
   size_t off_S, off_F, off_tot, off_G, off_O, total;
-  size_t off_segS, off_segSc, total_cont;  // the segment's own export (continuation)
+  size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
 SimtPlan plan_of(const ll_shape& s) {
@@ -79,6 +79,7 @@ SimtPlan plan_of(const ll_shape& s) {
   p.total = off;
   p.off_segS = off;  off = align_up(off + BH * (size_t)std::max(s.Ls, 1) * mat * sizeof(float), 256);
   p.off_segSc = off; off = align_up(off + BH * (size_t)std::max(s.Ls, 1) * sizeof(float), 256);
+  p.off_segDec = off; off = align_up(off + BH * sizeof(float), 256);
   p.total_cont = off;
   return p;
 }
@@ -334,8 +335,9 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
     simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
         F, G, segS, segSc, p.N, mat, s.Ls, p.lc);
     LL_CUDA_OK(cudaGetLastError());
-    const ll_status st = cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha, a.state_out,
-                                            a.scale_out, BH, s.T, mat, s.Ls, a.t0, a.stream);
+    const ll_status st = cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha,
+                                            reinterpret_cast<float*>(ws + p.off_segDec), a.state_out, a.scale_out,
+                                            BH, s.T, mat, s.Ls, a.t0, a.stream);
     if (st != LL_OK) return st;
   } else if (a.state_out) {
     simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
@@ -361,16 +363,14 @@ ll_status fwd_simt_launch(const FwdArgs& a) {
 }
 
 // (6): the decode states of t1 = t0 + T from the prefix states of t0 and the
-// segment's own export at T (relative); shared by both forward paths.  One
-// thread per matrix element; the segment's total decay is a block sum of its
-// log_alpha.
-__global__ void __launch_bounds__(kThreads) cont_export_kernel(
-    const float* __restrict__ pre_states, const float* __restrict__ pre_scales, const float* __restrict__ seg_states,
-    const float* __restrict__ seg_scales, const float* __restrict__ log_alpha, float* __restrict__ state_out,
-    float* __restrict__ scale_out, int T, int mat, int Ls, long long t0) {
+// segment's own export at T (relative); shared by both forward paths.  First
+// the segment's total decay per head (one block per head), then one thread
+// per matrix element writes every slot once, summing the buckets that land
+// on it.
+__global__ void __launch_bounds__(kThreads) segment_decay_kernel(const float* __restrict__ log_alpha,
+                                                                 float* __restrict__ seg_decay, int T) {
   __shared__ double part[kThreads];
-  const size_t bh = blockIdx.y;
-  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  const size_t bh = blockIdx.x;
   double g = 0.0;
   for (int i = threadIdx.x; i < T; i += kThreads) g += (double)log_alpha[bh * T + i];
   part[threadIdx.x] = g;
@@ -379,34 +379,46 @@ __global__ void __launch_bounds__(kThreads) cont_export_kernel(
     if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
     __syncthreads();
   }
-  const float seg_decay = expf((float)part[0]);
+  if (threadIdx.x == 0) seg_decay[bh] = expf((float)part[0]);
+}
+
+__global__ void __launch_bounds__(kThreads) cont_export_kernel(
+    const float* __restrict__ pre_states, const float* __restrict__ pre_scales, const float* __restrict__ seg_states,
+    const float* __restrict__ seg_scales, const float* __restrict__ seg_decay, float* __restrict__ state_out,
+    float* __restrict__ scale_out, int T, int mat, int Ls, long long t0) {
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
   const long long t1 = t0 + T;
   const int b = 64 - __clzll(t1 ^ t0);                         // bitlen(t1 xor t0)
   const long long P = 1ll << (64 - __clzll((long long)T - 1));  // smallest power of two >= T
+  const float dec = seg_decay[bh];
   if (idx < mat) {
-    for (int slot = 0; slot < Ls; ++slot) state_out[(bh * Ls + slot) * (size_t)mat + idx] = 0.f;
-    for (int slot = 0; slot < Ls; ++slot) {
-      if ((t0 >> slot) & 1) {  // prefix level slot+1
-        const int tgt = (slot + 1 > b ? slot + 1 : b) - 1;
-        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
-            pre_scales[bh * Ls + slot] * seg_decay * pre_states[(bh * Ls + slot) * (size_t)mat + idx];
+    for (int out = 0; out < Ls; ++out) {
+      float acc = 0.f;
+      if ((t1 >> out) & 1) {
+        for (int slot = 0; slot < Ls; ++slot) {
+          // prefix level slot+1 goes to max(slot+1, b), decayed over the segment
+          if (((t0 >> slot) & 1) && (slot + 1 > b ? slot + 1 : b) == out + 1)
+            acc = fmaf(pre_scales[bh * Ls + slot] * dec, pre_states[(bh * Ls + slot) * (size_t)mat + idx], acc);
+          // the segment's level slot+1 keeps it if T < P, else goes to b
+          if (((T >> slot) & 1) && (T < P ? slot + 1 : b) == out + 1)
+            acc = fmaf(seg_scales[bh * Ls + slot], seg_states[(bh * Ls + slot) * (size_t)mat + idx], acc);
+        }
       }
-      if ((T >> slot) & 1) {   // segment level slot+1
-        const int tgt = (T < P ? slot + 1 : b) - 1;
-        state_out[(bh * Ls + tgt) * (size_t)mat + idx] +=
-            seg_scales[bh * Ls + slot] * seg_states[(bh * Ls + slot) * (size_t)mat + idx];
-      }
+      state_out[(bh * Ls + out) * (size_t)mat + idx] = acc;
     }
   }
   if (blockIdx.x == 0 && threadIdx.x == 0)
-    for (int slot = 0; slot < Ls; ++slot) scale_out[bh * Ls + slot] = ((t1 >> slot) & 1) ? 1.f : 0.f;
+    for (int out = 0; out < Ls; ++out) scale_out[bh * Ls + out] = ((t1 >> out) & 1) ? 1.f : 0.f;
 }
 
 ll_status cont_export_launch(const float* pre_states, const float* pre_scales, const float* seg_states,
-                             const float* seg_scales, const float* log_alpha, float* state_out, float* scale_out,
-                             int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream) {
+                             const float* seg_scales, const float* log_alpha, float* seg_decay, float* state_out,
+                             float* scale_out, int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream) {
+  segment_decay_kernel<<<BH, kThreads, 0, stream>>>(log_alpha, seg_decay, T);
+  LL_CUDA_OK(cudaGetLastError());
   cont_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, stream>>>(
-      pre_states, pre_scales, seg_states, seg_scales, log_alpha, state_out, scale_out, T, mat, Ls, t0);
+      pre_states, pre_scales, seg_states, seg_scales, seg_decay, state_out, scale_out, T, mat, Ls, t0);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }

@@ -1020,7 +1020,7 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
 struct TcPlan {
   int Nt;
   size_t off_F, off_R, off_G, off_flags, off_rflags, total;
-  size_t off_segS, off_segSc, total_cont;  // the segment's own export (continuation)
+  size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
 // F holds the tiles' nodes, then kPreSlots prefix nodes per head (used by a
@@ -1040,6 +1040,7 @@ TcPlan tc_plan(const ll_shape& s) {
   const size_t slots = (size_t)std::max(s.Ls, 1);
   p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
   p.off_segSc = off;  off = align_up(off + BH * slots * 4, 256);
+  p.off_segDec = off; off = align_up(off + BH * 4, 256);
   p.total_cont = off;
   return p;
 }
@@ -1155,7 +1156,8 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
     float* segSc = reinterpret_cast<float*>(ws + plan.off_segSc);
     tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, segS, segSc, plan.Nt, s.Ls);
     LL_CUDA_OK(cudaGetLastError());
-    return cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha, a.state_out, a.scale_out, BH, s.T,
+    return cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha,
+                              reinterpret_cast<float*>(ws + plan.off_segDec), a.state_out, a.scale_out, BH, s.T,
                               kD * kD, s.Ls, a.t0, a.stream);
   }
   if (a.state_out) {

@@ -33,6 +33,10 @@ WORKLOADS = {
                              io="bf16", seed=2, shift=0.0),
     "gdn_bf16_t4k": dict(kind="gdn", B=2, H=16, T=4096, dk=128, dv=128, chunk=64, L=13,
                          io="bf16", seed=3, shift=2.0),
+    # prefill continuation: 16384 new tokens at position 49152 (prefix held as
+    # decode states, 17 slots), the long-context forward's distributions
+    "mamba2_cont_bf16_t16k": dict(kind="mamba2_cont", B=1, H=16, T=16384, t0=49152, dk=128, dv=128, chunk=64,
+                                  L=17, Ls=17, io="bf16", seed=2, shift=0.0),
     # the same workload under reading B (log-linear Mamba-2 on the delta-rule pseudo-values)
     "gdn_b_bf16_t4k": dict(kind="gdn_b", B=2, H=16, T=4096, dk=128, dv=128, chunk=64, L=13,
                            io="bf16", seed=3, shift=2.0),
