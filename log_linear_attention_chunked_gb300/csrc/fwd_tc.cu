@@ -238,6 +238,10 @@ __device__ __forceinline__ int node_of_level(int j, int h) { return ((j >> (h + 
 // prefix nodes (continuation) per head: one per tile height
 constexpr int kPreSlots = 16;
 
+// The roles are instantiated twice: kCont = false is the forward from
+// position 0 (no prefix levels), kCont = true a continuation.
+template <bool kCont> __device__ __forceinline__ int start_tile(const TcParams& p) { return kCont ? p.c0t : 0; }
+
 // Number of tiles CTA blockIdx.x processes (blockIdx.x < total).
 __device__ __forceinline__ int tiles_of_cta(int total) { return (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1; }
 
@@ -305,6 +309,7 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
 // released in shared memory, so the epilogue starts on level 0 before later
 // nodes are published) and loads the node.  Once a wait has expired nothing
 // new is armed.
+template <bool kCont>
 __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
@@ -322,13 +327,13 @@ __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
     st_release_cta_u32(nlr + (it & 1), (uint32_t)it << 8);
     float D = 0.f;
     uint32_t l = 0;
-    const int ja = jp | p.c0t;  // absolute tile index: the segment's bits, then the start tile's
+    const int ja = jp | start_tile<kCont>(p);  // absolute tile index: the segment's bits, then the start tile's
     for (int h = 0; (ja >> h) != 0 && !*c.abort_s; ++h) {
       if (!((ja >> h) & 1)) continue;
       // a prefix level (continuation) holds the prefix bucket, decayed to the
       // segment start and written before this kernel: no word to wait for,
       // and every later prefix level shares the same decay D
-      const bool pre = !((jp >> h) & 1);
+      const bool pre = kCont && !((jp >> h) & 1);
       const size_t node = pre ? (size_t)p.BH * p.Nt + (size_t)bhp * kPreSlots + h
                               : (size_t)bhp * p.Nt + node_of_level(jp, h);
       float g = 0.f;
@@ -427,6 +432,7 @@ __device__ void producer_pieces(const Ctx& c, const CUtensorMap* tf, const CUten
 }
 
 // ------------------------------------------------------------------ MMA issuer
+template <bool kCont>
 __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
@@ -460,7 +466,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   for (int it = 0; it <= n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     const int j = it < n ? u / p.BH : 0;
-    const int nlev_p = it >= 1 ? __popc(jp | p.c0t) : 0;
+    const int nlev_p = it >= 1 ? __popc(jp | start_tile<kCont>(p)) : 0;
     const uint32_t tR = tmem + kTmR0 + (it & 1) * 128;
     if (it < n) {
       // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
@@ -503,6 +509,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
 
 // ------------------------------------------------------------------ epilogue
 
+template <bool kCont>
 __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
@@ -571,8 +578,9 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
 #pragma unroll
       for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
       if (it + 1 < n) fetch(u + gridDim.x);
-      if (it >= 1 && (jp | p.c0t) != 0)  // the previous tile's first level lambda, ahead of its back half
-        lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jp | p.c0t) - 1));
+      const int jap = jp | start_tile<kCont>(p);  // the previous tile's absolute index bits
+      if (it >= 1 && jap != 0)  // the previous tile's first level lambda, ahead of its back half
+        lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jap) - 1));
 
       // inclusive cumsum of log_alpha over the tile
       float x = la;
@@ -728,7 +736,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // ================= back half of tile it-1: inter-tile levels + output
       const size_t rp = (size_t)bhp * p.T + (size_t)jp * kTile + row;
       // (the CTA's last tile has no front half after it to load this in)
-      if (it == n && (jp | p.c0t) != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jp | p.c0t) - 1));
+      const int jap = jp | start_tile<kCont>(p);
+      if (it == n && jap != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(jap) - 1));
       // log decays of the levels, handed over one by one by the level producer
       // under a step-tagged count; bounded wait until it covers `cnt` levels
       const uint32_t* nlr = reinterpret_cast<const uint32_t*>(s + kOffNode + 160) + (it & 1);
@@ -756,7 +765,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // inter-tile levels: Q'_l = lam_t[8 + h] exp(cs_t + D_l) Q_t goes to TMEM
       // as the A operand of a product the MMA accumulates onto the output
       int l = 0;
-      for (int rem = jp | p.c0t; rem != 0; ++l) {
+      for (int rem = jap; rem != 0; ++l) {
         rem &= rem - 1;
         const float lam_h = lam_c;
         // the next level's lambda loads while this level is written
@@ -917,6 +926,7 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
   bulk_wait0();
 }
 
+template <bool kCont>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf,
@@ -956,16 +966,16 @@ __global__ void __launch_bounds__(kThreads, 1)
   const uint32_t tmem = *tmem_slot;
 
   if (warp == 0) {
-    if (lane == 0) producer_levels(c, &tf);
+    if (lane == 0) producer_levels<kCont>(c, &tf);
     else if (lane == 1) producer_kvq(c, &tq, &tk, &tv);
   } else if (warp == kPieceWarp) {
     if (lane == 0) producer_pieces(c, &tf, &tr);
   } else if (warp == 1) {
-    if (lane == 0) mma_issuer(c, tmem);
+    if (lane == 0) mma_issuer<kCont>(c, tmem);
   } else if (warp == kPubWarp) {
     if (lane == 0) store_warp(c, &to, &tf, &tr);
   } else {
-    epilogue(c, tmem, warp, lane);
+    epilogue<kCont>(c, tmem, warp, lane);
   }
   __syncwarp();
 
@@ -1142,14 +1152,15 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   int dev = 0, sms = 0, per_sm = 0;
   LL_CUDA_OK(cudaGetDevice(&dev));
   LL_CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  LL_CUDA_OK(cudaFuncSetAttribute(fwd_tc_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
-  LL_CUDA_OK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, fwd_tc_kernel, kThreads, kSmemBytes));
+  const void* kern = a.state_in ? (const void*)fwd_tc_kernel<true> : (const void*)fwd_tc_kernel<false>;
+  LL_CUDA_OK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
+  LL_CUDA_OK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes));
   if (per_sm < 1) return LL_ERR_CUDA;
   const long long tiles = (long long)BH * plan.Nt;
   const int grid = (int)std::min<long long>(tiles, (long long)sms * per_sm);
 
   void* args[] = {&tq, &tk, &tv, &tf, &to, &tr, &p};
-  LL_CUDA_OK(cudaLaunchCooperativeKernel((const void*)fwd_tc_kernel, dim3(grid), dim3(kThreads), args, kSmemBytes,
+  LL_CUDA_OK(cudaLaunchCooperativeKernel(kern, dim3(grid), dim3(kThreads), args, kSmemBytes,
                                          a.stream));
   if (a.state_out && a.state_in) {
     float* segS = reinterpret_cast<float*>(ws + plan.off_segS);
