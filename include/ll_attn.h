@@ -78,7 +78,9 @@ typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
 
 /* Problem shape of a forward call.
  *   B, H      batch rows and heads (>= 1)
- *   T         sequence length (>= 1), a multiple of `chunk`
+ *   T         sequence length (>= 1); the Gated DeltaNet entry points need a
+ *             multiple of `chunk`, the Mamba-2 forward takes any T (a partial
+ *             last chunk runs on the CUDA-core path)
  *   dk, dv    key / value head dims, each in {16, 32, 64, 128}
  *   L         number of lambda levels per token, >= levels touched by T
  *             (1 if T == 1, else bit_length(T-1) + 1)

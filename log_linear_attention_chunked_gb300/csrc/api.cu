@@ -34,7 +34,6 @@ static ll_status check_shape(const ll_shape* s) {
   if (s->B < 1 || s->H < 1 || s->T < 1) return LL_ERR_INVALID_ARG;
   if (s->io != LL_F32 && s->io != LL_BF16) return LL_ERR_INVALID_ARG;
   if (!is_pow2_in(s->chunk, 16, 128)) return LL_ERR_INVALID_ARG;
-  if (s->T % s->chunk != 0) return LL_ERR_INVALID_ARG;
   if (s->L < levels_needed(s->T) || s->L > 64) return LL_ERR_INVALID_ARG;
   if (s->Ls < 0 || s->Ls > 62) return LL_ERR_INVALID_ARG;
   if (!head_dim_ok(s->dk) || !head_dim_ok(s->dv)) return LL_ERR_UNSUPPORTED;
@@ -194,7 +193,7 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
 }
 
 size_t ll_gdn_fwd_b_workspace_size(const ll_shape* s) {
-  if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
+  if (check_shape(s) != LL_OK || s->Ls != 0 || s->T % s->chunk != 0) return 0;
   return gdn_b_workspace(*s);
 }
 
@@ -203,6 +202,7 @@ ll_status ll_gdn_fwd_b(const ll_shape* s, const void* q, const void* k, const vo
                        void* stream) {
   ll_status st = check_shape(s);
   if (st != LL_OK) return st;
+  if (s->T % s->chunk != 0) return LL_ERR_INVALID_ARG;  // whole chunks only
   if (s->Ls != 0) return LL_ERR_INVALID_ARG;
   if (!q || !k || !v || !log_alpha || !beta || !lam || !o) return LL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(beta) ||
@@ -235,7 +235,7 @@ ll_status ll_gdn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io, 
 }
 
 size_t ll_gdn_fwd_workspace_size(const ll_shape* s) {
-  if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
+  if (check_shape(s) != LL_OK || s->Ls != 0 || s->T % s->chunk != 0) return 0;
   return gdn_workspace(*s);
 }
 
@@ -244,6 +244,7 @@ ll_status ll_gdn_fwd(const ll_shape* s, const void* q, const void* k, const void
                      void* stream) {
   ll_status st = check_shape(s);
   if (st != LL_OK) return st;
+  if (s->T % s->chunk != 0) return LL_ERR_INVALID_ARG;  // whole chunks only
   if (s->Ls != 0) return LL_ERR_INVALID_ARG;
   if (!q || !k || !v || !log_alpha || !beta || !lam || !o) return LL_ERR_INVALID_ARG;
   if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(beta) ||

@@ -21,6 +21,13 @@
 //   (5) export  : the level states of position T are F nodes of the Fenwick
 //                 prefix query of N = T/Ce, decayed to token T-1.
 //
+// Ragged T (T not a multiple of Ce): the last chunk holds the r = T mod Ce
+// remaining tokens; the kernels treat its missing rows as absent (zero keys
+// and values, log_alpha 0, no output).  At position T the levels above
+// log2(Ce) are the nodes of the floor(T/Ce) full chunks, decayed over the
+// partial chunk too; the levels up to log2(Ce) are the buckets of r inside the
+// partial chunk, written by their own kernel.
+//
 // Prefill continuation (the tokens are positions t0 .. t0+T-1, the prefix
 // enters as the decode states of position t0, decayed to t0-1; t0 is a
 // multiple of the smallest power of two P >= T, so the segment sits inside
@@ -65,7 +72,7 @@ SimtPlan plan_of(const ll_shape& s) {
   int d = std::max(s.dk, s.dv);
   p.Ce = s.chunk;
   while (p.Ce * d > kMaxChunkElems && p.Ce > 16) p.Ce >>= 1;
-  p.N = s.T / p.Ce;
+  p.N = (s.T + p.Ce - 1) / p.Ce;  // the last chunk may be partial
   p.lc = ilog2(p.Ce);
   const size_t BH = (size_t)s.B * s.H;
   const size_t mat = (size_t)s.dv * s.dk;
@@ -108,22 +115,23 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restri
 
   const size_t t0 = (size_t)c * Ce;
   const size_t row0 = bh * T + t0;
+  const int nv = min(Ce, T - (int)t0);  // rows present in this chunk
   if (tid == 0) {
     double acc = 0.0;
     for (int i = 0; i < Ce; ++i) {
-      acc += (double)log_alpha[row0 + i];
+      if (i < nv) acc += (double)log_alpha[row0 + i];
       cs[i] = acc;
     }
     tot[bh * N + c] = acc;
   }
   for (int x = tid; x < Ce * dk; x += kThreads) {
     int i = x / dk, f = x % dk;
-    qs[i * dkp + f] = to_f(q[(row0 + i) * dk + f]);
-    ks[i * dkp + f] = to_f(k[(row0 + i) * dk + f]);
+    qs[i * dkp + f] = i < nv ? to_f(q[(row0 + i) * dk + f]) : 0.f;
+    ks[i * dkp + f] = i < nv ? to_f(k[(row0 + i) * dk + f]) : 0.f;
   }
   for (int x = tid; x < Ce * dv; x += kThreads) {
     int i = x / dv, e = x % dv;
-    vs[i * dvp + e] = to_f(v[(row0 + i) * dv + e]);
+    vs[i * dvp + e] = i < nv ? to_f(v[(row0 + i) * dv + e]) : 0.f;
   }
   __syncthreads();
   for (int j = tid; j < Ce; j += kThreads) wdec[j] = expf((float)(cs[Ce - 1] - cs[j]));
@@ -132,7 +140,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restri
   for (int x = tid; x < Ce * Ce; x += kThreads) {
     int i = x / Ce, j = x % Ce;
     float p = 0.f;
-    if (j <= i) {
+    if (j <= i && i < nv) {
       float dot = 0.f;
       for (int f = 0; f < dk; ++f) dot = fmaf(qs[i * dkp + f], ks[j * dkp + f], dot);
       int lv = bitlen((unsigned)(i ^ j));
@@ -143,7 +151,7 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restri
   __syncthreads();
 
   // intra output
-  for (int x = tid; x < Ce * dv; x += kThreads) {
+  for (int x = tid; x < nv * dv; x += kThreads) {
     int i = x / dv, e = x % dv;
     float acc = 0.f;
     for (int j = 0; j <= i; ++j) acc = fmaf(P[i * Cp + j], vs[j * dvp + e], acc);
@@ -218,15 +226,16 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
   float* Oc = Fs + dv * dkp;
 
   const size_t row0 = bh * T + (size_t)c * Ce;
+  const int nv = min(Ce, T - c * Ce);  // rows present in this chunk
   if (tid == 0) {
     double acc = 0.0;
     for (int i = 0; i < Ce; ++i) {
-      acc += (double)log_alpha[row0 + i];
+      if (i < nv) acc += (double)log_alpha[row0 + i];
       cs[i] = acc;
     }
   }
-  for (int x = tid; x < Ce * dk; x += kThreads) qs[x] = to_f(q[row0 * dk + x]);
-  for (int x = tid; x < Ce * dv; x += kThreads) Oc[x] = o_intra[row0 * dv + x];
+  for (int x = tid; x < Ce * dk; x += kThreads) qs[x] = x < nv * dk ? to_f(q[row0 * dk + x]) : 0.f;
+  for (int x = tid; x < Ce * dv; x += kThreads) Oc[x] = x < nv * dv ? o_intra[row0 * dv + x] : 0.f;
   __syncthreads();
 
   const size_t mat = (size_t)dv * dk;
@@ -237,7 +246,7 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
     const float* Fe = F + (bh * N + e) * mat;
     for (int x = tid; x < (int)mat; x += kThreads) Fs[(x / dk) * dkp + (x % dk)] = Fe[x];
     for (int i = tid; i < Ce; i += kThreads)
-      w[i] = lam[(row0 + i) * L + lc + 1 + h] * expf((float)(cs[i] + D));
+      w[i] = i < nv ? lam[(row0 + i) * L + lc + 1 + h] * expf((float)(cs[i] + D)) : 0.f;
     __syncthreads();
     for (int x = tid; x < Ce * dv; x += kThreads) {
       int i = x / dv, ev = x % dv;
@@ -255,7 +264,8 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
       const float* Pe = pre_states + (bh * Ls + slot) * mat;
       const float g = pre_scales[bh * Ls + slot];
       for (int x = tid; x < (int)mat; x += kThreads) Fs[(x / dk) * dkp + (x % dk)] = Pe[x];
-      for (int i = tid; i < Ce; i += kThreads) w[i] = lam[(row0 + i) * L + slot + 1] * g * expf((float)(cs[i] + D));
+      for (int i = tid; i < Ce; i += kThreads)
+        w[i] = i < nv ? lam[(row0 + i) * L + slot + 1] * g * expf((float)(cs[i] + D)) : 0.f;
       __syncthreads();
       for (int x = tid; x < Ce * dv; x += kThreads) {
         int i = x / dv, ev = x % dv;
@@ -266,29 +276,70 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
       __syncthreads();
     }
   }
-  for (int x = tid; x < Ce * dv; x += kThreads) o[row0 * dv + x] = from_f<IO>(Oc[x]);
+  for (int x = tid; x < nv * dv; x += kThreads) o[row0 * dv + x] = from_f<IO>(Oc[x]);
 }
 
 // (5): level states of position T (= N chunks), decayed to token T-1.
 __global__ void __launch_bounds__(kThreads) simt_export_kernel(const float* __restrict__ F,
                                                                const double* __restrict__ G,
+                                                               const double* __restrict__ tot,
                                                                float* __restrict__ state_out,
-                                                               float* __restrict__ scale_out, int N, int mat, int Ls,
-                                                               int lc) {
+                                                               float* __restrict__ scale_out, int N, int Nq, int mat,
+                                                               int Ls, int lc) {
+  // N chunks in the arrays; the level states are those of the Nq full ones,
+  // decayed over the partial chunk N - 1 as well when Nq < N
   const size_t bh = blockIdx.y;
   const int idx = blockIdx.x * kThreads + threadIdx.x;
-  double D = 0.0;
+  double D = Nq < N ? tot[bh * N + N - 1] : 0.0;
   for (int slot = 0; slot < Ls; ++slot) {
     const int h = slot + 1 - (lc + 1);  // level slot+1 = lc + 1 + h
     float val = 0.f, sc = 0.f;
-    if (h >= 0 && h < 31 && ((N >> h) & 1)) {
-      const int e = ((N >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    if (h >= 0 && h < 31 && ((Nq >> h) & 1)) {
+      const int e = ((Nq >> (h + 1)) << (h + 1)) + (1 << h) - 1;
       if (idx < mat) val = expf((float)D) * F[(bh * N + e) * (size_t)mat + idx];
       sc = 1.f;
       D += G[bh * N + e];
     }
     if (idx < mat) state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
+  }
+}
+
+// (5) for ragged T: the levels 1..log2(Ce) of position T are the buckets of
+// r = T mod Ce inside the partial chunk; bucket l (bit l-1 of r) holds rows
+// [r_hi, r_hi + 2^(l-1)), r_hi = r with bits below l cleared, decayed to T-1.
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) simt_tail_export_kernel(const IO* __restrict__ k,
+                                                                    const IO* __restrict__ v,
+                                                                    const float* __restrict__ log_alpha,
+                                                                    float* __restrict__ state_out,
+                                                                    float* __restrict__ scale_out, int T, int dk,
+                                                                    int dv, int Ls, int r) {
+  __shared__ float dec[128];  // exp(cs[r-1] - cs[a]) for the partial chunk's rows (r < 128)
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  const size_t row0 = bh * T + (size_t)(T - r);
+  if (threadIdx.x == 0) {
+    double acc = 0.0;  // suffix sums: decay from row a to the last row
+    for (int a = r - 1; a >= 0; --a) {
+      dec[a] = expf((float)acc);
+      acc += (double)log_alpha[row0 + a];
+    }
+  }
+  __syncthreads();
+  const int mat = dv * dk;
+  for (int l = 1; l <= Ls && (1 << (l - 1)) <= r; ++l) {
+    const int slot = l - 1;
+    if (!((r >> slot) & 1)) continue;
+    const int lo = (r >> l) << l, hi = lo + (1 << slot);
+    if (idx < mat) {
+      const int e = idx / dk, f = idx % dk;
+      float acc = 0.f;
+      for (int a = lo; a < hi; ++a)
+        acc = fmaf(dec[a] * to_f(v[(row0 + a) * dv + e]), to_f(k[(row0 + a) * dk + f]), acc);
+      state_out[(bh * Ls + slot) * (size_t)mat + idx] = acc;
+    }
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = 1.f;
   }
 }
 
@@ -329,20 +380,29 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
                                                                      s.Ls, a.t0);
   LL_CUDA_OK(cudaGetLastError());
 
+  const int Nq = s.T / Ce, r = s.T % Ce;  // full chunks, rows of the partial one
+  auto export_states = [&](float* st, float* sc) -> ll_status {
+    simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
+        F, G, tot, st, sc, p.N, Nq, mat, s.Ls, p.lc);
+    LL_CUDA_OK(cudaGetLastError());
+    if (r > 0) {
+      simt_tail_export_kernel<IO><<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
+          static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, st, sc, s.T, s.dk, s.dv, s.Ls, r);
+      LL_CUDA_OK(cudaGetLastError());
+    }
+    return LL_OK;
+  };
   if (a.state_out && a.state_in) {
     float* segS = reinterpret_cast<float*>(ws + p.off_segS);
     float* segSc = reinterpret_cast<float*>(ws + p.off_segSc);
-    simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
-        F, G, segS, segSc, p.N, mat, s.Ls, p.lc);
-    LL_CUDA_OK(cudaGetLastError());
+    const ll_status es = export_states(segS, segSc);
+    if (es != LL_OK) return es;
     const ll_status st = cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha,
                                             reinterpret_cast<float*>(ws + p.off_segDec), a.state_out, a.scale_out,
                                             BH, s.T, mat, s.Ls, a.t0, a.stream);
     if (st != LL_OK) return st;
   } else if (a.state_out) {
-    simt_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, a.stream>>>(
-        F, G, a.state_out, a.scale_out, p.N, mat, s.Ls, p.lc);
-    LL_CUDA_OK(cudaGetLastError());
+    return export_states(a.state_out, a.scale_out);
   }
   return LL_OK;
 }
@@ -353,7 +413,7 @@ size_t fwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
 
 size_t fwd_simt_cont_workspace(const ll_shape& s) { return plan_of(s).total_cont; }
 
-int fwd_simt_launches(const ll_shape& s) { return s.Ls > 0 ? 4 : 3; }
+int fwd_simt_launches(const ll_shape& s) { return s.Ls > 0 ? (s.T % plan_of(s).Ce ? 5 : 4) : 3; }
 
 ll_status fwd_simt_launch(const FwdArgs& a) {
   SimtPlan p = plan_of(a.s);

@@ -54,7 +54,8 @@ def test_workspace_size_queries(L):
     from log_linear_attention_chunked_gb300 import binding
     assert binding.ll_attn_fwd_workspace_size(_shape()) > 0
     assert binding.ll_attn_fwd_workspace_size(_shape(chunk=24)) == 0      # not a power of two
-    assert binding.ll_attn_fwd_workspace_size(_shape(T=72)) == 0          # T % chunk != 0
+    assert binding.ll_attn_fwd_workspace_size(_shape(T=72, L=8)) > 0      # ragged T: partial last chunk
+    assert binding.ll_gdn_fwd_workspace_size(_shape(T=72, L=8)) == 0       # Gated DeltaNet: whole chunks only
     assert binding.ll_attn_fwd_workspace_size(_shape(L=6)) == 0           # too few levels for T=64
     assert binding.ll_attn_fwd_workspace_size(_shape(dk=96)) == 0         # unsupported head dim
     big = binding.ll_attn_fwd_workspace_size(_shape(B=1, H=16, T=16384, dk=128, dv=128, L=15, chunk=64,

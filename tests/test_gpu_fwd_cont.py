@@ -65,6 +65,8 @@ def _cont(B, inp, t0, T, Ls, chunk, S0, sc0):
     ("f32", 64, 128, 1024, 64),
     ("f32", 32, 128, 0, 32),       # no prefix
     ("bf16", 64, 256, 1792, 64),   # three prefix buckets
+    ("f32", 32, 100, 128, 32),       # ragged segment: a partial last chunk (P = 128 > T)
+    ("bf16", 64, 37, 192, 16),       # ragged, P = 64
     ("bf16", 128, 512, 1536, 128),   # from here on the tensor-core path (bf16, d = 128)
     ("bf16", 128, 128, 128, 64),     # prefix bucket at the first tile level
     ("bf16", 128, 256, 768, 64),     # two prefix buckets, the segment closes its block
