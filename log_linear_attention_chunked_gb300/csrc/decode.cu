@@ -75,19 +75,27 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int 
   const float alpha = expf(log_alpha[bh]);
   const float* lam_bh = lam + (size_t)bh * (Ls + 1);
   float* sc = scales + (size_t)bh * Ls;
-  if (threadIdx.x == 0) {
+  if (warp == 0) {  // the non-empty slots, compacted in order; one lane per slot, loads in parallel
     int n = 0;
-    for (int i = 0; i < Ls; ++i) {
-      if ((t >> i) & 1) {
-        const float g = sc[i] * alpha;
-        slot_of[n] = i;
-        coef[n] = lam_bh[i + 1] * g;
-        mcoef[n] = (i < j) ? g : 0.f;
-        gdec[n] = g;
-        ++n;
+    for (int base = 0; base < Ls; base += 32) {
+      const int i = base + lane;
+      const bool set = i < Ls && ((t >> i) & 1);
+      float g = 0.f, lm = 0.f;
+      if (set) {
+        g = sc[i] * alpha;
+        lm = lam_bh[i + 1];
       }
+      const unsigned m = __ballot_sync(0xffffffffu, set);
+      if (set) {
+        const int at = n + __popc(m & ((1u << lane) - 1u));
+        slot_of[at] = i;
+        coef[at] = lm * g;
+        mcoef[at] = (i < j) ? g : 0.f;
+        gdec[at] = g;
+      }
+      n += __popc(m);
     }
-    ns_sh = n;
+    if (lane == 0) ns_sh = n;
   }
   __syncthreads();
   const int ns = ns_sh;

@@ -72,17 +72,22 @@ __global__ void __launch_bounds__(kWarps * 32) gdn_decode_kernel(
   }
   const int j = __ffsll(t + 1) - 1;  // trailing ones of t: the carry slot
   const float* lam_bh = lam + (size_t)bh * (Ls + 1);
-  if (threadIdx.x == 0) {
+  if (warp == 0) {  // the non-empty slots, compacted in order; one lane per slot, loads in parallel
     int n = 0;
-    for (int i = 0; i < Ls; ++i) {
-      if ((t >> i) & 1) {
-        slot_of[n] = i;
-        lam_of[n] = lam_bh[i + 1];
-        merges[n] = i < j;
-        ++n;
+    for (int base = 0; base < Ls; base += 32) {
+      const int i = base + lane;
+      const bool set = i < Ls && ((t >> i) & 1);
+      const float lm = set ? lam_bh[i + 1] : 0.f;
+      const unsigned m = __ballot_sync(0xffffffffu, set);
+      if (set) {
+        const int at = n + __popc(m & ((1u << lane) - 1u));
+        slot_of[at] = i;
+        lam_of[at] = lm;
+        merges[at] = i < j;
       }
+      n += __popc(m);
     }
-    ns_sh = n;
+    if (lane == 0) ns_sh = n;
   }
   __syncthreads();
   const int ns = ns_sh;
