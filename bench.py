@@ -121,8 +121,8 @@ KERNEL_SOURCES = {
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
-    "gdn_b": ("gdn.cu", "fwd_tc.cu", "common.cuh", "sm100.cuh"),
-    "mamba2_cont": ("fwd_tc.cu", "fwd_simt.cu", "common.cuh", "sm100.cuh"),
+    "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the chunk preparation
+    "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
 }
 
 

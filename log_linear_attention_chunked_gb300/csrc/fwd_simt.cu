@@ -427,15 +427,25 @@ ll_status fwd_simt_launch(const FwdArgs& a) {
 // the segment's total decay per head (one block per head), then one thread
 // per matrix element writes every slot once, summing the buckets that land
 // on it.
-__global__ void __launch_bounds__(kThreads) segment_decay_kernel(const float* __restrict__ log_alpha,
-                                                                 float* __restrict__ seg_decay, int T) {
-  __shared__ double part[kThreads];
+constexpr int kDecThreads = 1024;
+
+__global__ void __launch_bounds__(kDecThreads) segment_decay_kernel(const float* __restrict__ log_alpha,
+                                                                    float* __restrict__ seg_decay, int T) {
+  __shared__ double part[kDecThreads];
   const size_t bh = blockIdx.x;
-  double g = 0.0;
-  for (int i = threadIdx.x; i < T; i += kThreads) g += (double)log_alpha[bh * T + i];
-  part[threadIdx.x] = g;
+  // four independent float64 chains per thread: the sum is latency-bound otherwise
+  double g0 = 0.0, g1 = 0.0, g2 = 0.0, g3 = 0.0;
+  int i = threadIdx.x;
+  for (; i + 3 * kDecThreads < T; i += 4 * kDecThreads) {
+    g0 += (double)log_alpha[bh * T + i];
+    g1 += (double)log_alpha[bh * T + i + kDecThreads];
+    g2 += (double)log_alpha[bh * T + i + 2 * kDecThreads];
+    g3 += (double)log_alpha[bh * T + i + 3 * kDecThreads];
+  }
+  for (; i < T; i += kDecThreads) g0 += (double)log_alpha[bh * T + i];
+  part[threadIdx.x] = (g0 + g1) + (g2 + g3);
   __syncthreads();
-  for (int o = kThreads / 2; o > 0; o >>= 1) {
+  for (int o = kDecThreads / 2; o > 0; o >>= 1) {
     if (threadIdx.x < o) part[threadIdx.x] += part[threadIdx.x + o];
     __syncthreads();
   }
@@ -475,7 +485,7 @@ __global__ void __launch_bounds__(kThreads) cont_export_kernel(
 ll_status cont_export_launch(const float* pre_states, const float* pre_scales, const float* seg_states,
                              const float* seg_scales, const float* log_alpha, float* seg_decay, float* state_out,
                              float* scale_out, int BH, int T, int mat, int Ls, long long t0, cudaStream_t stream) {
-  segment_decay_kernel<<<BH, kThreads, 0, stream>>>(log_alpha, seg_decay, T);
+  segment_decay_kernel<<<BH, kDecThreads, 0, stream>>>(log_alpha, seg_decay, T);
   LL_CUDA_OK(cudaGetLastError());
   cont_export_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, 0, stream>>>(
       pre_states, pre_scales, seg_states, seg_scales, seg_decay, state_out, scale_out, T, mat, Ls, t0);
