@@ -14,6 +14,10 @@
 // ("Log-Linear Attention" study note §3-4/§3-5; chunk-wise scan of the
 // gist.science (zh) summary §2.3; the per-level contractions are summed in
 // one accumulator per tile, the pages' "level fusion".)
+// A prefill continuation (tiles at absolute index c0t + j, c0t a multiple of
+// the smallest power of two >= the segment's tile count) walks the bits of
+// c0t + j: the bits of c0t are further levels whose nodes are the prefix
+// buckets of the decode states, written as bf16 nodes before this kernel.
 //
 // Roles (384 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
 // i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
