@@ -22,7 +22,7 @@
 // Roles (384 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
 // i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
 // tiles running at the same time are few positions of many heads and the
-// chains of node dependencies inside one round of tiles stay short):
+// chains of node dependencies inside one wave of tiles stay short):
 //   warp 0      lane 1: TMA loads of K, V, Q (+ L2 prefetch of the next tile);
 //               lane 0: the level nodes of the previous tile (F ring), once
 //               their publication words are seen, and their log decays

@@ -84,7 +84,7 @@ def test_onehot_levels(B, lvl):
 
 
 def test_many_heads_odd_tile_count(B):
-    # more tiles than CTAs, ragged last round, three heads of 13 tiles
+    # more tiles than CTAs, a partial last wave, three heads of 13 tiles
     inp = synth.make_inputs(_cfg(13 * 128, Bn=1, H=3), la_mode="slow", tag="tc13")
     assert rel_err(_run(B, inp), _oracle(inp)) <= TOL_BF16
 
