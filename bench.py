@@ -380,29 +380,65 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     o = torch.empty(Bn, H, T, dv, dtype=g["q"].dtype, device=dev)
     o_host = torch.empty(o.shape, dtype=o.dtype, pin_memory=True)
 
-    def step(i=0):
+    def run(x, out):  # one call of the public API on the current stream
         if cont:
-            binding.ll_attn_fwd_cont(t0, st_in, sc_in, g["q"], g["k"], g["v"], g["log_alpha"], g["lam"],
-                                     cfg["chunk"], o=o, state_out=st_out, scale_out=sc_out, workspace=ws)
+            binding.ll_attn_fwd_cont(t0, st_in, sc_in, x["q"], x["k"], x["v"], x["log_alpha"], x["lam"],
+                                     cfg["chunk"], o=out, state_out=st_out, scale_out=sc_out, workspace=ws)
         elif reading_b:
-            binding.ll_gdn_fwd_b(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
+            binding.ll_gdn_fwd_b(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["lam"], cfg["chunk"], o=out,
                                  workspace=ws)
         elif gdn:
-            binding.ll_gdn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["beta"], g["lam"], cfg["chunk"], o=o,
+            binding.ll_gdn_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["lam"], cfg["chunk"], o=out,
                                workspace=ws)
         else:
-            binding.ll_attn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["lam"], cfg["chunk"], o=o, workspace=ws)
+            binding.ll_attn_fwd(x["q"], x["k"], x["v"], x["log_alpha"], x["lam"], cfg["chunk"], o=out, workspace=ws)
+
+    def step(i=0):
+        run(g, o)
+
+    # End to end: every step uploads its inputs from pinned host memory and
+    # reads its output back; two device input sets and two outputs let the
+    # upload of step i+1 (one copy stream) and the read-back of step i-1
+    # (another) run while step i computes.
+    gset = [g, {n: torch.empty_like(g[n]) for n in names}]
+    oset = [o, torch.empty_like(o)]
+    ohost = [o_host, torch.empty(o.shape, dtype=o.dtype, pin_memory=True)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
 
     def e2e_step(i=0):
-        for n in names:
-            g[n].copy_(host[n], non_blocking=True)
-        step(i)
-        o_host.copy_(o, non_blocking=True)
+        b = i & 1
+        comp = torch.cuda.current_stream(dev)
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(ev_done[b])  # the call of step i-2 has read this input set
+            for n in names:
+                gset[b][n].copy_(host[n], non_blocking=True)
+            ev_in[b].record(s_in)
+        comp.wait_event(ev_in[b])
+        if used[b]:
+            comp.wait_event(ev_out[b])  # the output of step i-2 is back on the host
+        run(gset[b], oset[b])
+        ev_done[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            ohost[b].copy_(oset[b], non_blocking=True)
+            ev_out[b].record(s_out)
+        used[b] = True
+
+    def e2e_begin(ev0):  # the first timed upload starts after the start event
+        s_in.wait_event(ev0)
+
+    def e2e_end():  # the current stream waits for the last read-back
+        torch.cuda.current_stream(dev).wait_stream(s_out)
 
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = o_host.numel() * o_host.element_size()
-    return dict(step=step, e2e_step=e2e_step, units=Bn * H * T, h2d=h2d, d2h=d2h, launches=launches, flush=True,
-                abytes=algorithmic_bytes(cfg), aflops=algorithmic_flops(cfg))
+    return dict(step=step, e2e_step=e2e_step, e2e_begin=e2e_begin, e2e_end=e2e_end, units=Bn * H * T, h2d=h2d,
+                d2h=d2h, launches=launches, flush=True, abytes=algorithmic_bytes(cfg), aflops=algorithmic_flops(cfg))
 
 
 def decode_workload(cfg, dev, rank, binding, synth, torch):
@@ -586,7 +622,11 @@ def main():
             barrier()
             torch.cuda.synchronize()
             e0.record(stream)
+            if "e2e_begin" in w:
+                w["e2e_begin"](e0)
         w["e2e_step"](i)
+    if "e2e_end" in w:
+        w["e2e_end"]()
     e1.record(stream)
     torch.cuda.synchronize()
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
