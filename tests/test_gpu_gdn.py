@@ -23,8 +23,8 @@ def B():
     return binding
 
 
-def _cfg(T, d=128, Bn=1, H=2, io="bf16", chunk=64, seed=31):
-    return dict(synth.WORKLOADS["gdn_bf16_t4k"], B=Bn, H=H, T=T, dk=d, dv=d, chunk=chunk, L=levels_needed(T),
+def _cfg(T, d=128, Bn=1, H=2, io="bf16", chunk=64, seed=31, dv=None):
+    return dict(synth.WORKLOADS["gdn_bf16_t4k"], B=Bn, H=H, T=T, dk=d, dv=dv or d, chunk=chunk, L=levels_needed(T),
                 io=io, seed=seed)
 
 
@@ -99,3 +99,12 @@ def test_workload_gdn_t4k_sampled_rows(B):
         ref = gdn.gdn_rows_A(f["q"][b, h], f["k"][b, h], f["v"][b, h], f["beta"][b, h], f["log_alpha"][b, h],
                              f["lam"][b, h], rows)
         assert rel_err(out[b, h][rows][None, None], ref[None, None]) <= TOL_BF16, (b, h)
+
+
+@pytest.mark.parametrize("T,dk,dv,io", [(512, 128, 64, "f32"), (384, 64, 128, "bf16"), (256, 32, 16, "f32")])
+def test_key_and_value_dims_differ(B, T, dk, dv, io):
+    """dk != dv: the register-tiled scan takes d_k = 128 with any d_v multiple of 16,
+    the generic kernels the rest."""
+    inp = synth.make_inputs(_cfg(T, d=dk, dv=dv, io=io), tag=f"gdv{T}{dk}{dv}")
+    tol = TOL_GDN_F32 if io == "f32" else TOL_BF16
+    assert rel_err(_run(B, inp, 64), _oracle(inp)) <= tol

@@ -27,10 +27,10 @@ def _cfg(Bn, H, d, Ls, n, io, seed):
     return dict(W, B=Bn, H=H, dk=d, dv=d, Ls=Ls, steps=n, io=io, seed=seed)
 
 
-def _random_states(Bn, H, Ls, d, t0, seed):
+def _random_states(Bn, H, Ls, d, t0, seed, dv=None):
     """float32 states, N(0, 0.05^2) on the set bits of t0, zero elsewhere."""
     g = torch.Generator().manual_seed(seed)
-    st = torch.randn(Bn, H, Ls, d, d, generator=g) * 0.05
+    st = torch.randn(Bn, H, Ls, dv or d, d, generator=g) * 0.05
     ne = [((t0 >> i) & 1) == 1 for i in range(Ls)]
     st *= torch.tensor(ne, dtype=torch.float32)[None, None, :, None, None]
     return st, ne
@@ -110,3 +110,15 @@ def test_rejects_position_beyond_levels(B):
     t = torch.tensor([3, 4], dtype=torch.int64, device=dev)
     B.ll_gdn_decode_step(t, z, z, z, zh, zh, ones, st)
     assert B.ll_last_device_error() == 0
+
+
+@pytest.mark.parametrize("io,dk,dv", [("f32", 64, 128), ("bf16", 128, 32), ("f32", 16, 64)])
+def test_key_and_value_dims_differ(B, io, dk, dv):
+    Bn, H, n, t0 = 2, 2, 12, 77
+    Ls = (t0 + n).bit_length() + 1
+    cfg = dict(W, B=Bn, H=H, dk=dk, dv=dv, Ls=Ls, steps=n, io=io, seed=71)
+    dec = synth.make_decode_inputs(cfg)
+    S0, ne = _random_states(Bn, H, Ls, dk, t0, seed=9, dv=dv)
+    out, st = _run(B, dec, S0, t0, n)
+    _check(dec, S0, ne, t0, out, st, [(b, h) for b in range(Bn) for h in range(H)],
+           TOL_F32 if io == "f32" else TOL_BF16)
