@@ -158,3 +158,31 @@ def test_gdn_rejects_bad_args_on_host(L):
     assert L.ll_gdn_fwd(ctypes.byref(s), *([vp(FAKE)] * 8), ctypes.c_size_t(1 << 40), None) == 1
     s = _shape()
     assert L.ll_gdn_fwd(ctypes.byref(s), *([vp(FAKE)] * 7), None, ctypes.c_size_t(0), None) in (2, 5)
+
+
+def test_binding_fails_loudly_without_the_library(monkeypatch):
+    """No fallback: a missing libllattn.so is an error, not a slower path."""
+    from log_linear_attention_chunked_gb300 import binding
+    monkeypatch.setattr(binding, "_lib", None)
+    monkeypatch.setattr(binding, "LIB_PATH", binding.LIB_PATH + ".absent")
+    with pytest.raises(RuntimeError):
+        binding.lib()
+
+
+def test_product_path_does_not_reach_the_oracle():
+    """The package and the benchmark's GPU arm never import the oracle: only the
+    tests, smoke() and the benchmark's CPU-baseline and reference arms do."""
+    import ast
+    root = os.path.dirname(os.path.dirname(os.path.abspath(__file__)))
+    pkg = os.path.join(root, "log_linear_attention_chunked_gb300")
+    for f in sorted(os.listdir(pkg)):
+        if not f.endswith(".py"):
+            continue
+        tree = ast.parse(open(os.path.join(pkg, f)).read())
+        for node in ast.walk(tree):
+            names = []
+            if isinstance(node, ast.Import):
+                names = [a.name for a in node.names]
+            elif isinstance(node, ast.ImportFrom):
+                names = [node.module or ""]
+            assert not any(n == "oracle" or n.startswith("oracle.") for n in names), (f, names)
