@@ -78,9 +78,10 @@ def algorithmic_flops(cfg) -> int:
         per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d
         per_bh = N * per_chunk + P * (6 * C * d * d + 2 * C * C * d)
     elif cfg["kind"] == "gdn_b":
-        # the chunk factors (as above), the single-state pass (S W^T and the
-        # update, 4 C d^2 per chunk), then the log-linear Mamba-2 forward
-        per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d + 4 * C * d * d
+        # per chunk: K K^T (lower half), Tinv, U and W (triangular), S_c; the
+        # single-state pass (S W^T and the update, 4 C d^2); then the
+        # log-linear Mamba-2 forward on the pseudo-values
+        per_chunk = 3 * C * C * d + (2 * C ** 3) // 3 + 2 * C * d * d + 4 * C * d * d
         per_bh = N * per_chunk + 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
     else:
         per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P

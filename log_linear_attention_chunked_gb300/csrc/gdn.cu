@@ -912,7 +912,36 @@ __device__ __forceinline__ void pair_product(const float* A1, const float* A2, c
   }
 }
 
-template <typename IO>
+// C = A B for the same thread tile (reading B needs one product per pass)
+__device__ __forceinline__ void single_product(const float* A, const float* Bm, int ti, int tj, int mend,
+                                               float (&c1)[4][8]) {
+#pragma unroll
+  for (int r = 0; r < 4; ++r)
+#pragma unroll
+    for (int x = 0; x < 8; ++x) c1[r][x] = 0.f;
+  for (int m = 0; m < mend; m += 4) {
+    float4 a1[4];
+#pragma unroll
+    for (int r = 0; r < 4; ++r) a1[r] = ld4(A + (4 * ti + r) * kSa + m);
+#pragma unroll
+    for (int t = 0; t < 4; ++t) {
+      const float4 b0 = ld4(Bm + (m + t) * kSx + 4 * tj);
+      const float4 b1 = ld4(Bm + (m + t) * kSx + 64 + 4 * tj);
+#pragma unroll
+      for (int r = 0; r < 4; ++r) {
+        const float x = comp(a1[r], t);
+        c1[r][0] = fmaf(x, b0.x, c1[r][0]); c1[r][1] = fmaf(x, b0.y, c1[r][1]);
+        c1[r][2] = fmaf(x, b0.z, c1[r][2]); c1[r][3] = fmaf(x, b0.w, c1[r][3]);
+        c1[r][4] = fmaf(x, b1.x, c1[r][4]); c1[r][5] = fmaf(x, b1.y, c1[r][5]);
+        c1[r][6] = fmaf(x, b1.z, c1[r][6]); c1[r][7] = fmaf(x, b1.w, c1[r][7]);
+      }
+    }
+  }
+}
+
+// kB: reading B, which needs only U, W, Kt and S_c (no Q, Aqk, intra output
+// or Q'), so the chunk's Q is not loaded and four of the products drop out.
+template <typename IO, bool kB>
 __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
     const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v,
     const float* __restrict__ log_alpha, const float* __restrict__ beta, const float* __restrict__ lam,
@@ -937,7 +966,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
   float* lamI = ds + kCe;           // [64][8] lambda of the in-chunk levels
 
   const size_t row0 = bh * T + (size_t)c * kCe;
-  load_tile(qs, q + row0 * kDk, tid);
+  if constexpr (!kB) load_tile(qs, q + row0 * kDk, tid);
   load_tile(kk, k + row0 * kDk, tid);
   load_tile(vs, v + row0 * kDk, tid);
   if (warp == 0) {  // inclusive cumsum of log alpha (float64 across the warp)
@@ -961,10 +990,11 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
     bs[lane] = beta[row0 + lane];
     bs[32 + lane] = beta[row0 + 32 + lane];
   }
-  for (int x = tid; x < kCe * 8; x += kThreads) {
-    const int i = x >> 3, l = x & 7;
-    lamI[x] = l < L ? lam[(row0 + i) * L + l] : 0.f;
-  }
+  if constexpr (!kB)
+    for (int x = tid; x < kCe * 8; x += kThreads) {
+      const int i = x >> 3, l = x & 7;
+      lamI[x] = l < L ? lam[(row0 + i) * L + l] : 0.f;
+    }
   __syncthreads();
 
   // ---- L (strict lower, beta folded in) and Aqk (inclusive): rows ti + 16a, columns tj + 16b
@@ -981,7 +1011,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
 #pragma unroll
       for (int a = 0; a < 4; ++a) {
         kI[a] = ld4(kk + (ti + 16 * a) * kSx + f);
-        qI[a] = ld4(qs + (ti + 16 * a) * kSx + f);
+        if constexpr (!kB) qI[a] = ld4(qs + (ti + 16 * a) * kSx + f);
         kJ[a] = ld4(kk + (tj + 16 * a) * kSx + f);
       }
 #pragma unroll
@@ -990,8 +1020,10 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
         for (int b = 0; b < 4; ++b) {
           a1[a][b] = fmaf(kI[a].x, kJ[b].x, a1[a][b]); a1[a][b] = fmaf(kI[a].y, kJ[b].y, a1[a][b]);
           a1[a][b] = fmaf(kI[a].z, kJ[b].z, a1[a][b]); a1[a][b] = fmaf(kI[a].w, kJ[b].w, a1[a][b]);
-          a2[a][b] = fmaf(qI[a].x, kJ[b].x, a2[a][b]); a2[a][b] = fmaf(qI[a].y, kJ[b].y, a2[a][b]);
-          a2[a][b] = fmaf(qI[a].z, kJ[b].z, a2[a][b]); a2[a][b] = fmaf(qI[a].w, kJ[b].w, a2[a][b]);
+          if constexpr (!kB) {
+            a2[a][b] = fmaf(qI[a].x, kJ[b].x, a2[a][b]); a2[a][b] = fmaf(qI[a].y, kJ[b].y, a2[a][b]);
+            a2[a][b] = fmaf(qI[a].z, kJ[b].z, a2[a][b]); a2[a][b] = fmaf(qI[a].w, kJ[b].w, a2[a][b]);
+          }
         }
     }
 #pragma unroll
@@ -1006,7 +1038,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
           if (j < i) lv = bs[i] * a1[a][b] * g;
         }
         Lm[i * kSa + j] = lv;
-        Aq[i * kSa + j] = av;
+        if constexpr (!kB) Aq[i * kSa + j] = av;
       }
   }
   __syncthreads();
@@ -1064,7 +1096,7 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
   const int ti = tid >> 4, tj = tid & 15;
   const int mend = 8 * warp + 8;  // rows of this warp: 8 warp .. 8 warp + 7
   // ---- Cl = Aqk Tb (masked by the in-chunk levels, into Lm), Cle = Aqk Tbe (into Aq)
-  {
+  if constexpr (!kB) {
     float c1[4][4], c2[4][4];
 #pragma unroll
     for (int r = 0; r < 4; ++r)
@@ -1101,18 +1133,22 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
       st4(Lm + i * kSa + 4 * tj, w[0], w[1], w[2], w[3]);
       st4(Aq + i * kSa + 4 * tj, c2[r][0], c2[r][1], c2[r][2], c2[r][3]);
     }
+    __syncthreads();
   }
-  __syncthreads();
 
   // ---- intra output and U = Tb V (kept as diag(exp(g_end - g)) U in place of V)
   {
     float c1[4][8], c2[4][8];
-    pair_product(Lm, Tb, vs, ti, tj, mend, c1, c2);
+    if constexpr (kB) {
+      single_product(Tb, vs, ti, tj, mend, c2);
+    } else {
+      pair_product(Lm, Tb, vs, ti, tj, mend, c1, c2);
 #pragma unroll
-    for (int r = 0; r < 4; ++r) {
-      float* orow = Oacc + (row0 + 4 * ti + r) * kDk;
-      st4(orow + 4 * tj, c1[r][0], c1[r][1], c1[r][2], c1[r][3]);
-      st4(orow + 64 + 4 * tj, c1[r][4], c1[r][5], c1[r][6], c1[r][7]);
+      for (int r = 0; r < 4; ++r) {
+        float* orow = Oacc + (row0 + 4 * ti + r) * kDk;
+        st4(orow + 4 * tj, c1[r][0], c1[r][1], c1[r][2], c1[r][3]);
+        st4(orow + 64 + 4 * tj, c1[r][4], c1[r][5], c1[r][6], c1[r][7]);
+      }
     }
     if (Ug) {  // the chunk's own pseudo-values U (reading B)
 #pragma unroll
@@ -1134,7 +1170,8 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
   // ---- W = Tbe K, Q' = diag(e) Q - Cle K, Kt = diag(exp(g_end - g)) K
   {
     float c1[4][8], c2[4][8];
-    pair_product(Tbe, Aq, kk, ti, tj, mend, c1, c2);
+    if constexpr (kB) single_product(Tbe, kk, ti, tj, mend, c1);
+    else pair_product(Tbe, Aq, kk, ti, tj, mend, c1, c2);
 #pragma unroll
     for (int r = 0; r < 4; ++r) {
       const int i = 4 * ti + r;
@@ -1143,12 +1180,14 @@ __global__ void __launch_bounds__(kThreads, 1) gdn_prep128_kernel(
 #pragma unroll
       for (int hlf = 0; hlf < 2; ++hlf) {
         const int f = 64 * hlf + 4 * tj;
-        const float4 qv = ld4(qs + i * kSx + f);
         const float4 kv = ld4(kk + i * kSx + f);
         const int o = 4 * hlf;
         st4(Wg + go + f, c1[r][o], c1[r][o + 1], c1[r][o + 2], c1[r][o + 3]);
-        st4(Qp + go + f, ei * qv.x - c2[r][o], ei * qv.y - c2[r][o + 1], ei * qv.z - c2[r][o + 2],
-            ei * qv.w - c2[r][o + 3]);
+        if constexpr (!kB) {
+          const float4 qv = ld4(qs + i * kSx + f);
+          st4(Qp + go + f, ei * qv.x - c2[r][o], ei * qv.y - c2[r][o + 1], ei * qv.z - c2[r][o + 2],
+              ei * qv.w - c2[r][o + 3]);
+        }
         st4(Kt + go + f, di * kv.x, di * kv.y, di * kv.z, di * kv.w);
       }
     }
@@ -1200,9 +1239,9 @@ ll_status launch_typed(const FwdArgs& a, const GdnPlan& p) {
   const int BH = s.B * s.H;
   if (p.fast_prep && aligned16(a.q) && aligned16(a.k) && aligned16(a.v)) {
     const size_t sm1 = fast::prep_smem_floats() * 4;
-    LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_prep128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
-                                    (int)sm1));
-    fast::gdn_prep128_kernel<IO><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
+    LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_prep128_kernel<IO, false>,
+                                    cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
+    fast::gdn_prep128_kernel<IO, false><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
         static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha,
         a.beta, a.lam, Qp, W, Kt, S, lg, O, nullptr, s.T, s.L);
   } else {
@@ -1286,9 +1325,9 @@ ll_status launch_b_typed(const FwdArgs& a, const GdnBPlan& b) {
   IO* Uio = reinterpret_cast<IO*>(ws + b.off_Uio);
   const int BH = s.B * s.H;
   const size_t sm1 = fast::prep_smem_floats() * 4;
-  LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_prep128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+  LL_CUDA_OK(cudaFuncSetAttribute(fast::gdn_prep128_kernel<IO, true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)sm1));
-  fast::gdn_prep128_kernel<IO><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
+  fast::gdn_prep128_kernel<IO, true><<<dim3(p.N, BH), kThreads, sm1, a.stream>>>(
       static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.beta,
       a.lam, Qp, W, Kt, S, lg, O, Ul, s.T, s.L);
   LL_CUDA_OK(cudaGetLastError());
