@@ -122,7 +122,7 @@ KERNEL_SOURCES = {
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
-    "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the chunk preparation
+    "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
 }
 
