@@ -15,6 +15,13 @@
  *                        "Recurrent form" (o_t = sum_l lam_t^(l) q_t^T S_t^(l))
  *                        and §3-6 "Memory-efficient decoding"; carry/merge as in
  *                        the drawer analogy of the gist.science (zh) summary.
+ *   ll_attn_bwd          backward of ll_attn_fwd: the gradients of q, k, v,
+ *                        log_alpha and lam for an upstream gradient of o.  The
+ *                        pages name the backward, and in it the lambda-term
+ *                        gradient, as the hard part of an implementation
+ *                        (study note §4-5 "Implementation notes" and §6
+ *                        "Limitations"; gist.science (zh) summary §5) without
+ *                        printing it: it is the exact gradient of §3-4's O.
  *   ll_gdn_fwd           Log-Linear Gated DeltaNet forward, study note §3-5 and
  *                        gist.science (de) Technische Zusammenfassung §2; the
  *                        gated delta rule itself is not on the pages (reading A:
@@ -186,6 +193,41 @@ LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const flo
                                   const float* scale_in, const void* q, const void* k, const void* v,
                                   const float* log_alpha, const float* lam, void* o, float* state_out,
                                   float* scale_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* Bytes of workspace ll_attn_bwd needs for `shape` (0 on an invalid shape or
+ * shape->Ls != 0). */
+LL_API size_t ll_attn_bwd_workspace_size(const ll_shape* shape);
+
+/* Number of kernel launches one ll_attn_bwd call makes (0 on an invalid shape). */
+LL_API int ll_attn_bwd_launches(const ll_shape* shape);
+
+/* Backward of ll_attn_fwd.  For f = sum(o . dout) with o = ll_attn_fwd(q, k,
+ * v, log_alpha, lam), writes the exact gradients
+ *   dq = (dP . M) K,  dk = (dP . M)^T Q,  dv = (QK^T . M)^T dout,
+ *   dlam[t][l]     = sum over keys s of level l of query t of
+ *                    (dout_t . v_s)(q_t . k_s) Gamma(t,s),
+ *   dlog_alpha[r]  = sum over t >= r of dc_t, where dc_t is the derivative of
+ *                    f by the cumulative log-decay c_t (Gamma(t,s) = exp(c_t - c_s)),
+ * with M = M^S . M^H and dP = dout V^T on the causal triangle.
+ *   shape      as ll_attn_fwd; shape->Ls must be 0 (no state gradients)
+ *   q, k, v, log_alpha, lam   the forward's inputs, layouts of ll_attn_fwd
+ *   dout       [B,H,T,dv]  io dtype, upstream gradient of o
+ *   dq, dk     [B,H,T,dk]  io dtype, written
+ *   dv         [B,H,T,dv]  io dtype, written
+ *   dlog_alpha [B,H,T]     float32, written (dlog_alpha[0] of every row is 0
+ *                          up to rounding: no decay acts before the first token)
+ *   dlam       [B,H,T,L]   float32, written (levels no key reaches are 0)
+ *   workspace  >= ll_attn_bwd_workspace_size(shape) bytes, 256-byte aligned
+ * No output may overlap an input or another output (LL_ERR_INVALID_ARG).
+ * Any T is accepted (a partial last chunk is handled); accumulation is
+ * float32 on CUDA cores, with the cumulative decays and the suffix sums of
+ * dlog_alpha in float64.  The order of the float32 additions into the
+ * key-side level nodes is not fixed, so results can differ in the last bits
+ * between calls. */
+LL_API ll_status ll_attn_bwd(const ll_shape* shape, const void* q, const void* k, const void* v,
+                             const float* log_alpha, const float* lam, const void* dout, void* dq, void* dk,
+                             void* dv, float* dlog_alpha, float* dlam, void* workspace, size_t ws_bytes,
+                             void* stream);
 
 /* Size in bytes of the fixed device scratch of ll_attn_fwd_noalloc. */
 #define LL_NOALLOC_SCRATCH_BYTES (32u << 20)

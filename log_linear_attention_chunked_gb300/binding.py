@@ -26,7 +26,7 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
            "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
            "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b", "ll_attn_fwd_cont_workspace_size",
-           "ll_attn_fwd_cont")
+           "ll_attn_fwd_cont", "ll_attn_bwd_workspace_size", "ll_attn_bwd_launches", "ll_attn_bwd")
 
 
 class LLError(RuntimeError):
@@ -84,6 +84,12 @@ def lib() -> ctypes.CDLL:
     L.ll_gdn_fwd_b_workspace_size.argtypes = [shp]
     L.ll_gdn_fwd_b.restype = i32
     L.ll_gdn_fwd_b.argtypes = [shp, vp, vp, vp, fp, fp, fp, vp, vp, sz, vp]
+    L.ll_attn_bwd_workspace_size.restype = sz
+    L.ll_attn_bwd_workspace_size.argtypes = [shp]
+    L.ll_attn_bwd_launches.restype = i32
+    L.ll_attn_bwd_launches.argtypes = [shp]
+    L.ll_attn_bwd.restype = i32
+    L.ll_attn_bwd.argtypes = [shp, vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp, vp, sz, vp]
     _lib = L
     return L
 
@@ -168,6 +174,45 @@ def ll_attn_fwd(q, k, v, log_alpha, lam, chunk: int, *, o=None, state_out=None, 
                            _stream(q.device))
     _check(st, "ll_attn_fwd")
     return o
+
+
+def ll_attn_bwd_workspace_size(shape: ll_shape) -> int:
+    return int(lib().ll_attn_bwd_workspace_size(ctypes.byref(shape)))
+
+
+def ll_attn_bwd_launches(shape: ll_shape) -> int:
+    return int(lib().ll_attn_bwd_launches(ctypes.byref(shape)))
+
+
+def ll_attn_bwd(q, k, v, log_alpha, lam, dout, chunk: int, *, grads=None, workspace=None):
+    """Backward of ll_attn_fwd for the upstream gradient dout [B,H,T,dv] (io dtype).
+    Returns (dq, dk, dv, dlog_alpha, dlam); ``grads`` may pass those five
+    tensors to be written in place."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    io = _io(q.dtype)
+    for x, n in ((q, "q"), (k, "k"), (v, "v"), (dout, "dout")):
+        _need(x, n, q.dtype)
+    _need(log_alpha, "log_alpha", torch.float32)
+    _need(lam, "lam", torch.float32)
+    shape = make_shape(B, H, T, dk, dv, L, chunk, 0, io)
+    if grads is None:
+        grads = (torch.empty_like(q), torch.empty_like(k), torch.empty_like(v), torch.empty_like(log_alpha),
+                 torch.empty_like(lam))
+    gq, gk, gv, gla, glam = grads
+    for x, ref, n in ((gq, q, "dq"), (gk, k, "dk"), (gv, v, "dv"), (gla, log_alpha, "dlog_alpha"),
+                      (glam, lam, "dlam")):
+        _need(x, n, ref.dtype)
+        if x.shape != ref.shape:
+            raise ValueError(f"{n} must have shape {tuple(ref.shape)}")
+    if workspace is None:
+        workspace = alloc_workspace(ll_attn_bwd_workspace_size(shape), q.device)
+    st = lib().ll_attn_bwd(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(lam), _ptr(dout),
+                           _ptr(gq), _ptr(gk), _ptr(gv), _ptr(gla), _ptr(glam), _ptr(workspace),
+                           ctypes.c_size_t(workspace.numel()), _stream(q.device))
+    _check(st, "ll_attn_bwd")
+    return gq, gk, gv, gla, glam
 
 
 NOALLOC_SCRATCH_BYTES = 32 << 20  # LL_NOALLOC_SCRATCH_BYTES of the header

@@ -192,6 +192,53 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
                        static_cast<cudaStream_t>(stream), ew);
 }
 
+size_t ll_attn_bwd_workspace_size(const ll_shape* s) {
+  if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
+  return bwd_simt_workspace(*s);
+}
+
+int ll_attn_bwd_launches(const ll_shape* s) {
+  if (check_shape(s) != LL_OK || s->Ls != 0) return 0;
+  return bwd_simt_launches(*s);
+}
+
+ll_status ll_attn_bwd(const ll_shape* s, const void* q, const void* k, const void* v, const float* log_alpha,
+                      const float* lam, const void* dout, void* dq, void* dk, void* dv, float* dlog_alpha,
+                      float* dlam, void* workspace, size_t ws_bytes, void* stream) {
+  ll_status st = check_shape(s);
+  if (st != LL_OK) return st;
+  if (s->Ls != 0) return LL_ERR_INVALID_ARG;
+  const void* in[6] = {q, k, v, log_alpha, lam, dout};
+  const void* out[5] = {dq, dk, dv, dlog_alpha, dlam};
+  for (const void* p : in)
+    if (!p || !aligned16(p)) return LL_ERR_INVALID_ARG;
+  for (const void* p : out)
+    if (!p || !aligned16(p)) return LL_ERR_INVALID_ARG;
+  // the gradients are written while the inputs are still read: no output may
+  // overlap an input or another output
+  const size_t es = s->io == LL_F32 ? 4 : 2;
+  const size_t rows = (size_t)s->B * s->H * s->T;
+  const size_t in_bytes[6] = {rows * s->dk * es, rows * s->dk * es, rows * s->dv * es, rows * 4, rows * s->L * 4,
+                              rows * s->dv * es};
+  const size_t out_bytes[5] = {rows * s->dk * es, rows * s->dk * es, rows * s->dv * es, rows * 4, rows * s->L * 4};
+  auto overlap = [](const void* a, size_t na, const void* b, size_t nb) {
+    const uintptr_t x = reinterpret_cast<uintptr_t>(a), y = reinterpret_cast<uintptr_t>(b);
+    return x < y + nb && y < x + na;
+  };
+  for (int i = 0; i < 5; ++i) {
+    for (int j = 0; j < 6; ++j)
+      if (overlap(out[i], out_bytes[i], in[j], in_bytes[j])) return LL_ERR_INVALID_ARG;
+    for (int j = i + 1; j < 5; ++j)
+      if (overlap(out[i], out_bytes[i], out[j], out_bytes[j])) return LL_ERR_INVALID_ARG;
+  }
+  const size_t need_ws = bwd_simt_workspace(*s);
+  if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
+  BwdArgs a{*s, q, k, v, dout, log_alpha, lam, dq, dk, dv, dlog_alpha, dlam, workspace, ws_bytes,
+            static_cast<cudaStream_t>(stream)};
+  return bwd_simt_launch(a);
+}
+
 size_t ll_gdn_fwd_b_workspace_size(const ll_shape* s) {
   if (check_shape(s) != LL_OK || s->Ls != 0 || s->T % s->chunk != 0) return 0;
   return gdn_b_workspace(*s);

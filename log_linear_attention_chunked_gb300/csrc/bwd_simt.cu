@@ -1,0 +1,496 @@
+// Backward of the chunked log-linear Mamba-2 forward on CUDA cores (float32 FMA).
+//
+// The gradient of O = (A . M) V, A = Q K^T, M = Gamma . H with
+// Gamma(t,s) = exp(c_t - c_s), c the cumulative sum of log_alpha, and
+// H(t,s) = lam_t[level(t,s)] ("Log-Linear Attention" study note §3-4 parallel
+// form and §3-5 mask composition; the study note §4-5 / §6 and the
+// gist.science (zh) summary §5 name this backward, with its lambda terms, as
+// the hard part of an implementation but print no formulas).  With
+// P = A . M and dP = dO V^T on the causal triangle:
+//   dV = P^T dO,   dQ = (dP . M) K,   dK = (dP . M)^T Q,
+//   dlam_t[l] = sum over keys s of level l of dP_ts A_ts Gamma_ts,
+//   dc_t = sum_s dP_ts P_ts - sum_t' dP_t't P_t't
+//        = sum_l lam_t[l] dlam_t[l] - v_t . dv_t    (o_t is linear in lam_t, and
+//                                                    the column sum is v_t . dv_t),
+//   dlog_alpha_r = sum over t >= r of dc_t.
+//
+// Chunk-wise (chunk c of Ce tokens; cs = cumulative log_alpha inside the
+// chunk; F_e, G_e the forward's Fenwick nodes of keys, decayed to the end of
+// chunk e):
+//   (1) intra, one CTA per chunk: the dense Ce x Ce form of every gradient,
+//       levels 0..log2(Ce) of dlam; also the chunk state S_c and the chunk's
+//       total log-decay for (2), and it clears the chunk's key-side node R_c.
+//   (2) Fenwick nodes F_e, G_e from S_c (the forward's kernel).
+//   (3) query side, one CTA per chunk c; for every set bit h of c the node
+//       e = (c with bits 0..h cleared) + 2^h - 1 holds the keys of level
+//       lc+1+h of every query of c, and with D the decay from the end of e to
+//       the start of c:
+//         g_i = exp(cs_i + D) F_e^T do_i,   dq_i += lam_i[lc+1+h] g_i,
+//         dlam_i[lc+1+h] = g_i . q_i,
+//       and the chunk adds its queries to the key-side node of e,
+//         R_e += sum_i lam_i[lc+1+h] exp(cs_i + D) do_i q_i^T,
+//       so that R_e holds every query that sees the keys of e at that level,
+//       decayed to the end of e.
+//   (4) key side, one CTA per chunk c: the keys of c are in the block of e_h
+//       for every clear bit h of c (e_h as above); with E_c the sum of the
+//       R_{e_h} decayed from the end of e_h back to the end of c,
+//         dv_j += exp(cs_end - cs_j) E_c k_j,   dk_j += exp(cs_end - cs_j) E_c^T v_j;
+//       the rows of dk, dv are final here, so dc_j is formed here too.
+//   (5) per head: dlog_alpha as suffix sums of dc (float64).
+// Ragged T: the last chunk's missing rows are absent (zero inputs, log_alpha 0,
+// no outputs), as in the forward.
+#include <algorithm>
+
+#include "common.cuh"
+
+namespace llattn {
+
+namespace {
+
+constexpr int kThreads = 256;
+constexpr int kSuffixThreads = 1024;
+constexpr int kMaxChunkElems = 8192;           // Ce * max(dk, dv), as in the forward
+constexpr size_t kMaxSmem = 220 * 1024;        // dynamic shared memory of one CTA
+
+size_t intra_smem(int Ce, int dk, int dv) {
+  return Ce * sizeof(double) +
+         sizeof(float) * ((size_t)Ce + 2 * (size_t)Ce * (dk + 1) + 2 * (size_t)Ce * (dv + 1) + 3 * (size_t)Ce * (Ce + 1));
+}
+size_t query_smem(int Ce, int dk, int dv) {
+  return Ce * sizeof(double) +
+         sizeof(float) * (2 * (size_t)Ce + 3 * (size_t)Ce * dk + (size_t)Ce * dv + (size_t)dv * (dk + 1));
+}
+size_t key_smem(int Ce, int dk, int dv) {
+  return Ce * sizeof(double) +
+         sizeof(float) * ((size_t)Ce + (size_t)Ce * (dk + 1) + 2 * (size_t)Ce * (dv + 1) + (size_t)dv * (dk + 1));
+}
+
+struct BwdPlan {
+  int Ce, N, lc;
+  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_ctot, total;
+};
+
+BwdPlan plan_of(const ll_shape& s) {
+  BwdPlan p{};
+  const int d = std::max(s.dk, s.dv);
+  p.Ce = s.chunk;
+  while (p.Ce > 16 && (p.Ce * d > kMaxChunkElems || intra_smem(p.Ce, s.dk, s.dv) > kMaxSmem ||
+                       query_smem(p.Ce, s.dk, s.dv) > kMaxSmem || key_smem(p.Ce, s.dk, s.dv) > kMaxSmem))
+    p.Ce >>= 1;
+  p.N = (s.T + p.Ce - 1) / p.Ce;
+  p.lc = ilog2(p.Ce);
+  const size_t BH = (size_t)s.B * s.H;
+  const size_t mat = (size_t)s.dv * s.dk;
+  size_t off = 0;
+  p.off_S = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  p.off_F = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  p.off_R = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  p.off_tot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
+  p.off_G = off;   off = align_up(off + BH * p.N * sizeof(double), 256);
+  p.off_dc = off;  off = align_up(off + BH * (size_t)s.T * sizeof(float), 256);
+  p.off_ctot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
+  p.off_dq = p.off_dk = p.off_dv = off;
+  if (s.io != LL_F32) {  // float32 partial sums of dq, dk, dv (float32 io accumulates in the outputs)
+    p.off_dq = off; off = align_up(off + BH * (size_t)s.T * s.dk * sizeof(float), 256);
+    p.off_dk = off; off = align_up(off + BH * (size_t)s.T * s.dk * sizeof(float), 256);
+    p.off_dv = off; off = align_up(off + BH * (size_t)s.T * s.dv * sizeof(float), 256);
+  }
+  p.total = off;
+  return p;
+}
+
+// (1) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) bwd_intra_kernel(
+    const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v, const IO* __restrict__ dout,
+    const float* __restrict__ log_alpha, const float* __restrict__ lam, float* __restrict__ dq32,
+    float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam, float* __restrict__ S,
+    double* __restrict__ tot, float* __restrict__ R, int T, int dk, int dv, int L, int Ce, int lc) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int c = blockIdx.x;
+  const int N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int dkp = dk + 1, dvp = dv + 1, Cp = Ce + 1;
+
+  double* cs = reinterpret_cast<double*>(smem_raw);
+  float* wdec = reinterpret_cast<float*>(cs + Ce);
+  float* qs = wdec + Ce;
+  float* ks = qs + Ce * dkp;
+  float* vs = ks + Ce * dkp;
+  float* gs = vs + Ce * dvp;   // dO
+  float* P = gs + Ce * dvp;    // A . M
+  float* dA = P + Ce * Cp;     // dP . M
+  float* X = dA + Ce * Cp;     // dP . A . Gamma: its level sums are dlam
+
+  const size_t row0 = bh * T + (size_t)c * Ce;
+  const int nv = min(Ce, T - c * Ce);
+  if (tid == 0) {
+    double acc = 0.0;
+    for (int i = 0; i < Ce; ++i) {
+      if (i < nv) acc += (double)log_alpha[row0 + i];
+      cs[i] = acc;
+    }
+    tot[bh * N + c] = acc;
+  }
+  for (int x = tid; x < Ce * dk; x += kThreads) {
+    const int i = x / dk, f = x % dk;
+    qs[i * dkp + f] = i < nv ? to_f(q[(row0 + i) * dk + f]) : 0.f;
+    ks[i * dkp + f] = i < nv ? to_f(k[(row0 + i) * dk + f]) : 0.f;
+  }
+  for (int x = tid; x < Ce * dv; x += kThreads) {
+    const int i = x / dv, e = x % dv;
+    vs[i * dvp + e] = i < nv ? to_f(v[(row0 + i) * dv + e]) : 0.f;
+    gs[i * dvp + e] = i < nv ? to_f(dout[(row0 + i) * dv + e]) : 0.f;
+  }
+  __syncthreads();
+  for (int j = tid; j < Ce; j += kThreads) wdec[j] = expf((float)(cs[Ce - 1] - cs[j]));
+  for (int x = tid; x < Ce * Ce; x += kThreads) {
+    const int i = x / Ce, j = x % Ce;
+    float p = 0.f, da = 0.f, xx = 0.f;
+    if (j <= i && i < nv) {
+      float a = 0.f, g = 0.f;
+      for (int f = 0; f < dk; ++f) a = fmaf(qs[i * dkp + f], ks[j * dkp + f], a);
+      for (int e = 0; e < dv; ++e) g = fmaf(gs[i * dvp + e], vs[j * dvp + e], g);
+      const float ex = expf((float)(cs[i] - cs[j]));
+      const float lm = lam[(row0 + i) * L + bitlen((unsigned)(i ^ j))];
+      p = a * ex * lm;
+      da = g * ex * lm;
+      xx = g * a * ex;
+    }
+    P[i * Cp + j] = p;
+    dA[i * Cp + j] = da;
+    X[i * Cp + j] = xx;
+  }
+  __syncthreads();
+  for (int x = tid; x < nv * dk; x += kThreads) {
+    const int i = x / dk, f = x % dk;
+    float aq = 0.f, ak = 0.f;
+    for (int j = 0; j <= i; ++j) aq = fmaf(dA[i * Cp + j], ks[j * dkp + f], aq);
+    for (int r = i; r < nv; ++r) ak = fmaf(dA[r * Cp + i], qs[r * dkp + f], ak);  // i is the key row here
+    dq32[(row0 + i) * dk + f] = aq;
+    dk32[(row0 + i) * dk + f] = ak;
+  }
+  for (int x = tid; x < nv * dv; x += kThreads) {
+    const int j = x / dv, e = x % dv;
+    float acc = 0.f;
+    for (int i = j; i < nv; ++i) acc = fmaf(P[i * Cp + j], gs[i * dvp + e], acc);
+    dv32[(row0 + j) * dv + e] = acc;
+  }
+  // levels 0..lc: level l of query i (l >= 1, bit l-1 of i set) holds the keys
+  // of the lower half of i's aligned block of 2^l rows
+  const int nl = min(lc + 1, L);
+  for (int x = tid; x < nv * nl; x += kThreads) {
+    const int i = x / nl, l = x % nl;
+    float acc = 0.f;
+    if (l == 0) {
+      acc = X[i * Cp + i];
+    } else if ((i >> (l - 1)) & 1) {
+      const int lo = (i >> l) << l;
+      for (int j = lo; j < lo + (1 << (l - 1)); ++j) acc += X[i * Cp + j];
+    }
+    dlam[(row0 + i) * L + l] = acc;
+  }
+  // chunk state S_c[e][f] = sum_j wdec_j v_j[e] k_j[f]; the key-side node of c starts at 0
+  const size_t mat = (size_t)dv * dk;
+  float* Sc = S + (bh * N + c) * mat;
+  float* Rc = R + (bh * N + c) * mat;
+  for (int x = tid; x < (int)mat; x += kThreads) {
+    const int e = x / dk, f = x % dk;
+    float acc = 0.f;
+    for (int j = 0; j < nv; ++j) acc = fmaf(wdec[j] * vs[j * dvp + e], ks[j * dkp + f], acc);
+    Sc[x] = acc;
+    Rc[x] = 0.f;
+  }
+}
+
+// (3) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) bwd_query_kernel(
+    const IO* __restrict__ q, const IO* __restrict__ dout, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ F, const double* __restrict__ G,
+    const float* dq32, IO* dq, float* __restrict__ dlam, float* __restrict__ R, int T, int dk, int dv, int L,
+    int Ce, int lc) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  const int c = blockIdx.x;
+  const int N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int dkp = dk + 1;
+  double* cs = reinterpret_cast<double*>(smem_raw);
+  float* w = reinterpret_cast<float*>(cs + Ce);  // exp(cs_i + D)
+  float* lw = w + Ce;                            // lam_i[level] exp(cs_i + D)
+  float* qs = lw + Ce;                           // [Ce][dk]
+  float* gq = qs + Ce * dk;                      // [Ce][dk] g_i[f] q_i[f]
+  float* acc = gq + Ce * dk;                     // [Ce][dk] inter-chunk part of dq
+  float* gs = acc + Ce * dk;                     // [Ce][dv] dO
+  float* Fs = gs + Ce * dv;                      // [dv][dk + 1]
+
+  const size_t row0 = bh * T + (size_t)c * Ce;
+  const int nv = min(Ce, T - c * Ce);
+  if (tid == 0) {
+    double a = 0.0;
+    for (int i = 0; i < Ce; ++i) {
+      if (i < nv) a += (double)log_alpha[row0 + i];
+      cs[i] = a;
+    }
+  }
+  for (int x = tid; x < Ce * dk; x += kThreads) {
+    qs[x] = x < nv * dk ? to_f(q[row0 * dk + x]) : 0.f;
+    acc[x] = 0.f;
+  }
+  for (int x = tid; x < Ce * dv; x += kThreads) gs[x] = x < nv * dv ? to_f(dout[row0 * dv + x]) : 0.f;
+  __syncthreads();
+
+  const size_t mat = (size_t)dv * dk;
+  double D = 0.0;
+  for (int h = 0; (c >> h) != 0; ++h) {
+    if (!((c >> h) & 1)) continue;
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    const int lv = lc + 1 + h;
+    const float* Fe = F + (bh * N + e) * mat;
+    for (int x = tid; x < (int)mat; x += kThreads) Fs[(x / dk) * dkp + (x % dk)] = Fe[x];
+    for (int i = tid; i < Ce; i += kThreads) {
+      const float wi = i < nv ? expf((float)(cs[i] + D)) : 0.f;
+      w[i] = wi;
+      lw[i] = i < nv ? wi * lam[(row0 + i) * L + lv] : 0.f;
+    }
+    __syncthreads();
+    // g_i[f] = w_i sum_e F[e][f] do_i[e]
+    for (int x = tid; x < Ce * dk; x += kThreads) {
+      const int i = x / dk, f = x % dk;
+      float a = 0.f;
+      for (int ev = 0; ev < dv; ++ev) a = fmaf(Fs[ev * dkp + f], gs[i * dv + ev], a);
+      acc[x] = fmaf(lw[i], a, acc[x]);
+      gq[x] = w[i] * a * qs[x];
+    }
+    // this chunk's queries into the key-side node of e
+    float* Re = R + (bh * N + e) * mat;
+    for (int x = tid; x < (int)mat; x += kThreads) {
+      const int ev = x / dk, f = x % dk;
+      float a = 0.f;
+      for (int i = 0; i < nv; ++i) a = fmaf(lw[i] * gs[i * dv + ev], qs[i * dk + f], a);
+      atomicAdd(Re + x, a);
+    }
+    __syncthreads();
+    for (int i = tid; i < nv; i += kThreads) {
+      float a = 0.f;
+      for (int f = 0; f < dk; ++f) a += gq[i * dk + f];
+      dlam[(row0 + i) * L + lv] = a;
+    }
+    D += G[bh * N + e];
+    __syncthreads();
+  }
+  // the levels above lc that hold no key of this chunk's queries
+  const int nh = L - (lc + 1);
+  for (int x = tid; x < nv * max(nh, 0); x += kThreads) {
+    const int i = x / nh, h = x % nh;
+    if (!(h < 31 && ((c >> h) & 1))) dlam[(row0 + i) * L + lc + 1 + h] = 0.f;
+  }
+  for (int x = tid; x < nv * dk; x += kThreads) dq[row0 * dk + x] = from_f<IO>(dq32[row0 * dk + x] + acc[x]);
+}
+
+// (4) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(kThreads) bwd_key_kernel(
+    const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
+    const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv,
+    float* __restrict__ dc, double* __restrict__ ctot, int T, int dkd, int dvd, int L, int Ce) {
+  extern __shared__ __align__(16) unsigned char smem_raw[];
+  __shared__ float coef[32];
+  __shared__ int ent[32];
+  __shared__ int n_sh;
+  __shared__ float dcrow[128];  // dc of the chunk's rows (Ce <= 128)
+  const int c = blockIdx.x;
+  const int N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const int dkp = dkd + 1, dvp = dvd + 1;
+  double* cs = reinterpret_cast<double*>(smem_raw);
+  float* wdec = reinterpret_cast<float*>(cs + Ce);
+  float* ks = wdec + Ce;       // [Ce][dk + 1]
+  float* vs = ks + Ce * dkp;   // [Ce][dv + 1]
+  float* dvs = vs + Ce * dvp;  // [Ce][dv + 1] final dv rows
+  float* Es = dvs + Ce * dvp;  // [dv][dk + 1]
+
+  const size_t row0 = bh * T + (size_t)c * Ce;
+  const int nv = min(Ce, T - c * Ce);
+  if (tid == 0) {
+    double a = 0.0;
+    for (int i = 0; i < Ce; ++i) {
+      if (i < nv) a += (double)log_alpha[row0 + i];
+      cs[i] = a;
+    }
+    // the nodes whose blocks hold the keys of c and that have queries after them
+    int n = 0, cc = c;
+    double dec = 0.0;  // log-decay from the end of c to the end of e
+    for (int h = 0; h < 31 && n < 32; ++h) {
+      if ((c >> h) & 1) continue;
+      const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+      if (e + 1 >= N) break;  // e grows with h: no later node has queries either
+      while (cc < e) dec += tot[bh * N + (++cc)];
+      ent[n] = e;
+      coef[n] = expf((float)dec);
+      ++n;
+    }
+    n_sh = n;
+  }
+  for (int x = tid; x < Ce * dkd; x += kThreads) {
+    const int j = x / dkd, f = x % dkd;
+    ks[j * dkp + f] = j < nv ? to_f(k[(row0 + j) * dkd + f]) : 0.f;
+  }
+  for (int x = tid; x < Ce * dvd; x += kThreads) {
+    const int j = x / dvd, e = x % dvd;
+    vs[j * dvp + e] = j < nv ? to_f(v[(row0 + j) * dvd + e]) : 0.f;
+  }
+  __syncthreads();
+  const int n = n_sh;
+  for (int j = tid; j < Ce; j += kThreads) wdec[j] = expf((float)(cs[Ce - 1] - cs[j]));
+  const size_t mat = (size_t)dvd * dkd;
+  if (n > 0) {
+    for (int x = tid; x < (int)mat; x += kThreads) {
+      float a = 0.f;
+      for (int m = 0; m < n; ++m) a = fmaf(coef[m], R[(bh * N + ent[m]) * mat + x], a);
+      Es[(x / dkd) * dkp + (x % dkd)] = a;
+    }
+  }
+  __syncthreads();
+  for (int x = tid; x < nv * dvd; x += kThreads) {
+    const int j = x / dvd, e = x % dvd;
+    float a = 0.f;
+    if (n > 0)
+      for (int f = 0; f < dkd; ++f) a = fmaf(Es[e * dkp + f], ks[j * dkp + f], a);
+    const float r = fmaf(wdec[j], a, dv32[(row0 + j) * dvd + e]);
+    dvs[j * dvp + e] = r;
+    dv[(row0 + j) * dvd + e] = from_f<IO>(r);
+  }
+  for (int x = tid; x < nv * dkd; x += kThreads) {
+    const int j = x / dkd, f = x % dkd;
+    float a = 0.f;
+    if (n > 0)
+      for (int e = 0; e < dvd; ++e) a = fmaf(Es[e * dkp + f], vs[j * dvp + e], a);
+    dk[(row0 + j) * dkd + f] = from_f<IO>(fmaf(wdec[j], a, dk32[(row0 + j) * dkd + f]));
+  }
+  __syncthreads();
+  // dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j, one warp per row
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int j = warp; j < Ce; j += kThreads / 32) {
+    float a = 0.f;
+    if (j < nv) {
+      for (int l = lane; l < L; l += 32) a = fmaf(lam[(row0 + j) * L + l], dlam[(row0 + j) * L + l], a);
+      for (int e = lane; e < dvd; e += 32) a = fmaf(-vs[j * dvp + e], dvs[j * dvp + e], a);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == 0) {
+      if (j < nv) dc[row0 + j] = a;
+      dcrow[j] = a;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {  // the chunk's total, in row order
+    double a = 0.0;
+    for (int j = 0; j < nv; ++j) a += (double)dcrow[j];
+    ctot[bh * N + c] = a;
+  }
+}
+
+// (5) one CTA per head: dlog_alpha_r = sum_{t >= r} dc_t, in float64
+__global__ void __launch_bounds__(kSuffixThreads) bwd_suffix_kernel(const float* __restrict__ dc,
+                                                                    const double* __restrict__ ctot,
+                                                                    float* __restrict__ dla, int T, int N,
+                                                                    int Ce) {
+  __shared__ double part[kSuffixThreads];
+  const size_t bh = blockIdx.x;
+  const int tid = threadIdx.x;
+  // chunks are split over the threads in contiguous runs
+  const int per = (N + kSuffixThreads - 1) / kSuffixThreads;
+  const int c0 = min(N, tid * per), c1 = min(N, c0 + per);
+  double s = 0.0;
+  for (int c = c0; c < c1; ++c) s += ctot[bh * N + c];
+  part[tid] = s;
+  __syncthreads();
+  // exclusive suffix sums of the runs (Hillis-Steele over the threads)
+  for (int o = 1; o < kSuffixThreads; o <<= 1) {
+    const double add = tid + o < kSuffixThreads ? part[tid + o] : 0.0;
+    __syncthreads();
+    part[tid] += add;
+    __syncthreads();
+  }
+  double run = (tid + 1 < kSuffixThreads) ? part[tid + 1] : 0.0;
+  for (int c = c1 - 1; c >= c0; --c) {
+    const int hi = min(T, (c + 1) * Ce);
+    for (int t = hi - 1; t >= c * Ce; --t) {
+      run += (double)dc[bh * T + t];
+      dla[bh * T + t] = (float)run;
+    }
+  }
+}
+
+template <typename IO>
+ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
+  const ll_shape& s = a.s;
+  unsigned char* ws = static_cast<unsigned char*>(a.ws);
+  float* S = reinterpret_cast<float*>(ws + p.off_S);
+  float* F = reinterpret_cast<float*>(ws + p.off_F);
+  float* R = reinterpret_cast<float*>(ws + p.off_R);
+  double* tot = reinterpret_cast<double*>(ws + p.off_tot);
+  double* G = reinterpret_cast<double*>(ws + p.off_G);
+  float* dc = reinterpret_cast<float*>(ws + p.off_dc);
+  double* ctot = reinterpret_cast<double*>(ws + p.off_ctot);
+  const bool f32 = s.io == LL_F32;
+  float* dq32 = f32 ? static_cast<float*>(a.dq) : reinterpret_cast<float*>(ws + p.off_dq);
+  float* dk32 = f32 ? static_cast<float*>(a.dk) : reinterpret_cast<float*>(ws + p.off_dk);
+  float* dv32 = f32 ? static_cast<float*>(a.dv) : reinterpret_cast<float*>(ws + p.off_dv);
+  const int BH = s.B * s.H;
+  const int Ce = p.Ce;
+  const int mat = s.dv * s.dk;
+  const dim3 grid(p.N, BH);
+
+  const size_t sm1 = intra_smem(Ce, s.dk, s.dv);
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_intra_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));
+  bwd_intra_kernel<IO><<<grid, kThreads, sm1, a.stream>>>(
+      static_cast<const IO*>(a.q), static_cast<const IO*>(a.k), static_cast<const IO*>(a.v),
+      static_cast<const IO*>(a.dout), a.log_alpha, a.lam, dq32, dk32, dv32, a.dlam, S, tot, R, s.T, s.dk, s.dv, s.L,
+      Ce, p.lc);
+  LL_CUDA_OK(cudaGetLastError());
+
+  const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream);
+  if (fs != LL_OK) return fs;
+
+  const size_t sm3 = query_smem(Ce, s.dk, s.dv);
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_query_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm3));
+  bwd_query_kernel<IO><<<grid, kThreads, sm3, a.stream>>>(
+      static_cast<const IO*>(a.q), static_cast<const IO*>(a.dout), a.log_alpha, a.lam, F, G, dq32,
+      static_cast<IO*>(a.dq), a.dlam, R, s.T, s.dk, s.dv, s.L, Ce, p.lc);
+  LL_CUDA_OK(cudaGetLastError());
+
+  const size_t sm4 = key_smem(Ce, s.dk, s.dv);
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_key_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4));
+  bwd_key_kernel<IO><<<grid, kThreads, sm4, a.stream>>>(
+      static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32,
+      static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc, ctot, s.T, s.dk, s.dv, s.L, Ce);
+  LL_CUDA_OK(cudaGetLastError());
+
+  bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+  LL_CUDA_OK(cudaGetLastError());
+  return LL_OK;
+}
+
+}  // namespace
+
+size_t bwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
+
+int bwd_simt_launches(const ll_shape&) { return 5; }
+
+ll_status bwd_simt_launch(const BwdArgs& a) {
+  const BwdPlan p = plan_of(a.s);
+  if (a.ws_bytes < p.total) return LL_ERR_WORKSPACE;
+  if ((size_t)p.N * sizeof(double) > 200 * 1024) return LL_ERR_UNSUPPORTED;  // the Fenwick kernel's prefix table
+  if ((long long)a.s.B * a.s.H > 65535) return LL_ERR_UNSUPPORTED;            // heads on the grid's y axis
+  if (a.s.io == LL_F32) return launch_typed<float>(a, p);
+  return launch_typed<__nv_bfloat16>(a, p);
+}
+
+}  // namespace llattn

@@ -364,12 +364,8 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
       o_intra, S, tot, s.T, s.dk, s.dv, s.L, Ce);
   LL_CUDA_OK(cudaGetLastError());
 
-  size_t sm2 = (size_t)p.N * sizeof(double);
-  if (sm2 > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
-  LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm2));
-  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm2, a.stream>>>(S, F, tot, G, p.N,
-                                                                                              mat);
-  LL_CUDA_OK(cudaGetLastError());
+  const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream);
+  if (fs != LL_OK) return fs;
 
   size_t sm3 = Ce * sizeof(double) + Ce * sizeof(float) +
                sizeof(float) * ((size_t)Ce * s.dk + (size_t)s.dv * (s.dk + 1) + (size_t)Ce * s.dv);
@@ -408,6 +404,16 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 }
 
 }  // namespace
+
+ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
+                              cudaStream_t stream) {
+  const size_t sm = (size_t)N * sizeof(double);
+  if (sm > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
+  LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
+  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm, stream>>>(S, F, tot, G, N, mat);
+  LL_CUDA_OK(cudaGetLastError());
+  return LL_OK;
+}
 
 size_t fwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
 

@@ -23,7 +23,7 @@ import torch
 # Workloads.  Distributions: q, k ~ N(0,1)/sqrt(dk); v ~ N(0,1);
 # log_alpha = -softplus(N(0,1) + shift); lam = softplus(N(0,1));
 # Gated DeltaNet: k ~ N(0,1) then L2-normalised per token and head,
-# beta = sigmoid(N(0,1)).
+# beta = sigmoid(N(0,1)).  Backward: the upstream gradient dout ~ N(0,1).
 WORKLOADS = {
     "mamba2_fp32_t64": dict(kind="mamba2", B=1, H=2, T=64, dk=16, dv=16, chunk=16, L=7,
                             io="f32", seed=0, shift=0.0),
@@ -40,6 +40,9 @@ WORKLOADS = {
     # the same workload under reading B (log-linear Mamba-2 on the delta-rule pseudo-values)
     "gdn_b_bf16_t4k": dict(kind="gdn_b", B=2, H=16, T=4096, dk=128, dv=128, chunk=64, L=13,
                            io="bf16", seed=3, shift=2.0),
+    # backward of the long-context forward: its inputs plus an upstream gradient of o
+    "mamba2_bwd_bf16_t16k": dict(kind="mamba2_bwd", B=1, H=16, T=16384, dk=128, dv=128, chunk=64, L=15,
+                                 io="bf16", seed=2, shift=0.0),
     # prefix of 65536 tokens (forward with state export), then 256 decode steps
     "decode_b64_t64k": dict(kind="decode", B=64, H=32, T=65536, dk=128, dv=128, chunk=64, L=17,
                             Ls=17, steps=256, io="bf16", seed=4, shift=0.0),
@@ -92,8 +95,10 @@ def _fill(out, name, seed, draw, B, H, device, kind=None):
 
 
 def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="softplus",
-                lam_mode="softplus", lam_level=0, tag="") -> dict:
-    """Draw q, k, v, log_alpha, lam (and beta for Gated DeltaNet) for ``cfg``.
+                lam_mode="softplus", lam_level=0, tag="", dout=None) -> dict:
+    """Draw q, k, v, log_alpha, lam (and beta for Gated DeltaNet) for ``cfg``;
+    with ``dout`` (default: for the backward workloads) also the upstream
+    gradient dout [B,H,T,dv] in the io dtype.
 
     Shapes: q, k [B,H,T,dk]; v [B,H,T,dv] in the workload's io dtype;
     log_alpha [B,H,T], lam [B,H,T,L], beta [B,H,T] in float32.
@@ -137,6 +142,8 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
             return torch.nn.functional.softplus(_normal((T, L), s, dev))
         if name == "beta":
             return torch.sigmoid(_normal((T,), s, dev))
+        if name == "dout":
+            return _normal((T, dv), s, dev)
         raise KeyError(name)
 
     out = {}
@@ -144,10 +151,12 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
               "log_alpha": (B, H, T), "lam": (B, H, T, L)}
     if gdn:
         shapes["beta"] = (B, H, T)
+    if dout if dout is not None else cfg["kind"] == "mamba2_bwd":
+        shapes["dout"] = (B, H, T, dv)
     for name, shp in shapes.items():
         buf = torch.empty(shp, device=device, dtype=torch.float32)
         _fill(buf, name, seed, draw, B, H, device)
-        out[name] = buf.to(dt) if name in ("q", "k", "v") else buf
+        out[name] = buf.to(dt) if name in ("q", "k", "v", "dout") else buf
     return out
 
 

@@ -122,6 +122,42 @@ def test_cont_rejects_bad_args_on_host(L):
     assert L.ll_attn_fwd_cont(ctypes.byref(ok), 512, *same, vp(FAKE), ctypes.c_size_t(1 << 40), None) == 1
 
 
+def test_bwd_rejects_bad_args_on_host(L):
+    from log_linear_attention_chunked_gb300 import binding
+    vp = ctypes.c_void_p
+    ok = _shape()
+    assert binding.ll_attn_bwd_workspace_size(ok) > 0
+    assert binding.ll_attn_bwd_workspace_size(_shape(T=72, L=8)) > 0     # ragged T
+    assert binding.ll_attn_bwd_workspace_size(_shape(Ls=7)) == 0         # no state gradients
+    assert binding.ll_attn_bwd_workspace_size(_shape(dk=96)) == 0
+    assert binding.ll_attn_bwd_launches(ok) == 5
+
+    def bwd(shape, ptrs, ws=FAKE, ws_bytes=1 << 40):
+        return L.ll_attn_bwd(ctypes.byref(shape), *[vp(x) if x else None for x in ptrs],
+                             vp(ws) if ws else None, ctypes.c_size_t(ws_bytes), None)
+
+    # eleven tensors, each far from the others so that none overlap
+    ptrs = [FAKE + (i << 32) for i in range(11)]
+    assert bwd(_shape(Ls=7), ptrs) == 1
+    assert bwd(_shape(dk=96), ptrs) == 2
+    for i in range(11):     # every tensor is required
+        bad = list(ptrs)
+        bad[i] = 0
+        assert bwd(ok, bad) == 1, i
+    bad = list(ptrs)
+    bad[6] = ptrs[0] + 16   # dq inside q
+    assert bwd(ok, bad) == 1
+    bad = list(ptrs)
+    bad[10] = ptrs[7]       # dlam on dk
+    assert bwd(ok, bad) == 1
+    bad = list(ptrs)
+    bad[2] = ptrs[2] + 8    # misaligned v
+    assert bwd(ok, bad) == 1
+    assert bwd(ok, ptrs, ws=0) == 5
+    assert bwd(ok, ptrs, ws_bytes=16) == 5
+    assert bwd(ok, ptrs, ws=FAKE + (20 << 32) + 16) == 5
+
+
 def test_gdn_b_rejects_bad_args_on_host(L):
     vp = ctypes.c_void_p
     s = _shape(Ls=3)
