@@ -8,7 +8,9 @@ d=128, bf16 in / float32 accumulate.  One step = one ll_attn_fwd call over the
 whole workload (every step of the hot path: intra-chunk attention, chunk
 states, the Fenwick node tree and the inter-chunk levels).  Other workloads:
 `decode_b64_t64k` (one ll_attn_decode_step for 64 x 32 heads with 17 stored
-levels, positions 65536 onward) and `gdn_bf16_t4k` (one ll_gdn_fwd).
+levels, positions 65536 onward), `gdn_bf16_t4k` (one ll_gdn_fwd) and
+`mamba2_bwd_bf16_t16k` (one ll_attn_bwd over the default workload's shape,
+with an upstream gradient of o).
 
 Inputs are resident in HBM when a timed step starts.  The forward workloads
 flush L2 between steps (a write of 2x the L2 size, outside the timed
@@ -49,6 +51,7 @@ METRICS = {
                    "% of roofline",
     "gdn_decode": "log-linear Gated DeltaNet Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); "
                   "% of HBM roofline",
+    "mamba2_bwd": "log-linear Mamba-2 bwd tokens/s (dq, dk, dv, dlog_alpha, dlam) at T=16K,H=16,d=128",
 }
 
 
@@ -62,6 +65,8 @@ def algorithmic_bytes(cfg) -> int:
     per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
     if cfg["kind"] in ("gdn", "gdn_b"):
         per_bh += cfg["T"] * 4
+    if cfg["kind"] == "mamba2_bwd":  # dout read; dq, dk, dv, dlog_alpha, dlam written
+        per_bh += cfg["T"] * (cfg["dv"] * b_io + 2 * cfg["dk"] * b_io + cfg["dv"] * b_io + 4 + 4 * cfg["L"])
     if cfg["kind"] == "mamba2_cont":  # the prefix states read, the states of t0 + T written (float32)
         t0, t1, d = cfg["t0"], cfg["t0"] + cfg["T"], cfg["dk"]
         per_bh += (bin(t0).count("1") + bin(t1).count("1")) * d * d * 4 + 2 * cfg["Ls"] * 4
@@ -74,6 +79,8 @@ def algorithmic_flops(cfg) -> int:
     T, C, d = cfg["T"], cfg["chunk"], cfg["dk"]
     N = T // C
     P = sum(bin(c).count("1") for c in range(N))
+    if cfg["kind"] == "mamba2_bwd":
+        return backward_flops(cfg)
     if cfg["kind"] == "gdn":
         per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d
         per_bh = N * per_chunk + P * (6 * C * d * d + 2 * C * C * d)
@@ -87,6 +94,32 @@ def algorithmic_flops(cfg) -> int:
         per_bh = 2 * d * T * (C + 1) + 2 * T * d * d + 3 * d * d * N + 2 * d * d * C * P
         if cfg["kind"] == "mamba2_cont":  # every token also reads the prefix levels
             per_bh += 2 * d * d * T * bin(cfg["t0"]).count("1")
+    return per_bh * cfg["B"] * cfg["H"]
+
+
+def backward_flops(cfg) -> int:
+    """Backward, per chunk: the causal pairs' scores and dO V^T, then dq, dk, dv
+    (10 d flops per pair) and the chunk state; per set bit of a chunk, the
+    query side (F^T dO) and its share of the key-side node (4 C d^2); per chunk
+    with later queries, the key-side products (4 C d^2) and the node sum; the
+    Fenwick tree's combines."""
+    T, C, d = cfg["T"], cfg["chunk"], cfg["dk"]
+    N = (T + C - 1) // C
+    pairs = C * (C + 1) // 2
+    per_bh = N * (10 * d * pairs + 2 * C * d * d)
+    for c in range(N):
+        per_bh += 4 * C * d * d * bin(c).count("1")
+        n = 0
+        for h in range(31):
+            if (c >> h) & 1:
+                continue
+            e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1
+            if e + 1 >= N:
+                break
+            n += 1
+        if n:
+            per_bh += 4 * C * d * d + 2 * n * d * d
+        per_bh += 2 * d * d * ((~c & (c + 1)).bit_length() - 1)  # merges into node c
     return per_bh * cfg["B"] * cfg["H"]
 
 
@@ -124,6 +157,7 @@ KERNEL_SOURCES = {
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
+    "mamba2_bwd": ("bwd_simt.cu", "common.cuh"),
 }
 
 
@@ -225,6 +259,8 @@ def _oracle_init(cfg, tag):
         cfg = dict(cfg, kind="mamba2", T=cfg["t0"] + cfg["T"])
     inp = synth.make_inputs(dict(cfg, B=1, H=1), tag=tag)
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if cfg["kind"] in ("gdn", "gdn_b") else ())
+    if cfg["kind"] == "mamba2_bwd":
+        names += ("dout",)
     _W["x"] = tuple(synth.to_f64(inp[n][0, 0]) for n in names)
 
 
@@ -240,6 +276,11 @@ def _oracle_worker(job):
         from oracle import gdn
         q, k, v, la, lam, beta = _W["x"]
         gdn.gdn_rows_A(q, k, v, beta, la, lam, job)
+        return float(len(job))
+    if cfg["kind"] == "mamba2_bwd":  # a token's every gradient: its query row and its key row
+        from oracle import backward
+        backward.backward_query_rows(*_W["x"], job)
+        backward.backward_key_rows(*_W["x"], job)
         return float(len(job))
     if cfg["kind"] == "gdn_b":
         from oracle import gdn
@@ -283,7 +324,7 @@ def oracle_pool(cores: int, cfg: dict, tag: str = "oracle"):
 def oracle_jobs(cfg, cores, size, seed):
     import numpy as np
     rng = np.random.default_rng(seed)
-    if cfg["kind"] in ("mamba2", "gdn"):
+    if cfg["kind"] in ("mamba2", "gdn", "mamba2_bwd"):
         return [sorted(int(x) for x in rng.integers(0, cfg["T"], size)) for _ in range(cores)]
     if cfg["kind"] == "mamba2_cont":  # rows of the new tokens, positions t0 .. t0 + T - 1
         return [sorted(int(x) for x in rng.integers(cfg["t0"], cfg["t0"] + cfg["T"], size)) for _ in range(cores)]
@@ -318,6 +359,9 @@ def sample_desc(cfg, size):
                 "(each call builds its unit-triangular system)")
     if cfg["kind"] == "gdn_decode":
         return f"{size} float64 Gated DeltaNet decode steps of one (b, h) per process"
+    if cfg["kind"] == "mamba2_bwd":
+        return (f"{size} uniformly drawn tokens per process of the row-restricted dense float64 gradients "
+                "(query row: dq, dlam; key row: dk, dv; both: the token's dc)")
     if cfg["kind"] == "gdn_b":
         return (f"{size} whole (b, h) slices ({cfg['T']} tokens) per process of the dense float64 reading-B "
                 "form (one triangular solve per slice)")
@@ -438,6 +482,75 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
 
     h2d = sum(host[n].numel() * host[n].element_size() for n in names)
     d2h = o_host.numel() * o_host.element_size()
+    return dict(step=step, e2e_step=e2e_step, e2e_begin=e2e_begin, e2e_end=e2e_end, units=Bn * H * T, h2d=h2d,
+                d2h=d2h, launches=launches, flush=True, abytes=algorithmic_bytes(cfg), aflops=algorithmic_flops(cfg))
+
+
+def backward_workload(cfg, dev, rank, binding, synth, torch):
+    """Backward: the forward's inputs plus dout resident; one ll_attn_bwd per step."""
+    names = ("q", "k", "v", "log_alpha", "lam", "dout")
+    inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
+    host = {n: inp_host[n].pin_memory() for n in names}
+    g = {n: host[n].to(dev) for n in names}
+    Bn, H, T, dk = g["q"].shape
+    dv = g["v"].shape[-1]
+    shape = binding.make_shape(Bn, H, T, dk, dv, cfg["L"], cfg["chunk"], 0, binding._io(g["q"].dtype))
+    ws = binding.alloc_workspace(binding.ll_attn_bwd_workspace_size(shape), dev)
+    launches = binding.ll_attn_bwd_launches(shape)
+    gnames = ("q", "k", "v", "log_alpha", "lam")
+
+    def new_grads():
+        return tuple(torch.empty_like(g[n]) for n in gnames)
+
+    grads = new_grads()
+
+    def run(x, out):
+        binding.ll_attn_bwd(x["q"], x["k"], x["v"], x["log_alpha"], x["lam"], x["dout"], cfg["chunk"], grads=out,
+                            workspace=ws)
+
+    def step(i=0):
+        run(g, grads)
+
+    # End to end as for the forward: inputs up on one copy stream, the five
+    # gradients down on another, two sets of each
+    gset = [g, {n: torch.empty_like(g[n]) for n in names}]
+    oset = [grads, new_grads()]
+    ohost = [tuple(torch.empty(x.shape, dtype=x.dtype, pin_memory=True) for x in grads) for _ in range(2)]
+    s_in, s_out = torch.cuda.Stream(dev), torch.cuda.Stream(dev)
+    ev_in = [torch.cuda.Event() for _ in range(2)]
+    ev_done = [torch.cuda.Event() for _ in range(2)]
+    ev_out = [torch.cuda.Event() for _ in range(2)]
+    used = [False, False]
+
+    def e2e_step(i=0):
+        b = i & 1
+        comp = torch.cuda.current_stream(dev)
+        with torch.cuda.stream(s_in):
+            if used[b]:
+                s_in.wait_event(ev_done[b])
+            for n in names:
+                gset[b][n].copy_(host[n], non_blocking=True)
+            ev_in[b].record(s_in)
+        comp.wait_event(ev_in[b])
+        if used[b]:
+            comp.wait_event(ev_out[b])
+        run(gset[b], oset[b])
+        ev_done[b].record(comp)
+        with torch.cuda.stream(s_out):
+            s_out.wait_event(ev_done[b])
+            for hst, dev_grad in zip(ohost[b], oset[b]):
+                hst.copy_(dev_grad, non_blocking=True)
+            ev_out[b].record(s_out)
+        used[b] = True
+
+    def e2e_begin(ev0):
+        s_in.wait_event(ev0)
+
+    def e2e_end():
+        torch.cuda.current_stream(dev).wait_stream(s_out)
+
+    h2d = sum(host[n].numel() * host[n].element_size() for n in names)
+    d2h = sum(x.numel() * x.element_size() for x in grads)
     return dict(step=step, e2e_step=e2e_step, e2e_begin=e2e_begin, e2e_end=e2e_end, units=Bn * H * T, h2d=h2d,
                 d2h=d2h, launches=launches, flush=True, abytes=algorithmic_bytes(cfg), aflops=algorithmic_flops(cfg))
 
@@ -603,6 +716,8 @@ def main():
 
     if kind in ("decode", "gdn_decode"):
         w = decode_workload(cfg, dev, rank, binding, synth, torch)
+    elif kind == "mamba2_bwd":
+        w = backward_workload(cfg, dev, rank, binding, synth, torch)
     else:
         w = forward_workload(cfg, dev, rank, binding, synth, torch)
     l2 = torch.cuda.get_device_properties(dev).L2_cache_size
@@ -675,7 +790,7 @@ def main():
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic, "peak_source": f"{src} (HBM copy)",
                     "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname}
-    elif kind in ("gdn", "gdn_b"):
+    elif kind in ("gdn", "gdn_b", "mamba2_bwd"):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
         aflops = w["aflops"]
