@@ -428,6 +428,479 @@ __global__ void __launch_bounds__(kSuffixThreads) bwd_suffix_kernel(const float*
   }
 }
 
+// ------------------------------------------------ d_k = d_v = 128, 64-token chunks
+// The same five steps with register tiles: every product is an outer-product
+// loop over shared-memory tiles in which a thread keeps a 4 x 8 (or 8 x 8)
+// block of the result in registers and reads one or two 128-bit words of each
+// operand per step, instead of one output per thread with two loads per FMA.
+namespace fast {
+
+constexpr int kC = 64, kD = 128;
+constexpr int kP = kD + 4;   // pitch of [rows][128] tiles: rows 16-byte aligned, 4 banks apart
+constexpr int kPc = kC + 4;  // pitch of [rows][64] tiles
+
+// 4 consecutive io elements as floats (16-byte aligned float rows, 8-byte bf16)
+__device__ __forceinline__ float4 load4(const float* p) { return *reinterpret_cast<const float4*>(p); }
+__device__ __forceinline__ float4 load4(const __nv_bfloat16* p) {
+  const uint2 u = *reinterpret_cast<const uint2*>(p);
+  const float2 a = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.x));
+  const float2 b = __bfloat1622float2(*reinterpret_cast<const __nv_bfloat162*>(&u.y));
+  return make_float4(a.x, a.y, b.x, b.y);
+}
+__device__ __forceinline__ void store4(float* p, float4 v) { *reinterpret_cast<float4*>(p) = v; }
+__device__ __forceinline__ void store4(__nv_bfloat16* p, float4 v) {
+  __nv_bfloat162 a = __floats2bfloat162_rn(v.x, v.y), b = __floats2bfloat162_rn(v.z, v.w);
+  uint2 u;
+  u.x = *reinterpret_cast<unsigned*>(&a);
+  u.y = *reinterpret_cast<unsigned*>(&b);
+  *reinterpret_cast<uint2*>(p) = u;
+}
+
+// rows [0, nv) of a [64][128] io tile into shared [64][kP] floats; rows >= nv are 0
+template <typename IO>
+__device__ __forceinline__ void load_tile(float* dst, const IO* src, int nv, int tid) {
+#pragma unroll 4
+  for (int x = tid; x < kC * kD / 4; x += 256) {
+    const int r = x >> 5, c4 = (x & 31) * 4;
+    const float4 v = r < nv ? load4(src + (size_t)r * kD + c4) : make_float4(0.f, 0.f, 0.f, 0.f);
+    store4(dst + r * kP + c4, v);
+  }
+}
+
+// C[m][n] += sum_k At[k][m] B[k][n] for m = 4ty + i (64 rows), n = 4tx + j and
+// 64 + 4tx + j (128 columns); optional per-k scale of At
+template <bool kScale>
+__device__ __forceinline__ void tn64x128(float (&c)[4][8], const float* At, int lda, const float* B, int K,
+                                         const float* scale, int ty, int tx) {
+#pragma unroll 4
+  for (int k = 0; k < K; ++k) {
+    float4 a = load4(At + k * lda + 4 * ty);
+    if (kScale) {
+      const float s = scale[k];
+      a.x *= s; a.y *= s; a.z *= s; a.w *= s;
+    }
+    const float4 b0 = load4(B + k * kP + 4 * tx), b1 = load4(B + k * kP + 64 + 4 * tx);
+    const float av[4] = {a.x, a.y, a.z, a.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 4; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
+  }
+}
+
+// C[m][n] += sum_k s_k A[k][m] B[k][n] for m, n in {4t + i, 64 + 4t + i}: 128 x 128, TN
+template <bool kScale>
+__device__ __forceinline__ void tn128x128(float (&c)[8][8], const float* A, const float* B, int K,
+                                          const float* scale, int ty, int tx) {
+#pragma unroll 2
+  for (int k = 0; k < K; ++k) {
+    float4 a0 = load4(A + k * kP + 4 * ty), a1 = load4(A + k * kP + 64 + 4 * ty);
+    if (kScale) {
+      const float s = scale[k];
+      a0.x *= s; a0.y *= s; a0.z *= s; a0.w *= s;
+      a1.x *= s; a1.y *= s; a1.z *= s; a1.w *= s;
+    }
+    const float4 b0 = load4(B + k * kP + 4 * tx), b1 = load4(B + k * kP + 64 + 4 * tx);
+    const float av[8] = {a0.x, a0.y, a0.z, a0.w, a1.x, a1.y, a1.z, a1.w};
+    const float bv[8] = {b0.x, b0.y, b0.z, b0.w, b1.x, b1.y, b1.z, b1.w};
+#pragma unroll
+    for (int i = 0; i < 8; ++i)
+#pragma unroll
+      for (int j = 0; j < 8; ++j) c[i][j] = fmaf(av[i], bv[j], c[i][j]);
+  }
+}
+
+// C[m][n] += sum_k A[m][k] B[n][k] (both k-contiguous, K = 128) for
+// m = ty + 16 r (R rows), n = tx + 16 s (S columns)
+template <int R, int S>
+__device__ __forceinline__ void nt(float (&c)[R][S], const float* A, const float* B, int ty, int tx) {
+#pragma unroll 2
+  for (int k = 0; k < kD; k += 4) {
+    float4 a[R], b[S];
+#pragma unroll
+    for (int r = 0; r < R; ++r) a[r] = load4(A + (ty + 16 * r) * kP + k);
+#pragma unroll
+    for (int s = 0; s < S; ++s) b[s] = load4(B + (tx + 16 * s) * kP + k);
+#pragma unroll
+    for (int r = 0; r < R; ++r)
+#pragma unroll
+      for (int s = 0; s < S; ++s) {
+        c[r][s] = fmaf(a[r].x, b[s].x, c[r][s]);
+        c[r][s] = fmaf(a[r].y, b[s].y, c[r][s]);
+        c[r][s] = fmaf(a[r].z, b[s].z, c[r][s]);
+        c[r][s] = fmaf(a[r].w, b[s].w, c[r][s]);
+      }
+  }
+}
+
+__device__ __forceinline__ void chunk_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
+  double acc = 0.0;
+  for (int i = 0; i < kC; ++i) {
+    if (i < nv) acc += (double)log_alpha[row0 + i];
+    cs[i] = acc;
+  }
+}
+
+// rows 4ty + i of a 64 x 128 register tile to a float32 [.][128] array (rows < nv)
+__device__ __forceinline__ void store_rows(float* dst, const float (&c)[4][8], int nv, int ty, int tx) {
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = 4 * ty + i;
+    if (m < nv) {
+      store4(dst + (size_t)m * kD + 4 * tx, make_float4(c[i][0], c[i][1], c[i][2], c[i][3]));
+      store4(dst + (size_t)m * kD + 64 + 4 * tx, make_float4(c[i][4], c[i][5], c[i][6], c[i][7]));
+    }
+  }
+}
+
+constexpr size_t intra_smem() { return sizeof(float) * (4 * kC * kP + 4 * kC * kPc + kC) + sizeof(double) * kC; }
+constexpr size_t query_smem() {
+  return sizeof(float) * (2 * kC * kP + kD * kPc + kD * kP + 2 * kC) + sizeof(double) * kC;
+}
+constexpr size_t key_smem() { return sizeof(float) * (kC * kP + kD * kPc + kD * kP + kC) + sizeof(double) * kC; }
+
+// (1) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(256, 1) bwd_intra128_kernel(
+    const IO* __restrict__ q, const IO* __restrict__ k, const IO* __restrict__ v, const IO* __restrict__ dout,
+    const float* __restrict__ log_alpha, const float* __restrict__ lam, float* __restrict__ dq32,
+    float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam, float* __restrict__ S,
+    double* __restrict__ tot, float* __restrict__ R, int T, int L) {
+  extern __shared__ __align__(16) float sm[];
+  float* qs = sm;                 // [64][kP]
+  float* ks = qs + kC * kP;
+  float* vs = ks + kC * kP;
+  float* gs = vs + kC * kP;       // dO
+  float* P = gs + kC * kP;        // [64][kPc] A . M
+  float* dA = P + kC * kPc;       // [64][kPc] dP . M
+  float* dAt = dA + kC * kPc;     // its transpose
+  float* X = dAt + kC * kPc;      // dP . A . Gamma
+  float* wdec = X + kC * kPc;     // [64]
+  double* cs = reinterpret_cast<double*>(wdec + kC);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const size_t row0 = bh * T + (size_t)c * kC;
+  const int nv = min(kC, T - c * kC);
+  if (tid == 0) {
+    chunk_cumsum(cs, log_alpha, row0, nv);
+    tot[bh * N + c] = cs[kC - 1];
+  }
+  load_tile(qs, q + row0 * kD, nv, tid);
+  load_tile(ks, k + row0 * kD, nv, tid);
+  load_tile(vs, v + row0 * kD, nv, tid);
+  load_tile(gs, dout + row0 * kD, nv, tid);
+  __syncthreads();
+  if (tid < kC) wdec[tid] = expf((float)(cs[kC - 1] - cs[tid]));
+  {
+    float a[4][4] = {}, g[4][4] = {};
+    nt<4, 4>(a, qs, ks, ty, tx);
+    nt<4, 4>(g, gs, vs, ty, tx);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int i = ty + 16 * r;
+#pragma unroll
+      for (int s = 0; s < 4; ++s) {
+        const int j = tx + 16 * s;
+        float p = 0.f, da = 0.f, xx = 0.f;
+        if (j <= i && i < nv) {
+          const float ex = expf((float)(cs[i] - cs[j]));
+          const float lm = lam[(row0 + i) * L + bitlen((unsigned)(i ^ j))];
+          p = a[r][s] * ex * lm;
+          da = g[r][s] * ex * lm;
+          xx = g[r][s] * a[r][s] * ex;
+        }
+        P[i * kPc + j] = p;
+        dA[i * kPc + j] = da;
+        dAt[j * kPc + i] = da;
+        X[i * kPc + j] = xx;
+      }
+    }
+  }
+  __syncthreads();
+  {
+    float cq[4][8] = {};
+    tn64x128<false>(cq, dAt, kPc, ks, kC, nullptr, ty, tx);  // dq = dA K
+    store_rows(dq32 + row0 * kD, cq, nv, ty, tx);
+  }
+  {
+    float ck[4][8] = {};
+    tn64x128<false>(ck, dA, kPc, qs, kC, nullptr, ty, tx);  // dk = dA^T Q
+    store_rows(dk32 + row0 * kD, ck, nv, ty, tx);
+  }
+  {
+    float cv[4][8] = {};
+    tn64x128<false>(cv, P, kPc, gs, kC, nullptr, ty, tx);  // dv = P^T dO
+    store_rows(dv32 + row0 * kD, cv, nv, ty, tx);
+  }
+  // levels 0..6 of dlam (level l >= 1: the lower half of the aligned block of 2^l rows)
+  const int nl = min(7, L);
+  for (int x = tid; x < nv * nl; x += 256) {
+    const int i = x / nl, l = x % nl;
+    float acc = 0.f;
+    if (l == 0) {
+      acc = X[i * kPc + i];
+    } else if ((i >> (l - 1)) & 1) {
+      const int lo = (i >> l) << l;
+      for (int j = lo; j < lo + (1 << (l - 1)); ++j) acc += X[i * kPc + j];
+    }
+    dlam[(row0 + i) * L + l] = acc;
+  }
+  {  // chunk state S_c = (wdec V)^T K; the key-side node of c starts at 0
+    float cs8[8][8] = {};
+    tn128x128<true>(cs8, vs, ks, kC, wdec, ty, tx);
+    float* Sc = S + (bh * N + c) * (size_t)(kD * kD);
+    float* Rc = R + (bh * N + c) * (size_t)(kD * kD);
+    const float4 z = make_float4(0.f, 0.f, 0.f, 0.f);
+#pragma unroll
+    for (int i = 0; i < 8; ++i) {
+      const int e = (i < 4 ? 0 : 64) + 4 * ty + (i & 3);
+      store4(Sc + e * kD + 4 * tx, make_float4(cs8[i][0], cs8[i][1], cs8[i][2], cs8[i][3]));
+      store4(Sc + e * kD + 64 + 4 * tx, make_float4(cs8[i][4], cs8[i][5], cs8[i][6], cs8[i][7]));
+      store4(Rc + e * kD + 4 * tx, z);
+      store4(Rc + e * kD + 64 + 4 * tx, z);
+    }
+  }
+}
+
+// (3) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(256, 1) bwd_query128_kernel(
+    const IO* __restrict__ q, const IO* __restrict__ dout, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ F, const double* __restrict__ G, const float* dq32,
+    IO* dq, float* __restrict__ dlam, float* __restrict__ R, int T, int L) {
+  extern __shared__ __align__(16) float sm[];
+  float* qs = sm;              // [64][kP]
+  float* gs = qs + kC * kP;    // [64][kP] dO
+  float* gT = gs + kC * kP;    // [128][kPc] dO transposed
+  float* Fs = gT + kD * kPc;   // [128][kP]
+  float* w = Fs + kD * kP;     // [64] exp(cs_i + D)
+  float* lw = w + kC;          // [64] lam_i[level] exp(cs_i + D)
+  double* cs = reinterpret_cast<double*>(lw + kC);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const size_t row0 = bh * T + (size_t)c * kC;
+  const int nv = min(kC, T - c * kC);
+  constexpr int lc = 6;
+  if (tid == 0) chunk_cumsum(cs, log_alpha, row0, nv);
+  load_tile(qs, q + row0 * kD, nv, tid);
+  load_tile(gs, dout + row0 * kD, nv, tid);
+  __syncthreads();
+  // transpose dO: a warp takes 32 consecutive rows of one 4-column group
+  for (int x = tid; x < kC * kD / 4; x += 256) {
+    const int i = x & 63, e4 = (x >> 6) * 4;
+    const float4 t = load4(gs + i * kP + e4);
+    gT[(e4 + 0) * kPc + i] = t.x;
+    gT[(e4 + 1) * kPc + i] = t.y;
+    gT[(e4 + 2) * kPc + i] = t.z;
+    gT[(e4 + 3) * kPc + i] = t.w;
+  }
+  float acc[4][8] = {};
+  const size_t mat = (size_t)kD * kD;
+  double D = 0.0;
+  for (int h = 0; (c >> h) != 0; ++h) {
+    if (!((c >> h) & 1)) continue;
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    const int lv = lc + 1 + h;
+    const float* Fe = F + (bh * N + e) * mat;
+    for (int x = tid; x < kD * kD / 4; x += 256) {
+      const int r = x >> 5, c4 = (x & 31) * 4;
+      store4(Fs + r * kP + c4, load4(Fe + r * kD + c4));
+    }
+    if (tid < kC) {
+      const float wi = tid < nv ? expf((float)(cs[tid] + D)) : 0.f;
+      w[tid] = wi;
+      lw[tid] = tid < nv ? wi * lam[(row0 + tid) * L + lv] : 0.f;
+    }
+    __syncthreads();
+    {  // g_i = F^T do_i (unscaled): dq_i += lw_i g_i, dlam_i = w_i g_i . q_i
+      float cg[4][8] = {};
+      tn64x128<false>(cg, gT, kPc, Fs, kD, nullptr, ty, tx);
+#pragma unroll
+      for (int i = 0; i < 4; ++i) {
+        const int m = 4 * ty + i;
+        const float lwm = lw[m];
+        float part = 0.f;
+#pragma unroll
+        for (int j = 0; j < 8; ++j) {
+          const int n = (j < 4 ? 0 : 64) + 4 * tx + (j & 3);
+          acc[i][j] = fmaf(lwm, cg[i][j], acc[i][j]);
+          part = fmaf(cg[i][j], qs[m * kP + n], part);
+        }
+#pragma unroll
+        for (int o = 8; o > 0; o >>= 1) part += __shfl_xor_sync(0xffffffffu, part, o);
+        if (tx == 0 && m < nv) dlam[(row0 + m) * L + lv] = w[m] * part;
+      }
+    }
+    {  // R_e += sum_i lw_i do_i q_i^T
+      float cr[8][8] = {};
+      tn128x128<true>(cr, gs, qs, kC, lw, ty, tx);
+      float* Re = R + (bh * N + e) * mat;
+#pragma unroll
+      for (int i = 0; i < 8; ++i) {
+        const int ev = (i < 4 ? 0 : 64) + 4 * ty + (i & 3);
+        atomicAdd(reinterpret_cast<float4*>(Re + ev * kD + 4 * tx),
+                  make_float4(cr[i][0], cr[i][1], cr[i][2], cr[i][3]));
+        atomicAdd(reinterpret_cast<float4*>(Re + ev * kD + 64 + 4 * tx),
+                  make_float4(cr[i][4], cr[i][5], cr[i][6], cr[i][7]));
+      }
+    }
+    D += G[bh * N + e];
+    __syncthreads();
+  }
+  // the levels above 6 that hold no key of this chunk's queries
+  const int nh = L - (lc + 1);
+  for (int x = tid; x < nv * max(nh, 0); x += 256) {
+    const int i = x / nh, hh = x % nh;
+    if (!(hh < 31 && ((c >> hh) & 1))) dlam[(row0 + i) * L + lc + 1 + hh] = 0.f;
+  }
+#pragma unroll
+  for (int i = 0; i < 4; ++i) {
+    const int m = 4 * ty + i;
+    if (m < nv) {
+      const size_t o = (row0 + m) * kD;
+      const float4 p0 = load4(dq32 + o + 4 * tx), p1 = load4(dq32 + o + 64 + 4 * tx);
+      store4(dq + o + 4 * tx, make_float4(p0.x + acc[i][0], p0.y + acc[i][1], p0.z + acc[i][2], p0.w + acc[i][3]));
+      store4(dq + o + 64 + 4 * tx,
+             make_float4(p1.x + acc[i][4], p1.y + acc[i][5], p1.z + acc[i][6], p1.w + acc[i][7]));
+    }
+  }
+}
+
+// (4) one CTA per (chunk, head)
+template <typename IO>
+__global__ void __launch_bounds__(256, 1) bwd_key128_kernel(
+    const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
+    const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv, float* __restrict__ dc,
+    double* __restrict__ ctot, int T, int L) {
+  extern __shared__ __align__(16) float sm[];
+  __shared__ float coef[32];
+  __shared__ int ent[32];
+  __shared__ int n_sh;
+  __shared__ float dcrow[kC];
+  float* ks = sm;              // [64][kP]
+  float* vT = ks + kC * kP;    // [128][kPc] V transposed
+  float* Es = vT + kD * kPc;   // [128][kP]; first the staging of V
+  float* wdec = Es + kD * kP;  // [64]
+  double* cs = reinterpret_cast<double*>(wdec + kC);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
+  const size_t row0 = bh * T + (size_t)c * kC;
+  const int nv = min(kC, T - c * kC);
+  if (tid == 0) {
+    chunk_cumsum(cs, log_alpha, row0, nv);
+    int n = 0, cc = c;
+    double dec = 0.0;  // log-decay from the end of c to the end of e
+    for (int h = 0; h < 31 && n < 32; ++h) {
+      if ((c >> h) & 1) continue;
+      const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+      if (e + 1 >= N) break;  // e grows with h: no later node has queries either
+      while (cc < e) dec += tot[bh * N + (++cc)];
+      ent[n] = e;
+      coef[n] = expf((float)dec);
+      ++n;
+    }
+    n_sh = n;
+  }
+  load_tile(ks, k + row0 * kD, nv, tid);
+  load_tile(Es, v + row0 * kD, nv, tid);
+  __syncthreads();
+  for (int x = tid; x < kC * kD / 4; x += 256) {
+    const int j = x & 63, e4 = (x >> 6) * 4;
+    const float4 t = load4(Es + j * kP + e4);
+    vT[(e4 + 0) * kPc + j] = t.x;
+    vT[(e4 + 1) * kPc + j] = t.y;
+    vT[(e4 + 2) * kPc + j] = t.z;
+    vT[(e4 + 3) * kPc + j] = t.w;
+  }
+  if (tid < kC) wdec[tid] = expf((float)(cs[kC - 1] - cs[tid]));
+  const int n = n_sh;
+  __syncthreads();
+  const size_t mat = (size_t)kD * kD;
+  if (n > 0) {
+    for (int x = tid; x < kD * kD / 4; x += 256) {
+      const int r = x >> 5, c4 = (x & 31) * 4;
+      float4 a = make_float4(0.f, 0.f, 0.f, 0.f);
+      for (int m = 0; m < n; ++m) {
+        const float4 t = load4(R + (bh * N + ent[m]) * mat + r * kD + c4);
+        const float cf = coef[m];
+        a.x = fmaf(cf, t.x, a.x); a.y = fmaf(cf, t.y, a.y); a.z = fmaf(cf, t.z, a.z); a.w = fmaf(cf, t.w, a.w);
+      }
+      store4(Es + r * kP + c4, a);
+    }
+    __syncthreads();
+  }
+  {  // dv_j = dv32_j + wdec_j E k_j (rows j = ty + 16 r, columns e = tx + 16 s), and v_j . dv_j
+    float cv[4][8] = {};
+    if (n > 0) nt<4, 8>(cv, ks, Es, ty, tx);
+#pragma unroll
+    for (int r = 0; r < 4; ++r) {
+      const int j = ty + 16 * r;
+      float vdv = 0.f;
+#pragma unroll
+      for (int s = 0; s < 8; ++s) {
+        const int e = tx + 16 * s;
+        if (j < nv) {
+          const size_t o = (row0 + j) * kD + e;
+          const float val = fmaf(wdec[j], cv[r][s], dv32[o]);
+          dv[o] = from_f<IO>(val);
+          vdv = fmaf(vT[e * kPc + j], val, vdv);
+        }
+      }
+#pragma unroll
+      for (int o = 8; o > 0; o >>= 1) vdv += __shfl_xor_sync(0xffffffffu, vdv, o);
+      if (tx == 0) dcrow[j] = -vdv;
+    }
+  }
+  {  // dk_j = dk32_j + wdec_j E^T v_j
+    float ck[4][8] = {};
+    if (n > 0) tn64x128<false>(ck, vT, kPc, Es, kD, nullptr, ty, tx);
+#pragma unroll
+    for (int i = 0; i < 4; ++i) {
+      const int m = 4 * ty + i;
+      if (m < nv) {
+        const size_t o = (row0 + m) * kD;
+        const float wm = wdec[m];
+        const float4 p0 = load4(dk32 + o + 4 * tx), p1 = load4(dk32 + o + 64 + 4 * tx);
+        store4(dk + o + 4 * tx, make_float4(fmaf(wm, ck[i][0], p0.x), fmaf(wm, ck[i][1], p0.y),
+                                            fmaf(wm, ck[i][2], p0.z), fmaf(wm, ck[i][3], p0.w)));
+        store4(dk + o + 64 + 4 * tx, make_float4(fmaf(wm, ck[i][4], p1.x), fmaf(wm, ck[i][5], p1.y),
+                                                 fmaf(wm, ck[i][6], p1.z), fmaf(wm, ck[i][7], p1.w)));
+      }
+    }
+  }
+  __syncthreads();
+  // dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j, one warp per row
+  const int warp = tid >> 5, lane = tid & 31;
+  for (int j = warp; j < kC; j += 8) {
+    float a = 0.f;
+    if (j < nv)
+      for (int l = lane; l < L; l += 32) a = fmaf(lam[(row0 + j) * L + l], dlam[(row0 + j) * L + l], a);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
+    if (lane == 0) {
+      a += dcrow[j];
+      if (j < nv) dc[row0 + j] = a;
+      dcrow[j] = a;
+    }
+  }
+  __syncthreads();
+  if (tid == 0) {
+    double a = 0.0;
+    for (int j = 0; j < nv; ++j) a += (double)dcrow[j];
+    ctot[bh * N + c] = a;
+  }
+}
+
+}  // namespace fast
+
+// d_k = d_v = 128 with 64-token chunks runs on the register-tiled kernels
+bool fast_shape(const ll_shape& s, const BwdPlan& p) { return s.dk == 128 && s.dv == 128 && p.Ce == 64; }
+
 template <typename IO>
 ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const ll_shape& s = a.s;
@@ -447,6 +920,34 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const int Ce = p.Ce;
   const int mat = s.dv * s.dk;
   const dim3 grid(p.N, BH);
+  const IO* q = static_cast<const IO*>(a.q);
+  const IO* k = static_cast<const IO*>(a.k);
+  const IO* v = static_cast<const IO*>(a.v);
+  const IO* dout = static_cast<const IO*>(a.dout);
+
+  if (fast_shape(s, p)) {
+    LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_intra128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)fast::intra_smem()));
+    fast::bwd_intra128_kernel<IO><<<grid, 256, fast::intra_smem(), a.stream>>>(
+        q, k, v, dout, a.log_alpha, a.lam, dq32, dk32, dv32, a.dlam, S, tot, R, s.T, s.L);
+    LL_CUDA_OK(cudaGetLastError());
+    const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream);
+    if (fs != LL_OK) return fs;
+    LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_query128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)fast::query_smem()));
+    fast::bwd_query128_kernel<IO><<<grid, 256, fast::query_smem(), a.stream>>>(
+        q, dout, a.log_alpha, a.lam, F, G, dq32, static_cast<IO*>(a.dq), a.dlam, R, s.T, s.L);
+    LL_CUDA_OK(cudaGetLastError());
+    LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_key128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                    (int)fast::key_smem()));
+    fast::bwd_key128_kernel<IO><<<grid, 256, fast::key_smem(), a.stream>>>(
+        k, v, a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32, static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc,
+        ctot, s.T, s.L);
+    LL_CUDA_OK(cudaGetLastError());
+    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+    LL_CUDA_OK(cudaGetLastError());
+    return LL_OK;
+  }
 
   const size_t sm1 = intra_smem(Ce, s.dk, s.dv);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_intra_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm1));

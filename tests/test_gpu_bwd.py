@@ -91,6 +91,12 @@ def test_workload_bf16_t2k(B):
     (384, 128, 64, 64, "bf16"),  # chunk 128
     (300, 64, 128, 128, "bf16"),  # d = 128, ragged
     (1000, 32, 64, 32, "f32"),   # many chunks, ragged, every level of the tree
+    # d = 128 with 64-token chunks: the register-tiled kernels
+    (640, 64, 128, 128, "f32"),   # N = 10
+    (200, 64, 128, 128, "f32"),   # ragged: 3 full chunks and 8 rows
+    (64, 64, 128, 128, "bf16"),   # one chunk
+    (1024, 128, 128, 128, "bf16"),  # chunk 128 runs as 64-token chunks
+    (1, 64, 128, 128, "f32"),     # T = 1
 ])
 def test_shapes_and_edges(B, T, chunk, dk, dv, io):
     cfg = _cfg("mamba2_fp32_t64", io=io, T=T, dk=dk, dv=dv, L=levels_needed(T), B=2, H=3)
