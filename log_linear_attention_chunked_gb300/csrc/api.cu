@@ -235,7 +235,8 @@ ll_status ll_attn_bwd(const ll_shape* s, const void* q, const void* k, const voi
   if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
   BwdArgs a{*s, q, k, v, dout, log_alpha, lam, dq, dk, dv, dlog_alpha, dlam, workspace, ws_bytes,
-            static_cast<cudaStream_t>(stream)};
+            static_cast<cudaStream_t>(stream), err_word()};
+  if (!a.err) return LL_ERR_CUDA;
   return bwd_simt_launch(a);
 }
 

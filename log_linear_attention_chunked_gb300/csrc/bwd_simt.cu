@@ -74,7 +74,8 @@ BwdPlan plan_of(const ll_shape& s) {
   BwdPlan p{};
   const int d = std::max(s.dk, s.dv);
   p.Ce = s.chunk;
-  while (p.Ce > 16 && (p.Ce * d > kMaxChunkElems || intra_smem(p.Ce, s.dk, s.dv) > kMaxSmem ||
+  if (bwd_tc_supported(s)) p.Ce = 128;  // the tensor-core kernels' tiles, whatever the chunk
+  while (!bwd_tc_supported(s) && p.Ce > 16 && (p.Ce * d > kMaxChunkElems || intra_smem(p.Ce, s.dk, s.dv) > kMaxSmem ||
                        query_smem(p.Ce, s.dk, s.dv) > kMaxSmem || key_smem(p.Ce, s.dk, s.dv) > kMaxSmem))
     p.Ce >>= 1;
   p.N = (s.T + p.Ce - 1) / p.Ce;
@@ -925,6 +926,14 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const IO* v = static_cast<const IO*>(a.v);
   const IO* dout = static_cast<const IO*>(a.dout);
 
+  if (bwd_tc_supported(s)) {
+    const BwdTcBuffers b{dq32, dk32, dv32, S, F, R, tot, G, dc, ctot, a.err};
+    const ll_status st = bwd_tc_launch(a, b);
+    if (st != LL_OK) return st;
+    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+    LL_CUDA_OK(cudaGetLastError());
+    return LL_OK;
+  }
   if (fast_shape(s, p)) {
     LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_intra128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)fast::intra_smem()));

@@ -1,0 +1,613 @@
+// Backward of the log-linear Mamba-2 forward on the tensor cores (bf16 io,
+// d_k = d_v = 128): the chunk-wise algorithm of the CUDA-core backward with
+// 128-token tiles and every product a tcgen05.mma (bf16 operands staged in
+// 128-byte-swizzled shared memory, float32 accumulators in TMEM).
+//
+// Gradient of O = (Q K^T . M) V ("Log-Linear Attention" study note §3-4
+// parallel form, §3-5 mask composition), per tile c of 128 tokens:
+//   intra : A = Q K^T and G = dO V^T (TMEM); per row i the epilogue forms
+//           P = A . M and dA = G . M (bf16 tiles) and the levels 0..7 of
+//           dlam_i = sum over keys of level l of G A Gamma; then
+//           dq = dA K, dk = dA^T Q, dv = P^T dO and the chunk state
+//           S_c = (exp(cs_end - cs) V)^T K.  The in-tile part of v_j . dv_j
+//           (for dc_j) is the column sum of P . G, taken in float32 from the
+//           accumulators rather than from the bf16-rounded P: dc_j is a
+//           difference of two terms of the size of do . o, so their rounding
+//           would not cancel.
+//   query : for every set bit h of c (node e, level 8 + h, decay D from the
+//           end of e to the start of c; w_i = exp(cs_i + D), lw_i = lam_i w_i):
+//           g = dO F_e (dlam_i = w_i g_i . q_i), dq += diag(lw) dO F_e and
+//           R_e += (diag(lw) dO)^T Q, the key-side node of e.
+//   key   : E_c = the R nodes of the blocks that hold c's keys, decayed to the
+//           end of c; dv += diag(wdec) K E^T, dk += diag(wdec) V E, and
+//           dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j (the in-tile part of
+//           v_j . dv_j from the intra kernel).
+// The Fenwick nodes F_e and the suffix sums of dc are the CUDA-core kernels'.
+//
+// One CTA of 128 threads per (tile, head); thread t owns TMEM lane t (row t of
+// every accumulator).  The phases of a tile run in sequence: stage the
+// operands, one thread issues the MMAs and commits them to an mbarrier, every
+// thread waits (bounded: after 4 s the error word is set and the kernel
+// finishes without the results), then the row-wise epilogue.
+#include "common.cuh"
+#include "sm100.cuh"
+
+namespace llattn {
+
+namespace {
+
+using namespace sm100;
+
+constexpr int kT = 128;                        // tokens per tile
+constexpr int kD = 128;
+constexpr int kThreads = 128;
+constexpr uint32_t kHalf = kT * 64 * 2;        // a [128 x 64] bf16 swizzled block
+constexpr uint32_t kTileB = 2 * kHalf;         // a [128 x 128] bf16 tile: 32 KB
+constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr int kLc = 7;                         // log2 of the tile
+
+// byte offset of the 16-byte chunk c8 (elements 8 c8 .. 8 c8 + 7) of row r of a tile
+__device__ __forceinline__ uint32_t swz(int r, int c8) {
+  return (uint32_t)(c8 >> 3) * kHalf + (uint32_t)r * 128u + ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
+}
+// K-major operand (K along the tile's columns), k-step kk of 16
+__device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
+  return sw128_desc(tile + (kk >> 2) * kHalf + (kk & 3) * 32, 16, 1024);
+}
+// MN-major operand (K along the tile's rows), k-step kk of 16 rows
+__device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, kHalf, 1024); }
+
+// D (+)= A B over K = 128
+__device__ __forceinline__ void mma128(uint32_t d, uint32_t a, bool a_mn, uint32_t b, bool b_mn, bool acc) {
+  const uint32_t id = idesc_bf16(128, 128, a_mn, b_mn);
+#pragma unroll
+  for (int kk = 0; kk < 8; ++kk)
+    umma_bf16(d, a_mn ? desc_mn(a, kk) : desc_k(a, kk), b_mn ? desc_mn(b, kk) : desc_k(b, kk), id,
+              (acc || kk > 0) ? 1u : 0u);
+}
+
+// Bounded wait of every thread for the phase with parity `par`; false after a timeout.
+__device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t par, unsigned* err, int* abort_s) {
+  if (mbar_try_wait(bar, par)) return true;
+  const uint64_t t0 = globaltimer_ns();
+  while (!mbar_try_wait(bar, par)) {
+    if (*(volatile int*)abort_s) return false;
+    if (globaltimer_ns() - t0 > kTimeoutNs) {
+      if (atomicExch(abort_s, 1) == 0) raise_error(err, kErrTimeout);
+      return false;
+    }
+  }
+  return true;
+}
+
+// a [128][128] bf16 tile of rows [0, nv) from global (rows of 256 B) into a swizzled tile; rows >= nv are 0
+__device__ __forceinline__ void stage_bf16(unsigned char* tile, const __nv_bfloat16* src, int nv, int tid) {
+#pragma unroll 4
+  for (int x = tid; x < kT * 16; x += kThreads) {
+    const int r = x >> 4, c8 = x & 15;
+    uint4 v = make_uint4(0u, 0u, 0u, 0u);
+    if (r < nv) v = *reinterpret_cast<const uint4*>(src + (size_t)r * kD + 8 * c8);
+    *reinterpret_cast<uint4*>(tile + swz(r, c8)) = v;
+  }
+}
+
+// sum_m coef[m] * src_m (float32 [128][128] matrices) as a bf16 swizzled tile
+__device__ __forceinline__ void stage_f32_sum(unsigned char* tile, const float* const* src, const float* coef, int n,
+                                              int tid) {
+#pragma unroll 2
+  for (int x = tid; x < kT * 16; x += kThreads) {
+    const int r = x >> 4, c8 = x & 15;
+    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+    for (int m = 0; m < n; ++m) {
+      const float4 u = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8);
+      const float4 w = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8 + 4);
+      const float cf = coef[m];
+      a[0] = fmaf(cf, u.x, a[0]); a[1] = fmaf(cf, u.y, a[1]); a[2] = fmaf(cf, u.z, a[2]); a[3] = fmaf(cf, u.w, a[3]);
+      a[4] = fmaf(cf, w.x, a[4]); a[5] = fmaf(cf, w.y, a[5]); a[6] = fmaf(cf, w.z, a[6]); a[7] = fmaf(cf, w.w, a[7]);
+    }
+    *reinterpret_cast<uint4*>(tile + swz(r, c8)) =
+        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+  }
+}
+
+// row r of a swizzled tile, 8 elements of chunk c8, as floats
+__device__ __forceinline__ void row_chunk(const unsigned char* tile, int r, int c8, float* x) {
+  const uint4 u = *reinterpret_cast<const uint4*>(tile + swz(r, c8));
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+}
+
+__device__ __forceinline__ void chunk_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
+  double acc = 0.0;
+  for (int i = 0; i < kT; ++i) {
+    if (i < nv) acc += (double)log_alpha[row0 + i];
+    cs[i] = acc;
+  }
+}
+
+// Common prologue: the mbarrier and the TMEM allocation (warp 0).
+template <uint32_t kCols>
+__device__ __forceinline__ uint32_t setup_tmem(uint64_t* bar, uint32_t* slot) {
+  const int warp = threadIdx.x >> 5;
+  if (threadIdx.x == 0) {
+    mbar_init(bar, 1);
+    fence_mbar_init();
+  }
+  if (warp == 0) {
+    tmem_alloc(slot, kCols);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  return *slot;
+}
+
+template <uint32_t kCols>
+__device__ __forceinline__ void release_tmem(uint32_t tmem) {
+  tc_fence_before();
+  __syncthreads();
+  if ((threadIdx.x >> 5) == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, kCols);
+  }
+}
+
+// Hand the staged tiles to the tensor cores and the TMEM columns back to them.
+__device__ __forceinline__ void to_async() {
+  fence_proxy_async_shared();
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+}
+
+// this thread's TMEM lane (row threadIdx.x) at column col
+__device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
+  return tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + (uint32_t)col;
+}
+
+// ------------------------------------------------------------------ intra
+constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
+                   kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
+constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + 64; }
+
+// Reduce-scatter over a warp: lane l receives the sum over the 32 lanes of v[l].
+__device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
+  const int lane = threadIdx.x & 31;
+#pragma unroll
+  for (int half = 16; half >= 1; half >>= 1) {
+    const bool up = lane & half;
+#pragma unroll
+    for (int u = 0; u < half; ++u) {
+      const float send = up ? v[u] : v[u + half];
+      const float keep = up ? v[u + half] : v[u];
+      v[u] = keep + __shfl_xor_sync(0xffffffffu, send, half);
+    }
+  }
+  return v[0];
+}
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
+    const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
+    float* __restrict__ dq32, float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam,
+    float* __restrict__ S, double* __restrict__ tot, float* __restrict__ R, float* __restrict__ dc, int T, int L,
+    unsigned* err) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  double* cs = reinterpret_cast<double*>(base + kIntraEnd);
+  float* wdec = reinterpret_cast<float*>(cs + kT);
+  float* colpart = wdec + kT;  // [4 warps][128 columns] of sum_i P_ij G_ij
+  uint64_t* bar = reinterpret_cast<uint64_t*>(colpart + 4 * kT);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* abort_s = reinterpret_cast<int*>(slot + 1);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const size_t row0 = bh * T + (size_t)c * kT;
+  const int nv = min(kT, T - c * kT);
+  if (tid == 0) {
+    *abort_s = 0;
+    chunk_cumsum(cs, log_alpha, row0, nv);
+    tot[bh * N + c] = cs[kT - 1];
+  }
+  const uint32_t tmem = setup_tmem<512>(bar, slot);
+  stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
+  stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
+  stage_bf16(base + kIntraV, v + row0 * kD, nv, tid);
+  stage_bf16(base + kIntraG, dout + row0 * kD, nv, tid);
+  to_async();
+  const uint32_t sQ = smem_u32(base + kIntraQ), sK = smem_u32(base + kIntraK), sV = smem_u32(base + kIntraV),
+                 sG = smem_u32(base + kIntraG), sP = smem_u32(base + kIntraP), sA = smem_u32(base + kIntraA);
+  if (tid == 0) {
+    mma128(tmem + 0, sQ, false, sK, false, false);    // A = Q K^T
+    mma128(tmem + 128, sG, false, sV, false, false);  // G = dO V^T
+    umma_commit(bar);
+  }
+  bool ok = wait_phase(bar, 0, err, abort_s);
+  tc_fence_after();
+  wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+  {
+    // row i = tid: P, dA (bf16) and the in-tile levels of dlam
+    const int i = tid;
+    float lm[8], dl[8];
+#pragma unroll
+    for (int l = 0; l < 8; ++l) {
+      lm[l] = (i < nv && l < L) ? lam[(row0 + i) * L + l] : 0.f;
+      dl[l] = 0.f;
+    }
+    const double csi = cs[i];
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      float a[32], g[32];
+      tmem_ld32(lane_addr(tmem, 32 * cb), a);
+      tmem_ld32(lane_addr(tmem, 128 + 32 * cb), g);
+      tmem_ld_wait();
+      float p[32], da[32];
+#pragma unroll
+      for (int u = 0; u < 32; ++u) {
+        const int j = 32 * cb + u;
+        p[u] = 0.f;
+        da[u] = 0.f;
+        if (j <= i && i < nv) {
+          const float ex = expf((float)(csi - cs[j]));
+          const int lv = bitlen((unsigned)(i ^ j));
+          float lmv = lm[0];
+#pragma unroll
+          for (int l = 1; l < 8; ++l) lmv = lv == l ? lm[l] : lmv;
+          p[u] = a[u] * ex * lmv;
+          da[u] = g[u] * ex * lmv;
+          const float xx = g[u] * a[u] * ex;
+#pragma unroll
+          for (int l = 0; l < 8; ++l) dl[l] += lv == l ? xx : 0.f;
+        }
+      }
+      {  // v_j . dv_j inside the tile is the column sum of P . G, kept in float32
+        float pg[32];
+#pragma unroll
+        for (int u = 0; u < 32; ++u) pg[u] = p[u] * g[u];
+        colpart[(tid >> 5) * kT + 32 * cb + (tid & 31)] = warp_column_sums(pg);
+      }
+#pragma unroll
+      for (int w = 0; w < 4; ++w) {
+        const int c8 = 4 * cb + w;
+        *reinterpret_cast<uint4*>(base + kIntraP + swz(i, c8)) =
+            make_uint4(pack_bf16x2(p[8 * w], p[8 * w + 1]), pack_bf16x2(p[8 * w + 2], p[8 * w + 3]),
+                       pack_bf16x2(p[8 * w + 4], p[8 * w + 5]), pack_bf16x2(p[8 * w + 6], p[8 * w + 7]));
+        *reinterpret_cast<uint4*>(base + kIntraA + swz(i, c8)) =
+            make_uint4(pack_bf16x2(da[8 * w], da[8 * w + 1]), pack_bf16x2(da[8 * w + 2], da[8 * w + 3]),
+                       pack_bf16x2(da[8 * w + 4], da[8 * w + 5]), pack_bf16x2(da[8 * w + 6], da[8 * w + 7]));
+      }
+    }
+    if (i < nv)
+      for (int l = 0; l < 8 && l < L; ++l) dlam[(row0 + i) * L + l] = dl[l];
+  }
+  __syncthreads();  // wdec and the column sums of every row
+  if (tid < nv)  // the in-tile part of -v_j . dv_j; the key side adds the rest of dc_j
+    dc[row0 + tid] = -(colpart[tid] + colpart[kT + tid] + colpart[2 * kT + tid] + colpart[3 * kT + tid]);
+  // V rows scaled by wdec (the G product that read V has completed)
+  {
+    const int j = tid;
+    const float s = wdec[j];
+#pragma unroll 4
+    for (int c8 = 0; c8 < 16; ++c8) {
+      float x[8];
+      row_chunk(base + kIntraV, j, c8, x);
+      *reinterpret_cast<uint4*>(base + kIntraV + swz(j, c8)) =
+          make_uint4(pack_bf16x2(s * x[0], s * x[1]), pack_bf16x2(s * x[2], s * x[3]),
+                     pack_bf16x2(s * x[4], s * x[5]), pack_bf16x2(s * x[6], s * x[7]));
+    }
+  }
+  tmem_ld_wait();
+  to_async();
+  if (tid == 0 && ok) {
+    mma128(tmem + 0, sA, false, sK, true, false);    // dq = dA K
+    mma128(tmem + 128, sA, true, sQ, true, false);   // dk = dA^T Q
+    mma128(tmem + 256, sP, true, sG, true, false);   // dv = P^T dO
+    mma128(tmem + 384, sV, true, sK, true, false);   // S_c = (wdec V)^T K
+    umma_commit(bar);
+  }
+  ok = ok && wait_phase(bar, 1, err, abort_s);
+  tc_fence_after();
+  {
+    const int r = tid;
+    float* outs[4] = {dq32 + (row0 + r) * kD, dk32 + (row0 + r) * kD, dv32 + (row0 + r) * kD,
+                      S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD};
+#pragma unroll 1
+    for (int o = 0; o < 4; ++o) {
+      const bool keep = o == 3 || r < nv;  // S has every row; the gradients only the present ones
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float x[32];
+        tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
+        tmem_ld_wait();
+        if (keep)
+#pragma unroll
+          for (int u = 0; u < 32; u += 4)
+            *reinterpret_cast<float4*>(outs[o] + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+      }
+    }
+    float* Rc = R + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD;
+#pragma unroll 8
+    for (int u = 0; u < kD; u += 4) *reinterpret_cast<float4*>(Rc + u) = make_float4(0.f, 0.f, 0.f, 0.f);
+  }
+  release_tmem<512>(tmem);
+}
+
+// ------------------------------------------------------------------ query side
+constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryEnd = 4 * kTileB;
+constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
+    const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ F, const double* __restrict__ G,
+    const float* __restrict__ dq32, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam, float* __restrict__ R,
+    int T, int L, unsigned* err) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  double* cs = reinterpret_cast<double*>(base + kQryEnd);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(cs + kT);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* abort_s = reinterpret_cast<int*>(slot + 1);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const size_t row0 = bh * T + (size_t)c * kT;
+  const int nv = min(kT, T - c * kT);
+  if (tid == 0) {
+    *abort_s = 0;
+    chunk_cumsum(cs, log_alpha, row0, nv);
+  }
+  const uint32_t tmem = setup_tmem<512>(bar, slot);
+  stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
+  stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
+  __syncthreads();
+  const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
+                 sF = smem_u32(base + kQryF);
+  const size_t mat = (size_t)kD * kD;
+  const int i = tid;
+  double D = 0.0;
+  bool ok = true, first = true;
+  uint32_t phase = 0;
+  for (int h = 0; (c >> h) != 0; ++h) {
+    if (!((c >> h) & 1)) continue;
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    const int lv = kLc + 1 + h;
+    const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
+    const float lw = i < nv ? w * lam[(row0 + i) * L + lv] : 0.f;
+    // dO rows scaled by lw, and the node F_e in bf16
+#pragma unroll 4
+    for (int c8 = 0; c8 < 16; ++c8) {
+      float x[8];
+      row_chunk(base + kQryG, i, c8, x);
+      *reinterpret_cast<uint4*>(base + kQryL + swz(i, c8)) =
+          make_uint4(pack_bf16x2(lw * x[0], lw * x[1]), pack_bf16x2(lw * x[2], lw * x[3]),
+                     pack_bf16x2(lw * x[4], lw * x[5]), pack_bf16x2(lw * x[6], lw * x[7]));
+    }
+    const float* Fe = F + (bh * N + e) * mat;
+    const float one = 1.f;
+    stage_f32_sum(base + kQryF, &Fe, &one, 1, tid);
+    to_async();
+    if (tid == 0 && ok) {
+      mma128(tmem + 0, sG, false, sF, true, false);    // g = dO F_e
+      mma128(tmem + 128, sL, false, sF, true, !first); // dq += diag(lw) dO F_e
+      mma128(tmem + 256, sL, true, sQ, true, false);   // R_e part = (diag(lw) dO)^T Q
+      umma_commit(bar);
+    }
+    first = false;
+    ok = ok && wait_phase(bar, phase, err, abort_s);
+    phase ^= 1;
+    tc_fence_after();
+    {
+      float part = 0.f;
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float g[32];
+        tmem_ld32(lane_addr(tmem, 32 * cb), g);
+        tmem_ld_wait();
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          float x[8];
+          row_chunk(base + kQryQ, i, 4 * cb + w4, x);
+#pragma unroll
+          for (int u = 0; u < 8; ++u) part = fmaf(g[8 * w4 + u], x[u], part);
+        }
+      }
+      if (i < nv) dlam[(row0 + i) * L + lv] = w * part;
+      float* Re = R + (bh * N + e) * mat + (size_t)i * kD;  // row e' = i of R_e
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float x[32];
+        tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
+        tmem_ld_wait();
+        if (ok)
+#pragma unroll
+          for (int u = 0; u < 32; u += 4)
+            atomicAdd(reinterpret_cast<float4*>(Re + 32 * cb + u), make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]));
+      }
+    }
+    D += G[bh * N + e];
+    tc_fence_before();
+    __syncthreads();  // the next level rewrites the staged tiles and the TMEM columns
+  }
+  // the levels above 7 that hold no key of this tile's queries
+  if (i < nv)
+    for (int l = kLc + 1; l < L; ++l) {
+      const int hh = l - kLc - 1;
+      if (!(hh < 31 && ((c >> hh) & 1))) dlam[(row0 + i) * L + l] = 0.f;
+    }
+  {
+    const float* src = dq32 + (row0 + i) * kD;
+    __nv_bfloat16* dst = dq + (row0 + i) * kD;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      float x[32];
+      if (!first) {  // uniform over the CTA: the warp-collective loads run in every lane
+        tmem_ld32(lane_addr(tmem, 128 + 32 * cb), x);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = 0.f;
+      }
+      if (i < nv)
+#pragma unroll
+      for (int u = 0; u < 32; u += 8) {
+        const float4 a = *reinterpret_cast<const float4*>(src + 32 * cb + u);
+        const float4 b = *reinterpret_cast<const float4*>(src + 32 * cb + u + 4);
+        *reinterpret_cast<uint4*>(dst + 32 * cb + u) =
+            make_uint4(pack_bf16x2(a.x + x[u], a.y + x[u + 1]), pack_bf16x2(a.z + x[u + 2], a.w + x[u + 3]),
+                       pack_bf16x2(b.x + x[u + 4], b.y + x[u + 5]), pack_bf16x2(b.z + x[u + 6], b.w + x[u + 7]));
+      }
+    }
+  }
+  release_tmem<512>(tmem);
+}
+
+// ------------------------------------------------------------------ key side
+constexpr uint32_t kKeyK = 0, kKeyV = kTileB, kKeyE = 2 * kTileB, kKeyEnd = 3 * kTileB;
+constexpr size_t key_smem() { return 1024 + kKeyEnd + kT * 8 + kT * 4 + kT * 4 + 32 * 12 + 64; }
+
+__global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
+    const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
+    const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
+    const double* __restrict__ tot, const float* __restrict__ dk32, const float* __restrict__ dv32,
+    __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dc,
+    double* __restrict__ ctot, int T, int L, unsigned* err) {
+  extern __shared__ unsigned char sm_raw[];
+  unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
+  double* cs = reinterpret_cast<double*>(base + kKeyEnd);
+  float* wdec = reinterpret_cast<float*>(cs + kT);
+  float* dcrow = wdec + kT;
+  float* coef = dcrow + kT;                                      // [32]
+  const float** srcs = reinterpret_cast<const float**>(coef + 32);  // [32]
+  int* n_s = reinterpret_cast<int*>(srcs + 32);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(n_s + 2);
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  int* abort_s = reinterpret_cast<int*>(slot + 1);
+  const int c = blockIdx.x, N = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x;
+  const size_t row0 = bh * T + (size_t)c * kT;
+  const int nv = min(kT, T - c * kT);
+  const size_t mat = (size_t)kD * kD;
+  if (tid == 0) {
+    *abort_s = 0;
+    chunk_cumsum(cs, log_alpha, row0, nv);
+    int n = 0, cc = c;
+    double dec = 0.0;  // log-decay from the end of c to the end of e
+    for (int h = 0; h < 31 && n < 32; ++h) {
+      if ((c >> h) & 1) continue;
+      const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+      if (e + 1 >= N) break;  // e grows with h: no later node has queries either
+      while (cc < e) dec += tot[bh * N + (++cc)];
+      srcs[n] = R + (bh * N + e) * mat;
+      coef[n] = expf((float)dec);
+      ++n;
+    }
+    *n_s = n;
+  }
+  const uint32_t tmem = setup_tmem<256>(bar, slot);
+  const int n = *n_s;
+  wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+  stage_bf16(base + kKeyK, k + row0 * kD, nv, tid);
+  stage_bf16(base + kKeyV, v + row0 * kD, nv, tid);
+  if (n > 0) stage_f32_sum(base + kKeyE, srcs, coef, n, tid);
+  to_async();
+  if (n > 0) {
+    const uint32_t sK = smem_u32(base + kKeyK), sV = smem_u32(base + kKeyV), sE = smem_u32(base + kKeyE);
+    if (tid == 0) {
+      mma128(tmem + 0, sK, false, sE, false, false);   // (E k_j) over rows j
+      mma128(tmem + 128, sV, false, sE, true, false);  // (E^T v_j) over rows j
+      umma_commit(bar);
+    }
+    wait_phase(bar, 0, err, abort_s);  // after a timeout the error word is set; the results are not used
+    tc_fence_after();
+  }
+  const int j = tid;
+  const float wj = wdec[j];
+  float vdv = 0.f;
+#pragma unroll 1
+  for (int o = 0; o < 2; ++o) {  // 0: dv, 1: dk
+    const float* src = (o == 0 ? dv32 : dk32) + (row0 + j) * kD;
+    __nv_bfloat16* dst = (o == 0 ? dv : dk) + (row0 + j) * kD;
+#pragma unroll 1
+    for (int cb = 0; cb < 4; ++cb) {
+      float x[32];
+      if (n > 0) {
+        tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);
+        tmem_ld_wait();
+      } else {
+#pragma unroll
+        for (int u = 0; u < 32; ++u) x[u] = 0.f;
+      }
+      if (j < nv) {
+#pragma unroll
+        for (int u = 0; u < 32; u += 8) {
+          const float4 a = *reinterpret_cast<const float4*>(src + 32 * cb + u);
+          const float4 b = *reinterpret_cast<const float4*>(src + 32 * cb + u + 4);
+          float y[8] = {fmaf(wj, x[u], a.x),     fmaf(wj, x[u + 1], a.y), fmaf(wj, x[u + 2], a.z),
+                        fmaf(wj, x[u + 3], a.w), fmaf(wj, x[u + 4], b.x), fmaf(wj, x[u + 5], b.y),
+                        fmaf(wj, x[u + 6], b.z), fmaf(wj, x[u + 7], b.w)};
+          if (o == 0) {  // the part of v_j . dv_j from the later tiles
+            float vv[8];
+            row_chunk(base + kKeyV, j, (32 * cb + u) >> 3, vv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) vdv = fmaf(vv[t], wj * x[u + t], vdv);
+          }
+          *reinterpret_cast<uint4*>(dst + 32 * cb + u) =
+              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                         pack_bf16x2(y[6], y[7]));
+        }
+      }
+    }
+  }
+  float a = 0.f;
+  if (j < nv) {
+    for (int l = 0; l < L; ++l) a = fmaf(lam[(row0 + j) * L + l], dlam[(row0 + j) * L + l], a);
+    a += dc[row0 + j] - vdv;  // dc holds the in-tile part, -sum_i P_ij G_ij
+    dc[row0 + j] = a;
+  }
+  dcrow[j] = a;
+  __syncthreads();
+  if (tid == 0) {
+    double s = 0.0;
+    for (int r = 0; r < nv; ++r) s += (double)dcrow[r];
+    ctot[bh * N + c] = s;
+  }
+  release_tmem<256>(tmem);
+}
+
+}  // namespace
+
+bool bwd_tc_supported(const ll_shape& s) { return s.io == LL_BF16 && s.dk == 128 && s.dv == 128; }
+
+ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
+  const ll_shape& s = a.s;
+  const int N = (s.T + kT - 1) / kT;
+  const int BH = s.B * s.H;
+  const dim3 grid(N, BH);
+  const auto* q = static_cast<const __nv_bfloat16*>(a.q);
+  const auto* k = static_cast<const __nv_bfloat16*>(a.k);
+  const auto* v = static_cast<const __nv_bfloat16*>(a.v);
+  const auto* dout = static_cast<const __nv_bfloat16*>(a.dout);
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
+  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
+                                                                  b.dv32, a.dlam, b.S, b.tot, b.R, b.dc, s.T, s.L,
+                                                                  b.err);
+  LL_CUDA_OK(cudaGetLastError());
+  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream);
+  if (fs != LL_OK) return fs;
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
+  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(q, dout, a.log_alpha, a.lam, b.F, b.G, b.dq32,
+                                                                  static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
+                                                                  s.L, b.err);
+  LL_CUDA_OK(cudaGetLastError());
+  LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
+  bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
+      k, v, a.log_alpha, a.lam, a.dlam, b.R, b.tot, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
+      static_cast<__nv_bfloat16*>(a.dv), b.dc, b.ctot, s.T, s.L, b.err);
+  LL_CUDA_OK(cudaGetLastError());
+  return LL_OK;
+}
+
+}  // namespace llattn

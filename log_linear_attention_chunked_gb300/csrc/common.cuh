@@ -109,10 +109,22 @@ struct BwdArgs {
   void* ws;
   size_t ws_bytes;
   cudaStream_t stream;
+  unsigned* err;
 };
 size_t bwd_simt_workspace(const ll_shape& s);
 int bwd_simt_launches(const ll_shape& s);
 ll_status bwd_simt_launch(const BwdArgs& a);
+// the tensor-core backward (bf16 io, d_k = d_v = 128, 128-token tiles) on
+// buffers laid out by the CUDA-core backward's plan
+struct BwdTcBuffers {
+  float *dq32, *dk32, *dv32, *S, *F, *R;
+  double *tot, *G;
+  float* dc;
+  double* ctot;
+  unsigned* err;
+};
+bool bwd_tc_supported(const ll_shape& s);
+ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b);
 
 size_t gdn_workspace(const ll_shape& s);
 ll_status gdn_launch(const FwdArgs& a);

@@ -97,6 +97,10 @@ def test_workload_bf16_t2k(B):
     (64, 64, 128, 128, "bf16"),   # one chunk
     (1024, 128, 128, 128, "bf16"),  # chunk 128 runs as 64-token chunks
     (1, 64, 128, 128, "f32"),     # T = 1
+    # bf16 with d = 128: the tensor-core kernels (128-token tiles)
+    (1, 64, 128, 128, "bf16"),    # T = 1
+    (129, 64, 128, 128, "bf16"),  # a second tile of one row
+    (2048, 64, 128, 128, "bf16"),  # 16 tiles: levels 8..10 on the query and key sides
 ])
 def test_shapes_and_edges(B, T, chunk, dk, dv, io):
     cfg = _cfg("mamba2_fp32_t64", io=io, T=T, dk=dk, dv=dv, L=levels_needed(T), B=2, H=3)
