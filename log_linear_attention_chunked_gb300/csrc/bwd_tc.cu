@@ -169,7 +169,7 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
 // ------------------------------------------------------------------ intra
 constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
-constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + 64; }
+constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + 64; }
 
 // Reduce-scatter over a warp: lane l receives the sum over the 32 lanes of v[l].
 __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
@@ -198,7 +198,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   double* cs = reinterpret_cast<double*>(base + kIntraEnd);
   float* wdec = reinterpret_cast<float*>(cs + kT);
   float* colpart = wdec + kT;  // [4 warps][128 columns] of sum_i P_ij G_ij
-  uint64_t* bar = reinterpret_cast<uint64_t*>(colpart + 4 * kT);
+  float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(c2 + kT);
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
@@ -224,49 +225,75 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
     mma128(tmem + 128, sG, false, sV, false, false);  // G = dO V^T
     umma_commit(bar);
   }
+  c2[tid] = (float)cs[tid] * 1.4426950408889634f;
+  wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+  __syncthreads();
   bool ok = wait_phase(bar, 0, err, abort_s);
   tc_fence_after();
-  wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
   {
     // row i = tid: P, dA (bf16) and the in-tile levels of dlam
-    const int i = tid;
+    // Warp wi holds rows 32 wi .. 32 wi + 31: the 32-column blocks above its
+    // diagonal block are masked, those below it hold one level (5 + bitlen(wi ^ cb)).
+    const int i = tid, wi = tid >> 5, lane = tid & 31;
+    const bool row_ok = i < nv;
     float lm[8], dl[8];
 #pragma unroll
     for (int l = 0; l < 8; ++l) {
-      lm[l] = (i < nv && l < L) ? lam[(row0 + i) * L + l] : 0.f;
+      lm[l] = (row_ok && l < L) ? lam[(row0 + i) * L + l] : 0.f;
       dl[l] = 0.f;
     }
-    const double csi = cs[i];
+    const float ci = c2[i];
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
-      float a[32], g[32];
-      tmem_ld32(lane_addr(tmem, 32 * cb), a);
-      tmem_ld32(lane_addr(tmem, 128 + 32 * cb), g);
-      tmem_ld_wait();
       float p[32], da[32];
+      if (cb > wi) {
 #pragma unroll
-      for (int u = 0; u < 32; ++u) {
-        const int j = 32 * cb + u;
-        p[u] = 0.f;
-        da[u] = 0.f;
-        if (j <= i && i < nv) {
-          const float ex = expf((float)(csi - cs[j]));
-          const int lv = bitlen((unsigned)(i ^ j));
-          float lmv = lm[0];
+        for (int u = 0; u < 32; ++u) p[u] = da[u] = 0.f;
+        colpart[wi * kT + 32 * cb + lane] = 0.f;
+      } else {
+        float a[32], g[32];
+        tmem_ld32(lane_addr(tmem, 32 * cb), a);
+        tmem_ld32(lane_addr(tmem, 128 + 32 * cb), g);
+        tmem_ld_wait();
+        if (cb < wi) {
+          const int lvc = 5 + bitlen((unsigned)(wi ^ cb));
+          float lmv = lm[6];
+          if (lvc == 7) lmv = lm[7];
+          float acc = 0.f;
 #pragma unroll
-          for (int l = 1; l < 8; ++l) lmv = lv == l ? lm[l] : lmv;
-          p[u] = a[u] * ex * lmv;
-          da[u] = g[u] * ex * lmv;
-          const float xx = g[u] * a[u] * ex;
+          for (int u = 0; u < 32; ++u) {
+            const float ex = row_ok ? exp2f(ci - c2[32 * cb + u]) : 0.f;
+            p[u] = a[u] * ex * lmv;
+            da[u] = g[u] * ex * lmv;
+            acc = fmaf(g[u] * a[u], ex, acc);
+          }
+          if (lvc == 7) dl[7] += acc;
+          else dl[6] += acc;
+        } else {
 #pragma unroll
-          for (int l = 0; l < 8; ++l) dl[l] += lv == l ? xx : 0.f;
+          for (int u = 0; u < 32; ++u) {
+            const int j = 32 * cb + u;
+            p[u] = 0.f;
+            da[u] = 0.f;
+            if (j <= i && row_ok) {
+              const float ex = exp2f(ci - c2[j]);
+              const int lv = bitlen((unsigned)(i ^ j));  // 0..5 inside the diagonal block
+              float lmv = lm[0];
+#pragma unroll
+              for (int l = 1; l < 6; ++l) lmv = lv == l ? lm[l] : lmv;
+              p[u] = a[u] * ex * lmv;
+              da[u] = g[u] * ex * lmv;
+              const float xx = g[u] * a[u] * ex;
+#pragma unroll
+              for (int l = 0; l < 6; ++l) dl[l] += lv == l ? xx : 0.f;
+            }
+          }
         }
-      }
-      {  // v_j . dv_j inside the tile is the column sum of P . G, kept in float32
+        // v_j . dv_j inside the tile is the column sum of P . G, kept in float32
         float pg[32];
 #pragma unroll
         for (int u = 0; u < 32; ++u) pg[u] = p[u] * g[u];
-        colpart[(tid >> 5) * kT + 32 * cb + (tid & 31)] = warp_column_sums(pg);
+        colpart[wi * kT + 32 * cb + lane] = warp_column_sums(pg);
       }
 #pragma unroll
       for (int w = 0; w < 4; ++w) {
