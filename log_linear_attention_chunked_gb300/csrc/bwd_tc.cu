@@ -17,7 +17,8 @@
 //   query : for every set bit h of c (node e, level 8 + h, decay D from the
 //           end of e to the start of c; w_i = exp(cs_i + D), lw_i = lam_i w_i):
 //           g = dO F_e (dlam_i = w_i g_i . q_i), dq += diag(lw) dO F_e and
-//           R_e += (diag(lw) dO)^T Q, the key-side node of e.
+//           R_e += (diag(lw) dO)^T Q, the key-side node of e (rows staged in
+//           shared memory and added into R_e by bulk reductions).
 //   key   : E_c = the R nodes of the blocks that hold c's keys, decayed to the
 //           end of c; dv += diag(wdec) K E^T, dk += diag(wdec) V E, and
 //           dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j (the in-tile part of
@@ -81,32 +82,56 @@ __device__ __forceinline__ bool wait_phase(uint64_t* bar, uint32_t par, unsigned
 }
 
 // a [128][128] bf16 tile of rows [0, nv) from global (rows of 256 B) into a swizzled tile; rows >= nv are 0
+// (all 16 loads of a thread are issued before its stores: the staging is latency-bound)
 __device__ __forceinline__ void stage_bf16(unsigned char* tile, const __nv_bfloat16* src, int nv, int tid) {
-#pragma unroll 4
-  for (int x = tid; x < kT * 16; x += kThreads) {
-    const int r = x >> 4, c8 = x & 15;
-    uint4 v = make_uint4(0u, 0u, 0u, 0u);
-    if (r < nv) v = *reinterpret_cast<const uint4*>(src + (size_t)r * kD + 8 * c8);
-    *reinterpret_cast<uint4*>(tile + swz(r, c8)) = v;
+  uint4 v[16];
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int x = tid + u * kThreads, r = x >> 4, c8 = x & 15;
+    v[u] = r < nv ? *reinterpret_cast<const uint4*>(src + (size_t)r * kD + 8 * c8) : make_uint4(0u, 0u, 0u, 0u);
+  }
+#pragma unroll
+  for (int u = 0; u < 16; ++u) {
+    const int x = tid + u * kThreads, r = x >> 4, c8 = x & 15;
+    *reinterpret_cast<uint4*>(tile + swz(r, c8)) = v[u];
   }
 }
 
 // sum_m coef[m] * src_m (float32 [128][128] matrices) as a bf16 swizzled tile
+// (eight chunks of a thread at a time, their loads issued together)
 __device__ __forceinline__ void stage_f32_sum(unsigned char* tile, const float* const* src, const float* coef, int n,
                                               int tid) {
-#pragma unroll 2
-  for (int x = tid; x < kT * 16; x += kThreads) {
-    const int r = x >> 4, c8 = x & 15;
-    float a[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+#pragma unroll 1
+  for (int pass = 0; pass < 2; ++pass) {
+    float a[8][8];
+#pragma unroll
+    for (int q = 0; q < 8; ++q)
+#pragma unroll
+      for (int t = 0; t < 8; ++t) a[q][t] = 0.f;
     for (int m = 0; m < n; ++m) {
-      const float4 u = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8);
-      const float4 w = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8 + 4);
+      float4 u[8][2];
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        const int x = tid + (8 * pass + q) * kThreads, r = x >> 4, c8 = x & 15;
+        u[q][0] = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8);
+        u[q][1] = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8 + 4);
+      }
       const float cf = coef[m];
-      a[0] = fmaf(cf, u.x, a[0]); a[1] = fmaf(cf, u.y, a[1]); a[2] = fmaf(cf, u.z, a[2]); a[3] = fmaf(cf, u.w, a[3]);
-      a[4] = fmaf(cf, w.x, a[4]); a[5] = fmaf(cf, w.y, a[5]); a[6] = fmaf(cf, w.z, a[6]); a[7] = fmaf(cf, w.w, a[7]);
+#pragma unroll
+      for (int q = 0; q < 8; ++q) {
+        a[q][0] = fmaf(cf, u[q][0].x, a[q][0]); a[q][1] = fmaf(cf, u[q][0].y, a[q][1]);
+        a[q][2] = fmaf(cf, u[q][0].z, a[q][2]); a[q][3] = fmaf(cf, u[q][0].w, a[q][3]);
+        a[q][4] = fmaf(cf, u[q][1].x, a[q][4]); a[q][5] = fmaf(cf, u[q][1].y, a[q][5]);
+        a[q][6] = fmaf(cf, u[q][1].z, a[q][6]); a[q][7] = fmaf(cf, u[q][1].w, a[q][7]);
+      }
     }
-    *reinterpret_cast<uint4*>(tile + swz(r, c8)) =
-        make_uint4(pack_bf16x2(a[0], a[1]), pack_bf16x2(a[2], a[3]), pack_bf16x2(a[4], a[5]), pack_bf16x2(a[6], a[7]));
+#pragma unroll
+    for (int q = 0; q < 8; ++q) {
+      const int x = tid + (8 * pass + q) * kThreads, r = x >> 4, c8 = x & 15;
+      *reinterpret_cast<uint4*>(tile + swz(r, c8)) =
+          make_uint4(pack_bf16x2(a[q][0], a[q][1]), pack_bf16x2(a[q][2], a[q][3]), pack_bf16x2(a[q][4], a[q][5]),
+                     pack_bf16x2(a[q][6], a[q][7]));
+    }
   }
 }
 
@@ -191,8 +216,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
     float* __restrict__ dq32, float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam,
-    float* __restrict__ S, double* __restrict__ tot, float* __restrict__ R, float* __restrict__ dc, int T, int L,
-    unsigned* err) {
+    float* __restrict__ S, double* __restrict__ tot, float* __restrict__ dc, int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kIntraEnd);
@@ -354,15 +378,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
             *reinterpret_cast<float4*>(outs[o] + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
       }
     }
-    float* Rc = R + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD;
-#pragma unroll 8
-    for (int u = 0; u < kD; u += 4) *reinterpret_cast<float4*>(Rc + u) = make_float4(0.f, 0.f, 0.f, 0.f);
   }
   release_tmem<512>(tmem);
 }
 
 // ------------------------------------------------------------------ query side
-constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryEnd = 4 * kTileB;
+constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
+constexpr int kRowP = kD + 4;  // float pitch of the staged R rows (conflict-free row writes)
+constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
 constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
@@ -441,16 +464,23 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
         }
       }
       if (i < nv) dlam[(row0 + i) * L + lv] = w * part;
-      float* Re = R + (bh * N + e) * mat + (size_t)i * kD;  // row e' = i of R_e
+      // row e' = i of this tile's part of R_e: staged in shared memory, then
+      // added into R_e by the bulk-copy unit (one 512-byte reduction per row)
+      float* rrow = reinterpret_cast<float*>(base + kQryR) + i * kRowP;
+      bulk_wait_read0();  // the previous level's reduction has read this row
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         float x[32];
         tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
         tmem_ld_wait();
-        if (ok)
 #pragma unroll
-          for (int u = 0; u < 32; u += 4)
-            atomicAdd(reinterpret_cast<float4*>(Re + 32 * cb + u), make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]));
+        for (int u = 0; u < 32; u += 4)
+          *reinterpret_cast<float4*>(rrow + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+      }
+      if (ok) {
+        fence_proxy_async_shared();
+        bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD, rrow, kD * 4);
+        bulk_commit();
       }
     }
     D += G[bh * N + e];
@@ -487,6 +517,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       }
     }
   }
+  bulk_wait0();  // this thread's reductions into R are complete
   release_tmem<512>(tmem);
 }
 
@@ -613,14 +644,15 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int N = (s.T + kT - 1) / kT;
   const int BH = s.B * s.H;
   const dim3 grid(N, BH);
+  // the key-side nodes accumulate from 0
+  LL_CUDA_OK(cudaMemsetAsync(b.R, 0, (size_t)BH * N * kD * kD * sizeof(float), a.stream));
   const auto* q = static_cast<const __nv_bfloat16*>(a.q);
   const auto* k = static_cast<const __nv_bfloat16*>(a.k);
   const auto* v = static_cast<const __nv_bfloat16*>(a.v);
   const auto* dout = static_cast<const __nv_bfloat16*>(a.dout);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
   bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
-                                                                  b.dv32, a.dlam, b.S, b.tot, b.R, b.dc, s.T, s.L,
-                                                                  b.err);
+                                                                  b.dv32, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream);
   if (fs != LL_OK) return fs;
