@@ -79,8 +79,8 @@ def algorithmic_flops(cfg) -> int:
     T, C, d = cfg["T"], cfg["chunk"], cfg["dk"]
     N = T // C
     P = sum(bin(c).count("1") for c in range(N))
-    if cfg["kind"] == "mamba2_bwd":
-        return backward_flops(cfg)
+    if cfg["kind"] == "mamba2_bwd":  # counted for the tiles the path runs on
+        return backward_flops(dict(cfg, chunk=128) if backward_on_tensor_cores(cfg) else cfg)
     if cfg["kind"] == "gdn":
         per_chunk = 10 * C * C * d + (4 * C ** 3) // 3 + 2 * C * d * d
         per_bh = N * per_chunk + P * (6 * C * d * d + 2 * C * C * d)
@@ -123,6 +123,12 @@ def backward_flops(cfg) -> int:
     return per_bh * cfg["B"] * cfg["H"]
 
 
+def backward_on_tensor_cores(cfg) -> bool:
+    """The backward of bf16 io with d_k = d_v = 128 runs on the tensor cores over
+    128-token tiles; every other shape on the CUDA cores."""
+    return cfg["io"] == "bf16" and cfg["dk"] == 128 and cfg["dv"] == 128
+
+
 def gdn_decode_bytes(B, H, d, Ls, t) -> int:
     """One Gated DeltaNet decode step: the popcount(t) non-empty states read
     once; the ones above the carry written back transitioned and the merged
@@ -157,7 +163,7 @@ KERNEL_SOURCES = {
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
-    "mamba2_bwd": ("bwd_simt.cu", "common.cuh"),
+    "mamba2_bwd": ("bwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the query-side kernel
 }
 
 
@@ -790,7 +796,7 @@ def main():
         roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
                     "traffic": traffic, "peak_source": f"{src} (HBM copy)",
                     "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname}
-    elif kind in ("gdn", "gdn_b", "mamba2_bwd"):
+    elif kind in ("gdn", "gdn_b") or (kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg)):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
         aflops = w["aflops"]

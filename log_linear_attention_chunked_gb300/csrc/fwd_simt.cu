@@ -188,8 +188,15 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
   if (idx >= mat) return;
   const float* Sb = S + bh * N * (size_t)mat;
   float* Fb = F + bh * N * (size_t)mat;
+  // the chunk states do not depend on the chain: four are loaded ahead
+  float s0 = Sb[idx], s1 = N > 1 ? Sb[(size_t)mat + idx] : 0.f, s2 = N > 2 ? Sb[2 * (size_t)mat + idx] : 0.f,
+        s3 = N > 3 ? Sb[3 * (size_t)mat + idx] : 0.f;
   for (int i = 0; i < N; ++i) {
-    float acc = Sb[(size_t)i * mat + idx];
+    float acc = s0;
+    s0 = s1;
+    s1 = s2;
+    s2 = s3;
+    s3 = i + 4 < N ? Sb[(size_t)(i + 4) * mat + idx] : 0.f;
     double dec = tot[bh * N + i];
     for (int m = 0; (i >> m) & 1; ++m) {
       const int j = i - (1 << m);
