@@ -163,7 +163,7 @@ KERNEL_SOURCES = {
     "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
-    "mamba2_bwd": ("bwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the query-side kernel
+    "mamba2_bwd": ("bwd_tc.cu", "bwd.cuh", "common.cuh", "sm100.cuh"),  # dominant: the query-side kernel
 }
 
 

@@ -4,7 +4,7 @@
 // invalid call never touches device memory.
 #include <mutex>
 
-#include "common.cuh"
+#include "bwd.cuh"
 
 namespace llattn {
 

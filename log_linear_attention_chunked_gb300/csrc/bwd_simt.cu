@@ -41,7 +41,7 @@
 // no outputs), as in the forward.
 #include <algorithm>
 
-#include "common.cuh"
+#include "bwd.cuh"
 
 namespace llattn {
 

@@ -30,7 +30,7 @@
 // operands, one thread issues the MMAs and commits them to an mbarrier, every
 // thread waits (bounded: after 4 s the error word is set and the kernel
 // finishes without the results), then the row-wise epilogue.
-#include "common.cuh"
+#include "bwd.cuh"
 #include "sm100.cuh"
 
 namespace llattn {
@@ -46,6 +46,15 @@ constexpr uint32_t kHalf = kT * 64 * 2;        // a [128 x 64] bf16 swizzled blo
 constexpr uint32_t kTileB = 2 * kHalf;         // a [128 x 128] bf16 tile: 32 KB
 constexpr uint64_t kTimeoutNs = 4000000000ull;
 constexpr int kLc = 7;                         // log2 of the tile
+
+// Element-wise float32 add of a contiguous shared-memory range into global
+// memory by the bulk-copy unit (16-byte aligned addresses, size a multiple of
+// 16); completion is tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void bulk_reduce_add_f32(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.reduce.async.bulk.global.shared::cta.bulk_group.add.f32 [%0], [%1], %2;" ::"l"(dst),
+               "r"(smem_u32(src)), "r"(bytes)
+               : "memory");
+}
 
 // byte offset of the 16-byte chunk c8 (elements 8 c8 .. 8 c8 + 7) of row r of a tile
 __device__ __forceinline__ uint32_t swz(int r, int c8) {

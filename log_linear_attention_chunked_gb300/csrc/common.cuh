@@ -74,10 +74,6 @@ struct FwdArgs {
 };
 
 size_t fwd_simt_workspace(const ll_shape& s);
-// Fenwick nodes F, G of the chunk states S and chunk log-decays tot (BH heads
-// of N chunks, matrices of `mat` floats); shared by the forward and backward
-ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream);
 size_t fwd_simt_cont_workspace(const ll_shape& s);
 // the decode states of t0 + T after a continuation (both forward paths)
 ll_status cont_export_launch(const float* pre_states, const float* pre_scales, const float* seg_states,
@@ -100,32 +96,6 @@ ll_status decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const
 ll_status gdn_decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
                             const void* k, const void* v, const float* log_alpha, const float* beta,
                             const float* lam, float* states, void* o, cudaStream_t stream, unsigned* err);
-struct BwdArgs {
-  ll_shape s;
-  const void *q, *k, *v, *dout;
-  const float *log_alpha, *lam;
-  void *dq, *dk, *dv;
-  float *dlog_alpha, *dlam;
-  void* ws;
-  size_t ws_bytes;
-  cudaStream_t stream;
-  unsigned* err;
-};
-size_t bwd_simt_workspace(const ll_shape& s);
-int bwd_simt_launches(const ll_shape& s);
-ll_status bwd_simt_launch(const BwdArgs& a);
-// the tensor-core backward (bf16 io, d_k = d_v = 128, 128-token tiles) on
-// buffers laid out by the CUDA-core backward's plan
-struct BwdTcBuffers {
-  float *dq32, *dk32, *dv32, *S, *F, *R;
-  double *tot, *G;
-  float* dc;
-  double* ctot;
-  unsigned* err;
-};
-bool bwd_tc_supported(const ll_shape& s);
-ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b);
-
 size_t gdn_workspace(const ll_shape& s);
 ll_status gdn_launch(const FwdArgs& a);
 size_t gdn_b_workspace(const ll_shape& s);

@@ -48,7 +48,7 @@
 // float32 running sum would lose at long range.
 #include <algorithm>
 
-#include "common.cuh"
+#include "bwd.cuh"
 
 namespace llattn {
 
