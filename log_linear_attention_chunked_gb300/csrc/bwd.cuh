@@ -6,9 +6,11 @@
 namespace llattn {
 
 // Fenwick nodes F, G of the chunk states S and chunk log-decays tot (BH heads
-// of N chunks, matrices of `mat` floats); shared by the forward and backward
+// of N chunks, matrices of `mat` floats); shared by the forward and backward.
+// With Ft (d_k = d_v = 128) the nodes are also written as 128-byte-swizzled
+// bf16 tiles, the operand layout of the tensor-core kernels.
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream);
+                              cudaStream_t stream, __nv_bfloat16* Ft = nullptr);
 
 struct BwdArgs {
   ll_shape s;
@@ -28,6 +30,7 @@ ll_status bwd_simt_launch(const BwdArgs& a);
 // buffers laid out by the CUDA-core backward's plan
 struct BwdTcBuffers {
   float *dq32, *dk32, *dv32, *S, *F, *R;
+  __nv_bfloat16* Ft;  // the nodes F as bf16 tiles
   double *tot, *G;
   float* dc;
   double* ctot;

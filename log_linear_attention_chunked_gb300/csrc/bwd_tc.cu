@@ -56,6 +56,16 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* dst, const void* src, 
                : "memory");
 }
 
+// Bulk copy of a contiguous shared-memory range to global memory (16-byte
+// aligned addresses, size a multiple of 16), tracked by the thread's bulk groups.
+__device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
+  asm volatile("cp.async.bulk.global.shared::cta.bulk_group [%0], [%1], %2;" ::"l"(dst), "r"(smem_u32(src)),
+               "r"(bytes)
+               : "memory");
+}
+
+constexpr int kRowP = kD + 4;  // float pitch of rows staged for bulk copies (conflict-free row writes)
+
 // byte offset of the 16-byte chunk c8 (elements 8 c8 .. 8 c8 + 7) of row r of a tile
 __device__ __forceinline__ uint32_t swz(int r, int c8) {
   return (uint32_t)(c8 >> 3) * kHalf + (uint32_t)r * 128u + ((uint32_t)((c8 & 7) ^ (r & 7)) << 4);
@@ -370,43 +380,53 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   ok = ok && wait_phase(bar, 1, err, abort_s);
   tc_fence_after();
   {
+    // Every operand tile is free now: each output row is staged in shared
+    // memory (two alternating buffers of padded rows over the tiles) and
+    // written by one 512-byte bulk copy.
     const int r = tid;
     float* outs[4] = {dq32 + (row0 + r) * kD, dk32 + (row0 + r) * kD, dv32 + (row0 + r) * kD,
                       S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD};
 #pragma unroll 1
     for (int o = 0; o < 4; ++o) {
       const bool keep = o == 3 || r < nv;  // S has every row; the gradients only the present ones
+      float* rowp = reinterpret_cast<float*>(base + (o & 1) * (kT * kRowP * 4)) + r * kRowP;
+      if (o >= 2) bulk_wait_read0();  // the copy of output o - 2 has read this row
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         float x[32];
         tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
         tmem_ld_wait();
-        if (keep)
 #pragma unroll
-          for (int u = 0; u < 32; u += 4)
-            *reinterpret_cast<float4*>(outs[o] + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+        for (int u = 0; u < 32; u += 4)
+          *reinterpret_cast<float4*>(rowp + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+      }
+      if (keep && ok) {
+        fence_proxy_async_shared();
+        bulk_store(outs[o], rowp, kD * 4);
+        bulk_commit();
       }
     }
+    bulk_wait0();
   }
   release_tmem<512>(tmem);
 }
 
 // ------------------------------------------------------------------ query side
 constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
-constexpr int kRowP = kD + 4;  // float pitch of the staged R rows (conflict-free row writes)
 constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
-constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }
+constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }  // + cs, two mbarriers, TMEM slot, flag
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
-    const float* __restrict__ lam, const float* __restrict__ F, const double* __restrict__ G,
+    const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
     const float* __restrict__ dq32, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam, float* __restrict__ R,
     int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kQryEnd);
   uint64_t* bar = reinterpret_cast<uint64_t*>(cs + kT);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* ldbar = bar + 1;  // the bulk load of a node tile
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
@@ -416,6 +436,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
   if (tid == 0) {
     *abort_s = 0;
     chunk_cumsum(cs, log_alpha, row0, nv);
+    mbar_init(ldbar, 1);  // made visible by the fence in setup_tmem
   }
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
@@ -432,9 +453,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     if (!((c >> h) & 1)) continue;
     const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
     const int lv = kLc + 1 + h;
+    // the node F_e (a bf16 tile written by the Fenwick kernel) by one bulk copy
+    if (tid == 0 && ok) {
+      mbar_arrive_expect_tx(ldbar, kTileB);
+      bulk_load(base + kQryF, Ft + (bh * N + e) * mat, kTileB, ldbar);
+    }
     const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
     const float lw = i < nv ? w * lam[(row0 + i) * L + lv] : 0.f;
-    // dO rows scaled by lw, and the node F_e in bf16
+    // dO rows scaled by lw
 #pragma unroll 4
     for (int c8 = 0; c8 < 16; ++c8) {
       float x[8];
@@ -443,9 +469,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
           make_uint4(pack_bf16x2(lw * x[0], lw * x[1]), pack_bf16x2(lw * x[2], lw * x[3]),
                      pack_bf16x2(lw * x[4], lw * x[5]), pack_bf16x2(lw * x[6], lw * x[7]));
     }
-    const float* Fe = F + (bh * N + e) * mat;
-    const float one = 1.f;
-    stage_f32_sum(base + kQryF, &Fe, &one, 1, tid);
+    ok = ok && wait_phase(ldbar, phase, err, abort_s);
     to_async();
     if (tid == 0 && ok) {
       mma128(tmem + 0, sG, false, sF, true, false);    // g = dO F_e
@@ -663,10 +687,10 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
                                                                   b.dv32, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
-  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream);
+  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(q, dout, a.log_alpha, a.lam, b.F, b.G, b.dq32,
+  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dq32,
                                                                   static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
                                                                   s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());

@@ -169,9 +169,18 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restri
 }
 
 // (3): sequential over chunks, parallel over matrix elements and heads.
+// Element (r, c) of a [128][128] bf16 tile in the 128-byte-swizzled layout of
+// the tensor-core kernels: two [128][64] halves, 128-byte rows, the 16-byte
+// chunks of a row permuted by XOR with (r mod 8).
+__device__ __forceinline__ int swizzled_elem(int r, int c) {
+  return (c >> 6) * 8192 + r * 64 + ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
+}
+
+// With Ft (d_k = d_v = 128 only) every node is also written as such a bf16 tile.
 __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __restrict__ S, float* __restrict__ F,
                                                                 const double* __restrict__ tot,
-                                                                double* __restrict__ G, int N, int mat) {
+                                                                double* __restrict__ G, int N, int mat,
+                                                                __nv_bfloat16* __restrict__ Ft) {
   extern __shared__ double Gs[];  // [N]
   const size_t bh = blockIdx.y;
   if (threadIdx.x == 0) {
@@ -188,6 +197,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
   if (idx >= mat) return;
   const float* Sb = S + bh * N * (size_t)mat;
   float* Fb = F + bh * N * (size_t)mat;
+  const int tel = Ft ? swizzled_elem(idx >> 7, idx & 127) : 0;
   // the chunk states do not depend on the chain: four are loaded ahead
   float s0 = Sb[idx], s1 = N > 1 ? Sb[(size_t)mat + idx] : 0.f, s2 = N > 2 ? Sb[2 * (size_t)mat + idx] : 0.f,
         s3 = N > 3 ? Sb[3 * (size_t)mat + idx] : 0.f;
@@ -204,6 +214,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
       dec += Gs[j];
     }
     Fb[(size_t)i * mat + idx] = acc;
+    if (Ft) Ft[(bh * N + i) * (size_t)mat + tel] = __float2bfloat16_rn(acc);
   }
 }
 
@@ -413,11 +424,11 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 }  // namespace
 
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream) {
+                              cudaStream_t stream, __nv_bfloat16* Ft) {
   const size_t sm = (size_t)N * sizeof(double);
   if (sm > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
   LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm, stream>>>(S, F, tot, G, N, mat);
+  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm, stream>>>(S, F, tot, G, N, mat, Ft);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }
