@@ -406,7 +406,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
         bulk_commit();
       }
     }
-    bulk_wait0();
+    bulk_wait_read0();  // the copies have read their rows; the writes complete with the grid
   }
   release_tmem<512>(tmem);
 }
@@ -439,12 +439,25 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     mbar_init(ldbar, 1);  // made visible by the fence in setup_tmem
   }
   const uint32_t tmem = setup_tmem<512>(bar, slot);
+  const size_t mat = (size_t)kD * kD;
+  // the node tile of the lowest set bit of c streams in while Q and dO are staged;
+  // each later one as soon as the products of the level before have read the tile
+  auto load_node = [&](int h) {
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    mbar_arrive_expect_tx(ldbar, kTileB);
+    bulk_load(base + kQryF, Ft + (bh * N + e) * mat, kTileB, ldbar);
+  };
+  auto next_bit = [&](int h) {  // the set bit of c above h, or -1
+    for (++h; (c >> h) != 0; ++h)
+      if ((c >> h) & 1) return h;
+    return -1;
+  };
+  if (tid == 0 && c > 0) load_node(next_bit(-1));
   stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
   stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
   __syncthreads();
   const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
                  sF = smem_u32(base + kQryF);
-  const size_t mat = (size_t)kD * kD;
   const int i = tid;
   double D = 0.0;
   bool ok = true, first = true;
@@ -453,11 +466,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     if (!((c >> h) & 1)) continue;
     const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
     const int lv = kLc + 1 + h;
-    // the node F_e (a bf16 tile written by the Fenwick kernel) by one bulk copy
-    if (tid == 0 && ok) {
-      mbar_arrive_expect_tx(ldbar, kTileB);
-      bulk_load(base + kQryF, Ft + (bh * N + e) * mat, kTileB, ldbar);
-    }
     const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
     const float lw = i < nv ? w * lam[(row0 + i) * L + lv] : 0.f;
     // dO rows scaled by lw
@@ -481,6 +489,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     ok = ok && wait_phase(bar, phase, err, abort_s);
     phase ^= 1;
     tc_fence_after();
+    if (tid == 0 && ok && next_bit(h) >= 0) load_node(next_bit(h));  // the products have read the tile
     {
       float part = 0.f;
 #pragma unroll 1
@@ -550,7 +559,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       }
     }
   }
-  bulk_wait0();  // this thread's reductions into R are complete
+  bulk_wait_read0();  // this thread's reductions into R have read their rows
   release_tmem<512>(tmem);
 }
 
