@@ -219,11 +219,16 @@ LL_API int ll_attn_bwd_launches(const ll_shape* shape);
  *   dlam       [B,H,T,L]   float32, written (levels no key reaches are 0)
  *   workspace  >= ll_attn_bwd_workspace_size(shape) bytes, 256-byte aligned
  * No output may overlap an input or another output (LL_ERR_INVALID_ARG).
- * Any T is accepted (a partial last chunk is handled); accumulation is
- * float32 on CUDA cores, with the cumulative decays and the suffix sums of
- * dlog_alpha in float64.  The order of the float32 additions into the
- * key-side level nodes is not fixed, so results can differ in the last bits
- * between calls. */
+ * Any T is accepted (a partial last chunk is handled).  bf16 io with
+ * dk = dv = 128 runs on the tensor cores over 128-token tiles whatever
+ * `chunk` is (bf16 operands for the masked scores, their gradient, the
+ * Fenwick nodes and the scaled dout; float32 accumulation); every other
+ * shape runs in float32 on the CUDA cores.  Cumulative decays and the
+ * suffix sums of dlog_alpha are float64.  The order of the float32
+ * additions into the key-side level nodes is not fixed, so results can
+ * differ in the last bits between calls.  A bounded device-side wait that
+ * expires sets the device error word (LL_ERR_TIMEOUT from
+ * ll_last_device_error); the gradients are then unspecified. */
 LL_API ll_status ll_attn_bwd(const ll_shape* shape, const void* q, const void* k, const void* v,
                              const float* log_alpha, const float* lam, const void* dout, void* dq, void* dk,
                              void* dv, float* dlog_alpha, float* dlam, void* workspace, size_t ws_bytes,
