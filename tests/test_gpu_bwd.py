@@ -120,6 +120,19 @@ def test_decay_and_lambda_variants(B, io, la_mode, lam_mode):
                       (la_mode, lam_mode, lvl), _lam(inp))
 
 
+@pytest.mark.parametrize("la_mode,lam_mode,levels", [("zero", "softplus", [0]), ("slow", "softplus", [0]),
+                                                     ("slow", "onehot", [0, 5, 7, 8, 10])])
+def test_tensor_core_variants(B, la_mode, lam_mode, levels):
+    """bf16 d = 128 (the tensor-core kernels): alpha = 1, slow decay, and lam
+    on one level at a time, inside the diagonal 32-block (0, 5), in the
+    off-diagonal blocks of a tile (7) and between tiles (8, 10)."""
+    cfg = _cfg("mamba2_fp32_t64", io="bf16", T=1024, dk=128, dv=128, L=levels_needed(1024), B=1, H=2, chunk=64)
+    for lvl in levels:
+        inp = synth.make_inputs(cfg, la_mode=la_mode, lam_mode=lam_mode, lam_level=lvl,
+                                tag=f"bwdtc{la_mode}{lam_mode}", dout=True)
+        _assert_close(_run(B, inp, cfg["chunk"]), _oracle(inp), TOL_BF16, (la_mode, lam_mode, lvl), _lam(inp))
+
+
 def test_extra_levels_are_zero(B):
     # lam with more levels than T reaches: their gradient is exactly 0
     cfg = _cfg("mamba2_fp32_t64", T=200, L=levels_needed(200) + 3, B=1, H=2)
