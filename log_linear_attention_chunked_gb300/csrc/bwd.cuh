@@ -8,9 +8,10 @@ namespace llattn {
 // Fenwick nodes F, G of the chunk states S and chunk log-decays tot (BH heads
 // of N chunks, matrices of `mat` floats); shared by the forward and backward.
 // With Ft (d_k = d_v = 128) the nodes are also written as 128-byte-swizzled
-// bf16 tiles, the operand layout of the tensor-core kernels.
+// bf16 tiles, the operand layout of the tensor-core kernels; with cum, the
+// running sums over the chunks of their log-decay totals ([BH, N] float64).
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream, __nv_bfloat16* Ft = nullptr);
+                              cudaStream_t stream, __nv_bfloat16* Ft = nullptr, double* cum = nullptr);
 
 struct BwdArgs {
   ll_shape s;
@@ -31,7 +32,7 @@ ll_status bwd_simt_launch(const BwdArgs& a);
 struct BwdTcBuffers {
   float *dq32, *dk32, *dv32, *S, *F, *R;
   __nv_bfloat16* Ft;  // the nodes F as bf16 tiles
-  double *tot, *G;
+  double *tot, *G, *cum;
   float* dc;
   double* ctot;
   unsigned* err;

@@ -67,7 +67,7 @@ size_t key_smem(int Ce, int dk, int dv) {
 
 struct BwdPlan {
   int Ce, N, lc;
-  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_ctot, off_Ft, total;
+  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_ctot, off_Ft, off_cum, total;
 };
 
 BwdPlan plan_of(const ll_shape& s) {
@@ -92,6 +92,8 @@ BwdPlan plan_of(const ll_shape& s) {
   p.off_ctot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_Ft = off;
   if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * mat * 2, 256);  // the nodes as bf16 tiles
+  p.off_cum = off;
+  if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * sizeof(double), 256);  // running chunk totals
   p.off_dq = p.off_dk = p.off_dv = off;
   if (s.io != LL_F32) {  // float32 partial sums of dq, dk, dv (float32 io accumulates in the outputs)
     p.off_dq = off; off = align_up(off + BH * (size_t)s.T * s.dk * sizeof(float), 256);
@@ -929,8 +931,8 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const IO* dout = static_cast<const IO*>(a.dout);
 
   if (bwd_tc_supported(s)) {
-    const BwdTcBuffers b{dq32, dk32, dv32, S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G, dc,
-                         ctot, a.err};
+    const BwdTcBuffers b{dq32, dk32, dv32, S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G,
+                         reinterpret_cast<double*>(ws + p.off_cum), dc, ctot, a.err};
     const ll_status st = bwd_tc_launch(a, b);
     if (st != LL_OK) return st;
     bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);

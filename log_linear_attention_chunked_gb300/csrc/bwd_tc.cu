@@ -161,12 +161,22 @@ __device__ __forceinline__ void row_chunk(const unsigned char* tile, int r, int 
   x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
 }
 
-__device__ __forceinline__ void chunk_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
-  double acc = 0.0;
-  for (int i = 0; i < kT; ++i) {
-    if (i < nv) acc += (double)log_alpha[row0 + i];
-    cs[i] = acc;
+// cs[i] = the sum of log_alpha over rows 0..i of the tile (rows >= nv add 0),
+// float64; every thread takes part (a scan over each warp, then the warps'
+// totals); the caller synchronises before reading cs
+__device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
+  __shared__ double wsum[kThreads / 32];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  double x = t < nv ? (double)log_alpha[row0 + t] : 0.0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
   }
+  if (lane == 31) wsum[w] = x;
+  __syncthreads();
+  for (int ww = 0; ww < w; ++ww) x += wsum[ww];
+  cs[t] = x;
 }
 
 // Common prologue: the mbarrier and the TMEM allocation (warp 0).
@@ -250,11 +260,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   const int tid = threadIdx.x;
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
-  if (tid == 0) {
-    *abort_s = 0;
-    chunk_cumsum(cs, log_alpha, row0, nv);
-    tot[bh * N + c] = cs[kT - 1];
-  }
+  if (tid == 0) *abort_s = 0;
+  tile_cumsum(cs, log_alpha, row0, nv);
+  if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
   stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
@@ -435,9 +443,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
   const int nv = min(kT, T - c * kT);
   if (tid == 0) {
     *abort_s = 0;
-    chunk_cumsum(cs, log_alpha, row0, nv);
     mbar_init(ldbar, 1);  // made visible by the fence in setup_tmem
   }
+  tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   const size_t mat = (size_t)kD * kD;
   // the node tile of the lowest set bit of c streams in while Q and dO are staged;
@@ -570,7 +578,7 @@ constexpr size_t key_smem() { return 1024 + kKeyEnd + kT * 8 + kT * 4 + kT * 4 +
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
-    const double* __restrict__ tot, const float* __restrict__ dk32, const float* __restrict__ dv32,
+    const double* __restrict__ cum, const float* __restrict__ dk32, const float* __restrict__ dv32,
     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dc,
     double* __restrict__ ctot, int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
@@ -592,20 +600,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const size_t mat = (size_t)kD * kD;
   if (tid == 0) {
     *abort_s = 0;
-    chunk_cumsum(cs, log_alpha, row0, nv);
-    int n = 0, cc = c;
-    double dec = 0.0;  // log-decay from the end of c to the end of e
+    int n = 0;
+    const double cum_c = cum[bh * N + c];
     for (int h = 0; h < 31 && n < 32; ++h) {
       if ((c >> h) & 1) continue;
       const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
       if (e + 1 >= N) break;  // e grows with h: no later node has queries either
-      while (cc < e) dec += tot[bh * N + (++cc)];
       srcs[n] = R + (bh * N + e) * mat;
-      coef[n] = expf((float)dec);
+      coef[n] = expf((float)(cum[bh * N + e] - cum_c));  // the decay from the end of c to the end of e
       ++n;
     }
     *n_s = n;
   }
+  tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<256>(bar, slot);
   const int n = *n_s;
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
@@ -696,7 +703,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
                                                                   b.dv32, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
-  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft);
+  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
   bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dq32,
@@ -705,7 +712,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
-      k, v, a.log_alpha, a.lam, a.dlam, b.R, b.tot, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
+      k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), b.dc, b.ctot, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;

@@ -176,18 +176,24 @@ __device__ __forceinline__ int swizzled_elem(int r, int c) {
   return (c >> 6) * 8192 + r * 64 + ((((c & 63) >> 3) ^ (r & 7)) << 3) + (c & 7);
 }
 
-// With Ft (d_k = d_v = 128 only) every node is also written as such a bf16 tile.
+// With Ft (d_k = d_v = 128 only) every node is also written as such a bf16
+// tile; with cum, the running sums of the chunk totals (per head, float64).
 __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __restrict__ S, float* __restrict__ F,
                                                                 const double* __restrict__ tot,
                                                                 double* __restrict__ G, int N, int mat,
-                                                                __nv_bfloat16* __restrict__ Ft) {
+                                                                __nv_bfloat16* __restrict__ Ft,
+                                                                double* __restrict__ cum) {
   extern __shared__ double Gs[];  // [N]
   const size_t bh = blockIdx.y;
   if (threadIdx.x == 0) {
+    double run = 0.0;
     for (int i = 0; i < N; ++i) {
-      double g = tot[bh * N + i];
+      const double ti = tot[bh * N + i];
+      double g = ti;
       for (int m = 0; (i >> m) & 1; ++m) g += Gs[i - (1 << m)];
       Gs[i] = g;
+      run += ti;
+      if (cum && blockIdx.x == 0) cum[bh * N + i] = run;
     }
   }
   __syncthreads();
@@ -424,11 +430,11 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 }  // namespace
 
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream, __nv_bfloat16* Ft) {
+                              cudaStream_t stream, __nv_bfloat16* Ft, double* cum) {
   const size_t sm = (size_t)N * sizeof(double);
   if (sm > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
   LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
-  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm, stream>>>(S, F, tot, G, N, mat, Ft);
+  simt_fenwick_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, sm, stream>>>(S, F, tot, G, N, mat, Ft, cum);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }
