@@ -184,19 +184,49 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
                                                                 __nv_bfloat16* __restrict__ Ft,
                                                                 double* __restrict__ cum) {
   extern __shared__ double Gs[];  // [N]
+  __shared__ double wsum[kThreads / 32];
   const size_t bh = blockIdx.y;
-  if (threadIdx.x == 0) {
-    double run = 0.0;
-    for (int i = 0; i < N; ++i) {
-      const double ti = tot[bh * N + i];
-      double g = ti;
-      for (int m = 0; (i >> m) & 1; ++m) g += Gs[i - (1 << m)];
-      Gs[i] = g;
-      run += ti;
-      if (cum && blockIdx.x == 0) cum[bh * N + i] = run;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  // Running sums of the chunk totals (a block scan in rounds of kThreads
+  // chunks), then the node totals as their differences: node i covers the
+  // 2^cto(i) chunks ending at i, so G_i = cum_i - cum_{i - 2^cto(i)}.
+  double carry = 0.0;
+  for (int base = 0; base < N; base += kThreads) {
+    const int i = base + threadIdx.x;
+    double x = i < N ? tot[bh * N + i] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
     }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    double off = carry, round = carry;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) off += wsum[w];
+      round += wsum[w];
+    }
+    x += off;
+    if (i < N) {
+      Gs[i] = x;
+      if (cum && blockIdx.x == 0) cum[bh * N + i] = x;
+    }
+    carry = round;
+    __syncthreads();
   }
-  __syncthreads();
+  // top round first: a node reads a lower index, which a later round rewrites,
+  // and within a round every read precedes the writes
+  for (int base = ((N - 1) / kThreads) * kThreads; base >= 0; base -= kThreads) {
+    const int i = base + threadIdx.x;
+    double g = 0.0;
+    if (i < N) {
+      const int lo = i - (1 << (__ffs(~i) - 1));
+      g = Gs[i] - (lo >= 0 ? Gs[lo] : 0.0);
+    }
+    __syncthreads();
+    if (i < N) Gs[i] = g;
+    __syncthreads();
+  }
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < N; i += kThreads) G[bh * N + i] = Gs[i];
   const int idx = blockIdx.x * kThreads + threadIdx.x;
