@@ -30,6 +30,10 @@
 // operands, one thread issues the MMAs and commits them to an mbarrier, every
 // thread waits (bounded: after 4 s the error word is set and the kernel
 // finishes without the results), then the row-wise epilogue.
+#include <cudaTypedefs.h>
+
+#include <atomic>
+
 #include "bwd.cuh"
 #include "sm100.cuh"
 
@@ -179,6 +183,14 @@ __device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, 
   cs[t] = x;
 }
 
+// The full tile of rows row0 .. row0+127 of a [rows, 128] bf16 tensor by two
+// TMA boxes of [128 x 64] (128-byte swizzle: the layout of swz), completion
+// counted on `bar`.
+__device__ __forceinline__ void tma_tile(unsigned char* dst, const CUtensorMap* map, uint64_t* bar, size_t row0) {
+  tma_load_2d(dst, map, bar, 0, (int)row0);
+  tma_load_2d(dst + kHalf, map, bar, 64, (int)row0);
+}
+
 // Common prologue: the mbarrier and the TMEM allocation (warp 0).
 template <uint32_t kCols>
 __device__ __forceinline__ uint32_t setup_tmem(uint64_t* bar, uint32_t* slot) {
@@ -242,6 +254,8 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
 }
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
+    const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
     float* __restrict__ dq32, float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam,
@@ -253,25 +267,42 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   float* colpart = wdec + kT;  // [4 warps][128 columns] of sum_i P_ij G_ij
   float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
   uint64_t* bar = reinterpret_cast<uint64_t*>(c2 + kT);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
   const int tid = threadIdx.x;
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
-  if (tid == 0) *abort_s = 0;
+  const bool tma = use_tma && nv == kT;  // a partial tile: its missing rows are zeros, staged by the threads
+  if (tid == 0) {
+    *abort_s = 0;
+    mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
+  }
   tile_cumsum(cs, log_alpha, row0, nv);
   if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
   const uint32_t tmem = setup_tmem<512>(bar, slot);
-  stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
-  stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
-  stage_bf16(base + kIntraV, v + row0 * kD, nv, tid);
-  stage_bf16(base + kIntraG, dout + row0 * kD, nv, tid);
+  bool ok = true;
+  if (tma) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(inbar, 4 * kTileB);
+      tma_tile(base + kIntraQ, &tq, inbar, row0);
+      tma_tile(base + kIntraK, &tk, inbar, row0);
+      tma_tile(base + kIntraV, &tv, inbar, row0);
+      tma_tile(base + kIntraG, &tg, inbar, row0);
+    }
+    ok = wait_phase(inbar, 0, err, abort_s);
+  } else {
+    stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
+    stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
+    stage_bf16(base + kIntraV, v + row0 * kD, nv, tid);
+    stage_bf16(base + kIntraG, dout + row0 * kD, nv, tid);
+  }
   to_async();
   const uint32_t sQ = smem_u32(base + kIntraQ), sK = smem_u32(base + kIntraK), sV = smem_u32(base + kIntraV),
                  sG = smem_u32(base + kIntraG), sP = smem_u32(base + kIntraP), sA = smem_u32(base + kIntraA);
-  if (tid == 0) {
+  if (tid == 0 && ok) {
     mma128(tmem + 0, sQ, false, sK, false, false);    // A = Q K^T
     mma128(tmem + 128, sG, false, sV, false, false);  // G = dO V^T
     umma_commit(bar);
@@ -279,7 +310,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   c2[tid] = (float)cs[tid] * 1.4426950408889634f;
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
   __syncthreads();
-  bool ok = wait_phase(bar, 0, err, abort_s);
+  ok = ok && wait_phase(bar, 0, err, abort_s);
   tc_fence_after();
   {
     // row i = tid: P, dA (bf16) and the in-tile levels of dlam
@@ -422,9 +453,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
 // ------------------------------------------------------------------ query side
 constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
 constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
-constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }  // + cs, two mbarriers, TMEM slot, flag
+constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }  // + cs, three mbarriers, TMEM slot, flag
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
+    const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
     const float* __restrict__ dq32, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam, float* __restrict__ R,
@@ -434,16 +466,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
   double* cs = reinterpret_cast<double*>(base + kQryEnd);
   uint64_t* bar = reinterpret_cast<uint64_t*>(cs + kT);
   uint64_t* ldbar = bar + 1;  // the bulk load of a node tile
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
+  uint64_t* inbar = bar + 2;  // the TMA loads of the input tiles
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
   const int tid = threadIdx.x;
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
+  const bool tma = use_tma && nv == kT;
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(ldbar, 1);  // made visible by the fence in setup_tmem
+    mbar_init(inbar, 1);
   }
   tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<512>(bar, slot);
@@ -461,14 +496,24 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     return -1;
   };
   if (tid == 0 && c > 0) load_node(next_bit(-1));
-  stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
-  stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
+  bool ok = true;
+  if (tma) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(inbar, 2 * kTileB);
+      tma_tile(base + kQryQ, &tq, inbar, row0);
+      tma_tile(base + kQryG, &tg, inbar, row0);
+    }
+    ok = wait_phase(inbar, 0, err, abort_s);
+  } else {
+    stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
+    stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
+  }
   __syncthreads();
   const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
                  sF = smem_u32(base + kQryF);
   const int i = tid;
   double D = 0.0;
-  bool ok = true, first = true;
+  bool first = true;
   uint32_t phase = 0;
   for (int h = 0; (c >> h) != 0; ++h) {
     if (!((c >> h) & 1)) continue;
@@ -576,6 +621,7 @@ constexpr uint32_t kKeyK = 0, kKeyV = kTileB, kKeyE = 2 * kTileB, kKeyEnd = 3 * 
 constexpr size_t key_smem() { return 1024 + kKeyEnd + kT * 8 + kT * 4 + kT * 4 + 32 * 12 + 64; }
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
+    const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, int use_tma,
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
     const double* __restrict__ cum, const float* __restrict__ dk32, const float* __restrict__ dv32,
@@ -590,7 +636,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const float** srcs = reinterpret_cast<const float**>(coef + 32);  // [32]
   int* n_s = reinterpret_cast<int*>(srcs + 32);
   uint64_t* bar = reinterpret_cast<uint64_t*>(n_s + 2);
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 1);
+  uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
@@ -598,8 +645,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
   const size_t mat = (size_t)kD * kD;
+  const bool tma = use_tma && nv == kT;
   if (tid == 0) {
     *abort_s = 0;
+    mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
     int n = 0;
     const double cum_c = cum[bh * N + c];
     for (int h = 0; h < 31 && n < 32; ++h) {
@@ -616,9 +665,18 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const uint32_t tmem = setup_tmem<256>(bar, slot);
   const int n = *n_s;
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
-  stage_bf16(base + kKeyK, k + row0 * kD, nv, tid);
-  stage_bf16(base + kKeyV, v + row0 * kD, nv, tid);
-  if (n > 0) stage_f32_sum(base + kKeyE, srcs, coef, n, tid);
+  if (tma) {
+    if (tid == 0) {
+      mbar_arrive_expect_tx(inbar, 2 * kTileB);
+      tma_tile(base + kKeyK, &tk, inbar, row0);
+      tma_tile(base + kKeyV, &tv, inbar, row0);
+    }
+  } else {
+    stage_bf16(base + kKeyK, k + row0 * kD, nv, tid);
+    stage_bf16(base + kKeyV, v + row0 * kD, nv, tid);
+  }
+  if (n > 0) stage_f32_sum(base + kKeyE, srcs, coef, n, tid);  // overlaps the TMA loads
+  if (tma) wait_phase(inbar, 0, err, abort_s);
   to_async();
   if (n > 0) {
     const uint32_t sK = smem_u32(base + kKeyK), sV = smem_u32(base + kKeyV), sE = smem_u32(base + kKeyE);
@@ -686,6 +744,33 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
 
 }  // namespace
 
+PFN_cuTensorMapEncodeTiled_v12000 map_encoder() {
+  static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
+  static std::atomic<bool> tried{false};
+  if (!fn && !tried.exchange(true)) {
+    void* ptr = nullptr;
+    cudaDriverEntryPointQueryResult qr;
+    if (cudaGetDriverEntryPointByVersion("cuTensorMapEncodeTiled", &ptr, 12000, cudaEnableDefault, &qr) ==
+            cudaSuccess &&
+        qr == cudaDriverEntryPointSuccess)
+      fn = reinterpret_cast<PFN_cuTensorMapEncodeTiled_v12000>(ptr);
+  }
+  return fn;
+}
+
+// [rows, 128] bf16 with [128 x 64] boxes and the 128-byte swizzle: two boxes make a tile
+bool tile_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint32_t box[2] = {64, (cuuint32_t)kT};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool bwd_tc_supported(const ll_shape& s) { return s.io == LL_BF16 && s.dk == 128 && s.dv == 128; }
 
 ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
@@ -699,20 +784,26 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const auto* k = static_cast<const __nv_bfloat16*>(a.k);
   const auto* v = static_cast<const __nv_bfloat16*>(a.v);
   const auto* dout = static_cast<const __nv_bfloat16*>(a.dout);
+  // the input tiles by TMA where the row coordinate fits the copy's 32-bit
+  // operand; otherwise (and if the maps cannot be made) the threads stage them
+  const uint64_t rows = (uint64_t)BH * s.T;
+  CUtensorMap tq, tk, tv, tg;
+  const int use_tma = rows <= 0x7fffffffull && tile_map(&tq, q, rows) && tile_map(&tk, k, rows) &&
+                      tile_map(&tv, v, rows) && tile_map(&tg, dout, rows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
-  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
+  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
                                                                   b.dv32, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dq32,
+  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dq32,
                                                                   static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
                                                                   s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
-      k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
+      tk, tv, use_tma, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), b.dc, b.ctot, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
