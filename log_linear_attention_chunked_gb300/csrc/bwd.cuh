@@ -30,7 +30,8 @@ ll_status bwd_simt_launch(const BwdArgs& a);
 // the tensor-core backward (bf16 io, d_k = d_v = 128, 128-token tiles) on
 // buffers laid out by the CUDA-core backward's plan
 struct BwdTcBuffers {
-  float *dq32, *dk32, *dv32, *S, *F, *R;
+  __nv_bfloat16 *dqp, *dkp, *dvp;  // the in-tile parts of dq, dk, dv (bf16)
+  float *S, *F, *R;
   __nv_bfloat16* Ft;  // the nodes F as bf16 tiles
   double *tot, *G, *cum;
   float* dc;

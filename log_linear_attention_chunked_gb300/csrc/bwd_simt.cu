@@ -95,10 +95,12 @@ BwdPlan plan_of(const ll_shape& s) {
   p.off_cum = off;
   if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * sizeof(double), 256);  // running chunk totals
   p.off_dq = p.off_dk = p.off_dv = off;
-  if (s.io != LL_F32) {  // float32 partial sums of dq, dk, dv (float32 io accumulates in the outputs)
-    p.off_dq = off; off = align_up(off + BH * (size_t)s.T * s.dk * sizeof(float), 256);
-    p.off_dk = off; off = align_up(off + BH * (size_t)s.T * s.dk * sizeof(float), 256);
-    p.off_dv = off; off = align_up(off + BH * (size_t)s.T * s.dv * sizeof(float), 256);
+  if (s.io != LL_F32) {  // partial sums of dq, dk, dv (float32 io accumulates in the outputs):
+    // float32 on the CUDA cores, the in-tile parts in bf16 on the tensor-core path
+    const size_t pe = bwd_tc_supported(s) ? 2 : sizeof(float);
+    p.off_dq = off; off = align_up(off + BH * (size_t)s.T * s.dk * pe, 256);
+    p.off_dk = off; off = align_up(off + BH * (size_t)s.T * s.dk * pe, 256);
+    p.off_dv = off; off = align_up(off + BH * (size_t)s.T * s.dv * pe, 256);
   }
   p.total = off;
   return p;
@@ -931,7 +933,8 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const IO* dout = static_cast<const IO*>(a.dout);
 
   if (bwd_tc_supported(s)) {
-    const BwdTcBuffers b{dq32, dk32, dv32, S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G,
+    const BwdTcBuffers b{reinterpret_cast<__nv_bfloat16*>(dq32), reinterpret_cast<__nv_bfloat16*>(dk32),
+                         reinterpret_cast<__nv_bfloat16*>(dv32), S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G,
                          reinterpret_cast<double*>(ws + p.off_cum), dc, ctot, a.err};
     const ll_status st = bwd_tc_launch(a, b);
     if (st != LL_OK) return st;

@@ -159,6 +159,12 @@ __device__ __forceinline__ void stage_f32_sum(unsigned char* tile, const float* 
 }
 
 // row r of a swizzled tile, 8 elements of chunk c8, as floats
+// 8 bf16 of a 16-byte word as floats
+__device__ __forceinline__ void unpack8(const uint4& u, float* x) {
+  const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
+  x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
+}
+
 __device__ __forceinline__ void row_chunk(const unsigned char* tile, int r, int c8, float* x) {
   const uint4 u = *reinterpret_cast<const uint4*>(tile + swz(r, c8));
   const float2 a = unpack_bf16x2(u.x), b = unpack_bf16x2(u.y), c = unpack_bf16x2(u.z), d = unpack_bf16x2(u.w);
@@ -258,7 +264,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
-    float* __restrict__ dq32, float* __restrict__ dk32, float* __restrict__ dv32, float* __restrict__ dlam,
+    __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dkp, __nv_bfloat16* __restrict__ dvp,
+    float* __restrict__ dlam,
     float* __restrict__ S, double* __restrict__ tot, float* __restrict__ dc, int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -421,27 +428,40 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   {
     // Every operand tile is free now: each output row is staged in shared
     // memory (two alternating buffers of padded rows over the tiles) and
-    // written by one 512-byte bulk copy.
+    // written by one bulk copy: the in-tile parts of dq, dk, dv as bf16 rows
+    // (256 B; the later kernels add the inter-tile parts in float32), the
+    // chunk state S_c as float32 rows (512 B).
     const int r = tid;
-    float* outs[4] = {dq32 + (row0 + r) * kD, dk32 + (row0 + r) * kD, dv32 + (row0 + r) * kD,
-                      S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD};
+    __nv_bfloat16* parts[3] = {dqp + (row0 + r) * kD, dkp + (row0 + r) * kD, dvp + (row0 + r) * kD};
+    float* srow = S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD;
 #pragma unroll 1
     for (int o = 0; o < 4; ++o) {
       const bool keep = o == 3 || r < nv;  // S has every row; the gradients only the present ones
-      float* rowp = reinterpret_cast<float*>(base + (o & 1) * (kT * kRowP * 4)) + r * kRowP;
-      if (o >= 2) bulk_wait_read0();  // the copy of output o - 2 has read this row
+      unsigned char* buf = base + (o & 1) * (kT * kRowP * 4);
+      float* rowp = reinterpret_cast<float*>(buf) + r * kRowP;                    // float32 rows, 528 B apart
+      __nv_bfloat16* rowb = reinterpret_cast<__nv_bfloat16*>(buf) + r * (kD + 8);  // bf16 rows, 272 B apart
+      if (o >= 2) bulk_wait_read0();  // the copy of output o - 2 has read this buffer
 #pragma unroll 1
       for (int cb = 0; cb < 4; ++cb) {
         float x[32];
         tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
         tmem_ld_wait();
+        if (o == 3) {
 #pragma unroll
-        for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4*>(rowp + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+          for (int u = 0; u < 32; u += 4)
+            *reinterpret_cast<float4*>(rowp + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; u += 8)
+            *reinterpret_cast<uint4*>(rowb + 32 * cb + u) =
+                make_uint4(pack_bf16x2(x[u], x[u + 1]), pack_bf16x2(x[u + 2], x[u + 3]),
+                           pack_bf16x2(x[u + 4], x[u + 5]), pack_bf16x2(x[u + 6], x[u + 7]));
+        }
       }
       if (keep && ok) {
         fence_proxy_async_shared();
-        bulk_store(outs[o], rowp, kD * 4);
+        if (o == 3) bulk_store(srow, rowp, kD * 4);
+        else bulk_store(parts[o], rowb, kD * 2);
         bulk_commit();
       }
     }
@@ -459,7 +479,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
-    const float* __restrict__ dq32, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam, float* __restrict__ R,
+    const __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam,
+    float* __restrict__ R,
     int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
@@ -589,7 +610,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       if (!(hh < 31 && ((c >> hh) & 1))) dlam[(row0 + i) * L + l] = 0.f;
     }
   {
-    const float* src = dq32 + (row0 + i) * kD;
+    const __nv_bfloat16* src = dqp + (row0 + i) * kD;
     __nv_bfloat16* dst = dq + (row0 + i) * kD;
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
@@ -604,11 +625,11 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       if (i < nv)
 #pragma unroll
       for (int u = 0; u < 32; u += 8) {
-        const float4 a = *reinterpret_cast<const float4*>(src + 32 * cb + u);
-        const float4 b = *reinterpret_cast<const float4*>(src + 32 * cb + u + 4);
+        float a[8];
+        unpack8(*reinterpret_cast<const uint4*>(src + 32 * cb + u), a);
         *reinterpret_cast<uint4*>(dst + 32 * cb + u) =
-            make_uint4(pack_bf16x2(a.x + x[u], a.y + x[u + 1]), pack_bf16x2(a.z + x[u + 2], a.w + x[u + 3]),
-                       pack_bf16x2(b.x + x[u + 4], b.y + x[u + 5]), pack_bf16x2(b.z + x[u + 6], b.w + x[u + 7]));
+            make_uint4(pack_bf16x2(a[0] + x[u], a[1] + x[u + 1]), pack_bf16x2(a[2] + x[u + 2], a[3] + x[u + 3]),
+                       pack_bf16x2(a[4] + x[u + 4], a[5] + x[u + 5]), pack_bf16x2(a[6] + x[u + 6], a[7] + x[u + 7]));
       }
     }
   }
@@ -624,7 +645,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, int use_tma,
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
-    const double* __restrict__ cum, const float* __restrict__ dk32, const float* __restrict__ dv32,
+    const double* __restrict__ cum, const __nv_bfloat16* __restrict__ dkp, const __nv_bfloat16* __restrict__ dvp,
     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dc,
     double* __restrict__ ctot, int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
@@ -693,7 +714,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   float vdv = 0.f;
 #pragma unroll 1
   for (int o = 0; o < 2; ++o) {  // 0: dv, 1: dk
-    const float* src = (o == 0 ? dv32 : dk32) + (row0 + j) * kD;
+    const __nv_bfloat16* src = (o == 0 ? dvp : dkp) + (row0 + j) * kD;
     __nv_bfloat16* dst = (o == 0 ? dv : dk) + (row0 + j) * kD;
 #pragma unroll 1
     for (int cb = 0; cb < 4; ++cb) {
@@ -708,11 +729,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
       if (j < nv) {
 #pragma unroll
         for (int u = 0; u < 32; u += 8) {
-          const float4 a = *reinterpret_cast<const float4*>(src + 32 * cb + u);
-          const float4 b = *reinterpret_cast<const float4*>(src + 32 * cb + u + 4);
-          float y[8] = {fmaf(wj, x[u], a.x),     fmaf(wj, x[u + 1], a.y), fmaf(wj, x[u + 2], a.z),
-                        fmaf(wj, x[u + 3], a.w), fmaf(wj, x[u + 4], b.x), fmaf(wj, x[u + 5], b.y),
-                        fmaf(wj, x[u + 6], b.z), fmaf(wj, x[u + 7], b.w)};
+          float y[8];
+          unpack8(*reinterpret_cast<const uint4*>(src + 32 * cb + u), y);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) y[t] = fmaf(wj, x[u + t], y[t]);
           if (o == 0) {  // the part of v_j . dv_j from the later tiles
             float vv[8];
             row_chunk(base + kKeyV, j, (32 * cb + u) >> 3, vv);
@@ -791,19 +811,19 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int use_tma = rows <= 0x7fffffffull && tile_map(&tq, q, rows) && tile_map(&tk, k, rows) &&
                       tile_map(&tv, v, rows) && tile_map(&tg, dout, rows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
-  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dq32, b.dk32,
-                                                                  b.dv32, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
+  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp,
+                                                                  b.dvp, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dq32,
+  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
                                                                   static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
                                                                   s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
-      tk, tv, use_tma, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dk32, b.dv32, static_cast<__nv_bfloat16*>(a.dk),
+      tk, tv, use_tma, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dkp, b.dvp, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), b.dc, b.ctot, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
