@@ -175,18 +175,20 @@ __device__ __forceinline__ void row_chunk(const unsigned char* tile, int r, int 
 // float64; every thread takes part (a scan over each warp, then the warps'
 // totals); the caller synchronises before reading cs
 __device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
-  __shared__ double wsum[kThreads / 32];
+  __shared__ double wsum[8];  // the warps of the tile's rows (threads past 128 only synchronise)
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  double x = t < nv ? (double)log_alpha[row0 + t] : 0.0;
+  double x = (t < kT && t < nv) ? (double)log_alpha[row0 + t] : 0.0;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const double y = __shfl_up_sync(0xffffffffu, x, o);
     if (lane >= o) x += y;
   }
-  if (lane == 31) wsum[w] = x;
+  if (lane == 31 && w < 8) wsum[w] = x;
   __syncthreads();
-  for (int ww = 0; ww < w; ++ww) x += wsum[ww];
-  cs[t] = x;
+  if (t < kT) {
+    for (int ww = 0; ww < w; ++ww) x += wsum[ww];
+    cs[t] = x;
+  }
 }
 
 // The full tile of rows row0 .. row0+127 of a [rows, 128] bf16 tensor by two
@@ -233,15 +235,16 @@ __device__ __forceinline__ void to_async() {
   tc_fence_after();
 }
 
-// this thread's TMEM lane (row threadIdx.x) at column col
+// this thread's TMEM lane (row threadIdx.x mod 128: warp w reads lanes 32 (w mod 4) ..) at column col
 __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
-  return tmem + ((uint32_t)((threadIdx.x >> 5) * 32) << 16) + (uint32_t)col;
+  return tmem + ((uint32_t)(((threadIdx.x >> 5) & 3) * 32) << 16) + (uint32_t)col;
 }
 
 // ------------------------------------------------------------------ intra
 constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
-constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + 64; }
+constexpr int kIntraThreads = 256;  // two threads per row: columns 0..63 and 64..127
+constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + 64; }
 
 // Reduce-scatter over a warp: lane l receives the sum over the 32 lanes of v[l].
 __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
@@ -259,7 +262,7 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
   return v[0];
 }
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
+__global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
@@ -273,7 +276,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
   float* wdec = reinterpret_cast<float*>(cs + kT);
   float* colpart = wdec + kT;  // [4 warps][128 columns] of sum_i P_ij G_ij
   float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
-  uint64_t* bar = reinterpret_cast<uint64_t*>(c2 + kT);
+  float* dlhalf = c2 + kT;       // [128][8] the in-tile dlam of the columns 64..127
+  uint64_t* bar = reinterpret_cast<uint64_t*>(dlhalf + kT * 8);
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
@@ -300,7 +304,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
       tma_tile(base + kIntraG, &tg, inbar, row0);
     }
     ok = wait_phase(inbar, 0, err, abort_s);
-  } else {
+  } else if (tid < kT) {
     stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
     stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
     stage_bf16(base + kIntraV, v + row0 * kD, nv, tid);
@@ -314,26 +318,30 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
     mma128(tmem + 128, sG, false, sV, false, false);  // G = dO V^T
     umma_commit(bar);
   }
-  c2[tid] = (float)cs[tid] * 1.4426950408889634f;
-  wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+  // row i = tid mod 128, columns 64 hf .. 64 hf + 63 of it
+  const int i = tid & (kT - 1), hf = tid >> 7;
+  if (tid < kT) {
+    c2[tid] = (float)cs[tid] * 1.4426950408889634f;
+    wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+  }
+  float lm[8];  // the row's in-tile lambdas, loaded while the products run
+#pragma unroll
+  for (int l = 0; l < 8; ++l) lm[l] = (i < nv && l < L) ? lam[(row0 + i) * L + l] : 0.f;
   __syncthreads();
   ok = ok && wait_phase(bar, 0, err, abort_s);
   tc_fence_after();
   {
-    // row i = tid: P, dA (bf16) and the in-tile levels of dlam
+    // row i: P, dA (bf16) and the in-tile levels of dlam.
     // Warp wi holds rows 32 wi .. 32 wi + 31: the 32-column blocks above its
     // diagonal block are masked, those below it hold one level (5 + bitlen(wi ^ cb)).
-    const int i = tid, wi = tid >> 5, lane = tid & 31;
+    const int wi = (tid >> 5) & 3, lane = tid & 31;
     const bool row_ok = i < nv;
-    float lm[8], dl[8];
+    float dl[8];
 #pragma unroll
-    for (int l = 0; l < 8; ++l) {
-      lm[l] = (row_ok && l < L) ? lam[(row0 + i) * L + l] : 0.f;
-      dl[l] = 0.f;
-    }
+    for (int l = 0; l < 8; ++l) dl[l] = 0.f;
     const float ci = c2[i];
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
       float p[32], da[32];
       if (cb > wi) {
 #pragma unroll
@@ -395,18 +403,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
                        pack_bf16x2(da[8 * w + 4], da[8 * w + 5]), pack_bf16x2(da[8 * w + 6], da[8 * w + 7]));
       }
     }
-    if (i < nv)
-      for (int l = 0; l < 8 && l < L; ++l) dlam[(row0 + i) * L + l] = dl[l];
+    if (hf == 1)
+#pragma unroll
+      for (int l = 0; l < 8; ++l) dlhalf[i * 8 + l] = dl[l];
+    __syncthreads();  // the column sums and the second half's levels of every row
+    if (hf == 0 && i < nv)
+      for (int l = 0; l < 8 && l < L; ++l) dlam[(row0 + i) * L + l] = dl[l] + dlhalf[i * 8 + l];
   }
-  __syncthreads();  // wdec and the column sums of every row
   if (tid < nv)  // the in-tile part of -v_j . dv_j; the key side adds the rest of dc_j
     dc[row0 + tid] = -(colpart[tid] + colpart[kT + tid] + colpart[2 * kT + tid] + colpart[3 * kT + tid]);
-  // V rows scaled by wdec (the G product that read V has completed)
+  // V rows scaled by wdec (the G product that read V has completed): chunks 8 hf .. 8 hf + 7 of row i
   {
-    const int j = tid;
+    const int j = i;
     const float s = wdec[j];
 #pragma unroll 4
-    for (int c8 = 0; c8 < 16; ++c8) {
+    for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
       float x[8];
       row_chunk(base + kIntraV, j, c8, x);
       *reinterpret_cast<uint4*>(base + kIntraV + swz(j, c8)) =
@@ -431,9 +442,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
     // written by one bulk copy: the in-tile parts of dq, dk, dv as bf16 rows
     // (256 B; the later kernels add the inter-tile parts in float32), the
     // chunk state S_c as float32 rows (512 B).
-    const int r = tid;
-    __nv_bfloat16* parts[3] = {dqp + (row0 + r) * kD, dkp + (row0 + r) * kD, dvp + (row0 + r) * kD};
-    float* srow = S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD;
+    const int r = i;  // this thread's half row: columns 64 hf .. 64 hf + 63
+    __nv_bfloat16* parts[3] = {dqp + (row0 + r) * kD + 64 * hf, dkp + (row0 + r) * kD + 64 * hf,
+                               dvp + (row0 + r) * kD + 64 * hf};
+    float* srow = S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD + 64 * hf;
 #pragma unroll 1
     for (int o = 0; o < 4; ++o) {
       const bool keep = o == 3 || r < nv;  // S has every row; the gradients only the present ones
@@ -442,7 +454,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
       __nv_bfloat16* rowb = reinterpret_cast<__nv_bfloat16*>(buf) + r * (kD + 8);  // bf16 rows, 272 B apart
       if (o >= 2) bulk_wait_read0();  // the copy of output o - 2 has read this buffer
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
         float x[32];
         tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
         tmem_ld_wait();
@@ -460,8 +472,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_intra_kernel(
       }
       if (keep && ok) {
         fence_proxy_async_shared();
-        if (o == 3) bulk_store(srow, rowp, kD * 4);
-        else bulk_store(parts[o], rowb, kD * 2);
+        if (o == 3) bulk_store(srow, rowp + 64 * hf, 64 * 4);
+        else bulk_store(parts[o], rowb + 64 * hf, 64 * 2);
         bulk_commit();
       }
     }
@@ -811,7 +823,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int use_tma = rows <= 0x7fffffffull && tile_map(&tq, q, rows) && tile_map(&tk, k, rows) &&
                       tile_map(&tv, v, rows) && tile_map(&tg, dout, rows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
-  bwd_tc_intra_kernel<<<grid, kThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp,
+  bwd_tc_intra_kernel<<<grid, kIntraThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp,
                                                                   b.dvp, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
