@@ -485,9 +485,11 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
 // ------------------------------------------------------------------ query side
 constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
 constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
-constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + 64; }  // + cs, three mbarriers, TMEM slot, flag
+constexpr int kQryThreads = 256;  // two threads per row: columns 0..63 and 64..127
+// + cs, the second halves' dlam dots, three mbarriers, TMEM slot, flag
+constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + kT * 4 + 64; }
 
-__global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
+__global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
@@ -497,7 +499,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kQryEnd);
-  uint64_t* bar = reinterpret_cast<uint64_t*>(cs + kT);
+  float* qpart = reinterpret_cast<float*>(cs + kT);  // [128] the dlam dot of the columns 64..127
+  uint64_t* bar = reinterpret_cast<uint64_t*>(qpart + kT);
   uint64_t* ldbar = bar + 1;  // the bulk load of a node tile
   uint64_t* inbar = bar + 2;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
@@ -537,14 +540,14 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       tma_tile(base + kQryG, &tg, inbar, row0);
     }
     ok = wait_phase(inbar, 0, err, abort_s);
-  } else {
+  } else if (tid < kT) {
     stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
     stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
   }
   __syncthreads();
   const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
                  sF = smem_u32(base + kQryF);
-  const int i = tid;
+  const int i = tid & (kT - 1), hf = tid >> 7;  // row i, columns 64 hf .. 64 hf + 63
   double D = 0.0;
   bool first = true;
   uint32_t phase = 0;
@@ -554,9 +557,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     const int lv = kLc + 1 + h;
     const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
     const float lw = i < nv ? w * lam[(row0 + i) * L + lv] : 0.f;
-    // dO rows scaled by lw
+    // dO rows scaled by lw (this thread's half row)
 #pragma unroll 4
-    for (int c8 = 0; c8 < 16; ++c8) {
+    for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
       float x[8];
       row_chunk(base + kQryG, i, c8, x);
       *reinterpret_cast<uint4*>(base + kQryL + swz(i, c8)) =
@@ -576,10 +579,10 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     phase ^= 1;
     tc_fence_after();
     if (tid == 0 && ok && next_bit(h) >= 0) load_node(next_bit(h));  // the products have read the tile
+    float part = 0.f;
     {
-      float part = 0.f;
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
         float g[32];
         tmem_ld32(lane_addr(tmem, 32 * cb), g);
         tmem_ld_wait();
@@ -591,13 +594,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
           for (int u = 0; u < 8; ++u) part = fmaf(g[8 * w4 + u], x[u], part);
         }
       }
-      if (i < nv) dlam[(row0 + i) * L + lv] = w * part;
+      if (hf == 1) qpart[i] = part;
       // row e' = i of this tile's part of R_e: staged in shared memory, then
-      // added into R_e by the bulk-copy unit (one 512-byte reduction per row)
+      // added into R_e by the bulk-copy unit (a 256-byte reduction per half row)
       float* rrow = reinterpret_cast<float*>(base + kQryR) + i * kRowP;
       bulk_wait_read0();  // the previous level's reduction has read this row
 #pragma unroll 1
-      for (int cb = 0; cb < 4; ++cb) {
+      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
         float x[32];
         tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
         tmem_ld_wait();
@@ -607,16 +610,17 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
       }
       if (ok) {
         fence_proxy_async_shared();
-        bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD, rrow, kD * 4);
+        bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD + 64 * hf, rrow + 64 * hf, 64 * 4);
         bulk_commit();
       }
     }
     D += G[bh * N + e];
     tc_fence_before();
     __syncthreads();  // the next level rewrites the staged tiles and the TMEM columns
+    if (hf == 0 && i < nv) dlam[(row0 + i) * L + lv] = w * (part + qpart[i]);
   }
   // the levels above 7 that hold no key of this tile's queries
-  if (i < nv)
+  if (hf == 0 && i < nv)
     for (int l = kLc + 1; l < L; ++l) {
       const int hh = l - kLc - 1;
       if (!(hh < 31 && ((c >> hh) & 1))) dlam[(row0 + i) * L + l] = 0.f;
@@ -625,7 +629,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_query_kernel(
     const __nv_bfloat16* src = dqp + (row0 + i) * kD;
     __nv_bfloat16* dst = dq + (row0 + i) * kD;
 #pragma unroll 1
-    for (int cb = 0; cb < 4; ++cb) {
+    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
       float x[32];
       if (!first) {  // uniform over the CTA: the warp-collective loads run in every lane
         tmem_ld32(lane_addr(tmem, 128 + 32 * cb), x);
@@ -829,7 +833,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
+  bwd_tc_query_kernel<<<grid, kQryThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
                                                                   static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
                                                                   s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
