@@ -254,6 +254,90 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
   }
 }
 
+// (3) for N <= kFenFastN: the same nodes with the chain kept on chip.  The
+// prologue also tabulates, in float, the decay of each child of each node
+// (exp(cum_i - cum_{i - 2^m}) for child i - 2^m; node i's children start at
+// entry i - popcount(i) of the table), and each thread keeps the latest node
+// of every level (the children of the next nodes) in shared memory, so a
+// step of the chain reads no node back from global memory and does no
+// float64 arithmetic.
+constexpr int kFenFastN = 4096;
+constexpr int kFenLv = 13;  // levels of N <= 4096
+
+__global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float* __restrict__ S,
+                                                                     float* __restrict__ F,
+                                                                     const double* __restrict__ tot,
+                                                                     double* __restrict__ G, int N, int mat,
+                                                                     __nv_bfloat16* __restrict__ Ft,
+                                                                     double* __restrict__ cum) {
+  extern __shared__ double Gs[];                                  // [N]
+  float* coef = reinterpret_cast<float*>(Gs + N);                 // [N] child decays
+  float* last = coef + N;                                         // [kFenLv][kThreads]
+  __shared__ double wsum[kThreads / 32];
+  const size_t bh = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  double carry = 0.0;
+  for (int base = 0; base < N; base += kThreads) {  // running sums of the chunk totals
+    const int i = base + threadIdx.x;
+    double x = i < N ? tot[bh * N + i] : 0.0;
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const double y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) wsum[warp] = x;
+    __syncthreads();
+    double off = carry, round = carry;
+    for (int w = 0; w < kThreads / 32; ++w) {
+      if (w < warp) off += wsum[w];
+      round += wsum[w];
+    }
+    x += off;
+    if (i < N) {
+      Gs[i] = x;
+      if (cum && blockIdx.x == 0) cum[bh * N + i] = x;
+    }
+    carry = round;
+    __syncthreads();
+  }
+  for (int i = threadIdx.x; i < N; i += kThreads) {  // the children's decays
+    const int h = __ffs(~i) - 1, o = i - __popc(i);
+    for (int m = 0; m < h; ++m) coef[o + m] = expf((float)(Gs[i] - Gs[i - (1 << m)]));
+  }
+  for (int base = ((N - 1) / kThreads) * kThreads; base >= 0; base -= kThreads) {  // node totals
+    const int i = base + threadIdx.x;
+    double g = 0.0;
+    if (i < N) {
+      const int lo = i - (1 << (__ffs(~i) - 1));
+      g = Gs[i] - (lo >= 0 ? Gs[lo] : 0.0);
+    }
+    __syncthreads();
+    if (i < N) Gs[i] = g;
+    __syncthreads();
+  }
+  if (blockIdx.x == 0)
+    for (int i = threadIdx.x; i < N; i += kThreads) G[bh * N + i] = Gs[i];
+  const int idx = blockIdx.x * kThreads + threadIdx.x;
+  if (idx >= mat) return;
+  const float* Sb = S + bh * N * (size_t)mat;
+  float* Fb = F + bh * N * (size_t)mat;
+  const int tel = Ft ? swizzled_elem(idx >> 7, idx & 127) : 0;
+  float s0 = Sb[idx], s1 = N > 1 ? Sb[(size_t)mat + idx] : 0.f, s2 = N > 2 ? Sb[2 * (size_t)mat + idx] : 0.f,
+        s3 = N > 3 ? Sb[3 * (size_t)mat + idx] : 0.f;
+  for (int i = 0; i < N; ++i) {
+    float acc = s0;
+    s0 = s1;
+    s1 = s2;
+    s2 = s3;
+    s3 = i + 4 < N ? Sb[(size_t)(i + 4) * mat + idx] : 0.f;
+    const int h = __ffs(~i) - 1, o = i - __popc(i);
+    for (int m = 0; m < h; ++m) acc = fmaf(coef[o + m], last[m * kThreads + threadIdx.x], acc);
+    last[h * kThreads + threadIdx.x] = acc;
+    Fb[(size_t)i * mat + idx] = acc;
+    if (Ft) Ft[(bh * N + i) * (size_t)mat + tel] = __float2bfloat16_rn(acc);
+  }
+}
+
 // (4): one CTA per (chunk, head); adds the inter-chunk levels to the intra
 // result and writes o.
 template <typename IO>
@@ -461,6 +545,14 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
                               cudaStream_t stream, __nv_bfloat16* Ft, double* cum) {
+  if (N <= kFenFastN) {
+    const size_t smf = (size_t)N * (sizeof(double) + sizeof(float)) + (size_t)kFenLv * kThreads * sizeof(float);
+    LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
+    simt_fenwick_fast_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(S, F, tot, G, N,
+                                                                                                   mat, Ft, cum);
+    LL_CUDA_OK(cudaGetLastError());
+    return LL_OK;
+  }
   const size_t sm = (size_t)N * sizeof(double);
   if (sm > 200 * 1024) return LL_ERR_UNSUPPORTED;  // chunk count beyond the on-chip prefix table
   LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm));
