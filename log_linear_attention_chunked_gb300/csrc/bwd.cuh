@@ -35,7 +35,6 @@ struct BwdTcBuffers {
   __nv_bfloat16* Ft;  // the nodes F as bf16 tiles
   double *tot, *G, *cum;
   float* dc;
-  double* ctot;
   unsigned* err;
 };
 bool bwd_tc_supported(const ll_shape& s);

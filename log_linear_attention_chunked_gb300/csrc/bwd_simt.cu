@@ -67,7 +67,7 @@ size_t key_smem(int Ce, int dk, int dv) {
 
 struct BwdPlan {
   int Ce, N, lc;
-  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_ctot, off_Ft, off_cum, total;
+  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_Ft, off_cum, total;
 };
 
 BwdPlan plan_of(const ll_shape& s) {
@@ -89,7 +89,6 @@ BwdPlan plan_of(const ll_shape& s) {
   p.off_tot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_G = off;   off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_dc = off;  off = align_up(off + BH * (size_t)s.T * sizeof(float), 256);
-  p.off_ctot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_Ft = off;
   if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * mat * 2, 256);  // the nodes as bf16 tiles
   p.off_cum = off;
@@ -303,12 +302,11 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
     const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
     const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv,
-    float* __restrict__ dc, double* __restrict__ ctot, int T, int dkd, int dvd, int L, int Ce) {
+    float* __restrict__ dc, int T, int dkd, int dvd, int L, int Ce) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float coef[32];
   __shared__ int ent[32];
   __shared__ int n_sh;
-  __shared__ float dcrow[128];  // dc of the chunk's rows (Ce <= 128)
   const int c = blockIdx.x;
   const int N = gridDim.x;
   const size_t bh = blockIdx.y;
@@ -392,46 +390,52 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
     for (int o = 16; o > 0; o >>= 1) a += __shfl_xor_sync(0xffffffffu, a, o);
     if (lane == 0) {
       if (j < nv) dc[row0 + j] = a;
-      dcrow[j] = a;
     }
-  }
-  __syncthreads();
-  if (tid == 0) {  // the chunk's total, in row order
-    double a = 0.0;
-    for (int j = 0; j < nv; ++j) a += (double)dcrow[j];
-    ctot[bh * N + c] = a;
   }
 }
 
-// (5) one CTA per head: dlog_alpha_r = sum_{t >= r} dc_t, in float64
+// (5) one CTA per head: dlog_alpha_r = sum_{t >= r} dc_t, in float64.  The
+// tokens go in rounds of kSuffixThreads runs of kSuffixRun consecutive tokens,
+// from the end of the sequence: each thread sums its run, a suffix scan over
+// the threads gives each run the sum of everything after it, and the thread
+// writes its run's suffix sums.
+constexpr int kSuffixRun = 16;
+
 __global__ void __launch_bounds__(kSuffixThreads) bwd_suffix_kernel(const float* __restrict__ dc,
-                                                                    const double* __restrict__ ctot,
-                                                                    float* __restrict__ dla, int T, int N,
-                                                                    int Ce) {
+                                                                    float* __restrict__ dla, int T) {
   __shared__ double part[kSuffixThreads];
   const size_t bh = blockIdx.x;
   const int tid = threadIdx.x;
-  // chunks are split over the threads in contiguous runs
-  const int per = (N + kSuffixThreads - 1) / kSuffixThreads;
-  const int c0 = min(N, tid * per), c1 = min(N, c0 + per);
-  double s = 0.0;
-  for (int c = c0; c < c1; ++c) s += ctot[bh * N + c];
-  part[tid] = s;
-  __syncthreads();
-  // exclusive suffix sums of the runs (Hillis-Steele over the threads)
-  for (int o = 1; o < kSuffixThreads; o <<= 1) {
-    const double add = tid + o < kSuffixThreads ? part[tid + o] : 0.0;
-    __syncthreads();
-    part[tid] += add;
-    __syncthreads();
-  }
-  double run = (tid + 1 < kSuffixThreads) ? part[tid + 1] : 0.0;
-  for (int c = c1 - 1; c >= c0; --c) {
-    const int hi = min(T, (c + 1) * Ce);
-    for (int t = hi - 1; t >= c * Ce; --t) {
-      run += (double)dc[bh * T + t];
-      dla[bh * T + t] = (float)run;
+  constexpr int kRound = kSuffixThreads * kSuffixRun;
+  double carry = 0.0;  // the sum over the tokens after this round
+  for (int end = T; end > 0; end -= kRound) {
+    const int start = max(0, end - kRound);
+    const int t0 = start + tid * kSuffixRun, t1 = min(end, t0 + kSuffixRun);
+    float v[kSuffixRun];
+    double s = 0.0;
+#pragma unroll
+    for (int u = 0; u < kSuffixRun; ++u) {
+      v[u] = t0 + u < t1 ? dc[bh * T + t0 + u] : 0.f;
+      s += (double)v[u];
     }
+    part[tid] = s;
+    __syncthreads();
+    for (int o = 1; o < kSuffixThreads; o <<= 1) {  // part[tid] = sum of the runs from tid on
+      const double add = tid + o < kSuffixThreads ? part[tid + o] : 0.0;
+      __syncthreads();
+      part[tid] += add;
+      __syncthreads();
+    }
+    double run = carry + (tid + 1 < kSuffixThreads ? part[tid + 1] : 0.0);
+#pragma unroll
+    for (int u = kSuffixRun - 1; u >= 0; --u) {
+      if (t0 + u < t1) {
+        run += (double)v[u];
+        dla[bh * T + t0 + u] = (float)run;
+      }
+    }
+    carry += part[0];
+    __syncthreads();
   }
 }
 
@@ -782,7 +786,7 @@ __global__ void __launch_bounds__(256, 1) bwd_key128_kernel(
     const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
     const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv, float* __restrict__ dc,
-    double* __restrict__ ctot, int T, int L) {
+    int T, int L) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float coef[32];
   __shared__ int ent[32];
@@ -895,12 +899,6 @@ __global__ void __launch_bounds__(256, 1) bwd_key128_kernel(
       dcrow[j] = a;
     }
   }
-  __syncthreads();
-  if (tid == 0) {
-    double a = 0.0;
-    for (int j = 0; j < nv; ++j) a += (double)dcrow[j];
-    ctot[bh * N + c] = a;
-  }
 }
 
 }  // namespace fast
@@ -918,7 +916,6 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   double* tot = reinterpret_cast<double*>(ws + p.off_tot);
   double* G = reinterpret_cast<double*>(ws + p.off_G);
   float* dc = reinterpret_cast<float*>(ws + p.off_dc);
-  double* ctot = reinterpret_cast<double*>(ws + p.off_ctot);
   const bool f32 = s.io == LL_F32;
   float* dq32 = f32 ? static_cast<float*>(a.dq) : reinterpret_cast<float*>(ws + p.off_dq);
   float* dk32 = f32 ? static_cast<float*>(a.dk) : reinterpret_cast<float*>(ws + p.off_dk);
@@ -935,10 +932,10 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   if (bwd_tc_supported(s)) {
     const BwdTcBuffers b{reinterpret_cast<__nv_bfloat16*>(dq32), reinterpret_cast<__nv_bfloat16*>(dk32),
                          reinterpret_cast<__nv_bfloat16*>(dv32), S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G,
-                         reinterpret_cast<double*>(ws + p.off_cum), dc, ctot, a.err};
+                         reinterpret_cast<double*>(ws + p.off_cum), dc, a.err};
     const ll_status st = bwd_tc_launch(a, b);
     if (st != LL_OK) return st;
-    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
     LL_CUDA_OK(cudaGetLastError());
     return LL_OK;
   }
@@ -959,9 +956,9 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
                                     (int)fast::key_smem()));
     fast::bwd_key128_kernel<IO><<<grid, 256, fast::key_smem(), a.stream>>>(
         k, v, a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32, static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc,
-        ctot, s.T, s.L);
+        s.T, s.L);
     LL_CUDA_OK(cudaGetLastError());
-    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
     LL_CUDA_OK(cudaGetLastError());
     return LL_OK;
   }
@@ -988,10 +985,10 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_key_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4));
   bwd_key_kernel<IO><<<grid, kThreads, sm4, a.stream>>>(
       static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32,
-      static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc, ctot, s.T, s.dk, s.dv, s.L, Ce);
+      static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc, s.T, s.dk, s.dv, s.L, Ce);
   LL_CUDA_OK(cudaGetLastError());
 
-  bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, ctot, a.dlog_alpha, s.T, p.N, Ce);
+  bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }

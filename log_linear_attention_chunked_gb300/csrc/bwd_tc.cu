@@ -663,13 +663,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
     const double* __restrict__ cum, const __nv_bfloat16* __restrict__ dkp, const __nv_bfloat16* __restrict__ dvp,
     __nv_bfloat16* __restrict__ dk, __nv_bfloat16* __restrict__ dv, float* __restrict__ dc,
-    double* __restrict__ ctot, int T, int L, unsigned* err) {
+    int T, int L, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kKeyEnd);
   float* wdec = reinterpret_cast<float*>(cs + kT);
-  float* dcrow = wdec + kT;
-  float* coef = dcrow + kT;                                      // [32]
+  float* coef = wdec + 2 * kT;                                   // [32]
   const float** srcs = reinterpret_cast<const float**>(coef + 32);  // [32]
   int* n_s = reinterpret_cast<int*>(srcs + 32);
   uint64_t* bar = reinterpret_cast<uint64_t*>(n_s + 2);
@@ -768,13 +767,6 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     a += dc[row0 + j] - vdv;  // dc holds the in-tile part, -sum_i P_ij G_ij
     dc[row0 + j] = a;
   }
-  dcrow[j] = a;
-  __syncthreads();
-  if (tid == 0) {
-    double s = 0.0;
-    for (int r = 0; r < nv; ++r) s += (double)dcrow[r];
-    ctot[bh * N + c] = s;
-  }
   release_tmem<256>(tmem);
 }
 
@@ -840,7 +832,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
       tk, tv, use_tma, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dkp, b.dvp, static_cast<__nv_bfloat16*>(a.dk),
-      static_cast<__nv_bfloat16*>(a.dv), b.dc, b.ctot, s.T, s.L, b.err);
+      static_cast<__nv_bfloat16*>(a.dv), b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }
