@@ -685,17 +685,20 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
-    int n = 0;
-    const double cum_c = cum[bh * N + c];
-    for (int h = 0; h < 31 && n < 32; ++h) {
-      if ((c >> h) & 1) continue;
-      const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
-      if (e + 1 >= N) break;  // e grows with h: no later node has queries either
-      srcs[n] = R + (bh * N + e) * mat;
-      coef[n] = expf((float)(cum[bh * N + e] - cum_c));  // the decay from the end of c to the end of e
-      ++n;
+  }
+  if (tid < 32) {  // lane h: the node of level h whose block holds the keys of c, if it has queries after it
+    const int h = tid;
+    const int e = h < 31 ? ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1 : 0;
+    const bool has = h < 31 && !((c >> h) & 1) && e + 1 < N;
+    float cf = 0.f;
+    if (has) cf = expf((float)(cum[bh * N + e] - cum[bh * N + c]));  // the decay from the end of c to the end of e
+    const unsigned m = __ballot_sync(0xffffffffu, has);
+    if (has) {
+      const int at = __popc(m & ((1u << h) - 1u));  // in order of level
+      srcs[at] = R + (bh * N + e) * mat;
+      coef[at] = cf;
     }
-    *n_s = n;
+    if (h == 0) *n_s = __popc(m);
   }
   tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<256>(bar, slot);
