@@ -703,6 +703,9 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<256>(bar, slot);
   const int n = *n_s;
+  float lamdot = 0.f;  // sum_l lam_j[l] dlam_j[l] of this row, loaded ahead of its use
+  if (tid < nv)
+    for (int l = 0; l < L; ++l) lamdot = fmaf(lam[(row0 + tid) * L + l], dlam[(row0 + tid) * L + l], lamdot);
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
   if (tma) {
     if (tid == 0) {
@@ -764,12 +767,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
       }
     }
   }
-  float a = 0.f;
-  if (j < nv) {
-    for (int l = 0; l < L; ++l) a = fmaf(lam[(row0 + j) * L + l], dlam[(row0 + j) * L + l], a);
-    a += dc[row0 + j] - vdv;  // dc holds the in-tile part, -sum_i P_ij G_ij
-    dc[row0 + j] = a;
-  }
+  if (j < nv) dc[row0 + j] = lamdot + dc[row0 + j] - vdv;  // dc held the in-tile part, -sum_i P_ij G_ij
   release_tmem<256>(tmem);
 }
 
