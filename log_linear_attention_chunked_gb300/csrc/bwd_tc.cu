@@ -23,13 +23,19 @@
 //           end of c; dv += diag(wdec) K E^T, dk += diag(wdec) V E, and
 //           dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j (the in-tile part of
 //           v_j . dv_j from the intra kernel).
-// The Fenwick nodes F_e and the suffix sums of dc are the CUDA-core kernels'.
+// The Fenwick nodes F_e (with a bf16 tile copy of each, which the query
+// kernel fetches by one bulk copy) and the suffix sums of dc are the
+// CUDA-core kernels'.
 //
-// One CTA of 128 threads per (tile, head); thread t owns TMEM lane t (row t of
-// every accumulator).  The phases of a tile run in sequence: stage the
-// operands, one thread issues the MMAs and commits them to an mbarrier, every
-// thread waits (bounded: after 4 s the error word is set and the kernel
-// finishes without the results), then the row-wise epilogue.
+// One CTA per (tile, head); thread t owns TMEM lane t mod 128 (row t mod 128
+// of every accumulator): 256 threads in the intra and query kernels, the two
+// threads of a row taking one half of its columns each, 128 in the key
+// kernel.  Full input tiles arrive by TMA (the ragged last tile of a head is
+// staged by the threads, its missing rows as zeros).  The phases of a tile run
+// in sequence: stage the operands, one thread issues the MMAs and commits them
+// to an mbarrier, every thread waits (bounded: after 4 s the error word is set
+// and the kernel finishes without the results), then the row-wise epilogue,
+// whose rows leave by bulk copies (or bulk reductions) from shared memory.
 #include <cudaTypedefs.h>
 
 #include <atomic>
