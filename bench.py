@@ -60,13 +60,18 @@ METRICS = {
 # ----------------------------------------------------------------------------
 def algorithmic_bytes(cfg) -> int:
     """Forward: q, k, v read once, log_alpha and lam (float32) read once, o
-    written once; plus beta for Gated DeltaNet."""
+    written once; plus beta for Gated DeltaNet.  Backward: its inputs (the
+    forward's and dout) read once and the five gradients written once."""
     b_io = 2 if cfg["io"] == "bf16" else 4
+    if cfg["kind"] == "mamba2_bwd":
+        # q, k, v, dout read and dq, dk, dv written (io dtype); log_alpha and
+        # lam read and their gradients written (float32)
+        dk, dv = cfg["dk"], cfg["dv"]
+        per_bh = cfg["T"] * ((2 * dk + 2 * dv) * b_io + (2 * dk + dv) * b_io + 2 * (4 + 4 * cfg["L"]))
+        return per_bh * cfg["B"] * cfg["H"]
     per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
     if cfg["kind"] in ("gdn", "gdn_b"):
         per_bh += cfg["T"] * 4
-    if cfg["kind"] == "mamba2_bwd":  # dout read; dq, dk, dv, dlog_alpha, dlam written
-        per_bh += cfg["T"] * (cfg["dv"] * b_io + 2 * cfg["dk"] * b_io + cfg["dv"] * b_io + 4 + 4 * cfg["L"])
     if cfg["kind"] == "mamba2_cont":  # the prefix states read, the states of t0 + T written (float32)
         t0, t1, d = cfg["t0"], cfg["t0"] + cfg["T"], cfg["dk"]
         per_bh += (bin(t0).count("1") + bin(t1).count("1")) * d * d * 4 + 2 * cfg["Ls"] * 4
