@@ -92,7 +92,7 @@ BwdPlan plan_of(const ll_shape& s) {
   p.off_Ft = off;
   if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * mat * 2, 256);  // the nodes as bf16 tiles
   p.off_cum = off;
-  if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * sizeof(double), 256);  // running chunk totals
+  off = align_up(off + BH * p.N * sizeof(double), 256);  // running sums of the chunk totals
   p.off_dq = p.off_dk = p.off_dv = off;
   if (s.io != LL_F32) {  // partial sums of dq, dk, dv (float32 io accumulates in the outputs):
     // float32 on the CUDA cores, the in-tile parts in bf16 on the tensor-core path
@@ -103,6 +103,27 @@ BwdPlan plan_of(const ll_shape& s) {
   }
   p.total = off;
   return p;
+}
+
+// cs[i] = the sum of log_alpha over rows 0..i of the chunk (rows >= nv add 0),
+// float64, for i < Ce <= 128; every thread of the CTA takes part (a scan over
+// each warp, then the warps' totals); cs is complete after the caller's next
+// __syncthreads
+__device__ __forceinline__ void chunk_scan(double* cs, const float* log_alpha, size_t row0, int nv, int Ce) {
+  __shared__ double wsum[4];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  double x = (t < Ce && t < nv) ? (double)log_alpha[row0 + t] : 0.0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31 && w < 4) wsum[w] = x;
+  __syncthreads();
+  if (t < Ce) {
+    for (int ww = 0; ww < w; ++ww) x += wsum[ww];
+    cs[t] = x;
+  }
 }
 
 // (1) one CTA per (chunk, head)
@@ -131,14 +152,8 @@ __global__ void __launch_bounds__(kThreads) bwd_intra_kernel(
 
   const size_t row0 = bh * T + (size_t)c * Ce;
   const int nv = min(Ce, T - c * Ce);
-  if (tid == 0) {
-    double acc = 0.0;
-    for (int i = 0; i < Ce; ++i) {
-      if (i < nv) acc += (double)log_alpha[row0 + i];
-      cs[i] = acc;
-    }
-    tot[bh * N + c] = acc;
-  }
+  chunk_scan(cs, log_alpha, row0, nv, Ce);
+  if (tid == Ce - 1) tot[bh * N + c] = cs[Ce - 1];
   for (int x = tid; x < Ce * dk; x += kThreads) {
     const int i = x / dk, f = x % dk;
     qs[i * dkp + f] = i < nv ? to_f(q[(row0 + i) * dk + f]) : 0.f;
@@ -234,13 +249,7 @@ __global__ void __launch_bounds__(kThreads) bwd_query_kernel(
 
   const size_t row0 = bh * T + (size_t)c * Ce;
   const int nv = min(Ce, T - c * Ce);
-  if (tid == 0) {
-    double a = 0.0;
-    for (int i = 0; i < Ce; ++i) {
-      if (i < nv) a += (double)log_alpha[row0 + i];
-      cs[i] = a;
-    }
-  }
+  chunk_scan(cs, log_alpha, row0, nv, Ce);
   for (int x = tid; x < Ce * dk; x += kThreads) {
     qs[x] = x < nv * dk ? to_f(q[row0 * dk + x]) : 0.f;
     acc[x] = 0.f;
@@ -301,7 +310,7 @@ template <typename IO>
 __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
     const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
-    const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv,
+    const double* __restrict__ cum, const float* dk32, const float* dv32, IO* dk, IO* dv,
     float* __restrict__ dc, int T, int dkd, int dvd, int L, int Ce) {
   extern __shared__ __align__(16) unsigned char smem_raw[];
   __shared__ float coef[32];
@@ -322,25 +331,20 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
   const size_t row0 = bh * T + (size_t)c * Ce;
   const int nv = min(Ce, T - c * Ce);
   if (tid == 0) {
-    double a = 0.0;
-    for (int i = 0; i < Ce; ++i) {
-      if (i < nv) a += (double)log_alpha[row0 + i];
-      cs[i] = a;
-    }
-    // the nodes whose blocks hold the keys of c and that have queries after them
-    int n = 0, cc = c;
-    double dec = 0.0;  // log-decay from the end of c to the end of e
+    // the nodes whose blocks hold the keys of c and that have queries after
+    // them, with the log-decay from the end of c to the end of each
+    int n = 0;
     for (int h = 0; h < 31 && n < 32; ++h) {
       if ((c >> h) & 1) continue;
       const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
       if (e + 1 >= N) break;  // e grows with h: no later node has queries either
-      while (cc < e) dec += tot[bh * N + (++cc)];
       ent[n] = e;
-      coef[n] = expf((float)dec);
+      coef[n] = expf((float)(cum[bh * N + e] - cum[bh * N + c]));
       ++n;
     }
     n_sh = n;
   }
+  chunk_scan(cs, log_alpha, row0, nv, Ce);
   for (int x = tid; x < Ce * dkd; x += kThreads) {
     const int j = x / dkd, f = x % dkd;
     ks[j * dkp + f] = j < nv ? to_f(k[(row0 + j) * dkd + f]) : 0.f;
@@ -545,14 +549,6 @@ __device__ __forceinline__ void nt(float (&c)[R][S], const float* A, const float
   }
 }
 
-__device__ __forceinline__ void chunk_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
-  double acc = 0.0;
-  for (int i = 0; i < kC; ++i) {
-    if (i < nv) acc += (double)log_alpha[row0 + i];
-    cs[i] = acc;
-  }
-}
-
 // rows 4ty + i of a 64 x 128 register tile to a float32 [.][128] array (rows < nv)
 __device__ __forceinline__ void store_rows(float* dst, const float (&c)[4][8], int nv, int ty, int tx) {
 #pragma unroll
@@ -594,10 +590,8 @@ __global__ void __launch_bounds__(256, 1) bwd_intra128_kernel(
   const int tid = threadIdx.x, ty = tid >> 4, tx = tid & 15;
   const size_t row0 = bh * T + (size_t)c * kC;
   const int nv = min(kC, T - c * kC);
-  if (tid == 0) {
-    chunk_cumsum(cs, log_alpha, row0, nv);
-    tot[bh * N + c] = cs[kC - 1];
-  }
+  chunk_scan(cs, log_alpha, row0, nv, kC);
+  if (tid == kC - 1) tot[bh * N + c] = cs[kC - 1];
   load_tile(qs, q + row0 * kD, nv, tid);
   load_tile(ks, k + row0 * kD, nv, tid);
   load_tile(vs, v + row0 * kD, nv, tid);
@@ -695,7 +689,7 @@ __global__ void __launch_bounds__(256, 1) bwd_query128_kernel(
   const size_t row0 = bh * T + (size_t)c * kC;
   const int nv = min(kC, T - c * kC);
   constexpr int lc = 6;
-  if (tid == 0) chunk_cumsum(cs, log_alpha, row0, nv);
+  chunk_scan(cs, log_alpha, row0, nv, kC);
   load_tile(qs, q + row0 * kD, nv, tid);
   load_tile(gs, dout + row0 * kD, nv, tid);
   __syncthreads();
@@ -785,7 +779,7 @@ template <typename IO>
 __global__ void __launch_bounds__(256, 1) bwd_key128_kernel(
     const IO* __restrict__ k, const IO* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
-    const double* __restrict__ tot, const float* dk32, const float* dv32, IO* dk, IO* dv, float* __restrict__ dc,
+    const double* __restrict__ cum, const float* dk32, const float* dv32, IO* dk, IO* dv, float* __restrict__ dc,
     int T, int L) {
   extern __shared__ __align__(16) float sm[];
   __shared__ float coef[32];
@@ -803,20 +797,18 @@ __global__ void __launch_bounds__(256, 1) bwd_key128_kernel(
   const size_t row0 = bh * T + (size_t)c * kC;
   const int nv = min(kC, T - c * kC);
   if (tid == 0) {
-    chunk_cumsum(cs, log_alpha, row0, nv);
-    int n = 0, cc = c;
-    double dec = 0.0;  // log-decay from the end of c to the end of e
+    int n = 0;
     for (int h = 0; h < 31 && n < 32; ++h) {
       if ((c >> h) & 1) continue;
       const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
       if (e + 1 >= N) break;  // e grows with h: no later node has queries either
-      while (cc < e) dec += tot[bh * N + (++cc)];
       ent[n] = e;
-      coef[n] = expf((float)dec);
+      coef[n] = expf((float)(cum[bh * N + e] - cum[bh * N + c]));  // the decay from the end of c to the end of e
       ++n;
     }
     n_sh = n;
   }
+  chunk_scan(cs, log_alpha, row0, nv, kC);
   load_tile(ks, k + row0 * kD, nv, tid);
   load_tile(Es, v + row0 * kD, nv, tid);
   __syncthreads();
@@ -915,6 +907,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   float* R = reinterpret_cast<float*>(ws + p.off_R);
   double* tot = reinterpret_cast<double*>(ws + p.off_tot);
   double* G = reinterpret_cast<double*>(ws + p.off_G);
+  double* cum = reinterpret_cast<double*>(ws + p.off_cum);
   float* dc = reinterpret_cast<float*>(ws + p.off_dc);
   const bool f32 = s.io == LL_F32;
   float* dq32 = f32 ? static_cast<float*>(a.dq) : reinterpret_cast<float*>(ws + p.off_dq);
@@ -932,7 +925,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   if (bwd_tc_supported(s)) {
     const BwdTcBuffers b{reinterpret_cast<__nv_bfloat16*>(dq32), reinterpret_cast<__nv_bfloat16*>(dk32),
                          reinterpret_cast<__nv_bfloat16*>(dv32), S, F, R, reinterpret_cast<__nv_bfloat16*>(ws + p.off_Ft), tot, G,
-                         reinterpret_cast<double*>(ws + p.off_cum), dc, a.err};
+                         cum, dc, a.err};
     const ll_status st = bwd_tc_launch(a, b);
     if (st != LL_OK) return st;
     bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
@@ -945,7 +938,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
     fast::bwd_intra128_kernel<IO><<<grid, 256, fast::intra_smem(), a.stream>>>(
         q, k, v, dout, a.log_alpha, a.lam, dq32, dk32, dv32, a.dlam, S, tot, R, s.T, s.L);
     LL_CUDA_OK(cudaGetLastError());
-    const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream);
+    const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream, nullptr, cum);
     if (fs != LL_OK) return fs;
     LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_query128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)fast::query_smem()));
@@ -955,7 +948,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
     LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_key128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                     (int)fast::key_smem()));
     fast::bwd_key128_kernel<IO><<<grid, 256, fast::key_smem(), a.stream>>>(
-        k, v, a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32, static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc,
+        k, v, a.log_alpha, a.lam, a.dlam, R, cum, dk32, dv32, static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc,
         s.T, s.L);
     LL_CUDA_OK(cudaGetLastError());
     bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
@@ -971,7 +964,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
       Ce, p.lc);
   LL_CUDA_OK(cudaGetLastError());
 
-  const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream);
+  const ll_status fs = simt_fenwick_launch(S, F, tot, G, p.N, mat, BH, a.stream, nullptr, cum);
   if (fs != LL_OK) return fs;
 
   const size_t sm3 = query_smem(Ce, s.dk, s.dv);
@@ -984,7 +977,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   const size_t sm4 = key_smem(Ce, s.dk, s.dv);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_key_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)sm4));
   bwd_key_kernel<IO><<<grid, kThreads, sm4, a.stream>>>(
-      static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.lam, a.dlam, R, tot, dk32, dv32,
+      static_cast<const IO*>(a.k), static_cast<const IO*>(a.v), a.log_alpha, a.lam, a.dlam, R, cum, dk32, dv32,
       static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc, s.T, s.dk, s.dv, s.L, Ce);
   LL_CUDA_OK(cudaGetLastError());
 

@@ -91,6 +91,27 @@ SimtPlan plan_of(const ll_shape& s) {
   return p;
 }
 
+// cs[i] = the sum of log_alpha over rows 0..i of the chunk (rows >= nv add 0),
+// float64, for i < Ce <= 128; every thread of the CTA takes part (a scan over
+// each warp, then the warps' totals); cs is complete after the caller's next
+// __syncthreads
+__device__ __forceinline__ void chunk_scan(double* cs, const float* log_alpha, size_t row0, int nv, int Ce) {
+  __shared__ double wsum[4];
+  const int t = threadIdx.x, lane = t & 31, w = t >> 5;
+  double x = (t < Ce && t < nv) ? (double)log_alpha[row0 + t] : 0.0;
+#pragma unroll
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_up_sync(0xffffffffu, x, o);
+    if (lane >= o) x += y;
+  }
+  if (lane == 31 && w < 4) wsum[w] = x;
+  __syncthreads();
+  if (t < Ce) {
+    for (int ww = 0; ww < w; ++ww) x += wsum[ww];
+    cs[t] = x;
+  }
+}
+
 // (1) + (2): one CTA per (chunk, head).
 template <typename IO>
 __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restrict__ q, const IO* __restrict__ k,
@@ -116,14 +137,8 @@ __global__ void __launch_bounds__(kThreads) simt_chunk_kernel(const IO* __restri
   const size_t t0 = (size_t)c * Ce;
   const size_t row0 = bh * T + t0;
   const int nv = min(Ce, T - (int)t0);  // rows present in this chunk
-  if (tid == 0) {
-    double acc = 0.0;
-    for (int i = 0; i < Ce; ++i) {
-      if (i < nv) acc += (double)log_alpha[row0 + i];
-      cs[i] = acc;
-    }
-    tot[bh * N + c] = acc;
-  }
+  chunk_scan(cs, log_alpha, row0, nv, Ce);
+  if (tid == Ce - 1) tot[bh * N + c] = cs[Ce - 1];
   for (int x = tid; x < Ce * dk; x += kThreads) {
     int i = x / dk, f = x % dk;
     qs[i * dkp + f] = i < nv ? to_f(q[(row0 + i) * dk + f]) : 0.f;
@@ -365,13 +380,7 @@ __global__ void __launch_bounds__(kThreads) simt_inter_kernel(const IO* __restri
 
   const size_t row0 = bh * T + (size_t)c * Ce;
   const int nv = min(Ce, T - c * Ce);  // rows present in this chunk
-  if (tid == 0) {
-    double acc = 0.0;
-    for (int i = 0; i < Ce; ++i) {
-      if (i < nv) acc += (double)log_alpha[row0 + i];
-      cs[i] = acc;
-    }
-  }
+  chunk_scan(cs, log_alpha, row0, nv, Ce);
   for (int x = tid; x < Ce * dk; x += kThreads) qs[x] = x < nv * dk ? to_f(q[row0 * dk + x]) : 0.f;
   for (int x = tid; x < Ce * dv; x += kThreads) Oc[x] = x < nv * dv ? o_intra[row0 * dv + x] : 0.f;
   __syncthreads();
