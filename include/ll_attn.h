@@ -198,7 +198,9 @@ LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const flo
  * shape->Ls != 0). */
 LL_API size_t ll_attn_bwd_workspace_size(const ll_shape* shape);
 
-/* Number of kernel launches one ll_attn_bwd call makes (0 on an invalid shape). */
+/* Number of kernel launches one ll_attn_bwd call makes (0 on an invalid shape).
+ * The bf16 d = 128 path also clears its key-side level nodes in the workspace
+ * with one cudaMemsetAsync on `stream`, which this count leaves out. */
 LL_API int ll_attn_bwd_launches(const ll_shape* shape);
 
 /* Backward of ll_attn_fwd.  For f = sum(o . dout) with o = ll_attn_fwd(q, k,
