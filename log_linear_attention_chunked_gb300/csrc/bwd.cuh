@@ -10,8 +10,11 @@ namespace llattn {
 // With Ft (d_k = d_v = 128) the nodes are also written as 128-byte-swizzled
 // bf16 tiles, the operand layout of the tensor-core kernels; with cum, the
 // running sums over the chunks of their log-decay totals ([BH, N] float64).
+// With Ft, f32_nodes = false leaves F unwritten where the kernel allows it
+// (for the consumers of the bf16 tiles alone).
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream, __nv_bfloat16* Ft = nullptr, double* cum = nullptr);
+                              cudaStream_t stream, __nv_bfloat16* Ft = nullptr, double* cum = nullptr,
+                              bool f32_nodes = true);
 
 struct BwdArgs {
   ll_shape s;

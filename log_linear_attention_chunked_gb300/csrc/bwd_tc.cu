@@ -829,7 +829,8 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   bwd_tc_intra_kernel<<<grid, kIntraThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp,
                                                                   b.dvp, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
-  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum);
+  // the query kernel reads the nodes' bf16 tiles only: no float32 copy where the Fenwick kernel can skip it
+  const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum, false);
   if (fs != LL_OK) return fs;
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
   bwd_tc_query_kernel<<<grid, kQryThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,

@@ -284,7 +284,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
                                                                      const double* __restrict__ tot,
                                                                      double* __restrict__ G, int N, int mat,
                                                                      __nv_bfloat16* __restrict__ Ft,
-                                                                     double* __restrict__ cum) {
+                                                                     double* __restrict__ cum, int write_f) {
   extern __shared__ double Gs[];                                  // [N]
   float* coef = reinterpret_cast<float*>(Gs + N);                 // [N] child decays
   float* last = coef + N;                                         // [kFenLv][kThreads]
@@ -348,7 +348,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
     const int h = __ffs(~i) - 1, o = i - __popc(i);
     for (int m = 0; m < h; ++m) acc = fmaf(coef[o + m], last[m * kThreads + threadIdx.x], acc);
     last[h * kThreads + threadIdx.x] = acc;
-    Fb[(size_t)i * mat + idx] = acc;
+    if (write_f) Fb[(size_t)i * mat + idx] = acc;
     if (Ft) Ft[(bh * N + i) * (size_t)mat + tel] = __float2bfloat16_rn(acc);
   }
 }
@@ -553,12 +553,12 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 }  // namespace
 
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
-                              cudaStream_t stream, __nv_bfloat16* Ft, double* cum) {
+                              cudaStream_t stream, __nv_bfloat16* Ft, double* cum, bool f32_nodes) {
   if (N <= kFenFastN) {
     const size_t smf = (size_t)N * (sizeof(double) + sizeof(float)) + (size_t)kFenLv * kThreads * sizeof(float);
     LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
-    simt_fenwick_fast_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(S, F, tot, G, N,
-                                                                                                   mat, Ft, cum);
+    simt_fenwick_fast_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(
+        S, F, tot, G, N, mat, Ft, cum, f32_nodes || !Ft ? 1 : 0);
     LL_CUDA_OK(cudaGetLastError());
     return LL_OK;
   }
