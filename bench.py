@@ -12,6 +12,16 @@ levels, positions 65536 onward), `gdn_bf16_t4k` (one ll_gdn_fwd) and
 `mamba2_bwd_bf16_t16k` (one ll_attn_bwd over the default workload's shape,
 with an upstream gradient of o).
 
+A default run (the forward workload, no --workload) also times, in the same
+process and on the same GPU, the decode step (`decode_b64_t64k`, 256 steps)
+and the Gated DeltaNet forward (`gdn_bf16_t4k`), each with its own warm-up,
+clock record, roofline and end-to-end figure, under the line's `secondary`
+key (`--no-secondary` skips them).
+
+Roofline of a step: the slower of its algorithmic flops at the measured bf16
+tensor peak and its algorithmic bytes at the measured HBM copy bandwidth; the
+line reports the achieved rate of that resource and its fraction.
+
 Inputs are resident in HBM when a timed step starts.  The forward workloads
 flush L2 between steps (a write of 2x the L2 size, outside the timed
 events); the decode workload streams 2.3 GB of states, far larger than L2.
@@ -651,6 +661,28 @@ def decode_workload(cfg, dev, rank, binding, synth, torch):
                 d2h=d2h, launches=1, flush=False, step_bytes=lambda i: nbytes(Bn, H, d, Ls, cfg["T"] + (i % S)))
 
 
+DEFAULT_WORKLOAD = "mamba2_bf16_t16k"
+# timed after the primary in a default run: (workload, steps)
+SECONDARY = (("decode_b64_t64k", 256), ("gdn_bf16_t4k", 50))
+
+
+def workload_config(cfg, name, world):
+    """The `config` object of a JSON line: the workload and its sizes."""
+    kind = cfg["kind"]
+    config = {"workload": name, "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "dk": cfg["dk"],
+              "dv": cfg["dv"], "chunk": cfg["chunk"], "L": cfg["L"], "io": cfg["io"],
+              "parallelism": f"replicas x{world} (b,h) weak"}
+    if kind in ("decode", "gdn_decode"):
+        config.update(Ls=cfg["Ls"], positions=f"{cfg['T']}..{cfg['T'] + cfg['steps'] - 1} cycled",
+                      l2="states (2.3 GB) larger than L2, no flush")
+    elif kind == "mamba2_cont":
+        config.update(t0=cfg["t0"], Ls=cfg["Ls"], l2="flushed between steps (write of 2x L2)",
+                      prefix="decode states of position t0 (random values on its set bits), states of t0+T exported")
+    else:
+        config["l2"] = "flushed between steps (write of 2x L2)"
+    return config
+
+
 # ----------------------------------------------------------------------------
 def main():
     ap = argparse.ArgumentParser()
@@ -658,8 +690,10 @@ def main():
     ap.add_argument("--steps", type=int, default=400)
     ap.add_argument("--warmup", type=int, default=10)
     ap.add_argument("--impl", choices=["ours", "reference"], default="ours")
-    ap.add_argument("--workload", default="mamba2_bf16_t16k")
+    ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
+    ap.add_argument("--no-secondary", action="store_true",
+                    help="default workload only: skip the decode and Gated DeltaNet blocks")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
@@ -672,17 +706,7 @@ def main():
     cfg = dict(synth.WORKLOADS[args.workload])
     kind = cfg["kind"]
     metric = METRICS[kind]
-    config = {"workload": args.workload, "B": cfg["B"], "H": cfg["H"], "T": cfg["T"], "dk": cfg["dk"],
-              "dv": cfg["dv"], "chunk": cfg["chunk"], "L": cfg["L"], "io": cfg["io"],
-              "parallelism": f"replicas x{world} (b,h) weak"}
-    if kind in ("decode", "gdn_decode"):
-        config.update(Ls=cfg["Ls"], positions=f"{cfg['T']}..{cfg['T'] + cfg['steps'] - 1} cycled",
-                      l2="states (2.3 GB) larger than L2, no flush")
-    elif kind == "mamba2_cont":
-        config.update(t0=cfg["t0"], Ls=cfg["Ls"], l2="flushed between steps (write of 2x L2)",
-                      prefix="decode states of position t0 (random values on its set bits), states of t0+T exported")
-    else:
-        config["l2"] = "flushed between steps (write of 2x L2)"
+    config = workload_config(cfg, args.workload, world)
 
     cores = len(os.sched_getaffinity(0)) if hasattr(os, "sched_getaffinity") else (os.cpu_count() or 1)
 
@@ -725,6 +749,88 @@ def main():
     torch.cuda.set_device(dev)
     binding.lib()
 
+    r = measure(cfg, args.workload, args.steps, args.warmup, dev, rank, world, binding, synth, torch)
+
+    # the other hot-path steps, timed in the same run on the same GPU (their
+    # own inputs, warm-up and clock record); weak scaling like the primary
+    secondary = {}
+    if args.workload == DEFAULT_WORKLOAD and not args.no_secondary:
+        for name, steps in SECONDARY:
+            c2 = dict(synth.WORKLOADS[name])
+            r2 = measure(c2, name, steps, args.warmup, dev, rank, world, binding, synth, torch)
+            secondary[name] = {"metric": METRICS[c2["kind"]], "value": r2["value"], "unit": "tokens/s",
+                               "steps": steps, "warmup": args.warmup, "ms_per_step": r2["mean_ms"],
+                               "step_ms_median": statistics.median(r2["step_ms"]), "roofline": r2["roofline"],
+                               "e2e": r2["e2e"], "clocks": r2["clocks"], "gpu_launches": r2["launches"] * steps,
+                               "config": workload_config(c2, name, world)}
+
+    cpu = None
+    if pool is not None:
+        size = calibrate(pool, cfg, cores, budget_s=12.0)
+        tps, n, secs = oracle_sample(pool, cfg, cores, size)
+        pool.close()
+        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
+               "sample": sample_desc(cfg, size) + f" ({secs:.1f} s wall, {cores} single-threaded processes)"}
+
+    if rank == 0:
+        line = {"metric": metric, "value": r["value"], "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
+                "warmup": args.warmup, "ms_per_step": r["mean_ms"], "higher_is_better": True, "scaling": "weak",
+                "vs_baseline": None, "dtype": cfg["io"], "data": "synthetic", "config": config,
+                "roofline": r["roofline"], "cpu_baseline": cpu, "e2e": r["e2e"], "clocks": r["clocks"],
+                "gpu_launches": r["launches"] * args.steps, "wall_s_timed_region": r["wall"],
+                "step_ms_min": min(r["step_ms"]), "step_ms_median": statistics.median(r["step_ms"])}
+        if secondary:
+            line["secondary"] = secondary
+        print(json.dumps(line))
+    if world > 1:
+        torch.distributed.destroy_process_group()
+
+
+def roofline_of(cfg, workload, w, mean_ms, dev, torch):
+    """Roofline of one step: the slower of its algorithmic flops at the bf16
+    tensor peak and its algorithmic bytes at the HBM copy bandwidth; the
+    achieved rate of that resource over the measured step time."""
+    kind = cfg["kind"]
+    hbm, bf16, sm_mhz, src = measured_peaks()
+    traffic, kname = ncu_traffic(workload)
+    if kind in ("decode", "gdn_decode"):
+        abytes = sum(w["step_bytes"](i) for i in range(w["timed_steps"])) / w["timed_steps"]
+        achieved = abytes / (mean_ms * 1e-3) / 1e9
+        return {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
+                "traffic": traffic, "peak_source": f"{src} (HBM copy)", "algorithmic_bytes_per_launch": abytes,
+                "launches_per_step": w["launches"], "kernel": kname}
+    abytes, aflops = w["abytes"], w["aflops"]
+    if kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg):
+        sms = torch.cuda.get_device_properties(dev).multi_processor_count
+        alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
+        achieved = aflops / (mean_ms * 1e-3) / 1e12
+        return {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
+                "frac": achieved / alu_peak, "traffic": traffic,
+                "peak_source": f"float32 FMA: {sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz ({src} clock)",
+                "algorithmic_flops_per_step": aflops, "launches_per_step": w["launches"], "kernel": kname}
+    t_hbm = abytes / (hbm * 1e9)
+    t_tensor = aflops / (bf16 * 1e12)
+    gbs = abytes / (mean_ms * 1e-3) / 1e9
+    tfs = aflops / (mean_ms * 1e-3) / 1e12
+    other_hbm = {"achieved_gbs": gbs, "peak": hbm, "frac": gbs / hbm, "algorithmic_bytes": abytes}
+    other_tensor = {"achieved_tflops": tfs, "peak_tflops": bf16, "frac": tfs / bf16, "algorithmic_flops": aflops}
+    if t_tensor > t_hbm:
+        return {"bound": "tensor", "achieved": tfs, "peak": bf16, "unit": "TFLOP/s", "frac": tfs / bf16,
+                "traffic": traffic, "peak_source": f"{src} (cuBLAS bf16 burst)", "algorithmic_flops_per_step": aflops,
+                "launches_per_step": w["launches"], "kernel": kname, "hbm": other_hbm,
+                "roof_us": {"tensor": t_tensor * 1e6, "hbm": t_hbm * 1e6}}
+    return {"bound": "hbm", "achieved": gbs, "peak": hbm, "unit": "GB/s", "frac": gbs / hbm, "traffic": traffic,
+            "peak_source": f"{src} (HBM copy)", "algorithmic_bytes_per_launch": abytes,
+            "launches_per_step": w["launches"], "kernel": kname, "tensor": other_tensor,
+            "roof_us": {"tensor": t_tensor * 1e6, "hbm": t_hbm * 1e6}}
+
+
+def measure(cfg, workload, steps, warmup, dev, rank, world, binding, synth, torch):
+    """Warm up, then time `steps` steps of one workload (CUDA events on the
+    launching stream, clocks sampled meanwhile, barrier + synchronise on both
+    sides), then the same number of end-to-end steps through the public call
+    with host buffers.  Returns the figures of the JSON line."""
+    kind = cfg["kind"]
     if kind in ("decode", "gdn_decode"):
         w = decode_workload(cfg, dev, rank, binding, synth, torch)
     elif kind == "mamba2_bwd":
@@ -739,23 +845,23 @@ def main():
         if world > 1:
             torch.distributed.barrier()
 
-    for i in range(args.warmup):
+    for i in range(warmup):
         if flush is not None:
             flush.fill_(1.0)
         w["step"](i)
     torch.cuda.synchronize()
     if binding.ll_last_device_error() != 0:
-        raise RuntimeError("device error during warm-up")
+        raise RuntimeError(f"{workload}: device error during warm-up")
     if "reset" in w:
         w["reset"]()
 
-    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(args.steps)]
+    ev = [(torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)) for _ in range(steps)]
     sampler = ClockSampler(dev.index)
     time.sleep(0.1)
     barrier()
     torch.cuda.synchronize()
     wall0 = time.perf_counter()
-    for i in range(args.steps):
+    for i in range(steps):
         if flush is not None:
             flush.fill_(float(i))
         ev[i][0].record(stream)
@@ -766,7 +872,7 @@ def main():
     barrier()
     clocks = sampler.stop()
     if binding.ll_last_device_error() != 0:
-        raise RuntimeError("device error during the timed region")
+        raise RuntimeError(f"{workload}: device error during the timed region")
     step_ms = [a.elapsed_time(b) for a, b in ev]
     mean_ms = max_over_ranks(sum(step_ms) / len(step_ms), world, dev)
     value = whole_job_rate(w["units"], world, mean_ms)
@@ -774,7 +880,7 @@ def main():
     # end to end through the public call: host inputs in, host output out
     if "reset" in w:
         w["reset"]()
-    e2e_steps = max(3, args.steps)  # the same number of steps (decode: the same positions) as the timed loop
+    e2e_steps = max(3, steps)  # the same number of steps (decode: the same positions) as the timed loop
     e0, e1 = torch.cuda.Event(enable_timing=True), torch.cuda.Event(enable_timing=True)
     for i in range(e2e_steps + 2):
         if i == 2:
@@ -791,53 +897,14 @@ def main():
     e2e_ms = max_over_ranks(e0.elapsed_time(e1) / e2e_steps, world, dev)
     e2e = {"value": whole_job_rate(w["units"], world, e2e_ms), "unit": "tokens/s", "h2d_bytes_per_step": w["h2d"],
            "d2h_bytes_per_step": w["d2h"], "ms_per_step": e2e_ms}
-
-    # roofline of the dominant kernel
-    hbm, bf16, sm_mhz, src = measured_peaks()
-    traffic, kname = ncu_traffic(args.workload)
-    if kind in ("decode", "gdn_decode"):
-        abytes = sum(w["step_bytes"](i) for i in range(args.steps)) / args.steps
-        achieved = abytes / (mean_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": traffic, "peak_source": f"{src} (HBM copy)",
-                    "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname}
-    elif kind in ("gdn", "gdn_b") or (kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg)):
-        sms = torch.cuda.get_device_properties(dev).multi_processor_count
-        alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
-        aflops = w["aflops"]
-        achieved = aflops / (mean_ms * 1e-3) / 1e12
-        roofline = {"bound": "alu", "achieved": achieved, "peak": alu_peak, "unit": "TFLOP/s",
-                    "frac": achieved / alu_peak, "traffic": traffic,
-                    "peak_source": f"float32 FMA: {sms} SMs x 128 lanes x 2 x {sm_mhz:.0f} MHz ({src} clock)",
-                    "algorithmic_flops_per_step": aflops, "launches_per_step": w["launches"], "kernel": kname,
-                    "hbm": {"achieved_gbs": w["abytes"] / (mean_ms * 1e-3) / 1e9, "peak": hbm}}
-    else:
-        abytes, aflops = w["abytes"], w["aflops"]
-        achieved = abytes / (mean_ms * 1e-3) / 1e9
-        roofline = {"bound": "hbm", "achieved": achieved, "peak": hbm, "unit": "GB/s", "frac": achieved / hbm,
-                    "traffic": traffic, "peak_source": f"{src} (HBM copy)",
-                    "algorithmic_bytes_per_launch": abytes, "launches_per_step": w["launches"], "kernel": kname,
-                    "tensor": {"achieved_tflops": aflops / (mean_ms * 1e-3) / 1e12, "peak_tflops": bf16,
-                               "frac": aflops / (mean_ms * 1e-3) / 1e12 / bf16, "algorithmic_flops": aflops}}
-
-    cpu = None
-    if pool is not None:
-        size = calibrate(pool, cfg, cores, budget_s=12.0)
-        tps, n, secs = oracle_sample(pool, cfg, cores, size)
-        pool.close()
-        cpu = {"value": tps, "unit": "tokens/s", "cores": cores, "kind": "oracle",
-               "sample": sample_desc(cfg, size) + f" ({secs:.1f} s wall, {cores} single-threaded processes)"}
-
-    if rank == 0:
-        line = {"metric": metric, "value": value, "unit": "tokens/s", "n_gpus": world, "steps": args.steps,
-                "warmup": args.warmup, "ms_per_step": mean_ms, "higher_is_better": True, "scaling": "weak",
-                "vs_baseline": None, "dtype": cfg["io"], "data": "synthetic", "config": config,
-                "roofline": roofline, "cpu_baseline": cpu, "e2e": e2e, "clocks": clocks,
-                "gpu_launches": w["launches"] * args.steps, "wall_s_timed_region": wall,
-                "step_ms_min": min(step_ms), "step_ms_median": statistics.median(step_ms)}
-        print(json.dumps(line))
-    if world > 1:
-        torch.distributed.destroy_process_group()
+    w["timed_steps"] = steps
+    roofline = roofline_of(cfg, workload, w, mean_ms, dev, torch)
+    out = dict(value=value, mean_ms=mean_ms, step_ms=step_ms, wall=wall, clocks=clocks, e2e=e2e, roofline=roofline,
+               launches=w["launches"])
+    del w, flush
+    torch.cuda.synchronize()
+    torch.cuda.empty_cache()
+    return out
 
 
 if __name__ == "__main__":

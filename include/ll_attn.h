@@ -257,7 +257,11 @@ LL_API ll_status ll_attn_bwd(const ll_shape* shape, const void* q, const void* k
  *   call's contents (the forward needs none of it cleared): calls whose
  *   execution overlaps on the GPU (other streams, other host threads) race.
  *   The first call on each device (with that device current) looks up the
- *   array's device address; make that first call before any stream capture. */
+ *   array's device address; make that first call before any stream capture.
+ *   The address is kept for the life of the process: after cudaDeviceReset
+ *   (or anything else that destroys and re-creates the device's primary
+ *   context) the array may move, so this entry point must not be used on
+ *   that device again. */
 LL_API ll_status ll_attn_fwd_noalloc(const ll_shape* shape, const void* q, const void* k, const void* v,
                                      const float* log_alpha, const float* lam, void* o, float* state_out,
                                      float* scale_out, void* stream);

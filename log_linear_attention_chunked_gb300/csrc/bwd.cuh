@@ -11,7 +11,10 @@ namespace llattn {
 // bf16 tiles, the operand layout of the tensor-core kernels; with cum, the
 // running sums over the chunks of their log-decay totals ([BH, N] float64).
 // With Ft, f32_nodes = false leaves F unwritten where the kernel allows it
-// (for the consumers of the bf16 tiles alone).
+// (for the consumers of the bf16 tiles alone): that is every N up to
+// kFenwickOnChipChunks, whose chain stays on chip; beyond it the kernel reads
+// the children back from F, so F must be there.
+constexpr int kFenwickOnChipChunks = 4096;
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
                               cudaStream_t stream, __nv_bfloat16* Ft = nullptr, double* cum = nullptr,
                               bool f32_nodes = true);

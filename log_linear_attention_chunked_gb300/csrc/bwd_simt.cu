@@ -84,7 +84,10 @@ BwdPlan plan_of(const ll_shape& s) {
   const size_t mat = (size_t)s.dv * s.dk;
   size_t off = 0;
   p.off_S = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
-  p.off_F = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  // float32 nodes: the tensor-core path reads only their bf16 tiles, and the
+  // Fenwick kernel writes F there only when its chain cannot stay on chip
+  const bool need_f32_nodes = !bwd_tc_supported(s) || p.N > kFenwickOnChipChunks;
+  p.off_F = off;   off = align_up(off + (need_f32_nodes ? BH * p.N * mat * sizeof(float) : 0), 256);
   p.off_R = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
   p.off_tot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_G = off;   off = align_up(off + BH * p.N * sizeof(double), 256);

@@ -276,7 +276,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
 // of every level (the children of the next nodes) in shared memory, so a
 // step of the chain reads no node back from global memory and does no
 // float64 arithmetic.
-constexpr int kFenFastN = 4096;
+constexpr int kFenFastN = kFenwickOnChipChunks;
 constexpr int kFenLv = 13;  // levels of N <= 4096
 
 __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float* __restrict__ S,

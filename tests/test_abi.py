@@ -222,3 +222,11 @@ def test_product_path_does_not_reach_the_oracle():
             elif isinstance(node, ast.ImportFrom):
                 names = [node.module or ""]
             assert not any(n == "oracle" or n.startswith("oracle.") for n in names), (f, names)
+
+
+def test_noalloc_scratch_size_matches_header():
+    """The binding's copy of the no-allocation scratch size is the header's."""
+    from log_linear_attention_chunked_gb300 import binding
+    m = re.search(r"#define\s+LL_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", open(HEADER).read())
+    assert m, "LL_NOALLOC_SCRATCH_BYTES not found in the header"
+    assert int(m.group(1)) << int(m.group(2)) == binding.NOALLOC_SCRATCH_BYTES

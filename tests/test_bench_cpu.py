@@ -82,3 +82,20 @@ def test_every_workload_has_a_metric_and_a_sample_description(name):
     cfg = synth.WORKLOADS[name]
     assert bench.METRICS[cfg["kind"]]
     assert bench.sample_desc(cfg, 3)
+
+
+def test_roofline_is_the_slower_of_tensor_and_hbm():
+    """The bound of a step is the slower of its flops at the bf16 tensor peak
+    and its bytes at the HBM bandwidth: HBM for the 16K-token Mamba-2 forward,
+    the tensor cores for the Gated DeltaNet forward."""
+    hbm, bf16, _, _ = bench.measured_peaks()
+    for name, bound in (("mamba2_bf16_t16k", "hbm"), ("gdn_bf16_t4k", "tensor"), ("mamba2_bwd_bf16_t16k", "hbm")):
+        cfg = synth.WORKLOADS[name]
+        w = {"abytes": bench.algorithmic_bytes(cfg), "aflops": bench.algorithmic_flops(cfg), "launches": 1}
+        r = bench.roofline_of(cfg, name, w, 1.0, None, None)
+        assert r["bound"] == bound, name
+        if bound == "tensor":
+            assert r["peak"] == bf16 and abs(r["achieved"] - w["aflops"] / 1e-3 / 1e12) < 1e-6
+        else:
+            assert r["peak"] == hbm and abs(r["achieved"] - w["abytes"] / 1e-3 / 1e9) < 1e-6
+        assert abs(r["frac"] - r["achieved"] / r["peak"]) < 1e-12

@@ -148,3 +148,32 @@ def test_full_size_workload_sampled_rows(B):
     out = _run(B, inp)
     assert np.isfinite(out).all()
     assert _check_sampled(out, inp, _sampled_rows(cfg["T"], per_tile=(0, 127))) <= TOL_BF16
+
+
+def test_full_size_workload_slow_decay_sampled_rows(B):
+    """The benchmark's launch (B=1, H=16, T=16384: 2048 tiles, tile bits 0..6 =
+    levels 8..14) with slow decay, so that keys 8K tokens back still count and
+    every tile level is checked against non-vanishing values."""
+    cfg = dict(synth.WORKLOADS["mamba2_bf16_t16k"])
+    inp = synth.make_inputs(cfg, la_mode="slow", tag="tcslow16k")
+    out = _run(B, inp)
+    assert np.isfinite(out).all()
+    assert _check_sampled(out, inp, _sampled_rows(cfg["T"], per_tile=(0, 127))) <= TOL_BF16
+
+
+@pytest.mark.parametrize("lvl", [11, 12, 13, 14])
+def test_onehot_high_tile_levels(B, lvl):
+    """One-hot lambda at the tile levels of tile bits 3..6 (levels 11..14) at
+    T = 16384 with slow decay: only the bucket of that level reaches the
+    output, which is non-zero exactly for queries whose bit lvl-1 is set."""
+    T = 16384
+    inp = synth.make_inputs(_cfg(T, H=2), la_mode="slow", lam_mode="onehot", lam_level=lvl, tag=f"tcoh{lvl}")
+    out = _run(B, inp)
+    rows = _sampled_rows(T, per_tile=(0, 127))
+    err = _check_sampled(out, inp, rows)
+    assert err <= TOL_BF16, (lvl, err)
+    # the level is empty for rows with bit lvl-1 clear: their outputs are exactly zero
+    empty = [t for t in rows if not (t >> (lvl - 1)) & 1]
+    full = [t for t in rows if (t >> (lvl - 1)) & 1]
+    assert np.abs(out[:, :, empty]).max() == 0.0
+    assert np.abs(out[:, :, full]).max() > 1e-2

@@ -108,3 +108,30 @@ def test_key_and_value_dims_differ(B, T, dk, dv, io):
     inp = synth.make_inputs(_cfg(T, d=dk, dv=dv, io=io), tag=f"gdv{T}{dk}{dv}")
     tol = TOL_GDN_F32 if io == "f32" else TOL_BF16
     assert rel_err(_run(B, inp, 64), _oracle(inp)) <= tol
+
+
+@pytest.mark.parametrize("io", ["f32", "bf16"])
+@pytest.mark.parametrize("la_mode,lam_mode,lvl", [("zero", "softplus", 0), ("slow", "softplus", 0),
+                                                  ("slow", "onehot", 9), ("zero", "onehot", 11)])
+def test_d128_scan_levels_without_underflow(B, io, la_mode, lam_mode, lvl):
+    """The d = 128, 64-token-chunk scan (the workload's kernels) where the
+    level states above height 0 carry weight: alpha = 1 or slow decay, so keys
+    2048 tokens back still count.  32 chunks give heights 0..4 (levels 7..11);
+    the one-hot cases isolate one level (9 = height 2, 11 = height 4) so a
+    dropped or misplaced height cannot hide behind the others."""
+    T = 2048
+    inp = synth.make_inputs(_cfg(T, io=io), la_mode=la_mode, lam_mode=lam_mode, lam_level=lvl,
+                            tag=f"g128{la_mode}{lam_mode}")
+    ref = _oracle(inp)
+    if lam_mode == "onehot":
+        # rows whose level-lvl bucket is non-empty carry the whole output
+        assert np.abs(ref[:, :, (1 << (lvl - 1)):]).max() > 1e-3
+    tol = TOL_GDN_F32 if io == "f32" else TOL_BF16
+    assert rel_err(_run(B, inp, 64), ref) <= tol
+
+
+def test_d128_scan_all_heights_slow_decay_t4096(B):
+    """The workload's shape per head (T = 4096, heights 0..5) with slow decay,
+    bf16 io: every height of the level scan contributes."""
+    inp = synth.make_inputs(_cfg(4096, Bn=1, H=2, io="bf16"), la_mode="slow", tag="g128slow4k")
+    assert rel_err(_run(B, inp, 64), _oracle(inp)) <= TOL_BF16
