@@ -26,7 +26,9 @@ STATUS = {0: "LL_OK", 1: "LL_ERR_INVALID_ARG", 2: "LL_ERR_UNSUPPORTED", 3: "LL_E
 SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_workspace_size", "ll_attn_fwd_launches",
            "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
            "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b", "ll_attn_fwd_cont_workspace_size",
-           "ll_attn_fwd_cont", "ll_attn_bwd_workspace_size", "ll_attn_bwd_launches", "ll_attn_bwd")
+           "ll_attn_fwd_cont", "ll_attn_bwd_workspace_size", "ll_attn_bwd_launches", "ll_attn_bwd",
+           # test hooks (include/ll_attn_test.h)
+           "ll_test_fwd_withhold_node")
 
 
 class LLError(RuntimeError):
@@ -90,6 +92,9 @@ def lib() -> ctypes.CDLL:
     L.ll_attn_bwd_launches.argtypes = [shp]
     L.ll_attn_bwd.restype = i32
     L.ll_attn_bwd.argtypes = [shp, vp, vp, vp, fp, fp, vp, vp, vp, vp, fp, fp, vp, sz, vp]
+    L.ll_test_fwd_withhold_node.restype = i32
+    L.ll_test_fwd_withhold_node.argtypes = [shp, vp, vp, vp, fp, fp, vp, vp, sz, ctypes.c_longlong,
+                                            ctypes.c_ulonglong, vp]
     _lib = L
     return L
 
@@ -350,6 +355,23 @@ def ll_gdn_fwd_b(q, k, v, log_alpha, beta, lam, chunk: int, *, o=None, workspace
     delta-rule pseudo-values).  Arguments as ll_gdn_fwd."""
     return _gdn_forward("ll_gdn_fwd_b", ll_gdn_fwd_b_workspace_size, q, k, v, log_alpha, beta, lam, chunk, o,
                         workspace)
+
+def ll_test_fwd_withhold_node(q, k, v, log_alpha, lam, chunk: int, node: int, timeout_ns: int, *, o=None,
+                              workspace=None) -> int:
+    """Test hook: the tensor-core forward with Fenwick node `node` never
+    published and every bounded wait limited to `timeout_ns`.  Returns the
+    launch status (the expiry itself is reported by ll_last_device_error)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    shape = make_shape(B, H, T, dk, dv, lam.shape[-1], chunk, 0, _io(q.dtype))
+    if o is None:
+        o = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    if workspace is None:
+        workspace = alloc_workspace(ll_attn_fwd_workspace_size(shape), q.device)
+    return lib().ll_test_fwd_withhold_node(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
+                                           _ptr(lam), _ptr(o), _ptr(workspace), workspace.numel(), int(node),
+                                           int(timeout_ns), _stream(q.device))
+
 
 def ll_last_device_error(device=None) -> int:
     """Synchronise the current stream and return (and clear) the device error status."""

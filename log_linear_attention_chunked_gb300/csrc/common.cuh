@@ -71,6 +71,11 @@ struct FwdArgs {
   long long t0 = 0;
   const float* state_in = nullptr;
   const float* scale_in = nullptr;
+  // limit of every bounded device-side wait of the tensor-core forward
+  // (0 = the library default); and the test hook of its expiry: the index of
+  // one Fenwick node whose publication word is never written (-1 = none)
+  uint64_t timeout_ns = 0;
+  long long withhold_node = -1;
 };
 
 size_t fwd_simt_workspace(const ll_shape& s);

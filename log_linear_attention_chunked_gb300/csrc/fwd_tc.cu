@@ -78,7 +78,7 @@ constexpr int kEpi = 256;
 constexpr uint32_t kHalf = kTile * 64 * 2;  // one [128 x 64] bf16 swizzled block: 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalf;  // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
-constexpr uint64_t kTimeoutNs = 4000000000ull;
+constexpr uint64_t kTimeoutNs = 4000000000ull;  // default limit of a bounded wait
 
 // TMEM columns: two 128-column regions that hold the chunk state and then the
 // output (PV, then + the inter-tile levels) of alternating tiles; the scores
@@ -139,6 +139,8 @@ struct TcParams {
   // its levels read the prefix nodes at F[BH * Nt + bh * kPreSlots + h]
   int c0t;
   unsigned* err;
+  uint64_t timeout_ns;  // limit of every bounded wait
+  long long withhold;   // node whose publication is withheld (expiry test), or -1
 };
 
 struct Ctx {
@@ -164,7 +166,7 @@ __device__ __forceinline__ void wait_bar(const Ctx& c, int b, uint32_t par) {
   const uint64_t t0 = globaltimer_ns();
   while (!mbar_try_wait(bar, par)) {
     if (*c.abort_s) return;
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
+    if (globaltimer_ns() - t0 > c.p->timeout_ns) {
       note_abort(c);
       return;
     }
@@ -182,7 +184,7 @@ __device__ __forceinline__ void wait_bar_w(const Ctx& c, int b, uint32_t par) {
     ok = ok || mbar_try_wait(bar, par);
     if (__all_sync(0xffffffffu, ok)) return;
     if (__any_sync(0xffffffffu, *c.abort_s != 0)) return;
-    const bool late = globaltimer_ns() - t0 > kTimeoutNs;
+    const bool late = globaltimer_ns() - t0 > c.p->timeout_ns;
     if (__any_sync(0xffffffffu, late)) {
       if ((threadIdx.x & 31) == 0) note_abort(c);
       __syncwarp();
@@ -221,7 +223,7 @@ __device__ __forceinline__ uint64_t wait_flag(const Ctx& c, const uint64_t* flag
       *c.abort_s = 1;
       return w;
     }
-    if (globaltimer_ns() - t0 > kTimeoutNs) {
+    if (globaltimer_ns() - t0 > c.p->timeout_ns) {
       note_abort(c);
       return w;
     }
@@ -752,7 +754,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_cta_u32(nlr) < want) {
           if (*c.abort_s) return;
-          if (globaltimer_ns() - t0 > kTimeoutNs) {
+          if (globaltimer_ns() - t0 > c.p->timeout_ns) {
             note_abort(c);
             return;
           }
@@ -907,6 +909,7 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMa
   auto publish = [&](uint64_t* flags, size_t node, float g) {
     bulk_wait0();
     fence_proxy_async_global();
+    if (flags == p.flags && (long long)node == p.withhold) return;  // expiry test: nothing will publish it
     st_release_u64(flags + node, ((uint64_t)p.token << 32) | __float_as_uint(g));
   };
 
@@ -1147,6 +1150,8 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.L = s.L;
   p.err = a.err;
   p.c0t = a.state_in ? (int)(a.t0 / kTile) : 0;
+  p.timeout_ns = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
+  p.withhold = a.withhold_node;
   if (a.state_in) {
     tc_prefix_nodes_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(a.state_in, a.scale_in, p.F, BH, plan.Nt,
                                                                          s.Ls, a.t0);

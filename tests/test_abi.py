@@ -21,7 +21,8 @@ def L():
 
 
 def declared_symbols():
-    src = open(HEADER).read()
+    inc = os.path.dirname(HEADER)
+    src = "".join(open(os.path.join(inc, f)).read() for f in sorted(os.listdir(inc)) if f.endswith(".h"))
     return sorted(set(re.findall(r"LL_API\s+[\w\s\*]+?\b(ll_\w+)\s*\(", src)))
 
 
@@ -230,3 +231,16 @@ def test_noalloc_scratch_size_matches_header():
     m = re.search(r"#define\s+LL_NOALLOC_SCRATCH_BYTES\s+\((\d+)u\s*<<\s*(\d+)\)", open(HEADER).read())
     assert m, "LL_NOALLOC_SCRATCH_BYTES not found in the header"
     assert int(m.group(1)) << int(m.group(2)) == binding.NOALLOC_SCRATCH_BYTES
+
+
+def test_withhold_hook_rejects_bad_args_on_host(L):
+    from log_linear_attention_chunked_gb300 import binding
+    vp = ctypes.c_void_p
+    s = binding.make_shape(1, 1, 256, 128, 128, 9, 64, 0, binding.LL_BF16)
+    p = [vp(FAKE)] * 6
+    # node out of range, limit out of range: refused before any launch
+    assert L.ll_test_fwd_withhold_node(ctypes.byref(s), *p, vp(FAKE), 1 << 20, 2, 10 ** 6, None) == 1
+    assert L.ll_test_fwd_withhold_node(ctypes.byref(s), *p, vp(FAKE), 1 << 20, 0, 10, None) == 1
+    # a shape off the tensor-core path
+    s2 = binding.make_shape(1, 1, 256, 64, 64, 9, 64, 0, binding.LL_BF16)
+    assert L.ll_test_fwd_withhold_node(ctypes.byref(s2), *p, vp(FAKE), 1 << 20, 0, 10 ** 6, None) == 2
