@@ -101,6 +101,11 @@ ll_status decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const
 ll_status gdn_decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t, const void* q,
                             const void* k, const void* v, const float* log_alpha, const float* beta,
                             const float* lam, float* states, void* o, cudaStream_t stream, unsigned* err);
+// Gated DeltaNet forward (reading A) on the tensor cores: bf16 io, d = 128,
+// T a multiple of 128 (at most 256 chunks of 128 tokens)
+bool gdn_tc_supported(const ll_shape& s);
+size_t gdn_tc_workspace(const ll_shape& s);
+ll_status gdn_tc_launch(const FwdArgs& a);
 size_t gdn_workspace(const ll_shape& s);
 ll_status gdn_launch(const FwdArgs& a);
 size_t gdn_b_workspace(const ll_shape& s);

@@ -1271,11 +1271,13 @@ ll_status launch_typed(const FwdArgs& a, const GdnPlan& p) {
 }  // namespace
 
 size_t gdn_workspace(const ll_shape& s) {
+  if (gdn_tc_supported(s)) return gdn_tc_workspace(s);
   const GdnPlan p = gdn_plan(s);
   return p.ok ? p.total : 0;
 }
 
 ll_status gdn_launch(const FwdArgs& a) {
+  if (gdn_tc_supported(a.s)) return gdn_tc_launch(a);  // bf16 io: the tensor cores
   const GdnPlan p = gdn_plan(a.s);
   if (!p.ok) return LL_ERR_UNSUPPORTED;
   if (a.ws_bytes < p.total) return LL_ERR_WORKSPACE;
