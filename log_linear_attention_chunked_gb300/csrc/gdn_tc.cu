@@ -16,12 +16,13 @@
 // The result does not depend on the chunk length (the float32 path uses 64).
 //
 // Kernel 1 (gdn_tc_prep_kernel), one CTA per (chunk, head), 256 threads:
-// K K^T and Q K^T, then U, W and Aqk Tinv, then Aqk W and the masked intra
-// product, each a 128x128x128 UMMA with bf16 operands in 128-byte-swizzled
-// shared tiles and float32 accumulators in TMEM.  The triangular inverse runs
-// on the CUDA cores in float32 (16x16 blocks: the diagonal blocks by forward
-// substitution, then the block diagonals below them, T_IJ = -T_II sum_M L_IM
-// T_MJ).  Writes W, Q', U^T (bf16) and the intra output (bf16) per chunk.
+// K K^T and Q K^T, then U^T (as V^T Tb^T, so it leaves TMEM row by row), W
+// and Aqk Tinv, then Aqk W and the masked intra product, each a 128x128x128
+// UMMA with bf16 operands in 128-byte-swizzled shared tiles and float32
+// accumulators in TMEM.  The triangular inverse runs on the CUDA cores in
+// float32 (16x16 blocks: the diagonal blocks by forward substitution, then the
+// block diagonals below them, T_IJ = -T_II sum_M L_IM T_MJ, one block per
+// warp).  Writes W, Q', U^T (bf16) and the intra output (bf16) per chunk.
 //
 // Kernel 2 (gdn_tc_scan_kernel), one CTA per (32 d_v rows, head), 128
 // threads, sequential over the chunks of its head.  Every level state is held
@@ -112,9 +113,10 @@ constexpr uint32_t kPK = 0;                    // K tile; U^T staging after the 
 constexpr uint32_t kPQ = kPK + kTileB;         // Q tile
 constexpr uint32_t kPV = kPQ + kTileB;         // V tile
 constexpr uint32_t kPA = kPV + kTileB;         // Aqk (bf16); Q' staging at the end
-constexpr uint32_t kPBlk = 36 * 256 * 4;       // 36 lower 16x16 blocks, float32
-constexpr uint32_t kPL = kPA + kTileB;         // L (packed float32); then Tb; then Cm; then intra staging
-constexpr uint32_t kPT = kPL + kPBlk;          // Tinv (packed float32); then Tbe; then W
+constexpr int kBS = 20;                        // row stride (floats) of a 16x16 block: conflict-free 16-byte reads
+constexpr uint32_t kPBlk = 36 * 16 * kBS * 4;  // 36 lower 16x16 blocks, float32
+constexpr uint32_t kPL = kPA + kTileB;         // L, then T_II L_IM (blocks); then Tb; then Cm; then intra staging
+constexpr uint32_t kPT = kPL + kPBlk;          // Tinv (blocks); then Tbe; then W
 constexpr uint32_t kPTab = kPT + kPBlk;        // g[128], e[128], beta[128], quadrant totals[4]
 constexpr uint32_t kPBars = kPTab + (3 * 128 + 4) * 4;
 constexpr uint32_t kPrepSmem = kPBars + 4 * 8;
@@ -122,7 +124,8 @@ constexpr int kPrepThreads = 256;
 static_assert(kPL % 1024 == 0 && kPT % 1024 == 0, "tile alignment");
 static_assert(kPrepSmem <= 232448, "shared memory budget of one CTA");
 
-__device__ __forceinline__ int blk(int I, int J) { return I * (I + 1) / 2 + J; }
+// float offset of lower block (I, J), J <= I, in the block storage
+__device__ __forceinline__ int blk(int I, int J) { return (I * (I + 1) / 2 + J) * 16 * kBS; }
 
 struct PrepParams {
   const float* log_alpha;
@@ -238,7 +241,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       for (int b = 0; b < 2; ++b) {
         const int J = (j0 >> 4) + b, I = i >> 4;
         if (J <= I) {
-          float4* dst = reinterpret_cast<float4*>(Lp + blk(I, J) * 256 + (i & 15) * 16);
+          float4* dst = reinterpret_cast<float4*>(Lp + blk(I, J) + (i & 15) * kBS);
 #pragma unroll
           for (int v = 0; v < 4; ++v)
             dst[v] = make_float4(kk[16 * b + 4 * v], kk[16 * b + 4 * v + 1], kk[16 * b + 4 * v + 2],
@@ -259,11 +262,16 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   fence_proxy_async_shared();
   __syncthreads();
 
-  // ---- Tinv = (I + L)^{-1}: diagonal 16x16 blocks by forward substitution
+  // ---- Tinv = (I + L)^{-1} in 16x16 blocks.  Row block I of (I + L) T = I
+  // gives T_IJ = -T_II sum_{M=J}^{I-1} L_IM T_MJ for J < I.  First the
+  // diagonal blocks by forward substitution (one column per thread), then
+  // Lam_IM = T_II L_IM over L's blocks, then the block diagonals below, one
+  // block per warp: T_IJ = -sum_{M=J}^{I-1} Lam_IM T_MJ.  In a block product
+  // lane (r = lane / 2, c0 = 8 (lane % 2)) owns row r, columns c0 .. c0 + 7.
   if (tid < 128) {
     const int I = tid >> 4, cc = tid & 15;
-    const float* Lb = Lp + blk(I, I) * 256;
-    float* Tb = Tp + blk(I, I) * 256;
+    const float* Lb = Lp + blk(I, I);
+    float* Tb = Tp + blk(I, I);
     float col[16];
 #pragma unroll
     for (int r = 0; r < 16; ++r) {
@@ -271,63 +279,73 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (r > cc) {
 #pragma unroll
         for (int m = 0; m < 16; ++m)
-          if (m >= cc && m < r) acc = fmaf(-Lb[r * 16 + m], col[m], acc);
+          if (m >= cc && m < r) acc = fmaf(-Lb[r * kBS + m], col[m], acc);
       }
       col[r] = acc;
-      Tb[r * 16 + cc] = acc;
+      Tb[r * kBS + cc] = acc;
     }
   }
   __syncthreads();
-  // block diagonals below: T_IJ = -T_II sum_{M=J}^{I-1} L_IM T_MJ
-  for (int d = 1; d < 8; ++d) {
-    const int nout = (8 - d) * 256;
-    for (int idx = tid; idx < nout; idx += kPrepThreads) {
-      const int J = idx >> 8, I = J + d, e = idx & 255, r = e >> 4, cc = e & 15;
-      float acc = 0.f;
-      for (int M = J; M < I; ++M) {
-        const float* Lr = Lp + blk(I, M) * 256 + r * 16;
-        const float* Tc = Tp + blk(M, J) * 256 + cc;
+  {
+    const int r = lane >> 1, c0 = 8 * (lane & 1);
+    // acc[x] += sum_k A[r][k] B[k][c0 + x] over one 16x16 block pair
+    auto block_fma = [&](float* acc, const float* A, const float* B) {
 #pragma unroll
-        for (int m = 0; m < 16; ++m) acc = fmaf(Lr[m], Tc[m * 16], acc);
+      for (int k4 = 0; k4 < 4; ++k4) {
+        const float4 a = *reinterpret_cast<const float4*>(A + r * kBS + 4 * k4);
+        const float av[4] = {a.x, a.y, a.z, a.w};
+#pragma unroll
+        for (int kk = 0; kk < 4; ++kk) {
+          const float4 b0 = *reinterpret_cast<const float4*>(B + (4 * k4 + kk) * kBS + c0);
+          const float4 b1 = *reinterpret_cast<const float4*>(B + (4 * k4 + kk) * kBS + c0 + 4);
+          acc[0] = fmaf(av[kk], b0.x, acc[0]); acc[1] = fmaf(av[kk], b0.y, acc[1]);
+          acc[2] = fmaf(av[kk], b0.z, acc[2]); acc[3] = fmaf(av[kk], b0.w, acc[3]);
+          acc[4] = fmaf(av[kk], b1.x, acc[4]); acc[5] = fmaf(av[kk], b1.y, acc[5]);
+          acc[6] = fmaf(av[kk], b1.z, acc[6]); acc[7] = fmaf(av[kk], b1.w, acc[7]);
+        }
       }
-      Tp[blk(I, J) * 256 + e] = acc;  // the partial sum P, in the block's own slot
+    };
+    auto store_row = [&](float* dst, const float* acc, float sgn) {
+      *reinterpret_cast<float4*>(dst + r * kBS + c0) = make_float4(sgn * acc[0], sgn * acc[1], sgn * acc[2], sgn * acc[3]);
+      *reinterpret_cast<float4*>(dst + r * kBS + c0 + 4) =
+          make_float4(sgn * acc[4], sgn * acc[5], sgn * acc[6], sgn * acc[7]);
+    };
+    // Lam_IM = T_II L_IM for the 28 blocks below the diagonal, in place of L_IM
+    for (int b = warp; b < 28; b += kPrepThreads / 32) {
+      int I = 1, M = b;
+      while (M >= I) { M -= I; ++I; }  // b enumerates (I, M), M < I, row by row
+      float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+      block_fma(acc, Tp + blk(I, I), Lp + blk(I, M));
+      __syncwarp();
+      store_row(Lp + blk(I, M), acc, 1.f);
     }
     __syncthreads();
-    float res[7];
-#pragma unroll
-    for (int k = 0; k < 7; ++k) {
-      const int idx = tid + k * kPrepThreads;
-      res[k] = 0.f;
-      if (idx < nout) {
-        const int J = idx >> 8, I = J + d, e = idx & 255, r = e >> 4, cc = e & 15;
-        const float* Tr = Tp + blk(I, I) * 256 + r * 16;
-        const float* Pc = Tp + blk(I, J) * 256 + cc;
-        float acc = 0.f;
-#pragma unroll
-        for (int m = 0; m < 16; ++m)
-          if (m <= r) acc = fmaf(Tr[m], Pc[m * 16], acc);
-        res[k] = -acc;
+    for (int d = 1; d < 8; ++d) {
+      if (warp < 8 - d) {
+        const int J = warp, I = J + d;
+        float acc[8] = {0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f, 0.f};
+        for (int M = J; M < I; ++M) block_fma(acc, Lp + blk(I, M), Tp + blk(M, J));
+        store_row(Tp + blk(I, J), acc, -1.f);
       }
+      __syncthreads();
     }
-    __syncthreads();
-#pragma unroll
-    for (int k = 0; k < 7; ++k) {
-      const int idx = tid + k * kPrepThreads;
-      if (idx < nout) {
-        const int J = idx >> 8, I = J + d, e = idx & 255;
-        Tp[blk(I, J) * 256 + e] = res[k];
-      }
-    }
-    __syncthreads();
   }
 
   // ---- Tb = Tinv diag(beta) (into L's space), Tbe = Tinv diag(beta e) (over Tinv)
   {
     float t[64];
 #pragma unroll
-    for (int jj = 0; jj < 64; ++jj) {
-      const int j = 64 * hf + jj, I = i >> 4, J = j >> 4;
-      t[jj] = J <= I ? Tp[blk(I, J) * 256 + (i & 15) * 16 + (j & 15)] : 0.f;
+    for (int jb = 0; jb < 4; ++jb) {
+      const int I = i >> 4, J = 4 * hf + jb;
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        float4 x4 = make_float4(0.f, 0.f, 0.f, 0.f);
+        if (J <= I) x4 = *reinterpret_cast<const float4*>(Tp + blk(I, J) + (i & 15) * kBS + 4 * v);
+        t[16 * jb + 4 * v] = x4.x;
+        t[16 * jb + 4 * v + 1] = x4.y;
+        t[16 * jb + 4 * v + 2] = x4.z;
+        t[16 * jb + 4 * v + 3] = x4.w;
+      }
     }
     __syncthreads();
 #pragma unroll
@@ -349,10 +367,10 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   fence_proxy_async_shared();
   tc_fence_before();
   __syncthreads();
-  // U = Tb V -> 0, Cl = Aqk Tb -> 128, W = Tbe K -> 256
+  // U^T = V^T Tb^T -> 0 (lanes = d_v), Cl = Aqk Tb -> 128, W = Tbe K -> 256
   if (tid == 0) {
     tc_fence_after();
-    mma_128(tmem + 0, sL, false, sV, true, 0);
+    mma_128(tmem + 0, sV, true, sL, false, 0);
     mma_128(tmem + 128, sA, false, sL, true, 0);
     mma_128(tmem + 256, sT, false, sK, true, 0);
     umma_commit(bars + 1);
@@ -386,12 +404,12 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
             make_uint4(pack_bf16x2(cl[8 * c8], cl[8 * c8 + 1]), pack_bf16x2(cl[8 * c8 + 2], cl[8 * c8 + 3]),
                        pack_bf16x2(cl[8 * c8 + 4], cl[8 * c8 + 5]), pack_bf16x2(cl[8 * c8 + 6], cl[8 * c8 + 7]));
       }
-      // U^T[dv][i]: row dv, column i
+      // U^T: this thread's lane is d_v = i, its columns tokens j0 ..
 #pragma unroll
-      for (int jj = 0; jj < 32; ++jj) {
-        const __nv_bfloat16 b = __float2bfloat16_rn(u[jj]);
-        *reinterpret_cast<__nv_bfloat16*>(s + kPK + swz_off(j0 + jj, i, kC)) = b;
-      }
+      for (int c8 = 0; c8 < 4; ++c8)
+        *reinterpret_cast<uint4*>(s + kPK + swz16(i, (j0 >> 3) + c8)) =
+            make_uint4(pack_bf16x2(u[8 * c8], u[8 * c8 + 1]), pack_bf16x2(u[8 * c8 + 2], u[8 * c8 + 3]),
+                       pack_bf16x2(u[8 * c8 + 4], u[8 * c8 + 5]), pack_bf16x2(u[8 * c8 + 6], u[8 * c8 + 7]));
     }
   }
   fence_proxy_async_shared();
@@ -550,26 +568,41 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     tc_fence_after();
   };
 
+  // this token's log_alpha, intra output (bf16) and lambdas of the live
+  // heights, loaded one chunk ahead
+  float la_n;
+  uint4 oiv_n[4];
+  float lamh_n[kMaxHeights];
+  auto fetch = [&](int c1) {
+    const size_t r = (size_t)bh * p.T + (size_t)c1 * kC + tid;
+    la_n = p.log_alpha[r];
+    const uint4* oip = reinterpret_cast<const uint4*>(p.oi + r * kD + kSlice * sl);
+#pragma unroll
+    for (int v = 0; v < 4; ++v) oiv_n[v] = oip[v];
+#pragma unroll
+    for (int h = 0; h < kMaxHeights; ++h) lamh_n[h] = ((c1 >> h) & 1) ? p.lam[r * p.L + 8 + h] : 0.f;
+  };
+  fetch(0);
+
   for (int c = 0; c < p.Nc; ++c) {
     const int b = c & 1;
     const int row0 = bh * p.T + c * kC;
     const size_t rowt = (size_t)row0 + tid;  // this thread's token
+    float x = la_n;
+    uint4 oiv[4];
+    float lamh[kMaxHeights];
+#pragma unroll
+    for (int v = 0; v < 4; ++v) oiv[v] = oiv_n[v];
+#pragma unroll
+    for (int h = 0; h < kMaxHeights; ++h) lamh[h] = lamh_n[h];
+    if (c + 1 < p.Nc) fetch(c + 1);
     // cumulative log decay of the chunk
-    float x = p.log_alpha[rowt];
 #pragma unroll
     for (int o = 1; o < 32; o <<= 1) {
       const float y = __shfl_up_sync(0xffffffffu, x, o);
       if (lane >= o) x += y;
     }
     if (lane == 31) qtot[q] = x;
-    // this token's intra output (bf16) and lambdas of the live heights
-    uint4 oiv[4];
-    const uint4* oip = reinterpret_cast<const uint4*>(p.oi + rowt * kD + kSlice * sl);
-#pragma unroll
-    for (int v = 0; v < 4; ++v) oiv[v] = oip[v];
-    float lamh[kMaxHeights];
-#pragma unroll
-    for (int h = 0; h < kMaxHeights; ++h) lamh[h] = ((c >> h) & 1) ? p.lam[rowt * p.L + 8 + h] : 0.f;
     __syncthreads();
     float off = 0.f;
     for (int qq = 0; qq < q; ++qq) off += qtot[qq];
