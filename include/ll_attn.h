@@ -86,8 +86,10 @@ typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
 /* Problem shape of a forward call.
  *   B, H      batch rows and heads (>= 1)
  *   T         sequence length (>= 1); the Gated DeltaNet entry points need a
- *             multiple of `chunk`, the Mamba-2 forward takes any T (a partial
- *             last chunk runs on the CUDA-core path)
+ *             multiple of `chunk`, the Mamba-2 forward takes any T (with bf16
+ *             and d = 128 the whole 128-token tiles run on the tensor cores
+ *             and the last T % 128 tokens as a continuation from their decode
+ *             states, on the CUDA cores)
  *   dk, dv    key / value head dims, each in {16, 32, 64, 128}
  *   L         number of lambda levels per token, >= levels touched by T
  *             (1 if T == 1, else bit_length(T-1) + 1)
@@ -174,9 +176,15 @@ LL_API size_t ll_attn_fwd_cont_workspace_size(const ll_shape* shape, long long t
  * the gist.science (zh) summary §2.3 for the new tokens).
  *   shape      as ll_attn_fwd for the T new tokens; shape->Ls >= bit_length(t0+T)
  *              slots; shape->L >= bit_length(t0+T-1)+1 (lam indexes absolute levels)
- *   t0         position of the first new token; must be a multiple of the
- *              smallest power of two >= T (the new tokens sit in one aligned
- *              block of positions, as fixed-size power-of-two segments do)
+ *   t0         position of the first new token (>= 0).  When t0 is a
+ *              multiple of the smallest power of two >= T (the new tokens sit
+ *              in one aligned block of positions, as fixed-size power-of-two
+ *              segments do) the segment runs as one continuation; otherwise it
+ *              runs as its aligned pieces in turn (each the largest power of
+ *              two that divides its start and fits, or the whole remainder once
+ *              that is aligned), each piece on contiguous copies of its rows
+ *              and continued from the previous piece's decode states, so the
+ *              workspace then also holds those copies and two state buffers
  *   state_in   [B,H,Ls,dv,dk] float32, scale_in [B,H,Ls]: the decode states of
  *              position t0 (as ll_attn_fwd exports them or ll_attn_decode_step
  *              leaves them; true state = scale * S, decayed to t0-1)

@@ -76,6 +76,10 @@ struct FwdArgs {
   // one Fenwick node whose publication word is never written (-1 = none)
   uint64_t timeout_ns = 0;
   long long withhold_node = -1;
+  // row stride (tokens) between the (b, h) slices of q, k, v, o, log_alpha
+  // and lam when it differs from s.T (the tensor-core forward of the whole
+  // tiles of a longer sequence); 0 = s.T
+  int rows_per_head = 0;
 };
 
 size_t fwd_simt_workspace(const ll_shape& s);

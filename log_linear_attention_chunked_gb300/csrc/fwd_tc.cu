@@ -258,6 +258,16 @@ __device__ __forceinline__ uint64_t desc_k(uint32_t tile, int kk) {
 // MN-major operand (rows = K, 64-element M/N blocks 16 KB apart), k-step kk of 16 rows.
 __device__ __forceinline__ uint64_t desc_mn(uint32_t tile, int kk) { return sw128_desc(tile + kk * 2048, kHalf, 1024); }
 
+// L2 prefetch of the 16-byte-aligned interior of [ptr, ptr + bytes): a bulk
+// prefetch needs a 16-byte-aligned start and size, which the rows of
+// log_alpha and lam do not have when the row stride between heads is not a
+// multiple of the tile
+__device__ __forceinline__ void prefetch_l2_inside(const void* ptr, uint32_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  const uintptr_t lo = (a + 15) & ~(uintptr_t)15, hi = (a + bytes) & ~(uintptr_t)15;
+  if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+}
+
 // ------------------------------------------------------------------ producers (warp 0 lanes 0 and 1, warp 11)
 // Warp 0 lane 1 streams K, V and Q of every tile.
 __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
@@ -275,8 +285,8 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
       bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
       bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
       bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.log_alpha + rn, kTile * 4);
-      bulk_prefetch_l2(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+      prefetch_l2_inside(p.log_alpha + rn, kTile * 4);
+      prefetch_l2_inside(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
     }
     if (it > 0) {
       wait_bar(c, B_K_FREE, (it - 1) & 1);
@@ -1124,7 +1134,10 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   if (a.ws_bytes < (a.state_in ? plan.total_cont : plan.total)) return LL_ERR_WORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(a.ws);
   const int BH = s.B * s.H;
-  const uint64_t rows = (uint64_t)BH * s.T;
+  const int stride = a.rows_per_head ? a.rows_per_head : s.T;  // rows between (b, h) slices
+  if (stride < s.T || (a.state_in && stride != s.T) || (long long)BH * stride > (1ll << 31) - 1)
+    return LL_ERR_INVALID_ARG;
+  const uint64_t rows = (uint64_t)BH * stride;
   const uint64_t node_rows = ((uint64_t)BH * plan.Nt + (uint64_t)BH * kPreSlots) * kD;
   CUtensorMap tq, tk, tv, tf, to, tr;
   if (!make_map(&tq, a.q, rows) || !make_map(&tk, a.k, rows) || !make_map(&tv, a.v, rows) ||
@@ -1145,7 +1158,7 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.abort_word = p.flags + (size_t)BH * plan.Nt;
   p.token = next_token();
   p.BH = BH;
-  p.T = s.T;
+  p.T = stride;
   p.Nt = plan.Nt;
   p.L = s.L;
   p.err = a.err;

@@ -115,10 +115,40 @@ def test_chained_segments_from_the_forward_export(B):
     assert rel_err(np.concatenate(outs, 2), full[:, :, t0:]) <= TOL_F32
 
 
-def test_refuses_unaligned_start(B):
-    shape = B.make_shape(1, 1, 256, 32, 32, 12, 32, 11, 0)
-    assert B.ll_attn_fwd_cont_workspace_size(shape, 768) > 0
-    assert B.ll_attn_fwd_cont_workspace_size(shape, 640) == 0   # 640 is not a multiple of 256
+def test_pieces_of_an_unaligned_start():
+    # the host-side split of a segment into aligned single-block pieces
+    from log_linear_attention_chunked_gb300 import binding
+    binding.lib()
+    shape = binding.make_shape(1, 1, 256, 32, 32, 12, 32, 11, 0)
+    assert binding.ll_attn_fwd_cont_workspace_size(shape, 768) > 0
+    assert binding.ll_attn_fwd_cont_workspace_size(shape, 640) > 0   # 640 = 5 x 128: pieces 128 then 128
+
+
+@pytest.mark.parametrize("io,d,T,t0,chunk", [
+    ("f32", 32, 256, 640, 32),       # 640 is not a multiple of 256: pieces 128 + 128
+    ("f32", 16, 100, 37, 16),        # an odd start: pieces 1, 2, 8, 16, ... and a ragged remainder
+    ("bf16", 64, 300, 192, 64),      # pieces 64, 128 (ragged remainder 108)
+    ("bf16", 128, 1024, 384, 64),    # tensor-core pieces 128, 512, then 384 at 1024
+    ("bf16", 128, 1000, 3200, 128),  # tensor-core pieces and a ragged remainder on the CUDA cores
+])
+def test_unaligned_start_matches_dense_rows(B, io, d, T, t0, chunk):
+    """A continuation whose start is not a multiple of the smallest power of
+    two >= T runs as aligned pieces chained through their decode states; the
+    outputs and the states of t0 + T must still match the dense definition."""
+    inp, Ls = _inputs(io, d, T, t0, f"u{io}{d}{T}{t0}", la_mode="slow")
+    f = {n: synth.to_f64(inp[n]) for n in ("q", "k", "v", "log_alpha", "lam")}
+    S0 = _prefix_states(f, t0, Ls)
+    sc0 = np.array([[[1.0 if (t0 >> i) & 1 else 0.0 for i in range(Ls)]] * S0.shape[1]] * S0.shape[0])
+    out, st, sc = _cont(B, inp, t0, T, Ls, chunk, S0, sc0)
+    tol = TOL_F32 if io == "f32" else TOL_BF16
+    full = mamba2.forward_dense_bh(f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+    assert rel_err(out, full[:, :, t0:]) <= tol
+    t1 = t0 + T
+    want = _prefix_states(f, t1, Ls)
+    ne = [(t1 >> i) & 1 == 1 for i in range(Ls)]
+    assert list(sc[0, 0] != 0) == ne
+    true = st * sc[..., None, None]
+    assert rel_err(true[:, :, ne], want[:, :, ne]) <= tol
 
 
 def test_chained_segments_tensor_cores(B):

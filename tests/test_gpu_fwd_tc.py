@@ -177,3 +177,60 @@ def test_onehot_high_tile_levels(B, lvl):
     full = [t for t in rows if (t >> (lvl - 1)) & 1]
     assert np.abs(out[:, :, empty]).max() == 0.0
     assert np.abs(out[:, :, full]).max() > 1e-2
+
+
+def _run_ragged(B, inp, Ls=0):
+    """ll_attn_fwd for a bf16 d=128 shape with T % 128 != 0: the whole tiles on
+    the tensor cores, the remainder continued from their decode states."""
+    dev = torch.device("cuda")
+    g = {n: inp[n].to(dev) for n in ("q", "k", "v", "log_alpha", "lam")}
+    Bn, H, T, d = g["q"].shape
+    shape = B.make_shape(Bn, H, T, d, d, g["lam"].shape[-1], 64, Ls, B.LL_BF16)
+    full = B.make_shape(Bn, H, T - T % 128, d, d, g["lam"].shape[-1], 64, 0, B.LL_BF16)
+    # more launches than the whole-tile forward alone: the tail runs as a continuation
+    assert B.ll_attn_fwd_launches(shape) > B.ll_attn_fwd_launches(full)
+    o = Guarded((Bn, H, T, d), torch.bfloat16)
+    ws = Guarded((B.ll_attn_fwd_workspace_size(shape),), torch.uint8)
+    st = sc = None
+    if Ls:
+        st = Guarded((Bn, H, Ls, d, d), torch.float32)
+        sc = Guarded((Bn, H, Ls), torch.float32)
+    B.ll_attn_fwd(g["q"], g["k"], g["v"], g["log_alpha"], g["lam"], 64, o=o.view, workspace=ws.view,
+                  state_out=st.view if st else None, scale_out=sc.view if sc else None)
+    assert B.ll_last_device_error() == 0
+    for x in (o, ws, st, sc):
+        if x is not None:
+            assert x.intact(), "write outside the buffer"
+    out = o.view.float().cpu().numpy()
+    if Ls:
+        return out, st.view.cpu().numpy(), sc.view.cpu().numpy()
+    return out
+
+
+@pytest.mark.parametrize("T,la_mode", [(1000, "softplus"), (1000, "slow"), (129, "slow"), (2047, "slow")])
+def test_ragged_length(B, T, la_mode):
+    inp = synth.make_inputs(_cfg(T, Bn=2, H=2), la_mode=la_mode, tag=f"tcrag{T}")
+    assert rel_err(_run_ragged(B, inp), _oracle(inp)) <= TOL_BF16
+
+
+def test_ragged_length_state_export(B):
+    T = 1000
+    Ls = T.bit_length() + 1
+    inp = synth.make_inputs(_cfg(T, H=2), la_mode="slow", tag="tcragexp")
+    out, st, sc = _run_ragged(B, inp, Ls=Ls)
+    assert rel_err(out, _oracle(inp)) <= TOL_BF16
+    f = {n: synth.to_f64(inp[n]) for n in ("k", "v", "log_alpha")}
+    for h in range(2):
+        S, ne = mamba2.states_at(f["k"][0, h], f["v"][0, h], f["log_alpha"][0, h], T, Ls)
+        assert list(sc[0, h] > 0) == list(ne)
+        assert rel_err(st[0, h][None, None] * sc[0, h][None, None, :, None, None], S[None, None]) <= TOL_BF16
+
+
+def test_full_size_ragged_sampled_rows(B):
+    """The 16-head long-context shape with 37 tokens fewer: 127 whole tiles per
+    head on the tensor cores, then a 91-token tail."""
+    cfg = dict(synth.WORKLOADS["mamba2_bf16_t16k"], T=16384 - 37)
+    inp = synth.make_inputs(cfg, la_mode="slow", tag="tcrag16k")
+    out = _run_ragged(B, inp)
+    rows = np.array(sorted(set(list(_sampled_rows(16384 - 128, per_tile=(0, 127))) + list(range(16384 - 128, 16384 - 37)))))
+    assert _check_sampled(out, inp, rows) <= TOL_BF16
