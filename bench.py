@@ -175,7 +175,7 @@ KERNEL_SOURCES = {
     "mamba2": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
-    "gdn": ("gdn.cu", "common.cuh", "sm100.cuh"),
+    "gdn": ("gdn_tc.cu", "common.cuh", "sm100.cuh"),             # dominant: the tensor-core level scan
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
     "mamba2_bwd": ("bwd_tc.cu", "bwd.cuh", "common.cuh", "sm100.cuh"),  # dominant: the query-side kernel
