@@ -3,10 +3,10 @@
 //
 // The sequence of each head is cut into 128-token tiles (the MMA M).  Tile j
 // of head bh does, with cs = inclusive cumsum of log_alpha inside the tile:
-//   state   S_j = sum_s exp(cs_127 - cs_s) v_s k_s^T           (Vt^T K, 128x128x128)
+//   intra   P = (Q K^T) . exp(cs_t - cs_s) . lam_t[bitlen(t^s)] (s <= t), O = P V
+//   state   S_j = sum_s v_s exp(cs_127 - cs_s) k_s^T           (V^T Kdec, 128x128x128)
 //   Fenwick F_j = S_j + sum_{m < cto(j)} exp(dec_m) F_{j-2^m}   (cto = trailing ones)
 //           published to global memory (bf16) with its log-decay total G_j
-//   intra   P = (Q K^T) . exp(cs_t - cs_s) . lam_t[bitlen(t^s)] (s <= t), O = P V
 //   inter   for each set bit h of j, with e = (j with bits 0..h cleared) +
 //           2^h - 1:  O += Q'_h F_e^T,  Q'_h[t] = lam_t[8 + h] exp(cs_t + sum
 //           of G over the lower set bits) Q[t]  (the row weights go on Q, so
@@ -19,41 +19,37 @@
 // c0t + j: the bits of c0t are further levels whose nodes are the prefix
 // buckets of the decode states, written as bf16 nodes before this kernel.
 //
-// Roles (384 threads, one CTA per SM, persistent; tiles u = blockIdx.x +
-// i * gridDim.x, interleaved across heads: u = j * (B*H) + bh, so that the
-// tiles running at the same time are few positions of many heads and the
-// chains of node dependencies inside one wave of tiles stay short):
-//   warp 0      lane 1: TMA loads of K, V, Q (+ L2 prefetch of the next tile);
-//               lane 0: the level nodes of the previous tile (F ring), once
-//               their publication words are seen, and their log decays
+// Roles (512 threads in four warpgroups, one CTA per SM, persistent; tiles
+// u = blockIdx.x + i * gridDim.x, interleaved across heads: u = j * (B*H) +
+// bh, so that the tiles running at the same time are few positions of many
+// heads and the chains of node dependencies inside one wave stay short):
+//   warp 0      K, V, Q loads (TMA) and the L2 prefetch of the next tile; Q
+//               has one buffer, loaded for the tile's scores and again for
+//               its inter-tile levels one step later (an L2 hit)
 //   warp 1      TMEM owner and MMA issuer (one thread)
-//   warps 2..9  epilogue: thread (quadrant q = warp % 4, half hf) owns row
-//               32q + lane of every 128x128 accumulator
-//   warp 10     store warp: TMA stores of what the epilogue stages in X
-//               (nodes, raw states, outputs) and the gpu-scope publication of
-//               each node or raw state
-//   warp 11     the pieces of the odd-tile merges (into K and V)
-// Producer roles that wait on other CTAs have warps of their own: spinning
-// lanes of one warp take turns.
-// Software pipeline: in step i the epilogue runs the front half of tile i
-// (cumsum, decayed V, chunk state staged for publication, masked scores P),
-// then the back half of tile i-1 (inter-tile levels + output), then, for odd
-// j, the merge F_j = S_j + the decayed states of tiles (j - 2^cto(j), j).
-// Every tile publishes its chunk state right after the readout (as the node
-// for even j, as the raw state for odd j), and the merge pieces come from a
-// look-back that takes a published node for its whole block or else one
-// tile's raw state, so no merge waits for another merge.  The nodes the back
-// half reads were published by tiles of the previous step, so it rarely
-// waits; the tensor cores run tile i's products while the epilogue finishes
-// tile i-1.  Q is double-buffered for that; the state and PV accumulators of
-// consecutive tiles alternate between two TMEM regions.  P goes back to TMEM
-// (bf16, over the scores) as the A operand of PV, so the X buffer is free
-// after the state product and stages every global store for the TMA.
-// Cross-CTA dependencies only point to tiles of lower index, every CTA walks
-// its tiles in increasing order, and the cooperative launch makes all CTAs
-// co-resident, so the waits always make progress.  Every wait is bounded;
-// a wait that expires records LL_ERR_TIMEOUT and the kernel runs on to its
-// end without the missing data.
+//   warp 2      output stores (TMA) from the staging buffer
+//   warp 3      the level nodes of the previous tile (two-slot ring), once
+//               their publication words are seen, and their log decays
+//   warps 4-11  epilogue: thread (quadrant q = warp % 4, half hf) owns row
+//               32q + lane of the score / output accumulators
+//   warps 12-15 node warps, one per TMEM lane quadrant: the tile's chunk
+//               state from its own TMEM accumulator, the merge of the
+//               Fenwick children F_{j-2^m} (each waited for and loaded by
+//               TMA), the node's store and its gpu-scope publication
+// Step i of the epilogue: the front half of tile i (cumsum, K decayed in
+// place once the scores have read it, masked scores P back into TMEM), then
+// the back half of tile i-1 (level-weighted Q for each level product, the
+// output read out and staged).  The MMA issues per step: scores(i), the
+// chunk state(i) into the node warps' accumulator (once they have released
+// it), the levels of tile i-1 onto its output, then PV(i) into the output
+// accumulator once tile i-1's output has been read.  The node warps publish
+// each node as soon as its children are published, independently of the
+// epilogue, so a node never waits behind a back half.
+// Cross-CTA dependencies only point to tiles of lower index, every role
+// walks its tiles in increasing order, and the cooperative launch makes all
+// CTAs co-resident, so the waits always make progress.  Every wait is
+// bounded; a wait that expires records LL_ERR_TIMEOUT and the kernel runs on
+// to its end without the missing data.
 #include <cudaTypedefs.h>
 #include <cuda_fp16.h>
 
@@ -71,49 +67,48 @@ using namespace sm100;
 constexpr int kTile = 128;
 constexpr int kD = 128;
 constexpr int kLmax = 24;
-constexpr int kThreads = 384;
-constexpr int kPubWarp = 10;
-constexpr int kPieceWarp = 11;
+constexpr int kThreads = 512;
+constexpr int kEpiWarp0 = 4;    // warps 4..11
+constexpr int kNodeWarp0 = 12;  // warps 12..15
 constexpr int kEpi = 256;
+constexpr int kNodeThreads = 128;
 constexpr uint32_t kHalf = kTile * 64 * 2;  // one [128 x 64] bf16 swizzled block: 16 KB
 constexpr uint32_t kTileBytes = 2 * kHalf;  // 32 KB
 constexpr float kLog2e = 1.4426950408889634f;
 constexpr uint64_t kTimeoutNs = 4000000000ull;  // default limit of a bounded wait
 
-// TMEM columns: two 128-column regions that hold the chunk state and then the
-// output (PV, then + the inter-tile levels) of alternating tiles; the scores
-// (then P, bf16, in their first 64 columns); two 64-column buffers of
-// level-weighted Q (bf16), the A operand of the level products.
-constexpr uint32_t kTmR0 = 0, kTmS = 256, kTmQP = 384;
+// TMEM columns: the output accumulator (PV, then + the inter-tile levels);
+// the scores (then P, bf16, in their first 64 columns); two 64-column buffers
+// of level-weighted Q (bf16), the A operand of the level products; the node
+// warps' accumulator (the chunk state, then + the merged children).
+constexpr uint32_t kTmR = 0, kTmS = 128, kTmQP = 256, kTmM = 384;
 
-// shared-memory layout (offsets from the dynamic base, which must be 1024-aligned)
-constexpr uint32_t kOffQ0 = 0;
-constexpr uint32_t kOffQ1 = kOffQ0 + kTileBytes;
-constexpr uint32_t kOffK = kOffQ1 + kTileBytes;
+// shared memory (offsets from the dynamic base, which must be 1024-aligned)
+constexpr uint32_t kOffQ = 0;                      // Q: for the scores, then again for the levels
+constexpr uint32_t kOffK = kOffQ + kTileBytes;     // K, decayed in place for the chunk state
 constexpr uint32_t kOffV = kOffK + kTileBytes;
-constexpr uint32_t kOffX = kOffV + kTileBytes;  // decayed V, then staging of TMA stores
-constexpr uint32_t kOffF0 = kOffX + kTileBytes;
+constexpr uint32_t kOffF0 = kOffV + kTileBytes;    // level-node ring
 constexpr uint32_t kOffF1 = kOffF0 + kTileBytes;
-constexpr uint32_t kOffCs = kOffF1 + kTileBytes;  // float[128] cumsum x log2(e)
-constexpr uint32_t kOffCol = kOffCs + kTile * 4;  // float[128] exp(cs_e - cs_s), e = end of s's 32-group
-constexpr uint32_t kOffLam = kOffCol + kTile * 4; // half[6][128] lambda levels 0..5 / the row's max
-// misc: quadrant totals [0,16), abort flag 16, tmem base 32
+constexpr uint32_t kOffC = kOffF1 + kTileBytes;    // node warps: merge children, then the node
+constexpr uint32_t kOffX = kOffC + kTileBytes;     // output staging
+constexpr uint32_t kOffCs = kOffX + kTileBytes;    // float[128] cumsum x log2(e)
+constexpr uint32_t kOffCol = kOffCs + kTile * 4;   // float[128] exp(cs_e - cs_s), e = end of s's 32-group
+constexpr uint32_t kOffLam = kOffCol + kTile * 4;  // half[6][128] lambda levels 0..5 / the row's max
+// misc: epilogue quadrant totals [0,16), abort flag 16, tmem base 32, node-warp totals [48,64)
 constexpr uint32_t kOffMisc = kOffLam + 6 * kTile * 2;
-// node exchange between the producers and their consumers: level log decays
-// of the previous tile (float[2][16], by step parity) at 0, the merge piece
-// descriptors (R, R_end, last, own; float[2][4], by buffer K/V) at 128, the
-// step-tagged count of levels whose decay is ready (u32[2], by step parity)
-// at 160, the merge's "more pieces" words (int[2]) at 168
+// level producer -> epilogue: the level log decays of the previous tile
+// (float[2][16], by step parity) at 0 and the step-tagged count of levels
+// whose decay is ready (u32[2]) at 160; node leader -> node warps: the
+// child's log-decay total at 176
 constexpr uint32_t kOffNode = kOffMisc + 64;
-constexpr uint32_t kOffBars = kOffNode + 192;            // mbarriers
+constexpr uint32_t kOffBars = kOffNode + 192;  // mbarriers
 
 // mbarriers (all with arrival count 1: one producer arrive + TMA bytes, one
 // tcgen05.commit, or one elected thread)
 enum Bar : int {
-  B_K_FULL, B_V_FULL, B_Q_FULL0, B_Q_FULL1, B_F_FULL0, B_F_FULL1, B_F_FREE0, B_F_FREE1, B_K_FREE, B_V_FREE,
-  B_Q_FREE0, B_Q_FREE1, B_VT_READY, B_STATE_DONE, B_S_DONE, B_P_READY, B_QP_FULL0, B_QP_FULL1, B_QP_FREE0,
-  B_QP_FREE1, B_O_READY, B_FINAL, B_X_STAGED, B_X_FREE, B_LVLD_FREE, B_PC_FULL0, B_PC_FULL1,
-  B_PC_FREE0, B_PC_FREE1, B_KV_REL, kNumBars
+  B_K_FULL, B_V_FULL, B_QS_FULL, B_QB_FULL, B_Q_FREE, B_K_FREE, B_V_FREE, B_F_FULL0, B_F_FULL1, B_F_FREE0,
+  B_F_FREE1, B_S_DONE, B_KDEC, B_P_READY, B_QP_FULL0, B_QP_FULL1, B_QP_FREE0, B_QP_FREE1, B_O_READY, B_R_FREE,
+  B_STATE_DONE, B_M_FREE, B_C_FULL, B_X_STAGED, B_X_FREE, B_LVLD_FREE, B_FINAL, kNumBars
 };
 constexpr uint32_t kSmemBytes = kOffBars + kNumBars * 8;
 static_assert(kSmemBytes <= 232448, "shared memory budget of one CTA");
@@ -127,13 +122,11 @@ struct TcParams {
   __nv_bfloat16* F;  // [BH * Nt, 128, 128] Fenwick nodes
   float* G;          // [BH * Nt] log-decay totals of the nodes
   // [BH * Nt] publication words: this call's token in the high half, the
-  // log-decay total (node, or tile for a raw state) in the low half, so one
-  // atomic load gives both
-  uint64_t* flags;   // nodes
-  uint64_t* rflags;  // raw states of odd tiles (in the node rows of R)
+  // node's log-decay total in the low half, so one atomic load gives both
+  uint64_t* flags;
   uint64_t* abort_word;
   uint32_t token;    // per call, never 0
-  int BH, T, Nt, L;
+  int BH, T, Nt, L;  // T: rows between the (b, h) slices of the inputs
   // prefill continuation: absolute index of the first tile (a multiple of the
   // smallest power of two >= Nt, so its set bits lie above every tile's own);
   // its levels read the prefix nodes at F[BH * Nt + bh * kPreSlots + h]
@@ -268,58 +261,70 @@ __device__ __forceinline__ void prefetch_l2_inside(const void* ptr, uint32_t byt
   if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
 }
 
-// ------------------------------------------------------------------ producers (warp 0 lanes 0 and 1, warp 11)
-// Warp 0 lane 1 streams K, V and Q of every tile.
+// ------------------------------------------------------------------ producers (warps 0 and 3)
+// Warp 0 streams K, Q and V of every tile, and Q once more for the tile's
+// levels one step later: per step, K(i), Q(i) (the scores' copy), V(i), then
+// Q(i-1) again (the levels' copy) -- the one Q buffer alternates between the
+// two uses, each load waiting for the previous use to release it.
 __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
-  uint32_t kc = 0, vc = 0, qc[2] = {0, 0};
+  uint32_t kc = 0, vc = 0, qs = 0, qb = 0, ql = 0;
   unsigned char* s = c.base;
-  for (int it = 0; it < n && !*c.abort_s; ++it) {
+  auto load_q = [&](int row0, int bar) {
+    if (ql > 0) wait_bar(c, B_Q_FREE, (ql - 1) & 1);
+    if (*c.abort_s) return false;
+    mbar_arrive_expect_tx(c.bars + bar, kTileBytes);
+    tma_load_2d(s + kOffQ, tq, c.bars + bar, 0, row0);
+    tma_load_2d(s + kOffQ + kHalf, tq, c.bars + bar, 64, row0);
+    ++ql;
+    return true;
+  };
+  int row_prev = 0;
+  for (int it = 0; it <= n && !*c.abort_s; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
-    const int row0 = (u % p.BH) * p.T + (u / p.BH) * kTile;
-    // stage the next tile's inputs in L2 while this one is processed
-    if (it + 1 < n) {
-      const int un = u + gridDim.x;
-      const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
-      bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
-      bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
-      prefetch_l2_inside(p.log_alpha + rn, kTile * 4);
-      prefetch_l2_inside(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+    const int row0 = it < n ? (u % p.BH) * p.T + (u / p.BH) * kTile : 0;
+    if (it < n) {
+      // stage the next tile's inputs in L2 while this one is processed
+      if (it + 1 < n) {
+        const int un = u + gridDim.x;
+        const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
+        bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
+        bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
+        bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
+        prefetch_l2_inside(p.log_alpha + rn, kTile * 4);
+        prefetch_l2_inside(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
+      }
+      if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);  // the previous state product has read K
+      if (*c.abort_s) break;
+      mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
+      tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
+      tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_K_FULL, 64, row0);
+      ++kc;
+      // Q before V: the scores need it first, and V waits for the previous PV
+      if (!load_q(row0, B_QS_FULL)) break;
+      ++qs;
+      if (it > 0) wait_bar(c, B_V_FREE, (it - 1) & 1);  // PV and the state product have read V
+      if (*c.abort_s) break;
+      mbar_arrive_expect_tx(c.bars + B_V_FULL, kTileBytes);
+      tma_load_2d(s + kOffV, tv, c.bars + B_V_FULL, 0, row0);
+      tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_V_FULL, 64, row0);
+      ++vc;
     }
-    if (it > 0) {
-      wait_bar(c, B_K_FREE, (it - 1) & 1);
-      wait_bar(c, B_KV_REL, (it - 1) & 1);  // merge pieces of tile it-1 are done with K and V
+    if (it >= 1) {
+      if (!load_q(row_prev, B_QB_FULL)) break;
+      ++qb;
     }
-    if (*c.abort_s) break;
-    mbar_arrive_expect_tx(c.bars + B_K_FULL, kTileBytes);
-    tma_load_2d(s + kOffK, tk, c.bars + B_K_FULL, 0, row0);
-    tma_load_2d(s + kOffK + kHalf, tk, c.bars + B_K_FULL, 64, row0);
-    ++kc;
-    if (it > 0) wait_bar(c, B_V_FREE, (it - 1) & 1);
-    if (*c.abort_s) break;
-    mbar_arrive_expect_tx(c.bars + B_V_FULL, kTileBytes);
-    tma_load_2d(s + kOffV, tv, c.bars + B_V_FULL, 0, row0);
-    tma_load_2d(s + kOffV + kHalf, tv, c.bars + B_V_FULL, 64, row0);
-    ++vc;
-    const int qs = it & 1;
-    if (it >= 2) wait_bar(c, B_Q_FREE0 + qs, ((it - 2) >> 1) & 1);
-    if (*c.abort_s) break;
-    unsigned char* qdst = s + (qs ? kOffQ1 : kOffQ0);
-    mbar_arrive_expect_tx(c.bars + B_Q_FULL0 + qs, kTileBytes);
-    tma_load_2d(qdst, tq, c.bars + B_Q_FULL0 + qs, 0, row0);
-    tma_load_2d(qdst + kHalf, tq, c.bars + B_Q_FULL0 + qs, 64, row0);
-    ++qc[qs];
+    row_prev = row0;
   }
   // drain: every copy armed above has landed before the CTA may exit
   if (kc > 0) drain_bar(c, B_K_FULL, (kc - 1) & 1);
   if (vc > 0) drain_bar(c, B_V_FULL, (vc - 1) & 1);
-  for (int b = 0; b < 2; ++b)
-    if (qc[b] > 0) drain_bar(c, B_Q_FULL0 + b, (qc[b] - 1) & 1);
+  if (qs > 0) drain_bar(c, B_QS_FULL, (qs - 1) & 1);
+  if (qb > 0) drain_bar(c, B_QB_FULL, (qb - 1) & 1);
 }
 
-// Warp 0 lane 0 runs the F ring (two 32 KB slots) of the level nodes for
+// Warp 3 runs the F ring (two 32 KB slots) of the level nodes for
 // the MMA.  Per step i it acquires the Fenwick nodes of tile i-1's levels in
 // order, hands each level's log decay to the epilogue (a step-tagged count
 // released in shared memory, so the epilogue starts on level 0 before later
@@ -375,107 +380,66 @@ __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
   if (fcnt > 1) drain_bar(c, B_F_FULL0 + ((fcnt - 2) & 1), ((fcnt - 2) >> 1) & 1);
 }
 
-// Warp 11 brings the pieces of the merge F_j = S_j + sum of the decayed states
-// of tiles (j - 2^cto(j), j) for odd j into the K and V buffers (alternately,
-// once the products of tile j have read them): first the tile's own raw
-// state, then a look-back from j - 1 that takes a published node for its
-// whole block or else one tile's raw state (published right after its
-// readout), so no merge ever waits for another merge.  For even j it releases
-// the K and V buffers for the next tile (B_KV_REL) once the products of tile
-// j have read K; for odd j the epilogue does, after the last piece.
-__device__ void producer_pieces(const Ctx& c, const CUtensorMap* tf, const CUtensorMap* tr) {
-  const TcParams& p = *c.p;
-  const int n = tiles_of_cta(p.BH * p.Nt);
-  unsigned char* s = c.base;
-  float* pdesc = reinterpret_cast<float*>(s + kOffNode + 128);  // [2][4]
-  uint32_t npc[2] = {0, 0};
-  for (int it = 0; it < n && !*c.abort_s; ++it) {
-    const int u = blockIdx.x + it * gridDim.x;
-    const int j = u / p.BH;
-    if (!(j & 1)) {
-      wait_bar(c, B_K_FREE, it & 1);  // K of this tile was loaded: the release cannot run a phase ahead
-      mbar_arrive(c.bars + B_KV_REL);
-      continue;
-    }
-    const size_t node_j = (size_t)(u % p.BH) * p.Nt + j;
-    bool used[2] = {false, false};
-    auto place = [&](int b, const CUtensorMap* map, size_t node, const float* desc) {
-      if (!used[b]) {
-        wait_bar(c, b ? B_V_FREE : B_K_FREE, it & 1);  // the products of this tile have read the buffer
-        used[b] = true;
-      }
-      if (npc[b] > 0) wait_bar(c, B_PC_FREE0 + b, (npc[b] - 1) & 1);
-      if (*c.abort_s) return false;
-      for (int i = 0; i < 4; ++i) pdesc[4 * b + i] = desc[i];
-      unsigned char* dst = s + (b ? kOffV : kOffK);
-      mbar_arrive_expect_tx(c.bars + B_PC_FULL0 + b, kTileBytes);
-      tma_load_2d(dst, map, c.bars + B_PC_FULL0 + b, 0, (int)(node * kD));
-      tma_load_2d(dst + kHalf, map, c.bars + B_PC_FULL0 + b, 64, (int)(node * kD));
-      ++npc[b];
-      return true;
-    };
-    // the tile's own raw state, weight 1
-    wait_flag(c, p.rflags, node_j);
-    fence_proxy_async_global();
-    const float own[4] = {0.f, 0.f, 0.f, 1.f};
-    if (!place(0, tr, node_j, own)) break;
-    // look-back over tiles (stop, j - 1], most recent first
-    const int stop = j - (1 << (__ffs(~j) - 1));
-    float R = 0.f;
-    for (int e = j - 1, idx = 1; e > stop; ++idx) {
-      const size_t node = node_j - (size_t)(j - e);
-      bool full = true;
-      uint64_t w;
-      if (e & 1) {
-        w = ld_relaxed_u64(p.flags + node);
-        full = flag_ok(c, w);
-        if (full) fence_acq_rel_gpu();
-        else w = wait_flag(c, p.rflags, node);
-      } else {
-        w = wait_flag(c, p.flags, node);  // even tiles publish their state as the node at once
-      }
-      fence_proxy_async_global();
-      const float g = flag_g(w);
-      const int size = full ? 1 << (__ffs(~e) - 1) : 1;
-      const float desc[4] = {R, R + g, (e - size <= stop) ? 1.f : 0.f, 0.f};
-      if (!place(idx & 1, full ? tf : tr, node, desc)) break;
-      R += g;
-      e -= size;
-    }
-  }
-  for (int b = 0; b < 2; ++b)
-    if (npc[b] > 0) drain_bar(c, B_PC_FULL0 + b, (npc[b] - 1) & 1);
-}
-
 // ------------------------------------------------------------------ MMA issuer
 template <bool kCont>
 __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   const TcParams& p = *c.p;
-  const int total = p.BH * p.Nt;
-  const int n = tiles_of_cta(total);
-  const uint32_t sQ0 = smem_u32(c.base + kOffQ0), sQ1 = smem_u32(c.base + kOffQ1), sK = smem_u32(c.base + kOffK),
-                 sV = smem_u32(c.base + kOffV), sX = smem_u32(c.base + kOffX), sF0 = smem_u32(c.base + kOffF0),
-                 sF1 = smem_u32(c.base + kOffF1);
-  constexpr uint32_t id_state = idesc_bf16(128, 128, true, true);   // Vt^T (MN) x K (MN)
-  constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);    // Q (K) x K (K); Q' (TMEM) x F (K)
-  constexpr uint32_t id_pv = idesc_bf16(128, 128, false, true);     // P (TMEM) x V (MN)
+  const int n = tiles_of_cta(p.BH * p.Nt);
+  const uint32_t sQ = smem_u32(c.base + kOffQ), sK = smem_u32(c.base + kOffK), sV = smem_u32(c.base + kOffV),
+                 sF0 = smem_u32(c.base + kOffF0), sF1 = smem_u32(c.base + kOffF1);
+  constexpr uint32_t id_state = idesc_bf16(128, 128, true, true);  // V^T (MN) x Kdec (MN)
+  constexpr uint32_t id_qk = idesc_bf16(128, 128, false, false);   // Q (K) x K (K); Q' (TMEM) x F (K)
+  constexpr uint32_t id_pv = idesc_bf16(128, 128, false, true);    // P (TMEM) x V (MN)
   uint32_t fcnt = 0, qpc = 0;
 
   // one inter-tile level of the previous tile, accumulated onto its output:
   // D[t][dv] += Q'[t] . F[dv], Q' = the level-weighted Q from the epilogue (TMEM)
-  auto issue_level = [&](uint32_t d) {
+  auto issue_level = [&](auto&& wait) {
     const int b = qpc & 1;
     const int fs = fcnt & 1;
-    wait_bar(c, B_F_FULL0 + fs, (fcnt >> 1) & 1);
-    wait_bar(c, B_QP_FULL0 + b, (qpc >> 1) & 1);
+    wait(B_F_FULL0 + fs, (fcnt >> 1) & 1);
+    wait(B_QP_FULL0 + b, (qpc >> 1) & 1);
     tc_fence_after();
     const uint32_t sF = fs ? sF1 : sF0;
 #pragma unroll
-    for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(d, tmem + kTmQP + 64 * b + kk * 8, desc_k(sF, kk), id_qk, 1);
+    for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(tmem + kTmR, tmem + kTmQP + 64 * b + kk * 8, desc_k(sF, kk), id_qk, 1);
     umma_commit(c.bars + B_QP_FREE0 + b);
     umma_commit(c.bars + B_F_FREE0 + fs);
     ++fcnt;
     ++qpc;
+  };
+  // chunk state: D[dv][dk] = sum_s V[s][dv] Kdec[s][dk], into the node warps' accumulator
+  auto issue_state = [&]() {
+    tc_fence_after();
+#pragma unroll
+    for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmM, desc_mn(sV, kk), desc_mn(sK, kk), id_state, kk > 0);
+    umma_commit(c.bars + B_STATE_DONE);
+    umma_commit(c.bars + B_K_FREE);
+  };
+
+  // a deferred state product goes out as soon as M and V are ready, checked
+  // while this thread waits for anything else
+  bool state_pending = false;
+  uint32_t m_par = 0;  // parity of the M release the pending state needs
+  int pend_it = 0;
+  auto try_state = [&]() {
+    if (state_pending && mbar_test_wait(c.bars + B_M_FREE, m_par) && mbar_test_wait(c.bars + B_V_FULL, pend_it & 1)) {
+      issue_state();
+      state_pending = false;
+    }
+  };
+  auto wait_mma = [&](int b, uint32_t par) {
+    if (mbar_try_wait(c.bars + b, par)) return;
+    if (*c.abort_s) return;
+    const uint64_t t0 = globaltimer_ns();
+    while (!mbar_try_wait(c.bars + b, par)) {
+      try_state();
+      if (*c.abort_s) return;
+      if (globaltimer_ns() - t0 > p.timeout_ns) {
+        note_abort(c);
+        return;
+      }
+    }
   };
 
   int jp = 0;
@@ -483,39 +447,47 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
     const int u = blockIdx.x + it * gridDim.x;
     const int j = it < n ? u / p.BH : 0;
     const int nlev_p = it >= 1 ? __popc(jp | start_tile<kCont>(p)) : 0;
-    const uint32_t tR = tmem + kTmR0 + (it & 1) * 128;
     if (it < n) {
-      // chunk state: D[dv][dk] = sum_s Vt[s][dv] K[s][dk]
-      wait_bar(c, B_K_FULL, it & 1);
-      wait_bar(c, B_VT_READY, it & 1);
-      tc_fence_after();
-#pragma unroll
-      for (int kk = 0; kk < 8; ++kk) umma_bf16(tR, desc_mn(sX, kk), desc_mn(sK, kk), id_state, kk > 0);
-      umma_commit(c.bars + B_STATE_DONE);
       // scores: D[t][s] = Q[t] . K[s]
-      const uint32_t sQ = it & 1 ? sQ1 : sQ0;
-      wait_bar(c, B_Q_FULL0 + (it & 1), (it >> 1) & 1);
+      wait_bar(c, B_K_FULL, it & 1);
+      wait_bar(c, B_QS_FULL, it & 1);
       tc_fence_after();
 #pragma unroll
       for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + kTmS, desc_k(sQ, kk), desc_k(sK, kk), id_qk, kk > 0);
       umma_commit(c.bars + B_S_DONE);
-      umma_commit(c.bars + B_K_FREE);
+      umma_commit(c.bars + B_Q_FREE);
+      // the state as soon as K is decayed and V has landed, unless the node
+      // warps still hold the previous tile's node (then after this step's
+      // other products)
+      wait_bar(c, B_KDEC, it & 1);
+      if ((it == 0 || mbar_test_wait(c.bars + B_M_FREE, (it - 1) & 1)) && mbar_test_wait(c.bars + B_V_FULL, it & 1)) {
+        issue_state();
+      } else {
+        state_pending = true;
+        m_par = (it - 1) & 1;
+        pend_it = it;
+        if (it == 0) m_par = 1;  // no previous node: M is free (phase parity 1 reads as complete)
+      }
+    }
+    if (it >= 1) {
+      for (int l = 0; l < nlev_p; ++l) issue_level(wait_mma);
+      umma_commit(c.bars + B_O_READY);  // PV of the previous tile + its levels
     }
     if (it < n) {
-      // intra output: D[t][dv] = sum_s P[t][s] V[s][dv], P from TMEM, into the state's region
-      wait_bar(c, B_P_READY, it & 1);
+      // intra output: D[t][dv] = sum_s P[t][s] V[s][dv], P from TMEM, once the
+      // previous tile's output has been read out of the accumulator
+      wait_mma(B_V_FULL, it & 1);
+      wait_mma(B_P_READY, it & 1);
+      if (it >= 1) wait_mma(B_R_FREE, (it - 1) & 1);
       tc_fence_after();
 #pragma unroll
-      for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(tR, tmem + kTmS + kk * 8, desc_mn(sV, kk), id_pv, kk > 0);
-      umma_commit(c.bars + B_V_FREE);
-    }
-    // the previous tile's levels after PV, which never waits on another CTA;
-    // then its output (PV + levels) is complete, and its Q has been read
-    if (it >= 1) {
-      const uint32_t tRp = tmem + kTmR0 + ((it - 1) & 1) * 128;
-      for (int l = 0; l < nlev_p; ++l) issue_level(tRp);
-      umma_commit(c.bars + B_O_READY);
-      umma_commit(c.bars + B_Q_FREE0 + ((it - 1) & 1));
+      for (int kk = 0; kk < 8; ++kk) umma_bf16_ta(tmem + kTmR, tmem + kTmS + kk * 8, desc_mn(sV, kk), id_pv, kk > 0);
+      if (state_pending) {
+        wait_bar(c, B_M_FREE, m_par);
+        issue_state();
+        state_pending = false;
+      }
+      umma_commit(c.bars + B_V_FREE);  // PV and the state product have read V
     }
     jp = j;
   }
@@ -523,49 +495,24 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
   drain_bar(c, B_FINAL, 0);
 }
 
-// ------------------------------------------------------------------ epilogue
-
+// ------------------------------------------------------------------ epilogue (warps 4..11)
 template <bool kCont>
 __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
   const int n = tiles_of_cta(total);
   const int q = warp & 3;
-  const int hf = (warp - 2) >> 2;
+  const int hf = (warp - kEpiWarp0) >> 2;
   const int row = 32 * q + lane;
-  const bool leader = (warp == 2 && lane == 0);
+  const bool leader = (warp == kEpiWarp0 && lane == 0);
   const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);  // this warp's lane quadrant
   unsigned char* s = c.base;
   float* cs_s = reinterpret_cast<float*>(s + kOffCs);
   float* col_s = reinterpret_cast<float*>(s + kOffCol);
   __half* lamh = reinterpret_cast<__half*>(s + kOffLam);
   float* qtot = reinterpret_cast<float*>(s + kOffMisc);
-  volatile float* gpub_s = reinterpret_cast<volatile float*>(s + kOffMisc + 20);  // log-decay total to publish
-  unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;  // this thread's 128 B of a staged tile
-  uint32_t qpc = 0;          // level-weighted Q tiles written (two TMEM buffers)
-  uint32_t npc[2] = {0, 0};  // merge pieces consumed per buffer (K, V)
-  uint32_t xs = 0;          // X stagings so far
-
-  // stages a tile in X for the store warp (packed bf16 words, 8 per 16 bytes
-  // of this thread's row); the previous staging has been read out of X
-  auto stage_words = [&](const uint32_t* w) {
-    if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
-#pragma unroll
-    for (int c8 = 0; c8 < 8; ++c8)
-      *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) =
-          make_uint4(w[4 * c8], w[4 * c8 + 1], w[4 * c8 + 2], w[4 * c8 + 3]);
-    fence_proxy_async_shared();
-    __syncwarp();
-    named_bar_sync(1, kEpi);
-    if (leader) mbar_arrive(c.bars + B_X_STAGED);
-    ++xs;
-  };
-  auto stage = [&](const float* a) {
-    uint32_t w[32];
-#pragma unroll
-    for (int i = 0; i < 32; ++i) w[i] = pack_bf16x2(a[2 * i], a[2 * i + 1]);
-    stage_words(w);
-  };
+  uint32_t qpc = 0;  // level-weighted Q tiles written (two TMEM buffers)
+  uint32_t xs = 0;   // outputs staged
 
   // this row's log_alpha and intra-level lambdas, read one tile ahead
   float la_n = 0.f, lam_n[8];
@@ -583,8 +530,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   for (int it = 0; it <= n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     int bh = 0, j = 0;
-    float cs_t = 0.f, cs_end = 0.f;
-    uint32_t opk[32];  // the previous tile's output (bf16 pairs) until it is staged
+    float cs_t = 0.f;
     if (it < n) {
       // ================= front half of tile it
       bh = u % p.BH;
@@ -611,8 +557,8 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       float off = 0.f;
       for (int qq = 0; qq < q; ++qq) off += qtot[qq];
       cs_t = x + off;
-      const float cs2_t = cs_t * kLog2e;                                   // base-2 log decay
-      const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);      // end of this 32-group
+      const float cs2_t = cs_t * kLog2e;                               // base-2 log decay
+      const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);  // end of this 32-group
       if (hf == 0) {
         cs_s[row] = cs2_t;
         col_s[row] = ex2(cs2_grp_end - cs2_t);
@@ -631,53 +577,32 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       __syncwarp();
       named_bar_sync(1, kEpi);
       const float cs2_end = cs_s[kTile - 1];
-      cs_end = cs2_end * 0.69314718055994531f;  // natural log decay of the whole tile
 
-      // decayed V for the chunk state: X[s] = exp(cs_end - cs_s) V[s]
-      wait_bar_w(c, B_V_FULL, it & 1);
-      if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
+      // scores ready: K has been read by them, so it is decayed in place for
+      // the chunk state, K[s] <- exp(cs_end - cs_s) K[s]
+      wait_bar_w(c, B_S_DONE, it & 1);
+      __syncwarp();
+      tc_fence_after();
       {
         const float dec = ex2(cs2_end - cs2_t);
-        const uint32_t off_row = hf * kHalf + row * 128;
-        const uint4* src = reinterpret_cast<const uint4*>(s + kOffV + off_row);
-        uint4* dst = reinterpret_cast<uint4*>(s + kOffX + off_row);
+        uint4* kr = reinterpret_cast<uint4*>(s + kOffK + hf * kHalf + row * 128);
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
           const int cc = c8 ^ (row & 7);  // lanes of a warp spread over the banks
-          uint4 v = src[cc];
+          uint4 v = kr[cc];
           uint32_t* w = reinterpret_cast<uint32_t*>(&v);
 #pragma unroll
           for (int i = 0; i < 4; ++i) {
             const float2 f = unpack_bf16x2(w[i]);
             w[i] = pack_bf16x2(f.x * dec, f.y * dec);
           }
-          dst[cc] = v;
+          kr[cc] = v;
         }
       }
       fence_proxy_async_shared();
       __syncwarp();
       named_bar_sync(1, kEpi);
-      if (leader) mbar_arrive(c.bars + B_VT_READY);
-
-      // chunk state S_j (its TMEM region takes PV after P_READY); the state
-      // product has read X, so X stages it at once: for even j as the node
-      // F_j = S_j, for odd j as the raw state, merged after the mask
-      const uint32_t tR = tl + kTmR0 + (it & 1) * 128;
-      const size_t node_j = (size_t)bh * p.Nt + j;
-      {
-        wait_bar_w(c, B_STATE_DONE, it & 1);
-        __syncwarp();
-        tc_fence_after();
-        float acc[64];
-        tmem_ld32(tR + 64 * hf, acc);
-        tmem_ld32(tR + 64 * hf + 32, acc + 32);
-        tmem_ld_wait();
-        if (leader) {
-          if (!(j & 1)) p.G[node_j] = cs_end;
-          gpub_s[0] = cs_end;  // the word published with this node or raw state
-        }
-        stage(acc);
-      }
+      if (leader) mbar_arrive(c.bars + B_KDEC);
 
       // masked scores -> P (bf16) back into the scores' TMEM columns.  This
       // thread takes columns 32 g + 16 hf + [0, 16) of each 32-group g, so
@@ -686,9 +611,6 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // exp(cs_t - cs_e) exp(cs_e - cs_s), e = 32 g + 31, the second factor
       // from the per-tile table;  g == q: per element, levels 0..5 from the
       // half table;  g > q: zero.
-      wait_bar_w(c, B_S_DONE, it & 1);
-      __syncwarp();
-      tc_fence_after();
       uint32_t pw[2][8];
 #pragma unroll
       for (int g = 0; g < 4; ++g) {
@@ -741,11 +663,10 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         }
       }
       tmem_st_wait();
-      tc_fence_before();  // orders the state and score reads and the P writes before the PV product
+      tc_fence_before();  // orders the score reads and the P writes before the PV product
       __syncwarp();
       named_bar_sync(1, kEpi);
       if (leader) mbar_arrive(c.bars + B_P_READY);
-
     }
 
     if (it >= 1) {
@@ -764,20 +685,25 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         const uint64_t t0 = globaltimer_ns();
         while (ld_acquire_cta_u32(nlr) < want) {
           if (*c.abort_s) return;
-          if (globaltimer_ns() - t0 > c.p->timeout_ns) {
+          if (globaltimer_ns() - t0 > p.timeout_ns) {
             note_abort(c);
             return;
           }
         }
       };
       wait_levels(0);  // the level producer has reached this step
-      // this thread's half row of the previous tile's Q (bf16, from its smem tile)
+      // this thread's half row of the previous tile's Q (bf16, its second load);
+      // once every thread has it the buffer goes to the next tile's scores
+      wait_bar_w(c, B_QB_FULL, (it - 1) & 1);
       uint4 qv[8];
       {
-        const unsigned char* qrow = s + ((it - 1) & 1 ? kOffQ1 : kOffQ0) + hf * kHalf + row * 128;
+        const unsigned char* qrow = s + kOffQ + hf * kHalf + row * 128;
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) qv[c8] = *reinterpret_cast<const uint4*>(qrow + ((c8 ^ (row & 7)) << 4));
       }
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      if (leader) mbar_arrive(c.bars + B_Q_FREE);
       // inter-tile levels: Q'_l = lam_t[8 + h] exp(cs_t + D_l) Q_t goes to TMEM
       // as the A operand of a product the MMA accumulates onto the output
       int l = 0;
@@ -811,75 +737,37 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         ++qpc;
       }
 
-      // output = PV + levels, accumulated in TMEM; bf16, staged after this step's merge
+      // output = PV + levels, accumulated in TMEM; bf16, staged for the store warp
+      if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
       wait_bar_w(c, B_O_READY, (it - 1) & 1);
       __syncwarp();
       tc_fence_after();
-      const uint32_t tRp = tl + kTmR0 + ((it - 1) & 1) * 128 + 64 * hf;
+      {
+        unsigned char* xrow = s + kOffX + hf * kHalf + row * 128;
 #pragma unroll
-      for (int c32 = 0; c32 < 2; ++c32) {
-        float v[32];
-        tmem_ld32(tRp + 32 * c32, v);
-        tmem_ld_wait();
+        for (int c32 = 0; c32 < 2; ++c32) {
+          float v[32];
+          tmem_ld32(tl + kTmR + 64 * hf + 32 * c32, v);
+          tmem_ld_wait();
 #pragma unroll
-        for (int i = 0; i < 16; ++i) opk[16 * c32 + i] = pack_bf16x2(v[2 * i], v[2 * i + 1]);
-      }
-      // the region is free once every thread is past this point; the next
-      // tile's VT_READY arrival (after later named barriers) hands it back
-      tc_fence_before();
-      if (leader) mbar_arrive(c.bars + B_LVLD_FREE);
-      stage_words(opk);
-    }
-
-    if (it < n && (j & 1)) {
-      // odd j: F_j = S_j + the decayed states of tiles (j - 2^cto(j), j), from
-      // the piece producer in K and V: the tile's own raw state (weight 1),
-      // then published nodes or raw states, most recent first.  Merged after
-      // the back half, when its inputs are long published; K and V go to the
-      // next tile as soon as the last piece is read, and the result is staged
-      // in X while the output's store may still be reading it.
-      const float* pdesc = reinterpret_cast<const float*>(s + kOffNode + 128);
-      // the leader decides whether another piece follows, so every warp runs
-      // the same number of named barriers (alternating words)
-      volatile int* more_s = reinterpret_cast<volatile int*>(s + kOffNode + 168);
-      const int max_pieces = 1 << (__ffs(~j) - 1);
-      float acc[64];
-#pragma unroll
-      for (int i = 0; i < 64; ++i) acc[i] = 0.f;
-      float r_end = 0.f;
-      for (int idx = 0; idx < max_pieces; ++idx) {
-        const int b = idx & 1;
-        wait_bar_w(c, B_PC_FULL0 + b, npc[b] & 1);
-        const float* d = pdesc + 4 * b;
-        r_end = d[1];
-        // decay from the piece's end to the end of tile j
-        const float sc = d[3] != 0.f ? 1.f : ex2((cs_end + d[0]) * kLog2e);
-        const unsigned char* src = s + (b ? kOffV : kOffK) + hf * kHalf + row * 128;
-#pragma unroll
-        for (int c8 = 0; c8 < 8; ++c8) {
-          const uint4 v = *reinterpret_cast<const uint4*>(src + ((c8 ^ (row & 7)) << 4));
-          const uint32_t* w = reinterpret_cast<const uint32_t*>(&v);
-#pragma unroll
-          for (int i = 0; i < 4; ++i) {
-            const float2 f = unpack_bf16x2(w[i]);
-            acc[c8 * 8 + 2 * i] = fmaf(sc, f.x, acc[c8 * 8 + 2 * i]);
-            acc[c8 * 8 + 2 * i + 1] = fmaf(sc, f.y, acc[c8 * 8 + 2 * i + 1]);
+          for (int c4 = 0; c4 < 4; ++c4) {
+            const int c8 = 4 * c32 + c4;
+            *reinterpret_cast<uint4*>(xrow + ((c8 ^ (row & 7)) << 4)) =
+                make_uint4(pack_bf16x2(v[8 * c4], v[8 * c4 + 1]), pack_bf16x2(v[8 * c4 + 2], v[8 * c4 + 3]),
+                           pack_bf16x2(v[8 * c4 + 4], v[8 * c4 + 5]), pack_bf16x2(v[8 * c4 + 6], v[8 * c4 + 7]));
           }
         }
-        if (leader)
-          more_s[idx & 1] = (d[3] != 0.f || d[2] == 0.f) && !*c.abort_s && idx + 1 < max_pieces ? 1 : 0;
-        __syncwarp();
-        named_bar_sync(1, kEpi);  // every row of the piece is read
-        if (leader) mbar_arrive(c.bars + B_PC_FREE0 + b);
-        ++npc[b];
-        if (!more_s[idx & 1]) break;
       }
+      fence_proxy_async_shared();
+      tc_fence_before();  // the accumulator is free once every thread is past this point
+      __syncwarp();
+      named_bar_sync(1, kEpi);
       if (leader) {
-        mbar_arrive(c.bars + B_KV_REL);
-        p.G[(size_t)bh * p.Nt + j] = cs_end + r_end;
-        gpub_s[0] = cs_end + r_end;
+        mbar_arrive(c.bars + B_R_FREE);
+        mbar_arrive(c.bars + B_LVLD_FREE);
+        mbar_arrive(c.bars + B_X_STAGED);
       }
-      stage(acc);
+      ++xs;
     }
 
     cs_prev = cs_t;
@@ -888,66 +776,154 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   }
 }
 
-// ------------------------------------------------------------------ store warp (warp 10)
-// Stores what the epilogue staged in X with the TMA, in the epilogue's order
-// (per step: the node F_j, or for odd j the raw state S_j; the previous
-// tile's output; for odd j the merged node F_j), hands X back once the copy
-// has read it, and publishes each node or raw state at gpu scope once its
-// store is complete.
-__device__ void store_warp(const Ctx& c, const CUtensorMap* to, const CUtensorMap* tf, const CUtensorMap* tr) {
+// ------------------------------------------------------------------ store warp (warp 2)
+// Stores each staged output with the TMA and hands the staging buffer back
+// once the copy has read it.
+__device__ void store_warp(const Ctx& c, const CUtensorMap* to) {
   const TcParams& p = *c.p;
-  const int total = p.BH * p.Nt;
-  const int n = tiles_of_cta(total);
+  const int n = tiles_of_cta(p.BH * p.Nt);
   const unsigned char* x = c.base + kOffX;
-  uint32_t xs = 0;
-  const volatile float* gpub_s = reinterpret_cast<const volatile float*>(c.base + kOffMisc + 20);
-  float g = 0.f;
-  auto store = [&](const CUtensorMap* map, int row0) {
-    wait_bar(c, B_X_STAGED, xs & 1);
-    g = *gpub_s;
+  for (int it = 1; it <= n; ++it) {
+    const int up = blockIdx.x + (it - 1) * gridDim.x;
+    wait_bar(c, B_X_STAGED, (it - 1) & 1);
     fence_proxy_async_shared();
-    tma_store_2d(map, x, 0, row0);
-    tma_store_2d(map, x + kHalf, 64, row0);
+    const int row0 = (up % p.BH) * p.T + (up / p.BH) * kTile;
+    tma_store_2d(to, x, 0, row0);
+    tma_store_2d(to, x + kHalf, 64, row0);
     bulk_commit();
     bulk_wait_read0();
     mbar_arrive(c.bars + B_X_FREE);
-    ++xs;
-  };
-  // the node's bytes (async proxy) are complete and ordered before the
-  // release of its word, which carries the log-decay total the epilogue left
-  // in shared memory before X_STAGED (read before X is handed back)
-  auto publish = [&](uint64_t* flags, size_t node, float g) {
-    bulk_wait0();
-    fence_proxy_async_global();
-    if (flags == p.flags && (long long)node == p.withhold) return;  // expiry test: nothing will publish it
-    st_release_u64(flags + node, ((uint64_t)p.token << 32) | __float_as_uint(g));
-  };
+  }
+  bulk_wait0();
+}
 
-  for (int it = 0; it <= n; ++it) {
+// ------------------------------------------------------------------ node warps (warps 12..15)
+// Per tile j, in order: the chunk state S_j is in the accumulator M once the
+// state product is done.  For odd j the Fenwick children F_{j-2^m}, m <
+// cto(j), are added in float32: each is waited for (its publication word),
+// loaded by TMA into the C buffer and added row by row into M with its decay
+// exp(dec_m), dec_m = the log decay from the end of the child's block to the
+// end of tile j.  Then F_j leaves M as bf16 through C (TMA store), M goes
+// back to the MMA, and once the store is complete F_j is published with its
+// log-decay total G_j.  Thread t = 32 (warp % 4) + lane owns TMEM lane t: row
+// d_v = t of the node.
+__device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, const CUtensorMap* tf) {
+  const TcParams& p = *c.p;
+  const int n = tiles_of_cta(p.BH * p.Nt);
+  const int q = warp & 3;
+  const int t = 32 * q + lane;
+  const bool leader = (warp == kNodeWarp0 && lane == 0);
+  const uint32_t tm = tmem + ((uint32_t)(32 * q) << 16) + kTmM;
+  unsigned char* s = c.base;
+  float* nq = reinterpret_cast<float*>(s + kOffMisc + 48);        // [4] quadrant sums
+  volatile float* gch = reinterpret_cast<volatile float*>(s + kOffNode + 176);  // child's log-decay total
+  unsigned char* cb = s + kOffC;
+  uint32_t cf = 0;     // child loads waited for
+  uint32_t armed = 0;  // child loads armed (the leader)
+  for (int it = 0; it < n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     const int bh = u % p.BH, j = u / p.BH;
     const size_t node_j = (size_t)bh * p.Nt + j;
-    if (it < n) {
-      store(j & 1 ? tr : tf, (int)(node_j * kD));
-      publish(j & 1 ? p.rflags : p.flags, node_j, g);
+    // the tile's log-decay total (also the barrier after which the previous
+    // node's store has completed and C is free)
+    float x = __ldg(p.log_alpha + (size_t)bh * p.T + (size_t)j * kTile + t);
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) nq[q] = x;
+    __syncwarp();
+    named_bar_sync(6, kNodeThreads);
+    const float cs_end = (nq[0] + nq[1]) + (nq[2] + nq[3]);
+    float D = cs_end;  // log decay from the end of the next child's block to the end of tile j
+    wait_bar_w(c, B_STATE_DONE, it & 1);
+    __syncwarp();
+    tc_fence_after();
+    const int cto = __ffs(~j) - 1;  // trailing ones of j
+    for (int m = 0; m < cto; ++m) {
+      const size_t child = node_j - ((size_t)1 << m);
+      if (leader) {
+        const uint64_t w = wait_flag(c, p.flags, child);
+        fence_proxy_async_global();
+        *gch = flag_g(w);
+        if (!*c.abort_s) {
+          mbar_arrive_expect_tx(c.bars + B_C_FULL, kTileBytes);
+          tma_load_2d(cb, tf, c.bars + B_C_FULL, 0, (int)(child * kD));
+          tma_load_2d(cb + kHalf, tf, c.bars + B_C_FULL, 64, (int)(child * kD));
+          ++armed;
+        }
+      }
+      wait_bar_w(c, B_C_FULL, cf & 1);
+      ++cf;
+      __syncwarp();
+      const float g = *gch;
+      const float sc = ex2(D * kLog2e);
+      // row t of the child, 16-byte chunk c8 of its 128-byte-swizzled tile
+#pragma unroll
+      for (int c32 = 0; c32 < 4; ++c32) {
+        float a[32];
+        tmem_ld32(tm + 32 * c32, a);
+        uint4 ch[4];
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const int c8 = 4 * c32 + v;
+          ch[v] = *reinterpret_cast<const uint4*>(cb + (c8 >> 3) * kHalf + t * 128 + (((c8 & 7) ^ (t & 7)) << 4));
+        }
+        tmem_ld_wait();
+#pragma unroll
+        for (int v = 0; v < 4; ++v) {
+          const uint32_t* w = reinterpret_cast<const uint32_t*>(&ch[v]);
+#pragma unroll
+          for (int e = 0; e < 4; ++e) {
+            const float2 f = unpack_bf16x2(w[e]);
+            a[8 * v + 2 * e] = fmaf(sc, f.x, a[8 * v + 2 * e]);
+            a[8 * v + 2 * e + 1] = fmaf(sc, f.y, a[8 * v + 2 * e + 1]);
+          }
+        }
+        tmem_st32(tm + 32 * c32, reinterpret_cast<const uint32_t*>(a));
+      }
+      tmem_st_wait();
+      __syncwarp();
+      named_bar_sync(6, kNodeThreads);  // every row of the child is read: C is free
+      D += g;
     }
-    if (it >= 1) {
-      const int up = u - gridDim.x;
-      store(to, (up % p.BH) * p.T + (up / p.BH) * kTile);
+    const float G = D;  // cs_end plus the children's totals
+    // F_j as bf16 into C (row t), then M is free and the node is stored
+#pragma unroll
+    for (int c32 = 0; c32 < 4; ++c32) {
+      float a[32];
+      tmem_ld32(tm + 32 * c32, a);
+      tmem_ld_wait();
+#pragma unroll
+      for (int v = 0; v < 4; ++v) {
+        const int c8 = 4 * c32 + v;
+        *reinterpret_cast<uint4*>(cb + (c8 >> 3) * kHalf + t * 128 + (((c8 & 7) ^ (t & 7)) << 4)) =
+            make_uint4(pack_bf16x2(a[8 * v], a[8 * v + 1]), pack_bf16x2(a[8 * v + 2], a[8 * v + 3]),
+                       pack_bf16x2(a[8 * v + 4], a[8 * v + 5]), pack_bf16x2(a[8 * v + 6], a[8 * v + 7]));
+      }
     }
-    if (it < n && (j & 1)) {
-      store(tf, (int)(node_j * kD));
-      publish(p.flags, node_j, g);
+    fence_proxy_async_shared();
+    tc_fence_before();
+    __syncwarp();
+    named_bar_sync(6, kNodeThreads);
+    if (leader) {
+      mbar_arrive(c.bars + B_M_FREE);
+      p.G[node_j] = G;
+      tma_store_2d(tf, cb, 0, (int)(node_j * kD));
+      tma_store_2d(tf, cb + kHalf, 64, (int)(node_j * kD));
+      bulk_commit();
+      bulk_wait0();  // complete, before C is reused and before the node is published
+      fence_proxy_async_global();
+      if ((long long)node_j != p.withhold)  // (expiry test: a node nothing will publish)
+        st_release_u64(p.flags + node_j, ((uint64_t)p.token << 32) | __float_as_uint(G));
     }
   }
-  bulk_wait0();
+  if (leader && armed > 0) drain_bar(c, B_C_FULL, (armed - 1) & 1);  // (a copy armed before an abort)
 }
 
 template <bool kCont>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf,
-                  const __grid_constant__ CUtensorMap to, const __grid_constant__ CUtensorMap tr, TcParams p) {
+                  const __grid_constant__ CUtensorMap to, TcParams p) {
   extern __shared__ __align__(1024) unsigned char smem_raw[];
   // the 128-byte swizzle of the operand tiles assumes a 1024-aligned base;
   // the budget leaves no room to realign, so refuse (all threads) otherwise
@@ -971,8 +947,8 @@ __global__ void __launch_bounds__(kThreads, 1)
     prefetch_tmap(&tv);
     prefetch_tmap(&tf);
     prefetch_tmap(&to);
-    prefetch_tmap(&tr);
   }
+  __syncwarp();
   if (warp == 1) {
     tmem_alloc(tmem_slot, 512);
     tmem_relinquish();
@@ -982,16 +958,22 @@ __global__ void __launch_bounds__(kThreads, 1)
   tc_fence_after();
   const uint32_t tmem = *tmem_slot;
 
-  if (warp == 0) {
-    if (lane == 0) producer_levels<kCont>(c, &tf);
-    else if (lane == 1) producer_kvq(c, &tq, &tk, &tv);
-  } else if (warp == kPieceWarp) {
-    if (lane == 0) producer_pieces(c, &tf, &tr);
-  } else if (warp == 1) {
-    if (lane == 0) mma_issuer<kCont>(c, tmem);
-  } else if (warp == kPubWarp) {
-    if (lane == 0) store_warp(c, &to, &tf, &tr);
+  // registers by warpgroup: the single-thread roles give theirs to the
+  // epilogue (88 + 2 x 160 + 104 = 512 per four threads: the 128 of the launch)
+  const int wg = warp >> 2;
+  if (wg == 0) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
+    if (lane == 0) {
+      if (warp == 0) producer_kvq(c, &tq, &tk, &tv);
+      else if (warp == 1) mma_issuer<kCont>(c, tmem);
+      else if (warp == 2) store_warp(c, &to);
+      else producer_levels<kCont>(c, &tf);
+    }
+  } else if (wg == 3) {
+    asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
+    node_warps(c, tmem, warp, lane, &tf);
   } else {
+    asm volatile("setmaxnreg.inc.sync.aligned.u32 160;\n" ::: "memory");
     epilogue<kCont>(c, tmem, warp, lane);
   }
   __syncwarp();
@@ -1046,7 +1028,7 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
 // ------------------------------------------------------------------ host side
 struct TcPlan {
   int Nt;
-  size_t off_F, off_R, off_G, off_flags, off_rflags, total;
+  size_t off_F, off_G, off_flags, total;
   size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
@@ -1059,10 +1041,8 @@ TcPlan tc_plan(const ll_shape& s) {
   const size_t nodes = BH * p.Nt;
   size_t off = 0;
   p.off_F = off;      off = align_up(off + (nodes + BH * kPreSlots) * kD * kD * 2, 1024);
-  p.off_R = off;      off = align_up(off + nodes * kD * kD * 2, 1024);
   p.off_G = off;      off = align_up(off + nodes * 4, 256);
   p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
-  p.off_rflags = off; off = align_up(off + nodes * 8, 256);
   p.total = off;
   const size_t slots = (size_t)std::max(s.Ls, 1);
   p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
@@ -1139,10 +1119,9 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
     return LL_ERR_INVALID_ARG;
   const uint64_t rows = (uint64_t)BH * stride;
   const uint64_t node_rows = ((uint64_t)BH * plan.Nt + (uint64_t)BH * kPreSlots) * kD;
-  CUtensorMap tq, tk, tv, tf, to, tr;
+  CUtensorMap tq, tk, tv, tf, to;
   if (!make_map(&tq, a.q, rows) || !make_map(&tk, a.k, rows) || !make_map(&tv, a.v, rows) ||
-      !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows) ||
-      !make_map(&tr, ws + plan.off_R, node_rows))
+      !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows))
     return LL_ERR_CUDA;
 
   TcParams p;
@@ -1154,7 +1133,6 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.F = reinterpret_cast<__nv_bfloat16*>(ws + plan.off_F);
   p.G = reinterpret_cast<float*>(ws + plan.off_G);
   p.flags = reinterpret_cast<uint64_t*>(ws + plan.off_flags);
-  p.rflags = reinterpret_cast<uint64_t*>(ws + plan.off_rflags);
   p.abort_word = p.flags + (size_t)BH * plan.Nt;
   p.token = next_token();
   p.BH = BH;
@@ -1181,7 +1159,7 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   const long long tiles = (long long)BH * plan.Nt;
   const int grid = (int)std::min<long long>(tiles, (long long)sms * per_sm);
 
-  void* args[] = {&tq, &tk, &tv, &tf, &to, &tr, &p};
+  void* args[] = {&tq, &tk, &tv, &tf, &to, &p};
   LL_CUDA_OK(cudaLaunchCooperativeKernel(kern, dim3(grid), dim3(kThreads), args, kSmemBytes,
                                          a.stream));
   if (a.state_out && a.state_in) {
