@@ -32,4 +32,4 @@ Readings taken where the pages are silent (each is stated where it is used):
      versus B is unpinned by the pages.
 """
 
-from . import partition, mamba2, gdn, decode, backward  # noqa: F401
+from . import partition, mamba2, gdn, decode, backward, level_decay  # noqa: F401

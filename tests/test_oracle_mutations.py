@@ -145,3 +145,102 @@ def test_gdn_decode_write_transitioned_is_caught(monkeypatch):
 def test_gdn_decode_carry_to_wrong_level_is_caught(monkeypatch):
     monkeypatch.setattr(gdn, "gdn_level_step", _step_variant(carry_shift=1))
     assert not _gdn_decode_vs_dense_ok()
+
+
+# ----------------------------------------------------------------------------
+# the per-level-decay variant
+# ----------------------------------------------------------------------------
+def _ld_case(T=20, seed=3):
+    rng = np.random.default_rng(seed)
+    L = levels_needed(T)
+    q = rng.standard_normal((T, 3))
+    k = rng.standard_normal((T, 3))
+    v = rng.standard_normal((T, 2))
+    la = -rng.random((T, L))
+    lam = np.log1p(np.exp(rng.standard_normal((T, L))))
+    return q, k, v, la, lam
+
+
+def _ld_pins_ok():
+    from oracle import level_decay as ld
+    T = 24
+    L = levels_needed(T)
+    c = -0.05 * np.arange(L) - 0.01
+    la = np.tile(c, (T, 1))
+    want = np.zeros((T, T))
+    for t in range(T):
+        for s in range(t + 1):
+            if s == t:
+                want[t, s] = 1.0
+                continue
+            l = (t ^ s).bit_length()
+            e = sum(c[m] * 2 ** (m - 1) for m in range(1, l) if not (s >> (m - 1)) & 1)
+            want[t, s] = np.exp(e + c[l] * ((t % 2 ** (l - 1)) + 1))
+    closed = np.allclose(ld.decay_matrix(la), want, rtol=1e-12)
+    q, k, v, la, lam = _ld_case()
+    routes = np.allclose(ld.forward_dense(q, k, v, la, lam), ld.forward_recurrent(q, k, v, la, lam)[0],
+                         rtol=1e-10, atol=1e-12)
+    return closed and routes
+
+
+def test_level_decay_unmutated_pins_pass():
+    assert _ld_pins_ok()
+
+
+def test_level_decay_at_the_query_level_is_caught(monkeypatch):
+    # every step of (s, t] decayed at the rate of level(t, s), the level the
+    # key has for the query, instead of the level it occupies at each step
+    from oracle import level_decay as ld
+
+    def bad(la):
+        la = np.asarray(la, np.float64)
+        T = la.shape[0]
+        out = np.eye(T)
+        for t in range(T):
+            for s in range(t):
+                lv = (t ^ s).bit_length()
+                out[t, s] = np.exp(la[s + 1:t + 1, lv].sum())
+        return out
+    monkeypatch.setattr(ld, "decay_matrix", bad)
+    assert not _ld_pins_ok()
+
+
+def test_level_decay_one_step_late_is_caught(monkeypatch):
+    # the level of key s at step r taken as its level at step r - 1
+    from oracle import level_decay as ld
+
+    def bad(la):
+        la = np.asarray(la, np.float64)
+        T = la.shape[0]
+        out = np.eye(T)
+        for s in range(T):
+            acc = 0.0
+            for r in range(s + 1, T):
+                acc += la[r, mamba2.level_array(r - 1, s) if r - 1 > s else 1]
+                out[r, s] = np.exp(acc)
+        return out
+    monkeypatch.setattr(ld, "decay_matrix", bad)
+    assert not _ld_pins_ok()
+
+
+def test_level_decay_rate_index_off_by_one_is_caught(monkeypatch):
+    # recurrent form: the state of level l decayed at the rate of level l + 1
+    from oracle import level_decay as ld
+
+    def bad(states, t, q_t, k_t, v_t, la_t, lam_t):
+        for lv in list(states):
+            states[lv] = states[lv] * float(np.exp(la_t[min(lv + 1, len(la_t) - 1)]))
+        states[0] = np.outer(v_t, k_t)
+        o = np.zeros(v_t.shape[0])
+        for lv, S in states.items():
+            o += lam_t[lv] * (S @ q_t)
+        j = 0
+        while (t >> j) & 1:
+            j += 1
+        merged = states.pop(0)
+        for lv in range(1, j + 1):
+            merged = merged + states.pop(lv)
+        states[j + 1] = merged
+        return o
+    monkeypatch.setattr(ld, "fenwick_step", bad)
+    assert not _ld_pins_ok()
