@@ -62,6 +62,7 @@ METRICS = {
     "gdn_decode": "log-linear Gated DeltaNet Fenwick decode tokens/s (B=64, H=32, d=128, 17 levels); "
                   "% of HBM roofline",
     "mamba2_bwd": "log-linear Mamba-2 bwd tokens/s (dq, dk, dv, dlog_alpha, dlam) at T=16K,H=16,d=128",
+    "level_decay": "log-linear Mamba-2 fwd with one decay per level, tokens/s at T=16K,H=16,d=128",
 }
 
 
@@ -80,6 +81,8 @@ def algorithmic_bytes(cfg) -> int:
         per_bh = cfg["T"] * ((2 * dk + 2 * dv) * b_io + (2 * dk + dv) * b_io + 2 * (4 + 4 * cfg["L"]))
         return per_bh * cfg["B"] * cfg["H"]
     per_bh = cfg["T"] * (3 * cfg["dk"] * b_io + 4 + 4 * cfg["L"] + cfg["dv"] * b_io)
+    if cfg["kind"] == "level_decay":  # log_alpha has L columns
+        per_bh += cfg["T"] * 4 * (cfg["L"] - 1)
     if cfg["kind"] in ("gdn", "gdn_b"):
         per_bh += cfg["T"] * 4
     if cfg["kind"] == "mamba2_cont":  # the prefix states read, the states of t0 + T written (float32)
@@ -179,6 +182,7 @@ KERNEL_SOURCES = {
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
     "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
     "mamba2_bwd": ("bwd_tc.cu", "bwd.cuh", "common.cuh", "sm100.cuh"),  # dominant: the query-side kernel
+    "level_decay": ("fwd_level_decay.cu", "level_decay.cuh", "common.cuh"),
 }
 
 
@@ -293,6 +297,11 @@ def _oracle_worker(job):
         q, k, v, la, lam = _W["x"]
         mamba2.forward_rows(q, k, v, la, lam, job)
         return float(len(job))
+    if cfg["kind"] == "level_decay":
+        from oracle import level_decay
+        q, k, v, la, lam = _W["x"]
+        level_decay.forward_rows(q, k, v, la, lam, job)
+        return float(len(job))
     if cfg["kind"] == "gdn":
         from oracle import gdn
         q, k, v, la, lam, beta = _W["x"]
@@ -345,7 +354,7 @@ def oracle_pool(cores: int, cfg: dict, tag: str = "oracle"):
 def oracle_jobs(cfg, cores, size, seed):
     import numpy as np
     rng = np.random.default_rng(seed)
-    if cfg["kind"] in ("mamba2", "gdn", "mamba2_bwd"):
+    if cfg["kind"] in ("mamba2", "gdn", "mamba2_bwd", "level_decay"):
         return [sorted(int(x) for x in rng.integers(0, cfg["T"], size)) for _ in range(cores)]
     if cfg["kind"] == "mamba2_cont":  # rows of the new tokens, positions t0 .. t0 + T - 1
         return [sorted(int(x) for x in rng.integers(cfg["t0"], cfg["t0"] + cfg["T"], size)) for _ in range(cores)]
@@ -372,6 +381,9 @@ def calibrate(pool, cfg, cores, budget_s):
 def sample_desc(cfg, size):
     if cfg["kind"] == "mamba2":
         return f"{size} uniformly drawn query rows per process of the row-restricted dense float64 form"
+    if cfg["kind"] == "level_decay":
+        return (f"{size} uniformly drawn query rows per process of the row-restricted float64 form with one "
+                "decay per level")
     if cfg["kind"] == "mamba2_cont":
         return (f"{size} uniformly drawn rows of the new tokens per process of the row-restricted dense float64 "
                 "form over the whole sequence")
@@ -416,6 +428,7 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
     gdn = cfg["kind"] in ("gdn", "gdn_b")
     reading_b = cfg["kind"] == "gdn_b"
     cont = cfg["kind"] == "mamba2_cont"
+    per_level = cfg["kind"] == "level_decay"
     inp_host = synth.make_inputs(cfg, tag=f"rank{rank}" if rank else "")
     names = ("q", "k", "v", "log_alpha", "lam") + (("beta",) if gdn else ())
     host = {n: inp_host[n].pin_memory() for n in names}
@@ -434,6 +447,9 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
         sc_in = keep.expand(Bn, H, Ls).contiguous()
         st_out, sc_out = torch.empty_like(st_in), torch.empty_like(sc_in)
         launches = 5  # prefix nodes, forward, segment export, segment decay, merge
+    elif per_level:
+        ws = binding.alloc_workspace(binding.ll_attn_fwd_level_decay_workspace_size(shape), dev)
+        launches = binding.ll_attn_fwd_level_decay_launches(shape)
     elif reading_b:
         ws = binding.alloc_workspace(binding.ll_gdn_fwd_b_workspace_size(shape), dev)
         launches = 2 + binding.ll_attn_fwd_launches(shape)
@@ -450,6 +466,9 @@ def forward_workload(cfg, dev, rank, binding, synth, torch):
         if cont:
             binding.ll_attn_fwd_cont(t0, st_in, sc_in, x["q"], x["k"], x["v"], x["log_alpha"], x["lam"],
                                      cfg["chunk"], o=out, state_out=st_out, scale_out=sc_out, workspace=ws)
+        elif per_level:
+            binding.ll_attn_fwd_level_decay(x["q"], x["k"], x["v"], x["log_alpha"], x["lam"], cfg["chunk"], o=out,
+                                            workspace=ws)
         elif reading_b:
             binding.ll_gdn_fwd_b(x["q"], x["k"], x["v"], x["log_alpha"], x["beta"], x["lam"], cfg["chunk"], o=out,
                                  workspace=ws)
@@ -800,7 +819,7 @@ def roofline_of(cfg, workload, w, mean_ms, dev, torch):
                 "traffic": traffic, "peak_source": f"{src} (HBM copy)", "algorithmic_bytes_per_launch": abytes,
                 "launches_per_step": w["launches"], "kernel": kname}
     abytes, aflops = w["abytes"], w["aflops"]
-    if kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg):
+    if (kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg)) or kind == "level_decay":
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
         achieved = aflops / (mean_ms * 1e-3) / 1e12

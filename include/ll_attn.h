@@ -202,6 +202,46 @@ LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const flo
                                   const float* log_alpha, const float* lam, void* o, float* state_out,
                                   float* scale_out, void* workspace, size_t ws_bytes, void* stream);
 
+/* ---- one decay per level ----
+ * "Log-Linear Attention" study note §7 "Follow-up design" lists a learned
+ * memory decay per level and defines nothing more.  The reading implemented:
+ * the memory of level l decays at its own rate alpha_t^(l), so at every step
+ * r a key decays at the rate of the level it occupies then,
+ *   o_t = sum_{s<=t} lam_t[l(t,s)] prod_{r in (s,t]} alpha_r^(l(r,s)) (q_t.k_s) v_s,
+ * which is the recurrent form of §3-3 with one decay per level state (the
+ * carry-merge unchanged).  With every column of log_alpha equal it is
+ * ll_attn_fwd. */
+
+/* Bytes of workspace ll_attn_fwd_level_decay needs (0 on an invalid shape, or
+ * when T needs more than 4096 chunks of the effective chunk length). */
+LL_API size_t ll_attn_fwd_level_decay_workspace_size(const ll_shape* shape);
+
+/* Kernel launches of one ll_attn_fwd_level_decay call (0 when unsupported). */
+LL_API int ll_attn_fwd_level_decay_launches(const ll_shape* shape);
+
+/* The forward with one decay per level.  Arguments as ll_attn_fwd, except
+ *   log_alpha  [B,H,T,L]  float32: log_alpha[t][l] is the log decay of level
+ *              l at step t (column 0 is never read: a key is at level 0 only
+ *              at its own step, which applies no decay).
+ * state_out / scale_out: the level states of position T as in ll_attn_fwd
+ * (each bucket decayed to token T-1 under this rule), ready for
+ * ll_attn_decode_step_level_decay at t = T.
+ * Runs on the CUDA cores (float32 FMA, float64 running sums of the log
+ * decays) for every io dtype and head size; LL_ERR_UNSUPPORTED beyond 4096
+ * chunks. */
+LL_API ll_status ll_attn_fwd_level_decay(const ll_shape* shape, const void* q, const void* k, const void* v,
+                                         const float* log_alpha, const float* lam, void* o, float* state_out,
+                                         float* scale_out, void* workspace, size_t ws_bytes, void* stream);
+
+/* One decode step with one decay per level.  Arguments as
+ * ll_attn_decode_step, except log_alpha [B,H,Ls+1] float32 (entry l for level
+ * l; entry 0 is never read): the lazy scale of slot i is multiplied by
+ * alpha_t^(i+1). */
+LL_API ll_status ll_attn_decode_step_level_decay(int B, int H, int dk, int dv, int Ls, ll_dtype io,
+                                                 const int64_t* t, const void* q, const void* k, const void* v,
+                                                 const float* log_alpha, const float* lam, float* states,
+                                                 float* scales, void* o, void* stream);
+
 /* Bytes of workspace ll_attn_bwd needs for `shape` (0 on an invalid shape or
  * shape->Ls != 0). */
 LL_API size_t ll_attn_bwd_workspace_size(const ll_shape* shape);

@@ -27,6 +27,8 @@ SYMBOLS = ("ll_version", "ll_status_str", "ll_last_device_error", "ll_attn_fwd_w
            "ll_attn_fwd", "ll_attn_fwd_noalloc", "ll_attn_decode_step", "ll_gdn_fwd_workspace_size", "ll_gdn_fwd",
            "ll_gdn_decode_step", "ll_gdn_fwd_b_workspace_size", "ll_gdn_fwd_b", "ll_attn_fwd_cont_workspace_size",
            "ll_attn_fwd_cont", "ll_attn_bwd_workspace_size", "ll_attn_bwd_launches", "ll_attn_bwd",
+           "ll_attn_fwd_level_decay_workspace_size", "ll_attn_fwd_level_decay_launches", "ll_attn_fwd_level_decay",
+           "ll_attn_decode_step_level_decay",
            # test hooks (include/ll_attn_test.h)
            "ll_test_fwd_withhold_node")
 
@@ -72,6 +74,15 @@ def lib() -> ctypes.CDLL:
     L.ll_attn_fwd_noalloc.argtypes = [shp, vp, vp, vp, fp, fp, vp, fp, fp, vp]
     L.ll_attn_decode_step.restype = i32
     L.ll_attn_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp, vp]
+    L.ll_attn_decode_step_level_decay.restype = i32
+    L.ll_attn_decode_step_level_decay.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp,
+                                                  vp]
+    L.ll_attn_fwd_level_decay_workspace_size.restype = sz
+    L.ll_attn_fwd_level_decay_workspace_size.argtypes = [shp]
+    L.ll_attn_fwd_level_decay_launches.restype = i32
+    L.ll_attn_fwd_level_decay_launches.argtypes = [shp]
+    L.ll_attn_fwd_level_decay.restype = i32
+    L.ll_attn_fwd_level_decay.argtypes = [shp, vp, vp, vp, fp, fp, vp, fp, fp, vp, sz, vp]
     L.ll_gdn_decode_step.restype = i32
     L.ll_gdn_decode_step.argtypes = [i32, i32, i32, i32, i32, i32, vp, vp, vp, vp, fp, fp, fp, fp, vp, vp]
     L.ll_gdn_fwd_workspace_size.restype = sz
@@ -268,6 +279,71 @@ def ll_attn_decode_step(t, q, k, v, log_alpha, lam, states, scales, *, o=None):
     st = lib().ll_attn_decode_step(B, H, dk, dv, Ls, io, _ptr(t), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha),
                                    _ptr(lam), _ptr(states), _ptr(scales), _ptr(o), _stream(q.device))
     _check(st, "ll_attn_decode_step")
+    return o
+
+
+def ll_attn_fwd_level_decay_workspace_size(shape: ll_shape) -> int:
+    return int(lib().ll_attn_fwd_level_decay_workspace_size(ctypes.byref(shape)))
+
+
+def ll_attn_fwd_level_decay_launches(shape: ll_shape) -> int:
+    return int(lib().ll_attn_fwd_level_decay_launches(ctypes.byref(shape)))
+
+
+def ll_attn_fwd_level_decay(q, k, v, log_alpha, lam, chunk: int, *, o=None, state_out=None, scale_out=None,
+                            workspace=None):
+    """Forward with one decay per level.  As ll_attn_fwd, except log_alpha
+    [B,H,T,L] float32 (column l is level l's log decay; column 0 unused)."""
+    B, H, T, dk = q.shape
+    dv = v.shape[-1]
+    L = lam.shape[-1]
+    io = _io(q.dtype)
+    for x, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(x, n, q.dtype)
+    _need(log_alpha, "log_alpha", torch.float32)
+    _need(lam, "lam", torch.float32)
+    if tuple(log_alpha.shape) != tuple(lam.shape):
+        raise ValueError("log_alpha must have the shape of lam, [B,H,T,L]")
+    Ls = 0
+    if state_out is not None:
+        _need(state_out, "state_out", torch.float32)
+        _need(scale_out, "scale_out", torch.float32)
+        Ls = state_out.shape[2]
+    shape = make_shape(B, H, T, dk, dv, L, chunk, Ls, io)
+    if o is None:
+        o = torch.empty(B, H, T, dv, dtype=q.dtype, device=q.device)
+    _need(o, "o", q.dtype)
+    if workspace is None:
+        workspace = alloc_workspace(ll_attn_fwd_level_decay_workspace_size(shape), q.device)
+    st = lib().ll_attn_fwd_level_decay(ctypes.byref(shape), _ptr(q), _ptr(k), _ptr(v), _ptr(log_alpha), _ptr(lam),
+                                       _ptr(o), _ptr(state_out), _ptr(scale_out), _ptr(workspace),
+                                       ctypes.c_size_t(workspace.numel()), _stream(q.device))
+    _check(st, "ll_attn_fwd_level_decay")
+    return o
+
+
+def ll_attn_decode_step_level_decay(t, q, k, v, log_alpha, lam, states, scales, *, o=None):
+    """One decode step with one decay per level: as ll_attn_decode_step, except
+    log_alpha [B,H,Ls+1] (entry l for level l; entry 0 unused)."""
+    B, H, dk = q.shape
+    dv = v.shape[-1]
+    Ls = states.shape[2]
+    io = _io(q.dtype)
+    _need(t, "t", torch.int64)
+    for x, n in ((q, "q"), (k, "k"), (v, "v")):
+        _need(x, n, q.dtype)
+    _need(log_alpha, "log_alpha", torch.float32)
+    _need(lam, "lam", torch.float32)
+    _need(states, "states", torch.float32)
+    _need(scales, "scales", torch.float32)
+    if tuple(log_alpha.shape) != (B, H, Ls + 1):
+        raise ValueError("log_alpha must be [B,H,Ls+1]")
+    if o is None:
+        o = torch.empty(B, H, dv, dtype=q.dtype, device=q.device)
+    st = lib().ll_attn_decode_step_level_decay(B, H, dk, dv, Ls, io, _ptr(t), _ptr(q), _ptr(k), _ptr(v),
+                                               _ptr(log_alpha), _ptr(lam), _ptr(states), _ptr(scales), _ptr(o),
+                                               _stream(q.device))
+    _check(st, "ll_attn_decode_step_level_decay")
     return o
 
 

@@ -6,6 +6,7 @@
 #include <mutex>
 
 #include "bwd.cuh"
+#include "level_decay.cuh"
 
 namespace llattn {
 
@@ -410,6 +411,58 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
   if (!ew) return LL_ERR_CUDA;
   return decode_launch(B, H, dk, dv, Ls, io, t, q, k, v, log_alpha, lam, states, scales, o,
                        static_cast<cudaStream_t>(stream), ew);
+}
+
+size_t ll_attn_fwd_level_decay_workspace_size(const ll_shape* s) {
+  if (check_shape(s) != LL_OK) return 0;
+  return fwd_level_decay_workspace(*s);
+}
+
+int ll_attn_fwd_level_decay_launches(const ll_shape* s) {
+  if (check_shape(s) != LL_OK || fwd_level_decay_workspace(*s) == 0) return 0;
+  return fwd_level_decay_launches(*s);
+}
+
+ll_status ll_attn_fwd_level_decay(const ll_shape* s, const void* q, const void* k, const void* v,
+                                  const float* log_alpha, const float* lam, void* o, float* state_out,
+                                  float* scale_out, void* workspace, size_t ws_bytes, void* stream) {
+  ll_status st = check_shape(s);
+  if (st != LL_OK) return st;
+  if (!q || !k || !v || !log_alpha || !lam || !o) return LL_ERR_INVALID_ARG;
+  if (!aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) || !aligned16(lam) ||
+      !aligned16(o))
+    return LL_ERR_INVALID_ARG;
+  if ((state_out == nullptr) != (scale_out == nullptr)) return LL_ERR_INVALID_ARG;
+  if (state_out) {
+    if (s->Ls < 1 || !aligned16(state_out) || !aligned16(scale_out)) return LL_ERR_INVALID_ARG;
+    int need = 0;
+    for (unsigned x = (unsigned)s->T; x; x >>= 1) ++need;  // bit_length(T)
+    if (s->Ls < need) return LL_ERR_INVALID_ARG;
+  }
+  const size_t need_ws = fwd_level_decay_workspace(*s);
+  if (need_ws == 0) return LL_ERR_UNSUPPORTED;
+  if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
+  if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
+  FwdArgs a{*s, q, k, v, log_alpha, lam, nullptr, o, state_out, scale_out, workspace, ws_bytes,
+            static_cast<cudaStream_t>(stream), err_word()};
+  if (!a.err) return LL_ERR_CUDA;
+  return fwd_level_decay_launch(a);
+}
+
+ll_status ll_attn_decode_step_level_decay(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,
+                                          const void* q, const void* k, const void* v, const float* log_alpha,
+                                          const float* lam, float* states, float* scales, void* o, void* stream) {
+  if (B < 1 || H < 1 || Ls < 1 || Ls > 62) return LL_ERR_INVALID_ARG;
+  if (io != LL_F32 && io != LL_BF16) return LL_ERR_INVALID_ARG;
+  if (!head_dim_ok(dk) || !head_dim_ok(dv)) return LL_ERR_UNSUPPORTED;
+  if (!t || !q || !k || !v || !log_alpha || !lam || !states || !scales || !o) return LL_ERR_INVALID_ARG;
+  if (!aligned16(t) || !aligned16(q) || !aligned16(k) || !aligned16(v) || !aligned16(log_alpha) ||
+      !aligned16(lam) || !aligned16(states) || !aligned16(scales) || !aligned16(o))
+    return LL_ERR_INVALID_ARG;
+  unsigned* ew = err_word();
+  if (!ew) return LL_ERR_CUDA;
+  return decode_level_decay_launch(B, H, dk, dv, Ls, io, t, q, k, v, log_alpha, lam, states, scales, o,
+                                   static_cast<cudaStream_t>(stream), ew);
 }
 
 size_t ll_attn_bwd_workspace_size(const ll_shape* s) {

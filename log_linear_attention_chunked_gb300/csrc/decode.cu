@@ -4,7 +4,8 @@
 //
 // Per (b, h), at position t, with stored slots i = level i+1 (true state =
 // scale_i * S_i; non-empty slots are the set bits of t, decayed to t-1):
-//   g_i   = scale_i * alpha_t                       (lazy decay of every level)
+//   g_i   = scale_i * alpha_t                       (lazy decay of every level;
+//           with one decay per level, alpha_t^(i+1) for slot i)
 //   o_t   = lam_0 (q.k) v + sum_{i: bit i of t} lam_{i+1} g_i S_i q
 //   j     = ctz(t+1): slots 0..j-1 are full and merge into the empty slot j:
 //           S_j = v k^T + sum_{i<j} g_i S_i,  scale_j = 1,  scales 0..j-1 = 0,
@@ -13,7 +14,7 @@
 // is written.  One CTA per (b, h); each warp owns rows of dv, each lane dk/32
 // consecutive columns (128-bit loads for dk = 128), and all non-empty levels
 // of a row are loaded before any is used so their loads are in flight together.
-#include "common.cuh"
+#include "level_decay.cuh"
 
 namespace llattn {
 
@@ -54,7 +55,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int 
                                                              const float* __restrict__ log_alpha,
                                                              const float* __restrict__ lam, float* __restrict__ states,
                                                              float* __restrict__ scales, IO* __restrict__ o,
-                                                             unsigned* __restrict__ err) {
+                                                             unsigned* __restrict__ err, int per_level) {
   using V = typename Vec<DK>::T;
   constexpr int NV = Vec<DK>::n;
   __shared__ int slot_of[kMaxSlots];
@@ -72,7 +73,8 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int 
     return;
   }
   const int j = __ffsll(t + 1) - 1;  // trailing ones of t
-  const float alpha = expf(log_alpha[bh]);
+  // log_alpha is [B,H] or, with one decay per level, [B,H,Ls+1] (entry l for level l)
+  const float* la_bh = log_alpha + (size_t)bh * (per_level ? Ls + 1 : 1);
   const float* lam_bh = lam + (size_t)bh * (Ls + 1);
   float* sc = scales + (size_t)bh * Ls;
   if (warp == 0) {  // the non-empty slots, compacted in order; one lane per slot, loads in parallel
@@ -82,7 +84,7 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int 
       const bool set = i < Ls && ((t >> i) & 1);
       float g = 0.f, lm = 0.f;
       if (set) {
-        g = sc[i] * alpha;
+        g = sc[i] * expf(la_bh[per_level ? i + 1 : 0]);
         lm = lam_bh[i + 1];
       }
       const unsigned m = __ballot_sync(0xffffffffu, set);
@@ -168,10 +170,10 @@ __global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int 
 template <typename IO, int DK>
 ll_status launch(int B, int H, int dv, int Ls, const int64_t* t, const void* q, const void* k, const void* v,
                  const float* log_alpha, const float* lam, float* states, float* scales, void* o, cudaStream_t stream,
-                 unsigned* err) {
+                 unsigned* err, int per_level) {
   decode_kernel<IO, DK><<<B * H, kWarps * 32, 0, stream>>>(
       H, dv, Ls, t, static_cast<const IO*>(q), static_cast<const IO*>(k), static_cast<const IO*>(v), log_alpha, lam,
-      states, scales, static_cast<IO*>(o), err);
+      states, scales, static_cast<IO*>(o), err, per_level);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
 }
@@ -179,12 +181,12 @@ ll_status launch(int B, int H, int dv, int Ls, const int64_t* t, const void* q, 
 template <typename IO>
 ll_status launch_io(int B, int H, int dk, int dv, int Ls, const int64_t* t, const void* q, const void* k,
                     const void* v, const float* log_alpha, const float* lam, float* states, float* scales, void* o,
-                    cudaStream_t stream, unsigned* err) {
+                    cudaStream_t stream, unsigned* err, int pl) {
   switch (dk) {
-    case 128: return launch<IO, 128>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
-    case 64: return launch<IO, 64>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
-    case 32: return launch<IO, 32>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
-    case 16: return launch<IO, 16>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
+    case 128: return launch<IO, 128>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, pl);
+    case 64: return launch<IO, 64>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, pl);
+    case 32: return launch<IO, 32>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, pl);
+    case 16: return launch<IO, 16>(B, H, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, pl);
   }
   return LL_ERR_UNSUPPORTED;
 }
@@ -196,8 +198,18 @@ ll_status decode_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const
                         float* scales, void* o, cudaStream_t stream, unsigned* err) {
   if ((long long)B * H > 0x7fffffffll) return LL_ERR_UNSUPPORTED;
   if (io == LL_F32)
-    return launch_io<float>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
-  return launch_io<__nv_bfloat16>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err);
+    return launch_io<float>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, 0);
+  return launch_io<__nv_bfloat16>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, 0);
+}
+
+ll_status decode_level_decay_launch(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,
+                                    const void* q, const void* k, const void* v, const float* log_alpha,
+                                    const float* lam, float* states, float* scales, void* o, cudaStream_t stream,
+                                    unsigned* err) {
+  if ((long long)B * H > 0x7fffffffll) return LL_ERR_UNSUPPORTED;
+  if (io == LL_F32)
+    return launch_io<float>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, 1);
+  return launch_io<__nv_bfloat16>(B, H, dk, dv, Ls, t, q, k, v, log_alpha, lam, states, scales, o, stream, err, 1);
 }
 
 }  // namespace llattn

@@ -43,6 +43,10 @@ WORKLOADS = {
     # backward of the long-context forward: its inputs plus an upstream gradient of o
     "mamba2_bwd_bf16_t16k": dict(kind="mamba2_bwd", B=1, H=16, T=16384, dk=128, dv=128, chunk=64, L=15,
                                  io="bf16", seed=2, shift=0.0),
+    # one decay per level: the long-context forward's shape, log_alpha drawn
+    # per token and level with the base distribution
+    "level_decay_bf16_t16k": dict(kind="level_decay", B=1, H=16, T=16384, dk=128, dv=128, chunk=64, L=15,
+                                  io="bf16", seed=6, shift=0.0),
     # prefix of 65536 tokens (forward with state export), then 256 decode steps
     "decode_b64_t64k": dict(kind="decode", B=64, H=32, T=65536, dk=128, dv=128, chunk=64, L=17,
                             Ls=17, steps=256, io="bf16", seed=4, shift=0.0),
@@ -103,6 +107,8 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
     Shapes: q, k [B,H,T,dk]; v [B,H,T,dv] in the workload's io dtype;
     log_alpha [B,H,T], lam [B,H,T,L], beta [B,H,T] in float32.
 
+    Kind "level_decay": log_alpha is [B,H,T,L], one draw per token and level.
+
     Parity-only variants: la_mode "zero" (alpha = 1) or "slow"
     (log_alpha ~ -U(0, 0.01)); lam_mode "const" (all lam = 1.5) or "onehot"
     (lam = 1 at level ``lam_level``, 0 elsewhere).  ``tag`` salts the seed.
@@ -113,6 +119,7 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
     dk, dv, L = cfg["dk"], cfg["dv"], cfg["L"]
     seed = cfg["seed"] + (zlib.crc32(tag.encode()) << 8 if tag else 0)
     gdn = cfg["kind"] in ("gdn", "gdn_b")
+    per_level = cfg["kind"] == "level_decay"
     dt = io_dtype(cfg["io"])
     shift = float(cfg.get("shift", 0.0))
 
@@ -127,11 +134,12 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
         if name == "v":
             return _normal((T, dv), s, dev)
         if name == "log_alpha":
+            shp = (T, L) if per_level else (T,)
             if la_mode == "zero":
-                return torch.zeros(T, device=dev)
+                return torch.zeros(shp, device=dev)
             if la_mode == "slow":
-                return -0.01 * _uniform((T,), s, dev)
-            return -torch.nn.functional.softplus(_normal((T,), s, dev) + shift)
+                return -0.01 * _uniform(shp, s, dev)
+            return -torch.nn.functional.softplus(_normal(shp, s, dev) + shift)
         if name == "lam":
             if lam_mode == "const":
                 return torch.full((T, L), 1.5, device=dev)
@@ -148,7 +156,7 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
 
     out = {}
     shapes = {"q": (B, H, T, dk), "k": (B, H, T, dk), "v": (B, H, T, dv),
-              "log_alpha": (B, H, T), "lam": (B, H, T, L)}
+              "log_alpha": (B, H, T, L) if per_level else (B, H, T), "lam": (B, H, T, L)}
     if gdn:
         shapes["beta"] = (B, H, T)
     if dout if dout is not None else cfg["kind"] == "mamba2_bwd":
@@ -160,11 +168,12 @@ def make_inputs(cfg: dict, device="cpu", *, T=None, B=None, H=None, la_mode="sof
     return out
 
 
-def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None) -> dict:
+def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None, per_level=False) -> dict:
     """Per-step decode inputs: q, k [S,B,H,dk], v [S,B,H,dv] (io dtype),
     log_alpha [S,B,H], lam [S,B,H,Ls+1] (float32); config-1 distributions.
     For kind "gdn_decode" also beta [S,B,H], with k L2-normalised,
-    beta = sigmoid(N(0,1)) and log_alpha = -softplus(N(0,1) + shift)."""
+    beta = sigmoid(N(0,1)) and log_alpha = -softplus(N(0,1) + shift).
+    With ``per_level`` log_alpha is [S,B,H,Ls+1], one draw per level."""
     B = cfg["B"] if B is None else B
     H = cfg["H"] if H is None else H
     S = cfg["steps"] if steps is None else steps
@@ -185,7 +194,7 @@ def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None) -
         if name == "v":
             return _normal((S, dv), s, dev)
         if name == "log_alpha":
-            return -torch.nn.functional.softplus(_normal((S,), s, dev) + shift)
+            return -torch.nn.functional.softplus(_normal((S, Ls + 1) if per_level else (S,), s, dev) + shift)
         if name == "lam":
             return torch.nn.functional.softplus(_normal((S, Ls + 1), s, dev))
         if name == "beta":
@@ -194,7 +203,7 @@ def make_decode_inputs(cfg: dict, device="cpu", *, steps=None, B=None, H=None) -
 
     out = {}
     shapes = {"q": (B, H, S, dk), "k": (B, H, S, dk), "v": (B, H, S, dv),
-              "log_alpha": (B, H, S), "lam": (B, H, S, Ls + 1)}
+              "log_alpha": (B, H, S, Ls + 1) if per_level else (B, H, S), "lam": (B, H, S, Ls + 1)}
     if gdn:
         shapes["beta"] = (B, H, S)
     for name, shp in shapes.items():
