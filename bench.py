@@ -141,6 +141,13 @@ def backward_flops(cfg) -> int:
     return per_bh * cfg["B"] * cfg["H"]
 
 
+def level_decay_on_tensor_cores(cfg) -> bool:
+    """The per-level forward's tensor-core path: bf16, d = 128, whole 128-token
+    tiles, at most 16 levels (the CUDA-core kernels take every other shape)."""
+    return (cfg["io"] == "bf16" and cfg["dk"] == 128 and cfg["dv"] == 128 and cfg["T"] % 128 == 0
+            and cfg["L"] <= 16)
+
+
 def backward_on_tensor_cores(cfg) -> bool:
     """The backward of bf16 io with d_k = d_v = 128 runs on the tensor cores over
     128-token tiles; every other shape on the CUDA cores."""
@@ -175,14 +182,14 @@ def measured_peaks():
 # the sources each workload's kernels are built from: a traffic figure stays
 # valid while these files are unchanged
 KERNEL_SOURCES = {
-    "mamba2": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),
+    "mamba2": ("fwd_tc.cu", "level_decay.cuh", "common.cuh", "sm100.cuh"),
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn_tc.cu", "common.cuh", "sm100.cuh"),             # dominant: the tensor-core level scan
     "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
-    "mamba2_cont": ("fwd_tc.cu", "common.cuh", "sm100.cuh"),    # dominant: the tensor-core forward
+    "mamba2_cont": ("fwd_tc.cu", "level_decay.cuh", "common.cuh", "sm100.cuh"),  # dominant: the tensor-core forward
     "mamba2_bwd": ("bwd_tc.cu", "bwd.cuh", "common.cuh", "sm100.cuh"),  # dominant: the query-side kernel
-    "level_decay": ("fwd_level_decay.cu", "level_decay.cuh", "common.cuh"),
+    "level_decay": ("fwd_tc.cu", "level_decay.cuh", "common.cuh", "sm100.cuh"),  # dominant: the tensor-core forward
 }
 
 
@@ -819,7 +826,8 @@ def roofline_of(cfg, workload, w, mean_ms, dev, torch):
                 "traffic": traffic, "peak_source": f"{src} (HBM copy)", "algorithmic_bytes_per_launch": abytes,
                 "launches_per_step": w["launches"], "kernel": kname}
     abytes, aflops = w["abytes"], w["aflops"]
-    if (kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg)) or kind == "level_decay":
+    if (kind == "mamba2_bwd" and not backward_on_tensor_cores(cfg)) or (
+            kind == "level_decay" and not level_decay_on_tensor_cores(cfg)):
         sms = torch.cuda.get_device_properties(dev).multi_processor_count
         alu_peak = sms * 128 * 2 * sm_mhz * 1e6 / 1e12  # float32 FMA lanes x clock
         achieved = aflops / (mean_ms * 1e-3) / 1e12

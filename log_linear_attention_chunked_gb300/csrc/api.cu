@@ -415,11 +415,14 @@ ll_status ll_attn_decode_step(int B, int H, int dk, int dv, int Ls, ll_dtype io,
 
 size_t ll_attn_fwd_level_decay_workspace_size(const ll_shape* s) {
   if (check_shape(s) != LL_OK) return 0;
+  if (fwd_tc_level_decay_supported(*s)) return fwd_tc_level_decay_workspace(*s);
   return fwd_level_decay_workspace(*s);
 }
 
 int ll_attn_fwd_level_decay_launches(const ll_shape* s) {
-  if (check_shape(s) != LL_OK || fwd_level_decay_workspace(*s) == 0) return 0;
+  if (check_shape(s) != LL_OK) return 0;
+  if (fwd_tc_level_decay_supported(*s)) return fwd_tc_level_decay_launches(*s);
+  if (fwd_level_decay_workspace(*s) == 0) return 0;
   return fwd_level_decay_launches(*s);
 }
 
@@ -439,14 +442,15 @@ ll_status ll_attn_fwd_level_decay(const ll_shape* s, const void* q, const void* 
     for (unsigned x = (unsigned)s->T; x; x >>= 1) ++need;  // bit_length(T)
     if (s->Ls < need) return LL_ERR_INVALID_ARG;
   }
-  const size_t need_ws = fwd_level_decay_workspace(*s);
+  const bool tc = fwd_tc_level_decay_supported(*s);
+  const size_t need_ws = tc ? fwd_tc_level_decay_workspace(*s) : fwd_level_decay_workspace(*s);
   if (need_ws == 0) return LL_ERR_UNSUPPORTED;
   if (!workspace || ws_bytes < need_ws) return LL_ERR_WORKSPACE;
   if ((reinterpret_cast<uintptr_t>(workspace) & 255u) != 0) return LL_ERR_WORKSPACE;
   FwdArgs a{*s, q, k, v, log_alpha, lam, nullptr, o, state_out, scale_out, workspace, ws_bytes,
             static_cast<cudaStream_t>(stream), err_word()};
   if (!a.err) return LL_ERR_CUDA;
-  return fwd_level_decay_launch(a);
+  return tc ? fwd_tc_level_decay_launch(a) : fwd_level_decay_launch(a);
 }
 
 ll_status ll_attn_decode_step_level_decay(int B, int H, int dk, int dv, int Ls, ll_dtype io, const int64_t* t,

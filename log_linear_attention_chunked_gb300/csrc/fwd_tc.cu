@@ -45,6 +45,17 @@
 // accumulator once tile i-1's output has been read.  The node warps publish
 // each node as soon as its children are published, independently of the
 // epilogue, so a node never waits behind a back half.
+// With one decay per level (log_alpha [T, L], column l the decay of level l)
+// the same roles run with per-level factors: a key's log decay splits into a
+// key part K(s, l) and a query part Q(t, l) of the same level (the steps it
+// spends on the levels below l, and those on l from the start of t's block;
+// see the CUDA-core kernels of the per-level forward).  The epilogue builds
+// them per row from quadrant-local scans of the in-tile levels 1..7 (the
+// mask, the K decay exp(K(s, 8)) of the chunk state), and keeps the in-tile
+// running sums of the inter-tile levels for the back half; the decays across
+// tiles (the level producer's, and the node warps' child decays) come from a
+// table of per-level running sums over the tiles written by a small kernel
+// before this one.
 // Cross-CTA dependencies only point to tiles of lower index, every role
 // walks its tiles in increasing order, and the cooperative launch makes all
 // CTAs co-resident, so the waits always make progress.  Every wait is
@@ -55,7 +66,7 @@
 
 #include <atomic>
 
-#include "common.cuh"
+#include "level_decay.cuh"
 #include "sm100.cuh"
 
 namespace llattn {
@@ -91,9 +102,14 @@ constexpr uint32_t kOffF0 = kOffV + kTileBytes;    // level-node ring
 constexpr uint32_t kOffF1 = kOffF0 + kTileBytes;
 constexpr uint32_t kOffC = kOffF1 + kTileBytes;    // node warps: merge children, then the node
 constexpr uint32_t kOffX = kOffC + kTileBytes;     // output staging
-constexpr uint32_t kOffCs = kOffX + kTileBytes;    // float[128] cumsum x log2(e)
+constexpr uint32_t kOffCs = kOffX + kTileBytes;    // float[128] cumsum x log2(e); per-level mode:
+                                                   // float[4][16] quadrant totals of levels 1..16
 constexpr uint32_t kOffCol = kOffCs + kTile * 4;   // float[128] exp(cs_e - cs_s), e = end of s's 32-group
-constexpr uint32_t kOffLam = kOffCol + kTile * 4;  // half[6][128] lambda levels 0..5 / the row's max
+constexpr uint32_t kOffLam = kOffCol + kTile * 4;  // half[6][128] lambda levels 0..5 / the row's max;
+                                                   // per-level mode: half[6][128] exp(K(s, l)), l = 1..6
+// levels of log_alpha the per-level mode reads per row: 1..7 in the tile,
+// 8..15 across tiles (so T <= 32768 on this path)
+constexpr int kLdLv = 15;
 // misc: epilogue quadrant totals [0,16), abort flag 16, tmem base 32, node-warp totals [48,64)
 constexpr uint32_t kOffMisc = kOffLam + 6 * kTile * 2;
 // level producer -> epilogue: the level log decays of the previous tile
@@ -134,7 +150,13 @@ struct TcParams {
   unsigned* err;
   uint64_t timeout_ns;  // limit of every bounded wait
   long long withhold;   // node whose publication is withheld (expiry test), or -1
+  // per-level mode: running sums over the tiles of each inter-tile level's
+  // log decays, cumL[(bh * Lx + h) * Nt + j] = sum over tiles 0..j of level
+  // 8 + h, Lx = max(L - 8, 1)
+  const double* cumL;
 };
+
+__device__ __forceinline__ int ld_levels(const TcParams& p) { return p.L > 9 ? p.L - 8 : 1; }
 
 struct Ctx {
   unsigned char* base;
@@ -237,9 +259,17 @@ __device__ __forceinline__ int node_of_level(int j, int h) { return ((j >> (h + 
 // prefix nodes (continuation) per head: one per tile height
 constexpr int kPreSlots = 16;
 
-// The roles are instantiated twice: kCont = false is the forward from
-// position 0 (no prefix levels), kCont = true a continuation.
+// The roles are instantiated for kCont = false (the forward from position 0,
+// no prefix levels) and kCont = true (a continuation), and with kLD (one
+// decay per level; from position 0 only).
 template <bool kCont> __device__ __forceinline__ int start_tile(const TcParams& p) { return kCont ? p.c0t : 0; }
+
+// Per-level mode: the log decay of level 8 + h over tiles [a, b) of head bh.
+__device__ __forceinline__ float ld_span(const TcParams& p, int bh, int h, int a, int b) {
+  if (b <= a) return 0.f;
+  const double* cl = p.cumL + ((size_t)bh * ld_levels(p) + h) * p.Nt;
+  return (float)(__ldg(cl + b - 1) - (a > 0 ? __ldg(cl + a - 1) : 0.0));
+}
 
 // Number of tiles CTA blockIdx.x processes (blockIdx.x < total).
 __device__ __forceinline__ int tiles_of_cta(int total) { return (total - 1 - (int)blockIdx.x) / (int)gridDim.x + 1; }
@@ -266,6 +296,7 @@ __device__ __forceinline__ void prefetch_l2_inside(const void* ptr, uint32_t byt
 // levels one step later: per step, K(i), Q(i) (the scores' copy), V(i), then
 // Q(i-1) again (the levels' copy) -- the one Q buffer alternates between the
 // two uses, each load waiting for the previous use to release it.
+template <bool kLD>
 __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensorMap* tk, const CUtensorMap* tv) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
@@ -292,7 +323,8 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
         bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
         bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
         bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
-        prefetch_l2_inside(p.log_alpha + rn, kTile * 4);
+        const int la_row = kLD ? p.L : 1;  // floats of log_alpha per token
+        prefetch_l2_inside(p.log_alpha + rn * la_row, (uint32_t)(kTile * la_row * 4));
         prefetch_l2_inside(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
       }
       if (it > 0) wait_bar(c, B_K_FREE, (it - 1) & 1);  // the previous state product has read K
@@ -330,7 +362,7 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
 // released in shared memory, so the epilogue starts on level 0 before later
 // nodes are published) and loads the node.  Once a wait has expired nothing
 // new is armed.
-template <bool kCont>
+template <bool kCont, bool kLD>
 __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
@@ -363,7 +395,10 @@ __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
         fence_proxy_async_global();
         g = flag_g(w);
       }
-      dl[16 * (it & 1) + l] = D;
+      // the decay from the end of the node's block to the start of the tile:
+      // the node totals of the lower set bits, or (per-level mode) level
+      // 8 + h's own decays over those tiles
+      dl[16 * (it & 1) + l] = kLD ? ld_span(p, bhp, h, jp & ~((1 << h) - 1), jp) : D;
       D += g;
       st_release_cta_u32(nlr + (it & 1), ((uint32_t)it << 8) | ++l);
       const int fs = fcnt & 1;
@@ -496,7 +531,7 @@ __device__ void mma_issuer(const Ctx& c, uint32_t tmem) {
 }
 
 // ------------------------------------------------------------------ epilogue (warps 4..11)
-template <bool kCont>
+template <bool kCont, bool kLD>
 __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   const TcParams& p = *c.p;
   const int total = p.BH * p.Nt;
@@ -514,69 +549,159 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   uint32_t qpc = 0;  // level-weighted Q tiles written (two TMEM buffers)
   uint32_t xs = 0;   // outputs staged
 
-  // this row's log_alpha and intra-level lambdas, read one tile ahead
-  float la_n = 0.f, lam_n[8];
+  // this row's log_alpha (per-level mode: levels 1..kLdLv) and intra-level
+  // lambdas, read one tile ahead
+  float la_n = 0.f, lam_n[8], lal_n[kLD ? kLdLv : 1];
   auto fetch = [&](int u) {
     const size_t r = (size_t)(u % p.BH) * p.T + (size_t)(u / p.BH) * kTile + row;
-    la_n = __ldg(p.log_alpha + r);
+    if constexpr (kLD) {
+      const float* ar = p.log_alpha + r * p.L;
+#pragma unroll
+      for (int m = 0; m < kLdLv; ++m) lal_n[m] = m + 1 < p.L ? __ldg(ar + m + 1) : 0.f;
+    } else {
+      la_n = __ldg(p.log_alpha + r);
+    }
     const float* lr = p.lam + r * p.L;
 #pragma unroll
     for (int l = 0; l < 8; ++l) lam_n[l] = __ldg(lr + l);
   };
   fetch(blockIdx.x);
+  __half* kfh = reinterpret_cast<__half*>(s + kOffLam);  // per-level mode: exp(K(s, l)), l = 1..6
+  float* qtl = reinterpret_cast<float*>(s + kOffCs);     // per-level mode: quadrant totals [4][16]
 
   float cs_prev = 0.f, lam_c = 0.f;
+  float csI_prev[kLD ? 8 : 1];  // per-level mode: in-tile running sums of levels 8..15 (previous tile)
+#pragma unroll
+  for (int h = 0; h < (kLD ? 8 : 1); ++h) csI_prev[h] = 0.f;
   int jp = 0, bhp = 0;
   for (int it = 0; it <= n; ++it) {
     const int u = blockIdx.x + it * gridDim.x;
     int bh = 0, j = 0;
     float cs_t = 0.f;
+    float csI[kLD ? 8 : 1];
+#pragma unroll
+    for (int h = 0; h < (kLD ? 8 : 1); ++h) csI[h] = 0.f;
     if (it < n) {
       // ================= front half of tile it
       bh = u % p.BH;
       j = u / p.BH;
       const float la = la_n;
-      float lam[8];
+      float lam[8], lal[kLD ? kLdLv : 1];
 #pragma unroll
       for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
+      if constexpr (kLD) {
+#pragma unroll
+        for (int m = 0; m < kLdLv; ++m) lal[m] = lal_n[m];
+      }
       if (it + 1 < n) fetch(u + gridDim.x);
       const int jap = jp | start_tile<kCont>(p);  // the previous tile's absolute index bits
       if (it >= 1 && jap != 0)  // the previous tile's first level lambda, ahead of its back half
         lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jap) - 1));
 
-      // inclusive cumsum of log_alpha over the tile
-      float x = la;
+      // per-level mode: the key and query parts of the log decays of this row
+      float kdec2 = 0.f, rf6 = 0.f, rf7 = 0.f, gf0 = 0.f, rowq[kLD ? 6 : 1];
+      float cs2_t = 0.f, cs2_diag = 0.f, cs2_end = 0.f;
+      if constexpr (kLD) {
+        // quadrant-local running sums of levels 1..kLdLv (levels l = m + 1)
+        float cp[kLdLv];
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const float y = __shfl_up_sync(0xffffffffu, x, o);
-        if (lane >= o) x += y;
-      }
-      if (hf == 0 && lane == 31) qtot[q] = x;
-      __syncwarp();
-      named_bar_sync(1, kEpi);
-      float off = 0.f;
-      for (int qq = 0; qq < q; ++qq) off += qtot[qq];
-      cs_t = x + off;
-      const float cs2_t = cs_t * kLog2e;                               // base-2 log decay
-      const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);  // end of this 32-group
-      if (hf == 0) {
-        cs_s[row] = cs2_t;
-        col_s[row] = ex2(cs2_grp_end - cs2_t);
-      }
-      // lambda of levels 0..5 (the diagonal group), relative to the row's
-      // largest, as half; the largest rides in the exponent
-      float lmax = 0.f;
+        for (int m = 0; m < kLdLv; ++m) {
+          float x = lal[m];
 #pragma unroll
-      for (int l = 0; l < 6; ++l) lmax = fmaxf(lmax, lam[l]);
-      const float cs2_diag = cs2_t + (lmax > 0.f ? __log2f(lmax) : -INFINITY);
-      if (hf == 0) {
-        const float inv = lmax > 0.f ? 1.f / lmax : 0.f;
+          for (int o = 1; o < 32; o <<= 1) {
+            const float y = __shfl_up_sync(0xffffffffu, x, o);
+            if (lane >= o) x += y;
+          }
+          cp[m] = x;
+        }
+        if (hf == 0 && lane == 31) {
 #pragma unroll
-        for (int l = 0; l < 6; ++l) lamh[l * kTile + row] = __float2half_rn(lam[l] * inv);
+          for (int m = 0; m < kLdLv; ++m) qtl[q * 16 + m] = cp[m];
+        }
+        __syncwarp();
+        named_bar_sync(1, kEpi);
+        // Q(t, l): level l's decays from the start of t's block of 2^(l-1)
+        // rows through t; inside the quadrant for l <= 6, the quadrant pair for l = 7
+        float qf[6];
+        qf[0] = 0.f;
+#pragma unroll
+        for (int l = 1; l <= 5; ++l) {
+          const int src = ((lane >> (l - 1)) << (l - 1)) - 1;
+          const float pv = __shfl_sync(0xffffffffu, cp[l - 1], src < 0 ? 0 : src);
+          qf[l] = cp[l - 1] - (src < 0 ? 0.f : pv);
+        }
+        const float qf6 = cp[5];
+        const float qf7 = cp[6] + ((q & 1) ? qtl[(q - 1) * 16 + 6] : 0.f);
+        // K(t, l): the decays of the sibling blocks above t at the levels
+        // below l (bit m-1 of t clear: the next 2^(m-1) rows, at level m)
+        float kf[9], K = 0.f;
+        kf[1] = 0.f;
+#pragma unroll
+        for (int m = 1; m <= 5; ++m) {
+          const int ss = ((lane >> m) << m) + (1 << (m - 1)), se = ss + (1 << (m - 1)) - 1;
+          const float a1 = __shfl_sync(0xffffffffu, cp[m - 1], se & 31);
+          const float a0 = __shfl_sync(0xffffffffu, cp[m - 1], (ss - 1) & 31);
+          if (!((lane >> (m - 1)) & 1)) K += a1 - a0;
+          kf[m + 1] = K;
+        }
+        if (!(q & 1)) K += qtl[(q + 1) * 16 + 5];
+        kf[7] = K;
+        if (q < 2) K += qtl[2 * 16 + 6] + qtl[3 * 16 + 6];
+        kf[8] = K;
+        kdec2 = kf[8] * kLog2e;
+        rowq[0] = lam[0];
+#pragma unroll
+        for (int l = 1; l <= 5; ++l) rowq[l] = lam[l] * ex2(qf[l] * kLog2e);
+        rf6 = lam[6] * ex2(qf6 * kLog2e);
+        rf7 = lam[7] * ex2(qf7 * kLog2e);
+        gf0 = ex2(qtl[16 + 5] * kLog2e);  // keys of group 0 pass group 1 at level 6 on their way to level 7
+#pragma unroll
+        for (int h = 0; h < 8; ++h) {
+          float off = 0.f;
+          for (int qq = 0; qq < q; ++qq) off += qtl[qq * 16 + 7 + h];
+          csI[h] = cp[7 + h] + off;
+        }
+        if (hf == 0) {
+#pragma unroll
+          for (int l = 1; l <= 6; ++l) kfh[(l - 1) * kTile + row] = __float2half_rn(ex2(kf[l] * kLog2e));
+        }
+        __syncwarp();
+        named_bar_sync(1, kEpi);
+      } else {
+        // inclusive cumsum of log_alpha over the tile
+        float x = la;
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        if (hf == 0 && lane == 31) qtot[q] = x;
+        __syncwarp();
+        named_bar_sync(1, kEpi);
+        float off = 0.f;
+        for (int qq = 0; qq < q; ++qq) off += qtot[qq];
+        cs_t = x + off;
+        cs2_t = cs_t * kLog2e;                               // base-2 log decay
+        const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);  // end of this 32-group
+        if (hf == 0) {
+          cs_s[row] = cs2_t;
+          col_s[row] = ex2(cs2_grp_end - cs2_t);
+        }
+        // lambda of levels 0..5 (the diagonal group), relative to the row's
+        // largest, as half; the largest rides in the exponent
+        float lmax = 0.f;
+#pragma unroll
+        for (int l = 0; l < 6; ++l) lmax = fmaxf(lmax, lam[l]);
+        cs2_diag = cs2_t + (lmax > 0.f ? __log2f(lmax) : -INFINITY);
+        if (hf == 0) {
+          const float inv = lmax > 0.f ? 1.f / lmax : 0.f;
+#pragma unroll
+          for (int l = 0; l < 6; ++l) lamh[l * kTile + row] = __float2half_rn(lam[l] * inv);
+        }
+        __syncwarp();
+        named_bar_sync(1, kEpi);
+        cs2_end = cs_s[kTile - 1];
       }
-      __syncwarp();
-      named_bar_sync(1, kEpi);
-      const float cs2_end = cs_s[kTile - 1];
 
       // scores ready: K has been read by them, so it is decayed in place for
       // the chunk state, K[s] <- exp(cs_end - cs_s) K[s]
@@ -584,7 +709,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       __syncwarp();
       tc_fence_after();
       {
-        const float dec = ex2(cs2_end - cs2_t);
+        const float dec = kLD ? ex2(kdec2) : ex2(cs2_end - cs2_t);
         uint4* kr = reinterpret_cast<uint4*>(s + kOffK + hf * kHalf + row * 128);
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -618,14 +743,32 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         float v[16];
         if (g < q) {
           tmem_ld16(tl + kTmS + s0, v);
-          const float lg = (q ^ g) == 1 ? lam[6] : lam[7];  // level 5 + bitlen(q ^ g)
-          const float rf = lg * ex2(cs2_t - cs_s[32 * g + 31]);
-          const float4* cp = reinterpret_cast<const float4*>(col_s + s0);
-          float cf[16];
+          float rf, cf[16];
+          if constexpr (kLD) {
+            // level 6 (q ^ g == 1): Q(t, 6) K(s, 6); level 7: Q(t, 7) K(s, 7),
+            // K(s, 7) = K(s, 6) + group 1's level-6 decay for keys of group 0
+            rf = (q ^ g) == 1 ? rf6 : rf7 * (g == 0 ? gf0 : 1.f);
+            const uint4* kp = reinterpret_cast<const uint4*>(kfh + 5 * kTile + s0);
 #pragma unroll
-          for (int i4 = 0; i4 < 4; ++i4) {
-            const float4 f = cp[i4];
-            cf[4 * i4] = f.x; cf[4 * i4 + 1] = f.y; cf[4 * i4 + 2] = f.z; cf[4 * i4 + 3] = f.w;
+            for (int i8 = 0; i8 < 2; ++i8) {
+              const uint4 f = kp[i8];
+              const __half2* h2 = reinterpret_cast<const __half2*>(&f);
+#pragma unroll
+              for (int e = 0; e < 4; ++e) {
+                const float2 f2 = __half22float2(h2[e]);
+                cf[8 * i8 + 2 * e] = f2.x;
+                cf[8 * i8 + 2 * e + 1] = f2.y;
+              }
+            }
+          } else {
+            const float lg = (q ^ g) == 1 ? lam[6] : lam[7];  // level 5 + bitlen(q ^ g)
+            rf = lg * ex2(cs2_t - cs_s[32 * g + 31]);
+            const float4* cp = reinterpret_cast<const float4*>(col_s + s0);
+#pragma unroll
+            for (int i4 = 0; i4 < 4; ++i4) {
+              const float4 f = cp[i4];
+              cf[4 * i4] = f.x; cf[4 * i4 + 1] = f.y; cf[4 * i4 + 2] = f.z; cf[4 * i4 + 3] = f.w;
+            }
           }
           tmem_ld_wait();
 #pragma unroll
@@ -636,7 +779,17 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
 #pragma unroll
           for (int i = 0; i < 16; ++i) {
             const int x = 16 * hf + i;  // column inside the diagonal group
-            const float e = ex2(cs2_diag - cs_s[s0 + i]) * __half2float(lamh[(32 - __clz(lane ^ x)) * kTile + row]);
+            const int lv = 32 - __clz(lane ^ x);
+            float e;
+            if constexpr (kLD) {
+              // lam_t[l] Q(t, l) (a select over this row's six) times K(s, l) from the table
+              float rq = rowq[0];
+#pragma unroll
+              for (int l = 1; l <= 5; ++l) rq = lv == l ? rowq[l] : rq;
+              e = lv == 0 ? rq : rq * __half2float(kfh[(lv > 0 ? lv - 1 : 0) * kTile + 32 * q + x]);
+            } else {
+              e = ex2(cs2_diag - cs_s[s0 + i]) * __half2float(lamh[lv * kTile + row]);
+            }
             v[i] = (x <= lane) ? v[i] * e : 0.f;
           }
         } else {
@@ -708,12 +861,19 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // as the A operand of a product the MMA accumulates onto the output
       int l = 0;
       for (int rem = jap; rem != 0; ++l) {
+        const int hcur = __ffs(rem) - 1;  // level 8 + hcur
         rem &= rem - 1;
         const float lam_h = lam_c;
         // the next level's lambda loads while this level is written
         if (rem != 0) lam_c = __ldg(p.lam + rp * p.L + 8 + (__ffs(rem) - 1));
         wait_levels((uint32_t)(l + 1));
-        const float w = lam_h * ex2((cs_prev + dl[l]) * kLog2e);
+        float csl = cs_prev;
+        if constexpr (kLD) {  // the level's own running sum in the tile
+          csl = csI_prev[0];
+#pragma unroll
+          for (int h = 1; h < 8; ++h) csl = hcur == h ? csI_prev[h] : csl;
+        }
+        const float w = lam_h * ex2((csl + dl[l]) * kLog2e);
         uint32_t wq[32];
 #pragma unroll
         for (int c8 = 0; c8 < 8; ++c8) {
@@ -771,6 +931,10 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
     }
 
     cs_prev = cs_t;
+    if constexpr (kLD) {
+#pragma unroll
+      for (int h = 0; h < 8; ++h) csI_prev[h] = csI[h];
+    }
     jp = j;
     bhp = bh;
   }
@@ -807,6 +971,7 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to) {
 // back to the MMA, and once the store is complete F_j is published with its
 // log-decay total G_j.  Thread t = 32 (warp % 4) + lane owns TMEM lane t: row
 // d_v = t of the node.
+template <bool kLD>
 __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, const CUtensorMap* tf) {
   const TcParams& p = *c.p;
   const int n = tiles_of_cta(p.BH * p.Nt);
@@ -826,7 +991,7 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
     const size_t node_j = (size_t)bh * p.Nt + j;
     // the tile's log-decay total (also the barrier after which the previous
     // node's store has completed and C is free)
-    float x = __ldg(p.log_alpha + (size_t)bh * p.T + (size_t)j * kTile + t);
+    float x = kLD ? 0.f : __ldg(p.log_alpha + (size_t)bh * p.T + (size_t)j * kTile + t);
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
     if (lane == 0) nq[q] = x;
@@ -855,7 +1020,8 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
       ++cf;
       __syncwarp();
       const float g = *gch;
-      const float sc = ex2(D * kLog2e);
+      // per-level mode: the child's keys sit at level 8 + m over tiles (j - 2^m, j]
+      const float sc = ex2((kLD ? ld_span(p, bh, m, j - (1 << m) + 1, j + 1) : D) * kLog2e);
       // row t of the child, 16-byte chunk c8 of its 128-byte-swizzled tile
 #pragma unroll
       for (int c32 = 0; c32 < 4; ++c32) {
@@ -885,7 +1051,7 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
       named_bar_sync(6, kNodeThreads);  // every row of the child is read: C is free
       D += g;
     }
-    const float G = D;  // cs_end plus the children's totals
+    const float G = kLD ? 0.f : D;  // cs_end plus the children's totals (unused per level)
     // F_j as bf16 into C (row t), then M is free and the node is stored
 #pragma unroll
     for (int c32 = 0; c32 < 4; ++c32) {
@@ -919,7 +1085,7 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
   if (leader && armed > 0) drain_bar(c, B_C_FULL, (armed - 1) & 1);  // (a copy armed before an abort)
 }
 
-template <bool kCont>
+template <bool kCont, bool kLD>
 __global__ void __launch_bounds__(kThreads, 1)
     fwd_tc_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                   const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tf,
@@ -964,17 +1130,17 @@ __global__ void __launch_bounds__(kThreads, 1)
   if (wg == 0) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 88;\n" ::: "memory");
     if (lane == 0) {
-      if (warp == 0) producer_kvq(c, &tq, &tk, &tv);
+      if (warp == 0) producer_kvq<kLD>(c, &tq, &tk, &tv);
       else if (warp == 1) mma_issuer<kCont>(c, tmem);
       else if (warp == 2) store_warp(c, &to);
-      else producer_levels<kCont>(c, &tf);
+      else producer_levels<kCont, kLD>(c, &tf);
     }
   } else if (wg == 3) {
     asm volatile("setmaxnreg.dec.sync.aligned.u32 104;\n" ::: "memory");
-    node_warps(c, tmem, warp, lane, &tf);
+    node_warps<kLD>(c, tmem, warp, lane, &tf);
   } else {
     asm volatile("setmaxnreg.inc.sync.aligned.u32 160;\n" ::: "memory");
-    epilogue<kCont>(c, tmem, warp, lane);
+    epilogue<kCont, kLD>(c, tmem, warp, lane);
   }
   __syncwarp();
 
@@ -1025,24 +1191,95 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
   }
 }
 
+// Per-level mode: the running sums over the tiles of level 8 + h's log
+// decays, one CTA per (h, head): float sums inside a tile (a warp per tile),
+// float64 across the tiles (warp 0).
+__global__ void __launch_bounds__(256) tc_ld_tables_kernel(const float* __restrict__ la, double* __restrict__ cumL,
+                                                           int T, int Nt, int L, int Lx) {
+  extern __shared__ double tt[];  // [Nt] tile totals
+  const int h = blockIdx.x;
+  const size_t bh = blockIdx.y;
+  const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
+  const int lv = 8 + h;
+  for (int j = warp; j < Nt; j += 8) {
+    float x = 0.f;
+    if (lv < L) {
+      const float* b = la + ((size_t)bh * T + (size_t)j * kTile) * L + lv;
+#pragma unroll
+      for (int r = 0; r < 4; ++r) x += __ldg(b + (size_t)(lane + 32 * r) * L);
+    }
+#pragma unroll
+    for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
+    if (lane == 0) tt[j] = x;
+  }
+  __syncthreads();
+  if (warp == 0) {
+    double carry = 0.0;
+    for (int base = 0; base < Nt; base += 32) {
+      const int i = base + lane;
+      double y = i < Nt ? tt[i] : 0.0;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const double z = __shfl_up_sync(0xffffffffu, y, o);
+        if (lane >= o) y += z;
+      }
+      y += carry;
+      if (i < Nt) cumL[(bh * Lx + h) * Nt + i] = y;
+      carry = __shfl_sync(0xffffffffu, y, 31);
+    }
+  }
+}
+
+// Per-level mode: the level states of position T, each node decayed at its
+// own level over the tiles after its block.
+__global__ void __launch_bounds__(256) tc_ld_export_kernel(const __nv_bfloat16* __restrict__ F,
+                                                           const double* __restrict__ cumL,
+                                                           float* __restrict__ state_out,
+                                                           float* __restrict__ scale_out, int Nt, int Ls, int Lx) {
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  constexpr int mat = kD * kD;
+  for (int slot = 0; slot < Ls; ++slot) {
+    const int h = slot + 1 - 8;  // level slot+1 = 8 + h
+    float val = 0.f, sc = 0.f;
+    if (h >= 0 && h < 31 && ((Nt >> h) & 1)) {
+      const size_t e = bh * Nt + node_of_level(Nt, h);
+      const int cb = Nt & ~((1 << h) - 1);  // the node's keys are at level 8 + h from tile cb on
+      double D = 0.0;
+      if (cb < Nt && h < Lx) {
+        const double* cl = cumL + (bh * Lx + h) * (size_t)Nt;
+        D = cl[Nt - 1] - (cb > 0 ? cl[cb - 1] : 0.0);
+      }
+      val = exp2f((float)D * kLog2e) * __bfloat162float(F[e * mat + idx]);
+      sc = 1.f;
+    }
+    state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
+    if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
+  }
+}
+
 // ------------------------------------------------------------------ host side
 struct TcPlan {
-  int Nt;
-  size_t off_F, off_G, off_flags, total;
+  int Nt, Lx;
+  size_t off_F, off_G, off_flags, off_cum, total;
   size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
 // F holds the tiles' nodes, then kPreSlots prefix nodes per head (used by a
-// continuation only, always reserved so one layout serves both)
-TcPlan tc_plan(const ll_shape& s) {
+// continuation only, always reserved so one layout serves both); the
+// per-level mode adds its table of running sums
+TcPlan tc_plan(const ll_shape& s, bool ld = false) {
   TcPlan p{};
   p.Nt = s.T / kTile;
+  p.Lx = std::max(s.L - 8, 1);
   const size_t BH = (size_t)s.B * s.H;
   const size_t nodes = BH * p.Nt;
   size_t off = 0;
   p.off_F = off;      off = align_up(off + (nodes + BH * kPreSlots) * kD * kD * 2, 1024);
   p.off_G = off;      off = align_up(off + nodes * 4, 256);
   p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
+  p.off_cum = off;
+  if (ld) off = align_up(off + BH * p.Lx * p.Nt * sizeof(double), 256);
   p.total = off;
   const size_t slots = (size_t)std::max(s.Ls, 1);
   p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
@@ -1108,9 +1345,19 @@ size_t fwd_tc_workspace(const ll_shape& s) { return tc_plan(s).total; }
 
 int fwd_tc_launches(const ll_shape& s) { return s.Ls > 0 ? 2 : 1; }
 
-ll_status fwd_tc_launch(const FwdArgs& a) {
+bool fwd_tc_level_decay_supported(const ll_shape& s) {
+  return s.io == LL_BF16 && s.dk == kD && s.dv == kD && s.T % kTile == 0 && s.L <= kLdLv + 1 &&
+         (long long)s.B * s.H * (s.T + kPreSlots * kTile) <= (1ll << 31) - 1;
+}
+
+size_t fwd_tc_level_decay_workspace(const ll_shape& s) { return tc_plan(s, true).total; }
+
+int fwd_tc_level_decay_launches(const ll_shape& s) { return s.Ls > 0 ? 3 : 2; }
+
+static ll_status tc_launch(const FwdArgs& a, bool ld) {
   const ll_shape& s = a.s;
-  const TcPlan plan = tc_plan(s);
+  const TcPlan plan = tc_plan(s, ld);
+  if (ld && a.state_in) return LL_ERR_INVALID_ARG;
   if (a.ws_bytes < (a.state_in ? plan.total_cont : plan.total)) return LL_ERR_WORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(a.ws);
   const int BH = s.B * s.H;
@@ -1143,6 +1390,12 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   p.c0t = a.state_in ? (int)(a.t0 / kTile) : 0;
   p.timeout_ns = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
   p.withhold = a.withhold_node;
+  p.cumL = ld ? reinterpret_cast<const double*>(ws + plan.off_cum) : nullptr;
+  if (ld) {
+    tc_ld_tables_kernel<<<dim3(plan.Lx, BH), 256, plan.Nt * sizeof(double), a.stream>>>(
+        a.log_alpha, reinterpret_cast<double*>(ws + plan.off_cum), stride, plan.Nt, s.L, plan.Lx);
+    LL_CUDA_OK(cudaGetLastError());
+  }
   if (a.state_in) {
     tc_prefix_nodes_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(a.state_in, a.scale_in, p.F, BH, plan.Nt,
                                                                          s.Ls, a.t0);
@@ -1152,7 +1405,8 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
   int dev = 0, sms = 0, per_sm = 0;
   LL_CUDA_OK(cudaGetDevice(&dev));
   LL_CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
-  const void* kern = a.state_in ? (const void*)fwd_tc_kernel<true> : (const void*)fwd_tc_kernel<false>;
+  const void* kern = ld ? (const void*)fwd_tc_kernel<false, true>
+                        : a.state_in ? (const void*)fwd_tc_kernel<true, false> : (const void*)fwd_tc_kernel<false, false>;
   LL_CUDA_OK(cudaFuncSetAttribute(kern, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kSmemBytes));
   LL_CUDA_OK(cudaOccupancyMaxActiveBlocksPerMultiprocessor(&per_sm, kern, kThreads, kSmemBytes));
   if (per_sm < 1) return LL_ERR_CUDA;
@@ -1171,12 +1425,20 @@ ll_status fwd_tc_launch(const FwdArgs& a) {
                               reinterpret_cast<float*>(ws + plan.off_segDec), a.state_out, a.scale_out, BH, s.T,
                               kD * kD, s.Ls, a.t0, a.stream);
   }
-  if (a.state_out) {
+  if (a.state_out && ld) {
+    tc_ld_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.cumL, a.state_out, a.scale_out,
+                                                                      plan.Nt, s.Ls, plan.Lx);
+    LL_CUDA_OK(cudaGetLastError());
+  } else if (a.state_out) {
     tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, a.state_out, a.scale_out, plan.Nt,
                                                                    s.Ls);
     LL_CUDA_OK(cudaGetLastError());
   }
   return LL_OK;
 }
+
+ll_status fwd_tc_launch(const FwdArgs& a) { return tc_launch(a, false); }
+
+ll_status fwd_tc_level_decay_launch(const FwdArgs& a) { return tc_launch(a, true); }
 
 }  // namespace llattn

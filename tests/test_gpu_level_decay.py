@@ -96,6 +96,52 @@ def test_onehot_levels_slow_decay(B, lvl):
     assert rel_err(out, ref) <= TOL_F32
 
 
+@pytest.mark.parametrize("lvl", [0, 1, 3, 5, 6, 7, 8, 10, 12])
+def test_tensor_core_path_onehot_levels(B, lvl):
+    """bf16, d = 128, T a multiple of 128: the tensor-core path.  lam one-hot
+    at one level isolates that level's factors: levels 0..5 (the diagonal
+    32-row groups), 6 and 7 (the groups below them), 8 and up (the Fenwick
+    nodes across tiles), under decays that keep every key alive."""
+    T = 4096
+    cfg = _cfg(io="bf16", T=T, dk=128, dv=128, chunk=64, L=levels_needed(T))
+    inp = synth.make_inputs(cfg, B=1, H=2, la_mode="slow", lam_mode="onehot", lam_level=lvl, tag=f"ldtc{lvl}")
+    out = _run(B, inp, 64)
+    f = _f64(inp)
+    ref = ld.forward_dense_bh(f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+    assert rel_err(out, ref) <= TOL_BF16
+
+
+@pytest.mark.parametrize("T,la", [(128, "softplus"), (256, "slow"), (1024, "softplus"), (4096, "zero"),
+                                  (8192, "slow")])
+def test_tensor_core_path_matches_dense(B, T, la):
+    cfg = _cfg(io="bf16", T=T, dk=128, dv=128, chunk=64, L=levels_needed(T))
+    inp = synth.make_inputs(cfg, B=1, H=2, la_mode=la, tag=f"ldtcd{T}{la}")
+    out = _run(B, inp, 64)
+    f = _f64(inp)
+    if T <= 4096:
+        ref = ld.forward_dense_bh(f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+        assert rel_err(out, ref) <= TOL_BF16
+    else:
+        rows = np.r_[0, 127, 128, 1000, 4095, 4096, 6000, T - 1]
+        for h in range(2):
+            ref = ld.forward_rows(f["q"][0, h], f["k"][0, h], f["v"][0, h], f["log_alpha"][0, h], f["lam"][0, h],
+                                  rows)
+            assert rel_err(out[0, h][rows][None, None], ref[None, None]) <= TOL_BF16, h
+
+
+def test_tensor_core_and_cuda_core_paths_agree(B):
+    """The same bf16 d = 128 call on both paths: T % 128 == 0 takes the
+    tensor cores, one token more the CUDA cores (its first T tokens are the
+    same inputs, so their outputs must agree)."""
+    T = 2048
+    cfg = _cfg(io="bf16", T=T + 1, dk=128, dv=128, chunk=64, L=levels_needed(T + 1))
+    inp = synth.make_inputs(cfg, B=1, H=2, tag="ldpaths")
+    long_out = _run(B, inp, 64)
+    short = {n: x[:, :, :T].contiguous() for n, x in inp.items()}
+    short_out = _run(B, short, 64)
+    assert rel_err(short_out, long_out[:, :, :T]) <= 2 * TOL_BF16
+
+
 def test_equal_columns_match_the_base_forward(B):
     """Every level with the same decay: the per-level path and ll_attn_fwd
     compute the same function (both checked against the oracle too)."""
