@@ -31,6 +31,11 @@
  *                        delta-rule pseudo-values), study note §3-5.
  *   ll_gdn_decode_step   one token of Log-Linear Gated DeltaNet decoding over the
  *                        Fenwick level states (reading A), study note §3-5/§3-6.
+ *   ll_attn_fwd_level_decay, ll_attn_decode_step_level_decay
+ *                        the forward and the decode step with one decay per level
+ *                        (study note §7 "Follow-up design" names a learned memory
+ *                        decay per level; the reading implemented is stated at
+ *                        their declarations).
  *
  * Definitions used throughout:
  *   level l(t,s) = 0 if s == t, else floor(log2(t xor s)) + 1   (0 <= s <= t);
@@ -87,7 +92,7 @@ typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
  *   B, H      batch rows and heads (>= 1)
  *   T         sequence length (>= 1); the Gated DeltaNet entry points need a
  *             multiple of `chunk`, the Mamba-2 forward takes any T (with bf16
- *             and d = 128 the whole 128-token tiles run on the tensor cores
+ *             and d = 128 or 64 the whole 128-token tiles run on the tensor cores
  *             and the last T % 128 tokens as a continuation from their decode
  *             states, on the CUDA cores)
  *   dk, dv    key / value head dims, each in {16, 32, 64, 128}
@@ -96,7 +101,8 @@ typedef enum { LL_F32 = 0, LL_BF16 = 1 } ll_dtype;
  *   chunk     chunk length of the chunked algorithm, in {16, 32, 64, 128}; the
  *             result does not depend on it (up to rounding).  The bf16
  *             tensor-core path of ll_attn_fwd tiles by 128 tokens whatever
- *             `chunk` is (it needs T % 128 == 0 and dk == dv == 128).
+ *             `chunk` is (it needs T % 128 == 0 and dk == dv in {64, 128}; d = 64
+ *             runs as 128 with the operand tiles' upper halves zero).
  *   Ls        number of stored decode levels of state_out (levels 1..Ls);
  *             0 = no state export
  *   io        dtype of q, k, v and o (LL_F32 or LL_BF16); log_alpha, lam,
@@ -194,9 +200,9 @@ LL_API size_t ll_attn_fwd_cont_workspace_size(const ll_shape* shape, long long t
  *   workspace  >= ll_attn_fwd_cont_workspace_size(shape, t0) bytes, 256-aligned
  * o_t = sum over all keys s <= t (prefix included) of
  *       (q_t . k_s) Gamma(t,s) lam_t[l(t,s)] v_s.
- * bf16 io with d = 128 and T a multiple of 128 runs on the tensor-core path
- * (the prefix levels become extra level products of every tile), every other
- * shape on the CUDA-core path. */
+ * bf16 io with d = 128 or 64 and T a multiple of 128 runs on the tensor-core
+ * path (the prefix levels become extra level products of every tile), every
+ * other shape on the CUDA-core path. */
 LL_API ll_status ll_attn_fwd_cont(const ll_shape* shape, long long t0, const float* state_in,
                                   const float* scale_in, const void* q, const void* k, const void* v,
                                   const float* log_alpha, const float* lam, void* o, float* state_out,
@@ -226,9 +232,11 @@ LL_API int ll_attn_fwd_level_decay_launches(const ll_shape* shape);
  * state_out / scale_out: the level states of position T as in ll_attn_fwd
  * (each bucket decayed to token T-1 under this rule), ready for
  * ll_attn_decode_step_level_decay at t = T.
- * Runs on the CUDA cores (float32 FMA, float64 running sums of the log
- * decays) for every io dtype and head size; LL_ERR_UNSUPPORTED beyond 4096
- * chunks. */
+ * bf16 io with d = 128 or 64, T a multiple of 128 and L <= 16 runs on the
+ * tensor cores (the forward's persistent kernel in a per-level mode, after
+ * two small kernels that tabulate each level's decay over the tiles); every
+ * other shape on the CUDA cores (float32 FMA, float64 running sums of the log
+ * decays), LL_ERR_UNSUPPORTED there beyond 4096 chunks. */
 LL_API ll_status ll_attn_fwd_level_decay(const ll_shape* shape, const void* q, const void* k, const void* v,
                                          const float* log_alpha, const float* lam, void* o, float* state_out,
                                          float* scale_out, void* workspace, size_t ws_bytes, void* stream);

@@ -353,8 +353,9 @@ def ll_attn_fwd_cont_workspace_size(shape: ll_shape, t0: int) -> int:
 
 def ll_attn_fwd_cont(t0: int, state_in, scale_in, q, k, v, log_alpha, lam, chunk: int, *, o=None, state_out=None,
                      scale_out=None, workspace=None):
-    """Prefill continuation at position t0 (a multiple of the smallest power of
-    two >= T).  state_in [B,H,Ls,dv,dk] / scale_in [B,H,Ls]: the decode states
+    """Prefill continuation at position t0 (any t0 >= 0; a start that is not a
+    multiple of the smallest power of two >= T runs as aligned pieces).
+    state_in [B,H,Ls,dv,dk] / scale_in [B,H,Ls]: the decode states
     of position t0; q, k, v, log_alpha, lam: the T new tokens; optional
     state_out / scale_out receive the states of position t0 + T.  Returns o."""
     B, H, T, dk = q.shape

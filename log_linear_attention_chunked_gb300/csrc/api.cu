@@ -150,7 +150,7 @@ static int next_piece(long long pos, long long rem) {
 // Ragged T on the tensor-core path: the whole 128-token tiles in place, their
 // decode states at T_full, then the last T % 128 tokens as a continuation.
 static bool ragged_tc(const ll_shape& s) {
-  if (s.io != LL_BF16 || s.dk != 128 || s.dv != 128 || s.T <= 128 || s.T % 128 == 0) return false;
+  if (s.io != LL_BF16 || s.T <= 128 || s.T % 128 == 0) return false;
   ll_shape f = s;
   f.T = s.T - s.T % 128;
   return fwd_tc_supported(f);

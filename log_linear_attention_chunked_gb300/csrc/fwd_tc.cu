@@ -150,13 +150,20 @@ struct TcParams {
   unsigned* err;
   uint64_t timeout_ns;  // limit of every bounded wait
   long long withhold;   // node whose publication is withheld (expiry test), or -1
-  // per-level mode: running sums over the tiles of each inter-tile level's
-  // log decays, cumL[(bh * Lx + h) * Nt + j] = sum over tiles 0..j of level
-  // 8 + h, Lx = max(L - 8, 1)
-  const double* cumL;
+  // head size of q, k, v and o (64 or 128): with 64 the operand tiles are
+  // filled to 128 columns with zeros by the TMA (its out-of-range fill), every
+  // product runs as at 128, and only the first 64 output columns are stored
+  int d;
 };
 
+// Per-level mode: running sums over the tiles of each inter-tile level's log
+// decays, cumL[(bh * Lx + h) * Nt + j] = sum over tiles 0..j of level 8 + h,
+// Lx = max(L - 8, 1); the table follows the publication words (and the abort
+// word) in the workspace.
 __device__ __forceinline__ int ld_levels(const TcParams& p) { return p.L > 9 ? p.L - 8 : 1; }
+__device__ __forceinline__ const double* ld_table(const TcParams& p) {
+  return reinterpret_cast<const double*>(p.flags + (size_t)p.BH * p.Nt + 1);
+}
 
 struct Ctx {
   unsigned char* base;
@@ -267,7 +274,7 @@ template <bool kCont> __device__ __forceinline__ int start_tile(const TcParams& 
 // Per-level mode: the log decay of level 8 + h over tiles [a, b) of head bh.
 __device__ __forceinline__ float ld_span(const TcParams& p, int bh, int h, int a, int b) {
   if (b <= a) return 0.f;
-  const double* cl = p.cumL + ((size_t)bh * ld_levels(p) + h) * p.Nt;
+  const double* cl = ld_table(p) + ((size_t)bh * ld_levels(p) + h) * p.Nt;
   return (float)(__ldg(cl + b - 1) - (a > 0 ? __ldg(cl + a - 1) : 0.0));
 }
 
@@ -320,9 +327,10 @@ __device__ void producer_kvq(const Ctx& c, const CUtensorMap* tq, const CUtensor
       if (it + 1 < n) {
         const int un = u + gridDim.x;
         const size_t rn = (size_t)(un % p.BH) * p.T + (size_t)(un / p.BH) * kTile;
-        bulk_prefetch_l2(p.q + rn * kD, kTileBytes);
-        bulk_prefetch_l2(p.k + rn * kD, kTileBytes);
-        bulk_prefetch_l2(p.v + rn * kD, kTileBytes);
+        const uint32_t tb = (uint32_t)(kTile * p.d * 2);  // one tile of q, k or v
+        bulk_prefetch_l2(p.q + rn * p.d, tb);
+        bulk_prefetch_l2(p.k + rn * p.d, tb);
+        bulk_prefetch_l2(p.v + rn * p.d, tb);
         const int la_row = kLD ? p.L : 1;  // floats of log_alpha per token
         prefetch_l2_inside(p.log_alpha + rn * la_row, (uint32_t)(kTile * la_row * 4));
         prefetch_l2_inside(p.lam + rn * p.L, (uint32_t)(kTile * p.L * 4));
@@ -953,7 +961,7 @@ __device__ void store_warp(const Ctx& c, const CUtensorMap* to) {
     fence_proxy_async_shared();
     const int row0 = (up % p.BH) * p.T + (up / p.BH) * kTile;
     tma_store_2d(to, x, 0, row0);
-    tma_store_2d(to, x + kHalf, 64, row0);
+    if (p.d > 64) tma_store_2d(to, x + kHalf, 64, row0);  // (d = 64: the zero half is not stored)
     bulk_commit();
     bulk_wait_read0();
     mbar_arrive(c.bars + B_X_FREE);
@@ -1155,26 +1163,33 @@ __global__ void __launch_bounds__(kThreads, 1)
 // Level states of position T read from the Fenwick nodes (float32, decayed to T-1).
 // Continuation: the prefix states of position t0 (true state = scale * S,
 // decayed to t0 - 1) as bf16 nodes, one per tile height h (level 8 + h).
+// With d = 64 the states are [64][64] and the nodes [128][128] with zeros
+// outside the first 64 rows and columns.
 __global__ void __launch_bounds__(256) tc_prefix_nodes_kernel(const float* __restrict__ state_in,
                                                               const float* __restrict__ scale_in,
                                                               __nv_bfloat16* __restrict__ F, int BH, int Nt, int Ls,
-                                                              long long t0) {
+                                                              long long t0, int d) {
   const size_t bh = blockIdx.y;
   const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  const int r = idx >> 7, cc = idx & 127;
   constexpr int mat = kD * kD;
   for (int slot = 7; slot < Ls; ++slot) {  // levels 8 .. Ls (t0 is a multiple of the tile: no lower ones)
     if (!((t0 >> slot) & 1)) continue;
     const int h = slot + 1 - 8;              // tile height: bit h of t0 / 128
     const size_t node = (size_t)BH * Nt + bh * kPreSlots + h;
-    F[node * mat + idx] = __float2bfloat16_rn(scale_in[bh * Ls + slot] * state_in[(bh * Ls + slot) * (size_t)mat + idx]);
+    const float x = (r < d && cc < d) ? scale_in[bh * Ls + slot] * state_in[(bh * Ls + slot) * (size_t)d * d + r * d + cc]
+                                      : 0.f;
+    F[node * mat + idx] = __float2bfloat16_rn(x);
   }
 }
 
 __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __restrict__ F,
                                                         const float* __restrict__ G, float* __restrict__ state_out,
-                                                        float* __restrict__ scale_out, int Nt, int Ls) {
+                                                        float* __restrict__ scale_out, int Nt, int Ls, int d) {
   const size_t bh = blockIdx.y;
   const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  const int r = idx >> 7, cc = idx & 127;
+  const bool in = r < d && cc < d;  // (d = 64: the nodes' first 64 rows and columns)
   constexpr int mat = kD * kD;
   float D = 0.f;
   for (int slot = 0; slot < Ls; ++slot) {
@@ -1186,47 +1201,55 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
       sc = 1.f;
       D += G[e];
     }
-    state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
+    if (in) state_out[(bh * Ls + slot) * (size_t)d * d + r * d + cc] = val;
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
   }
 }
 
-// Per-level mode: the running sums over the tiles of level 8 + h's log
-// decays, one CTA per (h, head): float sums inside a tile (a warp per tile),
-// float64 across the tiles (warp 0).
-__global__ void __launch_bounds__(256) tc_ld_tables_kernel(const float* __restrict__ la, double* __restrict__ cumL,
-                                                           int T, int Nt, int L, int Lx) {
-  extern __shared__ double tt[];  // [Nt] tile totals
-  const int h = blockIdx.x;
+// Per-level mode, first step: the log-decay totals of every tile at the
+// inter-tile levels 8..L-1, one CTA per (tile, head), thread = row;
+// tot[(bh * Nt + j) * Lx + h] (float).
+__global__ void __launch_bounds__(kTile) tc_ld_tile_totals_kernel(const float* __restrict__ la,
+                                                                  float* __restrict__ tot, int T, int Nt, int L,
+                                                                  int Lx) {
+  __shared__ float part[kTile / 32][8];
+  const int j = blockIdx.x;
   const size_t bh = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
-  const int lv = 8 + h;
-  for (int j = warp; j < Nt; j += 8) {
-    float x = 0.f;
-    if (lv < L) {
-      const float* b = la + ((size_t)bh * T + (size_t)j * kTile) * L + lv;
+  const float* r = la + ((size_t)bh * T + (size_t)j * kTile + threadIdx.x) * L;
 #pragma unroll
-      for (int r = 0; r < 4; ++r) x += __ldg(b + (size_t)(lane + 32 * r) * L);
-    }
+  for (int h = 0; h < 8; ++h) {
+    float x = 8 + h < L ? __ldg(r + 8 + h) : 0.f;
 #pragma unroll
     for (int o = 16; o > 0; o >>= 1) x += __shfl_xor_sync(0xffffffffu, x, o);
-    if (lane == 0) tt[j] = x;
+    if (lane == 0) part[warp][h] = x;
   }
   __syncthreads();
-  if (warp == 0) {
-    double carry = 0.0;
-    for (int base = 0; base < Nt; base += 32) {
-      const int i = base + lane;
-      double y = i < Nt ? tt[i] : 0.0;
+  if (threadIdx.x < Lx && threadIdx.x < 8) {
+    const int h = threadIdx.x;
+    tot[((size_t)bh * Nt + j) * Lx + h] = (part[0][h] + part[1][h]) + (part[2][h] + part[3][h]);
+  }
+}
+
+// Second step: their running sums over the tiles, float64, one warp per level:
+// cumL[(bh * Lx + h) * Nt + j] = sum of tot over tiles 0..j.
+__global__ void __launch_bounds__(256) tc_ld_tile_scan_kernel(const float* __restrict__ tot,
+                                                              double* __restrict__ cumL, int Nt, int Lx) {
+  const size_t bh = blockIdx.x;
+  const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
+  if (h >= Lx) return;
+  double carry = 0.0;
+  for (int base = 0; base < Nt; base += 32) {
+    const int i = base + lane;
+    double y = i < Nt ? (double)tot[((size_t)bh * Nt + i) * Lx + h] : 0.0;
 #pragma unroll
-      for (int o = 1; o < 32; o <<= 1) {
-        const double z = __shfl_up_sync(0xffffffffu, y, o);
-        if (lane >= o) y += z;
-      }
-      y += carry;
-      if (i < Nt) cumL[(bh * Lx + h) * Nt + i] = y;
-      carry = __shfl_sync(0xffffffffu, y, 31);
+    for (int o = 1; o < 32; o <<= 1) {
+      const double z = __shfl_up_sync(0xffffffffu, y, o);
+      if (lane >= o) y += z;
     }
+    y += carry;
+    if (i < Nt) cumL[(bh * Lx + h) * Nt + i] = y;
+    carry = __shfl_sync(0xffffffffu, y, 31);
   }
 }
 
@@ -1235,9 +1258,11 @@ __global__ void __launch_bounds__(256) tc_ld_tables_kernel(const float* __restri
 __global__ void __launch_bounds__(256) tc_ld_export_kernel(const __nv_bfloat16* __restrict__ F,
                                                            const double* __restrict__ cumL,
                                                            float* __restrict__ state_out,
-                                                           float* __restrict__ scale_out, int Nt, int Ls, int Lx) {
+                                                           float* __restrict__ scale_out, int Nt, int Ls, int Lx,
+                                                           int d) {
   const size_t bh = blockIdx.y;
   const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  const int r = idx >> 7, cc = idx & 127;
   constexpr int mat = kD * kD;
   for (int slot = 0; slot < Ls; ++slot) {
     const int h = slot + 1 - 8;  // level slot+1 = 8 + h
@@ -1253,7 +1278,7 @@ __global__ void __launch_bounds__(256) tc_ld_export_kernel(const __nv_bfloat16* 
       val = exp2f((float)D * kLog2e) * __bfloat162float(F[e * mat + idx]);
       sc = 1.f;
     }
-    state_out[(bh * Ls + slot) * (size_t)mat + idx] = val;
+    if (r < d && cc < d) state_out[(bh * Ls + slot) * (size_t)d * d + r * d + cc] = val;
     if (blockIdx.x == 0 && threadIdx.x == 0) scale_out[bh * Ls + slot] = sc;
   }
 }
@@ -1261,7 +1286,7 @@ __global__ void __launch_bounds__(256) tc_ld_export_kernel(const __nv_bfloat16* 
 // ------------------------------------------------------------------ host side
 struct TcPlan {
   int Nt, Lx;
-  size_t off_F, off_G, off_flags, off_cum, total;
+  size_t off_F, off_G, off_flags, off_tot, off_cum, total;
   size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
@@ -1277,9 +1302,12 @@ TcPlan tc_plan(const ll_shape& s, bool ld = false) {
   size_t off = 0;
   p.off_F = off;      off = align_up(off + (nodes + BH * kPreSlots) * kD * kD * 2, 1024);
   p.off_G = off;      off = align_up(off + nodes * 4, 256);
-  p.off_flags = off;  off = align_up(off + (nodes + 1) * 8, 256);
-  p.off_cum = off;
-  if (ld) off = align_up(off + BH * p.Lx * p.Nt * sizeof(double), 256);
+  p.off_flags = off;  off += (nodes + 1) * 8;
+  p.off_cum = off;  // directly after the words: the kernel finds it there
+  if (ld) off += BH * p.Lx * p.Nt * sizeof(double);
+  off = align_up(off, 256);
+  p.off_tot = off;
+  if (ld) off = align_up(off + BH * p.Lx * p.Nt * sizeof(float), 256);
   p.total = off;
   const size_t slots = (size_t)std::max(s.Ls, 1);
   p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
@@ -1303,12 +1331,14 @@ PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   return fn;
 }
 
-// 2-D bf16 tensor map over [rows, 128] with [128 x 64] boxes, 128-byte swizzle.
-bool make_map(CUtensorMap* m, const void* base, uint64_t rows) {
+// 2-D bf16 tensor map over [rows, cols] with [128 x 64] boxes, 128-byte
+// swizzle; with cols = 64 a box at column 64 lies wholly outside and loads
+// as zeros.
+bool make_map(CUtensorMap* m, const void* base, uint64_t rows, int cols = kD) {
   auto fn = encode_fn();
   if (!fn) return false;
-  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
-  cuuint64_t strides[1] = {(cuuint64_t)kD * 2};
+  cuuint64_t dims[2] = {(cuuint64_t)cols, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)cols * 2};
   cuuint32_t box[2] = {64, (cuuint32_t)kTile};
   cuuint32_t estr[2] = {1, 1};
   return fn(m, CU_TENSOR_MAP_DATA_TYPE_BFLOAT16, 2, const_cast<void*>(base), dims, strides, box, estr,
@@ -1327,8 +1357,11 @@ uint32_t next_token() {
 
 }  // namespace
 
+// bf16 with d = 128, or d = 64 run as 128 with zero-filled tiles
+static bool tc_head_ok(const ll_shape& s) { return s.dk == s.dv && (s.dk == kD || s.dk == 64); }
+
 bool fwd_tc_supported(const ll_shape& s) {
-  return s.io == LL_BF16 && s.dk == kD && s.dv == kD && s.T % kTile == 0 && s.L <= kLmax &&
+  return s.io == LL_BF16 && tc_head_ok(s) && s.T % kTile == 0 && s.L <= kLmax &&
          (long long)s.B * s.H * (s.T + kPreSlots * kTile) <= (1ll << 31) - 1;
 }
 
@@ -1346,13 +1379,13 @@ size_t fwd_tc_workspace(const ll_shape& s) { return tc_plan(s).total; }
 int fwd_tc_launches(const ll_shape& s) { return s.Ls > 0 ? 2 : 1; }
 
 bool fwd_tc_level_decay_supported(const ll_shape& s) {
-  return s.io == LL_BF16 && s.dk == kD && s.dv == kD && s.T % kTile == 0 && s.L <= kLdLv + 1 &&
+  return s.io == LL_BF16 && tc_head_ok(s) && s.T % kTile == 0 && s.L <= kLdLv + 1 &&
          (long long)s.B * s.H * (s.T + kPreSlots * kTile) <= (1ll << 31) - 1;
 }
 
 size_t fwd_tc_level_decay_workspace(const ll_shape& s) { return tc_plan(s, true).total; }
 
-int fwd_tc_level_decay_launches(const ll_shape& s) { return s.Ls > 0 ? 3 : 2; }
+int fwd_tc_level_decay_launches(const ll_shape& s) { return s.Ls > 0 ? 4 : 3; }
 
 static ll_status tc_launch(const FwdArgs& a, bool ld) {
   const ll_shape& s = a.s;
@@ -1367,8 +1400,9 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
   const uint64_t rows = (uint64_t)BH * stride;
   const uint64_t node_rows = ((uint64_t)BH * plan.Nt + (uint64_t)BH * kPreSlots) * kD;
   CUtensorMap tq, tk, tv, tf, to;
-  if (!make_map(&tq, a.q, rows) || !make_map(&tk, a.k, rows) || !make_map(&tv, a.v, rows) ||
-      !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows))
+  const int d = s.dk;
+  if (!make_map(&tq, a.q, rows, d) || !make_map(&tk, a.k, rows, d) || !make_map(&tv, a.v, rows, d) ||
+      !make_map(&tf, ws + plan.off_F, node_rows) || !make_map(&to, a.o, rows, d))
     return LL_ERR_CUDA;
 
   TcParams p;
@@ -1390,15 +1424,19 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
   p.c0t = a.state_in ? (int)(a.t0 / kTile) : 0;
   p.timeout_ns = a.timeout_ns ? a.timeout_ns : kTimeoutNs;
   p.withhold = a.withhold_node;
-  p.cumL = ld ? reinterpret_cast<const double*>(ws + plan.off_cum) : nullptr;
+  p.d = s.dk;
   if (ld) {
-    tc_ld_tables_kernel<<<dim3(plan.Lx, BH), 256, plan.Nt * sizeof(double), a.stream>>>(
-        a.log_alpha, reinterpret_cast<double*>(ws + plan.off_cum), stride, plan.Nt, s.L, plan.Lx);
+    float* tot = reinterpret_cast<float*>(ws + plan.off_tot);
+    tc_ld_tile_totals_kernel<<<dim3(plan.Nt, BH), kTile, 0, a.stream>>>(a.log_alpha, tot, stride, plan.Nt, s.L,
+                                                                        plan.Lx);
+    LL_CUDA_OK(cudaGetLastError());
+    tc_ld_tile_scan_kernel<<<BH, 256, 0, a.stream>>>(tot, reinterpret_cast<double*>(ws + plan.off_cum), plan.Nt,
+                                                     plan.Lx);
     LL_CUDA_OK(cudaGetLastError());
   }
   if (a.state_in) {
     tc_prefix_nodes_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(a.state_in, a.scale_in, p.F, BH, plan.Nt,
-                                                                         s.Ls, a.t0);
+                                                                         s.Ls, a.t0, d);
     LL_CUDA_OK(cudaGetLastError());
   }
 
@@ -1419,19 +1457,19 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
   if (a.state_out && a.state_in) {
     float* segS = reinterpret_cast<float*>(ws + plan.off_segS);
     float* segSc = reinterpret_cast<float*>(ws + plan.off_segSc);
-    tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, segS, segSc, plan.Nt, s.Ls);
+    tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, segS, segSc, plan.Nt, s.Ls, d);
     LL_CUDA_OK(cudaGetLastError());
     return cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha,
                               reinterpret_cast<float*>(ws + plan.off_segDec), a.state_out, a.scale_out, BH, s.T,
-                              kD * kD, s.Ls, a.t0, a.stream);
+                              d * d, s.Ls, a.t0, a.stream);
   }
   if (a.state_out && ld) {
-    tc_ld_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.cumL, a.state_out, a.scale_out,
-                                                                      plan.Nt, s.Ls, plan.Lx);
+    tc_ld_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(
+        p.F, reinterpret_cast<const double*>(ws + plan.off_cum), a.state_out, a.scale_out, plan.Nt, s.Ls, plan.Lx, d);
     LL_CUDA_OK(cudaGetLastError());
   } else if (a.state_out) {
     tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, a.state_out, a.scale_out, plan.Nt,
-                                                                   s.Ls);
+                                                                   s.Ls, d);
     LL_CUDA_OK(cudaGetLastError());
   }
   return LL_OK;

@@ -243,5 +243,5 @@ def test_withhold_hook_rejects_bad_args_on_host(L):
     assert L.ll_test_fwd_withhold_node(ctypes.byref(s), *p, vp(FAKE), 1 << 20, 2, 10 ** 6, None) == 1
     assert L.ll_test_fwd_withhold_node(ctypes.byref(s), *p, vp(FAKE), 1 << 20, 0, 10, None) == 1
     # a shape off the tensor-core path
-    s2 = binding.make_shape(1, 1, 256, 64, 64, 9, 64, 0, binding.LL_BF16)
+    s2 = binding.make_shape(1, 1, 256, 32, 32, 9, 64, 0, binding.LL_BF16)
     assert L.ll_test_fwd_withhold_node(ctypes.byref(s2), *p, vp(FAKE), 1 << 20, 0, 10 ** 6, None) == 2
