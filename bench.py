@@ -8,15 +8,19 @@ d=128, bf16 in / float32 accumulate.  One step = one ll_attn_fwd call over the
 whole workload (every step of the hot path: intra-chunk attention, chunk
 states, the Fenwick node tree and the inter-chunk levels).  Other workloads:
 `decode_b64_t64k` (one ll_attn_decode_step for 64 x 32 heads with 17 stored
-levels, positions 65536 onward), `gdn_bf16_t4k` (one ll_gdn_fwd) and
+levels, positions 65536 onward), `gdn_bf16_t4k` (one ll_gdn_fwd),
+`gdn_b_bf16_t4k` (one ll_gdn_fwd_b), `gdn_decode_b64_t64k` (one
+ll_gdn_decode_step), `mamba2_cont_bf16_t16k` (one ll_attn_fwd_cont),
+`level_decay_bf16_t16k` (one ll_attn_fwd_level_decay) and
 `mamba2_bwd_bf16_t16k` (one ll_attn_bwd over the default workload's shape,
 with an upstream gradient of o).
 
 A default run (the forward workload, no --workload) also times, in the same
-process and on the same GPU, the decode step (`decode_b64_t64k`, 256 steps)
-and the Gated DeltaNet forward (`gdn_bf16_t4k`), each with its own warm-up,
-clock record, roofline and end-to-end figure, under the line's `secondary`
-key (`--no-secondary` skips them).
+process and on the same GPU, the decode step (`decode_b64_t64k`, 256 steps),
+the Gated DeltaNet forward (`gdn_bf16_t4k`) and the forward with one decay
+per level (`level_decay_bf16_t16k`), each with its own warm-up, clock
+record, roofline and end-to-end figure, under the line's `secondary` key
+(`--no-secondary` skips them).
 
 Roofline of a step: the slower of its algorithmic flops at the measured bf16
 tensor peak and its algorithmic bytes at the measured HBM copy bandwidth; the
@@ -689,7 +693,7 @@ def decode_workload(cfg, dev, rank, binding, synth, torch):
 
 DEFAULT_WORKLOAD = "mamba2_bf16_t16k"
 # timed after the primary in a default run: (workload, steps)
-SECONDARY = (("decode_b64_t64k", 256), ("gdn_bf16_t4k", 50))
+SECONDARY = (("decode_b64_t64k", 256), ("gdn_bf16_t4k", 50), ("level_decay_bf16_t16k", 100))
 
 
 def workload_config(cfg, name, world):
@@ -719,7 +723,7 @@ def main():
     ap.add_argument("--workload", default=DEFAULT_WORKLOAD)
     ap.add_argument("--no-cpu-baseline", action="store_true")
     ap.add_argument("--no-secondary", action="store_true",
-                    help="default workload only: skip the decode and Gated DeltaNet blocks")
+                    help="default workload only: skip the decode, Gated DeltaNet and per-level-decay blocks")
     args = ap.parse_args()
     if args.warmup < 3:
         ap.error("--warmup must be >= 3")
