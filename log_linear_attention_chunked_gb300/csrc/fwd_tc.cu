@@ -1206,6 +1206,75 @@ __global__ void __launch_bounds__(256) tc_export_kernel(const __nv_bfloat16* __r
   }
 }
 
+// Continuation: the decode states of t1 = t0 + T in one pass (no separate
+// export of the segment, no separate sum of its log decays).  With b =
+// bitlen(t1 xor t0) and P the smallest power of two >= T, the prefix bucket of
+// level l goes to level max(l, b), decayed over the whole segment (whose log
+// decay is the sum of the node totals of the tiles' Fenwick prefix); the
+// segment's own bucket of level l (the node of tile height l - 8, decayed
+// from the end of its block to T - 1) keeps its level if T < P and goes to b
+// if T = P.  Thread 0 lists, per output slot, the buckets that land on it and
+// their factors; every thread then sums its element of those.
+__global__ void __launch_bounds__(256) tc_cont_export_kernel(const __nv_bfloat16* __restrict__ F,
+                                                             const float* __restrict__ G,
+                                                             const float* __restrict__ state_in,
+                                                             const float* __restrict__ scale_in,
+                                                             float* __restrict__ state_out,
+                                                             float* __restrict__ scale_out, int Nt, int T, int Ls,
+                                                             long long t0, int d) {
+  constexpr int kMaxSrc = 2 * 64;
+  __shared__ int off[64 + 1];
+  __shared__ long long srcs[kMaxSrc];  // >= 0: the row offset of a prefix state; < 0: -(node + 1)
+  __shared__ float fac[kMaxSrc];
+  const size_t bh = blockIdx.y;
+  const int idx = blockIdx.x * 256 + threadIdx.x;  // < 128 * 128
+  const int r = idx >> 7, cc = idx & 127;
+  constexpr int mat = kD * kD;
+  const long long t1 = t0 + T;
+  if (threadIdx.x == 0) {
+    const int b = 64 - __clzll(t1 ^ t0);                         // bitlen(t1 xor t0)
+    const long long P = 1ll << (64 - __clzll((long long)T - 1));  // smallest power of two >= T
+    // the segment's buckets: node of height h decayed by the node totals of the lower set bits
+    float segD[32];
+    float D = 0.f;
+    for (int h = 0; h < 31; ++h) {
+      segD[h] = D;
+      if ((Nt >> h) & 1) D += G[bh * Nt + node_of_level(Nt, h)];
+    }
+    const float dec = exp2f(D * kLog2e);  // the whole segment's decay
+    int n = 0;
+    for (int o = 0; o < Ls; ++o) {
+      off[o] = n;
+      if (!((t1 >> o) & 1)) continue;
+      for (int sl = 0; sl < Ls && n < kMaxSrc; ++sl) {
+        if (((t0 >> sl) & 1) && (sl + 1 > b ? sl + 1 : b) == o + 1) {
+          srcs[n] = (long long)(bh * Ls + sl) * d * d;
+          fac[n++] = scale_in[bh * Ls + sl] * dec;
+        }
+        const int h = sl + 1 - 8;
+        if (h >= 0 && h < 31 && ((Nt >> h) & 1) && ((long long)T < P ? sl + 1 : b) == o + 1 && n < kMaxSrc) {
+          srcs[n] = -(long long)(bh * Nt + node_of_level(Nt, h)) - 1;
+          fac[n++] = exp2f(segD[h] * kLog2e);
+        }
+      }
+    }
+    off[Ls] = n;
+  }
+  __syncthreads();
+  if (r >= d || cc >= d) return;
+  for (int o = 0; o < Ls; ++o) {
+    float acc = 0.f;
+    for (int e = off[o]; e < off[o + 1]; ++e) {
+      const long long sv = srcs[e];
+      const float x = sv >= 0 ? state_in[sv + r * d + cc] : __bfloat162float(F[(size_t)(-sv - 1) * mat + idx]);
+      acc = fmaf(fac[e], x, acc);
+    }
+    state_out[(bh * Ls + o) * (size_t)d * d + r * d + cc] = acc;
+  }
+  if (blockIdx.x == 0 && threadIdx.x == 0)
+    for (int o = 0; o < Ls; ++o) scale_out[bh * Ls + o] = ((t1 >> o) & 1) ? 1.f : 0.f;
+}
+
 // Per-level mode, first step: the log-decay totals of every tile at the
 // inter-tile levels 8..L-1, one CTA per (tile, head), thread = row;
 // tot[(bh * Nt + j) * Lx + h] (float).
@@ -1287,7 +1356,6 @@ __global__ void __launch_bounds__(256) tc_ld_export_kernel(const __nv_bfloat16* 
 struct TcPlan {
   int Nt, Lx;
   size_t off_F, off_G, off_flags, off_tot, off_cum, total;
-  size_t off_segS, off_segSc, off_segDec, total_cont;  // the segment's own export (continuation)
 };
 
 // F holds the tiles' nodes, then kPreSlots prefix nodes per head (used by a
@@ -1309,11 +1377,6 @@ TcPlan tc_plan(const ll_shape& s, bool ld = false) {
   p.off_tot = off;
   if (ld) off = align_up(off + BH * p.Lx * p.Nt * sizeof(float), 256);
   p.total = off;
-  const size_t slots = (size_t)std::max(s.Ls, 1);
-  p.off_segS = off;   off = align_up(off + BH * slots * kD * kD * 4, 256);
-  p.off_segSc = off;  off = align_up(off + BH * slots * 4, 256);
-  p.off_segDec = off; off = align_up(off + BH * 4, 256);
-  p.total_cont = off;
   return p;
 }
 
@@ -1372,11 +1435,11 @@ bool fwd_tc_cont_supported(const ll_shape& s, long long t0) {
   return fwd_tc_supported(s) && t0 / kTile < (1ll << 30) && s.Ls <= 7 + kPreSlots;
 }
 
-size_t fwd_tc_cont_workspace(const ll_shape& s) { return tc_plan(s).total_cont; }
+size_t fwd_tc_cont_workspace(const ll_shape& s) { return tc_plan(s).total; }
 
 size_t fwd_tc_workspace(const ll_shape& s) { return tc_plan(s).total; }
 
-int fwd_tc_launches(const ll_shape& s) { return s.Ls > 0 ? 2 : 1; }
+int fwd_tc_launches(const ll_shape& s) { return s.Ls > 0 ? 2 : 1; }  // (a continuation: 3 with its prefix nodes)
 
 bool fwd_tc_level_decay_supported(const ll_shape& s) {
   return s.io == LL_BF16 && tc_head_ok(s) && s.T % kTile == 0 && s.L <= kLdLv + 1 &&
@@ -1391,7 +1454,7 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
   const ll_shape& s = a.s;
   const TcPlan plan = tc_plan(s, ld);
   if (ld && a.state_in) return LL_ERR_INVALID_ARG;
-  if (a.ws_bytes < (a.state_in ? plan.total_cont : plan.total)) return LL_ERR_WORKSPACE;
+  if (a.ws_bytes < plan.total) return LL_ERR_WORKSPACE;
   unsigned char* ws = static_cast<unsigned char*>(a.ws);
   const int BH = s.B * s.H;
   const int stride = a.rows_per_head ? a.rows_per_head : s.T;  // rows between (b, h) slices
@@ -1455,13 +1518,10 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
   LL_CUDA_OK(cudaLaunchCooperativeKernel(kern, dim3(grid), dim3(kThreads), args, kSmemBytes,
                                          a.stream));
   if (a.state_out && a.state_in) {
-    float* segS = reinterpret_cast<float*>(ws + plan.off_segS);
-    float* segSc = reinterpret_cast<float*>(ws + plan.off_segSc);
-    tc_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(p.F, p.G, segS, segSc, plan.Nt, s.Ls, d);
+    tc_cont_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(
+        p.F, p.G, a.state_in, a.scale_in, a.state_out, a.scale_out, plan.Nt, s.T, s.Ls, a.t0, d);
     LL_CUDA_OK(cudaGetLastError());
-    return cont_export_launch(a.state_in, a.scale_in, segS, segSc, a.log_alpha,
-                              reinterpret_cast<float*>(ws + plan.off_segDec), a.state_out, a.scale_out, BH, s.T,
-                              d * d, s.Ls, a.t0, a.stream);
+    return LL_OK;
   }
   if (a.state_out && ld) {
     tc_ld_export_kernel<<<dim3(kD * kD / 256, BH), 256, 0, a.stream>>>(
