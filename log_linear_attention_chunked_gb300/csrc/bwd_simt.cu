@@ -48,7 +48,9 @@ namespace llattn {
 namespace {
 
 constexpr int kThreads = 256;
-constexpr int kSuffixThreads = 1024;
+constexpr int kSuffixThreads = 256;
+constexpr int kSuffixRun = 8;
+constexpr int kSuffixPart = kSuffixThreads * kSuffixRun;  // tokens per CTA of the suffix sums
 constexpr int kMaxChunkElems = 8192;           // Ce * max(dk, dv), as in the forward
 constexpr size_t kMaxSmem = 220 * 1024;        // dynamic shared memory of one CTA
 
@@ -67,7 +69,7 @@ size_t key_smem(int Ce, int dk, int dv) {
 
 struct BwdPlan {
   int Ce, N, lc;
-  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_Ft, off_cum, total;
+  size_t off_S, off_F, off_R, off_tot, off_G, off_dq, off_dk, off_dv, off_dc, off_Ft, off_cum, off_sfx, off_ptot, total;
 };
 
 BwdPlan plan_of(const ll_shape& s) {
@@ -96,6 +98,9 @@ BwdPlan plan_of(const ll_shape& s) {
   if (bwd_tc_supported(s)) off = align_up(off + BH * p.N * mat * 2, 256);  // the nodes as bf16 tiles
   p.off_cum = off;
   off = align_up(off + BH * p.N * sizeof(double), 256);  // running sums of the chunk totals
+  // the suffix sums of dc: each part's own (float64) and the parts' totals
+  p.off_sfx = off;  off = align_up(off + BH * (size_t)s.T * sizeof(double), 256);
+  p.off_ptot = off; off = align_up(off + BH * (size_t)((s.T + kSuffixPart - 1) / kSuffixPart) * sizeof(double), 256);
   p.off_dq = p.off_dk = p.off_dv = off;
   if (s.io != LL_F32) {  // partial sums of dq, dk, dv (float32 io accumulates in the outputs):
     // float32 on the CUDA cores, the in-tile parts in bf16 on the tensor-core path
@@ -401,49 +406,82 @@ __global__ void __launch_bounds__(kThreads) bwd_key_kernel(
   }
 }
 
-// (5) one CTA per head: dlog_alpha_r = sum_{t >= r} dc_t, in float64.  The
-// tokens go in rounds of kSuffixThreads runs of kSuffixRun consecutive tokens,
-// from the end of the sequence: each thread sums its run, a suffix scan over
-// the threads gives each run the sum of everything after it, and the thread
-// writes its run's suffix sums.
-constexpr int kSuffixRun = 16;
-
-__global__ void __launch_bounds__(kSuffixThreads) bwd_suffix_kernel(const float* __restrict__ dc,
-                                                                    float* __restrict__ dla, int T) {
-  __shared__ double part[kSuffixThreads];
-  const size_t bh = blockIdx.x;
-  const int tid = threadIdx.x;
-  constexpr int kRound = kSuffixThreads * kSuffixRun;
-  double carry = 0.0;  // the sum over the tokens after this round
-  for (int end = T; end > 0; end -= kRound) {
-    const int start = max(0, end - kRound);
-    const int t0 = start + tid * kSuffixRun, t1 = min(end, t0 + kSuffixRun);
-    float v[kSuffixRun];
-    double s = 0.0;
+// (5) dlog_alpha_r = sum_{t >= r} dc_t, in float64, in two passes over parts
+// of kSuffixPart tokens (float64 arithmetic is scarce on this GPU: the parts
+// spread it over the SMs).  First pass, one CTA per (part, head): each thread
+// sums a run of kSuffixRun consecutive tokens (staged by coalesced loads,
+// rows padded against bank conflicts), a suffix scan over the threads (warp
+// shuffles, then over the warps) gives each run the sum of the part after it,
+// and the thread writes its tokens' suffix sums inside the part (float64) and
+// the part's total.  Second pass: each part adds the totals of the parts after
+// it and rounds to float32.
+__global__ void __launch_bounds__(kSuffixThreads) bwd_suffix_part_kernel(const float* __restrict__ dc,
+                                                                         double* __restrict__ sfx,
+                                                                         double* __restrict__ ptot, int T) {
+  __shared__ float sbuf[kSuffixThreads * (kSuffixRun + 1)];
+  __shared__ double wtot[kSuffixThreads / 32];
+  const int part = blockIdx.x, P = gridDim.x;
+  const size_t bh = blockIdx.y;
+  const int tid = threadIdx.x, lane = tid & 31, warp = tid >> 5;
+  constexpr int kWarps = kSuffixThreads / 32;
+  const int start = part * kSuffixPart, n = min(kSuffixPart, T - start);
+  for (int x = tid; x < kSuffixPart; x += kSuffixThreads)
+    sbuf[(x / kSuffixRun) * (kSuffixRun + 1) + x % kSuffixRun] = x < n ? dc[bh * T + start + x] : 0.f;
+  __syncthreads();
+  const float* run = sbuf + tid * (kSuffixRun + 1);
+  double sum = 0.0;
 #pragma unroll
-    for (int u = 0; u < kSuffixRun; ++u) {
-      v[u] = t0 + u < t1 ? dc[bh * T + t0 + u] : 0.f;
-      s += (double)v[u];
-    }
-    part[tid] = s;
-    __syncthreads();
-    for (int o = 1; o < kSuffixThreads; o <<= 1) {  // part[tid] = sum of the runs from tid on
-      const double add = tid + o < kSuffixThreads ? part[tid + o] : 0.0;
-      __syncthreads();
-      part[tid] += add;
-      __syncthreads();
-    }
-    double run = carry + (tid + 1 < kSuffixThreads ? part[tid + 1] : 0.0);
+  for (int u = 0; u < kSuffixRun; ++u) sum += (double)run[u];
+  double sw = sum;  // the runs from this lane to the end of the warp
 #pragma unroll
-    for (int u = kSuffixRun - 1; u >= 0; --u) {
-      if (t0 + u < t1) {
-        run += (double)v[u];
-        dla[bh * T + t0 + u] = (float)run;
-      }
-    }
-    carry += part[0];
-    __syncthreads();
+  for (int o = 1; o < 32; o <<= 1) {
+    const double y = __shfl_down_sync(0xffffffffu, sw, o);
+    if (lane + o < 32) sw += y;
   }
+  if (lane == 0) wtot[warp] = sw;
+  __syncthreads();
+  if (tid == 0) {  // the warps from each one to the end of the part
+    double acc = 0.0;
+    for (int w = kWarps - 1; w >= 0; --w) {
+      acc += wtot[w];
+      wtot[w] = acc;
+    }
+    ptot[bh * P + part] = acc;
+  }
+  __syncthreads();
+  double acc = (warp + 1 < kWarps ? wtot[warp + 1] : 0.0) + (sw - sum);  // the part after this run
+  const int t0 = start + tid * kSuffixRun;
+#pragma unroll
+  for (int u = kSuffixRun - 1; u >= 0; --u) {
+    acc += (double)run[u];
+    if (tid * kSuffixRun + u < n) sfx[bh * T + t0 + u] = acc;
+  }
+}
+
+__global__ void __launch_bounds__(256) bwd_suffix_apply_kernel(const double* __restrict__ sfx,
+                                                               const double* __restrict__ ptot,
+                                                               float* __restrict__ dla, int T) {
+  __shared__ double off_s;
+  const int part = blockIdx.x, P = gridDim.x;
+  const size_t bh = blockIdx.y;
+  if (threadIdx.x == 0) {
+    double o = 0.0;
+    for (int q = P - 1; q > part; --q) o += ptot[bh * P + q];
+    off_s = o;
+  }
+  __syncthreads();
+  const double o = off_s;
+  const int start = part * kSuffixPart, n = min(kSuffixPart, T - start);
+  for (int x = threadIdx.x; x < n; x += 256) dla[bh * T + start + x] = (float)(sfx[bh * T + start + x] + o);
+}
+
+ll_status suffix_launch(const float* dc, double* sfx, double* ptot, float* dla, int BH, int T, cudaStream_t stream) {
+  const int P = (T + kSuffixPart - 1) / kSuffixPart;
+  bwd_suffix_part_kernel<<<dim3(P, BH), kSuffixThreads, 0, stream>>>(dc, sfx, ptot, T);
+  LL_CUDA_OK(cudaGetLastError());
+  bwd_suffix_apply_kernel<<<dim3(P, BH), 256, 0, stream>>>(sfx, ptot, dla, T);
+  LL_CUDA_OK(cudaGetLastError());
+  return LL_OK;
 }
 
 // ------------------------------------------------ d_k = d_v = 128, 64-token chunks
@@ -912,6 +950,8 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
   double* G = reinterpret_cast<double*>(ws + p.off_G);
   double* cum = reinterpret_cast<double*>(ws + p.off_cum);
   float* dc = reinterpret_cast<float*>(ws + p.off_dc);
+  double* sfx = reinterpret_cast<double*>(ws + p.off_sfx);
+  double* ptot = reinterpret_cast<double*>(ws + p.off_ptot);
   const bool f32 = s.io == LL_F32;
   float* dq32 = f32 ? static_cast<float*>(a.dq) : reinterpret_cast<float*>(ws + p.off_dq);
   float* dk32 = f32 ? static_cast<float*>(a.dk) : reinterpret_cast<float*>(ws + p.off_dk);
@@ -931,9 +971,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
                          cum, dc, a.err};
     const ll_status st = bwd_tc_launch(a, b);
     if (st != LL_OK) return st;
-    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
-    LL_CUDA_OK(cudaGetLastError());
-    return LL_OK;
+    return suffix_launch(dc, sfx, ptot, a.dlog_alpha, BH, s.T, a.stream);
   }
   if (fast_shape(s, p)) {
     LL_CUDA_OK(cudaFuncSetAttribute(fast::bwd_intra128_kernel<IO>, cudaFuncAttributeMaxDynamicSharedMemorySize,
@@ -954,9 +992,7 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
         k, v, a.log_alpha, a.lam, a.dlam, R, cum, dk32, dv32, static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc,
         s.T, s.L);
     LL_CUDA_OK(cudaGetLastError());
-    bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
-    LL_CUDA_OK(cudaGetLastError());
-    return LL_OK;
+    return suffix_launch(dc, sfx, ptot, a.dlog_alpha, BH, s.T, a.stream);
   }
 
   const size_t sm1 = intra_smem(Ce, s.dk, s.dv);
@@ -984,16 +1020,14 @@ ll_status launch_typed(const BwdArgs& a, const BwdPlan& p) {
       static_cast<IO*>(a.dk), static_cast<IO*>(a.dv), dc, s.T, s.dk, s.dv, s.L, Ce);
   LL_CUDA_OK(cudaGetLastError());
 
-  bwd_suffix_kernel<<<BH, kSuffixThreads, 0, a.stream>>>(dc, a.dlog_alpha, s.T);
-  LL_CUDA_OK(cudaGetLastError());
-  return LL_OK;
+  return suffix_launch(dc, sfx, ptot, a.dlog_alpha, BH, s.T, a.stream);
 }
 
 }  // namespace
 
 size_t bwd_simt_workspace(const ll_shape& s) { return plan_of(s).total; }
 
-int bwd_simt_launches(const ll_shape&) { return 5; }
+int bwd_simt_launches(const ll_shape&) { return 6; }
 
 ll_status bwd_simt_launch(const BwdArgs& a) {
   const BwdPlan p = plan_of(a.s);

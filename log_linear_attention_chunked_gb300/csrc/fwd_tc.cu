@@ -1300,13 +1300,14 @@ __global__ void __launch_bounds__(kTile) tc_ld_tile_totals_kernel(const float* _
   }
 }
 
-// Second step: their running sums over the tiles, float64, one warp per level:
-// cumL[(bh * Lx + h) * Nt + j] = sum of tot over tiles 0..j.
-__global__ void __launch_bounds__(256) tc_ld_tile_scan_kernel(const float* __restrict__ tot,
-                                                              double* __restrict__ cumL, int Nt, int Lx) {
-  const size_t bh = blockIdx.x;
-  const int lane = threadIdx.x & 31, h = threadIdx.x >> 5;
-  if (h >= Lx) return;
+// Second step: their running sums over the tiles, float64, one single-warp
+// CTA per (level, head) (float64 arithmetic is scarce on this GPU: spread it
+// over the SMs): cumL[(bh * Lx + h) * Nt + j] = sum of tot over tiles 0..j.
+__global__ void __launch_bounds__(32) tc_ld_tile_scan_kernel(const float* __restrict__ tot,
+                                                             double* __restrict__ cumL, int Nt, int Lx) {
+  const int h = blockIdx.x;
+  const size_t bh = blockIdx.y;
+  const int lane = threadIdx.x;
   double carry = 0.0;
   for (int base = 0; base < Nt; base += 32) {
     const int i = base + lane;
@@ -1493,8 +1494,8 @@ static ll_status tc_launch(const FwdArgs& a, bool ld) {
     tc_ld_tile_totals_kernel<<<dim3(plan.Nt, BH), kTile, 0, a.stream>>>(a.log_alpha, tot, stride, plan.Nt, s.L,
                                                                         plan.Lx);
     LL_CUDA_OK(cudaGetLastError());
-    tc_ld_tile_scan_kernel<<<BH, 256, 0, a.stream>>>(tot, reinterpret_cast<double*>(ws + plan.off_cum), plan.Nt,
-                                                     plan.Lx);
+    tc_ld_tile_scan_kernel<<<dim3(plan.Lx, BH), 32, 0, a.stream>>>(tot, reinterpret_cast<double*>(ws + plan.off_cum),
+                                                                   plan.Nt, plan.Lx);
     LL_CUDA_OK(cudaGetLastError());
   }
   if (a.state_in) {
