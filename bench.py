@@ -190,7 +190,7 @@ KERNEL_SOURCES = {
     "decode": ("decode.cu", "common.cuh"),
     "gdn_decode": ("gdn_decode.cu", "common.cuh"),
     "gdn": ("gdn_tc.cu", "common.cuh", "sm100.cuh"),             # dominant: the tensor-core level scan
-    "gdn_b": ("gdn.cu", "common.cuh", "sm100.cuh"),            # dominant: the single-state pass
+    "gdn_b": ("gdn_tc.cu", "common.cuh", "sm100.cuh"),         # dominant: the tensor-core preparation
     "mamba2_cont": ("fwd_tc.cu", "level_decay.cuh", "common.cuh", "sm100.cuh"),  # dominant: the tensor-core forward
     "mamba2_bwd": ("bwd_tc.cu", "bwd.cuh", "common.cuh", "sm100.cuh"),  # dominant: the query-side kernel
     "level_decay": ("fwd_tc.cu", "level_decay.cuh", "common.cuh", "sm100.cuh"),  # dominant: the tensor-core forward

@@ -30,6 +30,10 @@
 
 namespace llattn {
 
+// the reading-B forward on the tensor cores (gdn_tc.cu): bf16, d = 128
+size_t gdn_tc_b_workspace(const ll_shape& s);
+ll_status gdn_tc_b_launch(const FwdArgs& a);
+
 namespace {
 
 constexpr int kThreads = 256;
@@ -1352,11 +1356,13 @@ ll_status launch_b_typed(const FwdArgs& a, const GdnBPlan& b) {
 }  // namespace
 
 size_t gdn_b_workspace(const ll_shape& s) {
+  if (gdn_tc_supported(s) && fwd_tc_supported(s)) return gdn_tc_b_workspace(s);  // bf16 io: the tensor cores
   const GdnBPlan b = gdn_b_plan(s);
   return b.ok ? b.total : 0;
 }
 
 ll_status gdn_b_launch(const FwdArgs& a) {
+  if (gdn_tc_supported(a.s) && fwd_tc_supported(a.s)) return gdn_tc_b_launch(a);
   const GdnBPlan b = gdn_b_plan(a.s);
   if (!b.ok) return LL_ERR_UNSUPPORTED;
   if (a.ws_bytes < b.total) return LL_ERR_WORKSPACE;

@@ -781,6 +781,202 @@ __global__ void __launch_bounds__(kScanThreads, 1)
   }
 }
 
+// ------------------------------------------------------------------ kernel 2, reading B
+// Reading B (log-linear Mamba-2 on the delta rule's pseudo-values) needs one
+// gated-delta state and no levels: per chunk, with X the state at the chunk
+// start (X = 0 for the first chunk),
+//   U_c = U - W X^T            (the pseudo-values, written in bf16)
+//   X^T <- gamma X^T + Kt^T U_c^T
+// with U, W from the preparation above and Kt = diag(exp(g_end - g)) K.  The
+// layout is the level scan's: one CTA per (32 d_v rows, head), X^T in TMEM
+// columns 0..31, Y^T = W X^T in columns 256..287, U_c built in place of the
+// chunk's U^T slice (thread = token) and used there as the update's operand.
+__global__ void __launch_bounds__(kScanThreads, 1)
+    gdn_tc_scan_b_kernel(const __grid_constant__ CUtensorMap tw, const __grid_constant__ CUtensorMap tk,
+                         const __grid_constant__ CUtensorMap tu32, const float* __restrict__ log_alpha,
+                         __nv_bfloat16* __restrict__ uc_out, int T, int Nc, unsigned* err) {
+  extern __shared__ __align__(1024) unsigned char smem_raw[];
+  if (smem_u32(smem_raw) & 1023u) {
+    if (threadIdx.x == 0) atomicOr(err, kErrDeviceArg);
+    return;
+  }
+  unsigned char* s = smem_raw;
+  const int tid = threadIdx.x, q = tid >> 5, lane = tid & 31;
+  const int sl = blockIdx.x;  // d_v slice: rows 32 sl .. 32 sl + 31
+  const int bh = blockIdx.y;
+  float* qtot = reinterpret_cast<float*>(s + kSTab);
+  uint64_t* bars = reinterpret_cast<uint64_t*>(s + kSBars);
+  uint32_t* tmem_slot = reinterpret_cast<uint32_t*>(s + kSBars + kScanBars * 8);
+  const uint32_t sW = smem_u32(s + kSW);
+
+  auto load_w = [&](int c) {
+    const int r = bh * T + c * kC;
+    mbar_arrive_expect_tx(bars + SB_WQ, kTileB);
+    tma_load_2d(s + kSW, &tw, bars + SB_WQ, 0, r);
+    tma_load_2d(s + kSW + kHalf, &tw, bars + SB_WQ, 64, r);
+  };
+  auto load_ku = [&](int c) {
+    const int b = c & 1;
+    const int r = bh * T + c * kC;
+    unsigned char* kd = s + kSK + b * kTileB;
+    mbar_arrive_expect_tx(bars + SB_K0 + b, kTileB);
+    tma_load_2d(kd, &tk, bars + SB_K0 + b, 0, r);
+    tma_load_2d(kd + kHalf, &tk, bars + SB_K0 + b, 64, r);
+    unsigned char* ud = s + kSU + b * kSliceB;
+    const int ur = (bh * Nc + c) * kD + kSlice * sl;
+    mbar_arrive_expect_tx(bars + SB_U0 + b, kSliceB);
+    tma_load_2d(ud, &tu32, bars + SB_U0 + b, 0, ur);
+    tma_load_2d(ud + kHalf32, &tu32, bars + SB_U0 + b, 64, ur);
+  };
+
+  if (tid == 0) {
+    for (int b = 0; b < kScanBars; ++b) mbar_init(bars + b, 1);
+    fence_mbar_init();
+    if (Nc > 1) load_w(1);  // the first chunk reads no W (its state is zero)
+    load_ku(0);
+    if (Nc > 1) load_ku(1);
+  }
+  __syncwarp();
+  if (q == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+  constexpr uint32_t idY = idesc_bf16(128, kSlice, false, false);  // W (K) x X (K, N = 32)
+  constexpr uint32_t idX = idesc_bf16(128, kSlice, true, false);   // Kt^T (MN) x U_c (K, N = 32)
+  uint32_t nmma = 0;
+  auto commit_wait = [&]() {
+    if (tid == 0) umma_commit(bars + SB_MMA);
+    wait_bar(bars + SB_MMA, nmma & 1, err);
+    ++nmma;
+    __syncwarp();
+    tc_fence_after();
+  };
+
+  float la_n = log_alpha[(size_t)bh * T + tid];
+  uint32_t nw = 0;  // W loads waited for
+  for (int c = 0; c < Nc; ++c) {
+    const int b = c & 1;
+    const size_t rowt = (size_t)bh * T + (size_t)c * kC + tid;  // this thread's token
+    float x = la_n;
+    if (c + 1 < Nc) la_n = log_alpha[rowt + kC];
+    // cumulative log decay of the chunk
+#pragma unroll
+    for (int o = 1; o < 32; o <<= 1) {
+      const float y = __shfl_up_sync(0xffffffffu, x, o);
+      if (lane >= o) x += y;
+    }
+    if (lane == 31) qtot[q] = x;
+    __syncthreads();
+    float off = 0.f;
+    for (int qq = 0; qq < q; ++qq) off += qtot[qq];
+    const float g_t = x + off;
+    const float g_end = qtot[0] + qtot[1] + qtot[2] + qtot[3];
+    const float gam = ex2(g_end * kLog2e);
+    const float dec = ex2((g_end - g_t) * kLog2e);
+    __syncthreads();  // qtot is rewritten by the next chunk
+
+    // Kt = diag(exp(g_end - g)) K in place (row = this token)
+    wait_bar(bars + SB_K0 + b, (c >> 1) & 1, err);
+    unsigned char* kt = s + kSK + b * kTileB;
+#pragma unroll
+    for (int c8 = 0; c8 < 16; ++c8) {
+      uint4 v = *reinterpret_cast<const uint4*>(kt + swz16(tid, c8));
+      uint32_t* w = reinterpret_cast<uint32_t*>(&v);
+#pragma unroll
+      for (int e = 0; e < 4; ++e) {
+        const float2 f = unpack_bf16x2(w[e]);
+        w[e] = pack_bf16x2(f.x * dec, f.y * dec);
+      }
+      *reinterpret_cast<uint4*>(kt + swz16(tid, c8)) = v;
+    }
+    const uint32_t sKt = smem_u32(kt);
+
+    float yv[kSlice];
+#pragma unroll
+    for (int r = 0; r < kSlice; ++r) yv[r] = 0.f;
+    if (c > 0) {
+      // X as bf16 operand [32 rows d_v][128 d_k]; gamma X back into TMEM; Y^T = W X^T
+      float xv[32];
+      tmem_ld32(tl, xv);
+      tmem_ld_wait();
+      unsigned char* xb = s + kSX;
+#pragma unroll
+      for (int r = 0; r < kSlice; ++r)
+        *reinterpret_cast<__nv_bfloat16*>(xb + swz_off(r, tid, kSlice)) = __float2bfloat16_rn(xv[r]);
+      uint32_t wv[32];
+#pragma unroll
+      for (int r = 0; r < 32; ++r) wv[r] = __float_as_uint(gam * xv[r]);
+      tmem_st32(tl, wv);
+      tmem_st_wait();
+      wait_bar(bars + SB_WQ, nw & 1, err);
+      ++nw;
+      fence_proxy_async_shared();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t xbs = smem_u32(xb);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + 256, desc_k(sW, kk), desc_k32(xbs, kk), idY, kk > 0);
+      }
+      commit_wait();
+      if (tid == 0 && c + 1 < Nc) load_w(c + 1);  // the Y product has read W
+      tmem_ld32(tl + 256, yv);
+      tmem_ld_wait();
+    } else {
+      fence_proxy_async_shared();  // (the Kt writes, before the update product reads them)
+    }
+    // U_c = U - Y (row = this token, 32 d_v): in place of the U^T slice, and out
+    wait_bar(bars + SB_U0 + b, (c >> 1) & 1, err);
+    unsigned char* ub = s + kSU + b * kSliceB;
+    uint32_t pk[kSlice / 2];
+#pragma unroll
+    for (int r = 0; r < kSlice; r += 2) {
+      __nv_bfloat16* e0 = reinterpret_cast<__nv_bfloat16*>(ub + swz_off(r, tid, kSlice));
+      __nv_bfloat16* e1 = reinterpret_cast<__nv_bfloat16*>(ub + swz_off(r + 1, tid, kSlice));
+      const __nv_bfloat16 u0 = __float2bfloat16_rn(__bfloat162float(*e0) - yv[r]);
+      const __nv_bfloat16 u1 = __float2bfloat16_rn(__bfloat162float(*e1) - yv[r + 1]);
+      *e0 = u0;
+      *e1 = u1;
+      pk[r / 2] = (uint32_t)__bfloat16_as_ushort(u0) | ((uint32_t)__bfloat16_as_ushort(u1) << 16);
+    }
+    {
+      uint4* op = reinterpret_cast<uint4*>(uc_out + rowt * kD + kSlice * sl);
+#pragma unroll
+      for (int v = 0; v < 4; ++v) op[v] = make_uint4(pk[4 * v], pk[4 * v + 1], pk[4 * v + 2], pk[4 * v + 3]);
+    }
+    if (c + 1 < Nc) {
+      // X^T <- gamma X^T + Kt^T U_c^T (the first chunk: Kt^T U^T)
+      fence_proxy_async_shared();
+      tc_fence_before();
+      __syncthreads();
+      if (tid == 0) {
+        tc_fence_after();
+        const uint32_t ubs = smem_u32(ub);
+#pragma unroll
+        for (int kk = 0; kk < 8; ++kk)
+          umma_bf16(tmem, desc_mn(sKt, kk), desc_k32(ubs, kk), idX, (c > 0 || kk > 0) ? 1u : 0u);
+      }
+      commit_wait();
+    } else {
+      __syncthreads();
+    }
+    // K and U^T buffers of this chunk are free: the chunk after next
+    if (tid == 0 && c + 2 < Nc) load_ku(c + 2);
+  }
+  tc_fence_before();
+  __syncthreads();
+  if (q == 0) {
+    tc_fence_after();
+    tmem_dealloc(tmem, 512);
+  }
+}
+
 // ------------------------------------------------------------------ host side
 PFN_cuTensorMapEncodeTiled_v12000 encode_fn() {
   static PFN_cuTensorMapEncodeTiled_v12000 fn = nullptr;
@@ -836,6 +1032,11 @@ TcPlan tc_plan(const ll_shape& s) {
 
 }  // namespace
 
+// Reading B on the tensor cores: the preparation, the single-state scan into
+// the pseudo-values (bf16, after the preparation's buffers), then the
+// log-linear Mamba-2 forward on them (its workspace after that).
+static size_t b_uc_bytes(const ll_shape& s) { return align_up((size_t)s.B * s.H * s.T * kD * 2, 1024); }
+
 bool gdn_tc_supported(const ll_shape& s) {
   return s.io == LL_BF16 && s.dk == kD && s.dv == kD && s.T % kC == 0 && s.T / kC <= (1 << kMaxHeights) &&
          (long long)s.B * s.H * s.T <= (1ll << 31) - 1;
@@ -868,6 +1069,43 @@ ll_status gdn_tc_launch(const FwdArgs& a) {
   gdn_tc_scan_kernel<<<dim3(kD / kSlice, BH), kScanThreads, kScanSmem, a.stream>>>(tw, tqp, tk, tu32, sp);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
+}
+
+size_t gdn_tc_b_workspace(const ll_shape& s) {
+  return tc_plan(s).total + b_uc_bytes(s) + (fwd_tc_supported(s) ? fwd_tc_workspace(s) : 0);
+}
+
+ll_status gdn_tc_b_launch(const FwdArgs& a) {
+  const ll_shape& s = a.s;
+  if (!fwd_tc_supported(s)) return LL_ERR_UNSUPPORTED;
+  const TcPlan plan = tc_plan(s);
+  if (a.ws_bytes < gdn_tc_b_workspace(s)) return LL_ERR_WORKSPACE;
+  unsigned char* ws = static_cast<unsigned char*>(a.ws);
+  const int BH = s.B * s.H;
+  const uint64_t rows = (uint64_t)BH * s.T;
+  __nv_bfloat16* uc = reinterpret_cast<__nv_bfloat16*>(ws + plan.total);
+  CUtensorMap tq, tk, tv, tw, tqp, tut, toi, tu32;
+  if (!make_map(&tq, a.q, rows, kC) || !make_map(&tk, a.k, rows, kC) || !make_map(&tv, a.v, rows, kC) ||
+      !make_map(&tw, ws + plan.off_W, rows, kC) || !make_map(&tqp, ws + plan.off_Qp, rows, kC) ||
+      !make_map(&tut, ws + plan.off_Ut, rows, kC) || !make_map(&toi, ws + plan.off_Oi, rows, kC) ||
+      !make_map(&tu32, ws + plan.off_Ut, rows, kSlice))
+    return LL_ERR_CUDA;
+  PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err};
+  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem));
+  gdn_tc_prep_kernel<<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi, pp);
+  LL_CUDA_OK(cudaGetLastError());
+  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_scan_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem));
+  gdn_tc_scan_b_kernel<<<dim3(kD / kSlice, BH), kScanThreads, kScanSmem, a.stream>>>(tw, tk, tu32, a.log_alpha, uc,
+                                                                                      s.T, plan.Nc, a.err);
+  LL_CUDA_OK(cudaGetLastError());
+  FwdArgs f = a;
+  f.v = uc;
+  f.beta = nullptr;
+  f.state_out = nullptr;
+  f.scale_out = nullptr;
+  f.ws = ws + plan.total + b_uc_bytes(s);
+  f.ws_bytes = fwd_tc_workspace(s);
+  return fwd_tc_launch(f);
 }
 
 }  // namespace llattn

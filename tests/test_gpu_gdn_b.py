@@ -57,6 +57,24 @@ def test_matches_oracle(B, T, io, chunk):
     assert rel_err(_run(B, inp, chunk), _oracle(inp)) <= tol
 
 
+@pytest.mark.parametrize("T,la_mode", [(2048, "zero"), (2048, "slow"), (4096, "slow"), (128, "softplus")])
+def test_tensor_core_path_long_state(B, T, la_mode):
+    """bf16, d = 128, T a multiple of 128: the tensor-core preparation and
+    single-state scan.  alpha = 1 and slow decay keep the gated-delta state
+    alive over every chunk, so each chunk's pseudo-values depend on all the
+    earlier ones."""
+    inp = synth.make_inputs(_cfg(T, io="bf16"), la_mode=la_mode, tag=f"gbtc{T}{la_mode}")
+    assert rel_err(_run(B, inp, 64), _oracle(inp)) <= TOL_BF16
+
+
+def test_tensor_core_path_full_size_heads(B):
+    """The benchmark's per-head shape (T=4096, d=128, bf16) at its own decay,
+    two heads."""
+    cfg = dict(synth.WORKLOADS["gdn_b_bf16_t4k"], B=1, H=2)
+    inp = synth.make_inputs(cfg)
+    assert rel_err(_run(B, inp, cfg["chunk"]), _oracle(inp)) <= TOL_BF16
+
+
 def test_differs_from_reading_a(B):
     """The two readings are different operators (same inputs, outputs far apart)."""
     inp = synth.make_inputs(_cfg(512, io="f32"), la_mode="zero", tag="gba")
