@@ -49,7 +49,7 @@ __device__ __forceinline__ float warp_sum(float x) {
 }
 
 template <typename IO, int DK>
-__global__ void __launch_bounds__(kWarps * 32) decode_kernel(int H, int dv, int Ls, const int64_t* __restrict__ tpos,
+__global__ void __launch_bounds__(kWarps * 32, 4) decode_kernel(int H, int dv, int Ls, const int64_t* __restrict__ tpos,
                                                              const IO* __restrict__ q, const IO* __restrict__ k,
                                                              const IO* __restrict__ v,
                                                              const float* __restrict__ log_alpha,
