@@ -135,6 +135,9 @@ struct PrepParams {
   unsigned* err;
 };
 
+// kB: reading B's preparation, which needs only U and W (no Q, Aqk, Q' or
+// intra output: no Q load, three products fewer, two stores fewer).
+template <bool kB>
 __global__ void __launch_bounds__(kPrepThreads, 1)
     gdn_tc_prep_kernel(const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
                        const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tw,
@@ -167,11 +170,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     mbar_init(bars + 0, 1);
     mbar_init(bars + 1, 1);
     fence_mbar_init();
-    mbar_arrive_expect_tx(bars + 0, 3 * kTileB);
+    mbar_arrive_expect_tx(bars + 0, (kB ? 2 : 3) * kTileB);
     tma_load_2d(s + kPK, &tk, bars + 0, 0, row0);
     tma_load_2d(s + kPK + kHalf, &tk, bars + 0, 64, row0);
-    tma_load_2d(s + kPQ, &tq, bars + 0, 0, row0);
-    tma_load_2d(s + kPQ + kHalf, &tq, bars + 0, 64, row0);
+    if (!kB) {
+      tma_load_2d(s + kPQ, &tq, bars + 0, 0, row0);
+      tma_load_2d(s + kPQ + kHalf, &tq, bars + 0, 64, row0);
+    }
     tma_load_2d(s + kPV, &tv, bars + 0, 0, row0);
     tma_load_2d(s + kPV + kHalf, &tv, bars + 0, 64, row0);
   }
@@ -205,7 +210,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   }
   float lam8[8];  // lambda of the intra-chunk levels 0..7 of row i
 #pragma unroll
-  for (int l = 0; l < 8; ++l) lam8[l] = p.lam[(size_t)(row0 + i) * p.L + l];
+  for (int l = 0; l < 8; ++l) lam8[l] = kB ? 0.f : p.lam[(size_t)(row0 + i) * p.L + l];
   __syncthreads();
 
   // ---- K K^T -> cols 0..127, Q K^T -> cols 128..255
@@ -213,7 +218,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   if (tid == 0) {
     tc_fence_after();
     mma_128(tmem + 0, sK, false, sK, false, 0);
-    mma_128(tmem + 128, sQ, false, sK, false, 0);
+    if (!kB) mma_128(tmem + 128, sQ, false, sK, false, 0);
     umma_commit(bars + 1);
   }
   wait_bar(bars + 1, 0, p.err);
@@ -227,7 +232,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const int j0 = 64 * hf + 32 * c32;
       float kk[32], qk[32];
       tmem_ld32(tl + j0, kk);
-      tmem_ld32(tl + 128 + j0, qk);
+      if (!kB) tmem_ld32(tl + 128 + j0, qk);
       tmem_ld_wait();
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
@@ -249,7 +254,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
         }
       }
 #pragma unroll
-      for (int c8 = 0; c8 < 4; ++c8) {
+      for (int c8 = 0; c8 < 4 && !kB; ++c8) {
         uint4 w;
         w.x = pack_bf16x2(qk[8 * c8], qk[8 * c8 + 1]);
         w.y = pack_bf16x2(qk[8 * c8 + 2], qk[8 * c8 + 3]);
@@ -371,7 +376,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   if (tid == 0) {
     tc_fence_after();
     mma_128(tmem + 0, sV, true, sL, false, 0);
-    mma_128(tmem + 128, sA, false, sL, true, 0);
+    if (!kB) mma_128(tmem + 128, sA, false, sL, true, 0);
     mma_128(tmem + 256, sT, false, sK, true, 0);
     umma_commit(bars + 1);
   }
@@ -386,13 +391,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       const int j0 = 64 * hf + 32 * c32;
       float w[32], cl[32], u[32];
       tmem_ld32(tl + 256 + j0, w);
-      tmem_ld32(tl + 128 + j0, cl);
+      if (!kB) tmem_ld32(tl + 128 + j0, cl);
       tmem_ld32(tl + 0 + j0, u);
       tmem_ld_wait();
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = j0 + jj;
-        cl[jj] = j <= i ? cl[jj] * lam8[32 - __clz(i ^ j)] : 0.f;
+        cl[jj] = (!kB && j <= i) ? cl[jj] * lam8[32 - __clz(i ^ j)] : 0.f;
       }
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
@@ -418,15 +423,26 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // Q'' = Aqk W -> 0, intra = Cm V -> 128; store U^T and W
   if (tid == 0) {
     tc_fence_after();
-    mma_128(tmem + 0, sA, false, sT, true, 0);
-    mma_128(tmem + 128, sL, false, sV, true, 0);
-    umma_commit(bars + 1);
+    if (!kB) {
+      mma_128(tmem + 0, sA, false, sT, true, 0);
+      mma_128(tmem + 128, sL, false, sV, true, 0);
+      umma_commit(bars + 1);
+    }
     const int urow = (bh * p.Nc + c) * kD;
     tma_store_2d(&tut, s + kPK, 0, urow);
     tma_store_2d(&tut, s + kPK + kHalf, 64, urow);
     tma_store_2d(&tw, s + kPT, 0, row0);
     tma_store_2d(&tw, s + kPT + kHalf, 64, row0);
     bulk_commit();
+    if (kB) bulk_wait0();
+  }
+  if (kB) {  // reading B: U^T and W are all it needs
+    __syncwarp();
+    if (warp == 0) {
+      tc_fence_after();
+      tmem_dealloc(tmem, 512);
+    }
+    return;
   }
   wait_bar(bars + 1, 0, p.err);
   __syncwarp();
@@ -1059,8 +1075,10 @@ ll_status gdn_tc_launch(const FwdArgs& a) {
     return LL_ERR_CUDA;
 
   PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err};
-  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem));
-  gdn_tc_prep_kernel<<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi, pp);
+  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kPrepSmem));
+  gdn_tc_prep_kernel<false><<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi,
+                                                                                       pp);
   LL_CUDA_OK(cudaGetLastError());
 
   ScanParams sp{a.log_alpha, a.lam, reinterpret_cast<const __nv_bfloat16*>(ws + plan.off_Oi),
@@ -1091,8 +1109,10 @@ ll_status gdn_tc_b_launch(const FwdArgs& a) {
       !make_map(&tu32, ws + plan.off_Ut, rows, kSlice))
     return LL_ERR_CUDA;
   PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err};
-  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kPrepSmem));
-  gdn_tc_prep_kernel<<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi, pp);
+  LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
+                                  (int)kPrepSmem));
+  gdn_tc_prep_kernel<true><<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi,
+                                                                                      pp);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_scan_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem));
   gdn_tc_scan_b_kernel<<<dim3(kD / kSlice, BH), kScanThreads, kScanSmem, a.stream>>>(tw, tk, tu32, a.log_alpha, uc,
