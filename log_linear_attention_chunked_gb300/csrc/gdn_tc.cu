@@ -35,6 +35,7 @@
 // summed in registers and added to the intra output.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "common.cuh"
@@ -133,6 +134,8 @@ struct PrepParams {
   const float* lam;
   int T, L, Nc;
   unsigned* err;
+  const __nv_bfloat16 *q, *k, *v;  // (the L2 prefetch of the next item's rows)
+  int BH;
 };
 
 // kB: reading B's preparation, which needs only U and W (no Q, Aqk, Q' or
@@ -152,9 +155,6 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   const int tid = threadIdx.x, warp = tid >> 5, lane = tid & 31;
   const int q = warp & 3, hf = warp >> 2;
   const int i = 32 * q + lane;  // this thread's row (TMEM lane)
-  const int c = blockIdx.x;
-  const int bh = blockIdx.y;
-  const int row0 = bh * p.T + c * kC;
   float* gs = reinterpret_cast<float*>(s + kPTab);
   float* es = gs + 128;
   float* bs = es + 128;
@@ -170,6 +170,28 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     mbar_init(bars + 0, 1);
     mbar_init(bars + 1, 1);
     fence_mbar_init();
+  }
+  __syncwarp();
+  if (warp == 0) {
+    tmem_alloc(tmem_slot, 512);
+    tmem_relinquish();
+  }
+  tc_fence_before();
+  __syncthreads();
+  tc_fence_after();
+  const uint32_t tmem = *tmem_slot;
+  const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
+  constexpr uint32_t kProducts = kB ? 2 : 3;  // product commits per item
+  const int items = p.Nc * p.BH;
+  // persistent: item w = (chunk w mod Nc, head w / Nc), one after another
+  uint32_t k_it = 0;
+  for (int w = blockIdx.x; w < items; w += gridDim.x, ++k_it) {
+  const int c = w % p.Nc;
+  const int bh = w / p.Nc;
+  const int row0 = bh * p.T + c * kC;
+  const uint32_t pb = k_it * kProducts;  // product commits before this item
+  if (tid == 0) {
+    bulk_wait_read0();  // the previous item's stores have read their tiles
     mbar_arrive_expect_tx(bars + 0, (kB ? 2 : 3) * kTileB);
     tma_load_2d(s + kPK, &tk, bars + 0, 0, row0);
     tma_load_2d(s + kPK + kHalf, &tk, bars + 0, 64, row0);
@@ -179,11 +201,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     }
     tma_load_2d(s + kPV, &tv, bars + 0, 0, row0);
     tma_load_2d(s + kPV + kHalf, &tv, bars + 0, 64, row0);
-  }
-  __syncwarp();
-  if (warp == 0) {
-    tmem_alloc(tmem_slot, 512);
-    tmem_relinquish();
+    const int wn = w + (int)gridDim.x;  // the next item's rows into L2 meanwhile
+    if (wn < items) {
+      const size_t rn = (size_t)(wn / p.Nc) * p.T + (size_t)(wn % p.Nc) * kC;
+      bulk_prefetch_l2(p.k + rn * kD, kTileB);
+      if (!kB) bulk_prefetch_l2(p.q + rn * kD, kTileB);
+      bulk_prefetch_l2(p.v + rn * kD, kTileB);
+    }
   }
   // inclusive cumsum of log_alpha over the chunk (both halves compute it)
   const float la = p.log_alpha[row0 + i];
@@ -195,11 +219,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     if (lane >= o) x += y;
   }
   if (hf == 0 && lane == 31) qtot[q] = x;
-  tc_fence_before();
   __syncthreads();
-  tc_fence_after();
-  const uint32_t tmem = *tmem_slot;
-  const uint32_t tl = tmem + ((uint32_t)(32 * q) << 16);
   float off = 0.f;
   for (int qq = 0; qq < q; ++qq) off += qtot[qq];
   const float g_i = x + off;
@@ -214,14 +234,14 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   __syncthreads();
 
   // ---- K K^T -> cols 0..127, Q K^T -> cols 128..255
-  wait_bar(bars + 0, 0, p.err);
+  wait_bar(bars + 0, k_it & 1, p.err);
   if (tid == 0) {
     tc_fence_after();
     mma_128(tmem + 0, sK, false, sK, false, 0);
     if (!kB) mma_128(tmem + 128, sQ, false, sK, false, 0);
     umma_commit(bars + 1);
   }
-  wait_bar(bars + 1, 0, p.err);
+  wait_bar(bars + 1, pb & 1, p.err);
   __syncwarp();
   tc_fence_after();
   // L_ij = beta_i (k_i.k_j) G_ij (j < i), packed lower blocks; Aqk_ij = (q_i.k_j) G_ij (j <= i), bf16 tile
@@ -380,7 +400,7 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     mma_128(tmem + 256, sT, false, sK, true, 0);
     umma_commit(bars + 1);
   }
-  wait_bar(bars + 1, 1, p.err);
+  wait_bar(bars + 1, (pb + 1) & 1, p.err);
   __syncwarp();
   tc_fence_after();
   // W (bf16, into Tbe's space: the B operand of Aqk W and the stored W);
@@ -434,17 +454,9 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tma_store_2d(&tw, s + kPT, 0, row0);
     tma_store_2d(&tw, s + kPT + kHalf, 64, row0);
     bulk_commit();
-    if (kB) bulk_wait0();
   }
-  if (kB) {  // reading B: U^T and W are all it needs
-    __syncwarp();
-    if (warp == 0) {
-      tc_fence_after();
-      tmem_dealloc(tmem, 512);
-    }
-    return;
-  }
-  wait_bar(bars + 1, 0, p.err);
+  if (kB) continue;  // reading B: U^T and W are all it needs
+  wait_bar(bars + 1, (pb + 2) & 1, p.err);
   __syncwarp();
   tc_fence_after();
   // Q' = diag(e) Q - Aqk W (into Aqk's space), intra (into Cm's space)
@@ -483,9 +495,11 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
     tma_store_2d(&toi, s + kPL, 0, row0);
     tma_store_2d(&toi, s + kPL + kHalf, 64, row0);
     bulk_commit();
-    bulk_wait0();
   }
-  __syncwarp();
+  }  // items
+  if (tid == 0) bulk_wait0();
+  tc_fence_before();
+  __syncthreads();
   if (warp == 0) {
     tc_fence_after();
     tmem_dealloc(tmem, 512);
@@ -1021,6 +1035,16 @@ bool make_map(CUtensorMap* m, const void* base, uint64_t rows, uint32_t box_rows
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// CTAs of the persistent preparation: one per SM (its shared memory allows
+// no second), at most one per item.
+cudaError_t prep_blocks(int items, int* grid) {
+  int dev = 0, sms = 0;
+  cudaError_t e = cudaGetDevice(&dev);
+  if (e == cudaSuccess) e = cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev);
+  *grid = std::max(1, std::min(items, sms));
+  return e;
+}
+
 int heights_of(int Nc) {
   int h = 0;
   while ((1 << h) < Nc) ++h;  // bit_length(Nc - 1)
@@ -1074,11 +1098,13 @@ ll_status gdn_tc_launch(const FwdArgs& a) {
       !make_map(&tu32, ws + plan.off_Ut, rows, kSlice))
     return LL_ERR_CUDA;
 
-  PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err};
+  PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err, static_cast<const __nv_bfloat16*>(a.q),
+                static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v), BH};
   LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel<false>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kPrepSmem));
-  gdn_tc_prep_kernel<false><<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi,
-                                                                                       pp);
+  int prep_grid = 0;
+  LL_CUDA_OK(prep_blocks(plan.Nc * BH, &prep_grid));
+  gdn_tc_prep_kernel<false><<<prep_grid, kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi, pp);
   LL_CUDA_OK(cudaGetLastError());
 
   ScanParams sp{a.log_alpha, a.lam, reinterpret_cast<const __nv_bfloat16*>(ws + plan.off_Oi),
@@ -1108,11 +1134,13 @@ ll_status gdn_tc_b_launch(const FwdArgs& a) {
       !make_map(&tut, ws + plan.off_Ut, rows, kC) || !make_map(&toi, ws + plan.off_Oi, rows, kC) ||
       !make_map(&tu32, ws + plan.off_Ut, rows, kSlice))
     return LL_ERR_CUDA;
-  PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err};
+  PrepParams pp{a.log_alpha, a.beta, a.lam, s.T, s.L, plan.Nc, a.err, static_cast<const __nv_bfloat16*>(a.q),
+                static_cast<const __nv_bfloat16*>(a.k), static_cast<const __nv_bfloat16*>(a.v), BH};
   LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_prep_kernel<true>, cudaFuncAttributeMaxDynamicSharedMemorySize,
                                   (int)kPrepSmem));
-  gdn_tc_prep_kernel<true><<<dim3(plan.Nc, BH), kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi,
-                                                                                      pp);
+  int prep_grid = 0;
+  LL_CUDA_OK(prep_blocks(plan.Nc * BH, &prep_grid));
+  gdn_tc_prep_kernel<true><<<prep_grid, kPrepThreads, kPrepSmem, a.stream>>>(tq, tk, tv, tw, tqp, tut, toi, pp);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(gdn_tc_scan_b_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)kScanSmem));
   gdn_tc_scan_b_kernel<<<dim3(kD / kSlice, BH), kScanThreads, kScanSmem, a.stream>>>(tw, tk, tu32, a.log_alpha, uc,
