@@ -38,6 +38,7 @@
 // whose rows leave by bulk copies (or bulk reductions) from shared memory.
 #include <cudaTypedefs.h>
 
+#include <algorithm>
 #include <atomic>
 
 #include "bwd.cuh"
@@ -275,7 +276,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
     __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dkp, __nv_bfloat16* __restrict__ dvp,
     float* __restrict__ dlam,
-    float* __restrict__ S, double* __restrict__ tot, float* __restrict__ dc, int T, int L, unsigned* err) {
+    float* __restrict__ S, double* __restrict__ tot, float* __restrict__ dc, int T, int L, int N, int BH,
+    unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kIntraEnd);
@@ -287,20 +289,35 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
-  const int c = blockIdx.x, N = gridDim.x;
-  const size_t bh = blockIdx.y;
   const int tid = threadIdx.x;
-  const size_t row0 = bh * T + (size_t)c * kT;
-  const int nv = min(kT, T - c * kT);
-  const bool tma = use_tma && nv == kT;  // a partial tile: its missing rows are zeros, staged by the threads
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
   }
+  const uint32_t tmem = setup_tmem<512>(bar, slot);
+  // persistent: tile item w = (tile w mod N, head w / N), one after another;
+  // each item's inputs are staged in L2 while the previous one is computed
+  uint32_t k_it = 0;
+  for (int w = blockIdx.x; w < N * BH; w += gridDim.x, ++k_it) {
+  const int c = w % N;
+  const size_t bh = (size_t)(w / N);
+  const size_t row0 = bh * T + (size_t)c * kT;
+  const int nv = min(kT, T - c * kT);
+  const bool tma = use_tma && nv == kT;  // a partial tile: its missing rows are zeros, staged by the threads
   tile_cumsum(cs, log_alpha, row0, nv);
   if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
-  const uint32_t tmem = setup_tmem<512>(bar, slot);
   bool ok = true;
+  if (tid == 0) {
+    const int wn = w + (int)gridDim.x;
+    if (wn < N * BH) {
+      const size_t rn = (size_t)(wn / N) * T + (size_t)(wn % N) * kT;
+      const uint32_t bytes = (uint32_t)(min(kT, T - (wn % N) * kT) * kD * 2);
+      bulk_prefetch_l2(q + rn * kD, bytes);
+      bulk_prefetch_l2(k + rn * kD, bytes);
+      bulk_prefetch_l2(v + rn * kD, bytes);
+      bulk_prefetch_l2(dout + rn * kD, bytes);
+    }
+  }
   if (tma) {
     if (tid == 0) {
       mbar_arrive_expect_tx(inbar, 4 * kTileB);
@@ -309,7 +326,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
       tma_tile(base + kIntraV, &tv, inbar, row0);
       tma_tile(base + kIntraG, &tg, inbar, row0);
     }
-    ok = wait_phase(inbar, 0, err, abort_s);
+    ok = wait_phase(inbar, k_it & 1, err, abort_s);
   } else if (tid < kT) {
     stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
     stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);
@@ -485,6 +502,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     }
     bulk_wait_read0();  // the copies have read their rows; the writes complete with the grid
   }
+  __syncthreads();  // every staged row has been read before the next item's tiles land
+  }  // items
   release_tmem<512>(tmem);
 }
 
@@ -826,8 +845,14 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int use_tma = rows <= 0x7fffffffull && tile_map(&tq, q, rows) && tile_map(&tk, k, rows) &&
                       tile_map(&tv, v, rows) && tile_map(&tg, dout, rows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_intra_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)intra_smem()));
-  bwd_tc_intra_kernel<<<grid, kIntraThreads, intra_smem(), a.stream>>>(tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp,
-                                                                  b.dvp, a.dlam, b.S, b.tot, b.dc, s.T, s.L, b.err);
+  int sms = 0, dev = 0;
+  LL_CUDA_OK(cudaGetDevice(&dev));
+  LL_CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
+  const int items = N * BH;
+  const int intra_grid = std::max(1, std::min(items, sms));  // persistent, one CTA per SM
+  bwd_tc_intra_kernel<<<intra_grid, kIntraThreads, intra_smem(), a.stream>>>(
+      tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp, b.dvp, a.dlam, b.S, b.tot, b.dc, s.T,
+      s.L, N, BH, b.err);
   LL_CUDA_OK(cudaGetLastError());
   // the query kernel reads the nodes' bf16 tiles only: no float32 copy where the Fenwick kernel can skip it
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum, false);
