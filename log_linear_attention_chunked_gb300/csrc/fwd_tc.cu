@@ -397,16 +397,17 @@ __device__ void producer_levels(const Ctx& c, const CUtensorMap* tf) {
       const bool pre = kCont && !((jp >> h) & 1);
       const size_t node = pre ? (size_t)p.BH * p.Nt + (size_t)bhp * kPreSlots + h
                               : (size_t)bhp * p.Nt + node_of_level(jp, h);
+      // the decay from the end of the node's block to the start of the tile:
+      // the node totals of the lower set bits, or (per-level mode) level
+      // 8 + h's own decays over those tiles (read before the node's wait)
+      const float dlv = kLD ? ld_span(p, bhp, h, jp & ~((1 << h) - 1), jp) : 0.f;
       float g = 0.f;
       if (!pre) {
         const uint64_t w = wait_flag(c, p.flags, node);
         fence_proxy_async_global();
         g = flag_g(w);
       }
-      // the decay from the end of the node's block to the start of the tile:
-      // the node totals of the lower set bits, or (per-level mode) level
-      // 8 + h's own decays over those tiles
-      dl[16 * (it & 1) + l] = kLD ? ld_span(p, bhp, h, jp & ~((1 << h) - 1), jp) : D;
+      dl[16 * (it & 1) + l] = kLD ? dlv : D;
       D += g;
       st_release_cta_u32(nlr + (it & 1), ((uint32_t)it << 8) | ++l);
       const int fs = fcnt & 1;
@@ -1013,6 +1014,9 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
     const int cto = __ffs(~j) - 1;  // trailing ones of j
     for (int m = 0; m < cto; ++m) {
       const size_t child = node_j - ((size_t)1 << m);
+      // per-level mode: the child's keys sit at level 8 + m over tiles (j - 2^m, j]
+      // (read before the child's wait)
+      const float dm = kLD ? ld_span(p, bh, m, j - (1 << m) + 1, j + 1) : 0.f;
       if (leader) {
         const uint64_t w = wait_flag(c, p.flags, child);
         fence_proxy_async_global();
@@ -1028,8 +1032,7 @@ __device__ void node_warps(const Ctx& c, uint32_t tmem, int warp, int lane, cons
       ++cf;
       __syncwarp();
       const float g = *gch;
-      // per-level mode: the child's keys sit at level 8 + m over tiles (j - 2^m, j]
-      const float sc = ex2((kLD ? ld_span(p, bh, m, j - (1 << m) + 1, j + 1) : D) * kLog2e);
+      const float sc = ex2((kLD ? dm : D) * kLog2e);
       // row t of the child, 16-byte chunk c8 of its 128-byte-swizzled tile
 #pragma unroll
       for (int c32 = 0; c32 < 4; ++c32) {
