@@ -1117,6 +1117,13 @@ __global__ void __launch_bounds__(kThreads, 1)
 
   if (threadIdx.x == 0) {
     *abort_s = 0;
+    // the level producer's step-tagged counts (and the decays they cover)
+    // start below every tag: shared memory keeps an earlier launch's values,
+    // which a back half would otherwise take for this launch's
+    uint32_t* nlr = reinterpret_cast<uint32_t*>(base + kOffNode + 160);
+    float* dl = reinterpret_cast<float*>(base + kOffNode);
+    nlr[0] = nlr[1] = 0;
+    for (int i = 0; i < 32; ++i) dl[i] = 0.f;
     for (int b = 0; b < kNumBars; ++b) mbar_init(bars + b, 1);
     fence_mbar_init();
     prefetch_tmap(&tq);

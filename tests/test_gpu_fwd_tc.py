@@ -234,3 +234,19 @@ def test_full_size_ragged_sampled_rows(B):
     out = _run_ragged(B, inp)
     rows = np.array(sorted(set(list(_sampled_rows(16384 - 128, per_tile=(0, 127))) + list(range(16384 - 128, 16384 - 37)))))
     assert _check_sampled(out, inp, rows) <= TOL_BF16
+
+
+@pytest.mark.parametrize("lvl", [8, 11])
+def test_repeated_calls_two_tiles_per_cta(B, lvl):
+    """Back-to-back calls at H = 2, T = 16384 (256 tiles on 152 CTAs: most
+    CTAs take two tiles, so the second tile's level decays are the first
+    use of one slot of the producer's hand-over in a launch).  Shared memory
+    keeps the previous launch's values there; every call must still match
+    the oracle, a one-hot lambda at the first tile level (8) or a higher one
+    (11) making any wrong level decay visible."""
+    T = 16384
+    inp = synth.make_inputs(_cfg(T, H=2), la_mode="slow", lam_mode="onehot", lam_level=lvl, tag=f"tcrep{lvl}")
+    rows = _sampled_rows(T, per_tile=(0, 77))
+    for _ in range(4):
+        out = _run(B, inp)
+        assert _check_sampled(out, inp, rows) <= TOL_BF16, lvl
