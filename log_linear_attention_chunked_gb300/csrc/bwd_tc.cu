@@ -67,6 +67,16 @@ __device__ __forceinline__ void bulk_reduce_add_f32(void* dst, const void* src, 
                : "memory");
 }
 
+// Element-wise float32 add of one [128 x 32] box (128-byte swizzle) from shared
+// memory into a [rows, 128] float32 tensor at column x, row y, by the TMA;
+// tracked by the issuing thread's bulk groups.
+__device__ __forceinline__ void tma_reduce_add_box(const CUtensorMap* map, const void* src, int x, int y) {
+  asm volatile("cp.reduce.async.bulk.tensor.2d.global.shared::cta.add.tile.bulk_group [%0, {%2, %3}], [%1];" ::"l"(
+                   reinterpret_cast<uint64_t>(map)),
+               "r"(smem_u32(src)), "r"(x), "r"(y)
+               : "memory");
+}
+
 // Bulk copy of a contiguous shared-memory range to global memory (16-byte
 // aligned addresses, size a multiple of 16), tracked by the thread's bulk groups.
 __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t bytes) {
@@ -76,6 +86,9 @@ __device__ __forceinline__ void bulk_store(void* dst, const void* src, uint32_t 
 }
 
 constexpr int kRowP = kD + 4;  // float pitch of rows staged for bulk copies (conflict-free row writes)
+// one [128 x 32] float32 box (128-byte swizzle) of a staged float32 tile: 16 KB
+constexpr uint32_t kRBox = kT * 32 * 4;
+static_assert(4 * kRBox <= kT * kRowP * 4, "a swizzled float32 tile fits the row staging's space");
 
 // byte offset of the 16-byte chunk c8 (elements 8 c8 .. 8 c8 + 7) of row r of a tile
 __device__ __forceinline__ uint32_t swz(int r, int c8) {
@@ -272,6 +285,8 @@ __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
 __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tk,
     const __grid_constant__ CUtensorMap tv, const __grid_constant__ CUtensorMap tg, int use_tma,
+    const __grid_constant__ CUtensorMap tdq, const __grid_constant__ CUtensorMap tdk,
+    const __grid_constant__ CUtensorMap tdv, const __grid_constant__ CUtensorMap tS, int use_omap,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v,
     const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha, const float* __restrict__ lam,
     __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dkp, __nv_bfloat16* __restrict__ dvp,
@@ -459,6 +474,55 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   }
   ok = ok && wait_phase(bar, 1, err, abort_s);
   tc_fence_after();
+  if (use_omap && nv == kT) {
+    // Every operand tile is free now: each output is staged in shared memory
+    // (two alternating buffers over the tiles) in the layout of its TMA boxes
+    // and written by thread 0's tensor stores: the in-tile parts of dq, dk, dv
+    // as bf16 tiles (two [128 x 64] boxes; the later kernels add the
+    // inter-tile parts in float32), the chunk state S_c as float32 (four
+    // [128 x 32] boxes).  Before each barrier thread 0 waits until its earlier
+    // stores have read their buffer, which the staging after the barrier reuses.
+    const int r = i;  // this thread's half row: columns 64 hf .. 64 hf + 63
+#pragma unroll 1
+    for (int o = 0; o < 4; ++o) {
+      unsigned char* buf = base + (o & 1) * (kT * kRowP * 4);
+#pragma unroll 1
+      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+        float x[32];
+        tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
+        tmem_ld_wait();
+        if (o == 3) {
+          unsigned char* box = buf + cb * kRBox + r * 128;
+#pragma unroll
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<float4*>(box + ((ch ^ (r & 7)) << 4)) =
+                make_float4(x[4 * ch], x[4 * ch + 1], x[4 * ch + 2], x[4 * ch + 3]);
+        } else {
+#pragma unroll
+          for (int w = 0; w < 4; ++w)
+            *reinterpret_cast<uint4*>(buf + swz(r, 4 * cb + w)) =
+                make_uint4(pack_bf16x2(x[8 * w], x[8 * w + 1]), pack_bf16x2(x[8 * w + 2], x[8 * w + 3]),
+                           pack_bf16x2(x[8 * w + 4], x[8 * w + 5]), pack_bf16x2(x[8 * w + 6], x[8 * w + 7]));
+        }
+      }
+      fence_proxy_async_shared();
+      if (tid == 0) bulk_wait_read0();
+      __syncthreads();
+      if (tid == 0 && ok) {
+        if (o == 3) {
+          const int y = (int)((bh * N + c) * kD);
+#pragma unroll
+          for (int cb = 0; cb < 4; ++cb) tma_store_2d(&tS, buf + cb * kRBox, 32 * cb, y);
+        } else {
+          const CUtensorMap* m = o == 0 ? &tdq : o == 1 ? &tdk : &tdv;
+          tma_store_2d(m, buf, 0, (int)row0);
+          tma_store_2d(m, buf + kHalf, 64, (int)row0);
+        }
+        bulk_commit();
+      }
+    }
+    if (tid == 0) bulk_wait_read0();  // the writes complete with the grid
+  } else
   {
     // Every operand tile is free now: each output row is staged in shared
     // memory (two alternating buffers of padded rows over the tiles) and
@@ -516,6 +580,7 @@ constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + kT * 4 + 64; }
 
 __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
+    const __grid_constant__ CUtensorMap tr, int use_rmap,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
     const __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam,
@@ -620,28 +685,54 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
         }
       }
       if (hf == 1) qpart[i] = part;
-      // row e' = i of this tile's part of R_e: staged in shared memory, then
-      // added into R_e by the bulk-copy unit (a 256-byte reduction per half row)
-      float* rrow = reinterpret_cast<float*>(base + kQryR) + i * kRowP;
-      bulk_wait_read0();  // the previous level's reduction has read this row
+      if (use_rmap) {
+        // this tile's part of R_e staged as four [128 x 32] float32 boxes
+        // (128-byte swizzle), row e' = i; thread 0 adds them into R_e by four
+        // tensor reductions after the level's barrier (it has waited for the
+        // previous level's to read the boxes before issuing this level's products)
 #pragma unroll 1
-      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-        float x[32];
-        tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
-        tmem_ld_wait();
+        for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+          float x[32];
+          tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
+          tmem_ld_wait();
+          unsigned char* box = base + kQryR + cb * kRBox + i * 128;
 #pragma unroll
-        for (int u = 0; u < 32; u += 4)
-          *reinterpret_cast<float4*>(rrow + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
-      }
-      if (ok) {
+          for (int ch = 0; ch < 8; ++ch)
+            *reinterpret_cast<float4*>(box + ((ch ^ (i & 7)) << 4)) =
+                make_float4(x[4 * ch], x[4 * ch + 1], x[4 * ch + 2], x[4 * ch + 3]);
+        }
         fence_proxy_async_shared();
-        bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD + 64 * hf, rrow + 64 * hf, 64 * 4);
-        bulk_commit();
+      } else {
+        // row e' = i of this tile's part of R_e: staged in shared memory, then
+        // added into R_e by the bulk-copy unit (a 256-byte reduction per half row)
+        float* rrow = reinterpret_cast<float*>(base + kQryR) + i * kRowP;
+        bulk_wait_read0();  // the previous level's reduction has read this row
+#pragma unroll 1
+        for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
+          float x[32];
+          tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 32; u += 4)
+            *reinterpret_cast<float4*>(rrow + 32 * cb + u) = make_float4(x[u], x[u + 1], x[u + 2], x[u + 3]);
+        }
+        if (ok) {
+          fence_proxy_async_shared();
+          bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD + 64 * hf, rrow + 64 * hf, 64 * 4);
+          bulk_commit();
+        }
       }
     }
     D += G[bh * N + e];
     tc_fence_before();
     __syncthreads();  // the next level rewrites the staged tiles and the TMEM columns
+    if (use_rmap && tid == 0 && ok) {
+      const int y = (int)((bh * N + e) * kD);
+#pragma unroll
+      for (int cb = 0; cb < 4; ++cb) tma_reduce_add_box(&tr, base + kQryR + cb * kRBox, 32 * cb, y);
+      bulk_commit();
+      bulk_wait_read0();  // the boxes are read before the next level's products (and staging)
+    }
     if (hf == 0 && i < nv) dlam[(row0 + i) * L + lv] = w * (part + qpart[i]);
   }
   // the levels above 7 that hold no key of this tile's queries
@@ -825,6 +916,19 @@ bool tile_map(CUtensorMap* m, const void* base, uint64_t rows) {
             CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
 }
 
+// [rows, 128] float32 with [128 x 32] boxes and the 128-byte swizzle (the key-side nodes)
+bool f32_box_map(CUtensorMap* m, const void* base, uint64_t rows) {
+  auto fn = map_encoder();
+  if (!fn) return false;
+  cuuint64_t dims[2] = {(cuuint64_t)kD, (cuuint64_t)rows};
+  cuuint64_t strides[1] = {(cuuint64_t)kD * 4};
+  cuuint32_t box[2] = {32, (cuuint32_t)kT};
+  cuuint32_t estr[2] = {1, 1};
+  return fn(m, CU_TENSOR_MAP_DATA_TYPE_FLOAT32, 2, const_cast<void*>(base), dims, strides, box, estr,
+            CU_TENSOR_MAP_INTERLEAVE_NONE, CU_TENSOR_MAP_SWIZZLE_128B, CU_TENSOR_MAP_L2_PROMOTION_L2_256B,
+            CU_TENSOR_MAP_FLOAT_OOB_FILL_NONE) == CUDA_SUCCESS;
+}
+
 bool bwd_tc_supported(const ll_shape& s) { return s.io == LL_BF16 && s.dk == 128 && s.dv == 128; }
 
 ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
@@ -850,15 +954,24 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   LL_CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int items = N * BH;
   const int intra_grid = std::max(1, std::min(items, sms));  // persistent, one CTA per SM
+  // the intra kernel's outputs by tensor stores where the maps can be made
+  CUtensorMap tdq, tdk, tdv, tS;
+  const uint64_t srows = (uint64_t)BH * N * kD;
+  const int use_omap = use_tma && srows <= 0x7fffffffull && tile_map(&tdq, b.dqp, rows) &&
+                       tile_map(&tdk, b.dkp, rows) && tile_map(&tdv, b.dvp, rows) && f32_box_map(&tS, b.S, srows);
   bwd_tc_intra_kernel<<<intra_grid, kIntraThreads, intra_smem(), a.stream>>>(
-      tq, tk, tv, tg, use_tma, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp, b.dvp, a.dlam, b.S, b.tot, b.dc, s.T,
+      tq, tk, tv, tg, use_tma, tdq, tdk, tdv, tS, use_omap, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp, b.dvp, a.dlam, b.S, b.tot, b.dc, s.T,
       s.L, N, BH, b.err);
   LL_CUDA_OK(cudaGetLastError());
   // the query kernel reads the nodes' bf16 tiles only: no float32 copy where the Fenwick kernel can skip it
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum, false);
   if (fs != LL_OK) return fs;
+  // the key-side nodes' rows by tensor reductions where their row coordinate fits
+  const uint64_t rrows = (uint64_t)BH * N * kD;
+  CUtensorMap tr;
+  const int use_rmap = rrows <= 0x7fffffffull && f32_box_map(&tr, b.R, rrows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kQryThreads, query_smem(), a.stream>>>(tq, tg, use_tma, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
+  bwd_tc_query_kernel<<<grid, kQryThreads, query_smem(), a.stream>>>(tq, tg, use_tma, tr, use_rmap, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
                                                                   static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
                                                                   s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
