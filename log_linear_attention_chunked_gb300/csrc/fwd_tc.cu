@@ -578,6 +578,152 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   __half* kfh = reinterpret_cast<__half*>(s + kOffLam);  // per-level mode: exp(K(s, l)), l = 1..6
   float* qtl = reinterpret_cast<float*>(s + kOffCs);     // per-level mode: quadrant totals [4][16]
 
+  // The front half's prologue of the CTA's k-th tile: the values of a row
+  // that depend on the tile's inputs alone (its cumsum or, per level, the key
+  // and query parts of its decays, and the level weights) and the per-tile
+  // tables in shared memory.  It runs one tile ahead -- in the previous back
+  // half, before that half waits for its output -- so that a front half
+  // starts at its scores; the tables are free by then (the front half before
+  // has read them before its last barrier).  The per-level mode runs it at
+  // the start of the front half instead: held across a back half, its
+  // per-row state would not fit the epilogue's registers.
+  float n_cs_t = 0.f, n_cs2_t = 0.f, n_cs2_diag = 0.f, n_cs2_end = 0.f, n_lam6 = 0.f, n_lam7 = 0.f;
+  float n_kdec2 = 0.f, n_rf6 = 0.f, n_rf7 = 0.f, n_gf0 = 0.f, n_rowq[kLD ? 6 : 1], n_csI[kLD ? 8 : 1];
+  auto prologue = [&](int k) {
+    const float la = la_n;
+    float lam[8], lal[kLD ? kLdLv : 1];
+#pragma unroll
+    for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
+    if constexpr (kLD) {
+#pragma unroll
+      for (int m = 0; m < kLdLv; ++m) lal[m] = lal_n[m];
+    }
+    if (k + 1 < n) fetch(blockIdx.x + (k + 1) * gridDim.x);
+
+    // per-level mode: the key and query parts of the log decays of this row
+    float kdec2 = 0.f, rf6 = 0.f, rf7 = 0.f, gf0 = 0.f, rowq[kLD ? 6 : 1];
+    float cs_t = 0.f, cs2_t = 0.f, cs2_diag = 0.f, cs2_end = 0.f;
+    float csI[kLD ? 8 : 1];
+#pragma unroll
+    for (int h = 0; h < (kLD ? 8 : 1); ++h) csI[h] = 0.f;
+    if constexpr (kLD) {
+      // quadrant-local running sums of levels 1..kLdLv (levels l = m + 1)
+      float cp[kLdLv];
+#pragma unroll
+      for (int m = 0; m < kLdLv; ++m) {
+        float x = lal[m];
+#pragma unroll
+        for (int o = 1; o < 32; o <<= 1) {
+          const float y = __shfl_up_sync(0xffffffffu, x, o);
+          if (lane >= o) x += y;
+        }
+        cp[m] = x;
+      }
+      if (hf == 0 && lane == 31) {
+#pragma unroll
+        for (int m = 0; m < kLdLv; ++m) qtl[q * 16 + m] = cp[m];
+      }
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      // Q(t, l): level l's decays from the start of t's block of 2^(l-1)
+      // rows through t; inside the quadrant for l <= 6, the quadrant pair for l = 7
+      float qf[6];
+      qf[0] = 0.f;
+#pragma unroll
+      for (int l = 1; l <= 5; ++l) {
+        const int src = ((lane >> (l - 1)) << (l - 1)) - 1;
+        const float pv = __shfl_sync(0xffffffffu, cp[l - 1], src < 0 ? 0 : src);
+        qf[l] = cp[l - 1] - (src < 0 ? 0.f : pv);
+      }
+      const float qf6 = cp[5];
+      const float qf7 = cp[6] + ((q & 1) ? qtl[(q - 1) * 16 + 6] : 0.f);
+      // K(t, l): the decays of the sibling blocks above t at the levels
+      // below l (bit m-1 of t clear: the next 2^(m-1) rows, at level m)
+      float kf[9], K = 0.f;
+      kf[1] = 0.f;
+#pragma unroll
+      for (int m = 1; m <= 5; ++m) {
+        const int ss = ((lane >> m) << m) + (1 << (m - 1)), se = ss + (1 << (m - 1)) - 1;
+        const float a1 = __shfl_sync(0xffffffffu, cp[m - 1], se & 31);
+        const float a0 = __shfl_sync(0xffffffffu, cp[m - 1], (ss - 1) & 31);
+        if (!((lane >> (m - 1)) & 1)) K += a1 - a0;
+        kf[m + 1] = K;
+      }
+      if (!(q & 1)) K += qtl[(q + 1) * 16 + 5];
+      kf[7] = K;
+      if (q < 2) K += qtl[2 * 16 + 6] + qtl[3 * 16 + 6];
+      kf[8] = K;
+      kdec2 = kf[8] * kLog2e;
+      rowq[0] = lam[0];
+#pragma unroll
+      for (int l = 1; l <= 5; ++l) rowq[l] = lam[l] * ex2(qf[l] * kLog2e);
+      rf6 = lam[6] * ex2(qf6 * kLog2e);
+      rf7 = lam[7] * ex2(qf7 * kLog2e);
+      gf0 = ex2(qtl[16 + 5] * kLog2e);  // keys of group 0 pass group 1 at level 6 on their way to level 7
+#pragma unroll
+      for (int h = 0; h < 8; ++h) {
+        float off = 0.f;
+        for (int qq = 0; qq < q; ++qq) off += qtl[qq * 16 + 7 + h];
+        csI[h] = cp[7 + h] + off;
+      }
+      if (hf == 0) {
+#pragma unroll
+        for (int l = 1; l <= 6; ++l) kfh[(l - 1) * kTile + row] = __float2half_rn(ex2(kf[l] * kLog2e));
+      }
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+    } else {
+      // inclusive cumsum of log_alpha over the tile
+      float x = la;
+#pragma unroll
+      for (int o = 1; o < 32; o <<= 1) {
+        const float y = __shfl_up_sync(0xffffffffu, x, o);
+        if (lane >= o) x += y;
+      }
+      if (hf == 0 && lane == 31) qtot[q] = x;
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      float off = 0.f;
+      for (int qq = 0; qq < q; ++qq) off += qtot[qq];
+      cs_t = x + off;
+      cs2_t = cs_t * kLog2e;                               // base-2 log decay
+      const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);  // end of this 32-group
+      if (hf == 0) {
+        cs_s[row] = cs2_t;
+        col_s[row] = ex2(cs2_grp_end - cs2_t);
+      }
+      // lambda of levels 0..5 (the diagonal group), relative to the row's
+      // largest, as half; the largest rides in the exponent
+      float lmax = 0.f;
+#pragma unroll
+      for (int l = 0; l < 6; ++l) lmax = fmaxf(lmax, lam[l]);
+      cs2_diag = cs2_t + (lmax > 0.f ? __log2f(lmax) : -INFINITY);
+      if (hf == 0) {
+        const float inv = lmax > 0.f ? 1.f / lmax : 0.f;
+#pragma unroll
+        for (int l = 0; l < 6; ++l) lamh[l * kTile + row] = __float2half_rn(lam[l] * inv);
+      }
+      __syncwarp();
+      named_bar_sync(1, kEpi);
+      cs2_end = cs_s[kTile - 1];
+    }
+    n_cs_t = cs_t;
+    n_cs2_t = cs2_t;
+    n_cs2_diag = cs2_diag;
+    n_cs2_end = cs2_end;
+    n_lam6 = lam[6];
+    n_lam7 = lam[7];
+    n_kdec2 = kdec2;
+    n_rf6 = rf6;
+    n_rf7 = rf7;
+    n_gf0 = gf0;
+#pragma unroll
+    for (int l = 0; l < (kLD ? 6 : 1); ++l) n_rowq[l] = kLD ? rowq[l] : 0.f;
+#pragma unroll
+    for (int h = 0; h < (kLD ? 8 : 1); ++h) n_csI[h] = csI[h];
+  };
+  if (!kLD) prologue(0);
+
   float cs_prev = 0.f, lam_c = 0.f;
   float csI_prev[kLD ? 8 : 1];  // per-level mode: in-tile running sums of levels 8..15 (previous tile)
 #pragma unroll
@@ -594,123 +740,20 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       // ================= front half of tile it
       bh = u % p.BH;
       j = u / p.BH;
-      const float la = la_n;
-      float lam[8], lal[kLD ? kLdLv : 1];
-#pragma unroll
-      for (int l = 0; l < 8; ++l) lam[l] = lam_n[l];
-      if constexpr (kLD) {
-#pragma unroll
-        for (int m = 0; m < kLdLv; ++m) lal[m] = lal_n[m];
-      }
-      if (it + 1 < n) fetch(u + gridDim.x);
       const int jap = jp | start_tile<kCont>(p);  // the previous tile's absolute index bits
       if (it >= 1 && jap != 0)  // the previous tile's first level lambda, ahead of its back half
         lam_c = __ldg(p.lam + ((size_t)bhp * p.T + (size_t)jp * kTile + row) * p.L + 8 + (__ffs(jap) - 1));
-
-      // per-level mode: the key and query parts of the log decays of this row
-      float kdec2 = 0.f, rf6 = 0.f, rf7 = 0.f, gf0 = 0.f, rowq[kLD ? 6 : 1];
-      float cs2_t = 0.f, cs2_diag = 0.f, cs2_end = 0.f;
-      if constexpr (kLD) {
-        // quadrant-local running sums of levels 1..kLdLv (levels l = m + 1)
-        float cp[kLdLv];
+      // this tile's values from its prologue (run one tile ahead; in the
+      // per-level mode, whose prologue holds more per-row state, here)
+      if (kLD) prologue(it);
+      cs_t = n_cs_t;
+      const float cs2_t = n_cs2_t, cs2_diag = n_cs2_diag, cs2_end = n_cs2_end, lam6 = n_lam6, lam7 = n_lam7;
+      const float kdec2 = n_kdec2, rf6 = n_rf6, rf7 = n_rf7, gf0 = n_gf0;
+      float rowq[kLD ? 6 : 1];
 #pragma unroll
-        for (int m = 0; m < kLdLv; ++m) {
-          float x = lal[m];
+      for (int l = 0; l < (kLD ? 6 : 1); ++l) rowq[l] = n_rowq[l];
 #pragma unroll
-          for (int o = 1; o < 32; o <<= 1) {
-            const float y = __shfl_up_sync(0xffffffffu, x, o);
-            if (lane >= o) x += y;
-          }
-          cp[m] = x;
-        }
-        if (hf == 0 && lane == 31) {
-#pragma unroll
-          for (int m = 0; m < kLdLv; ++m) qtl[q * 16 + m] = cp[m];
-        }
-        __syncwarp();
-        named_bar_sync(1, kEpi);
-        // Q(t, l): level l's decays from the start of t's block of 2^(l-1)
-        // rows through t; inside the quadrant for l <= 6, the quadrant pair for l = 7
-        float qf[6];
-        qf[0] = 0.f;
-#pragma unroll
-        for (int l = 1; l <= 5; ++l) {
-          const int src = ((lane >> (l - 1)) << (l - 1)) - 1;
-          const float pv = __shfl_sync(0xffffffffu, cp[l - 1], src < 0 ? 0 : src);
-          qf[l] = cp[l - 1] - (src < 0 ? 0.f : pv);
-        }
-        const float qf6 = cp[5];
-        const float qf7 = cp[6] + ((q & 1) ? qtl[(q - 1) * 16 + 6] : 0.f);
-        // K(t, l): the decays of the sibling blocks above t at the levels
-        // below l (bit m-1 of t clear: the next 2^(m-1) rows, at level m)
-        float kf[9], K = 0.f;
-        kf[1] = 0.f;
-#pragma unroll
-        for (int m = 1; m <= 5; ++m) {
-          const int ss = ((lane >> m) << m) + (1 << (m - 1)), se = ss + (1 << (m - 1)) - 1;
-          const float a1 = __shfl_sync(0xffffffffu, cp[m - 1], se & 31);
-          const float a0 = __shfl_sync(0xffffffffu, cp[m - 1], (ss - 1) & 31);
-          if (!((lane >> (m - 1)) & 1)) K += a1 - a0;
-          kf[m + 1] = K;
-        }
-        if (!(q & 1)) K += qtl[(q + 1) * 16 + 5];
-        kf[7] = K;
-        if (q < 2) K += qtl[2 * 16 + 6] + qtl[3 * 16 + 6];
-        kf[8] = K;
-        kdec2 = kf[8] * kLog2e;
-        rowq[0] = lam[0];
-#pragma unroll
-        for (int l = 1; l <= 5; ++l) rowq[l] = lam[l] * ex2(qf[l] * kLog2e);
-        rf6 = lam[6] * ex2(qf6 * kLog2e);
-        rf7 = lam[7] * ex2(qf7 * kLog2e);
-        gf0 = ex2(qtl[16 + 5] * kLog2e);  // keys of group 0 pass group 1 at level 6 on their way to level 7
-#pragma unroll
-        for (int h = 0; h < 8; ++h) {
-          float off = 0.f;
-          for (int qq = 0; qq < q; ++qq) off += qtl[qq * 16 + 7 + h];
-          csI[h] = cp[7 + h] + off;
-        }
-        if (hf == 0) {
-#pragma unroll
-          for (int l = 1; l <= 6; ++l) kfh[(l - 1) * kTile + row] = __float2half_rn(ex2(kf[l] * kLog2e));
-        }
-        __syncwarp();
-        named_bar_sync(1, kEpi);
-      } else {
-        // inclusive cumsum of log_alpha over the tile
-        float x = la;
-#pragma unroll
-        for (int o = 1; o < 32; o <<= 1) {
-          const float y = __shfl_up_sync(0xffffffffu, x, o);
-          if (lane >= o) x += y;
-        }
-        if (hf == 0 && lane == 31) qtot[q] = x;
-        __syncwarp();
-        named_bar_sync(1, kEpi);
-        float off = 0.f;
-        for (int qq = 0; qq < q; ++qq) off += qtot[qq];
-        cs_t = x + off;
-        cs2_t = cs_t * kLog2e;                               // base-2 log decay
-        const float cs2_grp_end = __shfl_sync(0xffffffffu, cs2_t, 31);  // end of this 32-group
-        if (hf == 0) {
-          cs_s[row] = cs2_t;
-          col_s[row] = ex2(cs2_grp_end - cs2_t);
-        }
-        // lambda of levels 0..5 (the diagonal group), relative to the row's
-        // largest, as half; the largest rides in the exponent
-        float lmax = 0.f;
-#pragma unroll
-        for (int l = 0; l < 6; ++l) lmax = fmaxf(lmax, lam[l]);
-        cs2_diag = cs2_t + (lmax > 0.f ? __log2f(lmax) : -INFINITY);
-        if (hf == 0) {
-          const float inv = lmax > 0.f ? 1.f / lmax : 0.f;
-#pragma unroll
-          for (int l = 0; l < 6; ++l) lamh[l * kTile + row] = __float2half_rn(lam[l] * inv);
-        }
-        __syncwarp();
-        named_bar_sync(1, kEpi);
-        cs2_end = cs_s[kTile - 1];
-      }
+      for (int h = 0; h < (kLD ? 8 : 1); ++h) csI[h] = n_csI[h];
 
       // scores ready: K has been read by them, so it is decayed in place for
       // the chunk state, K[s] <- exp(cs_end - cs_s) K[s]
@@ -770,7 +813,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
               }
             }
           } else {
-            const float lg = (q ^ g) == 1 ? lam[6] : lam[7];  // level 5 + bitlen(q ^ g)
+            const float lg = (q ^ g) == 1 ? lam6 : lam7;  // level 5 + bitlen(q ^ g)
             rf = lg * ex2(cs2_t - cs_s[32 * g + 31]);
             const float4* cp = reinterpret_cast<const float4*>(col_s + s0);
 #pragma unroll
@@ -829,6 +872,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
       __syncwarp();
       named_bar_sync(1, kEpi);
       if (leader) mbar_arrive(c.bars + B_P_READY);
+      if (!kLD && it == 0 && n > 1) prologue(1);  // (no back half in this step)
     }
 
     if (it >= 1) {
@@ -905,6 +949,9 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         if (leader) mbar_arrive(c.bars + B_QP_FULL0 + b);
         ++qpc;
       }
+
+      // the next tile's prologue while the last level products run
+      if (!kLD && it + 1 < n) prologue(it + 1);
 
       // output = PV + levels, accumulated in TMEM; bf16, staged for the store warp
       if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
