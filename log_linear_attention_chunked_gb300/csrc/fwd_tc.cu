@@ -582,7 +582,7 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
   // that depend on the tile's inputs alone (its cumsum or, per level, the key
   // and query parts of its decays, and the level weights) and the per-tile
   // tables in shared memory.  It runs one tile ahead -- in the previous back
-  // half, before that half waits for its output -- so that a front half
+  // half, once that half has handed its first level over -- so that a front half
   // starts at its scores; the tables are free by then (the front half before
   // has read them before its last barrier).  The per-level mode runs it at
   // the start of the front half instead: held across a back half, its
@@ -948,10 +948,12 @@ __device__ void epilogue(const Ctx& c, uint32_t tmem, int warp, int lane) {
         named_bar_sync(1, kEpi);
         if (leader) mbar_arrive(c.bars + B_QP_FULL0 + b);
         ++qpc;
+        // the next tile's prologue once the first level product can start
+        if (!kLD && l == 0 && it + 1 < n) prologue(it + 1);
       }
 
-      // the next tile's prologue while the last level products run
-      if (!kLD && it + 1 < n) prologue(it + 1);
+      // (the next tile's prologue when this tile has no level to hand over)
+      if (!kLD && it + 1 < n && jap == 0) prologue(it + 1);
 
       // output = PV + levels, accumulated in TMEM; bf16, staged for the store warp
       if (xs > 0) wait_bar_w(c, B_X_FREE, (xs - 1) & 1);
