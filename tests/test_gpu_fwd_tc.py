@@ -250,3 +250,12 @@ def test_repeated_calls_two_tiles_per_cta(B, lvl):
     for _ in range(4):
         out = _run(B, inp)
         assert _check_sampled(out, inp, rows) <= TOL_BF16, lvl
+
+
+def test_more_heads_than_ctas(B):
+    """B=2, H=96 (192 heads) x 2 tiles: tiles are dealt as u = j * (B*H) + bh,
+    so the first tiles of heads 152..191 (no inter-tile level) run as the
+    second step of a CTA, after a tile with levels; slow decay keeps the
+    second tiles' level-8 bucket visible."""
+    inp = synth.make_inputs(_cfg(256, Bn=2, H=96), la_mode="slow", tag="tcheads")
+    assert rel_err(_run(B, inp), _oracle(inp)) <= TOL_BF16

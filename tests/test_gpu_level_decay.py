@@ -247,3 +247,17 @@ def test_rejects_bad_arguments(B):
     assert B.ll_attn_fwd_level_decay_workspace_size(bad) == 0
     big = B.make_shape(1, 1, 4097 * 64, 16, 16, 20, 64, 0, B.LL_F32)  # more than 4096 chunks
     assert B.ll_attn_fwd_level_decay_workspace_size(big) == 0
+
+
+def test_tc_more_heads_than_ctas(B):
+    """The tensor-core mode with B=2, H=96 (192 heads) x 2 tiles: the first
+    tiles of heads 152..191 run as a CTA's second step, and the per-level
+    decay table is indexed by head beyond the grid."""
+    cfg = _cfg(io="bf16", T=256, dk=128, dv=128, chunk=64, L=levels_needed(256))
+    inp = synth.make_inputs(cfg, B=2, H=96, la_mode="slow", tag="ldheads")
+    shape = B.make_shape(2, 96, 256, 128, 128, cfg["L"], 64, 0, B.LL_BF16)
+    assert B.ll_attn_fwd_level_decay_launches(shape) == 3, "tensor-core path not selected"
+    out = _run(B, inp, 64)
+    f = _f64(inp)
+    ref = ld.forward_dense_bh(f["q"], f["k"], f["v"], f["log_alpha"], f["lam"])
+    assert rel_err(out, ref) <= TOL_BF16
