@@ -211,6 +211,15 @@ __device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, 
   }
 }
 
+// L2 prefetch of the 16-byte-aligned interior of [ptr, ptr + bytes) (a bulk
+// prefetch needs a 16-byte-aligned start and size, which rows of log_alpha and
+// lam do not have when T is not a multiple of 4)
+__device__ __forceinline__ void prefetch_l2_inside(const void* ptr, uint32_t bytes) {
+  const uintptr_t a = reinterpret_cast<uintptr_t>(ptr);
+  const uintptr_t lo = (a + 15) & ~(uintptr_t)15, hi = (a + bytes) & ~(uintptr_t)15;
+  if (hi > lo) bulk_prefetch_l2(reinterpret_cast<const void*>(lo), (uint32_t)(hi - lo));
+}
+
 // The full tile of rows row0 .. row0+127 of a [rows, 128] bf16 tensor by two
 // TMA boxes of [128 x 64] (128-byte swizzle: the layout of swz), completion
 // counted on `bar`.
@@ -319,28 +328,33 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
   const bool tma = use_tma && nv == kT;  // a partial tile: its missing rows are zeros, staged by the threads
-  tile_cumsum(cs, log_alpha, row0, nv);
-  if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
   bool ok = true;
   if (tid == 0) {
-    const int wn = w + (int)gridDim.x;
-    if (wn < N * BH) {
-      const size_t rn = (size_t)(wn / N) * T + (size_t)(wn % N) * kT;
-      const uint32_t bytes = (uint32_t)(min(kT, T - (wn % N) * kT) * kD * 2);
-      bulk_prefetch_l2(q + rn * kD, bytes);
-      bulk_prefetch_l2(k + rn * kD, bytes);
-      bulk_prefetch_l2(v + rn * kD, bytes);
-      bulk_prefetch_l2(dout + rn * kD, bytes);
-    }
-  }
-  if (tma) {
-    if (tid == 0) {
+    // this item's input tiles (the previous item's outputs have been read
+    // out of these buffers), then the next item's rows staged in L2
+    if (tma) {
       mbar_arrive_expect_tx(inbar, 4 * kTileB);
       tma_tile(base + kIntraQ, &tq, inbar, row0);
       tma_tile(base + kIntraK, &tk, inbar, row0);
       tma_tile(base + kIntraV, &tv, inbar, row0);
       tma_tile(base + kIntraG, &tg, inbar, row0);
     }
+    const int wn = w + (int)gridDim.x;
+    if (wn < N * BH) {
+      const size_t rn = (size_t)(wn / N) * T + (size_t)(wn % N) * kT;
+      const int nn = min(kT, T - (wn % N) * kT);
+      const uint32_t bytes = (uint32_t)(nn * kD * 2);
+      bulk_prefetch_l2(q + rn * kD, bytes);
+      bulk_prefetch_l2(k + rn * kD, bytes);
+      bulk_prefetch_l2(v + rn * kD, bytes);
+      bulk_prefetch_l2(dout + rn * kD, bytes);
+      prefetch_l2_inside(log_alpha + rn, (uint32_t)(nn * 4));
+      prefetch_l2_inside(lam + rn * L, (uint32_t)(nn * L * 4));
+    }
+  }
+  tile_cumsum(cs, log_alpha, row0, nv);  // while the tiles land
+  if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
+  if (tma) {
     ok = wait_phase(inbar, k_it & 1, err, abort_s);
   } else if (tid < kT) {
     stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
