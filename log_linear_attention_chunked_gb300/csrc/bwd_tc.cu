@@ -615,13 +615,6 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
   const bool tma = use_tma && nv == kT;
-  if (tid == 0) {
-    *abort_s = 0;
-    mbar_init(ldbar, 1);  // made visible by the fence in setup_tmem
-    mbar_init(inbar, 1);
-  }
-  tile_cumsum(cs, log_alpha, row0, nv);
-  const uint32_t tmem = setup_tmem<512>(bar, slot);
   const size_t mat = (size_t)kD * kD;
   // the node tile of the lowest set bit of c streams in while Q and dO are staged;
   // each later one as soon as the products of the level before have read the tile
@@ -635,14 +628,24 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       if ((c >> h) & 1) return h;
     return -1;
   };
-  if (tid == 0 && c > 0) load_node(next_bit(-1));
-  bool ok = true;
-  if (tma) {
-    if (tid == 0) {
+  if (tid == 0) {
+    *abort_s = 0;
+    mbar_init(ldbar, 1);
+    mbar_init(inbar, 1);
+    fence_mbar_init();  // the copies below arrive on them
+    // the first node tile and the input tiles go out before the cumsum and
+    // the TMEM allocation, which run while they land
+    if (c > 0) load_node(next_bit(-1));
+    if (tma) {
       mbar_arrive_expect_tx(inbar, 2 * kTileB);
       tma_tile(base + kQryQ, &tq, inbar, row0);
       tma_tile(base + kQryG, &tg, inbar, row0);
     }
+  }
+  tile_cumsum(cs, log_alpha, row0, nv);
+  const uint32_t tmem = setup_tmem<512>(bar, slot);
+  bool ok = true;
+  if (tma) {
     ok = wait_phase(inbar, 0, err, abort_s);
   } else if (tid < kT) {
     stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
@@ -814,7 +817,13 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const bool tma = use_tma && nv == kT;
   if (tid == 0) {
     *abort_s = 0;
-    mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
+    mbar_init(inbar, 1);
+    fence_mbar_init();  // the copies below arrive on it
+    if (tma) {  // the input tiles go out first; the node list, cumsum and TMEM allocation run while they land
+      mbar_arrive_expect_tx(inbar, 2 * kTileB);
+      tma_tile(base + kKeyK, &tk, inbar, row0);
+      tma_tile(base + kKeyV, &tv, inbar, row0);
+    }
   }
   if (tid < 32) {  // lane h: the node of level h whose block holds the keys of c, if it has queries after it
     const int h = tid;
@@ -837,13 +846,7 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   if (tid < nv)
     for (int l = 0; l < L; ++l) lamdot = fmaf(lam[(row0 + tid) * L + l], dlam[(row0 + tid) * L + l], lamdot);
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
-  if (tma) {
-    if (tid == 0) {
-      mbar_arrive_expect_tx(inbar, 2 * kTileB);
-      tma_tile(base + kKeyK, &tk, inbar, row0);
-      tma_tile(base + kKeyV, &tv, inbar, row0);
-    }
-  } else {
+  if (!tma) {
     stage_bf16(base + kKeyK, k + row0 * kD, nv, tid);
     stage_bf16(base + kKeyV, v + row0 * kD, nv, tid);
   }
