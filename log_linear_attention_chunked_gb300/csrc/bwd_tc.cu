@@ -497,14 +497,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     // [128 x 32] boxes).  Before each barrier thread 0 waits until its earlier
     // stores have read their buffer, which the staging after the barrier reuses.
     const int r = i;  // this thread's half row: columns 64 hf .. 64 hf + 63
+    // the two column blocks of an output are loaded from TMEM together, and
+    // the next output's first block is in flight across the barrier
+    float xs[2][32];
+    tmem_ld32(lane_addr(tmem, 32 * (2 * hf)), xs[0]);  // warp-collective: every lane loads
 #pragma unroll 1
     for (int o = 0; o < 4; ++o) {
       unsigned char* buf = base + (o & 1) * (kT * kRowP * 4);
-#pragma unroll 1
-      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-        float x[32];
-        tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);  // warp-collective: every lane loads
-        tmem_ld_wait();
+      tmem_ld32(lane_addr(tmem, 128 * o + 32 * (2 * hf + 1)), xs[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int cb = 2 * hf + hb;
+        const float* x = xs[hb];
         if (o == 3) {
           unsigned char* box = buf + cb * kRBox + r * 128;
 #pragma unroll
@@ -519,6 +524,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
                            pack_bf16x2(x[8 * w + 4], x[8 * w + 5]), pack_bf16x2(x[8 * w + 6], x[8 * w + 7]));
         }
       }
+      if (o < 3) tmem_ld32(lane_addr(tmem, 128 * (o + 1) + 32 * (2 * hf)), xs[0]);
       fence_proxy_async_shared();
       if (tid == 0) bulk_wait_read0();
       __syncthreads();
