@@ -694,17 +694,20 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     if (tid == 0 && ok && next_bit(h) >= 0) load_node(next_bit(h));  // the products have read the tile
     float part = 0.f;
     {
-#pragma unroll 1
-      for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-        float g[32];
-        tmem_ld32(lane_addr(tmem, 32 * cb), g);
-        tmem_ld_wait();
+      // both column blocks of g from TMEM together
+      float gs[2][32];
+      tmem_ld32(lane_addr(tmem, 32 * (2 * hf)), gs[0]);
+      tmem_ld32(lane_addr(tmem, 32 * (2 * hf + 1)), gs[1]);
+      tmem_ld_wait();
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const int cb = 2 * hf + hb;
 #pragma unroll
         for (int w4 = 0; w4 < 4; ++w4) {
           float x[8];
           row_chunk(base + kQryQ, i, 4 * cb + w4, x);
 #pragma unroll
-          for (int u = 0; u < 8; ++u) part = fmaf(g[8 * w4 + u], x[u], part);
+          for (int u = 0; u < 8; ++u) part = fmaf(gs[hb][8 * w4 + u], x[u], part);
         }
       }
       if (hf == 1) qpart[i] = part;
@@ -713,11 +716,14 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
         // (128-byte swizzle), row e' = i; thread 0 adds them into R_e by four
         // tensor reductions after the level's barrier (it has waited for the
         // previous level's to read the boxes before issuing this level's products)
-#pragma unroll 1
-        for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-          float x[32];
-          tmem_ld32(lane_addr(tmem, 256 + 32 * cb), x);
-          tmem_ld_wait();
+        float xs[2][32];  // both column blocks of the R part from TMEM together
+        tmem_ld32(lane_addr(tmem, 256 + 32 * (2 * hf)), xs[0]);
+        tmem_ld32(lane_addr(tmem, 256 + 32 * (2 * hf + 1)), xs[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          const int cb = 2 * hf + hb;
+          const float* x = xs[hb];
           unsigned char* box = base + kQryR + cb * kRBox + i * 128;
 #pragma unroll
           for (int ch = 0; ch < 8; ++ch)
@@ -767,16 +773,19 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   {
     const __nv_bfloat16* src = dqp + (row0 + i) * kD;
     __nv_bfloat16* dst = dq + (row0 + i) * kD;
-#pragma unroll 1
-    for (int cb = 2 * hf; cb < 2 * hf + 2; ++cb) {
-      float x[32];
-      if (!first) {  // uniform over the CTA: the warp-collective loads run in every lane
-        tmem_ld32(lane_addr(tmem, 128 + 32 * cb), x);
-        tmem_ld_wait();
-      } else {
+    float xs[2][32];
+    if (!first) {  // uniform over the CTA: the warp-collective loads run in every lane
+      tmem_ld32(lane_addr(tmem, 128 + 32 * (2 * hf)), xs[0]);
+      tmem_ld32(lane_addr(tmem, 128 + 32 * (2 * hf + 1)), xs[1]);
+      tmem_ld_wait();
+    } else {
 #pragma unroll
-        for (int u = 0; u < 32; ++u) x[u] = 0.f;
-      }
+      for (int u = 0; u < 32; ++u) xs[0][u] = xs[1][u] = 0.f;
+    }
+#pragma unroll
+    for (int hb = 0; hb < 2; ++hb) {
+      const int cb = 2 * hf + hb;
+      const float* x = xs[hb];
       if (i < nv)
 #pragma unroll
       for (int u = 0; u < 32; u += 8) {
