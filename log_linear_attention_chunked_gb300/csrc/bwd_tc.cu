@@ -273,7 +273,7 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
 constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
 constexpr int kIntraThreads = 256;  // two threads per row: columns 0..63 and 64..127
-constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + 64; }
+constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 64; }
 
 // Reduce-scatter over a warp: lane l receives the sum over the 32 lanes of v[l].
 __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
@@ -309,7 +309,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   float* colpart = wdec + kT;  // [4 warps][128 columns] of sum_i P_ij G_ij
   float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
   float* dlhalf = c2 + kT;       // [128][8] the in-tile dlam of the columns 64..127
-  uint64_t* bar = reinterpret_cast<uint64_t*>(dlhalf + kT * 8);
+  float* colf = dlhalf + kT * 8;  // exp2(c2_e - c2_j), e = the end of j's 32-column block
+  uint64_t* bar = reinterpret_cast<uint64_t*>(colf + kT);
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
@@ -375,6 +376,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   if (tid < kT) {
     c2[tid] = (float)cs[tid] * 1.4426950408889634f;
     wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
+    colf[tid] = exp2f((float)(cs[(tid | 31)] - cs[tid]) * 1.4426950408889634f);
   }
   float lm[8];  // the row's in-tile lambdas, loaded while the products run
 #pragma unroll
@@ -408,14 +410,21 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           const int lvc = 5 + bitlen((unsigned)(wi ^ cb));
           float lmv = lm[6];
           if (lvc == 7) lmv = lm[7];
+          // all keys of the block lie before the row: exp2(c_i - c_j) = exp2(c_i -
+          // c_e) exp2(c_e - c_j), e = the block's end, both factors <= 1, the
+          // second from the per-tile column table
+          const float rf = row_ok ? exp2f(ci - c2[32 * cb + 31]) : 0.f;
+          const float rl = rf * lmv;
           float acc = 0.f;
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float ex = row_ok ? exp2f(ci - c2[32 * cb + u]) : 0.f;
-            p[u] = a[u] * ex * lmv;
-            da[u] = g[u] * ex * lmv;
-            acc = fmaf(g[u] * a[u], ex, acc);
+            const float cf = colf[32 * cb + u];
+            const float w = rl * cf;
+            p[u] = a[u] * w;
+            da[u] = g[u] * w;
+            acc = fmaf(g[u] * a[u], cf, acc);
           }
+          acc *= rf;
           if (lvc == 7) dl[7] += acc;
           else dl[6] += acc;
         } else {
