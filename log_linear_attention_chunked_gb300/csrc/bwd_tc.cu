@@ -672,6 +672,7 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   const int i = tid & (kT - 1), hf = tid >> 7;  // row i, columns 64 hf .. 64 hf + 63
   double D = 0.0;
   bool first = true;
+  bool pend = false;  // a level's tensor reductions may still read the staged boxes
   uint32_t phase = 0;
   for (int h = 0; (c >> h) != 0; ++h) {
     if (!((c >> h) & 1)) continue;
@@ -723,12 +724,18 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       if (use_rmap) {
         // this tile's part of R_e staged as four [128 x 32] float32 boxes
         // (128-byte swizzle), row e' = i; thread 0 adds them into R_e by four
-        // tensor reductions after the level's barrier (it has waited for the
-        // previous level's to read the boxes before issuing this level's products)
+        // tensor reductions after the level's barrier and goes on: the
+        // reductions read the boxes while the next level stages its operand
+        // and runs its products, and are waited for only here, before the
+        // boxes are rewritten
         float xs[2][32];  // both column blocks of the R part from TMEM together
         tmem_ld32(lane_addr(tmem, 256 + 32 * (2 * hf)), xs[0]);
         tmem_ld32(lane_addr(tmem, 256 + 32 * (2 * hf + 1)), xs[1]);
         tmem_ld_wait();
+        if (pend) {
+          if (tid == 0) bulk_wait_read0();
+          __syncthreads();
+        }
 #pragma unroll
         for (int hb = 0; hb < 2; ++hb) {
           const int cb = 2 * hf + hb;
@@ -769,8 +776,8 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
 #pragma unroll
       for (int cb = 0; cb < 4; ++cb) tma_reduce_add_box(&tr, base + kQryR + cb * kRBox, 32 * cb, y);
       bulk_commit();
-      bulk_wait_read0();  // the boxes are read before the next level's products (and staging)
     }
+    pend = use_rmap;
     if (hf == 0 && i < nv) dlam[(row0 + i) * L + lv] = w * (part + qpart[i]);
   }
   // the levels above 7 that hold no key of this tile's queries
@@ -806,7 +813,7 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       }
     }
   }
-  bulk_wait_read0();  // this thread's reductions into R have read their rows
+  bulk_wait_read0();  // this thread's reductions into R (its rows, or thread 0's boxes) have read their sources
   release_tmem<512>(tmem);
 }
 
