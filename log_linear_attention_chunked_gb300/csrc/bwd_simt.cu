@@ -90,7 +90,8 @@ BwdPlan plan_of(const ll_shape& s) {
   // Fenwick kernel writes F there only when its chain cannot stay on chip
   const bool need_f32_nodes = !bwd_tc_supported(s) || p.N > kFenwickOnChipChunks;
   p.off_F = off;   off = align_up(off + (need_f32_nodes ? BH * p.N * mat * sizeof(float) : 0), 256);
-  p.off_R = off;   off = align_up(off + BH * p.N * mat * sizeof(float), 256);
+  // (the tensor-core path keeps its query kernel's item counter in the word after R)
+  p.off_R = off;   off = align_up(off + BH * p.N * mat * sizeof(float) + (bwd_tc_supported(s) ? sizeof(unsigned) : 0), 256);
   p.off_tot = off; off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_G = off;   off = align_up(off + BH * p.N * sizeof(double), 256);
   p.off_dc = off;  off = align_up(off + BH * (size_t)s.T * sizeof(float), 256);

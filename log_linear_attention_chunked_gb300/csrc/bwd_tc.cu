@@ -604,17 +604,26 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
 constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
 constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
 constexpr int kQryThreads = 256;  // two threads per row: columns 0..63 and 64..127
-// + cs, the second halves' dlam dots, three mbarriers, TMEM slot, flag
+// + cs, the second halves' dlam dots, three mbarriers, TMEM slot, flag, next item
 constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + kT * 4 + 64; }
+
+// Persistent over the (tile, head) items, one CTA per SM.  Item j is tile
+// c = N - 1 - j / BH of head j mod BH: the items of all heads' last tiles
+// first, the light ones of the first tiles (few set bits of c) at the end.
+// CTA b starts with item b and claims each later item from the counter *qctr
+// (zero at the launch) when it starts the item before, so that the later
+// item's first node tile and its input tiles stream in while the earlier one
+// finishes.
 
 __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
     const __grid_constant__ CUtensorMap tr, int use_rmap,
+    const __grid_constant__ CUtensorMap tdi, const __grid_constant__ CUtensorMap tdo, int use_dmap,
     const __nv_bfloat16* __restrict__ q, const __nv_bfloat16* __restrict__ dout, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const __nv_bfloat16* __restrict__ Ft, const double* __restrict__ G,
     const __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dq, float* __restrict__ dlam,
     float* __restrict__ R,
-    int T, int L, unsigned* err) {
+    int T, int L, int N, int BH, unsigned* __restrict__ qctr, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kQryEnd);
@@ -622,58 +631,92 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   uint64_t* bar = reinterpret_cast<uint64_t*>(qpart + kT);
   uint64_t* ldbar = bar + 1;  // the bulk load of a node tile
   uint64_t* inbar = bar + 2;  // the TMA loads of the input tiles
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
+  uint64_t* obar = bar + 3;   // the TMA load of the in-tile dq tile
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 4);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
-  const int c = blockIdx.x, N = gridDim.x;
-  const size_t bh = blockIdx.y;
+  int* next_s = abort_s + 1;  // the item after the current one (or items: none)
   const int tid = threadIdx.x;
-  const size_t row0 = bh * T + (size_t)c * kT;
-  const int nv = min(kT, T - c * kT);
-  const bool tma = use_tma && nv == kT;
+  const int items = N * BH;
   const size_t mat = (size_t)kD * kD;
-  // the node tile of the lowest set bit of c streams in while Q and dO are staged;
-  // each later one as soon as the products of the level before have read the tile
-  auto load_node = [&](int h) {
-    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
-    mbar_arrive_expect_tx(ldbar, kTileB);
-    bulk_load(base + kQryF, Ft + (bh * N + e) * mat, kTileB, ldbar);
-  };
-  auto next_bit = [&](int h) {  // the set bit of c above h, or -1
+  auto tile_of = [&](int j) { return N - 1 - j / BH; };
+  auto head_of = [&](int j) { return (size_t)(j % BH); };
+  auto full_tile = [&](int j) { return use_tma && T - tile_of(j) * kT >= kT; };  // its inputs by TMA
+  auto next_bit = [](int c, int h) {  // the set bit of c above h, or -1
     for (++h; (c >> h) != 0; ++h)
       if ((c >> h) & 1) return h;
     return -1;
   };
+  // thread 0: node tile e(c, h) of head bh into the node buffer; one load per
+  // level, each issued once the products of the level before have read the buffer
+  auto load_node = [&](int c, size_t bh, int h) {
+    const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
+    mbar_arrive_expect_tx(ldbar, kTileB);
+    bulk_load(base + kQryF, Ft + (bh * N + e) * mat, kTileB, ldbar);
+  };
+  // thread 0: item j's Q and dO tiles (full tiles only)
+  auto load_inputs = [&](int j) {
+    const size_t r = head_of(j) * T + (size_t)tile_of(j) * kT;
+    mbar_arrive_expect_tx(inbar, 2 * kTileB);
+    tma_tile(base + kQryQ, &tq, inbar, r);
+    tma_tile(base + kQryG, &tg, inbar, r);
+  };
+  // thread 0: item j's rows of log_alpha and lam into L2 (and the in-tile dq
+  // where the threads read it)
+  auto stage_l2 = [&](int j) {
+    const int cn = tile_of(j);
+    const size_t r = head_of(j) * T + (size_t)cn * kT;
+    const int nn = min(kT, T - cn * kT);
+    prefetch_l2_inside(log_alpha + r, (uint32_t)(nn * 4));
+    prefetch_l2_inside(lam + r * L, (uint32_t)(nn * L * 4));
+    if (!(use_dmap && full_tile(j))) bulk_prefetch_l2(dqp + r * kD, (uint32_t)(nn * kD * 2));
+  };
+  // thread 0: the in-tile dq tile of rows r.. into the operand buffer, free
+  // once the item's last products have read it
+  auto load_dqp = [&](size_t r) {
+    mbar_arrive_expect_tx(obar, kTileB);
+    tma_tile(base + kQryL, &tdi, obar, r);
+  };
+  int j = blockIdx.x;
+  int jn = items;  // thread 0: the item claimed after j
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(ldbar, 1);
     mbar_init(inbar, 1);
+    mbar_init(obar, 1);
     fence_mbar_init();  // the copies below arrive on them
-    // the first node tile and the input tiles go out before the cumsum and
-    // the TMEM allocation, which run while they land
-    if (c > 0) load_node(next_bit(-1));
-    if (tma) {
-      mbar_arrive_expect_tx(inbar, 2 * kTileB);
-      tma_tile(base + kQryQ, &tq, inbar, row0);
-      tma_tile(base + kQryG, &tg, inbar, row0);
-    }
+    // the first item's first node tile and input tiles go out before the
+    // TMEM allocation and the cumsum, which run while they land
+    if (tile_of(j) > 0) load_node(tile_of(j), head_of(j), next_bit(tile_of(j), -1));
+    if (full_tile(j)) load_inputs(j);
   }
-  tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<512>(bar, slot);
-  bool ok = true;
-  if (tma) {
-    ok = wait_phase(inbar, 0, err, abort_s);
-  } else if (tid < kT) {
-    stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
-    stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
-  }
-  __syncthreads();
   const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
                  sF = smem_u32(base + kQryF);
   const int i = tid & (kT - 1), hf = tid >> 7;  // row i, columns 64 hf .. 64 hf + 63
+  uint32_t nlev = 0, nin = 0, nout = 0;  // the levels (node loads, product commits), the TMA input and dq loads so far
+  bool pend = false;  // a level's tensor reductions may still read the staged boxes
+  for (;;) {
+  const int c = tile_of(j);
+  const size_t bh = head_of(j);
+  const size_t row0 = bh * T + (size_t)c * kT;
+  const int nv = min(kT, T - c * kT);
+  const bool tma = full_tile(j);
+  const bool dtma = use_dmap && tma;  // dq in and out by TMA through the operand buffer
+  if (tid == 0) jn = (int)gridDim.x + (int)atomicAdd(qctr, 1u);  // used from the first level's products on
+  tile_cumsum(cs, log_alpha, row0, nv);
+  bool ok = true;
+  if (tma) {
+    ok = wait_phase(inbar, nin & 1, err, abort_s);
+    ++nin;
+  } else if (tid < kT) {
+    stage_bf16(base + kQryQ, q + row0 * kD, nv, tid);
+    stage_bf16(base + kQryG, dout + row0 * kD, nv, tid);
+    fence_proxy_async_shared();  // a later item's tiles land in these buffers by TMA
+  }
+  if (tid == 0) bulk_wait_read0();  // the previous item's dq store has read the operand buffer
+  __syncthreads();
   double D = 0.0;
   bool first = true;
-  bool pend = false;  // a level's tensor reductions may still read the staged boxes
-  uint32_t phase = 0;
   for (int h = 0; (c >> h) != 0; ++h) {
     if (!((c >> h) & 1)) continue;
     const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
@@ -689,7 +732,7 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
           make_uint4(pack_bf16x2(lw * x[0], lw * x[1]), pack_bf16x2(lw * x[2], lw * x[3]),
                      pack_bf16x2(lw * x[4], lw * x[5]), pack_bf16x2(lw * x[6], lw * x[7]));
     }
-    ok = ok && wait_phase(ldbar, phase, err, abort_s);
+    ok = ok && wait_phase(ldbar, nlev & 1, err, abort_s);
     to_async();
     if (tid == 0 && ok) {
       mma128(tmem + 0, sG, false, sF, true, false);    // g = dO F_e
@@ -698,10 +741,18 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       umma_commit(bar);
     }
     first = false;
-    ok = ok && wait_phase(bar, phase, err, abort_s);
-    phase ^= 1;
+    ok = ok && wait_phase(bar, nlev & 1, err, abort_s);
+    ++nlev;
     tc_fence_after();
-    if (tid == 0 && ok && next_bit(h) >= 0) load_node(next_bit(h));  // the products have read the tile
+    if (tid == 0 && ok) {  // the products have read the node buffer: this item's next node, or the next item's first
+      const int hn = next_bit(c, h);
+      if (hn >= 0) {
+        load_node(c, bh, hn);
+      } else {
+        if (jn < items && tile_of(jn) > 0) load_node(tile_of(jn), head_of(jn), next_bit(tile_of(jn), -1));
+        if (dtma) load_dqp(row0);  // the last products have read the operand buffer too
+      }
+    }
     float part = 0.f;
     {
       // both column blocks of g from TMEM together
@@ -780,6 +831,15 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     pend = use_rmap;
     if (hf == 0 && i < nv) dlam[(row0 + i) * L + lv] = w * (part + qpart[i]);
   }
+  // Q and dO have had their last readers (before the level's barrier): the
+  // next item's tiles load while this item's dq is written; with no level
+  // here, the node buffer is free for the next item's first node as well
+  if (tid == 0 && ok && c == 0 && dtma) load_dqp(row0);
+  if (tid == 0 && ok && jn < items) {
+    if (c == 0 && tile_of(jn) > 0) load_node(tile_of(jn), head_of(jn), next_bit(tile_of(jn), -1));
+    if (full_tile(jn)) load_inputs(jn);
+    stage_l2(jn);
+  }
   // the levels above 7 that hold no key of this tile's queries
   if (hf == 0 && i < nv)
     for (int l = kLc + 1; l < L; ++l) {
@@ -798,6 +858,32 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
 #pragma unroll
       for (int u = 0; u < 32; ++u) xs[0][u] = xs[1][u] = 0.f;
     }
+    if (dtma) {
+      // dq = the in-tile part + the node part, in place in the operand
+      // buffer, then out by two tensor stores
+      ok = ok && wait_phase(obar, nout & 1, err, abort_s);
+      ++nout;
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int c8 = 4 * (2 * hf + hb) + w4;
+          float a[8];
+          row_chunk(base + kQryL, i, c8, a);
+          const float* x = xs[hb] + 8 * w4;
+          *reinterpret_cast<uint4*>(base + kQryL + swz(i, c8)) =
+              make_uint4(pack_bf16x2(a[0] + x[0], a[1] + x[1]), pack_bf16x2(a[2] + x[2], a[3] + x[3]),
+                         pack_bf16x2(a[4] + x[4], a[5] + x[5]), pack_bf16x2(a[6] + x[6], a[7] + x[7]));
+        }
+      }
+      fence_proxy_async_shared();
+      __syncthreads();
+      if (tid == 0 && ok) {
+        tma_store_2d(&tdo, base + kQryL, 0, (int)row0);
+        tma_store_2d(&tdo, base + kQryL + kHalf, 64, (int)row0);
+        bulk_commit();
+      }
+    } else
 #pragma unroll
     for (int hb = 0; hb < 2; ++hb) {
       const int cb = 2 * hf + hb;
@@ -812,6 +898,16 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
                        pack_bf16x2(a[4] + x[u + 4], a[5] + x[u + 5]), pack_bf16x2(a[6] + x[u + 6], a[7] + x[u + 7]));
       }
     }
+  }
+  // the next item, published by thread 0 once every thread is past this one
+  // (no wait of this item can raise the abort flag after the first barrier);
+  // the barriers also order this item's TMEM reads before the next one's products
+  tc_fence_before();
+  __syncthreads();
+  if (tid == 0) *next_s = *(volatile int*)abort_s ? items : jn;
+  __syncthreads();
+  j = *next_s;
+  if (j >= items) break;
   }
   bulk_wait_read0();  // this thread's reductions into R (its rows, or thread 0's boxes) have read their sources
   release_tmem<512>(tmem);
@@ -985,7 +1081,9 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int BH = s.B * s.H;
   const dim3 grid(N, BH);
   // the key-side nodes accumulate from 0
-  LL_CUDA_OK(cudaMemsetAsync(b.R, 0, (size_t)BH * N * kD * kD * sizeof(float), a.stream));
+  // (and the query kernel's item counter, the word after them)
+  unsigned* qctr = reinterpret_cast<unsigned*>(b.R + (size_t)BH * N * kD * kD);
+  LL_CUDA_OK(cudaMemsetAsync(b.R, 0, (size_t)BH * N * kD * kD * sizeof(float) + sizeof(unsigned), a.stream));
   const auto* q = static_cast<const __nv_bfloat16*>(a.q);
   const auto* k = static_cast<const __nv_bfloat16*>(a.k);
   const auto* v = static_cast<const __nv_bfloat16*>(a.v);
@@ -1001,13 +1099,13 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   LL_CUDA_OK(cudaGetDevice(&dev));
   LL_CUDA_OK(cudaDeviceGetAttribute(&sms, cudaDevAttrMultiProcessorCount, dev));
   const int items = N * BH;
-  const int intra_grid = std::max(1, std::min(items, sms));  // persistent, one CTA per SM
+  const int pgrid = std::max(1, std::min(items, sms));  // the persistent kernels: one CTA per SM
   // the intra kernel's outputs by tensor stores where the maps can be made
   CUtensorMap tdq, tdk, tdv, tS;
   const uint64_t srows = (uint64_t)BH * N * kD;
   const int use_omap = use_tma && srows <= 0x7fffffffull && tile_map(&tdq, b.dqp, rows) &&
                        tile_map(&tdk, b.dkp, rows) && tile_map(&tdv, b.dvp, rows) && f32_box_map(&tS, b.S, srows);
-  bwd_tc_intra_kernel<<<intra_grid, kIntraThreads, intra_smem(), a.stream>>>(
+  bwd_tc_intra_kernel<<<pgrid, kIntraThreads, intra_smem(), a.stream>>>(
       tq, tk, tv, tg, use_tma, tdq, tdk, tdv, tS, use_omap, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp, b.dvp, a.dlam, b.S, b.tot, b.dc, s.T,
       s.L, N, BH, b.err);
   LL_CUDA_OK(cudaGetLastError());
@@ -1019,9 +1117,12 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   CUtensorMap tr;
   const int use_rmap = rrows <= 0x7fffffffull && f32_box_map(&tr, b.R, rrows);
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_query_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)query_smem()));
-  bwd_tc_query_kernel<<<grid, kQryThreads, query_smem(), a.stream>>>(tq, tg, use_tma, tr, use_rmap, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp,
-                                                                  static_cast<__nv_bfloat16*>(a.dq), a.dlam, b.R, s.T,
-                                                                  s.L, b.err);
+  // dq's two parts in and out by TMA where the maps can be made
+  CUtensorMap tdi, tdo;
+  const int use_dmap = use_tma && tile_map(&tdi, b.dqp, rows) && tile_map(&tdo, a.dq, rows);
+  bwd_tc_query_kernel<<<pgrid, kQryThreads, query_smem(), a.stream>>>(
+      tq, tg, use_tma, tr, use_rmap, tdi, tdo, use_dmap, q, dout, a.log_alpha, a.lam, b.Ft, b.G, b.dqp, static_cast<__nv_bfloat16*>(a.dq),
+      a.dlam, b.R, s.T, s.L, N, BH, qctr, b.err);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
