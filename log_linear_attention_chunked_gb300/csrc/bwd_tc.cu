@@ -191,13 +191,18 @@ __device__ __forceinline__ void row_chunk(const unsigned char* tile, int r, int 
   x[0] = a.x; x[1] = a.y; x[2] = b.x; x[3] = b.y; x[4] = c.x; x[5] = c.y; x[6] = d.x; x[7] = d.y;
 }
 
-// cs[i] = the sum of log_alpha over rows 0..i of the tile (rows >= nv add 0),
-// float64; every thread takes part (a scan over each warp, then the warps'
-// totals); the caller synchronises before reading cs
-__device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
+// this thread's log_alpha of the tile (threads 0..127: rows; 0 past the tile's nv rows and for the other threads)
+__device__ __forceinline__ double tile_log_alpha(const float* log_alpha, size_t row0, int nv) {
+  const int t = threadIdx.x;
+  return (t < kT && t < nv) ? (double)log_alpha[row0 + t] : 0.0;
+}
+
+// cs[i] = x_0 + .. + x_i for the values x of tile_log_alpha, float64; every
+// thread takes part (a scan over each warp, then the warps' totals); the
+// caller synchronises before reading cs
+__device__ __forceinline__ void tile_scan(double* cs, double x) {
   __shared__ double wsum[8];  // the warps of the tile's rows (threads past 128 only synchronise)
   const int t = threadIdx.x, lane = t & 31, w = t >> 5;
-  double x = (t < kT && t < nv) ? (double)log_alpha[row0 + t] : 0.0;
 #pragma unroll
   for (int o = 1; o < 32; o <<= 1) {
     const double y = __shfl_up_sync(0xffffffffu, x, o);
@@ -209,6 +214,11 @@ __device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, 
     for (int ww = 0; ww < w; ++ww) x += wsum[ww];
     cs[t] = x;
   }
+}
+
+// cs[i] = the sum of log_alpha over rows 0..i of the tile (rows >= nv add 0)
+__device__ __forceinline__ void tile_cumsum(double* cs, const float* log_alpha, size_t row0, int nv) {
+  tile_scan(cs, tile_log_alpha(log_alpha, row0, nv));
 }
 
 // L2 prefetch of the 16-byte-aligned interior of [ptr, ptr + bytes) (a bulk
@@ -604,16 +614,19 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
 constexpr uint32_t kQryQ = 0, kQryG = kTileB, kQryL = 2 * kTileB, kQryF = 3 * kTileB, kQryR = 4 * kTileB;
 constexpr uint32_t kQryEnd = kQryR + kT * kRowP * 4;
 constexpr int kQryThreads = 256;  // two threads per row: columns 0..63 and 64..127
-// + cs, the second halves' dlam dots, three mbarriers, TMEM slot, flag, next item
-constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + kT * 4 + 64; }
+constexpr int kQryLamL = 32;  // lam rows of up to this many levels staged in shared memory
+// + cs, the second halves' dlam dots, an item's log_alpha and lam rows, five
+// mbarriers, TMEM slot, flags, next item
+constexpr size_t query_smem() { return 1024 + kQryEnd + kT * 8 + kT * 4 + kT * 4 + kT * kQryLamL * 4 + 64; }
 
 // Persistent over the (tile, head) items, one CTA per SM.  Item j is tile
 // c = N - 1 - j / BH of head j mod BH: the items of all heads' last tiles
 // first, the light ones of the first tiles (few set bits of c) at the end.
-// CTA b starts with item b and claims each later item from the counter *qctr
-// (zero at the launch) when it starts the item before, so that the later
-// item's first node tile and its input tiles stream in while the earlier one
-// finishes.
+// CTA b takes items b and b + gridDim.x, then claims items 2 gridDim.x + k
+// from the counter *qctr (zero at the launch), each when it starts the item
+// two before: the item after the current one is always known, so that its
+// first node tile, its input tiles and its rows of log_alpha and lam stream
+// in, and its cumsum is taken, while the current one finishes.
 
 __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     const __grid_constant__ CUtensorMap tq, const __grid_constant__ CUtensorMap tg, int use_tma,
@@ -628,19 +641,25 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kQryEnd);
   float* qpart = reinterpret_cast<float*>(cs + kT);  // [128] the dlam dot of the columns 64..127
-  uint64_t* bar = reinterpret_cast<uint64_t*>(qpart + kT);
+  float* la_s = qpart + kT;    // [128] an item's log_alpha
+  float* lam_s = la_s + kT;    // [128][L] an item's lam rows (L <= kQryLamL)
+  uint64_t* bar = reinterpret_cast<uint64_t*>(lam_s + kT * kQryLamL);
   uint64_t* ldbar = bar + 1;  // the bulk load of a node tile
   uint64_t* inbar = bar + 2;  // the TMA loads of the input tiles
   uint64_t* obar = bar + 3;   // the TMA load of the in-tile dq tile
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 4);
+  uint64_t* sbar = bar + 4;   // the bulk loads of an item's log_alpha and lam rows
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 5);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
-  int* next_s = abort_s + 1;  // the item after the current one (or items: none)
+  int* next_s = abort_s + 1;  // [2] the item after the current one (or items: none), by the parity of the item count
+  int* stop_s = next_s + 2;   // an abort seen at an item's end
   const int tid = threadIdx.x;
   const int items = N * BH;
   const size_t mat = (size_t)kD * kD;
   auto tile_of = [&](int j) { return N - 1 - j / BH; };
   auto head_of = [&](int j) { return (size_t)(j % BH); };
   auto full_tile = [&](int j) { return use_tma && T - tile_of(j) * kT >= kT; };  // its inputs by TMA
+  // its log_alpha and lam rows by bulk copies (16-byte aligned: T a multiple of 4)
+  auto rows_smem = [&](int j) { return T - tile_of(j) * kT >= kT && (T & 3) == 0 && L <= kQryLamL; };
   auto next_bit = [](int c, int h) {  // the set bit of c above h, or -1
     for (++h; (c >> h) != 0; ++h)
       if ((c >> h) & 1) return h;
@@ -660,15 +679,26 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     tma_tile(base + kQryQ, &tq, inbar, r);
     tma_tile(base + kQryG, &tg, inbar, r);
   };
-  // thread 0: item j's rows of log_alpha and lam into L2 (and the in-tile dq
-  // where the threads read it)
+  // thread 0: item j's rows that the threads read from global into L2: of
+  // log_alpha and lam where they are not copied to shared memory, of the
+  // in-tile dq where it is not loaded by TMA
   auto stage_l2 = [&](int j) {
     const int cn = tile_of(j);
     const size_t r = head_of(j) * T + (size_t)cn * kT;
     const int nn = min(kT, T - cn * kT);
-    prefetch_l2_inside(log_alpha + r, (uint32_t)(nn * 4));
-    prefetch_l2_inside(lam + r * L, (uint32_t)(nn * L * 4));
+    if (!rows_smem(j)) {
+      prefetch_l2_inside(log_alpha + r, (uint32_t)(nn * 4));
+      prefetch_l2_inside(lam + r * L, (uint32_t)(nn * L * 4));
+    }
     if (!(use_dmap && full_tile(j))) bulk_prefetch_l2(dqp + r * kD, (uint32_t)(nn * kD * 2));
+  };
+  // thread 0: item j's rows of log_alpha and lam into shared memory (after
+  // the last reads of the previous ones)
+  auto load_rows = [&](int j) {
+    const size_t r = head_of(j) * T + (size_t)tile_of(j) * kT;
+    mbar_arrive_expect_tx(sbar, (uint32_t)(kT * 4 + kT * L * 4));
+    bulk_load(la_s, log_alpha + r, (uint32_t)(kT * 4), sbar);
+    bulk_load(lam_s, lam + r * L, (uint32_t)(kT * L * 4), sbar);
   };
   // thread 0: the in-tile dq tile of rows r.. into the operand buffer, free
   // once the item's last products have read it
@@ -677,34 +707,59 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     tma_tile(base + kQryL, &tdi, obar, r);
   };
   int j = blockIdx.x;
-  int jn = items;  // thread 0: the item claimed after j
+  int jn = j + (int)gridDim.x < items ? j + (int)gridDim.x : items;  // thread 0: the item after j
+  unsigned jraw = 0;  // thread 0: the claim made during the current item (read at its end)
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(ldbar, 1);
     mbar_init(inbar, 1);
     mbar_init(obar, 1);
+    mbar_init(sbar, 1);
     fence_mbar_init();  // the copies below arrive on them
     // the first item's first node tile and input tiles go out before the
     // TMEM allocation and the cumsum, which run while they land
     if (tile_of(j) > 0) load_node(tile_of(j), head_of(j), next_bit(tile_of(j), -1));
     if (full_tile(j)) load_inputs(j);
+    if (rows_smem(j)) load_rows(j);
   }
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   const uint32_t sQ = smem_u32(base + kQryQ), sG = smem_u32(base + kQryG), sL = smem_u32(base + kQryL),
                  sF = smem_u32(base + kQryF);
   const int i = tid & (kT - 1), hf = tid >> 7;  // row i, columns 64 hf .. 64 hf + 63
-  uint32_t nlev = 0, nin = 0, nout = 0;  // the levels (node loads, product commits), the TMA input and dq loads so far
+  // the levels (node loads, product commits), the TMA input, dq and row loads so far
+  uint32_t nlev = 0, nin = 0, nout = 0, nrow = 0;
   bool pend = false;  // a level's tensor reductions may still read the staged boxes
-  for (;;) {
+  // item jj's cumsum (its rows of log_alpha from shared memory where they
+  // were copied there): every thread, after the last reads of cs
+  auto cumsum_of = [&](int jj) -> bool {
+    bool okr = true;
+    double x;
+    if (rows_smem(jj)) {
+      okr = wait_phase(sbar, nrow & 1, err, abort_s);
+      ++nrow;
+      x = tid < kT ? (double)la_s[tid] : 0.0;
+    } else {
+      x = tile_log_alpha(log_alpha, head_of(jj) * T + (size_t)tile_of(jj) * kT, min(kT, T - tile_of(jj) * kT));
+    }
+    tile_scan(cs, x);
+    return okr;
+  };
+  bool okc = cumsum_of(j);
+  for (uint32_t it = 0;; ++it) {
   const int c = tile_of(j);
   const size_t bh = head_of(j);
   const size_t row0 = bh * T + (size_t)c * kT;
   const int nv = min(kT, T - c * kT);
   const bool tma = full_tile(j);
   const bool dtma = use_dmap && tma;  // dq in and out by TMA through the operand buffer
-  if (tid == 0) jn = (int)gridDim.x + (int)atomicAdd(qctr, 1u);  // used from the first level's products on
-  tile_cumsum(cs, log_alpha, row0, nv);
-  bool ok = true;
+  const bool rsm = rows_smem(j);  // lam from shared memory
+  if (tid == 0) {
+    next_s[it & 1] = jn;  // read after the barrier below
+    // the item after jn (a claim past the end, also when jn is none, takes
+    // nothing: the claims are handed out in order)
+    jraw = atomicAdd(qctr, 1u);
+  }
+  bool ok = okc;
   if (tma) {
     ok = wait_phase(inbar, nin & 1, err, abort_s);
     ++nin;
@@ -715,14 +770,17 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
   }
   if (tid == 0) bulk_wait_read0();  // the previous item's dq store has read the operand buffer
   __syncthreads();
+  const int jx = next_s[it & 1];  // the next item, known to every thread
   double D = 0.0;
   bool first = true;
   for (int h = 0; (c >> h) != 0; ++h) {
     if (!((c >> h) & 1)) continue;
     const int e = ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1;
     const int lv = kLc + 1 + h;
+    const int hn = next_bit(c, h);  // the item's next level, or -1
+    const double g_e = G[bh * N + e];  // added to D at the level's end
     const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
-    const float lw = i < nv ? w * lam[(row0 + i) * L + lv] : 0.f;
+    const float lw = i < nv ? w * (rsm ? lam_s[i * L + lv] : lam[(row0 + i) * L + lv]) : 0.f;
     // dO rows scaled by lw (this thread's half row)
 #pragma unroll 4
     for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
@@ -745,7 +803,6 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     ++nlev;
     tc_fence_after();
     if (tid == 0 && ok) {  // the products have read the node buffer: this item's next node, or the next item's first
-      const int hn = next_bit(c, h);
       if (hn >= 0) {
         load_node(c, bh, hn);
       } else {
@@ -819,9 +876,16 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
         }
       }
     }
-    D += G[bh * N + e];
+    D += g_e;
     tc_fence_before();
     __syncthreads();  // the next level rewrites the staged tiles and the TMEM columns
+    if (hn < 0 && tid == 0 && ok && jn < items) {
+      // the item's last level: Q and dO have had their last readers, and the
+      // next item's tiles go out ahead of this level's reductions
+      if (full_tile(jn)) load_inputs(jn);
+      if (rows_smem(jn)) load_rows(jn);  // this level has read the item's lam rows
+      stage_l2(jn);
+    }
     if (use_rmap && tid == 0 && ok) {
       const int y = (int)((bh * N + e) * kD);
 #pragma unroll
@@ -831,14 +895,16 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     pend = use_rmap;
     if (hf == 0 && i < nv) dlam[(row0 + i) * L + lv] = w * (part + qpart[i]);
   }
-  // Q and dO have had their last readers (before the level's barrier): the
-  // next item's tiles load while this item's dq is written; with no level
-  // here, the node buffer is free for the next item's first node as well
-  if (tid == 0 && ok && c == 0 && dtma) load_dqp(row0);
-  if (tid == 0 && ok && jn < items) {
-    if (c == 0 && tile_of(jn) > 0) load_node(tile_of(jn), head_of(jn), next_bit(tile_of(jn), -1));
-    if (full_tile(jn)) load_inputs(jn);
-    stage_l2(jn);
+  // an item with no level: the buffers are free for its dq tile and the
+  // next item's node and input tiles
+  if (tid == 0 && ok && c == 0) {
+    if (dtma) load_dqp(row0);
+    if (jn < items) {
+      if (tile_of(jn) > 0) load_node(tile_of(jn), head_of(jn), next_bit(tile_of(jn), -1));
+      if (full_tile(jn)) load_inputs(jn);
+      if (rows_smem(jn)) load_rows(jn);
+      stage_l2(jn);
+    }
   }
   // the levels above 7 that hold no key of this tile's queries
   if (hf == 0 && i < nv)
@@ -899,15 +965,20 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       }
     }
   }
-  // the next item, published by thread 0 once every thread is past this one
-  // (no wait of this item can raise the abort flag after the first barrier);
-  // the barriers also order this item's TMEM reads before the next one's products
+  if (jx < items) okc = cumsum_of(jx);  // this item's levels have read cs
+  // an abort, published by thread 0 once every thread is past this item (no
+  // wait of it can raise the flag after the first barrier); the barriers also
+  // order this item's TMEM reads before the next one's products
   tc_fence_before();
   __syncthreads();
-  if (tid == 0) *next_s = *(volatile int*)abort_s ? items : jn;
+  if (tid == 0) {
+    *stop_s = *(volatile int*)abort_s;
+    const int cand = 2 * (int)gridDim.x + (int)jraw;
+    jn = cand < items ? cand : items;
+  }
   __syncthreads();
-  j = *next_s;
-  if (j >= items) break;
+  if (jx >= items || *stop_s) break;
+  j = jx;
   }
   bulk_wait_read0();  // this thread's reductions into R (its rows, or thread 0's boxes) have read their sources
   release_tmem<512>(tmem);
