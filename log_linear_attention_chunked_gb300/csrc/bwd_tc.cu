@@ -990,6 +990,8 @@ constexpr size_t key_smem() { return 1024 + kKeyEnd + kT * 8 + kT * 4 + kT * 4 +
 
 __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     const __grid_constant__ CUtensorMap tk, const __grid_constant__ CUtensorMap tv, int use_tma,
+    const __grid_constant__ CUtensorMap tkpi, const __grid_constant__ CUtensorMap tvpi,
+    const __grid_constant__ CUtensorMap tko, const __grid_constant__ CUtensorMap tvo, int use_kmap,
     const __nv_bfloat16* __restrict__ k, const __nv_bfloat16* __restrict__ v, const float* __restrict__ log_alpha,
     const float* __restrict__ lam, const float* __restrict__ dlam, const float* __restrict__ R,
     const double* __restrict__ cum, const __nv_bfloat16* __restrict__ dkp, const __nv_bfloat16* __restrict__ dvp,
@@ -1004,7 +1006,8 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   int* n_s = reinterpret_cast<int*>(srcs + 32);
   uint64_t* bar = reinterpret_cast<uint64_t*>(n_s + 2);
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
-  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
+  uint64_t* obar = bar + 2;   // the TMA loads of the in-tile dk and dv tiles
+  uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 3);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
   const int c = blockIdx.x, N = gridDim.x;
   const size_t bh = blockIdx.y;
@@ -1013,10 +1016,12 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   const int nv = min(kT, T - c * kT);
   const size_t mat = (size_t)kD * kD;
   const bool tma = use_tma && nv == kT;
+  const bool otma = use_kmap && tma;  // dk and dv in and out by TMA through the K and E buffers
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(inbar, 1);
-    fence_mbar_init();  // the copies below arrive on it
+    mbar_init(obar, 1);
+    fence_mbar_init();  // the copies below arrive on them
     if (tma) {  // the input tiles go out first; the node list, cumsum and TMEM allocation run while they land
       mbar_arrive_expect_tx(inbar, 2 * kTileB);
       tma_tile(base + kKeyK, &tk, inbar, row0);
@@ -1040,9 +1045,21 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
   tile_cumsum(cs, log_alpha, row0, nv);
   const uint32_t tmem = setup_tmem<256>(bar, slot);
   const int n = *n_s;
-  float lamdot = 0.f;  // sum_l lam_j[l] dlam_j[l] of this row, loaded ahead of its use
-  if (tid < nv)
-    for (int l = 0; l < L; ++l) lamdot = fmaf(lam[(row0 + tid) * L + l], dlam[(row0 + tid) * L + l], lamdot);
+  float lamdot = 0.f;  // sum_l lam_j[l] dlam_j[l] of this row (16 levels' loads issued together)
+  if (tid < nv) {
+    const float* lr = lam + (row0 + tid) * L;
+    const float* dr = dlam + (row0 + tid) * L;
+    for (int l0 = 0; l0 < L; l0 += 16) {
+      float a[16], d[16];
+#pragma unroll
+      for (int u = 0; u < 16; ++u) {
+        a[u] = l0 + u < L ? lr[l0 + u] : 0.f;
+        d[u] = l0 + u < L ? dr[l0 + u] : 0.f;
+      }
+#pragma unroll
+      for (int u = 0; u < 16; ++u) lamdot = fmaf(a[u], d[u], lamdot);
+    }
+  }
   wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
   if (!tma) {
     stage_bf16(base + kKeyK, k + row0 * kD, nv, tid);
@@ -1061,9 +1078,68 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     wait_phase(bar, 0, err, abort_s);  // after a timeout the error word is set; the results are not used
     tc_fence_after();
   }
+  // the products have read K and E (or there were none): the in-tile dv and
+  // dk tiles load into them while the node parts come out of TMEM
+  if (otma && tid == 0) {
+    mbar_arrive_expect_tx(obar, 2 * kTileB);
+    tma_tile(base + kKeyE, &tvpi, obar, row0);
+    tma_tile(base + kKeyK, &tkpi, obar, row0);
+  }
   const int j = tid;
   const float wj = wdec[j];
   float vdv = 0.f;
+  if (otma) {
+    bool okd = true, waited = false;
+#pragma unroll 1
+    for (int o = 0; o < 2; ++o) {  // 0: dv (in the E buffer), 1: dk (in the K buffer)
+      unsigned char* tile = base + (o == 0 ? kKeyE : kKeyK);
+#pragma unroll 1
+      for (int cb = 0; cb < 4; ++cb) {
+        float x[32];
+        if (n > 0) {
+          tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);
+          tmem_ld_wait();
+        } else {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) x[u] = 0.f;
+        }
+        if (o == 0) {  // the part of v_j . dv_j from the later tiles
+#pragma unroll
+          for (int w4 = 0; w4 < 4; ++w4) {
+            float vv[8];
+            row_chunk(base + kKeyV, j, 4 * cb + w4, vv);
+#pragma unroll
+            for (int t = 0; t < 8; ++t) vdv = fmaf(vv[t], wj * x[8 * w4 + t], vdv);
+          }
+        }
+        if (!waited) {
+          okd = wait_phase(obar, 0, err, abort_s);
+          waited = true;
+        }
+#pragma unroll
+        for (int w4 = 0; w4 < 4; ++w4) {
+          const int c8 = 4 * cb + w4;
+          float y[8];
+          row_chunk(tile, j, c8, y);
+#pragma unroll
+          for (int t = 0; t < 8; ++t) y[t] = fmaf(wj, x[8 * w4 + t], y[t]);
+          *reinterpret_cast<uint4*>(tile + swz(j, c8)) =
+              make_uint4(pack_bf16x2(y[0], y[1]), pack_bf16x2(y[2], y[3]), pack_bf16x2(y[4], y[5]),
+                         pack_bf16x2(y[6], y[7]));
+        }
+      }
+    }
+    fence_proxy_async_shared();
+    __syncthreads();
+    if (tid == 0 && okd) {
+      tma_store_2d(&tvo, base + kKeyE, 0, (int)row0);
+      tma_store_2d(&tvo, base + kKeyE + kHalf, 64, (int)row0);
+      tma_store_2d(&tko, base + kKeyK, 0, (int)row0);
+      tma_store_2d(&tko, base + kKeyK + kHalf, 64, (int)row0);
+      bulk_commit();
+      bulk_wait_read0();  // the tiles are read before the CTA's shared memory goes
+    }
+  } else
 #pragma unroll 1
   for (int o = 0; o < 2; ++o) {  // 0: dv, 1: dk
     const __nv_bfloat16* src = (o == 0 ? dvp : dkp) + (row0 + j) * kD;
@@ -1196,8 +1272,12 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
       a.dlam, b.R, s.T, s.L, N, BH, qctr, b.err);
   LL_CUDA_OK(cudaGetLastError());
   LL_CUDA_OK(cudaFuncSetAttribute(bwd_tc_key_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)key_smem()));
+  // dk's and dv's two parts in and out by TMA where the maps can be made
+  CUtensorMap tkpi, tvpi, tko, tvo;
+  const int use_kmap = use_tma && tile_map(&tkpi, b.dkp, rows) && tile_map(&tvpi, b.dvp, rows) &&
+                       tile_map(&tko, a.dk, rows) && tile_map(&tvo, a.dv, rows);
   bwd_tc_key_kernel<<<grid, kThreads, key_smem(), a.stream>>>(
-      tk, tv, use_tma, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dkp, b.dvp, static_cast<__nv_bfloat16*>(a.dk),
+      tk, tv, use_tma, tkpi, tvpi, tko, tvo, use_kmap, k, v, a.log_alpha, a.lam, a.dlam, b.R, b.cum, b.dkp, b.dvp, static_cast<__nv_bfloat16*>(a.dk),
       static_cast<__nv_bfloat16*>(a.dv), b.dc, s.T, s.L, b.err);
   LL_CUDA_OK(cudaGetLastError());
   return LL_OK;
