@@ -438,23 +438,24 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           if (lvc == 7) dl[7] += acc;
           else dl[6] += acc;
         } else {
+          // the diagonal block, keys j <= i: branch-free over the columns (the
+          // masked ones take exp2(0) and are selected away), so that the 32
+          // columns' loads and exponentials overlap instead of running one
+          // after another
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const int j = 32 * cb + u;
-            p[u] = 0.f;
-            da[u] = 0.f;
-            if (j <= i && row_ok) {
-              const float ex = exp2f(ci - c2[j]);
-              const int lv = bitlen((unsigned)(i ^ j));  // 0..5 inside the diagonal block
-              float lmv = lm[0];
+            const bool on = j <= i && row_ok;
+            const float ex = exp2f(on ? ci - c2[j] : 0.f);
+            const int lv = bitlen((unsigned)(i ^ j));  // 0..5 inside the diagonal block
+            float lmv = lm[0];
 #pragma unroll
-              for (int l = 1; l < 6; ++l) lmv = lv == l ? lm[l] : lmv;
-              p[u] = a[u] * ex * lmv;
-              da[u] = g[u] * ex * lmv;
-              const float xx = g[u] * a[u] * ex;
+            for (int l = 1; l < 6; ++l) lmv = lv == l ? lm[l] : lmv;
+            p[u] = on ? a[u] * ex * lmv : 0.f;
+            da[u] = on ? g[u] * ex * lmv : 0.f;
+            const float xx = on ? g[u] * a[u] * ex : 0.f;
 #pragma unroll
-              for (int l = 0; l < 6; ++l) dl[l] += lv == l ? xx : 0.f;
-            }
+            for (int l = 0; l < 6; ++l) dl[l] += lv == l ? xx : 0.f;
           }
         }
         // v_j . dv_j inside the tile is the column sum of P . G, kept in float32
