@@ -283,7 +283,32 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
 constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
 constexpr int kIntraThreads = 256;  // two threads per row: columns 0..63 and 64..127
-constexpr size_t intra_smem() { return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 64; }
+constexpr size_t intra_smem() {
+  return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 8 * 6 * 32 * 4 + 64;
+}
+
+// v[idx] for a runtime idx < n (n a power of two), by a tree of selects on
+// the bits of idx (the values stay in registers)
+template <int n>
+__device__ __forceinline__ float pick(const float* v, int idx) {
+  float r[n / 2];
+#pragma unroll
+  for (int m = 0; m < n / 2; ++m) r[m] = (idx & 1) ? v[2 * m + 1] : v[2 * m];
+  if constexpr (n == 2) {
+    return r[0];
+  } else {
+    return pick<n / 2>(r, idx >> 1);
+  }
+}
+
+// 2^x by the hardware approximation (relative error ~2^-22, subnormal
+// results flushed to 0): for the in-tile decays, whose products end in bf16
+// operands or float32 sums of many terms
+__device__ __forceinline__ float ex2(float x) {
+  float y;
+  asm("ex2.approx.ftz.f32 %0, %1;" : "=f"(y) : "f"(x));
+  return y;
+}
 
 // Reduce-scatter over a warp: lane l receives the sum over the 32 lanes of v[l].
 __device__ __forceinline__ float warp_column_sums(float (&v)[32]) {
@@ -320,7 +345,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
   float* dlhalf = c2 + kT;       // [128][8] the in-tile dlam of the columns 64..127
   float* colf = dlhalf + kT * 8;  // exp2(c2_e - c2_j), e = the end of j's 32-column block
-  uint64_t* bar = reinterpret_cast<uint64_t*>(colf + kT);
+  float* lmt = colf + kT;         // [8 warps][6 levels][32 lanes] the in-block lambdas of a warp's rows
+  uint64_t* bar = reinterpret_cast<uint64_t*>(lmt + 8 * 6 * 32);
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
@@ -386,7 +412,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   if (tid < kT) {
     c2[tid] = (float)cs[tid] * 1.4426950408889634f;
     wdec[tid] = expf((float)(cs[kT - 1] - cs[tid]));
-    colf[tid] = exp2f((float)(cs[(tid | 31)] - cs[tid]) * 1.4426950408889634f);
+    colf[tid] = ex2((float)(cs[(tid | 31)] - cs[tid]) * 1.4426950408889634f);
   }
   float lm[8];  // the row's in-tile lambdas, loaded while the products run
 #pragma unroll
@@ -423,7 +449,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           // all keys of the block lie before the row: exp2(c_i - c_j) = exp2(c_i -
           // c_e) exp2(c_e - c_j), e = the block's end, both factors <= 1, the
           // second from the per-tile column table
-          const float rf = row_ok ? exp2f(ci - c2[32 * cb + 31]) : 0.f;
+          const float rf = row_ok ? ex2(ci - c2[32 * cb + 31]) : 0.f;
           const float rl = rf * lmv;
           float acc = 0.f;
 #pragma unroll
@@ -441,22 +467,42 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           // the diagonal block, keys j <= i: branch-free over the columns (the
           // masked ones take exp2(0) and are selected away), so that the 32
           // columns' loads and exponentials overlap instead of running one
-          // after another
+          // after another; i ^ j = lane ^ u, and the lambda of its level comes
+          // from the warp's table in shared memory
+          float* lmw = lmt + (tid >> 5) * (6 * 32);
+#pragma unroll
+          for (int l = 0; l < 6; ++l) lmw[l * 32 + lane] = lm[l];
+          __syncwarp();
+          float xx[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const int j = 32 * cb + u;
             const bool on = j <= i && row_ok;
-            const float ex = exp2f(on ? ci - c2[j] : 0.f);
-            const int lv = bitlen((unsigned)(i ^ j));  // 0..5 inside the diagonal block
-            float lmv = lm[0];
-#pragma unroll
-            for (int l = 1; l < 6; ++l) lmv = lv == l ? lm[l] : lmv;
+            const float ex = ex2(on ? ci - c2[j] : 0.f);
+            const float lmv = lmw[bitlen((unsigned)(lane ^ u)) * 32 + lane];  // levels 0..5
             p[u] = on ? a[u] * ex * lmv : 0.f;
             da[u] = on ? g[u] * ex * lmv : 0.f;
-            const float xx = on ? g[u] * a[u] * ex : 0.f;
-#pragma unroll
-            for (int l = 0; l < 6; ++l) dl[l] += lv == l ? xx : 0.f;
+            xx[u] = on ? g[u] * a[u] * ex : 0.f;
           }
+          // row i's keys of level l >= 1 are the aligned block of 2^(l-1)
+          // columns beside the row's own block of that size (level 0: its own
+          // column; the masked columns hold 0): sums over aligned blocks, the
+          // row's picked by the bits of its lane
+          float b1[16], b2[8], b3[4], b4[2];
+#pragma unroll
+          for (int m = 0; m < 16; ++m) b1[m] = xx[2 * m] + xx[2 * m + 1];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) b2[m] = b1[2 * m] + b1[2 * m + 1];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) b3[m] = b2[2 * m] + b2[2 * m + 1];
+#pragma unroll
+          for (int m = 0; m < 2; ++m) b4[m] = b3[2 * m] + b3[2 * m + 1];
+          dl[0] += pick<32>(xx, lane);
+          dl[1] += pick<32>(xx, lane ^ 1);
+          dl[2] += pick<16>(b1, (lane >> 1) ^ 1);
+          dl[3] += pick<8>(b2, (lane >> 2) ^ 1);
+          dl[4] += pick<4>(b3, (lane >> 3) ^ 1);
+          dl[5] += pick<2>(b4, (lane >> 4) ^ 1);
         }
         // v_j . dv_j inside the tile is the column sum of P . G, kept in float32
         float pg[32];
