@@ -49,6 +49,7 @@
 #include <algorithm>
 
 #include "bwd.cuh"
+#include "sm100.cuh"
 
 namespace llattn {
 
@@ -278,6 +279,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
 // float64 arithmetic.
 constexpr int kFenFastN = kFenwickOnChipChunks;
 constexpr int kFenLv = 13;  // levels of N <= 4096
+constexpr int kFenD = 16;   // ring slots of the chunk states streamed ahead
 
 __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float* __restrict__ S,
                                                                      float* __restrict__ F,
@@ -337,14 +339,19 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
   const float* Sb = S + bh * N * (size_t)mat;
   float* Fb = F + bh * N * (size_t)mat;
   const int tel = Ft ? swizzled_elem(idx >> 7, idx & 127) : 0;
-  float s0 = Sb[idx], s1 = N > 1 ? Sb[(size_t)mat + idx] : 0.f, s2 = N > 2 ? Sb[2 * (size_t)mat + idx] : 0.f,
-        s3 = N > 3 ? Sb[3 * (size_t)mat + idx] : 0.f;
+  // the thread's element of each chunk state streams through a ring of kFenD
+  // slots in shared memory, kFenD - 1 chunks ahead, by per-thread
+  // asynchronous copies (each thread reads back only what it copied)
+  float* ring = last + kFenLv * kThreads;  // [kFenD][kThreads]
+  auto stream_in = [&](int i) {  // chunk i's element (past the end: an empty group)
+    if (i < N) sm100::cp_async4(ring + (i % kFenD) * kThreads + threadIdx.x, Sb + (size_t)i * mat + idx);
+    sm100::cp_async_commit();
+  };
+  for (int i = 0; i < kFenD - 1; ++i) stream_in(i);
   for (int i = 0; i < N; ++i) {
-    float acc = s0;
-    s0 = s1;
-    s1 = s2;
-    s2 = s3;
-    s3 = i + 4 < N ? Sb[(size_t)(i + 4) * mat + idx] : 0.f;
+    stream_in(i + kFenD - 1);  // into the slot of chunk i - 1, read in the iteration before
+    sm100::cp_async_wait<kFenD - 1>();  // chunk i's copy has landed
+    float acc = ring[(i % kFenD) * kThreads + threadIdx.x];
     const int h = __ffs(~i) - 1, o = i - __popc(i);
     for (int m = 0; m < h; ++m) acc = fmaf(coef[o + m], last[m * kThreads + threadIdx.x], acc);
     last[h * kThreads + threadIdx.x] = acc;
@@ -555,7 +562,7 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
                               cudaStream_t stream, __nv_bfloat16* Ft, double* cum, bool f32_nodes) {
   if (N <= kFenFastN) {
-    const size_t smf = (size_t)N * (sizeof(double) + sizeof(float)) + (size_t)kFenLv * kThreads * sizeof(float);
+    const size_t smf = (size_t)N * (sizeof(double) + sizeof(float)) + (size_t)(kFenLv + kFenD) * kThreads * sizeof(float);
     LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
     simt_fenwick_fast_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(
         S, F, tot, G, N, mat, Ft, cum, f32_nodes || !Ft ? 1 : 0);

@@ -354,15 +354,11 @@ namespace fast {
 using sm100::smem_u32;
 using sm100::bulk_prefetch_l2;
 
-__device__ __forceinline__ void cp_async16(float* dst, const float* src) {
-  asm volatile("cp.async.cg.shared.global [%0], [%1], 16;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async4(float* dst, const float* src) {
-  asm volatile("cp.async.ca.shared.global [%0], [%1], 4;" ::"r"(smem_u32(dst)), "l"(src) : "memory");
-}
-__device__ __forceinline__ void cp_async_commit() { asm volatile("cp.async.commit_group;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait0() { asm volatile("cp.async.wait_group 0;" ::: "memory"); }
-__device__ __forceinline__ void cp_async_wait1() { asm volatile("cp.async.wait_group 1;" ::: "memory"); }
+using sm100::cp_async16;
+using sm100::cp_async4;
+using sm100::cp_async_commit;
+__device__ __forceinline__ void cp_async_wait0() { sm100::cp_async_wait<0>(); }
+__device__ __forceinline__ void cp_async_wait1() { sm100::cp_async_wait<1>(); }
 
 // 64 rows x 128 floats (contiguous in global) into a padded shared tile.
 __device__ __forceinline__ void stage_tile(float* dst, const float* src, int tid) {
