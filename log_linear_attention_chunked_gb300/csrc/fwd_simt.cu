@@ -279,8 +279,18 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
 // float64 arithmetic.
 constexpr int kFenFastN = kFenwickOnChipChunks;
 constexpr int kFenLv = 13;  // levels of N <= 4096
-constexpr int kFenD = 16;   // ring slots of the chunk states streamed ahead
+// ring slots of the chunk states streamed ahead, for kVec elements per thread
+__host__ __device__ constexpr int fen_ring(int kVec) { return kVec == 4 ? 8 : 16; }
+// dynamic shared memory: the prefix table, the child decays, then (16-byte
+// aligned) the latest nodes of each level and the ring
+constexpr size_t fen_smem(int N, int kVec) {
+  return (size_t)N * (sizeof(double) + sizeof(float)) + 16 +
+         (size_t)(kFenLv + fen_ring(kVec)) * kThreads * kVec * sizeof(float);
+}
 
+// Each thread follows kVec consecutive elements of the matrix (4 where the
+// matrix size allows 16-byte copies, else 1).
+template <int kVec>
 __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float* __restrict__ S,
                                                                      float* __restrict__ F,
                                                                      const double* __restrict__ tot,
@@ -289,7 +299,8 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
                                                                      double* __restrict__ cum, int write_f) {
   extern __shared__ double Gs[];                                  // [N]
   float* coef = reinterpret_cast<float*>(Gs + N);                 // [N] child decays
-  float* last = coef + N;                                         // [kFenLv][kThreads]
+  // [kFenLv][kThreads][kVec] the latest node of each level, then the ring
+  float* last = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(coef + N) + 15) & ~uintptr_t(15));
   __shared__ double wsum[kThreads / 32];
   const size_t bh = blockIdx.y;
   const int lane = threadIdx.x & 31, warp = threadIdx.x >> 5;
@@ -334,29 +345,66 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
   }
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < N; i += kThreads) G[bh * N + i] = Gs[i];
-  const int idx = blockIdx.x * kThreads + threadIdx.x;
-  if (idx >= mat) return;
-  const float* Sb = S + bh * N * (size_t)mat;
-  float* Fb = F + bh * N * (size_t)mat;
-  const int tel = Ft ? swizzled_elem(idx >> 7, idx & 127) : 0;
-  // the thread's element of each chunk state streams through a ring of kFenD
-  // slots in shared memory, kFenD - 1 chunks ahead, by per-thread
-  // asynchronous copies (each thread reads back only what it copied)
-  float* ring = last + kFenLv * kThreads;  // [kFenD][kThreads]
-  auto stream_in = [&](int i) {  // chunk i's element (past the end: an empty group)
-    if (i < N) sm100::cp_async4(ring + (i % kFenD) * kThreads + threadIdx.x, Sb + (size_t)i * mat + idx);
+  const int e0 = (blockIdx.x * kThreads + threadIdx.x) * kVec;  // the thread's first element
+  if (e0 >= mat) return;
+  constexpr int kD = fen_ring(kVec);
+  // the thread's elements of each chunk state stream through a ring of kD
+  // slots in shared memory, kD - 1 chunks ahead, by per-thread asynchronous
+  // copies (each thread reads back only what it copied); the addresses
+  // advance by one matrix per chunk
+  float* ring = last + kFenLv * kThreads * kVec;  // [kD][kThreads][kVec]
+  const float* next = S + bh * N * (size_t)mat + e0;
+  int issued = 0;
+  auto stream_in = [&]() {  // the next chunk's elements (past the end: an empty group)
+    if (issued < N) {
+      float* slot = ring + ((issued % kD) * kThreads + threadIdx.x) * kVec;
+      if constexpr (kVec == 4) {
+        sm100::cp_async16(slot, next);
+      } else {
+        sm100::cp_async4(slot, next);
+      }
+      next += mat;
+    }
+    ++issued;
     sm100::cp_async_commit();
   };
-  for (int i = 0; i < kFenD - 1; ++i) stream_in(i);
+  float* fdst = F + bh * N * (size_t)mat + e0;
+  __nv_bfloat16* tdst = Ft ? Ft + bh * N * (size_t)mat + swizzled_elem(e0 >> 7, e0 & 127) : nullptr;
+  for (int k = 0; k < kD - 1; ++k) stream_in();
   for (int i = 0; i < N; ++i) {
-    stream_in(i + kFenD - 1);  // into the slot of chunk i - 1, read in the iteration before
-    sm100::cp_async_wait<kFenD - 1>();  // chunk i's copy has landed
-    float acc = ring[(i % kFenD) * kThreads + threadIdx.x];
+    stream_in();  // into the slot of chunk i - 1, read in the iteration before
+    sm100::cp_async_wait<kD - 1>();  // chunk i's copy has landed
+    float acc[kVec];
+    const float* s = ring + ((i % kD) * kThreads + threadIdx.x) * kVec;
+    if constexpr (kVec == 4) {
+      const float4 x = *reinterpret_cast<const float4*>(s);
+      acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w;
+    } else {
+      acc[0] = s[0];
+    }
     const int h = __ffs(~i) - 1, o = i - __popc(i);
-    for (int m = 0; m < h; ++m) acc = fmaf(coef[o + m], last[m * kThreads + threadIdx.x], acc);
-    last[h * kThreads + threadIdx.x] = acc;
-    if (write_f) Fb[(size_t)i * mat + idx] = acc;
-    if (Ft) Ft[(bh * N + i) * (size_t)mat + tel] = __float2bfloat16_rn(acc);
+    for (int m = 0; m < h; ++m) {
+      const float cf = coef[o + m];
+      const float* lp = last + (m * kThreads + threadIdx.x) * kVec;
+#pragma unroll
+      for (int v = 0; v < kVec; ++v) acc[v] = fmaf(cf, lp[v], acc[v]);
+    }
+    float* lw = last + (h * kThreads + threadIdx.x) * kVec;
+    if constexpr (kVec == 4) {
+      *reinterpret_cast<float4*>(lw) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if (write_f) *reinterpret_cast<float4*>(fdst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
+      if (tdst) {  // four consecutive columns: 8 contiguous bytes of the swizzled tile
+        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
+        *reinterpret_cast<uint2*>(tdst) =
+            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
+      }
+    } else {
+      lw[0] = acc[0];
+      if (write_f) fdst[0] = acc[0];
+      if (tdst) tdst[0] = __float2bfloat16_rn(acc[0]);
+    }
+    fdst += mat;
+    if (tdst) tdst += mat;
   }
 }
 
@@ -562,10 +610,18 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
                               cudaStream_t stream, __nv_bfloat16* Ft, double* cum, bool f32_nodes) {
   if (N <= kFenFastN) {
-    const size_t smf = (size_t)N * (sizeof(double) + sizeof(float)) + (size_t)(kFenLv + kFenD) * kThreads * sizeof(float);
-    LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
-    simt_fenwick_fast_kernel<<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(
-        S, F, tot, G, N, mat, Ft, cum, f32_nodes || !Ft ? 1 : 0);
+    const int wf = f32_nodes || !Ft ? 1 : 0;
+    if (mat % 4 == 0) {  // four elements per thread, 16-byte copies
+      const size_t smf = fen_smem(N, 4);
+      LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
+      simt_fenwick_fast_kernel<4><<<dim3((mat + 4 * kThreads - 1) / (4 * kThreads), BH), kThreads, smf, stream>>>(
+          S, F, tot, G, N, mat, Ft, cum, wf);
+    } else {
+      const size_t smf = fen_smem(N, 1);
+      LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
+      simt_fenwick_fast_kernel<1><<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(
+          S, F, tot, G, N, mat, Ft, cum, wf);
+    }
     LL_CUDA_OK(cudaGetLastError());
     return LL_OK;
   }
