@@ -151,15 +151,17 @@ __device__ __forceinline__ void stage_f32_sum(unsigned char* tile, const float* 
     for (int q = 0; q < 8; ++q)
 #pragma unroll
       for (int t = 0; t < 8; ++t) a[q][t] = 0.f;
-    for (int m = 0; m < n; ++m) {
-      float4 u[8][2];
+    // node m's part of the pass, loaded one node ahead of its use (two
+    // register buffers, the nodes taken in pairs)
+    auto load = [&](float4 (&u)[8][2], int m) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         const int x = tid + (8 * pass + q) * kThreads, r = x >> 4, c8 = x & 15;
         u[q][0] = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8);
         u[q][1] = *reinterpret_cast<const float4*>(src[m] + r * kD + 8 * c8 + 4);
       }
-      const float cf = coef[m];
+    };
+    auto add = [&](const float4 (&u)[8][2], float cf) {
 #pragma unroll
       for (int q = 0; q < 8; ++q) {
         a[q][0] = fmaf(cf, u[q][0].x, a[q][0]); a[q][1] = fmaf(cf, u[q][0].y, a[q][1]);
@@ -167,6 +169,15 @@ __device__ __forceinline__ void stage_f32_sum(unsigned char* tile, const float* 
         a[q][4] = fmaf(cf, u[q][1].x, a[q][4]); a[q][5] = fmaf(cf, u[q][1].y, a[q][5]);
         a[q][6] = fmaf(cf, u[q][1].z, a[q][6]); a[q][7] = fmaf(cf, u[q][1].w, a[q][7]);
       }
+    };
+    float4 ua[8][2], ub[8][2];
+    load(ua, 0);
+#pragma unroll 1
+    for (int m = 0; m < n; m += 2) {
+      if (m + 1 < n) load(ub, m + 1);
+      add(ua, coef[m]);
+      if (m + 2 < n) load(ua, m + 2);
+      if (m + 1 < n) add(ub, coef[m + 1]);
     }
 #pragma unroll
     for (int q = 0; q < 8; ++q) {
