@@ -1086,6 +1086,19 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
       tma_tile(base + kKeyV, &tv, inbar, row0);
     }
   }
+  // this row's log_alpha and its lam, dlam of levels 0..15 go out first: their
+  // latency runs under the node list's loads
+  const double la = tile_log_alpha(log_alpha, row0, nv);
+  float lam16[16], dlam16[16];
+  {
+    const float* lr = lam + (row0 + tid) * L;
+    const float* dr = dlam + (row0 + tid) * L;
+#pragma unroll
+    for (int u = 0; u < 16; ++u) {
+      lam16[u] = tid < nv && u < L ? lr[u] : 0.f;
+      dlam16[u] = tid < nv && u < L ? dr[u] : 0.f;
+    }
+  }
   if (tid < 32) {  // lane h: the node of level h whose block holds the keys of c, if it has queries after it
     const int h = tid;
     const int e = h < 31 ? ((c >> (h + 1)) << (h + 1)) + (1 << h) - 1 : 0;
@@ -1100,14 +1113,16 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
     }
     if (h == 0) *n_s = __popc(m);
   }
-  tile_cumsum(cs, log_alpha, row0, nv);
+  tile_scan(cs, la);
   const uint32_t tmem = setup_tmem<256>(bar, slot);
   const int n = *n_s;
-  float lamdot = 0.f;  // sum_l lam_j[l] dlam_j[l] of this row (16 levels' loads issued together)
+  float lamdot = 0.f;  // sum_l lam_j[l] dlam_j[l] of this row, in order of l
+#pragma unroll
+  for (int u = 0; u < 16; ++u) lamdot = fmaf(lam16[u], dlam16[u], lamdot);
   if (tid < nv) {
     const float* lr = lam + (row0 + tid) * L;
     const float* dr = dlam + (row0 + tid) * L;
-    for (int l0 = 0; l0 < L; l0 += 16) {
+    for (int l0 = 16; l0 < L; l0 += 16) {
       float a[16], d[16];
 #pragma unroll
       for (int u = 0; u < 16; ++u) {
@@ -1151,12 +1166,15 @@ __global__ void __launch_bounds__(kThreads, 1) bwd_tc_key_kernel(
 #pragma unroll 1
     for (int o = 0; o < 2; ++o) {  // 0: dv (in the E buffer), 1: dk (in the K buffer)
       unsigned char* tile = base + (o == 0 ? kKeyE : kKeyK);
-#pragma unroll 1
+      // each column block's TMEM load is in flight while the block before is added
+      float xs[2][32];
+      if (n > 0) tmem_ld32(lane_addr(tmem, 128 * o), xs[0]);
+#pragma unroll
       for (int cb = 0; cb < 4; ++cb) {
-        float x[32];
+        float* x = xs[cb & 1];
         if (n > 0) {
-          tmem_ld32(lane_addr(tmem, 128 * o + 32 * cb), x);
           tmem_ld_wait();
+          if (cb < 3) tmem_ld32(lane_addr(tmem, 128 * o + 32 * (cb + 1)), xs[(cb + 1) & 1]);
         } else {
 #pragma unroll
           for (int u = 0; u < 32; ++u) x[u] = 0.f;
