@@ -295,7 +295,7 @@ constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG 
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
 constexpr int kIntraThreads = 256;  // two threads per row: columns 0..63 and 64..127
 constexpr size_t intra_smem() {
-  return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 8 * 6 * 32 * 4 + 64;
+  return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 64;
 }
 
 // v[idx] for a runtime idx < n (n a power of two), by a tree of selects on
@@ -356,8 +356,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   float* c2 = colpart + 4 * kT;  // cs x log2(e), float: the in-tile decays are exp2(c2_i - c2_j)
   float* dlhalf = c2 + kT;       // [128][8] the in-tile dlam of the columns 64..127
   float* colf = dlhalf + kT * 8;  // exp2(c2_e - c2_j), e = the end of j's 32-column block
-  float* lmt = colf + kT;         // [8 warps][6 levels][32 lanes] the in-block lambdas of a warp's rows
-  uint64_t* bar = reinterpret_cast<uint64_t*>(lmt + 8 * 6 * 32);
+  uint64_t* bar = reinterpret_cast<uint64_t*>(colf + kT);
   uint64_t* inbar = bar + 1;  // the TMA loads of the input tiles
   uint32_t* slot = reinterpret_cast<uint32_t*>(bar + 2);
   int* abort_s = reinterpret_cast<int*>(slot + 1);
@@ -475,25 +474,32 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           if (lvc == 7) dl[7] += acc;
           else dl[6] += acc;
         } else {
-          // the diagonal block, keys j <= i: branch-free over the columns (the
-          // masked ones take exp2(0) and are selected away), so that the 32
-          // columns' loads and exponentials overlap instead of running one
-          // after another; i ^ j = lane ^ u, and the lambda of its level comes
-          // from the warp's table in shared memory
-          float* lmw = lmt + (tid >> 5) * (6 * 32);
+          // the diagonal block, keys j <= i: branch-free over the columns, so
+          // that the 32 columns' loads and exponentials overlap instead of
+          // running one after another (a masked column's exp2 is selected away,
+          // whatever its value).  Column u's level is bitlen(lane ^ u): its
+          // lambda by a tree of selects on the lane's bits, tk[m] holding the
+          // lambda for the columns whose low k + 1 bits are m
+          float t1[2], t2[4], t3[8], t4[16];
 #pragma unroll
-          for (int l = 0; l < 6; ++l) lmw[l * 32 + lane] = lm[l];
-          __syncwarp();
+          for (int m = 0; m < 2; ++m) t1[m] = ((lane & 1) != (m & 1)) ? lm[1] : lm[0];
+#pragma unroll
+          for (int m = 0; m < 4; ++m) t2[m] = ((lane & 2) != (m & 2)) ? lm[2] : t1[m & 1];
+#pragma unroll
+          for (int m = 0; m < 8; ++m) t3[m] = ((lane & 4) != (m & 4)) ? lm[3] : t2[m & 3];
+#pragma unroll
+          for (int m = 0; m < 16; ++m) t4[m] = ((lane & 8) != (m & 8)) ? lm[4] : t3[m & 7];
           float xx[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const int j = 32 * cb + u;
             const bool on = j <= i && row_ok;
-            const float ex = ex2(on ? ci - c2[j] : 0.f);
-            const float lmv = lmw[bitlen((unsigned)(lane ^ u)) * 32 + lane];  // levels 0..5
-            p[u] = on ? a[u] * ex * lmv : 0.f;
-            da[u] = on ? g[u] * ex * lmv : 0.f;
-            xx[u] = on ? g[u] * a[u] * ex : 0.f;
+            const float exm = on ? ex2(ci - c2[j]) : 0.f;
+            const float lmv = ((lane & 16) != (u & 16)) ? lm[5] : t4[u & 15];
+            const float w = exm * lmv;
+            p[u] = a[u] * w;
+            da[u] = g[u] * w;
+            xx[u] = g[u] * a[u] * exm;
           }
           // row i's keys of level l >= 1 are the aligned block of 2^(l-1)
           // columns beside the row's own block of that size (level 0: its own
