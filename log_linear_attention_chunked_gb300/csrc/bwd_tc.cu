@@ -538,27 +538,36 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
                        pack_bf16x2(da[8 * w + 4], da[8 * w + 5]), pack_bf16x2(da[8 * w + 6], da[8 * w + 7]));
       }
     }
+    // V rows scaled by wdec (the G product that read V has completed) by the
+    // warps with time to spare in this phase: the two with no block at or
+    // below the diagonal (rows 0..63, columns 64..127) scale rows 0..95, the
+    // two that hold only a diagonal block rows 96..127 after it
+    auto scale_v = [&](int j, int c0, int nc) {
+      const float s = wdec[j];
+#pragma unroll 4
+      for (int c8 = c0; c8 < c0 + nc; ++c8) {
+        float x[8];
+        row_chunk(base + kIntraV, j, c8, x);
+        *reinterpret_cast<uint4*>(base + kIntraV + swz(j, c8)) =
+            make_uint4(pack_bf16x2(s * x[0], s * x[1]), pack_bf16x2(s * x[2], s * x[3]),
+                       pack_bf16x2(s * x[4], s * x[5]), pack_bf16x2(s * x[6], s * x[7]));
+      }
+    };
+    if (hf == 1 && wi < 2) {  // threads t = 0..63: row t, and half of row 64 + t / 2
+      const int t = tid - 128;
+      scale_v(t, 0, 16);
+      scale_v(64 + (t >> 1), 8 * (t & 1), 8);
+    } else if ((hf == 0 && wi == 0) || (hf == 1 && wi == 2)) {  // threads t = 0..63: half of row 96 + t / 2
+      const int t = hf == 0 ? tid : tid - 160;
+      scale_v(96 + (t >> 1), 8 * (t & 1), 8);
+    }
     if (hf == 1)
 #pragma unroll
       for (int l = 0; l < 8; ++l) dlhalf[i * 8 + l] = dl[l];
     __syncthreads();  // the column sums and the second half's levels of every row
-    if (hf == 0 && i < nv)
-      for (int l = 0; l < 8 && l < L; ++l) dlam[(row0 + i) * L + l] = dl[l] + dlhalf[i * 8 + l];
-  }
-  if (tid < nv)  // the in-tile part of -v_j . dv_j; the key side adds the rest of dc_j
-    dc[row0 + tid] = -(colpart[tid] + colpart[kT + tid] + colpart[2 * kT + tid] + colpart[3 * kT + tid]);
-  // V rows scaled by wdec (the G product that read V has completed): chunks 8 hf .. 8 hf + 7 of row i
-  {
-    const int j = i;
-    const float s = wdec[j];
-#pragma unroll 4
-    for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
-      float x[8];
-      row_chunk(base + kIntraV, j, c8, x);
-      *reinterpret_cast<uint4*>(base + kIntraV + swz(j, c8)) =
-          make_uint4(pack_bf16x2(s * x[0], s * x[1]), pack_bf16x2(s * x[2], s * x[3]),
-                     pack_bf16x2(s * x[4], s * x[5]), pack_bf16x2(s * x[6], s * x[7]));
-    }
+    if (hf == 0)  // the row's in-tile levels of dlam, written out while the products run
+#pragma unroll
+      for (int l = 0; l < 8; ++l) dlhalf[i * 8 + l] += dl[l];
   }
   tmem_ld_wait();
   to_async();
@@ -569,6 +578,16 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     mma128(tmem + 384, sV, true, sK, true, false);   // S_c = (wdec V)^T K
     umma_commit(bar);
   }
+  // while the products run: the in-tile levels of dlam (levels 0..7 of a
+  // row are contiguous: a warp's store covers four rows) and the in-tile
+  // part of -v_j . dv_j (the key side adds the rest of dc_j)
+#pragma unroll
+  for (int e = tid; e < kT * 8; e += kIntraThreads) {
+    const int r = e >> 3, l = e & 7;
+    if (r < nv && l < L) dlam[(row0 + r) * L + l] = dlhalf[e];
+  }
+  if (tid < nv)
+    dc[row0 + tid] = -(colpart[tid] + colpart[kT + tid] + colpart[2 * kT + tid] + colpart[3 * kT + tid]);
   ok = ok && wait_phase(bar, 1, err, abort_s);
   tc_fence_after();
   if (use_omap && nv == kT) {
