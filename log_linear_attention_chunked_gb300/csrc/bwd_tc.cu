@@ -877,10 +877,10 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     to_async();
     if (tid == 0 && ok) {
       mma128(tmem + 0, sG, false, sF, true, false);    // g = dO F_e
-      mma128(tmem + 128, sL, false, sF, true, !first); // dq += diag(lw) dO F_e
       mma128(tmem + 256, sL, true, sQ, true, false);   // R_e part = (diag(lw) dO)^T Q
       umma_commit(bar);
     }
+    const bool first_lv = first;
     first = false;
     ok = ok && wait_phase(bar, nlev & 1, err, abort_s);
     ++nlev;
@@ -911,6 +911,25 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
           for (int u = 0; u < 8; ++u) part = fmaf(gs[hb][8 * w4 + u], x[u], part);
         }
       }
+      // dq += diag(lw) dO F_e = lw g: the node part of dq accumulates in TMEM
+      // columns 128.. from the float32 g (no product of its own)
+#pragma unroll
+      for (int hb = 0; hb < 2; ++hb) {
+        const uint32_t dcol = lane_addr(tmem, 128 + 32 * (2 * hf + hb));
+        uint32_t wv[32];
+        if (first_lv) {
+#pragma unroll
+          for (int u = 0; u < 32; ++u) wv[u] = __float_as_uint(lw * gs[hb][u]);
+        } else {
+          float prev[32];
+          tmem_ld32(dcol, prev);
+          tmem_ld_wait();
+#pragma unroll
+          for (int u = 0; u < 32; ++u) wv[u] = __float_as_uint(fmaf(lw, gs[hb][u], prev[u]));
+        }
+        tmem_st32(dcol, wv);
+      }
+      tmem_st_wait();
       if (hf == 1) qpart[i] = part;
       if (use_rmap) {
         // this tile's part of R_e staged as four [128 x 32] float32 boxes
