@@ -864,14 +864,20 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     const double g_e = G[bh * N + e];  // added to D at the level's end
     const float w = i < nv ? expf((float)(cs[i] + D)) : 0.f;
     const float lw = i < nv ? w * (rsm ? lam_s[i * L + lv] : lam[(row0 + i) * L + lv]) : 0.f;
-    // dO rows scaled by lw (this thread's half row)
-#pragma unroll 4
-    for (int c8 = 8 * hf; c8 < 8 * hf + 8; ++c8) {
-      float x[8];
-      row_chunk(base + kQryG, i, c8, x);
-      *reinterpret_cast<uint4*>(base + kQryL + swz(i, c8)) =
-          make_uint4(pack_bf16x2(lw * x[0], lw * x[1]), pack_bf16x2(lw * x[2], lw * x[3]),
-                     pack_bf16x2(lw * x[4], lw * x[5]), pack_bf16x2(lw * x[6], lw * x[7]));
+    // dO rows scaled by lw (this thread's half row): its eight 16-byte chunks
+    // loaded together, then scaled and stored
+    {
+      uint4 raw[8];
+#pragma unroll
+      for (int k = 0; k < 8; ++k) raw[k] = *reinterpret_cast<const uint4*>(base + kQryG + swz(i, 8 * hf + k));
+#pragma unroll
+      for (int k = 0; k < 8; ++k) {
+        float x[8];
+        unpack8(raw[k], x);
+        *reinterpret_cast<uint4*>(base + kQryL + swz(i, 8 * hf + k)) =
+            make_uint4(pack_bf16x2(lw * x[0], lw * x[1]), pack_bf16x2(lw * x[2], lw * x[3]),
+                       pack_bf16x2(lw * x[4], lw * x[5]), pack_bf16x2(lw * x[6], lw * x[7]));
+      }
     }
     ok = ok && wait_phase(ldbar, nlev & 1, err, abort_s);
     to_async();
@@ -913,21 +919,26 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
       }
       // dq += diag(lw) dO F_e = lw g: the node part of dq accumulates in TMEM
       // columns 128.. from the float32 g (no product of its own)
+      if (first_lv) {
 #pragma unroll
-      for (int hb = 0; hb < 2; ++hb) {
-        const uint32_t dcol = lane_addr(tmem, 128 + 32 * (2 * hf + hb));
-        uint32_t wv[32];
-        if (first_lv) {
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t wv[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) wv[u] = __float_as_uint(lw * gs[hb][u]);
-        } else {
-          float prev[32];
-          tmem_ld32(dcol, prev);
-          tmem_ld_wait();
-#pragma unroll
-          for (int u = 0; u < 32; ++u) wv[u] = __float_as_uint(fmaf(lw, gs[hb][u], prev[u]));
+          tmem_st32(lane_addr(tmem, 128 + 32 * (2 * hf + hb)), wv);
         }
-        tmem_st32(dcol, wv);
+      } else {  // both column blocks of the running dq loaded together
+        float prev[2][32];
+        tmem_ld32(lane_addr(tmem, 128 + 32 * (2 * hf)), prev[0]);
+        tmem_ld32(lane_addr(tmem, 128 + 32 * (2 * hf + 1)), prev[1]);
+        tmem_ld_wait();
+#pragma unroll
+        for (int hb = 0; hb < 2; ++hb) {
+          uint32_t wv[32];
+#pragma unroll
+          for (int u = 0; u < 32; ++u) wv[u] = __float_as_uint(fmaf(lw, gs[hb][u], prev[hb][u]));
+          tmem_st32(lane_addr(tmem, 128 + 32 * (2 * hf + hb)), wv);
+        }
       }
       tmem_st_wait();
       if (hf == 1) qpart[i] = part;
