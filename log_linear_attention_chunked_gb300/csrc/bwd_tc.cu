@@ -461,10 +461,16 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           // second from the per-tile column table
           const float rf = row_ok ? ex2(ci - c2[32 * cb + 31]) : 0.f;
           const float rl = rf * lmv;
+          float cfv[32];  // the block's column factors, eight 16-byte loads
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 f = reinterpret_cast<const float4*>(colf + 32 * cb)[u4];
+            cfv[4 * u4] = f.x; cfv[4 * u4 + 1] = f.y; cfv[4 * u4 + 2] = f.z; cfv[4 * u4 + 3] = f.w;
+          }
           float acc = 0.f;
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
-            const float cf = colf[32 * cb + u];
+            const float cf = cfv[u];
             const float w = rl * cf;
             p[u] = a[u] * w;
             da[u] = g[u] * w;
@@ -489,12 +495,18 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
           for (int m = 0; m < 8; ++m) t3[m] = ((lane & 4) != (m & 4)) ? lm[3] : t2[m & 3];
 #pragma unroll
           for (int m = 0; m < 16; ++m) t4[m] = ((lane & 8) != (m & 8)) ? lm[4] : t3[m & 7];
+          float cjv[32];  // the block's column cumsums, eight 16-byte loads
+#pragma unroll
+          for (int u4 = 0; u4 < 8; ++u4) {
+            const float4 f = reinterpret_cast<const float4*>(c2 + 32 * cb)[u4];
+            cjv[4 * u4] = f.x; cjv[4 * u4 + 1] = f.y; cjv[4 * u4 + 2] = f.z; cjv[4 * u4 + 3] = f.w;
+          }
           float xx[32];
 #pragma unroll
           for (int u = 0; u < 32; ++u) {
             const int j = 32 * cb + u;
             const bool on = j <= i && row_ok;
-            const float exm = on ? ex2(ci - c2[j]) : 0.f;
+            const float exm = on ? ex2(ci - cjv[u]) : 0.f;
             const float lmv = ((lane & 16) != (u & 16)) ? lm[5] : t4[u & 15];
             const float w = exm * lmv;
             p[u] = a[u] * w;
@@ -542,15 +554,21 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     // warps with time to spare in this phase: the two with no block at or
     // below the diagonal (rows 0..63, columns 64..127) scale rows 0..95, the
     // two that hold only a diagonal block rows 96..127 after it
-    auto scale_v = [&](int j, int c0, int nc) {
+    auto scale_v = [&](int j, int c0, int nc) {  // nc = 8 or 16 chunks, eight loads issued together
       const float s = wdec[j];
-#pragma unroll 4
-      for (int c8 = c0; c8 < c0 + nc; ++c8) {
-        float x[8];
-        row_chunk(base + kIntraV, j, c8, x);
-        *reinterpret_cast<uint4*>(base + kIntraV + swz(j, c8)) =
-            make_uint4(pack_bf16x2(s * x[0], s * x[1]), pack_bf16x2(s * x[2], s * x[3]),
-                       pack_bf16x2(s * x[4], s * x[5]), pack_bf16x2(s * x[6], s * x[7]));
+#pragma unroll 1
+      for (int cc = c0; cc < c0 + nc; cc += 8) {
+        uint4 raw[8];
+#pragma unroll
+        for (int k = 0; k < 8; ++k) raw[k] = *reinterpret_cast<const uint4*>(base + kIntraV + swz(j, cc + k));
+#pragma unroll
+        for (int k = 0; k < 8; ++k) {
+          float x[8];
+          unpack8(raw[k], x);
+          *reinterpret_cast<uint4*>(base + kIntraV + swz(j, cc + k)) =
+              make_uint4(pack_bf16x2(s * x[0], s * x[1]), pack_bf16x2(s * x[2], s * x[3]),
+                         pack_bf16x2(s * x[4], s * x[5]), pack_bf16x2(s * x[6], s * x[7]));
+        }
       }
     };
     if (hf == 1 && wi < 2) {  // threads t = 0..63: row t, and half of row 64 + t / 2
