@@ -347,7 +347,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     __nv_bfloat16* __restrict__ dqp, __nv_bfloat16* __restrict__ dkp, __nv_bfloat16* __restrict__ dvp,
     float* __restrict__ dlam,
     float* __restrict__ S, double* __restrict__ tot, float* __restrict__ dc, int T, int L, int N, int BH,
-    unsigned* err) {
+    unsigned* __restrict__ qctr, unsigned* err) {
   extern __shared__ unsigned char sm_raw[];
   unsigned char* base = reinterpret_cast<unsigned char*>((reinterpret_cast<uintptr_t>(sm_raw) + 1023) & ~uintptr_t(1023));
   double* cs = reinterpret_cast<double*>(base + kIntraEnd);
@@ -364,6 +364,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   if (tid == 0) {
     *abort_s = 0;
     mbar_init(inbar, 1);  // made visible by the fence in setup_tmem
+    if (blockIdx.x == 0) *qctr = 0;  // the query kernel's item counter (that kernel runs after this one)
   }
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   // persistent: tile item w = (tile w mod N, head w / N), one after another;
@@ -1002,7 +1003,11 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
         }
         if (ok) {
           fence_proxy_async_shared();
-          bulk_reduce_add_f32(R + (bh * N + e) * mat + (size_t)i * kD + 64 * hf, rrow + 64 * hf, 64 * 4);
+          float* rdst = R + (bh * N + e) * mat + (size_t)i * kD + 64 * hf;
+          if (h == 0)  // the node's only query tile: stored (its memory is not cleared)
+            bulk_store(rdst, rrow + 64 * hf, 64 * 4);
+          else
+            bulk_reduce_add_f32(rdst, rrow + 64 * hf, 64 * 4);
           bulk_commit();
         }
       }
@@ -1020,7 +1025,12 @@ __global__ void __launch_bounds__(kQryThreads, 1) bwd_tc_query_kernel(
     if (use_rmap && tid == 0 && ok) {
       const int y = (int)((bh * N + e) * kD);
 #pragma unroll
-      for (int cb = 0; cb < 4; ++cb) tma_reduce_add_box(&tr, base + kQryR + cb * kRBox, 32 * cb, y);
+      for (int cb = 0; cb < 4; ++cb) {
+        if (h == 0)  // the node's only query tile: stored (its memory is not cleared)
+          tma_store_2d(&tr, base + kQryR + cb * kRBox, 32 * cb, y);
+        else
+          tma_reduce_add_box(&tr, base + kQryR + cb * kRBox, 32 * cb, y);
+      }
       bulk_commit();
     }
     pend = use_rmap;
@@ -1376,10 +1386,18 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
   const int N = (s.T + kT - 1) / kT;
   const int BH = s.B * s.H;
   const dim3 grid(N, BH);
-  // the key-side nodes accumulate from 0
-  // (and the query kernel's item counter, the word after them)
+  // The key-side nodes of the levels above the first (odd e) accumulate from
+  // 0, the tensor reductions of several query tiles; a first-level node (even
+  // e) has one query tile, which stores it.  With N even the odd nodes
+  // alternate with the even ones through R, and one pitched memset clears
+  // them; otherwise R is cleared whole.  The query kernel's item counter, the
+  // word after R, is cleared by the intra kernel.
   unsigned* qctr = reinterpret_cast<unsigned*>(b.R + (size_t)BH * N * kD * kD);
-  LL_CUDA_OK(cudaMemsetAsync(b.R, 0, (size_t)BH * N * kD * kD * sizeof(float) + sizeof(unsigned), a.stream));
+  const size_t node_bytes = (size_t)kD * kD * sizeof(float);
+  if (N % 2 == 0)
+    LL_CUDA_OK(cudaMemset2DAsync(b.R + (size_t)kD * kD, 2 * node_bytes, 0, node_bytes, (size_t)BH * N / 2, a.stream));
+  else
+    LL_CUDA_OK(cudaMemsetAsync(b.R, 0, (size_t)BH * N * node_bytes, a.stream));
   const auto* q = static_cast<const __nv_bfloat16*>(a.q);
   const auto* k = static_cast<const __nv_bfloat16*>(a.k);
   const auto* v = static_cast<const __nv_bfloat16*>(a.v);
@@ -1403,7 +1421,7 @@ ll_status bwd_tc_launch(const BwdArgs& a, const BwdTcBuffers& b) {
                        tile_map(&tdk, b.dkp, rows) && tile_map(&tdv, b.dvp, rows) && f32_box_map(&tS, b.S, srows);
   bwd_tc_intra_kernel<<<pgrid, kIntraThreads, intra_smem(), a.stream>>>(
       tq, tk, tv, tg, use_tma, tdq, tdk, tdv, tS, use_omap, q, k, v, dout, a.log_alpha, a.lam, b.dqp, b.dkp, b.dvp, a.dlam, b.S, b.tot, b.dc, s.T,
-      s.L, N, BH, b.err);
+      s.L, N, BH, qctr, b.err);
   LL_CUDA_OK(cudaGetLastError());
   // the query kernel reads the nodes' bf16 tiles only: no float32 copy where the Fenwick kernel can skip it
   const ll_status fs = simt_fenwick_launch(b.S, b.F, b.tot, b.G, N, kD * kD, BH, a.stream, b.Ft, b.cum, false);
