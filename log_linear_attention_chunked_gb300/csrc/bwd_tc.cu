@@ -293,7 +293,8 @@ __device__ __forceinline__ uint32_t lane_addr(uint32_t tmem, int col) {
 // ------------------------------------------------------------------ intra
 constexpr uint32_t kIntraQ = 0, kIntraK = kTileB, kIntraV = 2 * kTileB, kIntraG = 3 * kTileB, kIntraP = 4 * kTileB,
                    kIntraA = 5 * kTileB, kIntraEnd = 6 * kTileB;
-constexpr int kIntraThreads = 256;  // two threads per row: columns 0..63 and 64..127
+constexpr int kIntraThreads = 256;
+constexpr uint64_t kIntraStaggerNs = 8000;  // the start delay of the CTAs with one item fewer (measured: 3-12 us)  // two threads per row: columns 0..63 and 64..127
 constexpr size_t intra_smem() {
   return 1024 + kIntraEnd + kT * 8 + kT * 4 + 4 * kT * 4 + kT * 4 + kT * 8 * 4 + kT * 4 + 64;
 }
@@ -369,6 +370,17 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   const uint32_t tmem = setup_tmem<512>(bar, slot);
   // persistent: tile item w = (tile w mod N, head w / N), one after another;
   // each item's inputs are staged in L2 while the previous one is computed
+  // The items' memory phases (inputs in, outputs out) are bursts that run at
+  // the HBM rate when every SM is in them at once.  The CTAs with one item
+  // fewer than the rest start about two thirds of an item later, so that their
+  // bursts fall in the others' compute phases; they end no later for it.
+  {
+    const int items = N * BH, rem = items % (int)gridDim.x;
+    if (rem != 0 && items >= 2 * (int)gridDim.x && (int)blockIdx.x >= rem) {
+      const uint64_t t0 = globaltimer_ns();
+      while (globaltimer_ns() - t0 < kIntraStaggerNs) __nanosleep(256);
+    }
+  }
   uint32_t k_it = 0;
   for (int w = blockIdx.x; w < N * BH; w += gridDim.x, ++k_it) {
   const int c = w % N;
