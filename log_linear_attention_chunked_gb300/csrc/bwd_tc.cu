@@ -381,8 +381,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
       while (globaltimer_ns() - t0 < kIntraStaggerNs) __nanosleep(256);
     }
   }
-  uint32_t k_it = 0;
-  for (int w = blockIdx.x; w < N * BH; w += gridDim.x, ++k_it) {
+  uint32_t n_in = 0;  // the items whose inputs came by TMA so far (one phase of inbar each)
+  for (int w = blockIdx.x; w < N * BH; w += gridDim.x) {
   const int c = w % N;
   const size_t bh = (size_t)(w / N);
   const size_t row0 = bh * T + (size_t)c * kT;
@@ -415,7 +415,8 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
   tile_cumsum(cs, log_alpha, row0, nv);  // while the tiles land
   if (tid == kT - 1) tot[bh * N + c] = cs[kT - 1];
   if (tma) {
-    ok = wait_phase(inbar, k_it & 1, err, abort_s);
+    ok = wait_phase(inbar, n_in & 1, err, abort_s);
+    ++n_in;
   } else if (tid < kT) {
     stage_bf16(base + kIntraQ, q + row0 * kD, nv, tid);
     stage_bf16(base + kIntraK, k + row0 * kD, nv, tid);

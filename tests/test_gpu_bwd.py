@@ -133,6 +133,18 @@ def test_tensor_core_variants(B, la_mode, lam_mode, levels):
         _assert_close(_run(B, inp, cfg["chunk"]), _oracle(inp), TOL_BF16, (la_mode, lam_mode, lvl), _lam(inp))
 
 
+@pytest.mark.parametrize("T", [2650, 2816])
+def test_tensor_core_many_items(B, T):
+    """bf16 d = 128 with more (tile, head) items than two per SM: the query
+    kernel then claims items from its counter and the intra kernel starts the
+    CTAs with one item fewer later.  2650 tokens: 21 tiles, the last ragged
+    (an odd count: the key-side nodes are cleared whole); 2816: 22 tiles (the
+    odd nodes cleared by the pitched memset, the even ones stored); 16 heads."""
+    cfg = _cfg("mamba2_fp32_t64", io="bf16", T=T, dk=128, dv=128, L=levels_needed(T), B=1, H=16, chunk=64)
+    inp = synth.make_inputs(cfg, tag=f"bwdtcmany{T}", dout=True)
+    _assert_close(_run(B, inp, cfg["chunk"]), _oracle(inp), TOL_BF16, ("many items", T), _lam(inp))
+
+
 def test_extra_levels_are_zero(B):
     # lam with more levels than T reaches: their gradient is exactly 0
     cfg = _cfg("mamba2_fp32_t64", T=200, L=levels_needed(200) + 3, B=1, H=2)
