@@ -279,18 +279,16 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_kernel(const float* __r
 // float64 arithmetic.
 constexpr int kFenFastN = kFenwickOnChipChunks;
 constexpr int kFenLv = 13;  // levels of N <= 4096
-// ring slots of the chunk states streamed ahead, for kVec elements per thread
-__host__ __device__ constexpr int fen_ring(int kVec) { return kVec == 4 ? 8 : 16; }
+constexpr int kFenVec = 4;   // consecutive matrix elements per thread (dk dv is a multiple of 256)
+constexpr int kFenRing = 8;  // ring slots of the chunk states streamed ahead
 // dynamic shared memory: the prefix table, the child decays, then (16-byte
 // aligned) the latest nodes of each level and the ring
-constexpr size_t fen_smem(int N, int kVec) {
+constexpr size_t fen_smem(int N) {
   return (size_t)N * (sizeof(double) + sizeof(float)) + 16 +
-         (size_t)(kFenLv + fen_ring(kVec)) * kThreads * kVec * sizeof(float);
+         (size_t)(kFenLv + kFenRing) * kThreads * kFenVec * sizeof(float);
 }
 
-// Each thread follows kVec consecutive elements of the matrix (4 where the
-// matrix size allows 16-byte copies, else 1).
-template <int kVec>
+// Each thread follows kFenVec consecutive elements of the matrix.
 __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float* __restrict__ S,
                                                                      float* __restrict__ F,
                                                                      const double* __restrict__ tot,
@@ -299,7 +297,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
                                                                      double* __restrict__ cum, int write_f) {
   extern __shared__ double Gs[];                                  // [N]
   float* coef = reinterpret_cast<float*>(Gs + N);                 // [N] child decays
-  // [kFenLv][kThreads][kVec] the latest node of each level, then the ring
+  // [kFenLv][kThreads][kFenVec] the latest node of each level, then the ring
   float* last = reinterpret_cast<float*>((reinterpret_cast<uintptr_t>(coef + N) + 15) & ~uintptr_t(15));
   __shared__ double wsum[kThreads / 32];
   const size_t bh = blockIdx.y;
@@ -345,9 +343,9 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
   }
   if (blockIdx.x == 0)
     for (int i = threadIdx.x; i < N; i += kThreads) G[bh * N + i] = Gs[i];
+  constexpr int kVec = kFenVec, kD = kFenRing;
   const int e0 = (blockIdx.x * kThreads + threadIdx.x) * kVec;  // the thread's first element
   if (e0 >= mat) return;
-  constexpr int kD = fen_ring(kVec);
   // the thread's elements of each chunk state stream through a ring of kD
   // slots in shared memory, kD - 1 chunks ahead, by per-thread asynchronous
   // copies (each thread reads back only what it copied); the addresses
@@ -357,12 +355,7 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
   int issued = 0;
   auto stream_in = [&]() {  // the next chunk's elements (past the end: an empty group)
     if (issued < N) {
-      float* slot = ring + ((issued % kD) * kThreads + threadIdx.x) * kVec;
-      if constexpr (kVec == 4) {
-        sm100::cp_async16(slot, next);
-      } else {
-        sm100::cp_async4(slot, next);
-      }
+      sm100::cp_async16(ring + ((issued % kD) * kThreads + threadIdx.x) * kVec, next);
       next += mat;
     }
     ++issued;
@@ -375,12 +368,9 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
     stream_in();  // into the slot of chunk i - 1, read in the iteration before
     sm100::cp_async_wait<kD - 1>();  // chunk i's copy has landed
     float acc[kVec];
-    const float* s = ring + ((i % kD) * kThreads + threadIdx.x) * kVec;
-    if constexpr (kVec == 4) {
-      const float4 x = *reinterpret_cast<const float4*>(s);
+    {
+      const float4 x = *reinterpret_cast<const float4*>(ring + ((i % kD) * kThreads + threadIdx.x) * kVec);
       acc[0] = x.x; acc[1] = x.y; acc[2] = x.z; acc[3] = x.w;
-    } else {
-      acc[0] = s[0];
     }
     const int h = __ffs(~i) - 1, o = i - __popc(i);
     for (int m = 0; m < h; ++m) {
@@ -389,19 +379,13 @@ __global__ void __launch_bounds__(kThreads) simt_fenwick_fast_kernel(const float
 #pragma unroll
       for (int v = 0; v < kVec; ++v) acc[v] = fmaf(cf, lp[v], acc[v]);
     }
-    float* lw = last + (h * kThreads + threadIdx.x) * kVec;
-    if constexpr (kVec == 4) {
-      *reinterpret_cast<float4*>(lw) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      if (write_f) *reinterpret_cast<float4*>(fdst) = make_float4(acc[0], acc[1], acc[2], acc[3]);
-      if (tdst) {  // four consecutive columns: 8 contiguous bytes of the swizzled tile
-        const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
-        *reinterpret_cast<uint2*>(tdst) =
-            make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
-      }
-    } else {
-      lw[0] = acc[0];
-      if (write_f) fdst[0] = acc[0];
-      if (tdst) tdst[0] = __float2bfloat16_rn(acc[0]);
+    const float4 a4 = make_float4(acc[0], acc[1], acc[2], acc[3]);
+    *reinterpret_cast<float4*>(last + (h * kThreads + threadIdx.x) * kVec) = a4;
+    if (write_f) *reinterpret_cast<float4*>(fdst) = a4;
+    if (tdst) {  // four consecutive columns: 8 contiguous bytes of the swizzled tile
+      const __nv_bfloat162 lo = __floats2bfloat162_rn(acc[0], acc[1]), hi = __floats2bfloat162_rn(acc[2], acc[3]);
+      *reinterpret_cast<uint2*>(tdst) =
+          make_uint2(*reinterpret_cast<const uint32_t*>(&lo), *reinterpret_cast<const uint32_t*>(&hi));
     }
     fdst += mat;
     if (tdst) tdst += mat;
@@ -610,18 +594,12 @@ ll_status launch_typed(const FwdArgs& a, const SimtPlan& p) {
 ll_status simt_fenwick_launch(const float* S, float* F, const double* tot, double* G, int N, int mat, int BH,
                               cudaStream_t stream, __nv_bfloat16* Ft, double* cum, bool f32_nodes) {
   if (N <= kFenFastN) {
-    const int wf = f32_nodes || !Ft ? 1 : 0;
-    if (mat % 4 == 0) {  // four elements per thread, 16-byte copies
-      const size_t smf = fen_smem(N, 4);
-      LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel<4>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
-      simt_fenwick_fast_kernel<4><<<dim3((mat + 4 * kThreads - 1) / (4 * kThreads), BH), kThreads, smf, stream>>>(
-          S, F, tot, G, N, mat, Ft, cum, wf);
-    } else {
-      const size_t smf = fen_smem(N, 1);
-      LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel<1>, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
-      simt_fenwick_fast_kernel<1><<<dim3((mat + kThreads - 1) / kThreads, BH), kThreads, smf, stream>>>(
-          S, F, tot, G, N, mat, Ft, cum, wf);
-    }
+    if (mat % kFenVec != 0) return LL_ERR_UNSUPPORTED;  // head dims of 16..128 make it a multiple of 256
+    const size_t smf = fen_smem(N);
+    LL_CUDA_OK(cudaFuncSetAttribute(simt_fenwick_fast_kernel, cudaFuncAttributeMaxDynamicSharedMemorySize, (int)smf));
+    const int per = kFenVec * kThreads;
+    simt_fenwick_fast_kernel<<<dim3((mat + per - 1) / per, BH), kThreads, smf, stream>>>(S, F, tot, G, N, mat, Ft, cum,
+                                                                                   f32_nodes || !Ft ? 1 : 0);
     LL_CUDA_OK(cudaGetLastError());
     return LL_OK;
   }

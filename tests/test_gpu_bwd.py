@@ -145,6 +145,16 @@ def test_tensor_core_many_items(B, T):
     _assert_close(_run(B, inp, cfg["chunk"]), _oracle(inp), TOL_BF16, ("many items", T), _lam(inp))
 
 
+def test_tensor_core_more_heads_than_sms(B):
+    """bf16 d = 128 with 160 heads of 300 tokens (three tiles, the last
+    ragged): more heads than SMs, so a persistent CTA meets the ragged tile
+    (staged by its threads) as a later item too, after and before TMA-loaded
+    ones, and the query kernel claims items from its counter."""
+    cfg = _cfg("mamba2_fp32_t64", io="bf16", T=300, dk=128, dv=128, L=levels_needed(300), B=1, H=160, chunk=64)
+    inp = synth.make_inputs(cfg, tag="bwdtc160", dout=True)
+    _assert_close(_run(B, inp, cfg["chunk"]), _oracle(inp), TOL_BF16, ("160 heads",), _lam(inp))
+
+
 def test_extra_levels_are_zero(B):
     # lam with more levels than T reaches: their gradient is exactly 0
     cfg = _cfg("mamba2_fp32_t64", T=200, L=levels_needed(200) + 3, B=1, H=2)
