@@ -164,6 +164,19 @@ def test_extra_levels_are_zero(B):
     _assert_close(out, _oracle(inp), TOL_F32, lam=_lam(inp))
 
 
+def test_tensor_core_many_levels_are_zero(B):
+    """bf16 d = 128 with L = 40 levels: lam rows too long for the query
+    kernel's shared-memory copy (read from global instead) and a second
+    block of levels in the key kernel's lam . dlam; the levels past those T
+    reaches have gradient exactly 0."""
+    T = 1024
+    cfg = _cfg("mamba2_fp32_t64", io="bf16", T=T, dk=128, dv=128, L=40, B=1, H=2, chunk=64)
+    inp = synth.make_inputs(cfg, tag="bwdtcL40", dout=True)
+    out = _run(B, inp, cfg["chunk"])
+    assert np.all(out[4][..., levels_needed(T):] == 0.0)
+    _assert_close(out, _oracle(inp), TOL_BF16, ("L = 40",), _lam(inp))
+
+
 @pytest.mark.parametrize("io", ["f32", "bf16"])
 def test_independent_of_chunk(B, io):
     cfg = _cfg("mamba2_fp32_t64", io=io, T=1024, dk=64, dv=64, L=levels_needed(1024), B=1, H=2)
