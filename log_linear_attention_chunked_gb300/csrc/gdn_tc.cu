@@ -406,6 +406,20 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
   // W (bf16, into Tbe's space: the B operand of Aqk W and the stored W);
   // Cm = Cl . lambda-mask (bf16, into Tb's space); U^T staged in K's space
   {
+    // the lambda of level bitlen(i ^ j) without indexing lam8 at run time
+    // (which puts it in local memory): a 32-column block off the row's own
+    // has one level, 6 or 7; inside the row's own block, column jj has level
+    // bitlen((i ^ jj) & 31), picked by a tree of selects on the row's bits
+    // (tk[m]: the columns whose low k + 1 bits are m)
+    float t1[2], t2[4], t3[8], t4[16];
+#pragma unroll
+    for (int m = 0; m < 2; ++m) t1[m] = ((i & 1) != (m & 1)) ? lam8[1] : lam8[0];
+#pragma unroll
+    for (int m = 0; m < 4; ++m) t2[m] = ((i & 2) != (m & 2)) ? lam8[2] : t1[m & 1];
+#pragma unroll
+    for (int m = 0; m < 8; ++m) t3[m] = ((i & 4) != (m & 4)) ? lam8[3] : t2[m & 3];
+#pragma unroll
+    for (int m = 0; m < 16; ++m) t4[m] = ((i & 8) != (m & 8)) ? lam8[4] : t3[m & 7];
 #pragma unroll
     for (int c32 = 0; c32 < 2; ++c32) {
       const int j0 = 64 * hf + 32 * c32;
@@ -414,10 +428,13 @@ __global__ void __launch_bounds__(kPrepThreads, 1)
       if (!kB) tmem_ld32(tl + 128 + j0, cl);
       tmem_ld32(tl + 0 + j0, u);
       tmem_ld_wait();
+      const bool own = ((i ^ j0) >> 5) == 0;                // the row's own 32-column block
+      const float lblk = ((i ^ j0) & 64) ? lam8[7] : lam8[6];  // another block: level 6 or 7
 #pragma unroll
       for (int jj = 0; jj < 32; ++jj) {
         const int j = j0 + jj;
-        cl[jj] = (!kB && j <= i) ? cl[jj] * lam8[32 - __clz(i ^ j)] : 0.f;
+        const float lv = own ? (((i & 16) != (jj & 16)) ? lam8[5] : t4[jj & 15]) : lblk;
+        cl[jj] = (!kB && j <= i) ? cl[jj] * lv : 0.f;
       }
 #pragma unroll
       for (int c8 = 0; c8 < 4; ++c8) {
