@@ -684,8 +684,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
     // (256 B; the later kernels add the inter-tile parts in float32), the
     // chunk state S_c as float32 rows (512 B).
     const int r = i;  // this thread's half row: columns 64 hf .. 64 hf + 63
-    __nv_bfloat16* parts[3] = {dqp + (row0 + r) * kD + 64 * hf, dkp + (row0 + r) * kD + 64 * hf,
-                               dvp + (row0 + r) * kD + 64 * hf};
+    const size_t poff = (row0 + r) * kD + 64 * hf;  // this half row in dq, dk, dv
     float* srow = S + (bh * N + c) * (size_t)(kD * kD) + (size_t)r * kD + 64 * hf;
 #pragma unroll 1
     for (int o = 0; o < 4; ++o) {
@@ -714,7 +713,7 @@ __global__ void __launch_bounds__(kIntraThreads, 1) bwd_tc_intra_kernel(
       if (keep && ok) {
         fence_proxy_async_shared();
         if (o == 3) bulk_store(srow, rowp + 64 * hf, 64 * 4);
-        else bulk_store(parts[o], rowb + 64 * hf, 64 * 2);
+        else bulk_store((o == 0 ? dqp : o == 1 ? dkp : dvp) + poff, rowb + 64 * hf, 64 * 2);
         bulk_commit();
       }
     }

@@ -685,17 +685,18 @@ __global__ void __launch_bounds__(kScanThreads, 1)
     int hs = 0;
     bool wq_reloaded = false;
     while (true) {
-      int grp[4], ng = 0;
+      uint32_t grp = 0;  // the group's heights, 8 bits each (a packed word, not an array indexed at run time)
+      int ng = 0;
       for (int h = hs; h < p.nh && ng < 4; ++h)
         if ((c >> h) & 1) {
-          grp[ng++] = h;
+          grp |= (uint32_t)h << (8 * ng++);
           hs = h + 1;
         }
       if (ng == 0) break;
       // (a) X_h as bf16 operand [32 rows d_v][128 d_k]; gamma X_h back into TMEM
       for (int g = 0; g < ng; ++g) {
         float xv[32];
-        tmem_ld32(tl + 32 * grp[g], xv);
+        tmem_ld32(tl + 32 * ((grp >> (8 * g)) & 255u), xv);
         tmem_ld_wait();
         unsigned char* xb = s + kSX + g * kSliceB;
 #pragma unroll
@@ -704,7 +705,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         uint32_t wv[32];
 #pragma unroll
         for (int r = 0; r < 32; ++r) wv[r] = __float_as_uint(gam * xv[r]);
-        tmem_st32(tl + 32 * grp[g], wv);
+        tmem_st32(tl + 32 * ((grp >> (8 * g)) & 255u), wv);
       }
       tmem_st_wait();
       fence_proxy_async_shared();
@@ -735,7 +736,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         float lw = 0.f;
 #pragma unroll
         for (int h = 0; h < kMaxHeights; ++h)
-          if (h == grp[g]) lw = lamh[h];
+          if (h == (int)((grp >> (8 * g)) & 255u)) lw = lamh[h];
 #pragma unroll
         for (int r = 0; r < kSlice; ++r) oacc[r] = fmaf(lw, pv[r], oacc[r]);
       }
@@ -751,7 +752,7 @@ __global__ void __launch_bounds__(kScanThreads, 1)
         for (int g = 0; g < ng; ++g) {
           const uint32_t yb = smem_u32(s + kSX + g * kSliceB);
 #pragma unroll
-          for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + 32 * grp[g], desc_mn(sKt, kk), desc_k32(yb, kk), idX, 1);
+          for (int kk = 0; kk < 8; ++kk) umma_bf16(tmem + 32 * ((grp >> (8 * g)) & 255u), desc_mn(sKt, kk), desc_k32(yb, kk), idX, 1);
         }
       }
       if (hs >= p.nh || (c >> hs) == 0) wq_reloaded = true;
