@@ -16,9 +16,11 @@
 //           would not cancel.
 //   query : for every set bit h of c (node e, level 8 + h, decay D from the
 //           end of e to the start of c; w_i = exp(cs_i + D), lw_i = lam_i w_i):
-//           g = dO F_e (dlam_i = w_i g_i . q_i), dq += diag(lw) dO F_e and
-//           R_e += (diag(lw) dO)^T Q, the key-side node of e (rows staged in
-//           shared memory and added into R_e by bulk reductions).
+//           g = dO F_e (dlam_i = w_i g_i . q_i), dq += diag(lw) dO F_e = lw g
+//           (from the float32 g, into a TMEM accumulator) and
+//           R_e += (diag(lw) dO)^T Q, the key-side node of e (staged in shared
+//           memory and added into R_e by tensor reductions; a first-level node
+//           has this one query tile, which stores it).
 //   key   : E_c = the R nodes of the blocks that hold c's keys, decayed to the
 //           end of c; dv += diag(wdec) K E^T, dk += diag(wdec) V E, and
 //           dc_j = sum_l lam_j[l] dlam_j[l] - v_j . dv_j (the in-tile part of
@@ -27,15 +29,17 @@
 // kernel fetches by one bulk copy) and the suffix sums of dc are the
 // CUDA-core kernels'.
 //
-// One CTA per (tile, head); thread t owns TMEM lane t mod 128 (row t mod 128
-// of every accumulator): 256 threads in the intra and query kernels, the two
-// threads of a row taking one half of its columns each, 128 in the key
-// kernel.  Full input tiles arrive by TMA (the ragged last tile of a head is
+// Thread t owns TMEM lane t mod 128 (row t mod 128 of every accumulator).
+// The intra and query kernels are persistent, one CTA of 256 threads per SM
+// over the (tile, head) items (the two threads of a row taking one half of its
+// columns each); the key kernel runs one CTA of 128 threads per item, two per
+// SM.  Full input tiles arrive by TMA (the ragged last tile of a head is
 // staged by the threads, its missing rows as zeros).  The phases of a tile run
 // in sequence: stage the operands, one thread issues the MMAs and commits them
 // to an mbarrier, every thread waits (bounded: after 4 s the error word is set
 // and the kernel finishes without the results), then the row-wise epilogue,
-// whose rows leave by bulk copies (or bulk reductions) from shared memory.
+// whose tiles leave by tensor stores (or reductions) of swizzled staged boxes
+// (row-wise bulk copies for a ragged tile).
 #include <cudaTypedefs.h>
 
 #include <algorithm>
